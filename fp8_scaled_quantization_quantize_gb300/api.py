@@ -1,0 +1,162 @@
+"""Thin PyTorch binding of libfp8q: argument marshalling only.
+
+torch provides device memory and the current CUDA stream; every step of the
+quantize / GEMM path runs in the library's kernels (include/fp8q.h).  There
+is no fallback: without the built library every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+from dataclasses import dataclass
+
+import torch
+
+from . import _lib as L
+from ._lib import (BLOCK_1x128, BLOCK_128x128, E4M3, E5M2, MXFP8_1x32, PERTENSOR_CURRENT,  # noqa: F401
+                   PERTENSOR_DELAYED, Fp8qError)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def scale_bytes(kind: int, rows: int, cols: int, rowwise: bool, colwise: bool):
+    rb, cb = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    rc = L.Recipe(kind, E4M3, int(rowwise), int(colwise))
+    L.check(L.load().fp8q_scale_bytes(ctypes.byref(rc), rows, cols, ctypes.byref(rb), ctypes.byref(cb)),
+            "fp8q_scale_bytes")
+    return rb.value, cb.value
+
+
+@dataclass
+class QTensor:
+    """Device buffers of one quantized tensor (see fp8q_tensor)."""
+    kind: int
+    fmt: int
+    rows: int
+    cols: int
+    data_row: torch.Tensor | None
+    data_col: torch.Tensor | None
+    scale_row: torch.Tensor | None   # raw bytes (uint8)
+    scale_col: torch.Tensor | None
+    amax: torch.Tensor               # fp32[1]
+    scale: torch.Tensor              # fp32[1]
+    scale_inv: torch.Tensor          # fp32[1]
+    counters: torch.Tensor           # int64[3]: sat_row, sat_col, nonfinite
+
+    def c_struct(self) -> L.Tensor:
+        return L.Tensor(_ptr(self.data_row), _ptr(self.data_col), _ptr(self.scale_row), _ptr(self.scale_col),
+                        _ptr(self.amax), _ptr(self.scale), _ptr(self.scale_inv), _ptr(self.counters),
+                        self.rows, self.cols, self.fmt, self.kind)
+
+    @property
+    def rowwise(self) -> bool:
+        return self.data_row is not None
+
+    @property
+    def colwise(self) -> bool:
+        return self.data_col is not None
+
+
+def alloc(kind: int, fmt: int, rows: int, cols: int, rowwise: bool = True, colwise: bool = False,
+          device="cuda") -> QTensor:
+    rb, cb = scale_bytes(kind, rows, cols, rowwise, colwise)
+    u8 = dict(dtype=torch.uint8, device=device)
+    f32 = dict(dtype=torch.float32, device=device)
+    return QTensor(kind, fmt, rows, cols,
+                   torch.empty((rows, cols), **u8) if rowwise else None,
+                   torch.empty((cols, rows), **u8) if colwise else None,
+                   torch.empty(max(rb, 16), **u8) if rowwise and rb else None,
+                   torch.empty(max(cb, 16), **u8) if colwise and cb else None,
+                   torch.zeros(1, **f32), torch.ones(1, **f32), torch.ones(1, **f32),
+                   torch.zeros(3, dtype=torch.int64, device=device))
+
+
+class DelayedState:
+    """Library-owned per-tensor delayed-scaling state (amax history)."""
+
+    def __init__(self, history_len: int = 16, fmt: int = E4M3, margin: int = 0):
+        h = ctypes.c_void_p(0)
+        L.check(L.load().fp8q_delayed_create(history_len, fmt, margin, ctypes.byref(h)), "fp8q_delayed_create")
+        self.handle = h
+        self.history_len, self.fmt, self.margin = history_len, fmt, margin
+
+    def update(self, amax: torch.Tensor, nonfinite: torch.Tensor | None = None, stream=None):
+        L.check(L.load().fp8q_delayed_update(self.handle, _ptr(amax), _ptr(nonfinite), _stream(stream)),
+                "fp8q_delayed_update")
+
+    def get(self):
+        """(history fp32 list, head, scale, scale_inv); synchronises."""
+        hist = (ctypes.c_float * self.history_len)()
+        head, s, si = ctypes.c_int(0), ctypes.c_float(0), ctypes.c_float(0)
+        L.check(L.load().fp8q_delayed_get(self.handle, hist, ctypes.byref(head), ctypes.byref(s), ctypes.byref(si)),
+                "fp8q_delayed_get")
+        return list(hist), head.value, s.value, si.value
+
+    def set(self, hist, head: int, scale: float, scale_inv: float):
+        arr = (ctypes.c_float * self.history_len)(*hist)
+        L.check(L.load().fp8q_delayed_set(self.handle, arr, head, scale, scale_inv), "fp8q_delayed_set")
+
+    def close(self):
+        if getattr(self, "handle", None):
+            L.load().fp8q_delayed_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def quantize_into(x: torch.Tensor, qt: QTensor, state: DelayedState | None = None, stream=None) -> QTensor:
+    """Quantizes bf16 x [rows, cols] into preallocated qt (same kind / fmt / copies)."""
+    if x.dtype != torch.bfloat16 or x.dim() != 2 or not x.is_contiguous():
+        raise ValueError("x must be a contiguous 2-D bf16 tensor")
+    rc = L.Recipe(qt.kind, qt.fmt, int(qt.rowwise), int(qt.colwise))
+    ct = qt.c_struct()
+    L.check(L.load().fp8q_quantize(ctypes.byref(rc), _ptr(x), x.shape[0], x.shape[1],
+                                   state.handle if state is not None else None, ctypes.byref(ct), _stream(stream)),
+            "fp8q_quantize")
+    return qt
+
+
+def quantize(x: torch.Tensor, kind: int, fmt: int = E4M3, rowwise: bool = True, colwise: bool = False,
+             state: DelayedState | None = None, stream=None) -> QTensor:
+    qt = alloc(kind, fmt, x.shape[0], x.shape[1], rowwise, colwise, device=x.device)
+    return quantize_into(x, qt, state, stream)
+
+
+def scaled_gemm(A: QTensor, a_use_col: bool, B: QTensor, b_use_col: bool, out_dtype=torch.bfloat16,
+                out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """D = A_q . B_q^T (fp32 accumulate) with the recipes' scales applied."""
+    M = A.cols if a_use_col else A.rows
+    K = A.rows if a_use_col else A.cols
+    N = B.cols if b_use_col else B.rows
+    if out is None:
+        dev = (A.data_col if a_use_col else A.data_row).device
+        out = torch.empty((M, N), dtype=out_dtype, device=dev)
+    od = {torch.bfloat16: 0, torch.float32: 1}[out.dtype]
+    ca, cb = A.c_struct(), B.c_struct()
+    L.check(L.load().fp8q_scaled_gemm(ctypes.byref(ca), int(a_use_col), ctypes.byref(cb), int(b_use_col), _ptr(out),
+                                      od, M, N, K, _stream(stream)), "fp8q_scaled_gemm")
+    return out
+
+
+def cast_f32_bits(start: int, count: int, fmt: int, out: torch.Tensor, stream=None) -> torch.Tensor:
+    L.check(L.load().fp8q_cast_f32_bits(start, count, fmt, _ptr(out), _stream(stream)), "fp8q_cast_f32_bits")
+    return out
+
+
+def device_errors(stream=None) -> int:
+    v = ctypes.c_uint(0)
+    L.check(L.load().fp8q_device_errors(ctypes.byref(v), _stream(stream)), "fp8q_device_errors")
+    return v.value

@@ -1,0 +1,274 @@
+// C-ABI entry points of libfp8q: argument validation, scale-buffer sizing,
+// the delayed-scaling state, and dispatch to the kernels.
+#include <stdlib.h>
+#include <string.h>
+
+#include "fp8q_internal.cuh"
+
+struct fp8q_delayed_state {
+    fp8q::DelayedDev* dev;
+    int H;
+    int fmt;
+    int margin;
+    int device;
+};
+
+using namespace fp8q;
+
+namespace {
+
+constexpr int64_t kMaxElems = (int64_t)1 << 40;
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+bool valid_fmt(int f) { return f == FP8Q_E4M3 || f == FP8Q_E5M2; }
+
+bool valid_kind(int k) { return k >= FP8Q_PERTENSOR_CURRENT && k <= FP8Q_MXFP8_1x32; }
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Scale bytes of one copy with logical shape [R][C] (blocks along C).
+size_t copy_scale_bytes(int kind, int64_t R, int64_t C) {
+    switch (kind) {
+        case FP8Q_BLOCK_1x128:
+            return (size_t)(cdiv(C, 128) * cdiv(R, 128) * 128) * sizeof(float);
+        case FP8Q_BLOCK_128x128:
+            return (size_t)(cdiv(R, 128) * cdiv(C, 128)) * sizeof(float);
+        case FP8Q_MXFP8_1x32:
+            return (size_t)(cdiv(R, 128) * cdiv(C, 128)) * 512u;
+        default:
+            return 0;
+    }
+}
+
+}  // namespace
+
+extern "C" {
+
+int fp8q_version(void) { return 100; }
+
+const char* fp8q_status_str(fp8q_status s) {
+    switch (s) {
+        case FP8Q_OK: return "ok";
+        case FP8Q_ERR_ARG: return "invalid argument";
+        case FP8Q_ERR_SHAPE: return "invalid shape";
+        case FP8Q_ERR_ALIGN: return "misaligned pointer or row pitch";
+        case FP8Q_ERR_DTYPE: return "format / recipe combination not allowed";
+        case FP8Q_ERR_UNSUPPORTED: return "not supported by this build";
+        case FP8Q_ERR_CUDA: return "CUDA error";
+        case FP8Q_ERR_TIMEOUT: return "device wait timed out";
+        case FP8Q_WARN_NONFINITE: return "nonfinite input";
+    }
+    return "unknown status";
+}
+
+fp8q_status fp8q_scale_bytes(const fp8q_recipe* rc, int64_t rows, int64_t cols, size_t* row_bytes,
+                             size_t* col_bytes) {
+    if (!rc || !valid_kind(rc->kind)) return FP8Q_ERR_ARG;
+    if (rows < 0 || cols < 0) return FP8Q_ERR_SHAPE;
+    if (row_bytes) *row_bytes = rc->want_rowwise ? copy_scale_bytes(rc->kind, rows, cols) : 0;
+    if (col_bytes) *col_bytes = rc->want_colwise ? copy_scale_bytes(rc->kind, cols, rows) : 0;
+    return FP8Q_OK;
+}
+
+fp8q_status fp8q_quantize(const fp8q_recipe* rc, const void* x, int64_t rows, int64_t cols,
+                          fp8q_delayed_state* st, fp8q_tensor* out, void* stream) {
+    if (!rc || !out) return FP8Q_ERR_ARG;
+    if (!valid_kind(rc->kind) || !valid_fmt(rc->fmt)) return FP8Q_ERR_ARG;
+    const bool row = rc->want_rowwise != 0, col = rc->want_colwise != 0;
+    if (!row && !col) return FP8Q_ERR_ARG;
+    if (rows < 0 || cols < 0) return FP8Q_ERR_SHAPE;
+    if (rows > 0 && cols > 0 && rows > kMaxElems / cols) return FP8Q_ERR_SHAPE;
+    if (cols % 16 != 0) return FP8Q_ERR_SHAPE;
+    if (col && rows % 16 != 0) return FP8Q_ERR_SHAPE;
+    const bool empty = rows == 0 || cols == 0;
+    const bool per_tensor = rc->kind == FP8Q_PERTENSOR_CURRENT || rc->kind == FP8Q_PERTENSOR_DELAYED;
+    if (!out->counters) return FP8Q_ERR_ARG;
+    if (((uintptr_t)out->counters & 7u) != 0) return FP8Q_ERR_ALIGN;
+    if (!empty) {
+        if (!x || (row && !out->data_row) || (col && !out->data_col)) return FP8Q_ERR_ARG;
+        if (!aligned16(x) || (row && !aligned16(out->data_row)) || (col && !aligned16(out->data_col)))
+            return FP8Q_ERR_ALIGN;
+    }
+    if (per_tensor) {
+        if (!out->amax || !out->scale || !out->scale_inv) return FP8Q_ERR_ARG;
+        if (((uintptr_t)out->amax | (uintptr_t)out->scale | (uintptr_t)out->scale_inv) & 3u) return FP8Q_ERR_ALIGN;
+    } else if (!empty) {
+        if ((row && !out->scale_row) || (col && !out->scale_col)) return FP8Q_ERR_ARG;
+        if ((row && !aligned16(out->scale_row)) || (col && !aligned16(out->scale_col))) return FP8Q_ERR_ALIGN;
+    }
+    if (rc->kind == FP8Q_PERTENSOR_DELAYED) {
+        if (!st) return FP8Q_ERR_ARG;
+        if (st->fmt != rc->fmt) return FP8Q_ERR_DTYPE;
+        int dev = -1;
+        cudaGetDevice(&dev);
+        if (dev != st->device) return FP8Q_ERR_ARG;
+    }
+
+    QuantArgs a;
+    memset(&a, 0, sizeof(a));
+    a.x = (const uint16_t*)x;
+    a.R = rows;
+    a.C = cols;
+    a.q_row = row ? (uint8_t*)out->data_row : nullptr;
+    a.q_col = col ? (uint8_t*)out->data_col : nullptr;
+    a.s_row = row ? out->scale_row : nullptr;
+    a.s_col = col ? out->scale_col : nullptr;
+    a.amax = out->amax;
+    a.scale = out->scale;
+    a.scale_inv = out->scale_inv;
+    a.counters = out->counters;
+    a.st = st ? st->dev : nullptr;
+    a.tiles_r = empty ? 0 : cdiv(rows, 128);
+    a.tiles_c = empty ? 0 : cdiv(cols, 128);
+    out->rows = rows;
+    out->cols = cols;
+    out->fmt = rc->fmt;
+    out->kind = rc->kind;
+    return launch_quantize(rc, a, st ? st->dev : nullptr, (cudaStream_t)stream);
+}
+
+fp8q_status fp8q_delayed_create(int history_len, int fmt, int margin, fp8q_delayed_state** out) {
+    if (!out || !valid_fmt(fmt)) return FP8Q_ERR_ARG;
+    if (history_len < 1 || history_len > 4096 || margin < 0 || margin > 64) return FP8Q_ERR_ARG;
+    *out = nullptr;
+    const size_t bytes = sizeof(DelayedDev) + sizeof(float) * (size_t)history_len;
+    DelayedDev* dev = nullptr;
+    if (cudaMalloc(&dev, bytes) != cudaSuccess) return FP8Q_ERR_CUDA;
+    DelayedDev* host = (DelayedDev*)calloc(1, bytes);
+    if (!host) {
+        cudaFree(dev);
+        return FP8Q_ERR_ARG;
+    }
+    host->scale = 1.0f;
+    host->scale_inv = 1.0f;
+    host->head = 0;
+    host->H = history_len;
+    host->fmt = fmt;
+    host->margin = margin;
+    const cudaError_t e = cudaMemcpy(dev, host, bytes, cudaMemcpyHostToDevice);
+    free(host);
+    if (e != cudaSuccess) {
+        cudaFree(dev);
+        return FP8Q_ERR_CUDA;
+    }
+    fp8q_delayed_state* st = (fp8q_delayed_state*)calloc(1, sizeof(fp8q_delayed_state));
+    if (!st) {
+        cudaFree(dev);
+        return FP8Q_ERR_ARG;
+    }
+    st->dev = dev;
+    st->H = history_len;
+    st->fmt = fmt;
+    st->margin = margin;
+    cudaGetDevice(&st->device);
+    *out = st;
+    return FP8Q_OK;
+}
+
+fp8q_status fp8q_delayed_update(fp8q_delayed_state* st, const float* amax, const unsigned long long* nonfinite,
+                                void* stream) {
+    if (!st || !amax) return FP8Q_ERR_ARG;
+    return launch_delayed_update(st->dev, amax, nonfinite, (cudaStream_t)stream);
+}
+
+fp8q_status fp8q_delayed_get(const fp8q_delayed_state* st, float* hist, int* head, float* scale,
+                             float* scale_inv) {
+    if (!st) return FP8Q_ERR_ARG;
+    const size_t bytes = sizeof(DelayedDev) + sizeof(float) * (size_t)st->H;
+    DelayedDev* host = (DelayedDev*)malloc(bytes);
+    if (!host) return FP8Q_ERR_ARG;
+    if (cudaDeviceSynchronize() != cudaSuccess || cudaMemcpy(host, st->dev, bytes, cudaMemcpyDeviceToHost) != cudaSuccess) {
+        free(host);
+        return FP8Q_ERR_CUDA;
+    }
+    if (hist) memcpy(hist, host->hist, sizeof(float) * (size_t)st->H);
+    if (head) *head = host->head;
+    if (scale) *scale = host->scale;
+    if (scale_inv) *scale_inv = host->scale_inv;
+    free(host);
+    return FP8Q_OK;
+}
+
+fp8q_status fp8q_delayed_set(fp8q_delayed_state* st, const float* hist, int head, float scale, float scale_inv) {
+    if (!st || !hist) return FP8Q_ERR_ARG;
+    if (head < 0 || head >= st->H) return FP8Q_ERR_ARG;
+    const size_t bytes = sizeof(DelayedDev) + sizeof(float) * (size_t)st->H;
+    DelayedDev* host = (DelayedDev*)calloc(1, bytes);
+    if (!host) return FP8Q_ERR_ARG;
+    host->scale = scale;
+    host->scale_inv = scale_inv;
+    host->head = head;
+    host->H = st->H;
+    host->fmt = st->fmt;
+    host->margin = st->margin;
+    memcpy(host->hist, hist, sizeof(float) * (size_t)st->H);
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = cudaMemcpy(st->dev, host, bytes, cudaMemcpyHostToDevice);
+    free(host);
+    return e == cudaSuccess ? FP8Q_OK : FP8Q_ERR_CUDA;
+}
+
+int fp8q_delayed_history_len(const fp8q_delayed_state* st) { return st ? st->H : 0; }
+
+void fp8q_delayed_destroy(fp8q_delayed_state* st) {
+    if (!st) return;
+    cudaFree(st->dev);
+    free(st);
+}
+
+fp8q_status fp8q_scaled_gemm(const fp8q_tensor* A, int a_use_col, const fp8q_tensor* B, int b_use_col, void* D,
+                             int out_dtype, int64_t M, int64_t N, int64_t K, void* stream) {
+    if (!A || !B || !D) return FP8Q_ERR_ARG;
+    if (out_dtype != 0 && out_dtype != 1) return FP8Q_ERR_ARG;
+    if (M < 1 || N < 1 || K < 1) return FP8Q_ERR_SHAPE;
+    if (K % 16 != 0 || N % 8 != 0) return FP8Q_ERR_SHAPE;
+    if (!valid_kind(A->kind) || !valid_kind(B->kind) || !valid_fmt(A->fmt) || !valid_fmt(B->fmt)) return FP8Q_ERR_ARG;
+    // logical shapes of the chosen copies
+    const int64_t am = a_use_col ? A->cols : A->rows, ak = a_use_col ? A->rows : A->cols;
+    const int64_t bn = b_use_col ? B->cols : B->rows, bk = b_use_col ? B->rows : B->cols;
+    if (am != M || ak != K || bn != N || bk != K) return FP8Q_ERR_SHAPE;
+    const bool a_pt = A->kind == FP8Q_PERTENSOR_CURRENT || A->kind == FP8Q_PERTENSOR_DELAYED;
+    const bool b_pt = B->kind == FP8Q_PERTENSOR_CURRENT || B->kind == FP8Q_PERTENSOR_DELAYED;
+    if (a_pt != b_pt) return FP8Q_ERR_DTYPE;
+    if (!a_pt) {
+        if (A->kind == FP8Q_MXFP8_1x32 || B->kind == FP8Q_MXFP8_1x32) {
+            if (A->kind != B->kind) return FP8Q_ERR_DTYPE;
+        } else if (A->kind != FP8Q_BLOCK_1x128) {
+            return FP8Q_ERR_DTYPE;  // blockwise: A must be 1x128, B 1x128 or 128x128
+        }
+    }
+    GemmOperand ga, gb;
+    ga.data = (const uint8_t*)(a_use_col ? A->data_col : A->data_row);
+    ga.scale = a_use_col ? A->scale_col : A->scale_row;
+    ga.scale_inv = A->scale_inv;
+    ga.rows = M;
+    ga.kind = A->kind;
+    ga.fmt = A->fmt;
+    gb.data = (const uint8_t*)(b_use_col ? B->data_col : B->data_row);
+    gb.scale = b_use_col ? B->scale_col : B->scale_row;
+    gb.scale_inv = B->scale_inv;
+    gb.rows = N;
+    gb.kind = B->kind;
+    gb.fmt = B->fmt;
+    if (!ga.data || !gb.data) return FP8Q_ERR_ARG;
+    if (a_pt ? !ga.scale_inv || !gb.scale_inv : !ga.scale || !gb.scale) return FP8Q_ERR_ARG;
+    if (!aligned16(ga.data) || !aligned16(gb.data) || !aligned16(D)) return FP8Q_ERR_ALIGN;
+    if (!a_pt && (!aligned16(ga.scale) || !aligned16(gb.scale))) return FP8Q_ERR_ALIGN;
+    return launch_gemm(ga, gb, D, out_dtype, M, N, K, (cudaStream_t)stream);
+}
+
+fp8q_status fp8q_device_errors(unsigned int* flags, void* stream) {
+    if (!flags) return FP8Q_ERR_ARG;
+    return read_device_errors(flags, (cudaStream_t)stream);
+}
+
+fp8q_status fp8q_cast_f32_bits(uint32_t start, uint64_t count, int fmt, void* out, void* stream) {
+    if (!valid_fmt(fmt)) return FP8Q_ERR_ARG;
+    if (count > 0 && !out) return FP8Q_ERR_ARG;
+    if (count > ((uint64_t)1 << 32)) return FP8Q_ERR_SHAPE;
+    if (!aligned16(out)) return FP8Q_ERR_ALIGN;
+    return launch_cast_bits(start, count, fmt, (uint8_t*)out, (cudaStream_t)stream);
+}
+
+}  // extern "C"

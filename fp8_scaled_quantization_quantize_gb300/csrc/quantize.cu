@@ -1,0 +1,459 @@
+// Quantize kernels: per-tensor current / delayed, blockwise 1x128 / 128x128,
+// MXFP8 1x32 ("2025 FP8 quantized-training guide", sec. 2.1-2.3; "mastering
+// FP8 LLM training 1.5x speedup", scaling strategies 1-4).
+//
+// One tile kernel serves every recipe.  A CTA of 256 threads walks 128x128
+// tiles of x (persistent grid).  Each thread loads eight 16-byte vectors (rows
+// rsub + 16 i, columns 8 vcol .. 8 vcol + 7), so a 1x128 row block lives in a
+// half-warp and a 1x32 block in four lanes: block amaxes are shuffle
+// reductions.  The row-wise copy is converted straight from registers.  For
+// the column-wise copy the bf16 tile is staged in shared memory and read back
+// down its columns (32 rows x 2 columns per thread), where the 1x32 / 1x128
+// column blocks are reduced and converted; the 128-aligned tiles make every
+// scale-layout pad entry the scale of an all-zero block (code 127 / 1.0).
+#include "fp8q_internal.cuh"
+
+namespace fp8q {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kTile = 128;
+
+__device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// Largest finite |x| of the two bf16 in w, as bf16 magnitude bits (0 if none),
+// and the number of NaN / Inf among them.
+__device__ __forceinline__ uint32_t absmax_bits(uint32_t w, uint32_t& nonfinite) {
+    uint32_t lo = w & 0x7FFFu, hi = (w >> 16) & 0x7FFFu;
+    uint32_t flo = lo < 0x7F80u, fhi = hi < 0x7F80u;
+    nonfinite += (1u - flo) + (1u - fhi);
+    lo = flo ? lo : 0u;
+    hi = fhi ? hi : 0u;
+    return lo > hi ? lo : hi;
+}
+
+__device__ __forceinline__ uint32_t vec_absmax(const uint4& v, uint32_t& nonfinite) {
+    uint32_t a = absmax_bits(v.x, nonfinite), b = absmax_bits(v.y, nonfinite);
+    uint32_t c = absmax_bits(v.z, nonfinite), d = absmax_bits(v.w, nonfinite);
+    a = a > b ? a : b;
+    c = c > d ? c : d;
+    return a > c ? a : c;
+}
+
+// Scaled value of one element for the recipe's scale rule.
+template <int KIND>
+__device__ __forceinline__ float scaled(float x, float k) {
+    if constexpr (KIND == kB1 || KIND == kB128)
+        return __fdiv_rn(x, k);  // blockwise: x / d
+    else
+        return __fmul_rn(x, k);  // per-tensor x * s, MXFP8 x * 2^-e (exact)
+}
+
+template <int FMT>
+__device__ __forceinline__ uint32_t sat_count(float x, float y) {
+    return (fabsf(x) <= 3.402823466e38f && fabsf(y) > Fmt<FMT>::fmax) ? 1u : 0u;
+}
+
+// Converts the 8 bf16 of v with factor k; returns 8 codes, counts saturation.
+template <int KIND, int FMT>
+__device__ __forceinline__ uint2 convert8(const uint4& v, float k, uint32_t& nsat) {
+    float f[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
+                  bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
+    float y[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        y[j] = scaled<KIND>(f[j], k);
+        nsat += sat_count<FMT>(f[j], y[j]);
+    }
+    return make_uint2(cvt4<FMT>(y[0], y[1], y[2], y[3]), cvt4<FMT>(y[4], y[5], y[6], y[7]));
+}
+
+template <int KIND, int FMT>
+__device__ __forceinline__ float pertensor_factor(const QuantArgs& a) {
+    if constexpr (KIND == kCur)
+        return pertensor_scale<FMT>(*a.amax);
+    else
+        return a.st->scale;
+}
+
+template <int KIND, int FMT, bool ROW, bool COL>
+__global__ void __launch_bounds__(kThreads) quant_tile_kernel(QuantArgs a) {
+    constexpr bool kPerTensor = (KIND == kCur || KIND == kDel);
+    __shared__ __align__(16) uint32_t tile[COL ? kTile * kTile / 2 : 1];  // bf16 pairs
+    __shared__ uint32_t colred[COL && KIND == kB1 ? 4 * kTile : 1];
+    __shared__ uint32_t red[kThreads / 32];
+
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const int vcol = t & 15, rsub = t >> 4;
+
+    float ks = 1.0f;
+    if constexpr (kPerTensor) {
+        ks = pertensor_factor<KIND, FMT>(a);
+        if (blockIdx.x == 0 && t == 0) {
+            *a.scale = ks;
+            *a.scale_inv = (KIND == kDel) ? a.st->scale_inv : __fdiv_rn(1.0f, ks);
+        }
+    }
+
+    uint32_t nsat_row = 0, nsat_col = 0, nnf = 0, tmax_all = 0;
+    const int64_t ntiles = a.tiles_r * a.tiles_c;
+
+    for (int64_t tileid = blockIdx.x; tileid < ntiles; tileid += gridDim.x) {
+        const int64_t tr = tileid / a.tiles_c, tc = tileid % a.tiles_c;
+        const int64_t r0 = tr * kTile, c0 = tc * kTile;
+        const int64_t c = c0 + vcol * 8;
+        const bool cin = c < a.C;
+
+        uint4 v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int64_t r = r0 + rsub + 16 * i;
+            v[i] = (cin && r < a.R) ? ld_nc_v4(a.x + r * a.C + c) : make_uint4(0, 0, 0, 0);
+        }
+        uint32_t vmax[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) vmax[i] = vec_absmax(v[i], nnf);
+
+        // 128x128 tile amax (also the delayed recipe's running tensor amax)
+        float kd_tile = 1.0f;
+        if constexpr (KIND == kB128 || KIND == kDel) {
+            uint32_t m = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) m = m > vmax[i] ? m : vmax[i];
+            if constexpr (KIND == kDel) {
+                tmax_all = tmax_all > m ? tmax_all : m;
+            } else {
+                m = warp_max_u32(m);
+                if (lane == 0) red[warp] = m;
+                __syncthreads();
+                uint32_t mm = 0;
+#pragma unroll
+                for (int w = 0; w < kThreads / 32; ++w) mm = mm > red[w] ? mm : red[w];
+                __syncthreads();
+                kd_tile = block_scale<FMT>(__uint_as_float(mm << 16));
+                if (t == 0) {
+                    if (ROW) ((float*)a.s_row)[tr * a.tiles_c + tc] = kd_tile;
+                    if (COL) ((float*)a.s_col)[tc * a.tiles_r + tr] = kd_tile;
+                }
+            }
+        }
+
+        // ---------------- row-wise copy
+        if constexpr (ROW) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int64_t r = r0 + rsub + 16 * i;
+                float k;
+                if constexpr (kPerTensor) {
+                    k = ks;
+                } else if constexpr (KIND == kB128) {
+                    k = kd_tile;
+                } else if constexpr (KIND == kB1) {
+                    uint32_t m = vmax[i];
+                    m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
+                    m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
+                    m = max(m, __shfl_xor_sync(0xffffffffu, m, 4));
+                    m = max(m, __shfl_xor_sync(0xffffffffu, m, 8));
+                    k = block_scale<FMT>(__uint_as_float(m << 16));
+                    if (vcol == 0) {
+                        const int64_t Rp = a.tiles_r * kTile;
+                        ((float*)a.s_row)[tc * Rp + r] = k;
+                    }
+                } else {  // MXFP8
+                    uint32_t m = vmax[i];
+                    m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
+                    m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
+                    const int e = mx_exponent<FMT>(m << 16);
+                    k = exp2_neg(e);
+                    // gather the four block codes of this row segment into lane vcol == 0
+                    const uint32_t code = (uint32_t)(e + 127);
+                    const uint32_t c1 = __shfl_down_sync(0xffffffffu, code, 4);
+                    const uint32_t c2 = __shfl_down_sync(0xffffffffu, code, 8);
+                    const uint32_t c3 = __shfl_down_sync(0xffffffffu, code, 12);
+                    if (vcol == 0) {
+                        const int rr = (int)(r & 127);
+                        uint8_t* tileb = (uint8_t*)a.s_row + (tr * a.tiles_c + tc) * 512;
+                        *(uint32_t*)(tileb + (rr & 31) * 16 + (rr >> 5) * 4) = code | (c1 << 8) | (c2 << 16) | (c3 << 24);
+                    }
+                }
+                const uint2 q = convert8<KIND, FMT>(v[i], k, nsat_row);
+                if (cin && r < a.R) *(uint2*)(a.q_row + r * a.C + c) = q;
+            }
+        }
+
+        // ---------------- column-wise copy
+        if constexpr (COL) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) *(uint4*)&tile[(rsub + 16 * i) * (kTile / 2) + vcol * 4] = v[i];
+            __syncthreads();
+            const int p = t & 63, qd = t >> 6;  // column pair, 32-row quarter
+            uint32_t w[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) w[j] = tile[(32 * qd + j) * (kTile / 2) + p];
+            float k0, k1;
+            if constexpr (kPerTensor) {
+                k0 = k1 = ks;
+            } else if constexpr (KIND == kB128) {
+                k0 = k1 = kd_tile;
+            } else {
+                uint32_t m0 = 0, m1 = 0, dummy = 0;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    uint32_t lo = w[j] & 0x7FFFu, hi = (w[j] >> 16) & 0x7FFFu;
+                    m0 = (lo < 0x7F80u && lo > m0) ? lo : m0;
+                    m1 = (hi < 0x7F80u && hi > m1) ? hi : m1;
+                }
+                (void)dummy;
+                const int64_t cc = c0 + 2 * p;
+                if constexpr (KIND == kMX) {
+                    const int e0 = mx_exponent<FMT>(m0 << 16), e1 = mx_exponent<FMT>(m1 << 16);
+                    k0 = exp2_neg(e0);
+                    k1 = exp2_neg(e1);
+                    // column-wise scales: logical [C][ceil(R/32)], tiles over (c/128, kb/4)
+                    uint8_t* tileb = (uint8_t*)a.s_col + (tc * a.tiles_r + tr) * 512;
+                    const int cr = 2 * p;
+                    tileb[(cr & 31) * 16 + (cr >> 5) * 4 + qd] = (uint8_t)(e0 + 127);
+                    tileb[((cr + 1) & 31) * 16 + ((cr + 1) >> 5) * 4 + qd] = (uint8_t)(e1 + 127);
+                } else {  // 1x128 along the rows of x: reduce the four quarters
+                    colred[qd * kTile + 2 * p] = m0;
+                    colred[qd * kTile + 2 * p + 1] = m1;
+                    __syncthreads();
+                    m0 = max(max(colred[2 * p], colred[kTile + 2 * p]),
+                             max(colred[2 * kTile + 2 * p], colred[3 * kTile + 2 * p]));
+                    m1 = max(max(colred[2 * p + 1], colred[kTile + 2 * p + 1]),
+                             max(colred[2 * kTile + 2 * p + 1], colred[3 * kTile + 2 * p + 1]));
+                    k0 = block_scale<FMT>(__uint_as_float(m0 << 16));
+                    k1 = block_scale<FMT>(__uint_as_float(m1 << 16));
+                    if (qd == 0) {
+                        const int64_t Cp = a.tiles_c * kTile;
+                        float* sc = (float*)a.s_col + tr * Cp + cc;
+                        sc[0] = k0;
+                        sc[1] = k1;
+                    }
+                }
+            }
+            // convert 32 rows of columns 2p, 2p+1
+            uint32_t o0[8], o1[8];
+            uint32_t ns = 0;
+#pragma unroll
+            for (int j = 0; j < 32; j += 4) {
+                float a0 = bf16_lo(w[j]), a1 = bf16_lo(w[j + 1]), a2 = bf16_lo(w[j + 2]), a3 = bf16_lo(w[j + 3]);
+                float b0 = bf16_hi(w[j]), b1 = bf16_hi(w[j + 1]), b2 = bf16_hi(w[j + 2]), b3 = bf16_hi(w[j + 3]);
+                float ya0 = scaled<KIND>(a0, k0), ya1 = scaled<KIND>(a1, k0), ya2 = scaled<KIND>(a2, k0),
+                      ya3 = scaled<KIND>(a3, k0);
+                float yb0 = scaled<KIND>(b0, k1), yb1 = scaled<KIND>(b1, k1), yb2 = scaled<KIND>(b2, k1),
+                      yb3 = scaled<KIND>(b3, k1);
+                if constexpr (KIND == kB1 || KIND == kMX) {
+                    ns += sat_count<FMT>(a0, ya0) + sat_count<FMT>(a1, ya1) + sat_count<FMT>(a2, ya2) +
+                          sat_count<FMT>(a3, ya3) + sat_count<FMT>(b0, yb0) + sat_count<FMT>(b1, yb1) +
+                          sat_count<FMT>(b2, yb2) + sat_count<FMT>(b3, yb3);
+                }
+                o0[j / 4] = cvt4<FMT>(ya0, ya1, ya2, ya3);
+                o1[j / 4] = cvt4<FMT>(yb0, yb1, yb2, yb3);
+            }
+            nsat_col += ns;
+            const int64_t cc = c0 + 2 * p, rr = r0 + 32 * qd;
+            if (rr < a.R) {
+                const bool full = rr + 32 <= a.R;  // R % 16 == 0: else exactly 16 rows remain
+                if (cc < a.C) {
+                    uint4* dst = (uint4*)(a.q_col + cc * a.R + rr);
+                    dst[0] = make_uint4(o0[0], o0[1], o0[2], o0[3]);
+                    if (full) dst[1] = make_uint4(o0[4], o0[5], o0[6], o0[7]);
+                }
+                if (cc + 1 < a.C) {
+                    uint4* dst = (uint4*)(a.q_col + (cc + 1) * a.R + rr);
+                    dst[0] = make_uint4(o1[0], o1[1], o1[2], o1[3]);
+                    if (full) dst[1] = make_uint4(o1[4], o1[5], o1[6], o1[7]);
+                }
+            }
+            __syncthreads();  // tile / colred reused by the next tile
+        }
+    }
+
+    // ---------------- counters (and the delayed recipe's tensor amax)
+    nsat_row = warp_sum_u32(nsat_row);
+    nsat_col = warp_sum_u32(nsat_col);
+    nnf = warp_sum_u32(nnf);
+    if (lane == 0) {
+        if (nsat_row) atomicAdd(&a.counters[0], (unsigned long long)nsat_row);
+        if (nsat_col) atomicAdd(&a.counters[1], (unsigned long long)nsat_col);
+        if (KIND != kCur && nnf) atomicAdd(&a.counters[2], (unsigned long long)nnf);
+    }
+    if constexpr (KIND == kDel) {
+        tmax_all = warp_max_u32(tmax_all);
+        if (lane == 0 && tmax_all) atomicMax((unsigned int*)a.amax, tmax_all << 16);
+    }
+}
+
+// Per-tensor current scaling, pass 1: amax over the finite elements of x and
+// the NaN / Inf count.  Four independent 16-byte loads in flight per thread.
+__global__ void __launch_bounds__(kThreads) amax_kernel(const uint16_t* x, int64_t nvec, float* amax,
+                                                        unsigned long long* counters) {
+    __shared__ uint32_t redm[kThreads / 32], redn[kThreads / 32];
+    const uint4* xv = (const uint4*)x;
+    uint32_t m = 0, nf = 0;
+    const int64_t stride = (int64_t)gridDim.x * kThreads;
+    int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    for (; i + 3 * stride < nvec; i += 4 * stride) {
+        uint4 v0 = ld_nc_v4(xv + i), v1 = ld_nc_v4(xv + i + stride);
+        uint4 v2 = ld_nc_v4(xv + i + 2 * stride), v3 = ld_nc_v4(xv + i + 3 * stride);
+        m = max(m, max(max(vec_absmax(v0, nf), vec_absmax(v1, nf)), max(vec_absmax(v2, nf), vec_absmax(v3, nf))));
+    }
+    for (; i < nvec; i += stride) m = max(m, vec_absmax(ld_nc_v4(xv + i), nf));
+    m = warp_max_u32(m);
+    nf = warp_sum_u32(nf);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (lane == 0) {
+        redm[warp] = m;
+        redn[warp] = nf;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        uint32_t mm = 0, nn = 0;
+        for (int w = 0; w < kThreads / 32; ++w) {
+            mm = max(mm, redm[w]);
+            nn += redn[w];
+        }
+        if (mm) atomicMax((unsigned int*)amax, mm << 16);
+        if (nn) atomicAdd(&counters[2], (unsigned long long)nn);
+    }
+}
+
+__global__ void delayed_update_kernel(DelayedDev* st, const float* amax, const unsigned long long* nonfinite) {
+    if (threadIdx.x != 0 || blockIdx.x != 0) return;
+    if (nonfinite != nullptr && *nonfinite != 0ull) return;
+    const float am = *amax;
+    if (!(fabsf(am) <= 3.402823466e38f)) return;
+    const int H = st->H;
+    st->hist[st->head] = am;
+    st->head = (st->head + 1) % H;
+    float m = 0.0f;
+    for (int i = 0; i < H; ++i) m = fmaxf(m, st->hist[i]);
+    float s;
+    if (!(m > 0.0f)) {
+        s = 1.0f;
+    } else {
+        s = __fdiv_rn(st->fmt == FP8Q_E4M3 ? 448.0f : 57344.0f, m);
+        s = __fmul_rn(s, exp2_neg(st->margin));
+        if (isinf(s)) s = 3.402823466e38f;
+    }
+    st->scale = s;
+    st->scale_inv = __fdiv_rn(1.0f, s);
+}
+
+template <int FMT>
+__global__ void cast_bits_kernel(uint32_t start, uint64_t count, uint8_t* out) {
+    const uint64_t i0 = ((uint64_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
+    if (i0 >= count) return;
+    float f[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) f[j] = __uint_as_float((uint32_t)(start + i0 + j));
+    const uint32_t q = cvt4<FMT>(f[0], f[1], f[2], f[3]);
+    if (i0 + 4 <= count) {
+        *(uint32_t*)(out + i0) = q;
+    } else {
+        for (uint64_t j = 0; i0 + j < count; ++j) out[i0 + j] = (uint8_t)(q >> (8 * j));
+    }
+}
+
+int g_num_sms = 0;
+
+int num_sms() {
+    if (g_num_sms == 0) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
+        if (g_num_sms <= 0) g_num_sms = 1;
+    }
+    return g_num_sms;
+}
+
+template <int KIND, int FMT, bool ROW, bool COL>
+fp8q_status launch_tile(const QuantArgs& a, cudaStream_t s) {
+    static int per_sm = 0;
+    auto kern = quant_tile_kernel<KIND, FMT, ROW, COL>;
+    if (per_sm == 0) {
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, 0) != cudaSuccess || per_sm < 1)
+            per_sm = 1;
+    }
+    const int64_t ntiles = a.tiles_r * a.tiles_c;
+    int64_t grid = (int64_t)num_sms() * per_sm;
+    if (ntiles < grid) grid = ntiles;
+    if (grid < 1) grid = 1;
+    kern<<<(unsigned)grid, kThreads, 0, s>>>(a);
+    return cudaGetLastError() == cudaSuccess ? FP8Q_OK : FP8Q_ERR_CUDA;
+}
+
+template <int KIND, int FMT>
+fp8q_status launch_tile_rc(const QuantArgs& a, bool row, bool col, cudaStream_t s) {
+    if (row && col) return launch_tile<KIND, FMT, true, true>(a, s);
+    if (row) return launch_tile<KIND, FMT, true, false>(a, s);
+    return launch_tile<KIND, FMT, false, true>(a, s);
+}
+
+template <int KIND>
+fp8q_status launch_tile_fmt(const QuantArgs& a, int fmt, bool row, bool col, cudaStream_t s) {
+    return fmt == FP8Q_E4M3 ? launch_tile_rc<KIND, FP8Q_E4M3>(a, row, col, s)
+                            : launch_tile_rc<KIND, FP8Q_E5M2>(a, row, col, s);
+}
+
+}  // namespace
+
+fp8q_status launch_quantize(const fp8q_recipe* rc, const QuantArgs& a, DelayedDev* st, cudaStream_t s) {
+    const bool row = rc->want_rowwise != 0, col = rc->want_colwise != 0;
+    if (cudaMemsetAsync(a.counters, 0, 3 * sizeof(unsigned long long), s) != cudaSuccess) return FP8Q_ERR_CUDA;
+    switch (rc->kind) {
+        case kCur: {
+            if (cudaMemsetAsync(a.amax, 0, sizeof(float), s) != cudaSuccess) return FP8Q_ERR_CUDA;
+            const int64_t nvec = a.R * a.C / 8;
+            if (nvec > 0) {
+                int64_t grid = (int64_t)num_sms() * 4;
+                const int64_t need = (nvec + kThreads * 4 - 1) / (kThreads * 4);
+                if (need < grid) grid = need;
+                amax_kernel<<<(unsigned)grid, kThreads, 0, s>>>(a.x, nvec, a.amax, a.counters);
+                if (cudaGetLastError() != cudaSuccess) return FP8Q_ERR_CUDA;
+            }
+            return launch_tile_fmt<kCur>(a, rc->fmt, row, col, s);
+        }
+        case kDel: {
+            if (cudaMemsetAsync(a.amax, 0, sizeof(float), s) != cudaSuccess) return FP8Q_ERR_CUDA;
+            fp8q_status r = launch_tile_fmt<kDel>(a, rc->fmt, row, col, s);
+            if (r != FP8Q_OK) return r;
+            return launch_delayed_update(st, a.amax, a.counters + 2, s);
+        }
+        case kB1:
+            return launch_tile_fmt<kB1>(a, rc->fmt, row, col, s);
+        case kB128:
+            return launch_tile_fmt<kB128>(a, rc->fmt, row, col, s);
+        case kMX:
+            return launch_tile_fmt<kMX>(a, rc->fmt, row, col, s);
+        default:
+            return FP8Q_ERR_ARG;
+    }
+}
+
+fp8q_status launch_delayed_update(DelayedDev* st, const float* amax, const unsigned long long* nonfinite,
+                                  cudaStream_t s) {
+    delayed_update_kernel<<<1, 32, 0, s>>>(st, amax, nonfinite);
+    return cudaGetLastError() == cudaSuccess ? FP8Q_OK : FP8Q_ERR_CUDA;
+}
+
+fp8q_status launch_cast_bits(uint32_t start, uint64_t count, int fmt, uint8_t* out, cudaStream_t s) {
+    if (count == 0) return FP8Q_OK;
+    const uint64_t threads = (count + 3) / 4;
+    const uint64_t blocks = (threads + 255) / 256;
+    if (fmt == FP8Q_E4M3)
+        cast_bits_kernel<FP8Q_E4M3><<<(unsigned)blocks, 256, 0, s>>>(start, count, out);
+    else
+        cast_bits_kernel<FP8Q_E5M2><<<(unsigned)blocks, 256, 0, s>>>(start, count, out);
+    return cudaGetLastError() == cudaSuccess ? FP8Q_OK : FP8Q_ERR_CUDA;
+}
+
+}  // namespace fp8q

@@ -1,0 +1,245 @@
+/*
+ * fp8q -- FP8 scaled quantization and scaled GEMM for NVIDIA GB300 (sm_103a).
+ *
+ * C ABI of libfp8q.so.  Every entry point takes plain pointers and sizes; a
+ * "device" pointer is CUDA global memory of the current device, a "host"
+ * pointer is ordinary process memory.  `stream` is a cudaStream_t passed as
+ * void* (NULL = the legacy default stream).  All work is enqueued on that
+ * stream and returns without synchronising, except where a function says
+ * otherwise.  Host-side argument errors are returned before anything is
+ * enqueued; FP8Q_ERR_CUDA reports a failed launch or CUDA call.
+ *
+ * The method is FP8 training's quantize-then-scaled-GEMM as described by the
+ * web pages "2025 FP8 quantized-training guide" (blog.gitcode.com; cited as
+ * [guide]), bjdmk.com.cn/news/5220490 ([essay]) and "mastering FP8 LLM
+ * training 1.5x speedup" (nmedialink.com; [nemo]).
+ *
+ * Number formats ([guide] sec. 1.1; [essay] sec. 2):
+ *   FP8Q_E4M3  1 sign, 4 exponent (bias 7), 3 mantissa bits; max 448,
+ *              subnormals down to 2^-9, no Inf, NaN = S.1111.111
+ *              (torch.float8_e4m3fn).
+ *   FP8Q_E5M2  1/5/2 bits, bias 15; max 57344, subnormals down to 2^-16
+ *              (torch.float8_e5m2).
+ * The cast is saturating round-to-nearest-even: ties go to the even code,
+ * finite overflow and +-Inf clamp to +-max, NaN stays NaN.
+ *
+ * Layouts: every matrix is row-major.  x is bf16 [rows][cols].  The row-wise
+ * copy is uint8 [rows][cols]; the column-wise copy is the quantized transpose,
+ * uint8 [cols][rows].  Each copy carries scales in the layout of its own
+ * logical matrix (a copy of logical shape [R][C] with blocks along C):
+ *
+ *   kind                     scale buffer of a copy [R][C]            dequant
+ *   PERTENSOR_CURRENT/DELAYED none (scalar *scale / *scale_inv)         s_inv
+ *   BLOCK_1x128              fp32 [ceil(C/128)][Rp], Rp = R up to 128, d
+ *                            pad rows 1.0 (K-block-major)
+ *   BLOCK_128x128            fp32 [ceil(R/128)][ceil(C/128)]           d
+ *   MXFP8_1x32               E8M0 bytes in 128x4 tiles: tile (i, j) of  2^(code-127)
+ *                            512 B at (i * ceil(C/128) + j) * 512 holds
+ *                            rows 128i.., scale columns 4j..; row r,
+ *                            column k at (r%32)*16 + (r%128/32)*4 + k%4;
+ *                            pad entries 127
+ *
+ * The column-wise copy of BLOCK_1x128 and MXFP8_1x32 re-quantizes x^T with
+ * its blocks along the rows of x (the contraction dimension of the wgrad
+ * GEMM); for per-tensor and 128x128 kinds it is the byte transpose of the
+ * row-wise copy with the same (transposed) scales.
+ */
+#ifndef FP8Q_H
+#define FP8Q_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define FP8Q_API __attribute__((visibility("default")))
+#else
+#define FP8Q_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FP8Q_OK = 0,
+    FP8Q_ERR_ARG = 1,          /* NULL pointer, bad enum, bad flag combination */
+    FP8Q_ERR_SHAPE = 2,        /* negative or inconsistent sizes, size limits */
+    FP8Q_ERR_ALIGN = 3,        /* pointer or row pitch not 16-byte aligned */
+    FP8Q_ERR_DTYPE = 4,        /* format / recipe combination not allowed */
+    FP8Q_ERR_UNSUPPORTED = 5,  /* valid request this build does not implement */
+    FP8Q_ERR_CUDA = 6,         /* a CUDA call or kernel launch failed */
+    FP8Q_ERR_TIMEOUT = 7,      /* a bounded device wait gave up (see fp8q_device_errors) */
+    FP8Q_WARN_NONFINITE = 8    /* reserved: nonfinite inputs are reported via counters */
+} fp8q_status;
+
+typedef enum { FP8Q_E4M3 = 0, FP8Q_E5M2 = 1 } fp8q_format;
+
+/* Recipes: [guide] sec. 2.1-2.3, [nemo] scaling strategies 1-4. */
+typedef enum {
+    FP8Q_PERTENSOR_CURRENT = 0,  /* s = fmax / amax(x) of this tensor; q = sat_rne(x * s) */
+    FP8Q_PERTENSOR_DELAYED = 1,  /* s from the max of an amax history of past steps */
+    FP8Q_BLOCK_1x128 = 2,        /* d = amax / fmax per 1x128 block; q = sat_rne(x / d) */
+    FP8Q_BLOCK_128x128 = 3,      /* same per 128x128 tile (weights) */
+    FP8Q_MXFP8_1x32 = 4          /* e = floor(log2 amax) - emax_elem per 1x32 block,
+                                    E8M0 code e + 127, q = sat_rne(x * 2^-e) */
+} fp8q_recipe_kind;
+
+typedef struct {
+    int kind;           /* fp8q_recipe_kind */
+    int fmt;            /* fp8q_format of the quantized data */
+    int want_rowwise;   /* 1: write data_row (+ scale_row) */
+    int want_colwise;   /* 1: write data_col (+ scale_col) */
+} fp8q_recipe;
+
+/*
+ * Output of one quantize call.  All pointers are device memory owned by the
+ * caller; unused ones may be NULL.
+ *   data_row   uint8 [rows][cols]      (want_rowwise)
+ *   data_col   uint8 [cols][rows]      (want_colwise)
+ *   scale_row  scales of data_row      (block / MX kinds; size: fp8q_scale_bytes)
+ *   scale_col  scales of data_col
+ *   amax       fp32[1]  per-tensor kinds: max |x| over finite elements
+ *   scale      fp32[1]  per-tensor kinds: the multiplier s the cast used
+ *   scale_inv  fp32[1]  per-tensor kinds: fp32(1 / s), the GEMM's dequant scale
+ *   counters   uint64[3], always required: [0] elements of the row-wise cast
+ *              whose scaled fp32 value exceeded fmax (saturated), [1] the same
+ *              for a re-quantized column-wise copy (0 when the column-wise
+ *              copy is a byte transpose), [2] NaN / Inf elements of x.
+ * rows / cols / fmt / kind are filled in by fp8q_quantize and read by
+ * fp8q_scaled_gemm.
+ */
+typedef struct {
+    void* data_row;
+    void* data_col;
+    void* scale_row;
+    void* scale_col;
+    float* amax;
+    float* scale;
+    float* scale_inv;
+    unsigned long long* counters;
+    int64_t rows;
+    int64_t cols;
+    int fmt;
+    int kind;
+} fp8q_tensor;
+
+/* Opaque per-tensor delayed-scaling state, owned by the library: an amax ring
+ * of history_len fp32 entries, its head index, and the current s / s_inv, all
+ * in device memory of the device current at creation. */
+typedef struct fp8q_delayed_state fp8q_delayed_state;
+
+/* Version of this ABI (major * 100 + minor). */
+FP8Q_API int fp8q_version(void);
+
+/* Human-readable name of a status code (static string). */
+FP8Q_API const char* fp8q_status_str(fp8q_status s);
+
+/*
+ * Bytes of the scale buffers of a quantize call with this recipe and x shape
+ * [rows][cols]: *row_bytes for scale_row, *col_bytes for scale_col (0 for
+ * per-tensor kinds).  Either output pointer may be NULL.  Host only.
+ */
+FP8Q_API fp8q_status fp8q_scale_bytes(const fp8q_recipe* recipe, int64_t rows, int64_t cols,
+                             size_t* row_bytes, size_t* col_bytes);
+
+/*
+ * Quantize x (device, bf16 [rows][cols]) with `recipe` into `out` (host
+ * struct whose pointers are device buffers).  Sources: [guide] sec. 2.1
+ * (per-tensor current / delayed), 2.2 (blockwise), 2.3 (MXFP8); [nemo]
+ * strategies 1-4; [essay] sec. 3.3 (DelayedScaling margin / interval 1).
+ *
+ * Constraints: cols % 16 == 0; rows % 16 == 0 when want_colwise; x and every
+ * data / scale pointer 16-byte aligned; rows * cols < 2^40.  rows or cols 0
+ * is allowed (nothing but the per-tensor scalars and counters is written).
+ *
+ * Per-tensor current: amax over x first, then s = fmax / amax (amax 0 -> 1,
+ * +Inf -> FLT_MAX), scale_inv = 1 / s.  Per-tensor delayed: `st` (required,
+ * same fmt) supplies s; the call writes amax / scale / scale_inv / counters,
+ * then records amax in st's history and derives the next step's scale
+ * (st is left unchanged when x held a NaN / Inf).  Blockwise d = amax / fmax
+ * (amax 0 -> 1).  Amax always excludes NaN / Inf.  Counters are overwritten.
+ */
+FP8Q_API fp8q_status fp8q_quantize(const fp8q_recipe* recipe, const void* x, int64_t rows, int64_t cols,
+                          fp8q_delayed_state* st, fp8q_tensor* out, void* stream);
+
+/*
+ * Creates a delayed-scaling state on the current device: history_len in
+ * [1, 4096] (the [guide] sec. 2.1 history; 16 by default in the tests),
+ * margin in [0, 64] (s = fmax / max(history) * 2^-margin; [essay] sec. 3.3
+ * uses 0).  The history starts all zero, so the first step casts with s = 1.
+ * Allocates device memory (cudaMalloc) and synchronises.  *out receives the
+ * handle; free it with fp8q_delayed_destroy.
+ */
+FP8Q_API fp8q_status fp8q_delayed_create(int history_len, int fmt, int margin, fp8q_delayed_state** out);
+
+/*
+ * Records amax (device fp32[1]) as this step's amax and derives the next
+ * scale, on `stream`.  nonfinite (device uint64[1], may be NULL) nonzero
+ * leaves the state unchanged.  fp8q_quantize does this itself for the
+ * delayed kind; this entry point serves callers that combine amax values
+ * from elsewhere (e.g. a max over data-parallel replicas).
+ */
+FP8Q_API fp8q_status fp8q_delayed_update(fp8q_delayed_state* st, const float* amax,
+                                const unsigned long long* nonfinite, void* stream);
+
+/*
+ * Checkpoint: copies the state to host memory.  hist (host fp32
+ * [history_len]), head, scale and scale_inv may each be NULL.  Synchronises
+ * the device.
+ */
+FP8Q_API fp8q_status fp8q_delayed_get(const fp8q_delayed_state* st, float* hist, int* head,
+                             float* scale, float* scale_inv);
+
+/* Restore: overwrites history (host fp32 [history_len]), head, and the scale
+ * pair from host memory.  Synchronises the device. */
+FP8Q_API fp8q_status fp8q_delayed_set(fp8q_delayed_state* st, const float* hist, int head,
+                             float scale, float scale_inv);
+
+/* History length of a state (host). */
+FP8Q_API int fp8q_delayed_history_len(const fp8q_delayed_state* st);
+
+/* Frees a state (NULL is ignored). */
+FP8Q_API void fp8q_delayed_destroy(fp8q_delayed_state* st);
+
+/*
+ * Scaled FP8 GEMM, D[M][N] = A_q . B_q^T with fp32 accumulation ([guide]
+ * sec. 3.1: the fprop, dgrad and wgrad GEMMs take quantized inputs and keep
+ * BF16/FP32 outputs).  A_q is A's row-wise copy (a_use_col = 0, logical
+ * [A->rows][A->cols]) or column-wise copy (a_use_col = 1, logical
+ * [A->cols][A->rows]) and must be [M][K]; B_q likewise [N][K].  With a
+ * layer's X [T][H], W [F][H], dY [T][F]:
+ *   fprop  Y  = X . W^T     : A = X row,  B = W row   (M=T, N=F, K=H)
+ *   dgrad  dX = dY . W      : A = dY row, B = W col   (M=T, N=H, K=F)
+ *   wgrad  dW = dY^T . X    : A = dY col, B = X col   (M=F, N=H, K=T)
+ * Recipe pairs: both per-tensor (current or delayed, E4M3 / E5M2 in any
+ * mix): D = s_inv_A * s_inv_B * (q_A . q_B^T).  A BLOCK_1x128 with B
+ * BLOCK_128x128 or BLOCK_1x128 (E4M3 or E5M2): partial sums over each
+ * 128-wide K block are scaled by d_A[m][kb] * d_B[n(/128)][kb] and summed in
+ * fp32.  Both MXFP8_1x32: every 32-wide K block scaled by 2^(eA + eB) in the
+ * tensor core.
+ * out_dtype 0 = bf16 (RNE), 1 = fp32; D is device [M][N] row-major, 16-byte
+ * aligned, N % 8 == 0.  M, N, K >= 1; K % 16 == 0.  D is fully overwritten.
+ * A bounded wait inside the kernel that gives up records FP8Q_ERR_TIMEOUT in
+ * the word read by fp8q_device_errors and the kernel exits early.
+ */
+FP8Q_API fp8q_status fp8q_scaled_gemm(const fp8q_tensor* A, int a_use_col, const fp8q_tensor* B, int b_use_col,
+                             void* D, int out_dtype, int64_t M, int64_t N, int64_t K, void* stream);
+
+/*
+ * Reads and clears the library's device error word on the current device
+ * (bit 0: a GEMM pipeline wait timed out).  Synchronises `stream`.
+ */
+FP8Q_API fp8q_status fp8q_device_errors(unsigned int* flags, void* stream);
+
+/*
+ * The saturating RNE cast on its own: out[i] = cast(float with bit pattern
+ * start + i) for i < count (device uint8 out).  Serves exhaustive checks of
+ * the device conversion over all 2^32 fp32 inputs.
+ */
+FP8Q_API fp8q_status fp8q_cast_f32_bits(uint32_t start, uint64_t count, int fmt, void* out, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8Q_H */

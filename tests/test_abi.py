@@ -1,0 +1,113 @@
+"""CPU checks of the C ABI: the library loads, exports every entry point that
+include/fp8q.h declares, sizes scale buffers per the documented layouts, and
+rejects bad arguments before touching the GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from fp8_scaled_quantization_quantize_gb300 import _lib as L
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fp8q.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from fp8_scaled_quantization_quantize_gb300 import build
+    build.build()
+    return L.load()
+
+
+def declared():
+    src = open(HEADER).read()
+    return re.findall(r"FP8Q_API\s+[\w\s\*]+?\b(fp8q_\w+)\s*\(", src)
+
+
+def test_header_declares_the_boundary():
+    names = set(declared())
+    assert {"fp8q_quantize", "fp8q_scaled_gemm", "fp8q_delayed_create", "fp8q_delayed_update",
+            "fp8q_delayed_get", "fp8q_delayed_set", "fp8q_delayed_destroy", "fp8q_scale_bytes"} <= names
+    assert names == set(L.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared():
+        assert hasattr(lib, name), name
+
+
+def test_version_and_status_strings(lib):
+    assert lib.fp8q_version() == 100
+    assert L.status_str(L.OK) == "ok"
+    assert L.status_str(L.ERR_SHAPE) == "invalid shape"
+
+
+def _sb(lib, kind, rows, cols, row=True, col=True):
+    rc = L.Recipe(kind, L.E4M3, int(row), int(col))
+    rb, cb = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    st = lib.fp8q_scale_bytes(ctypes.byref(rc), rows, cols, ctypes.byref(rb), ctypes.byref(cb))
+    return st, rb.value, cb.value
+
+
+def test_scale_bytes(lib):
+    assert _sb(lib, L.PERTENSOR_CURRENT, 256, 256) == (L.OK, 0, 0)
+    # 1x128: [ceil(C/128)][R up to 128] fp32, and the column copy [ceil(R/128)][C up to 128]
+    assert _sb(lib, L.BLOCK_1x128, 4096, 4096) == (L.OK, 32 * 4096 * 4, 32 * 4096 * 4)
+    assert _sb(lib, L.BLOCK_1x128, 200, 272) == (L.OK, 3 * 256 * 4, 2 * 384 * 4)
+    # 128x128: [ceil(R/128)][ceil(C/128)] fp32
+    assert _sb(lib, L.BLOCK_128x128, 14336, 4096) == (L.OK, 112 * 32 * 4, 32 * 112 * 4)
+    # MX: 512-byte tiles of 128 rows x 4 scale columns
+    assert _sb(lib, L.MXFP8_1x32, 8192, 4096) == (L.OK, 64 * 32 * 512, 32 * 64 * 512)
+    assert _sb(lib, L.MXFP8_1x32, 130, 48, True, False) == (L.OK, 2 * 1 * 512, 0)
+    assert _sb(lib, 9, 16, 16)[0] == L.ERR_ARG
+    assert _sb(lib, L.MXFP8_1x32, -1, 16)[0] == L.ERR_SHAPE
+
+
+def _q(lib, kind=L.MXFP8_1x32, fmt=L.E4M3, rows=32, cols=32, row=True, col=False, x=16, t=None, st=None):
+    rc = L.Recipe(kind, fmt, int(row), int(col))
+    if t is None:
+        t = L.Tensor(16, 32, 64, 128, 256, 272, 288, 512, 0, 0, 0, 0)
+    return lib.fp8q_quantize(ctypes.byref(rc), x, rows, cols, st, ctypes.byref(t), None)
+
+
+def test_quantize_validation_without_gpu(lib):
+    assert _q(lib, cols=40) == L.ERR_SHAPE                  # cols % 16
+    assert _q(lib, rows=40, col=True) == L.ERR_SHAPE        # rows % 16 with a column copy
+    assert _q(lib, rows=-16) == L.ERR_SHAPE
+    assert _q(lib, kind=7) == L.ERR_ARG
+    assert _q(lib, fmt=3) == L.ERR_ARG
+    assert _q(lib, row=False, col=False) == L.ERR_ARG
+    assert _q(lib, x=24) == L.ERR_ALIGN                     # x not 16-byte aligned
+    assert _q(lib, x=0) == L.ERR_ARG                        # NULL x
+    t = L.Tensor(16, 32, 64, 128, 256, 272, 288, 0, 0, 0, 0, 0)
+    assert _q(lib, t=t) == L.ERR_ARG                        # NULL counters
+    t = L.Tensor(16, 32, 64 + 4, 128, 256, 272, 288, 512, 0, 0, 0, 0)
+    assert _q(lib, t=t) == L.ERR_ALIGN                      # misaligned scale buffer
+    assert _q(lib, kind=L.PERTENSOR_DELAYED) == L.ERR_ARG   # delayed needs a state
+    assert _q(lib, rows=1 << 30, cols=1 << 11) == L.ERR_SHAPE
+
+
+def test_gemm_validation_without_gpu(lib):
+    a = L.Tensor(16, 32, 64, 128, 256, 272, 288, 512, 64, 128, L.E4M3, L.MXFP8_1x32)
+    b = L.Tensor(16, 32, 64, 128, 256, 272, 288, 512, 96, 128, L.E4M3, L.MXFP8_1x32)
+    g = lambda M, N, K, od=0, ac=0, bc=0, A=a, B=b, D=1024: lib.fp8q_scaled_gemm(
+        ctypes.byref(A), ac, ctypes.byref(B), bc, D, od, M, N, K, None)
+    assert g(64, 96, 64) == L.ERR_SHAPE                     # K mismatch with the operands
+    assert g(64, 96, 128, od=2) == L.ERR_ARG
+    assert g(0, 96, 128) == L.ERR_SHAPE
+    assert g(64, 96, 128, D=1032) == L.ERR_ALIGN
+    pt = L.Tensor(16, 32, 64, 128, 256, 272, 288, 512, 96, 128, L.E4M3, L.PERTENSOR_CURRENT)
+    assert g(64, 96, 128, B=pt) == L.ERR_DTYPE              # MX with per-tensor
+    blk = L.Tensor(16, 32, 64, 128, 256, 272, 288, 512, 64, 128, L.E4M3, L.BLOCK_128x128)
+    blkb = L.Tensor(16, 32, 64, 128, 256, 272, 288, 512, 96, 128, L.E4M3, L.BLOCK_128x128)
+    assert g(64, 96, 128, A=blk, B=blkb) == L.ERR_DTYPE     # blockwise A must be 1x128
+
+
+def test_delayed_validation_without_gpu(lib):
+    h = ctypes.c_void_p(0)
+    assert lib.fp8q_delayed_create(0, L.E4M3, 0, ctypes.byref(h)) == L.ERR_ARG
+    assert lib.fp8q_delayed_create(16, 5, 0, ctypes.byref(h)) == L.ERR_ARG
+    assert lib.fp8q_delayed_create(16, L.E4M3, -1, ctypes.byref(h)) == L.ERR_ARG
+    assert lib.fp8q_delayed_update(None, None, None, None) == L.ERR_ARG
+    assert lib.fp8q_cast_f32_bits(0, 16, 9, 16, None) == L.ERR_ARG

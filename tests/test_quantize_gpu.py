@@ -1,0 +1,171 @@
+"""Parity of the CUDA quantize kernels with the oracle: every byte of every
+row-wise / column-wise copy, every scale (in the library's packed layout),
+the per-tensor scalars and the saturation / nonfinite counters bit-exact, on
+seeded inputs that span several 128x128 tiles with ragged edges, on the edge
+cases of each recipe, and at the full workload shapes."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from fp8_scaled_quantization_quantize_gb300 import inputs
+from tests._helpers import assert_quant_equal, bits_of, gpu_outputs
+
+pytestmark = pytest.mark.gpu
+
+KINDS = [O.PERTENSOR_CURRENT, O.BLOCK_1x128, O.BLOCK_128x128, O.MXFP8_1x32]
+COPIES = [(True, False), (False, True), (True, True)]
+
+
+def _api():
+    from fp8_scaled_quantization_quantize_gb300 import api
+    return api
+
+
+def _run(kind, fmt, x, rowwise, colwise, state=None, ostate=None, ctx=""):
+    api = _api()
+    qt = api.quantize(x.cuda(), kind, fmt, rowwise, colwise, state=state)
+    got = gpu_outputs(qt)
+    ref = O.quantize(kind, fmt, bits_of(x), rowwise, colwise, state=ostate)
+    assert_quant_equal(kind, got, ref, rowwise, colwise, ctx)
+    return qt, got, ref
+
+
+def _mixed(shape, seed):
+    """N(0,1) with 1% outliers x1000, a zeroed stripe, tiny subnormal-range
+    values and a few exact block-max ties."""
+    x = inputs.normal_f32(shape, seed)
+    x = inputs.with_outlier_elements(x, 0.01, 1000.0, seed + 7)
+    x[: min(3, shape[0]), :] = 0.0
+    g = np.random.default_rng(seed)
+    idx = g.choice(x.size, size=max(1, x.size // 200), replace=False)
+    x.reshape(-1)[idx] *= np.float32(2.0 ** -120)
+    return inputs.to_bf16(x)
+
+
+@pytest.mark.parametrize("kind", KINDS)
+@pytest.mark.parametrize("fmt", [O.E4M3, O.E5M2])
+@pytest.mark.parametrize("rowwise,colwise", COPIES)
+@pytest.mark.parametrize("shape", [(272, 400), (128, 128), (16, 16), (400, 1040)])
+def test_quantize_matches_oracle(kind, fmt, rowwise, colwise, shape):
+    x = _mixed(shape, 11 + shape[0])
+    _run(kind, fmt, x, rowwise, colwise, ctx=f"{kind} {fmt} {shape}")
+
+
+@pytest.mark.parametrize("kind", KINDS)
+def test_quantize_special_values(kind):
+    """NaN (both signs), +-Inf, -0, bf16 subnormals, bf16 max, all-zero blocks."""
+    x = inputs.normal_f32((256, 384), 3)
+    x[5, :] = 0.0
+    x[:, 200:232] = 0.0
+    x[7, 9] = np.inf
+    x[8, 10] = -np.inf
+    x[9, 11] = -0.0
+    x[10, 12:20] = np.float32(2.0 ** -130)
+    x[11, 300] = np.float32(3.3895e38)
+    xb = inputs.to_bf16(x)
+    xb[12, 13] = float("nan")          # torch stores 0x7FC0
+    bits = bits_of(xb).copy()
+    bits[13, 14] = 0xFFC1               # negative NaN with a payload
+    xb = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16)
+    for fmt in (O.E4M3, O.E5M2):
+        _run(kind, fmt, xb, True, True, ctx=f"special {kind} {fmt}")
+
+
+@pytest.mark.parametrize("kind", KINDS)
+def test_quantize_all_zero_and_empty(kind):
+    _run(kind, O.E4M3, torch.zeros((144, 160), dtype=torch.bfloat16), True, True, ctx="zeros")
+    api = _api()
+    for shape in ((0, 64), (32, 0), (0, 0)):
+        qt = api.quantize(torch.zeros(shape, dtype=torch.bfloat16, device="cuda"), kind, O.E4M3, True, True)
+        got = gpu_outputs(qt)
+        assert got["nonfinite"] == 0 and got["sat_row"] == 0
+        if kind == O.PERTENSOR_CURRENT:
+            assert got["scale"] == 1.0 and got["scale_inv"] == 1.0 and got["amax"] == 0.0
+
+
+def test_delayed_steps_and_checkpoint():
+    """32 steps of per-tensor delayed scaling (history 16, E5M2 as for dY)
+    against the oracle state machine, a spike and a NaN step included; then a
+    checkpoint restore replays steps 16..31 bit-exactly."""
+    api = _api()
+    mags = inputs.delayed_magnitudes(32)
+    st = api.DelayedState(16, O.E5M2, 0)
+    ost = O.Delayed(16, O.E5M2, 0)
+    saved = None
+    outs = []
+    xs = []
+    for t in range(32):
+        x = inputs.normal_bf16((96, 160), 500 + t, 1e-4 * float(mags[t, 2]))
+        if t == 25:
+            x[3, 3] = float("nan")
+        xs.append(x)
+        if t == 16:
+            saved = st.get()
+            osaved = (ost.hist.copy(), ost.head, ost.scale, ost.scale_inv)
+        _, got, ref = _run(O.PERTENSOR_DELAYED, O.E5M2, x, True, True, state=st, ostate=ost, ctx=f"step {t}")
+        outs.append(got)
+        hist, head, s, si = st.get()
+        assert head == ost.head and np.array_equal(np.float32(hist), ost.hist)
+        assert np.float32(s) == ost.scale and np.float32(si) == ost.scale_inv
+    assert osaved[1] == saved[1]
+    # restore and replay
+    st.set(*saved)
+    for t in range(16, 32):
+        qt = api.quantize(xs[t].cuda(), O.PERTENSOR_DELAYED, O.E5M2, True, True, state=st)
+        got = gpu_outputs(qt)
+        assert np.array_equal(got["data_row"], outs[t]["data_row"]) and got["scale"] == outs[t]["scale"]
+
+
+def test_delayed_update_entry_point():
+    api = _api()
+    st = api.DelayedState(4, O.E4M3, 1)
+    ost = O.Delayed(4, O.E4M3, 1)
+    for a in (3.0, 0.0, 17.5, 2.0, 1.0, 0.25):
+        st.update(torch.tensor([a], dtype=torch.float32, device="cuda"))
+        ost.update(a)
+        hist, head, s, si = st.get()
+        assert np.float32(s) == ost.scale and head == ost.head
+    nf = torch.tensor([1], dtype=torch.int64, device="cuda")
+    st.update(torch.tensor([1e6], dtype=torch.float32, device="cuda"), nf)
+    assert np.float32(st.get()[2]) == ost.scale
+
+
+CONFIG_SHAPES = [
+    # (name, kind, fmt, shape, rowwise, colwise, maker)
+    ("cfg1 A", O.PERTENSOR_CURRENT, O.E4M3, None, True, True, lambda: inputs.pertensor_256()[0]),
+    ("cfg2 X", O.BLOCK_1x128, O.E4M3, None, True, True, lambda: inputs.llama8b_up_proj()[0]),
+    ("cfg2 W", O.BLOCK_128x128, O.E4M3, None, True, True, lambda: inputs.llama8b_up_proj()[1]),
+    ("cfg3 X", O.MXFP8_1x32, O.E4M3, None, True, True, lambda: inputs.llama8b_mlp()[0]),
+]
+
+
+@pytest.mark.parametrize("name,kind,fmt,shape,rowwise,colwise,maker", CONFIG_SHAPES, ids=[c[0] for c in CONFIG_SHAPES])
+def test_quantize_full_config_shapes(name, kind, fmt, shape, rowwise, colwise, maker):
+    _run(kind, fmt, maker(), rowwise, colwise, ctx=name)
+
+
+def test_quantize_full_mx_dy_and_w():
+    X, W, dY = inputs.llama8b_mlp()
+    del X
+    _run(O.MXFP8_1x32, O.E4M3, W, True, True, ctx="cfg3 W")
+    _run(O.MXFP8_1x32, O.E4M3, dY, True, True, ctx="cfg3 dY")
+
+
+def test_quantize_sweep_tensor_pertensor_and_mx():
+    x = inputs.sweep_tensor(64)
+    _run(O.PERTENSOR_CURRENT, O.E4M3, x, True, False, ctx="sweep 64MiB current")
+    _run(O.MXFP8_1x32, O.E4M3, x, True, False, ctx="sweep 64MiB mx")
+
+
+def test_rejects_bad_arguments():
+    api = _api()
+    x = torch.zeros((32, 40), dtype=torch.bfloat16, device="cuda")   # cols % 16 != 0
+    with pytest.raises(api.Fp8qError) as e:
+        api.quantize(x, O.MXFP8_1x32, O.E4M3, True, False)
+    assert e.value.status == 2
+    x = torch.zeros((40, 32), dtype=torch.bfloat16, device="cuda")   # rows % 16 != 0 with colwise
+    with pytest.raises(api.Fp8qError):
+        api.quantize(x, O.BLOCK_1x128, O.E4M3, True, True)
+    with pytest.raises(api.Fp8qError):                                 # delayed without a state
+        api.quantize(torch.zeros((32, 32), dtype=torch.bfloat16, device="cuda"), O.PERTENSOR_DELAYED)
