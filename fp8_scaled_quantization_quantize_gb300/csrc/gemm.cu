@@ -1,9 +1,536 @@
-// Scaled FP8 GEMM (placeholder until the tcgen05 kernels land).
+// Scaled FP8 GEMM on the 5th-generation tensor cores (tcgen05) of sm_103a.
+//
+// D[M][N] = A_q[M][K] . B_q[N][K]^T, both operands K-contiguous ("2025 FP8
+// quantized-training guide", sec. 3.1: fprop / dgrad / wgrad take quantized
+// inputs, outputs stay BF16 / FP32).  Three scale treatments:
+//   per-tensor   one MMA chain per tile, D = s_inv_A * s_inv_B * acc in the
+//                epilogue (sec. 2.1);
+//   MXFP8        kind::mxf8f6f4.block_scale: the tensor core applies the E8M0
+//                scale of every 32-wide K block itself (sec. 2.3; "mastering FP8
+//                LLM training", strategy 4: hardware-native on Blackwell);
+//   blockwise    each 128-wide K block is its own MMA chain into one of two
+//                TMEM buffers; the epilogue warps scale that partial by
+//                d_A[m][kb] * d_B[n(/128)][kb] and add it to fp32 register
+//                accumulators (sec. 2.2 1x128 x 128x128 tiles, or 1x128 x 1x128).
+//
+// Persistent kernel, one CTA per SM, 320 threads:
+//   warp 0      TMA producer: A box 128x128 B, B box 256x128 B (128-byte
+//               swizzle) per stage, plus the MX scale tiles (bulk copies);
+//   warp 1      TMEM allocator and single-thread MMA issuer (M128 N256 K32);
+//   warps 2-9   epilogue: warp w reads TMEM lanes 32 (w % 4) .. +31 (its rows)
+//               and columns 128 ((w - 2) / 4) .. +127.
+// Every mbarrier wait is bounded (about one second of %globaltimer); a wait
+// that gives up sets bit 0 of g_device_errors, raises a CTA-wide abort flag,
+// and the CTA drains its in-flight copies and MMAs (bounded) and frees TMEM.
+#include <cuda.h>
+
 #include "fp8q_internal.cuh"
 
 namespace fp8q {
 
 __device__ unsigned int g_device_errors = 0;
+
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 128, STAGES = 4;
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 64 + 32 * kEpiWarps;
+constexpr uint32_t A_STAGE = BM * BK, B_STAGE = BN * BK;
+constexpr uint32_t SFA_STAGE = 512, SFB_STAGE = 1024;
+constexpr uint32_t OFF_A = 0;
+constexpr uint32_t OFF_B = OFF_A + STAGES * A_STAGE;
+constexpr uint32_t OFF_SFA = OFF_B + STAGES * B_STAGE;
+constexpr uint32_t OFF_SFB = OFF_SFA + STAGES * SFA_STAGE;
+constexpr uint32_t OFF_SBW = OFF_SFB + STAGES * SFB_STAGE;      // per-epilogue-warp 1x128 B scales
+constexpr uint32_t OFF_BAR = OFF_SBW + kEpiWarps * 128 * 4;
+constexpr uint32_t NBARS = 2 * STAGES + 5;
+constexpr uint32_t OFF_MISC = OFF_BAR + 8 * NBARS;
+constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;            // + alignment slack
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t SF_TMEM_COL = 256;                            // MX scale slots: 12 columns per stage
+constexpr uint64_t kWaitNs = 1000000000ull;
+
+enum { REC_PT = 0, REC_MX = 1, REC_B2D = 2, REC_B1D = 3 };
+
+struct Params {
+    int64_t M, N, K;
+    int64_t tiles_m, tiles_n, nkb;
+    void* D;
+    const float* sa_inv;    // per-tensor
+    const float* sb_inv;
+    const uint8_t* sfa;     // MX packed tiles
+    const uint8_t* sfb;
+    const float* bsa;       // blockwise [nkb][Mp]
+    const float* bsb;       // [nkb][Np] (1x128) or [ceil(N/128)][nkb] (128x128)
+    int64_t Mp, Np, nbn128;
+    uint32_t idesc;
+};
+
+// ------------------------------------------------------------ PTX wrappers
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ uint64_t gtimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t a, uint32_t n) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(a), "r"(n) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t a, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(a), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t a) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(a) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint32_t a, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(a), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait on an mbarrier phase; false on abort or timeout.
+__device__ __noinline__ bool mbar_wait(uint32_t a, uint32_t parity, volatile int* abort_flag) {
+    if (mbar_try(a, parity)) return true;
+    const uint64_t t0 = gtimer();
+    while (true) {
+        if (mbar_try(a, parity)) return true;
+        if (*abort_flag) return false;
+        if (gtimer() - t0 > kWaitNs) {
+            atomicOr(&g_device_errors, 1u);
+            *abort_flag = 1;
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t mbar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            dst),
+        "l"(map), "r"(x), "r"(y), "r"(mbar)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t mbar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(mbar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_commit(uint32_t mbar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(mbar) : "memory");
+}
+
+// Shared-memory matrix descriptor: start >> 4, leading byte offset >> 4,
+// stride byte offset >> 4, fixed 0b001 at bit 46, swizzle mode at bit 61.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo, uint32_t swz) {
+    return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | ((uint64_t)swz << 61);
+}
+// K-major operand tile, rows of 128 bytes in the 128-byte swizzle: 8-row
+// groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t addr) { return smem_desc(addr, 16, 1024, 2); }
+
+__device__ __forceinline__ void mma_f8(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc));
+}
+__device__ __forceinline__ void mma_mx(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
+                                       uint32_t sfb, uint32_t acc) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n}\n" ::"r"(
+            d),
+        "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc));
+}
+__device__ __forceinline__ void tc_cp_32x128b(uint32_t taddr, uint64_t desc) {
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc));
+}
+
+#define FP8Q_LD32(addr, r)                                                                                          \
+    asm volatile(                                                                                                   \
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18," \
+        "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"                                              \
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),         \
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),    \
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),  \
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])   \
+        : "r"(addr))
+
+__device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Tile order: groups of 8 M-blocks, N-blocks outer inside a group, so the
+// CTAs working at one time share A and B panels in L2.
+__device__ __forceinline__ void tile_coords(int64_t t, int64_t tiles_m, int64_t tiles_n, int64_t& mb, int64_t& nb) {
+    const int64_t G = 8;
+    const int64_t group = t / (G * tiles_n);
+    const int64_t first = group * G;
+    const int64_t gs = (tiles_m - first) < G ? (tiles_m - first) : G;
+    const int64_t in = t - group * G * tiles_n;
+    mb = first + in % gs;
+    nb = in / gs;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));
+    return r;
+}
+
+// Writes 32 consecutive fp32 results of one output row (masked by N).
+template <bool OUT_F32>
+__device__ __forceinline__ void store_row32(const Params& p, int64_t row, int64_t col, const float* v) {
+    if (OUT_F32) {
+        float* dst = (float*)p.D + row * p.N + col;
+#pragma unroll
+        for (int j = 0; j < 32; j += 4)
+            if (col + j < p.N) *(float4*)(dst + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+    } else {
+        uint16_t* dst = (uint16_t*)p.D + row * p.N + col;
+#pragma unroll
+        for (int j = 0; j < 32; j += 8)
+            if (col + j < p.N)
+                *(uint4*)(dst + j) = make_uint4(pack_bf16(v[j], v[j + 1]), pack_bf16(v[j + 2], v[j + 3]),
+                                                pack_bf16(v[j + 4], v[j + 5]), pack_bf16(v[j + 6], v[j + 7]));
+    }
+}
+
+template <int REC, bool OUT_F32>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    const uint32_t sb = smem_u32(smem);
+    auto full = [&](int s) { return sb + OFF_BAR + 8u * s; };
+    auto empty = [&](int s) { return sb + OFF_BAR + 8u * (STAGES + s); };
+    auto tfull = [&](int b) { return sb + OFF_BAR + 8u * (2 * STAGES + b); };
+    auto tempty = [&](int b) { return sb + OFF_BAR + 8u * (2 * STAGES + 2 + b); };
+    const uint32_t mma_done = sb + OFF_BAR + 8u * (2 * STAGES + 4);
+    uint32_t* tmem_slot = (uint32_t*)(smem + OFF_MISC);
+    volatile int* abort_flag = (volatile int*)(smem + OFF_MISC + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full(s), 1);
+            mbar_init(empty(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(tfull(b), 1);
+            mbar_init(tempty(b), kEpiWarps);
+        }
+        mbar_init(mma_done, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0 && lane == 0) {
+        asm volatile("prefetch.tensormap [%0];" ::"l"(&tmA) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(&tmB) : "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const int64_t ntiles = p.tiles_m * p.tiles_n;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            uint32_t filled = 0, fill_par = 0;  // per-stage bits for the abort drain
+            bool ok = true;
+            for (int64_t t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+                int64_t mb, nb;
+                tile_coords(t, p.tiles_m, p.tiles_n, mb, nb);
+                const bool b2 = (2 * nb + 1) < p.nbn128;  // second 128-row scale tile of B exists
+                for (int64_t kb = 0; kb < p.nkb; ++kb) {
+                    if (!mbar_wait(empty(s), ph ^ 1u, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    uint32_t bytes = A_STAGE + B_STAGE;
+                    if (REC == REC_MX) bytes += SFA_STAGE + (b2 ? 1024u : 512u);
+                    mbar_expect_tx(full(s), bytes);
+                    tma_load_2d(sb + OFF_A + s * A_STAGE, &tmA, (int)(kb * BK), (int)(mb * BM), full(s));
+                    tma_load_2d(sb + OFF_B + s * B_STAGE, &tmB, (int)(kb * BK), (int)(nb * BN), full(s));
+                    if (REC == REC_MX) {
+                        bulk_load(sb + OFF_SFA + s * SFA_STAGE, p.sfa + (mb * p.nkb + kb) * 512, 512, full(s));
+                        bulk_load(sb + OFF_SFB + s * SFB_STAGE, p.sfb + (2 * nb * p.nkb + kb) * 512, 512, full(s));
+                        if (b2)
+                            bulk_load(sb + OFF_SFB + s * SFB_STAGE + 512, p.sfb + ((2 * nb + 1) * p.nkb + kb) * 512,
+                                      512, full(s));
+                    }
+                    filled |= 1u << s;
+                    fill_par = (fill_par & ~(1u << s)) | (ph << s);
+                    if (++s == STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            if (*abort_flag) {
+                // let copies already issued land before the CTA exits (bounded)
+                for (int i = 0; i < STAGES; ++i) {
+                    if (!(filled >> i & 1u)) continue;
+                    const uint64_t t0 = gtimer();
+                    while (!mbar_try(full(i), (fill_par >> i) & 1u) && gtimer() - t0 < kWaitNs / 10) {
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            uint32_t tile_i = 0;
+            uint64_t kbg = 0;
+            bool ok = true;
+            for (int64_t t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++tile_i) {
+                if (REC == REC_PT || REC == REC_MX) {
+                    if (!mbar_wait(tempty(0), (tile_i & 1u) ^ 1u, abort_flag)) break;
+                    tc_fence_after();
+                }
+                for (int64_t kb = 0; kb < p.nkb; ++kb) {
+                    uint32_t dcol = 0;
+                    if (REC == REC_B2D || REC == REC_B1D) {
+                        const uint32_t buf = (uint32_t)(kbg & 1u);
+                        if (!mbar_wait(tempty(buf), (uint32_t)((kbg >> 1) & 1u) ^ 1u, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        dcol = buf * BN;
+                    }
+                    if (!mbar_wait(full(s), ph, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a0 = sb + OFF_A + s * A_STAGE, b0 = sb + OFF_B + s * B_STAGE;
+                    if (REC == REC_MX) {
+                        const uint32_t sfa_t = tmem + SF_TMEM_COL + 12u * s;
+                        tc_cp_32x128b(sfa_t, smem_desc(sb + OFF_SFA + s * SFA_STAGE, 0, 128, 0));
+                        tc_cp_32x128b(sfa_t + 4, smem_desc(sb + OFF_SFB + s * SFB_STAGE, 0, 128, 0));
+                        tc_cp_32x128b(sfa_t + 8, smem_desc(sb + OFF_SFB + s * SFB_STAGE + 512, 0, 128, 0));
+#pragma unroll
+                        for (int k = 0; k < BK / 32; ++k) {
+                            const uint32_t idesc = p.idesc | ((uint32_t)k << 4) | ((uint32_t)k << 29);
+                            mma_mx(tmem, desc_sw128(a0 + 32 * k), desc_sw128(b0 + 32 * k), idesc, sfa_t, sfa_t + 4,
+                                   (kb > 0 || k > 0) ? 1u : 0u);
+                        }
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < BK / 32; ++k) {
+                            const uint32_t acc = (REC == REC_PT) ? ((kb > 0 || k > 0) ? 1u : 0u) : (k > 0 ? 1u : 0u);
+                            mma_f8(tmem + dcol, desc_sw128(a0 + 32 * k), desc_sw128(b0 + 32 * k), p.idesc, acc);
+                        }
+                    }
+                    tc_commit(empty(s));
+                    if (REC == REC_B2D || REC == REC_B1D) {
+                        tc_commit(tfull((uint32_t)(kbg & 1u)));
+                        ++kbg;
+                    }
+                    if (++s == STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                if (REC == REC_PT || REC == REC_MX) tc_commit(tfull(0));
+            }
+            // every MMA / copy this thread issued has completed once mma_done fires
+            tc_commit(mma_done);
+            const uint64_t t0 = gtimer();
+            while (!mbar_try(mma_done, 0) && gtimer() - t0 < kWaitNs) {
+            }
+        }
+    } else {
+        // ------------------------------------------------ epilogue warps
+        const int ew = warp - 2, q = warp & 3, h = ew >> 2;
+        const uint32_t lane_base = (uint32_t)(32 * q) << 16;
+        float sab = 1.0f;
+        if (REC == REC_PT) sab = __fmul_rn(*p.sa_inv, *p.sb_inv);
+        float* sbw = (float*)(smem + OFF_SBW) + ew * 128;
+        uint32_t tile_i = 0;
+        uint64_t kbg = 0;
+        for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++tile_i) {
+            int64_t mb, nb;
+            tile_coords(t, p.tiles_m, p.tiles_n, mb, nb);
+            const int64_t row = mb * BM + 32 * q + lane;
+            const int64_t col0 = nb * BN + 128 * h;
+            if (REC == REC_PT || REC == REC_MX) {
+                if (!mbar_wait(tfull(0), tile_i & 1u, abort_flag)) break;
+                tc_fence_after();
+                // drain the accumulator into registers, hand TMEM back, then store
+                uint32_t r[128];
+                FP8Q_LD32(tmem + lane_base + 128 * h, r);
+                FP8Q_LD32(tmem + lane_base + 128 * h + 32, (r + 32));
+                FP8Q_LD32(tmem + lane_base + 128 * h + 64, (r + 64));
+                FP8Q_LD32(tmem + lane_base + 128 * h + 96, (r + 96));
+                tc_wait_ld();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tempty(0));
+                if (row < p.M) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        float v[32];
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[32 * c + j]) * sab;
+                        store_row32<OUT_F32>(p, row, col0 + 32 * c, v);
+                    }
+                }
+            } else {
+                float acc[128];
+#pragma unroll
+                for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
+                const bool hvalid = (col0 < p.N);
+                float sa_next = p.bsa[row];  // kb = 0 (row < Mp always)
+                bool ok = true;
+                for (int64_t kb = 0; kb < p.nkb; ++kb, ++kbg) {
+                    const float sa = sa_next;
+                    if (kb + 1 < p.nkb) sa_next = p.bsa[(kb + 1) * p.Mp + row];
+                    float sbk = 0.0f;
+                    if (REC == REC_B2D) {
+                        const int64_t nblk = 2 * nb + h;
+                        sbk = (nblk < p.nbn128) ? p.bsb[nblk * p.nkb + kb] : 0.0f;
+                    } else {
+                        __syncwarp();
+                        float4 v4 = make_float4(0.f, 0.f, 0.f, 0.f);
+                        if (hvalid) v4 = *(const float4*)(p.bsb + kb * p.Np + col0 + 4 * lane);
+                        *(float4*)(sbw + 4 * lane) = v4;
+                        __syncwarp();
+                    }
+                    const uint32_t buf = (uint32_t)(kbg & 1u);
+                    if (!mbar_wait(tfull(buf), (uint32_t)((kbg >> 1) & 1u), abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t r[32];
+                        FP8Q_LD32(tmem + lane_base + buf * BN + 128 * h + 32 * c, r);
+                        tc_wait_ld();
+                        if (REC == REC_B2D) {
+                            const float sc = __fmul_rn(sa, sbk);
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) acc[32 * c + j] = fmaf(__uint_as_float(r[j]), sc, acc[32 * c + j]);
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 32; j += 4) {
+                                const float4 s4 = *(const float4*)(sbw + 32 * c + j);
+                                acc[32 * c + j] = fmaf(__uint_as_float(r[j]), __fmul_rn(sa, s4.x), acc[32 * c + j]);
+                                acc[32 * c + j + 1] =
+                                    fmaf(__uint_as_float(r[j + 1]), __fmul_rn(sa, s4.y), acc[32 * c + j + 1]);
+                                acc[32 * c + j + 2] =
+                                    fmaf(__uint_as_float(r[j + 2]), __fmul_rn(sa, s4.z), acc[32 * c + j + 2]);
+                                acc[32 * c + j + 3] =
+                                    fmaf(__uint_as_float(r[j + 3]), __fmul_rn(sa, s4.w), acc[32 * c + j + 3]);
+                            }
+                        }
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(tempty(buf));
+                }
+                if (!ok) break;
+                if (row < p.M) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) store_row32<OUT_F32>(p, row, col0 + 32 * c, acc + 32 * c);
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
+    }
+}
+
+// ------------------------------------------------------------------ host
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (EncodeTiledFn)p;
+    }
+    return fn;
+}
+
+// 2-D map over a K-contiguous uint8 matrix [rows][K], box 128 bytes x box_rows, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t K, uint32_t box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)K};
+    cuuint32_t box[2] = {128, box_rows};
+    cuuint32_t es[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int g_sms = 0;
+
+template <int REC, bool F32>
+fp8q_status launch_t(const CUtensorMap& ma, const CUtensorMap& mb, const Params& p, cudaStream_t s) {
+    auto kern = gemm_kernel<REC, F32>;
+    static bool attr = false;
+    if (!attr) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) != cudaSuccess)
+            return FP8Q_ERR_CUDA;
+        attr = true;
+    }
+    if (g_sms == 0) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&g_sms, cudaDevAttrMultiProcessorCount, dev);
+        if (g_sms < 1) g_sms = 1;
+    }
+    const int64_t ntiles = p.tiles_m * p.tiles_n;
+    const int grid = (int)(ntiles < g_sms ? ntiles : g_sms);
+    kern<<<grid, kThreads, SMEM_BYTES, s>>>(ma, mb, p);
+    return cudaGetLastError() == cudaSuccess ? FP8Q_OK : FP8Q_ERR_CUDA;
+}
+
+template <int REC>
+fp8q_status launch_rec(const CUtensorMap& ma, const CUtensorMap& mb, const Params& p, int out_dtype, cudaStream_t s) {
+    return out_dtype == 1 ? launch_t<REC, true>(ma, mb, p, s) : launch_t<REC, false>(ma, mb, p, s);
+}
+
+}  // namespace
 
 fp8q_status read_device_errors(unsigned int* flags, cudaStream_t s) {
     if (cudaStreamSynchronize(s) != cudaSuccess) return FP8Q_ERR_CUDA;
@@ -15,9 +542,44 @@ fp8q_status read_device_errors(unsigned int* flags, cudaStream_t s) {
     return FP8Q_OK;
 }
 
-fp8q_status launch_gemm(const GemmOperand&, const GemmOperand&, void*, int, int64_t, int64_t, int64_t,
-                        cudaStream_t) {
-    return FP8Q_ERR_UNSUPPORTED;
+fp8q_status launch_gemm(const GemmOperand& A, const GemmOperand& B, void* D, int out_dtype, int64_t M, int64_t N,
+                        int64_t K, cudaStream_t s) {
+    if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return FP8Q_ERR_SHAPE;
+    CUtensorMap ma, mb;
+    if (!make_map(&ma, A.data, M, K, BM) || !make_map(&mb, B.data, N, K, BN)) return FP8Q_ERR_CUDA;
+    Params p;
+    memset(&p, 0, sizeof(p));
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.tiles_m = (M + BM - 1) / BM;
+    p.tiles_n = (N + BN - 1) / BN;
+    p.nkb = (K + BK - 1) / BK;
+    p.D = D;
+    p.Mp = p.tiles_m * BM;
+    p.Np = (N + 127) / 128 * 128;
+    p.nbn128 = (N + 127) / 128;
+    const bool pt = A.kind == FP8Q_PERTENSOR_CURRENT || A.kind == FP8Q_PERTENSOR_DELAYED;
+    // instruction descriptor: M = 128 (bits 24-28: M >> 4), N = 256 (bits 17-22: N >> 3),
+    // A / B formats at bits 7-9 / 10-12 (0 = E4M3, 1 = E5M2)
+    const uint32_t shape = ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+    const uint32_t fmts = ((uint32_t)A.fmt << 7) | ((uint32_t)B.fmt << 10);
+    if (A.kind == FP8Q_MXFP8_1x32) {
+        p.sfa = (const uint8_t*)A.scale;
+        p.sfb = (const uint8_t*)B.scale;
+        p.idesc = shape | fmts | (1u << 23);  // scale type UE8M0; scale-factor ids added per MMA
+        return launch_rec<REC_MX>(ma, mb, p, out_dtype, s);
+    }
+    p.idesc = shape | fmts | (1u << 4);  // D format F32
+    if (pt) {
+        p.sa_inv = A.scale_inv;
+        p.sb_inv = B.scale_inv;
+        return launch_rec<REC_PT>(ma, mb, p, out_dtype, s);
+    }
+    p.bsa = (const float*)A.scale;
+    p.bsb = (const float*)B.scale;
+    if (B.kind == FP8Q_BLOCK_128x128) return launch_rec<REC_B2D>(ma, mb, p, out_dtype, s);
+    return launch_rec<REC_B1D>(ma, mb, p, out_dtype, s);
 }
 
 }  // namespace fp8q

@@ -47,6 +47,15 @@ __device__ __forceinline__ uint32_t vec_absmax(const uint4& v, uint32_t& nonfini
     return a > c ? a : c;
 }
 
+// The hardware conversion returns the canonical NaN 0x7F whatever the input's
+// sign; a NaN keeps its sign bit here (S.1111111, as torch's float8 casts do).
+// q holds the codes of the two bf16 of w in its low (x0) and next (x1) byte.
+__device__ __forceinline__ uint32_t nan_sign2(uint32_t q, uint32_t w) {
+    if ((w & 0x7FFFu) > 0x7F80u) q = (q & ~0xFFu) | ((w >> 8) & 0x80u) | 0x7Fu;
+    if ((w & 0x7FFF0000u) > 0x7F800000u) q = (q & ~0xFF00u) | ((w >> 16) & 0x8000u) | 0x7F00u;
+    return q;
+}
+
 // Scaled value of one element for the recipe's scale rule.
 template <int KIND>
 __device__ __forceinline__ float scaled(float x, float k) {
@@ -63,7 +72,7 @@ __device__ __forceinline__ uint32_t sat_count(float x, float y) {
 
 // Converts the 8 bf16 of v with factor k; returns 8 codes, counts saturation.
 template <int KIND, int FMT>
-__device__ __forceinline__ uint2 convert8(const uint4& v, float k, uint32_t& nsat) {
+__device__ __forceinline__ uint2 convert8(const uint4& v, float k, uint32_t& nsat, bool nonfinite) {
     float f[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
                   bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
     float y[8];
@@ -72,7 +81,12 @@ __device__ __forceinline__ uint2 convert8(const uint4& v, float k, uint32_t& nsa
         y[j] = scaled<KIND>(f[j], k);
         nsat += sat_count<FMT>(f[j], y[j]);
     }
-    return make_uint2(cvt4<FMT>(y[0], y[1], y[2], y[3]), cvt4<FMT>(y[4], y[5], y[6], y[7]));
+    uint2 q = make_uint2(cvt4<FMT>(y[0], y[1], y[2], y[3]), cvt4<FMT>(y[4], y[5], y[6], y[7]));
+    if (nonfinite) {
+        q.x = nan_sign2(q.x & 0xFFFFu, v.x) | (nan_sign2(q.x >> 16, v.y) << 16);
+        q.y = nan_sign2(q.y & 0xFFFFu, v.z) | (nan_sign2(q.y >> 16, v.w) << 16);
+    }
+    return q;
 }
 
 template <int KIND, int FMT>
@@ -118,8 +132,13 @@ __global__ void __launch_bounds__(kThreads) quant_tile_kernel(QuantArgs a) {
             v[i] = (cin && r < a.R) ? ld_nc_v4(a.x + r * a.C + c) : make_uint4(0, 0, 0, 0);
         }
         uint32_t vmax[8];
+        uint32_t vnf = 0;  // bit i: vector i holds a NaN / Inf
 #pragma unroll
-        for (int i = 0; i < 8; ++i) vmax[i] = vec_absmax(v[i], nnf);
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t before = nnf;
+            vmax[i] = vec_absmax(v[i], nnf);
+            vnf |= (nnf != before ? 1u : 0u) << i;
+        }
 
         // 128x128 tile amax (also the delayed recipe's running tensor amax)
         float kd_tile = 1.0f;
@@ -183,7 +202,7 @@ __global__ void __launch_bounds__(kThreads) quant_tile_kernel(QuantArgs a) {
                         *(uint32_t*)(tileb + (rr & 31) * 16 + (rr >> 5) * 4) = code | (c1 << 8) | (c2 << 16) | (c3 << 24);
                     }
                 }
-                const uint2 q = convert8<KIND, FMT>(v[i], k, nsat_row);
+                const uint2 q = convert8<KIND, FMT>(v[i], k, nsat_row, (vnf >> i) & 1u);
                 if (cin && r < a.R) *(uint2*)(a.q_row + r * a.C + c) = q;
             }
         }
@@ -192,7 +211,7 @@ __global__ void __launch_bounds__(kThreads) quant_tile_kernel(QuantArgs a) {
         if constexpr (COL) {
 #pragma unroll
             for (int i = 0; i < 8; ++i) *(uint4*)&tile[(rsub + 16 * i) * (kTile / 2) + vcol * 4] = v[i];
-            __syncthreads();
+            const bool tile_nf = __syncthreads_or(vnf != 0) != 0;
             const int p = t & 63, qd = t >> 6;  // column pair, 32-row quarter
             uint32_t w[32];
 #pragma unroll
@@ -257,6 +276,13 @@ __global__ void __launch_bounds__(kThreads) quant_tile_kernel(QuantArgs a) {
                 }
                 o0[j / 4] = cvt4<FMT>(ya0, ya1, ya2, ya3);
                 o1[j / 4] = cvt4<FMT>(yb0, yb1, yb2, yb3);
+                if (tile_nf) {
+                    // rebuild the bf16 pairs of each output column to reuse nan_sign2
+                    const uint32_t a01 = (w[j] & 0xFFFFu) | (w[j + 1] << 16), a23 = (w[j + 2] & 0xFFFFu) | (w[j + 3] << 16);
+                    const uint32_t b01 = (w[j] >> 16) | (w[j + 1] & 0xFFFF0000u), b23 = (w[j + 2] >> 16) | (w[j + 3] & 0xFFFF0000u);
+                    o0[j / 4] = nan_sign2(o0[j / 4] & 0xFFFFu, a01) | (nan_sign2(o0[j / 4] >> 16, a23) << 16);
+                    o1[j / 4] = nan_sign2(o1[j / 4] & 0xFFFFu, b01) | (nan_sign2(o1[j / 4] >> 16, b23) << 16);
+                }
             }
             nsat_col += ns;
             const int64_t cc = c0 + 2 * p, rr = r0 + 32 * qd;
@@ -355,7 +381,12 @@ __global__ void cast_bits_kernel(uint32_t start, uint64_t count, uint8_t* out) {
     float f[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) f[j] = __uint_as_float((uint32_t)(start + i0 + j));
-    const uint32_t q = cvt4<FMT>(f[0], f[1], f[2], f[3]);
+    uint32_t q = cvt4<FMT>(f[0], f[1], f[2], f[3]);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t u = __float_as_uint(f[j]);
+        if ((u & 0x7FFFFFFFu) > 0x7F800000u) q = (q & ~(0xFFu << (8 * j))) | ((((u >> 24) & 0x80u) | 0x7Fu) << (8 * j));
+    }
     if (i0 + 4 <= count) {
         *(uint32_t*)(out + i0) = q;
     } else {

@@ -1,0 +1,168 @@
+"""Parity of the tcgen05 scaled GEMM with the oracle's fp64 dequantize-and-sum
+GEMM on the same quantized operands (the GPU's own quantize outputs, which
+the quantize tests pin bit-exactly to the oracle).  Bar: normwise relative
+error ||D - D64||_F / ||D64||_F <= 2e-3 (bf16 output rounding alone gives
+about 1.5e-3), plus a per-element bound for fp32 output."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from fp8_scaled_quantization_quantize_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+TOL = 2e-3
+
+
+def _api():
+    from fp8_scaled_quantization_quantize_gb300 import api
+    return api
+
+
+def _host_scales(api, qt, use_col):
+    """Plain-layout dequantization scales of a quantized copy for the oracle
+    GEMM: (array, block rows, block cols)."""
+    R, C = (qt.cols, qt.rows) if use_col else (qt.rows, qt.cols)
+    if qt.kind in (api.PERTENSOR_CURRENT, api.PERTENSOR_DELAYED):
+        return np.array([[qt.scale_inv.item()]], dtype=np.float32), max(R, 1), max(C, 1)
+    buf = (qt.scale_col if use_col else qt.scale_row).cpu().numpy()
+    if qt.kind == api.BLOCK_128x128:
+        return buf.view(np.float32)[: -(-R // 128) * -(-C // 128)].reshape(-(-R // 128), -(-C // 128)), 128, 128
+    if qt.kind == api.BLOCK_1x128:
+        Rp = -(-R // 128) * 128
+        packed = buf.view(np.float32)[: -(-C // 128) * Rp].reshape(-(-C // 128), Rp)
+        return np.ascontiguousarray(packed[:, :R].T), 1, 128
+    if qt.kind == api.MXFP8_1x32:
+        S = -(-C // 32)
+        tiles_c = -(-C // 128)
+        r = np.arange(R)[:, None]
+        c = np.arange(S)[None, :]
+        off = ((r // 128) * tiles_c + c // 4) * 512 + (r % 32) * 16 + ((r % 128) // 32) * 4 + c % 4
+        codes = buf[off].astype(np.int32)
+        return np.ldexp(np.float32(1), codes - 127).astype(np.float32), 1, 32
+    raise ValueError(qt.kind)
+
+
+def _operand(api, qt, use_col):
+    data = (qt.data_col if use_col else qt.data_row).cpu().numpy()
+    s, bm, bk = _host_scales(api, qt, use_col)
+    return data, qt.fmt, s, bm, bk
+
+
+def _check(api, qa, ac, qb, bc, out_dtype=torch.bfloat16, sample=None, ctx=""):
+    D = api.scaled_gemm(qa, ac, qb, bc, out_dtype)
+    torch.cuda.synchronize()
+    A, fa, sa, abm, abk = _operand(api, qa, ac)
+    B, fb, sbb, bbn, bbk = _operand(api, qb, bc)
+    M, N = A.shape[0], B.shape[0]
+    if sample is None:
+        pm, pn = [g.ravel() for g in np.meshgrid(np.arange(M), np.arange(N), indexing="ij")]
+    else:
+        pm, pn = sample(M, N)
+    ref = O.gemm_points(A, fa, sa, abm, abk, B, fb, sbb, bbn, bbk, pm, pn)
+    got = D.float().cpu().numpy()[pm, pn].astype(np.float64)
+    rel = np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-300)
+    assert np.all(np.isfinite(got)), f"{ctx}: nonfinite outputs"
+    assert rel <= TOL, f"{ctx}: normwise relative error {rel:.3e} > {TOL}"
+    if out_dtype == torch.float32:
+        # fp32 accumulation over K products: |err| <= K * 2^-22 * sum |a b| is
+        # far looser than what a correct kernel shows; use a relative bound
+        assert rel <= 1e-4, f"{ctx}: fp32-output normwise error {rel:.3e}"
+    return rel
+
+
+def _layer(T, H, F, seed):
+    X = inputs.normal_bf16((T, H), seed)
+    W = inputs.normal_bf16((F, H), seed + 1, 0.02)
+    dY = inputs.normal_bf16((T, F), seed + 2, 1e-4)
+    return X, W, dY
+
+
+RECIPES = [
+    # name, kind X, kind W, kind dY, fmt X, fmt W, fmt dY
+    ("pertensor_e4m3", 0, 0, 0, O.E4M3, O.E4M3, O.E4M3),
+    ("pertensor_hybrid", 0, 0, 0, O.E4M3, O.E4M3, O.E5M2),
+    ("mxfp8", 4, 4, 4, O.E4M3, O.E4M3, O.E4M3),
+    ("block_1x128_128x128", 2, 3, 2, O.E4M3, O.E4M3, O.E4M3),
+]
+
+
+@pytest.mark.parametrize("name,kx,kw,kd,fx,fw,fd", RECIPES, ids=[r[0] for r in RECIPES])
+@pytest.mark.parametrize("T,H,F", [(256, 256, 512), (208, 272, 400), (384, 640, 528)])
+@pytest.mark.parametrize("out", [torch.bfloat16, torch.float32])
+def test_fprop_dgrad_wgrad(name, kx, kw, kd, fx, fw, fd, T, H, F, out):
+    api = _api()
+    X, W, dY = _layer(T, H, F, 40 + T)
+    qx = api.quantize(X.cuda(), kx, fx, True, True)
+    qw = api.quantize(W.cuda(), kw, fw, True, True)
+    qd = api.quantize(dY.cuda(), kd, fd, True, True)
+    _check(api, qx, False, qw, False, out, ctx=f"{name} fprop")      # Y  = X . W^T
+    _check(api, qd, False, qw, True, out, ctx=f"{name} dgrad")       # dX = dY . W
+    if kx == 2:   # blockwise wgrad: 1x128 x 1x128 along the token dim
+        _check(api, qd, True, qx, True, out, ctx=f"{name} wgrad")
+    else:
+        _check(api, qd, True, qx, True, out, ctx=f"{name} wgrad")    # dW = dY^T . X
+
+
+def test_gemm_k_sweep_and_ragged_k():
+    api = _api()
+    for K in (16, 48, 128, 144, 1040):
+        a = inputs.normal_bf16((130, K), K)
+        b = inputs.normal_bf16((264, K), K + 1)
+        for kind in (0, 4):
+            qa = api.quantize(a.cuda(), kind, O.E4M3, True, False)
+            qb = api.quantize(b.cuda(), kind, O.E4M3, True, False)
+            _check(api, qa, False, qb, False, ctx=f"K={K} kind={kind}")
+        qa = api.quantize(a.cuda(), 2, O.E4M3, True, False)
+        qb = api.quantize(b.cuda(), 3, O.E4M3, True, False)
+        _check(api, qa, False, qb, False, ctx=f"K={K} block")
+
+
+def test_gemm_outlier_columns_blockwise():
+    """1% outlier input channels x100 (the blockwise workload's activation)."""
+    api = _api()
+    x = inputs.to_bf16(inputs.with_outlier_columns(inputs.normal_f32((512, 1024), 3), 0.01, 100.0, 2))
+    w = inputs.normal_bf16((768, 1024), 4, 0.02)
+    qx = api.quantize(x.cuda(), 2, O.E4M3, True, False)
+    qw = api.quantize(w.cuda(), 3, O.E4M3, True, False)
+    _check(api, qx, False, qw, False, ctx="outliers")
+
+
+def _edge_sample(k):
+    def f(M, N):
+        g = np.random.default_rng(M * 7 + N)
+        rows = np.unique(np.concatenate([[0, M - 1], g.choice(M, k, replace=False)]))
+        cols = np.unique(np.concatenate([[0, N - 1], g.choice(N, k, replace=False)]))
+        pm1, pn1 = [a.ravel() for a in np.meshgrid(rows, np.arange(N), indexing="ij")]
+        pm2, pn2 = [a.ravel() for a in np.meshgrid(np.arange(M), cols, indexing="ij")]
+        return np.concatenate([pm1, pm2]), np.concatenate([pn1, pn2])
+    return f
+
+
+def test_full_config_pertensor_256():
+    api = _api()
+    A, B = inputs.pertensor_256()
+    qa = api.quantize(A.cuda(), 0, O.E4M3, True, False)
+    qb = api.quantize(B.cuda(), 0, O.E4M3, True, False)
+    _check(api, qa, False, qb, False, ctx="cfg1 full")
+
+
+def test_full_config_blockwise_llama8b_up_proj():
+    api = _api()
+    X, W = inputs.llama8b_up_proj()
+    qx = api.quantize(X.cuda(), 2, O.E4M3, True, False)
+    qw = api.quantize(W.cuda(), 3, O.E4M3, True, False)
+    _check(api, qx, False, qw, False, sample=_edge_sample(14), ctx="cfg2 fprop (16 rows + 16 cols)")
+
+
+def test_full_config_mxfp8_llama8b_mlp():
+    api = _api()
+    X, W, dY = inputs.llama8b_mlp()
+    qx = api.quantize(X.cuda(), 4, O.E4M3, True, True)
+    qw = api.quantize(W.cuda(), 4, O.E4M3, True, True)
+    qd = api.quantize(dY.cuda(), 4, O.E4M3, True, True)
+    s = _edge_sample(6)
+    _check(api, qx, False, qw, False, sample=s, ctx="cfg3 fprop")
+    _check(api, qd, False, qw, True, sample=s, ctx="cfg3 dgrad")
+    _check(api, qd, True, qx, True, sample=s, ctx="cfg3 wgrad")
