@@ -1,0 +1,371 @@
+"""Benchmark of the FP8 quantize -> scaled-GEMM hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Workload (one step): the blockwise-scaled Llama-3-8B FFN up-projection -- X
+bf16 [4096 tokens x 4096] quantized with 1x128 blocks, W bf16 [14336 x 4096]
+with 128x128 tiles (fp32 scale = amax / 448), both with their row-wise and
+column-wise copies (the backward GEMMs' operands), then the fprop GEMM
+Y = X . W^T with fp32 accumulation and bf16 output.  X ~ N(0,1) with 1% of its
+columns x100, W ~ N(0, 0.02^2), seeded, synthetic.  The same line also reports
+the MXFP8 Llama-3-8B MLP layer (X [8192 x 4096], W [14336 x 4096],
+dY [8192 x 14336]; quantize with both copies, fprop / dgrad / wgrad).
+
+`value` is the step's effective throughput, 2 M N K / step time, in TFLOP/s,
+with inputs resident in HBM; L2 (129 MB) is flushed by writing a 512 MiB
+buffer before every timed step (the flush is outside the timed region).
+`e2e` is the same metric through the C ABI with the step's inputs copied from
+pinned host memory and the output copied back inside the timed region.
+`--impl reference` times the CPU oracle (plain C, one core) on a bounded
+sample of the same step and extrapolates it to the full step.
+Multi-GPU (torchrun): replicas only, every rank runs the full step.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "MXFP8/blockwise GEMM TFLOPS & quantize GB/s, as fraction of GB300 peak"
+UNIT = "TFLOP/s"
+T, H, F = 4096, 4096, 14336
+WORKLOAD = ("blockwise Llama-3-8B FFN up-proj: X[4096x4096] 1x128 + W[14336x4096] 128x128 quantize "
+            "(row+col copies) + fprop GEMM, bf16 out")
+# algorithmic bytes per element of a quantize call with both copies:
+# read bf16 (2) + write the two fp8 copies (1 + 1) + the scales of both copies
+BYTES_1x128 = 2 + 1 + 1 + 2 * 4 / 128
+BYTES_128x128 = 2 + 1 + 1 + 2 * 4 / (128 * 128)
+BYTES_MX = 2 + 1 + 1 + 2 * 1 / 32
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.tmp, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        try:
+            rows = [[c.strip() for c in r.split(",")] for r in open(self.tmp.name).read().strip().splitlines()
+                    if r.strip()]
+            os.unlink(self.tmp.name)
+        except Exception:
+            return None
+        if not rows:
+            return None
+
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+
+        sm = [num(r[1]) for r in rows if len(r) > 1 and num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if len(r) > 2 and num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4)
+                          if len(r) > 5 + i and r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def dist_setup(n):
+    import torch
+    if n <= 1 and "RANK" not in os.environ:
+        return 0, 1, 0
+    import torch.distributed as dist
+    rank, world = int(os.environ["RANK"]), int(os.environ["WORLD_SIZE"])
+    local = int(os.environ.get("LOCAL_RANK", rank))
+    torch.cuda.set_device(local)
+    dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ ours
+
+def run_ours(args):
+    import torch
+
+    from fp8_scaled_quantization_quantize_gb300 import api, inputs
+
+    rank, world, local = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    hbm_peak, bf16_peak, peak_kind = peaks()
+    fp8_peak = 2.0 * bf16_peak   # dense FP8 = 2 x dense BF16 (nominal 4.5 vs 2.25 PFLOP/s)
+
+    Xh, Wh = inputs.llama8b_up_proj(T, H, F)
+    X, W = Xh.to(dev), Wh.to(dev)
+    qx = api.alloc(api.BLOCK_1x128, api.E4M3, T, H, True, True, dev)
+    qw = api.alloc(api.BLOCK_128x128, api.E4M3, F, H, True, True, dev)
+    Y = torch.empty((T, F), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    flops = 2.0 * T * F * H
+    qbytes = T * H * BYTES_1x128 + F * H * BYTES_128x128
+
+    def step(ev=None):
+        if ev:
+            ev[0].record()
+        api.quantize_into(X, qx, stream=stream)
+        api.quantize_into(W, qw, stream=stream)
+        if ev:
+            ev[1].record()
+        api.scaled_gemm(qx, False, qw, False, out=Y, stream=stream)
+        if ev:
+            ev[2].record()
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    with ClockSampler(local) as cs:
+        barrier(world)
+        torch.cuda.synchronize()
+        for i in range(args.steps):
+            flush.zero_()
+            step(evs[i])
+        torch.cuda.synchronize()
+        barrier(world)
+    clocks = cs.summary()
+    q_avg = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    g_avg = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    ms_step = max_over_ranks(statistics.mean(e[0].elapsed_time(e[2]) for e in evs), world)
+    errs = api.device_errors()
+
+    # ---- end to end through the C ABI with host buffers
+    Xp, Wp = Xh.pin_memory(), Wh.pin_memory()
+    Yp = torch.empty((T, F), dtype=torch.bfloat16).pin_memory()
+    e2e_ms = []
+    for i in range(args.warmup + args.steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        X.copy_(Xp, non_blocking=True)
+        W.copy_(Wp, non_blocking=True)
+        step()
+        Yp.copy_(Y, non_blocking=True)
+        e1.record()
+        torch.cuda.synchronize()
+        if i >= args.warmup:
+            e2e_ms.append(e0.elapsed_time(e1))
+    e2e_step = max_over_ranks(statistics.mean(e2e_ms), world)
+
+    # ---- MXFP8 Llama-3-8B MLP layer: quantize (both copies) + fprop / dgrad / wgrad
+    mx = None
+    launches = 3 * args.steps
+    if not args.skip_mx:
+        T3 = 8192
+        X3, W3, D3 = [t.to(dev) for t in inputs.llama8b_mlp(T3, H, F)]
+        q3 = [api.alloc(api.MXFP8_1x32, api.E4M3, *t.shape, True, True, dev) for t in (X3, W3, D3)]
+        outs = [torch.empty(s, dtype=torch.bfloat16, device=dev) for s in ((T3, F), (T3, H), (F, H))]
+
+        def mx_step(ev=None):
+            if ev:
+                ev[0].record()
+            for t, q in zip((X3, W3, D3), q3):
+                api.quantize_into(t, q, stream=stream)
+            if ev:
+                ev[1].record()
+            api.scaled_gemm(q3[0], False, q3[1], False, out=outs[0], stream=stream)   # fprop
+            if ev:
+                ev[2].record()
+            api.scaled_gemm(q3[2], False, q3[1], True, out=outs[1], stream=stream)    # dgrad
+            if ev:
+                ev[3].record()
+            api.scaled_gemm(q3[2], True, q3[0], True, out=outs[2], stream=stream)     # wgrad
+            if ev:
+                ev[4].record()
+
+        for _ in range(args.warmup):
+            flush.zero_()
+            mx_step()
+        mevs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+        for i in range(args.steps):
+            flush.zero_()
+            mx_step(mevs[i])
+        torch.cuda.synchronize()
+        f3 = 2.0 * T3 * F * H
+        qb3 = (X3.numel() + W3.numel() + D3.numel()) * BYTES_MX
+        qms = statistics.mean(e[0].elapsed_time(e[1]) for e in mevs)
+        gms = [statistics.mean(e[j].elapsed_time(e[j + 1]) for e in mevs) for j in (1, 2, 3)]
+        sms = statistics.mean(e[0].elapsed_time(e[4]) for e in mevs)
+        names = ("fprop", "dgrad", "wgrad")
+        mx = {"workload": "MXFP8 Llama-3-8B MLP: X[8192x4096], W[14336x4096], dY[8192x14336] 1x32 E8M0, "
+                          "row+col quantize + fprop/dgrad/wgrad, bf16 out",
+              "step_tflops": round(3 * f3 / sms / 1e9, 1),
+              "gemm_tflops": {k: round(f3 / g / 1e9, 1) for k, g in zip(names, gms)},
+              "gemm_frac_of_fp8_peak": {k: round(f3 / g / 1e9 / fp8_peak, 3) for k, g in zip(names, gms)},
+              "quantize_gbs": round(qb3 / qms / 1e6, 1),
+              "quantize_frac_of_hbm": round(qb3 / qms / 1e6 / hbm_peak, 3),
+              "ms_per_step": round(sms, 4)}
+        errs |= api.device_errors()
+        launches += 6 * args.steps
+
+    value = world * flops / ms_step / 1e9
+    gemm_tflops = flops / g_avg / 1e9
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "fp8e4m3 x fp8e4m3 -> fp32 accumulate (quantize in fp32)",
+        "data": "synthetic (seeded N(0,1) with 1% outlier columns x100; W N(0,0.02^2))",
+        "config": {"workload": WORKLOAD, "M": T, "N": F, "K": H, "recipe": "blockwise 1x128 / 128x128",
+                   "l2": "flushed (512 MiB write) before every timed step", "parallelism": f"replicas x{world}"},
+        "gemm_tflops": round(gemm_tflops, 1),
+        "quantize_gbs": round(qbytes / q_avg / 1e6, 1),
+        "quantize_frac_of_hbm": round(qbytes / q_avg / 1e6 / hbm_peak, 3),
+        "roofline": {"kernel": "gemm_kernel<blockwise 1x128 x 128x128, bf16 out>", "bound": "tensor",
+                     "achieved": round(gemm_tflops, 1), "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
+                     "frac": round(gemm_tflops / fp8_peak, 3),
+                     "peak_source": f"{peak_kind} bf16 burst x2 (dense FP8 / BF16 nominal ratio)",
+                     "traffic": None},
+        "e2e": {"value": round(world * flops / e2e_step / 1e9, 1), "unit": UNIT,
+                "h2d_bytes_per_step": X.numel() * 2 + W.numel() * 2, "d2h_bytes_per_step": Y.numel() * 2},
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "device_errors": errs,
+        "mxfp8": mx,
+    }
+    if rank == 0 and not args.skip_cpu:
+        line["cpu_baseline"] = cpu_baseline(args.cpu_budget)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# -------------------------------------------------------------- oracle arm
+
+def cpu_baseline(budget_s: float = 15.0) -> dict:
+    """The oracle timed on a bounded sample of the step, extrapolated to the
+    full step: quantize 128 rows of X (1x128, both copies) and 1024 rows of W
+    (128x128, both copies), and fprop GEMM output points until the budget."""
+    import numpy as np
+
+    import oracle as O
+    from fp8_scaled_quantization_quantize_gb300 import inputs
+
+    Xh, Wh = inputs.llama8b_up_proj(T, H, F)
+    xb, wb = inputs.bf16_bits(Xh), inputs.bf16_bits(Wh)
+    t0 = time.perf_counter()
+    qx = O.quantize(O.BLOCK_1x128, O.E4M3, xb[:128], True, True)
+    t1 = time.perf_counter()
+    qw = O.quantize(O.BLOCK_128x128, O.E4M3, wb[:128 * 8], True, True)
+    t2 = time.perf_counter()
+    per_x = (t1 - t0) / (128 * H)
+    per_w = (t2 - t1) / (128 * 8 * H)
+    A, sA = qx["data_row"], qx["scale_row"]
+    B, sB = qw["data_row"], qw["scale_row"]
+    n, pts, tg = 256, 0, 0.0
+    while True:
+        pm = np.zeros(n, dtype=np.int64)
+        pn = np.arange(n, dtype=np.int64) % B.shape[0]
+        g0 = time.perf_counter()
+        O.gemm_points(A, O.E4M3, sA, 1, 128, B, O.E4M3, sB, 128, 128, pm, pn)
+        tg += time.perf_counter() - g0
+        pts += n
+        if tg + (t2 - t0) > budget_s or n >= 1 << 16:
+            break
+        n *= 2
+    per_point = tg / pts
+    full_s = per_x * T * H + per_w * F * H + per_point * T * F
+    return {"value": round(2.0 * T * F * H / full_s / 1e12, 6), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"quantize 128 rows of X and 1024 rows of W, {pts} GEMM output points (K={H}); "
+                      f"extrapolated to the full step ({full_s:.1f} s)"}
+
+
+def run_reference(args):
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    for _ in range(args.warmup):
+        cpu_baseline(min(2.0, args.cpu_budget))
+    vals = [cpu_baseline(args.cpu_budget / max(1, args.steps)) for _ in range(args.steps)]
+    v = statistics.mean(x["value"] for x in vals)
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT,
+            "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps, "warmup": args.warmup,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
+            "data": "synthetic", "config": {"workload": WORKLOAD, "M": T, "N": F, "K": H},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": vals[-1]["sample"]},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--skip-mx", action="store_true")
+    ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    args.warmup = max(args.warmup, 3)
+    run_ours(args)
+
+
+if __name__ == "__main__":
+    main()
