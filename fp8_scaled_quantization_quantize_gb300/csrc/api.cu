@@ -260,7 +260,9 @@ fp8q_status fp8q_scaled_gemm(const fp8q_tensor* A, int a_use_col, const fp8q_ten
 
 fp8q_status fp8q_device_errors(unsigned int* flags, void* stream) {
     if (!flags) return FP8Q_ERR_ARG;
-    return read_device_errors(flags, (cudaStream_t)stream);
+    fp8q_status st = read_device_errors(flags, (cudaStream_t)stream);
+    if (st != FP8Q_OK) return st;
+    return read_quant_errors(flags);
 }
 
 fp8q_status fp8q_cast_f32_bits(uint32_t start, uint64_t count, int fmt, void* out, void* stream) {

@@ -25,6 +25,7 @@
 #include <cuda.h>
 
 #include "fp8q_internal.cuh"
+#include "ptx.cuh"
 
 namespace fp8q {
 
@@ -68,59 +69,8 @@ struct Params {
 
 // ------------------------------------------------------------ PTX wrappers
 
-__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-__device__ __forceinline__ uint64_t gtimer() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t a, uint32_t n) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(a), "r"(n) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t a, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(a), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t a) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(a) : "memory");
-}
-__device__ __forceinline__ bool mbar_try(uint32_t a, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok)
-        : "r"(a), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// Bounded wait on an mbarrier phase; false on abort or timeout.
-__device__ __noinline__ bool mbar_wait(uint32_t a, uint32_t parity, volatile int* abort_flag) {
-    if (mbar_try(a, parity)) return true;
-    const uint64_t t0 = gtimer();
-    while (true) {
-        if (mbar_try(a, parity)) return true;
-        if (*abort_flag) return false;
-        if (gtimer() - t0 > kWaitNs) {
-            atomicOr(&g_device_errors, 1u);
-            *abort_flag = 1;
-            return false;
-        }
-    }
-}
-
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t mbar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-            dst),
-        "l"(map), "r"(x), "r"(y), "r"(mbar)
-        : "memory");
-}
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t mbar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-                 "l"(src), "r"(bytes), "r"(mbar)
-                 : "memory");
+__device__ __forceinline__ bool mbar_wait(uint32_t a, uint32_t parity, volatile int* abort_flag) {
+    return mbar_wait_bounded(a, parity, abort_flag, &g_device_errors, 1u, kWaitNs);
 }
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -231,11 +181,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(mma_done, 1);
         *abort_flag = 0;
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        mbar_fence_init();
     }
     if (warp == 0 && lane == 0) {
-        asm volatile("prefetch.tensormap [%0];" ::"l"(&tmA) : "memory");
-        asm volatile("prefetch.tensormap [%0];" ::"l"(&tmB) : "memory");
+        prefetch_map(&tmA);
+        prefetch_map(&tmB);
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
@@ -287,12 +237,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (*abort_flag) {
                 // let copies already issued land before the CTA exits (bounded)
-                for (int i = 0; i < STAGES; ++i) {
-                    if (!(filled >> i & 1u)) continue;
-                    const uint64_t t0 = gtimer();
-                    while (!mbar_try(full(i), (fill_par >> i) & 1u) && gtimer() - t0 < kWaitNs / 10) {
-                    }
-                }
+                for (int i = 0; i < STAGES; ++i)
+                    if (filled >> i & 1u) mbar_drain(full(i), (fill_par >> i) & 1u, kWaitNs / 10);
             }
         }
     } else if (warp == 1) {
@@ -358,9 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // every MMA / copy this thread issued has completed once mma_done fires
             tc_commit(mma_done);
-            const uint64_t t0 = gtimer();
-            while (!mbar_try(mma_done, 0) && gtimer() - t0 < kWaitNs) {
-            }
+            mbar_drain(mma_done, 0, kWaitNs);
         }
     } else {
         // ------------------------------------------------ epilogue warps
@@ -472,34 +416,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ------------------------------------------------------------------ host
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    if (!fn) {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = (EncodeTiledFn)p;
-    }
-    return fn;
-}
-
 // 2-D map over a K-contiguous uint8 matrix [rows][K], box 128 bytes x box_rows, 128-byte swizzle.
 bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t K, uint32_t box_rows) {
-    EncodeTiledFn fn = encode_fn();
-    if (!fn) return false;
-    cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)K};
-    cuuint32_t box[2] = {128, box_rows};
-    cuuint32_t es[2] = {1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return make_map_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, base, rows, K, 128, box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 int g_sms = 0;

@@ -11,14 +11,24 @@
 // down its columns (32 rows x 2 columns per thread), where the 1x32 / 1x128
 // column blocks are reduced and converted; the 128-aligned tiles make every
 // scale-layout pad entry the scale of an all-zero block (code 127 / 1.0).
+#include <string.h>
+
 #include "fp8q_internal.cuh"
+#include "ptx.cuh"
 
 namespace fp8q {
+
+// Device error word of the quantize kernels (bit 1: a tile-load wait timed out).
+__device__ unsigned int g_quant_errors = 0;
 
 namespace {
 
 constexpr int kThreads = 256;
 constexpr int kTile = 128;
+constexpr int kStages = 3;
+constexpr uint32_t kStageBytes = kTile * kTile * 2;  // one bf16 tile
+constexpr uint32_t kTileSmem = kStages * kStageBytes + 128;
+constexpr uint64_t kQuantWaitNs = 1000000000ull;
 
 __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
     uint4 v;
@@ -98,14 +108,40 @@ __device__ __forceinline__ float pertensor_factor(const QuantArgs& a) {
 }
 
 template <int KIND, int FMT, bool ROW, bool COL>
-__global__ void __launch_bounds__(kThreads) quant_tile_kernel(QuantArgs a) {
+__global__ void __launch_bounds__(kThreads, 2)
+    quant_tile_kernel(const __grid_constant__ CUtensorMap tmx, QuantArgs a) {
     constexpr bool kPerTensor = (KIND == kCur || KIND == kDel);
-    __shared__ __align__(16) uint32_t tile[COL ? kTile * kTile / 2 : 1];  // bf16 pairs
+    extern __shared__ uint8_t qsmem_raw[];
+    uint8_t* qsmem = (uint8_t*)(((uintptr_t)qsmem_raw + 127) & ~(uintptr_t)127);
+    const uint32_t sbase = smem_u32(qsmem);
     __shared__ uint32_t colred[COL && KIND == kB1 ? 4 * kTile : 1];
     __shared__ uint32_t red[kThreads / 32];
+    __shared__ __align__(8) uint64_t bars[kStages];
+    __shared__ int abort_flag;
 
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
     const int vcol = t & 15, rsub = t >> 4;
+    const int64_t ntiles = a.tiles_r * a.tiles_c;
+    auto bar = [&](int s) { return smem_u32(&bars[s]); };
+
+    // stage s holds one bf16 tile [128][128] (row pitch 256 bytes), loaded by TMA
+    auto issue = [&](int64_t it) {
+        const int64_t tileid = blockIdx.x + it * (int64_t)gridDim.x;
+        if (tileid >= ntiles) return;
+        const int s = (int)(it % kStages);
+        const int64_t tr = tileid / a.tiles_c, tc = tileid % a.tiles_c;
+        mbar_expect_tx(bar(s), kStageBytes);
+        tma_load_2d(sbase + s * kStageBytes, &tmx, (int)(tc * kTile), (int)(tr * kTile), bar(s));
+    };
+    if (t == 0) {
+        for (int s = 0; s < kStages; ++s) mbar_init(bar(s), 1);
+        abort_flag = 0;
+        mbar_fence_init();
+        if (ntiles > 0) prefetch_map(&tmx);
+    }
+    __syncthreads();
+    if (t == 0)
+        for (int j = 0; j < kStages; ++j) issue(j);
 
     float ks = 1.0f;
     if constexpr (kPerTensor) {
@@ -117,20 +153,22 @@ __global__ void __launch_bounds__(kThreads) quant_tile_kernel(QuantArgs a) {
     }
 
     uint32_t nsat_row = 0, nsat_col = 0, nnf = 0, tmax_all = 0;
-    const int64_t ntiles = a.tiles_r * a.tiles_c;
-
-    for (int64_t tileid = blockIdx.x; tileid < ntiles; tileid += gridDim.x) {
+    int64_t it = 0;
+    for (int64_t tileid = blockIdx.x; tileid < ntiles; tileid += gridDim.x, ++it) {
         const int64_t tr = tileid / a.tiles_c, tc = tileid % a.tiles_c;
         const int64_t r0 = tr * kTile, c0 = tc * kTile;
         const int64_t c = c0 + vcol * 8;
         const bool cin = c < a.C;
+        const int stg = (int)(it % kStages);
+        const bool ok = mbar_wait_bounded(bar(stg), (uint32_t)((it / kStages) & 1), &abort_flag, &g_quant_errors,
+                                          2u, kQuantWaitNs);
+        if (__syncthreads_or(!ok)) break;  // the whole CTA leaves together
+        const uint8_t* tile8 = qsmem + stg * kStageBytes;
+        const uint32_t* tile = (const uint32_t*)tile8;
 
         uint4 v[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int64_t r = r0 + rsub + 16 * i;
-            v[i] = (cin && r < a.R) ? ld_nc_v4(a.x + r * a.C + c) : make_uint4(0, 0, 0, 0);
-        }
+        for (int i = 0; i < 8; ++i) v[i] = *(const uint4*)(tile8 + (rsub + 16 * i) * (kTile * 2) + vcol * 16);
         uint32_t vmax[8];
         uint32_t vnf = 0;  // bit i: vector i holds a NaN / Inf
 #pragma unroll
@@ -163,7 +201,6 @@ __global__ void __launch_bounds__(kThreads) quant_tile_kernel(QuantArgs a) {
                 }
             }
         }
-
         // ---------------- row-wise copy
         if constexpr (ROW) {
 #pragma unroll
@@ -209,8 +246,6 @@ __global__ void __launch_bounds__(kThreads) quant_tile_kernel(QuantArgs a) {
 
         // ---------------- column-wise copy
         if constexpr (COL) {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) *(uint4*)&tile[(rsub + 16 * i) * (kTile / 2) + vcol * 4] = v[i];
             const bool tile_nf = __syncthreads_or(vnf != 0) != 0;
             const int p = t & 63, qd = t >> 6;  // column pair, 32-row quarter
             uint32_t w[32];
@@ -299,8 +334,15 @@ __global__ void __launch_bounds__(kThreads) quant_tile_kernel(QuantArgs a) {
                     if (full) dst[1] = make_uint4(o1[4], o1[5], o1[6], o1[7]);
                 }
             }
-            __syncthreads();  // tile / colred reused by the next tile
         }
+        __syncthreads();  // stage and colred are free again: refill the stage
+        if (t == 0) issue(it + kStages);
+    }
+    if (abort_flag && t == 0) {
+        // let the tile loads already issued land before the CTA exits (bounded)
+        for (int64_t j = it; j < it + kStages; ++j)
+            if (blockIdx.x + j * (int64_t)gridDim.x < ntiles)
+                mbar_drain(bar((int)(j % kStages)), (uint32_t)((j / kStages) & 1), kQuantWaitNs / 10);
     }
 
     // ---------------- counters (and the delayed recipe's tensor amax)
@@ -408,17 +450,23 @@ int num_sms() {
 
 template <int KIND, int FMT, bool ROW, bool COL>
 fp8q_status launch_tile(const QuantArgs& a, cudaStream_t s) {
-    static int per_sm = 0;
+    static bool attr = false;
     auto kern = quant_tile_kernel<KIND, FMT, ROW, COL>;
-    if (per_sm == 0) {
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, 0) != cudaSuccess || per_sm < 1)
-            per_sm = 1;
+    if (!attr) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kTileSmem) != cudaSuccess)
+            return FP8Q_ERR_CUDA;
+        attr = true;
     }
     const int64_t ntiles = a.tiles_r * a.tiles_c;
-    int64_t grid = (int64_t)num_sms() * per_sm;
+    CUtensorMap tm;
+    memset(&tm, 0, sizeof(tm));
+    if (ntiles > 0 && !make_map_2d(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.x, a.R, a.C, kTile, kTile,
+                                   CU_TENSOR_MAP_SWIZZLE_NONE))
+        return FP8Q_ERR_CUDA;
+    int64_t grid = (int64_t)num_sms() * 2;
     if (ntiles < grid) grid = ntiles;
     if (grid < 1) grid = 1;
-    kern<<<(unsigned)grid, kThreads, 0, s>>>(a);
+    kern<<<(unsigned)grid, kThreads, kTileSmem, s>>>(tm, a);
     return cudaGetLastError() == cudaSuccess ? FP8Q_OK : FP8Q_ERR_CUDA;
 }
 
@@ -468,6 +516,15 @@ fp8q_status launch_quantize(const fp8q_recipe* rc, const QuantArgs& a, DelayedDe
         default:
             return FP8Q_ERR_ARG;
     }
+}
+
+fp8q_status read_quant_errors(unsigned int* flags) {
+    unsigned int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_quant_errors, sizeof(v)) != cudaSuccess) return FP8Q_ERR_CUDA;
+    const unsigned int zero = 0;
+    if (cudaMemcpyToSymbol(g_quant_errors, &zero, sizeof(zero)) != cudaSuccess) return FP8Q_ERR_CUDA;
+    *flags |= v;
+    return FP8Q_OK;
 }
 
 fp8q_status launch_delayed_update(DelayedDev* st, const float* amax, const unsigned long long* nonfinite,

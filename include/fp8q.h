@@ -226,8 +226,9 @@ FP8Q_API fp8q_status fp8q_scaled_gemm(const fp8q_tensor* A, int a_use_col, const
                              void* D, int out_dtype, int64_t M, int64_t N, int64_t K, void* stream);
 
 /*
- * Reads and clears the library's device error word on the current device
- * (bit 0: a GEMM pipeline wait timed out).  Synchronises `stream`.
+ * Reads and clears the library's device error words on the current device
+ * (bit 0: a GEMM pipeline wait timed out, bit 1: a quantize tile-load wait
+ * timed out).  Synchronises `stream`.
  */
 FP8Q_API fp8q_status fp8q_device_errors(unsigned int* flags, void* stream);
 
