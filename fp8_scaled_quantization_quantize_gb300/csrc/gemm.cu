@@ -34,7 +34,8 @@ __device__ unsigned int g_device_errors = 0;
 namespace {
 
 constexpr int BM = 128, BN = 256, BK = 128, STAGES = 4;
-constexpr int kEpiWarps = 8;
+constexpr int kEpiWarps = 16;
+constexpr int kEpiCols = BN / (kEpiWarps / 4);  // accumulator columns per epilogue warp
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr uint32_t A_STAGE = BM * BK, B_STAGE = BN * BK;
 constexpr uint32_t SFA_STAGE = 512, SFB_STAGE = 1024;
@@ -43,7 +44,7 @@ constexpr uint32_t OFF_B = OFF_A + STAGES * A_STAGE;
 constexpr uint32_t OFF_SFA = OFF_B + STAGES * B_STAGE;
 constexpr uint32_t OFF_SFB = OFF_SFA + STAGES * SFA_STAGE;
 constexpr uint32_t OFF_SBW = OFF_SFB + STAGES * SFB_STAGE;      // per-epilogue-warp 1x128 B scales
-constexpr uint32_t OFF_BAR = OFF_SBW + kEpiWarps * 128 * 4;
+constexpr uint32_t OFF_BAR = OFF_SBW + kEpiWarps * kEpiCols * 4;
 constexpr uint32_t NBARS = 2 * STAGES + 5;
 constexpr uint32_t OFF_MISC = OFF_BAR + 8 * NBARS;
 constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;            // + alignment slack
@@ -116,6 +117,27 @@ __device__ __forceinline__ void tc_cp_32x128b(uint32_t taddr, uint64_t desc) {
           "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),  \
           "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])   \
         : "r"(addr))
+
+#define FP8Q_LD16(addr, r)                                                                                     \
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, " \
+                 "[%16];"                                                                                      \
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),          \
+                   "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),      \
+                   "=r"(r[14]), "=r"(r[15])                                                                     \
+                 : "r"(addr))
+
+// Registers written by tcgen05.ld are valid only after tcgen05.wait::ld; this
+// empty asm, placed after the wait, keeps the compiler from hoisting their
+// uses above it.
+__device__ __forceinline__ void reg_fence16(uint32_t* r) {
+    asm volatile("" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+                 "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
+                 "+r"(r[14]), "+r"(r[15]));
+}
+__device__ __forceinline__ void reg_fence32(uint32_t* r) {
+    reg_fence16(r);
+    reg_fence16(r + 16);
+}
 
 __device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
@@ -308,87 +330,107 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ------------------------------------------------ epilogue warps
-        const int ew = warp - 2, q = warp & 3, h = ew >> 2;
+        // warp w owns TMEM lanes 32 (w % 4) .. +31 (its rows) and columns
+        // 64 j .. 64 j + 63, j = (w - 2) / 4, of the 256-column accumulator
+        const int ew = warp - 2, q = warp & 3, j = ew >> 2;
         const uint32_t lane_base = (uint32_t)(32 * q) << 16;
         float sab = 1.0f;
         if (REC == REC_PT) sab = __fmul_rn(*p.sa_inv, *p.sb_inv);
-        float* sbw = (float*)(smem + OFF_SBW) + ew * 128;
+        float* sbw = (float*)(smem + OFF_SBW) + ew * kEpiCols;
         uint32_t tile_i = 0;
         uint64_t kbg = 0;
         for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++tile_i) {
             int64_t mb, nb;
             tile_coords(t, p.tiles_m, p.tiles_n, mb, nb);
             const int64_t row = mb * BM + 32 * q + lane;
-            const int64_t col0 = nb * BN + 128 * h;
+            const int64_t col0 = nb * BN + kEpiCols * j;
+            const uint32_t tcol = (uint32_t)(kEpiCols * j);
             if (REC == REC_PT || REC == REC_MX) {
                 if (!mbar_wait(tfull(0), tile_i & 1u, abort_flag)) break;
                 tc_fence_after();
-                // drain the accumulator into registers, hand TMEM back, then store
-                uint32_t r[128];
-                FP8Q_LD32(tmem + lane_base + 128 * h, r);
-                FP8Q_LD32(tmem + lane_base + 128 * h + 32, (r + 32));
-                FP8Q_LD32(tmem + lane_base + 128 * h + 64, (r + 64));
-                FP8Q_LD32(tmem + lane_base + 128 * h + 96, (r + 96));
+                // drain this warp's 64 columns into registers, hand TMEM back, then store
+                uint32_t r[64];
+                FP8Q_LD32(tmem + lane_base + tcol, r);
+                FP8Q_LD32(tmem + lane_base + tcol + 32, (r + 32));
                 tc_wait_ld();
+                reg_fence32(r);
+                reg_fence32(r + 32);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(tempty(0));
                 if (row < p.M) {
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
+                    for (int c = 0; c < 2; ++c) {
                         float v[32];
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[32 * c + j]) * sab;
+                        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[32 * c + i]) * sab;
                         store_row32<OUT_F32>(p, row, col0 + 32 * c, v);
                     }
                 }
             } else {
-                float acc[128];
+                float acc[kEpiCols];
 #pragma unroll
-                for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
-                const bool hvalid = (col0 < p.N);
-                float sa_next = p.bsa[row];  // kb = 0 (row < Mp always)
+                for (int i = 0; i < kEpiCols; ++i) acc[i] = 0.0f;
+                const bool cvalid = (col0 < p.N);
+                // scales for the next two K blocks are loaded ahead of use
+                const int nkb = (int)p.nkb;
+                const int64_t nblk = (nb * BN + kEpiCols * j) / 128;
+                const bool bvalid = nblk < p.nbn128;
+                const float* pa = p.bsa + row;                               // [kb][Mp]
+                const float* pb = p.bsb + (bvalid ? nblk * p.nkb : 0);       // 128x128: [nblk][kb]
+                const float* pv = p.bsb + (cvalid ? col0 : 0) + 2 * lane;    // 1x128: [kb][Np]
+                const int64_t Mp = p.Mp, Np = p.Np;
+                auto load_sa = [&](int kb) { return kb < nkb ? __ldg(pa + kb * Mp) : 0.0f; };
+                auto load_sb = [&](int kb) { return (REC == REC_B2D && bvalid && kb < nkb) ? __ldg(pb + kb) : 0.0f; };
+                auto load_sbv = [&](int kb) {
+                    float2 v = make_float2(0.f, 0.f);
+                    if (REC == REC_B1D && cvalid && kb < nkb) v = __ldg((const float2*)(pv + kb * Np));
+                    return v;
+                };
+                float sa0 = load_sa(0), sa1 = load_sa(1), sb0 = load_sb(0), sb1 = load_sb(1);
+                float2 sv0 = load_sbv(0), sv1 = load_sbv(1);
                 bool ok = true;
-                for (int64_t kb = 0; kb < p.nkb; ++kb, ++kbg) {
-                    const float sa = sa_next;
-                    if (kb + 1 < p.nkb) sa_next = p.bsa[(kb + 1) * p.Mp + row];
-                    float sbk = 0.0f;
-                    if (REC == REC_B2D) {
-                        const int64_t nblk = 2 * nb + h;
-                        sbk = (nblk < p.nbn128) ? p.bsb[nblk * p.nkb + kb] : 0.0f;
-                    } else {
+                for (int kb = 0; kb < nkb; ++kb, ++kbg) {
+                    const float sa = sa0, sbk = sb0;
+                    const float2 sv = sv0;
+                    sa0 = sa1;
+                    sb0 = sb1;
+                    sv0 = sv1;
+                    sa1 = load_sa(kb + 2);
+                    sb1 = load_sb(kb + 2);
+                    sv1 = load_sbv(kb + 2);
+                    if (REC == REC_B1D) {
                         __syncwarp();
-                        float4 v4 = make_float4(0.f, 0.f, 0.f, 0.f);
-                        if (hvalid) v4 = *(const float4*)(p.bsb + kb * p.Np + col0 + 4 * lane);
-                        *(float4*)(sbw + 4 * lane) = v4;
+                        *(float2*)(sbw + 2 * lane) = make_float2(sa * sv.x, sa * sv.y);
                         __syncwarp();
                     }
+                    const float sc = __fmul_rn(sa, sbk);
                     const uint32_t buf = (uint32_t)(kbg & 1u);
                     if (!mbar_wait(tfull(buf), (uint32_t)((kbg >> 1) & 1u), abort_flag)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
+                    const uint32_t base = tmem + lane_base + buf * BN + tcol;
+                    // 16-column chunks; the four warps sharing an SM sub-partition
+                    // hide each other's TMEM load latency
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        uint32_t r[32];
-                        FP8Q_LD32(tmem + lane_base + buf * BN + 128 * h + 32 * c, r);
+                    for (int c = 0; c < kEpiCols / 16; ++c) {
+                        uint32_t r[16];
+                        FP8Q_LD16(base + 16 * c, r);
                         tc_wait_ld();
+                        reg_fence16(r);
                         if (REC == REC_B2D) {
-                            const float sc = __fmul_rn(sa, sbk);
 #pragma unroll
-                            for (int j = 0; j < 32; ++j) acc[32 * c + j] = fmaf(__uint_as_float(r[j]), sc, acc[32 * c + j]);
+                            for (int i = 0; i < 16; ++i) acc[16 * c + i] = fmaf(__uint_as_float(r[i]), sc, acc[16 * c + i]);
                         } else {
 #pragma unroll
-                            for (int j = 0; j < 32; j += 4) {
-                                const float4 s4 = *(const float4*)(sbw + 32 * c + j);
-                                acc[32 * c + j] = fmaf(__uint_as_float(r[j]), __fmul_rn(sa, s4.x), acc[32 * c + j]);
-                                acc[32 * c + j + 1] =
-                                    fmaf(__uint_as_float(r[j + 1]), __fmul_rn(sa, s4.y), acc[32 * c + j + 1]);
-                                acc[32 * c + j + 2] =
-                                    fmaf(__uint_as_float(r[j + 2]), __fmul_rn(sa, s4.z), acc[32 * c + j + 2]);
-                                acc[32 * c + j + 3] =
-                                    fmaf(__uint_as_float(r[j + 3]), __fmul_rn(sa, s4.w), acc[32 * c + j + 3]);
+                            for (int i = 0; i < 16; i += 4) {
+                                const float4 s4 = *(const float4*)(sbw + 16 * c + i);
+                                acc[16 * c + i] = fmaf(__uint_as_float(r[i]), s4.x, acc[16 * c + i]);
+                                acc[16 * c + i + 1] = fmaf(__uint_as_float(r[i + 1]), s4.y, acc[16 * c + i + 1]);
+                                acc[16 * c + i + 2] = fmaf(__uint_as_float(r[i + 2]), s4.z, acc[16 * c + i + 2]);
+                                acc[16 * c + i + 3] = fmaf(__uint_as_float(r[i + 3]), s4.w, acc[16 * c + i + 3]);
                             }
                         }
                     }
@@ -399,7 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!ok) break;
                 if (row < p.M) {
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) store_row32<OUT_F32>(p, row, col0 + 32 * c, acc + 32 * c);
+                    for (int c = 0; c < kEpiCols / 32; ++c) store_row32<OUT_F32>(p, row, col0 + 32 * c, acc + 32 * c);
                 }
             }
         }
