@@ -156,6 +156,16 @@ def cast_f32_bits(start: int, count: int, fmt: int, out: torch.Tensor, stream=No
     return out
 
 
+def selftest_division(d: torch.Tensor, fmt: int, stream=None):
+    """(FP8 code mismatches, fp32 mismatches) of the blockwise division shortcut
+    against IEEE division over every finite bf16 x and every divisor in d."""
+    out = torch.zeros(2, dtype=torch.int64, device=d.device)
+    L.check(L.load().fp8q_selftest_division(_ptr(d), d.numel(), fmt, _ptr(out), _stream(stream)),
+            "fp8q_selftest_division")
+    torch.cuda.synchronize()
+    return int(out[0].item()), int(out[1].item())
+
+
 def device_errors(stream=None) -> int:
     v = ctypes.c_uint(0)
     L.check(L.load().fp8q_device_errors(ctypes.byref(v), _stream(stream)), "fp8q_device_errors")

@@ -265,6 +265,13 @@ fp8q_status fp8q_device_errors(unsigned int* flags, void* stream) {
     return read_quant_errors(flags);
 }
 
+fp8q_status fp8q_selftest_division(const float* d, int64_t nd, int fmt, unsigned long long* mismatches,
+                                   void* stream) {
+    if (!valid_fmt(fmt) || !mismatches || nd < 0 || (nd > 0 && !d)) return FP8Q_ERR_ARG;
+    if (((uintptr_t)mismatches & 7u) != 0 || ((uintptr_t)d & 3u) != 0) return FP8Q_ERR_ALIGN;
+    return launch_div_selftest(d, nd, fmt, mismatches, (cudaStream_t)stream);
+}
+
 fp8q_status fp8q_cast_f32_bits(uint32_t start, uint64_t count, int fmt, void* out, void* stream) {
     if (!valid_fmt(fmt)) return FP8Q_ERR_ARG;
     if (count > 0 && !out) return FP8Q_ERR_ARG;

@@ -99,6 +99,82 @@ __device__ __forceinline__ uint2 convert8(const uint4& v, float k, uint32_t& nsa
     return q;
 }
 
+__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("max.u16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+// Per-half maxima of |x| over the 8 bf16 of v, NaN / Inf included (their
+// magnitude bits are >= 0x7F80, so a fold of 0x7F80 or more flags them).
+__device__ __forceinline__ uint32_t vec_pmax(const uint4& v) {
+    const uint32_t M = 0x7FFF7FFFu;
+    return max_u16x2(max_u16x2(v.x & M, v.y & M), max_u16x2(v.z & M, v.w & M));
+}
+__device__ __forceinline__ uint32_t fold16(uint32_t p) { return max(p & 0xFFFFu, p >> 16); }
+
+// Scale factor of one block: the multiplier k (per-tensor s, MX 2^-e), or for
+// the blockwise recipes the divisor d = k with r = RN(1 / d).
+struct Factor {
+    float k, r;
+    bool fast;
+};
+
+template <int KIND>
+__device__ __forceinline__ Factor make_factor(float k) {
+    Factor f;
+    f.k = k;
+    if constexpr (KIND == kB1 || KIND == kB128) {
+        f.r = __frcp_rn(k);
+        f.fast = k >= 0x1p-80f;  // keeps the residual below exact in fp32
+    } else {
+        f.r = 0.0f;
+        f.fast = true;
+    }
+    return f;
+}
+
+// x / d correctly rounded from r = RN(1 / d): q = RN(x r) lies within one ulp
+// of x / d, the residual x - d q is exactly representable and one FMA gives
+// it, and RN(q + residual * r) = RN(x / d) (Markstein's theorem on division
+// with a correctly rounded reciprocal).  Quotients that underflow keep the
+// sign of x (d > 0).  Valid for finite x and d in [2^-80, 2^128).
+__device__ __forceinline__ float div_rn_recip(float x, float d, float r) {
+    const float q = __fmul_rn(x, r);
+    const float e = __fmaf_rn(-q, d, x);
+    const float q2 = __fmaf_rn(e, r, q);
+    return __uint_as_float((__float_as_uint(q2) & 0x7FFFFFFFu) | (__float_as_uint(x) & 0x80000000u));
+}
+
+// The recipe's scaled value of a finite element.
+template <int KIND>
+__device__ __forceinline__ float apply(float x, const Factor& f) {
+    if constexpr (KIND == kB1 || KIND == kB128)
+        return f.fast ? div_rn_recip(x, f.k, f.r) : __fdiv_rn(x, f.k);
+    else
+        return __fmul_rn(x, f.k);
+}
+
+// Converts the 8 finite bf16 of v; counts saturation only when the caller
+// found that the vector's largest magnitude can exceed fmax once scaled
+// (the scaled value is monotone in |x|).
+template <int KIND, int FMT>
+__device__ __forceinline__ uint2 convert8_fast(const uint4& v, const Factor& f, uint32_t& nsat, bool count) {
+    float y[8] = {apply<KIND>(bf16_lo(v.x), f), apply<KIND>(bf16_hi(v.x), f), apply<KIND>(bf16_lo(v.y), f),
+                  apply<KIND>(bf16_hi(v.y), f), apply<KIND>(bf16_lo(v.z), f), apply<KIND>(bf16_hi(v.z), f),
+                  apply<KIND>(bf16_lo(v.w), f), apply<KIND>(bf16_hi(v.w), f)};
+    if (count) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) nsat += fabsf(y[j]) > Fmt<FMT>::fmax ? 1u : 0u;
+    }
+    return make_uint2(cvt4<FMT>(y[0], y[1], y[2], y[3]), cvt4<FMT>(y[4], y[5], y[6], y[7]));
+}
+
+template <int KIND, int FMT>
+__device__ __forceinline__ bool may_saturate(uint32_t max_bits16, const Factor& f) {
+    return fabsf(apply<KIND>(__uint_as_float(max_bits16 << 16), f)) > Fmt<FMT>::fmax;
+}
+
 template <int KIND, int FMT>
 __device__ __forceinline__ float pertensor_factor(const QuantArgs& a) {
     if constexpr (KIND == kCur)
@@ -173,9 +249,12 @@ __global__ void __launch_bounds__(kThreads, 2)
         uint32_t vnf = 0;  // bit i: vector i holds a NaN / Inf
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const uint32_t before = nnf;
-            vmax[i] = vec_absmax(v[i], nnf);
-            vnf |= (nnf != before ? 1u : 0u) << i;
+            uint32_t m = fold16(vec_pmax(v[i]));
+            if (m >= 0x7F80u) {  // NaN / Inf in this vector: exact finite max and count
+                m = vec_absmax(v[i], nnf);
+                vnf |= 1u << i;
+            }
+            vmax[i] = m;
         }
 
         // 128x128 tile amax (also the delayed recipe's running tensor amax)
@@ -239,7 +318,13 @@ __global__ void __launch_bounds__(kThreads, 2)
                         *(uint32_t*)(tileb + (rr & 31) * 16 + (rr >> 5) * 4) = code | (c1 << 8) | (c2 << 16) | (c3 << 24);
                     }
                 }
-                const uint2 q = convert8<KIND, FMT>(v[i], k, nsat_row, (vnf >> i) & 1u);
+                uint2 q;
+                if (!((vnf >> i) & 1u)) {
+                    const Factor f = make_factor<KIND>(k);
+                    q = convert8_fast<KIND, FMT>(v[i], f, nsat_row, may_saturate<KIND, FMT>(vmax[i], f));
+                } else {
+                    q = convert8<KIND, FMT>(v[i], k, nsat_row, true);
+                }
                 if (cin && r < a.R) *(uint2*)(a.q_row + r * a.C + c) = q;
             }
         }
@@ -252,19 +337,27 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
             for (int j = 0; j < 32; ++j) w[j] = tile[(32 * qd + j) * (kTile / 2) + p];
             float k0, k1;
+            uint32_t cm0 = 0x7F7Fu, cm1 = 0x7F7Fu;  // column maxima (re-quantized kinds)
             if constexpr (kPerTensor) {
                 k0 = k1 = ks;
             } else if constexpr (KIND == kB128) {
                 k0 = k1 = kd_tile;
             } else {
-                uint32_t m0 = 0, m1 = 0, dummy = 0;
+                uint32_t pm = 0;
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    uint32_t lo = w[j] & 0x7FFFu, hi = (w[j] >> 16) & 0x7FFFu;
-                    m0 = (lo < 0x7F80u && lo > m0) ? lo : m0;
-                    m1 = (hi < 0x7F80u && hi > m1) ? hi : m1;
+                for (int j = 0; j < 32; ++j) pm = max_u16x2(pm, w[j] & 0x7FFF7FFFu);
+                uint32_t m0 = pm & 0xFFFFu, m1 = pm >> 16;
+                if (m0 >= 0x7F80u || m1 >= 0x7F80u) {  // NaN / Inf: exact finite maxima
+                    m0 = m1 = 0;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const uint32_t lo = w[j] & 0x7FFFu, hi = (w[j] >> 16) & 0x7FFFu;
+                        m0 = (lo < 0x7F80u && lo > m0) ? lo : m0;
+                        m1 = (hi < 0x7F80u && hi > m1) ? hi : m1;
+                    }
                 }
-                (void)dummy;
+                cm0 = m0;
+                cm1 = m1;
                 const int64_t cc = c0 + 2 * p;
                 if constexpr (KIND == kMX) {
                     const int e0 = mx_exponent<FMT>(m0 << 16), e1 = mx_exponent<FMT>(m1 << 16);
@@ -285,6 +378,8 @@ __global__ void __launch_bounds__(kThreads, 2)
                              max(colred[2 * kTile + 2 * p + 1], colred[3 * kTile + 2 * p + 1]));
                     k0 = block_scale<FMT>(__uint_as_float(m0 << 16));
                     k1 = block_scale<FMT>(__uint_as_float(m1 << 16));
+                    cm0 = m0;
+                    cm1 = m1;
                     if (qd == 0) {
                         const int64_t Cp = a.tiles_c * kTile;
                         float* sc = (float*)a.s_col + tr * Cp + cc;
@@ -296,27 +391,45 @@ __global__ void __launch_bounds__(kThreads, 2)
             // convert 32 rows of columns 2p, 2p+1
             uint32_t o0[8], o1[8];
             uint32_t ns = 0;
+            if (!tile_nf) {
+                const Factor f0 = make_factor<KIND>(k0), f1 = make_factor<KIND>(k1);
+                const bool req = (KIND == kB1 || KIND == kMX);
+                const bool c0s = req && may_saturate<KIND, FMT>(cm0, f0), c1s = req && may_saturate<KIND, FMT>(cm1, f1);
 #pragma unroll
-            for (int j = 0; j < 32; j += 4) {
-                float a0 = bf16_lo(w[j]), a1 = bf16_lo(w[j + 1]), a2 = bf16_lo(w[j + 2]), a3 = bf16_lo(w[j + 3]);
-                float b0 = bf16_hi(w[j]), b1 = bf16_hi(w[j + 1]), b2 = bf16_hi(w[j + 2]), b3 = bf16_hi(w[j + 3]);
-                float ya0 = scaled<KIND>(a0, k0), ya1 = scaled<KIND>(a1, k0), ya2 = scaled<KIND>(a2, k0),
-                      ya3 = scaled<KIND>(a3, k0);
-                float yb0 = scaled<KIND>(b0, k1), yb1 = scaled<KIND>(b1, k1), yb2 = scaled<KIND>(b2, k1),
-                      yb3 = scaled<KIND>(b3, k1);
-                if constexpr (KIND == kB1 || KIND == kMX) {
-                    ns += sat_count<FMT>(a0, ya0) + sat_count<FMT>(a1, ya1) + sat_count<FMT>(a2, ya2) +
-                          sat_count<FMT>(a3, ya3) + sat_count<FMT>(b0, yb0) + sat_count<FMT>(b1, yb1) +
-                          sat_count<FMT>(b2, yb2) + sat_count<FMT>(b3, yb3);
+                for (int j = 0; j < 32; j += 4) {
+                    const float ya0 = apply<KIND>(bf16_lo(w[j]), f0), ya1 = apply<KIND>(bf16_lo(w[j + 1]), f0);
+                    const float ya2 = apply<KIND>(bf16_lo(w[j + 2]), f0), ya3 = apply<KIND>(bf16_lo(w[j + 3]), f0);
+                    const float yb0 = apply<KIND>(bf16_hi(w[j]), f1), yb1 = apply<KIND>(bf16_hi(w[j + 1]), f1);
+                    const float yb2 = apply<KIND>(bf16_hi(w[j + 2]), f1), yb3 = apply<KIND>(bf16_hi(w[j + 3]), f1);
+                    if (c0s)
+                        ns += (fabsf(ya0) > Fmt<FMT>::fmax) + (fabsf(ya1) > Fmt<FMT>::fmax) +
+                              (fabsf(ya2) > Fmt<FMT>::fmax) + (fabsf(ya3) > Fmt<FMT>::fmax);
+                    if (c1s)
+                        ns += (fabsf(yb0) > Fmt<FMT>::fmax) + (fabsf(yb1) > Fmt<FMT>::fmax) +
+                              (fabsf(yb2) > Fmt<FMT>::fmax) + (fabsf(yb3) > Fmt<FMT>::fmax);
+                    o0[j / 4] = cvt4<FMT>(ya0, ya1, ya2, ya3);
+                    o1[j / 4] = cvt4<FMT>(yb0, yb1, yb2, yb3);
                 }
-                o0[j / 4] = cvt4<FMT>(ya0, ya1, ya2, ya3);
-                o1[j / 4] = cvt4<FMT>(yb0, yb1, yb2, yb3);
-                if (tile_nf) {
+            } else {
+#pragma unroll 1
+                for (int j = 0; j < 32; j += 4) {
+                    float a0 = bf16_lo(w[j]), a1 = bf16_lo(w[j + 1]), a2 = bf16_lo(w[j + 2]), a3 = bf16_lo(w[j + 3]);
+                    float b0 = bf16_hi(w[j]), b1 = bf16_hi(w[j + 1]), b2 = bf16_hi(w[j + 2]), b3 = bf16_hi(w[j + 3]);
+                    float ya0 = scaled<KIND>(a0, k0), ya1 = scaled<KIND>(a1, k0), ya2 = scaled<KIND>(a2, k0),
+                          ya3 = scaled<KIND>(a3, k0);
+                    float yb0 = scaled<KIND>(b0, k1), yb1 = scaled<KIND>(b1, k1), yb2 = scaled<KIND>(b2, k1),
+                          yb3 = scaled<KIND>(b3, k1);
+                    if constexpr (KIND == kB1 || KIND == kMX) {
+                        ns += sat_count<FMT>(a0, ya0) + sat_count<FMT>(a1, ya1) + sat_count<FMT>(a2, ya2) +
+                              sat_count<FMT>(a3, ya3) + sat_count<FMT>(b0, yb0) + sat_count<FMT>(b1, yb1) +
+                              sat_count<FMT>(b2, yb2) + sat_count<FMT>(b3, yb3);
+                    }
                     // rebuild the bf16 pairs of each output column to reuse nan_sign2
                     const uint32_t a01 = (w[j] & 0xFFFFu) | (w[j + 1] << 16), a23 = (w[j + 2] & 0xFFFFu) | (w[j + 3] << 16);
                     const uint32_t b01 = (w[j] >> 16) | (w[j + 1] & 0xFFFF0000u), b23 = (w[j + 2] >> 16) | (w[j + 3] & 0xFFFF0000u);
-                    o0[j / 4] = nan_sign2(o0[j / 4] & 0xFFFFu, a01) | (nan_sign2(o0[j / 4] >> 16, a23) << 16);
-                    o1[j / 4] = nan_sign2(o1[j / 4] & 0xFFFFu, b01) | (nan_sign2(o1[j / 4] >> 16, b23) << 16);
+                    const uint32_t qa = cvt4<FMT>(ya0, ya1, ya2, ya3), qb = cvt4<FMT>(yb0, yb1, yb2, yb3);
+                    o0[j / 4] = nan_sign2(qa & 0xFFFFu, a01) | (nan_sign2(qa >> 16, a23) << 16);
+                    o1[j / 4] = nan_sign2(qb & 0xFFFFu, b01) | (nan_sign2(qb >> 16, b23) << 16);
                 }
             }
             nsat_col += ns;
@@ -436,6 +549,31 @@ __global__ void cast_bits_kernel(uint32_t start, uint64_t count, uint8_t* out) {
     }
 }
 
+// For every finite bf16 x and each divisor d[j] in the fast range, compares
+// div_rn_recip(x, d, RN(1/d)) with the IEEE quotient: [0] counts FP8 codes that
+// differ, [1] fp32 results that differ.
+template <int FMT>
+__global__ void div_selftest_kernel(const float* d, int64_t nd, unsigned long long* mismatch) {
+    const uint32_t xb = blockIdx.x * blockDim.x + threadIdx.x;  // bf16 pattern
+    const float x = __uint_as_float(xb << 16);
+    const bool xfin = (xb & 0x7F80u) != 0x7F80u;
+    uint32_t bad_code = 0, bad_bits = 0;
+    for (int64_t j = blockIdx.y; j < nd; j += gridDim.y) {
+        const float dj = d[j];
+        if (!xfin || !(dj >= 0x1p-80f) || !(dj < 0x1p+128f)) continue;
+        const float exact = __fdiv_rn(x, dj);
+        const float fast = div_rn_recip(x, dj, __frcp_rn(dj));
+        bad_bits += __float_as_uint(exact) != __float_as_uint(fast);
+        bad_code += (cvt2<FMT>(exact, 0.0f) & 0xFFu) != (cvt2<FMT>(fast, 0.0f) & 0xFFu);
+    }
+    bad_code = warp_sum_u32(bad_code);
+    bad_bits = warp_sum_u32(bad_bits);
+    if ((threadIdx.x & 31) == 0) {
+        if (bad_code) atomicAdd(&mismatch[0], (unsigned long long)bad_code);
+        if (bad_bits) atomicAdd(&mismatch[1], (unsigned long long)bad_bits);
+    }
+}
+
 int g_num_sms = 0;
 
 int num_sms() {
@@ -516,6 +654,17 @@ fp8q_status launch_quantize(const fp8q_recipe* rc, const QuantArgs& a, DelayedDe
         default:
             return FP8Q_ERR_ARG;
     }
+}
+
+fp8q_status launch_div_selftest(const float* d, int64_t nd, int fmt, unsigned long long* mismatch, cudaStream_t s) {
+    if (cudaMemsetAsync(mismatch, 0, 2 * sizeof(unsigned long long), s) != cudaSuccess) return FP8Q_ERR_CUDA;
+    if (nd <= 0) return FP8Q_OK;
+    const dim3 grid(65536 / 256, (unsigned)(nd < 4096 ? nd : 4096));
+    if (fmt == FP8Q_E4M3)
+        div_selftest_kernel<FP8Q_E4M3><<<grid, 256, 0, s>>>(d, nd, mismatch);
+    else
+        div_selftest_kernel<FP8Q_E5M2><<<grid, 256, 0, s>>>(d, nd, mismatch);
+    return cudaGetLastError() == cudaSuccess ? FP8Q_OK : FP8Q_ERR_CUDA;
 }
 
 fp8q_status read_quant_errors(unsigned int* flags) {

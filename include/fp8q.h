@@ -239,6 +239,19 @@ FP8Q_API fp8q_status fp8q_device_errors(unsigned int* flags, void* stream);
  */
 FP8Q_API fp8q_status fp8q_cast_f32_bits(uint32_t start, uint64_t count, int fmt, void* out, void* stream);
 
+/*
+ * Self-test of the blockwise recipes' division.  The quantize kernels compute
+ * x / d (d = amax / fmax, [guide] sec. 2.2) as q = RN(x * r) with r = RN(1/d),
+ * then one FMA residual correction, which yields the correctly rounded
+ * quotient for d in [2^-80, 2^128) (smaller d takes the IEEE division).  This
+ * entry point compares that computation with the IEEE quotient for every
+ * finite bf16 x and every d[j] (device fp32 [nd]) and writes the mismatch
+ * counts to mismatches (device uint64[2]: [0] FP8 codes of format fmt, [1]
+ * fp32 bits).  Both must be 0.
+ */
+FP8Q_API fp8q_status fp8q_selftest_division(const float* d, int64_t nd, int fmt, unsigned long long* mismatches,
+                                            void* stream);
+
 #ifdef __cplusplus
 }
 #endif
