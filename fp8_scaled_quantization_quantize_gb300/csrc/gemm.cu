@@ -180,6 +180,7 @@ __device__ __forceinline__ void store_row32(const Params& p, int64_t row, int64_
 template <int REC, bool OUT_F32>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Params p) {
+    constexpr uint32_t kAcc = (REC == REC_PT) ? 2u : 1u;  // TMEM accumulator buffers of 256 columns
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const uint32_t sb = smem_u32(smem);
@@ -273,11 +274,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             for (int64_t t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++tile_i) {
                 if (REC == REC_PT || REC == REC_MX) {
-                    if (!mbar_wait(tempty(0), (tile_i & 1u) ^ 1u, abort_flag)) break;
+                    // per-tensor: two accumulator buffers, so the epilogue of tile i
+                    // overlaps the MMAs of tile i + 1; MX: one (its scale slots use the rest)
+                    if (!mbar_wait(tempty(tile_i % kAcc), ((tile_i / kAcc) & 1u) ^ 1u, abort_flag)) break;
                     tc_fence_after();
                 }
                 for (int64_t kb = 0; kb < p.nkb; ++kb) {
-                    uint32_t dcol = 0;
+                    uint32_t dcol = (REC == REC_PT) ? (tile_i % kAcc) * BN : 0;
                     if (REC == REC_B2D || REC == REC_B1D) {
                         const uint32_t buf = (uint32_t)(kbg & 1u);
                         if (!mbar_wait(tempty(buf), (uint32_t)((kbg >> 1) & 1u) ^ 1u, abort_flag)) {
@@ -322,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 if (!ok) break;
-                if (REC == REC_PT || REC == REC_MX) tc_commit(tfull(0));
+                if (REC == REC_PT || REC == REC_MX) tc_commit(tfull(tile_i % kAcc));
             }
             // every MMA / copy this thread issued has completed once mma_done fires
             tc_commit(mma_done);
@@ -346,18 +349,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int64_t col0 = nb * BN + kEpiCols * j;
             const uint32_t tcol = (uint32_t)(kEpiCols * j);
             if (REC == REC_PT || REC == REC_MX) {
-                if (!mbar_wait(tfull(0), tile_i & 1u, abort_flag)) break;
+                const uint32_t abuf = tile_i % kAcc;
+                if (!mbar_wait(tfull(abuf), (tile_i / kAcc) & 1u, abort_flag)) break;
                 tc_fence_after();
                 // drain this warp's 64 columns into registers, hand TMEM back, then store
                 uint32_t r[64];
-                FP8Q_LD32(tmem + lane_base + tcol, r);
-                FP8Q_LD32(tmem + lane_base + tcol + 32, (r + 32));
+                FP8Q_LD32(tmem + lane_base + abuf * BN + tcol, r);
+                FP8Q_LD32(tmem + lane_base + abuf * BN + tcol + 32, (r + 32));
                 tc_wait_ld();
                 reg_fence32(r);
                 reg_fence32(r + 32);
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(tempty(0));
+                if (lane == 0) mbar_arrive(tempty(abuf));
                 if (row < p.M) {
 #pragma unroll
                     for (int c = 0; c < 2; ++c) {
@@ -401,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     sv1 = load_sbv(kb + 2);
                     if (REC == REC_B1D) {
                         __syncwarp();
-                        *(float2*)(sbw + 2 * lane) = make_float2(sa * sv.x, sa * sv.y);
+                        *(float2*)(sbw + 2 * lane) = sv;  // B scales of this warp's 64 columns
                         __syncwarp();
                     }
                     const float sc = __fmul_rn(sa, sbk);
@@ -426,11 +430,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         } else {
 #pragma unroll
                             for (int i = 0; i < 16; i += 4) {
+                                // d_A[m][kb] (this thread's row) x d_B[n][kb] (shared by the warp)
                                 const float4 s4 = *(const float4*)(sbw + 16 * c + i);
-                                acc[16 * c + i] = fmaf(__uint_as_float(r[i]), s4.x, acc[16 * c + i]);
-                                acc[16 * c + i + 1] = fmaf(__uint_as_float(r[i + 1]), s4.y, acc[16 * c + i + 1]);
-                                acc[16 * c + i + 2] = fmaf(__uint_as_float(r[i + 2]), s4.z, acc[16 * c + i + 2]);
-                                acc[16 * c + i + 3] = fmaf(__uint_as_float(r[i + 3]), s4.w, acc[16 * c + i + 3]);
+                                acc[16 * c + i] = fmaf(__uint_as_float(r[i]), __fmul_rn(sa, s4.x), acc[16 * c + i]);
+                                acc[16 * c + i + 1] =
+                                    fmaf(__uint_as_float(r[i + 1]), __fmul_rn(sa, s4.y), acc[16 * c + i + 1]);
+                                acc[16 * c + i + 2] =
+                                    fmaf(__uint_as_float(r[i + 2]), __fmul_rn(sa, s4.z), acc[16 * c + i + 2]);
+                                acc[16 * c + i + 3] =
+                                    fmaf(__uint_as_float(r[i + 3]), __fmul_rn(sa, s4.w), acc[16 * c + i + 3]);
                             }
                         }
                     }
