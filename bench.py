@@ -294,6 +294,112 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+# ------------------------------------------------------- single-op modes
+
+KINDS = {"current": 0, "delayed": 1, "1x128": 2, "128x128": 3, "mx": 4}
+QBYTES_SCALE = {0: 0.0, 1: 0.0, 2: 4 / 128, 3: 4 / (128 * 128), 4: 1 / 32}
+
+
+def _device_tensor(rows, cols, seed, outlier_frac=0.001, factor=1000.0):
+    """Seeded synthetic N(0,1) bf16 on the device with a fraction of elements
+    x factor (the sweep workload); drawn by torch's seeded CUDA generator."""
+    import torch
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    x = torch.randn((rows, cols), generator=g, device="cuda", dtype=torch.float32)
+    n = max(1, int(outlier_frac * x.numel()))
+    idx = torch.randint(0, x.numel(), (n,), generator=g, device="cuda")
+    x.view(-1)[idx] *= factor
+    return x.to(torch.bfloat16)
+
+
+def _time_ms(fn, steps, warmup, flush=None):
+    import torch
+    for _ in range(warmup):
+        if flush is not None:
+            flush.zero_()
+        fn()
+    torch.cuda.synchronize()
+    ms = []
+    for _ in range(steps):
+        if flush is not None:
+            flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        ms.append((e0, e1))
+    torch.cuda.synchronize()
+    return statistics.mean(a.elapsed_time(b) for a, b in ms)
+
+
+def quantize_point(kind, rows, cols, rowwise, colwise, steps, warmup, flush, x=None):
+    import torch
+
+    from fp8_scaled_quantization_quantize_gb300 import api
+    hbm_peak = peaks()[0]
+    if x is None:
+        x = _device_tensor(rows, cols, 5)
+    st = api.DelayedState(16, api.E4M3, 0) if kind == 1 else None
+    qt = api.alloc(kind, api.E4M3, rows, cols, rowwise, colwise, "cuda")
+    ms = _time_ms(lambda: api.quantize_into(x, qt, st), steps, warmup, flush)
+    copies = int(rowwise) + int(colwise)
+    per_elem = 2 + copies * (1 + QBYTES_SCALE[kind]) + (2 if kind == 0 else 0)
+    gbs = rows * cols * per_elem / ms / 1e6
+    del qt
+    torch.cuda.synchronize()
+    return {"mode": "quantize", "kind": [k for k, v in KINDS.items() if v == kind][0], "rows": rows, "cols": cols,
+            "mib": rows * cols * 2 / 2 ** 20, "rowwise": rowwise, "colwise": colwise, "ms": round(ms, 4),
+            "gbs": round(gbs, 1), "frac_of_hbm": round(gbs / hbm_peak, 3),
+            "algorithmic_bytes_per_elem": round(per_elem, 4)}
+
+
+def gemm_point(kind, M, N, K, steps, warmup, flush, out="bf16"):
+    import torch
+
+    from fp8_scaled_quantization_quantize_gb300 import api
+    fp8_peak = 2.0 * peaks()[1]
+    a = _device_tensor(M, K, 11)
+    b = _device_tensor(N, K, 12)
+    kb = 3 if kind == 2 else kind
+    qa = api.quantize(a, kind, api.E4M3, True, False)
+    qb = api.quantize(b, kb, api.E4M3, True, False)
+    del a, b
+    D = torch.empty((M, N), dtype=torch.bfloat16 if out == "bf16" else torch.float32, device="cuda")
+    ms = _time_ms(lambda: api.scaled_gemm(qa, False, qb, False, out=D), steps, warmup, flush)
+    tf = 2.0 * M * N * K / ms / 1e9
+    name = {0: "pertensor", 2: "blockwise 1x128 x 128x128", 4: "mxfp8"}[kind]
+    del qa, qb, D
+    torch.cuda.synchronize()
+    return {"mode": "gemm", "recipe": name, "M": M, "N": N, "K": K, "out": out, "ms": round(ms, 4),
+            "tflops": round(tf, 1), "frac_of_fp8_peak": round(tf / fp8_peak, 3)}
+
+
+def run_modes(args):
+    import torch
+    torch.cuda.set_device(0)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda") if not args.no_flush else None
+    if args.mode == "quantize":
+        print(json.dumps(quantize_point(KINDS[args.kind], args.rows, args.cols, not args.no_rowwise, args.colwise,
+                                        args.steps, args.warmup, flush)), flush=True)
+    elif args.mode == "gemm":
+        print(json.dumps(gemm_point(KINDS[args.kind], args.M, args.N, args.K, args.steps, args.warmup, flush,
+                                    args.out)), flush=True)
+    else:  # sweep: the roofline sweep workload
+        for mib in (16, 32, 64, 128, 256, 512, 1024, 2048):
+            rows = mib * 2 ** 20 // 2 // 4096
+            x = _device_tensor(rows, 4096, 5)
+            for kind in (0, 2, 3, 4):
+                print(json.dumps(quantize_point(kind, rows, 4096, True, True, args.steps, args.warmup, flush, x)),
+                      flush=True)
+            del x
+        for kind in (4, 2, 0):
+            for K in (1024, 2048, 4096, 8192, 16384):
+                print(json.dumps(gemm_point(kind, 8192, 8192, K, args.steps, args.warmup, flush)), flush=True)
+        for kind in (4, 2, 0):
+            print(json.dumps(gemm_point(kind, 8192, 53248, 16384, args.steps, args.warmup, flush)), flush=True)
+
+
 # -------------------------------------------------------------- oracle arm
 
 def cpu_baseline(budget_s: float = 15.0) -> dict:
@@ -359,7 +465,22 @@ def main():
     ap.add_argument("--skip-mx", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--mode", choices=["step", "quantize", "gemm", "sweep"], default="step",
+                    help="step: the benchmark line (default); quantize / gemm: one kernel; sweep: roofline sweep")
+    ap.add_argument("--kind", choices=list(KINDS), default="mx")
+    ap.add_argument("--rows", type=int, default=16384)
+    ap.add_argument("--cols", type=int, default=8192)
+    ap.add_argument("--no-rowwise", action="store_true")
+    ap.add_argument("--colwise", action="store_true")
+    ap.add_argument("--M", type=int, default=8192)
+    ap.add_argument("--N", type=int, default=8192)
+    ap.add_argument("--K", type=int, default=8192)
+    ap.add_argument("--out", choices=["bf16", "fp32"], default="bf16")
+    ap.add_argument("--no-flush", action="store_true")
     args = ap.parse_args()
+    if args.mode != "step" and args.impl == "ours":
+        run_modes(args)
+        return
     if args.impl == "reference":
         run_reference(args)
         return

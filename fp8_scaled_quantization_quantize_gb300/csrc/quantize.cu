@@ -411,7 +411,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                     o1[j / 4] = cvt4<FMT>(yb0, yb1, yb2, yb3);
                 }
             } else {
-#pragma unroll 1
+#pragma unroll
                 for (int j = 0; j < 32; j += 4) {
                     float a0 = bf16_lo(w[j]), a1 = bf16_lo(w[j + 1]), a2 = bf16_lo(w[j + 2]), a3 = bf16_lo(w[j + 3]);
                     float b0 = bf16_hi(w[j]), b1 = bf16_hi(w[j + 1]), b2 = bf16_hi(w[j + 2]), b3 = bf16_hi(w[j + 3]);

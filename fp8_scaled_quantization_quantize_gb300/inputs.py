@@ -96,15 +96,19 @@ def delayed_magnitudes(steps: int = 32, walk_sigma: float = 0.3, spike_step: int
     return m
 
 
-def llama70b_ffn_step(t: int, tokens: int = 4096, hidden: int = 8192, ffn: int = 28672,
-                      mags: np.ndarray | None = None):
-    """Delayed-scaling case, step t: X [tokens, hidden], W [ffn, hidden],
-    dY [tokens, ffn], base tensors seeded 100 t + {0, 1, 2}, each scaled by
-    its base sigma times the step's walk multiplier."""
+def llama70b_ffn_bases(tokens: int = 4096, hidden: int = 8192, ffn: int = 28672):
+    """Delayed-scaling case: the fp32 N(0,1) base tensors X [tokens, hidden],
+    W [ffn, hidden], dY [tokens, ffn], seeds 0, 1, 2."""
+    shapes = ((tokens, hidden), (ffn, hidden), (tokens, ffn))
+    return tuple(torch.from_numpy(normal_f32(shapes[i], i)) for i in range(3))
+
+
+def llama70b_ffn_step(t: int, bases, mags: np.ndarray | None = None):
+    """Step t of the delayed-scaling case: each base tensor times its sigma
+    (1, 0.02, 1e-4) times the step's walk multiplier, cast to bf16."""
     if mags is None:
         mags = delayed_magnitudes()
-    shapes = ((tokens, hidden), (ffn, hidden), (tokens, ffn))
-    return tuple(normal_bf16(shapes[i], 100 * t + i, DELAYED_SIGMA[i] * float(mags[t, i])) for i in range(3))
+    return tuple((bases[i] * float(DELAYED_SIGMA[i] * mags[t, i])).to(torch.bfloat16) for i in range(3))
 
 
 def sweep_tensor(mib: int, cols: int = 4096, seed: int = 5) -> torch.Tensor:

@@ -73,6 +73,7 @@ def lib():
         L.orc_mx_exponent.argtypes = [f32, i32]
         L.orc_quant_blocks.argtypes = [P, i64, i64, i64, i64, i32, i32, P, P, P, P, P, P]
         L.orc_cast_scaled.argtypes = [P, i64, f32, i32, P, P, P, P]
+        L.orc_amax_sat.argtypes = [P, i64, f32, i32, P, P, P]
         L.orc_delayed_sizeof.restype = i32
         L.orc_delayed_init.restype = i32
         L.orc_delayed_init.argtypes = [P, i32, i32, i32]
@@ -168,6 +169,16 @@ def cast_scaled(x_bits: np.ndarray, s: float, fmt: int):
     nf = np.zeros(1, dtype=np.uint64)
     lib().orc_cast_scaled(_p(x), x.size, np.float32(s), fmt, _p(q), _p(am), _p(sat), _p(nf))
     return q, float(am[0]), int(sat[0]), int(nf[0])
+
+
+def amax_sat(x_bits: np.ndarray, s: float, fmt: int):
+    """(amax, sat, nonfinite) of a per-tensor cast with multiplier s, no codes."""
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    am = np.zeros(1, dtype=np.float32)
+    sat = np.zeros(1, dtype=np.uint64)
+    nf = np.zeros(1, dtype=np.uint64)
+    lib().orc_amax_sat(_p(x), x.size, np.float32(s), fmt, _p(am), _p(sat), _p(nf))
+    return float(am[0]), int(sat[0]), int(nf[0])
 
 
 class Delayed:

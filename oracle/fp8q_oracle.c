@@ -301,6 +301,32 @@ void orc_cast_scaled(const uint16_t* x, int64_t n, float s, int fmt, uint8_t* q,
         *nonfinite = nnf;
 }
 
+/* The scalars of a per-tensor cast with multiplier s without the codes:
+ * amax over finite elements, saturated and nonfinite counts (same rules as
+ * orc_cast_scaled). */
+void orc_amax_sat(const uint16_t* x, int64_t n, float s, int fmt, float* amax_out, uint64_t* sat,
+                  uint64_t* nonfinite)
+{
+    double fmax = orc_fmax(fmt);
+    float amax = 0.0f;
+    uint64_t nsat = 0, nnf = 0;
+    for (int64_t i = 0; i < n; ++i) {
+        float f = orc_bf16_to_f32(x[i]);
+        if (!isfinite(f)) {
+            ++nnf;
+            continue;
+        }
+        if (fabsf(f) > amax)
+            amax = fabsf(f);
+        float y = f * s;
+        if (fabs((double)y) > fmax)
+            ++nsat;
+    }
+    *amax_out = amax;
+    *sat = nsat;
+    *nonfinite = nnf;
+}
+
 /* ------------------------------------------------------- delayed scaling */
 
 #define ORC_MAX_HIST 4096

@@ -235,3 +235,13 @@ def test_pack_block1x128_positions():
     assert p.shape == (5, 128)
     assert p[4, 2] == d[2, 4] and p[0, 1] == d[1, 0]
     assert np.all(p[:, 3:] == 1.0)
+
+
+def test_amax_sat_matches_cast_scaled():
+    x = _rand_bits((64, 96), 8)
+    x[3, 4] = 0x7F80      # +Inf
+    x[5, 6] = 0xFFC1      # -NaN
+    for s in (np.float32(3.0), np.float32(448.0 / 7.0), np.float32(1e4)):
+        for fmt in (O.E4M3, O.E5M2):
+            q, amax, sat, nf = O.cast_scaled(x, s, fmt)
+            assert O.amax_sat(x, s, fmt) == (amax, sat, nf)
