@@ -2,14 +2,15 @@
 // MXFP8 1x32 ("2025 FP8 quantized-training guide", sec. 2.1-2.3; "mastering
 // FP8 LLM training 1.5x speedup", scaling strategies 1-4).
 //
-// One tile kernel serves every recipe.  A CTA of 256 threads walks 128x128
-// tiles of x (persistent grid).  Each thread loads eight 16-byte vectors (rows
-// rsub + 16 i, columns 8 vcol .. 8 vcol + 7), so a 1x128 row block lives in a
-// half-warp and a 1x32 block in four lanes: block amaxes are shuffle
-// reductions.  The row-wise copy is converted straight from registers.  For
-// the column-wise copy the bf16 tile is staged in shared memory and read back
-// down its columns (32 rows x 2 columns per thread), where the 1x32 / 1x128
-// column blocks are reduced and converted; the 128-aligned tiles make every
+// One tile kernel serves every recipe.  A persistent CTA of 256 threads walks
+// 128x128 tiles of x; TMA loads each tile (two 64-column boxes in the 128-byte
+// swizzle) into a 3-stage shared-memory ring.  Row path: thread t owns row
+// t % 128 and the 64-column half t / 128, i.e. two whole 1x32 blocks or half
+// of a 1x128 block, so block maxima are packed u16x2 maxima inside the thread
+// and each scale is computed once per 32 or 64 elements.  Column path: thread
+// t reads rows 32 (t / 64) .. +31 of columns 2 (t % 64), +1 from the same
+// swizzled tile (conflict-free), reduces the 1x32 / 1x128 column blocks and
+// stores 32-byte runs of the transposed copy.  The 128-aligned tiles make every
 // scale-layout pad entry the scale of an all-zero block (code 127 / 1.0).
 #include <string.h>
 
@@ -27,7 +28,7 @@ constexpr int kThreads = 256;
 constexpr int kTile = 128;
 constexpr int kStages = 3;
 constexpr uint32_t kStageBytes = kTile * kTile * 2;  // one bf16 tile
-constexpr uint32_t kTileSmem = kStages * kStageBytes + 128;
+constexpr uint32_t kTileSmem = kStages * kStageBytes + 1024;
 constexpr uint64_t kQuantWaitNs = 1000000000ull;
 
 __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
@@ -183,24 +184,45 @@ __device__ __forceinline__ float pertensor_factor(const QuantArgs& a) {
         return a.st->scale;
 }
 
+// Byte offset of the 16-byte chunk `chunk` (8 bf16) of row r inside one
+// 128-byte-swizzled half tile [128 rows][64 bf16], as the TMA writes it.
+__device__ __forceinline__ uint32_t swz(int r, int chunk) { return (uint32_t)(r * 128 + ((chunk ^ (r & 7)) << 4)); }
+
+// Exact largest finite |x| over vectors [j0, j1) of v, counting NaN / Inf and
+// marking the vectors that hold them (the rare path behind the packed maxima).
+template <int J0, int J1>
+__device__ __forceinline__ uint32_t exact_max(const uint4 (&v)[8], uint32_t& nnf, uint32_t& vnf) {
+    uint32_t m = 0;
+#pragma unroll
+    for (int j = J0; j < J1; ++j) {
+        const uint32_t before = nnf;
+        const uint32_t mj = vec_absmax(v[j], nnf);
+        m = m > mj ? m : mj;
+        if (nnf != before) vnf |= 1u << j;
+    }
+    return m;
+}
+
 template <int KIND, int FMT, bool ROW, bool COL>
 __global__ void __launch_bounds__(kThreads, 2)
     quant_tile_kernel(const __grid_constant__ CUtensorMap tmx, QuantArgs a) {
     constexpr bool kPerTensor = (KIND == kCur || KIND == kDel);
     extern __shared__ uint8_t qsmem_raw[];
-    uint8_t* qsmem = (uint8_t*)(((uintptr_t)qsmem_raw + 127) & ~(uintptr_t)127);
+    uint8_t* qsmem = (uint8_t*)(((uintptr_t)qsmem_raw + 1023) & ~(uintptr_t)1023);
     const uint32_t sbase = smem_u32(qsmem);
     __shared__ uint32_t colred[COL && KIND == kB1 ? 4 * kTile : 1];
+    __shared__ uint32_t rowred[KIND == kB1 ? 2 * kTile : 1];
     __shared__ uint32_t red[kThreads / 32];
     __shared__ __align__(8) uint64_t bars[kStages];
     __shared__ int abort_flag;
 
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-    const int vcol = t & 15, rsub = t >> 4;
+    const int rr = t & (kTile - 1), hh = t >> 7;  // row-path: row and 64-column half of the tile
     const int64_t ntiles = a.tiles_r * a.tiles_c;
     auto bar = [&](int s) { return smem_u32(&bars[s]); };
 
-    // stage s holds one bf16 tile [128][128] (row pitch 256 bytes), loaded by TMA
+    // stage s: the tile's two 64-column halves, each [128 rows][128 bytes] in the
+    // 128-byte swizzle, loaded by two TMA boxes
     auto issue = [&](int64_t it) {
         const int64_t tileid = blockIdx.x + it * (int64_t)gridDim.x;
         if (tileid >= ntiles) return;
@@ -208,6 +230,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int64_t tr = tileid / a.tiles_c, tc = tileid % a.tiles_c;
         mbar_expect_tx(bar(s), kStageBytes);
         tma_load_2d(sbase + s * kStageBytes, &tmx, (int)(tc * kTile), (int)(tr * kTile), bar(s));
+        tma_load_2d(sbase + s * kStageBytes + kStageBytes / 2, &tmx, (int)(tc * kTile + 64), (int)(tr * kTile), bar(s));
     };
     if (t == 0) {
         for (int s = 0; s < kStages; ++s) mbar_init(bar(s), 1);
@@ -233,99 +256,94 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (int64_t tileid = blockIdx.x; tileid < ntiles; tileid += gridDim.x, ++it) {
         const int64_t tr = tileid / a.tiles_c, tc = tileid % a.tiles_c;
         const int64_t r0 = tr * kTile, c0 = tc * kTile;
-        const int64_t c = c0 + vcol * 8;
-        const bool cin = c < a.C;
         const int stg = (int)(it % kStages);
         const bool ok = mbar_wait_bounded(bar(stg), (uint32_t)((it / kStages) & 1), &abort_flag, &g_quant_errors,
                                           2u, kQuantWaitNs);
         if (__syncthreads_or(!ok)) break;  // the whole CTA leaves together
-        const uint8_t* tile8 = qsmem + stg * kStageBytes;
-        const uint32_t* tile = (const uint32_t*)tile8;
+        const uint8_t* stage = qsmem + stg * kStageBytes;
 
+        // ---------------- analysis: row rr, columns 64 hh .. 64 hh + 63 of the tile
+        const uint8_t* half = stage + hh * (kStageBytes / 2);
         uint4 v[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] = *(const uint4*)(tile8 + (rsub + 16 * i) * (kTile * 2) + vcol * 16);
-        uint32_t vmax[8];
-        uint32_t vnf = 0;  // bit i: vector i holds a NaN / Inf
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            uint32_t m = fold16(vec_pmax(v[i]));
-            if (m >= 0x7F80u) {  // NaN / Inf in this vector: exact finite max and count
-                m = vec_absmax(v[i], nnf);
-                vnf |= 1u << i;
+        for (int j = 0; j < 8; ++j) v[j] = *(const uint4*)(half + swz(rr, j));
+        uint32_t vnf = 0;       // bit j: vector j holds a NaN / Inf
+        uint32_t mq[2];         // MX: the two 1x32 blocks' maxima; else mq[0] = the half-row maximum
+        {
+            const uint32_t p0 = max_u16x2(max_u16x2(vec_pmax(v[0]), vec_pmax(v[1])),
+                                          max_u16x2(vec_pmax(v[2]), vec_pmax(v[3])));
+            const uint32_t p1 = max_u16x2(max_u16x2(vec_pmax(v[4]), vec_pmax(v[5])),
+                                          max_u16x2(vec_pmax(v[6]), vec_pmax(v[7])));
+            if constexpr (KIND == kMX) {
+                mq[0] = fold16(p0);
+                mq[1] = fold16(p1);
+                if (mq[0] >= 0x7F80u) mq[0] = exact_max<0, 4>(v, nnf, vnf);
+                if (mq[1] >= 0x7F80u) mq[1] = exact_max<4, 8>(v, nnf, vnf);
+            } else {
+                mq[0] = fold16(max_u16x2(p0, p1));
+                if (mq[0] >= 0x7F80u) mq[0] = exact_max<0, 8>(v, nnf, vnf);
+                mq[1] = mq[0];
             }
-            vmax[i] = m;
         }
 
-        // 128x128 tile amax (also the delayed recipe's running tensor amax)
-        float kd_tile = 1.0f;
-        if constexpr (KIND == kB128 || KIND == kDel) {
-            uint32_t m = 0;
+        // ---------------- block scales
+        float kq[2] = {ks, ks};
+        if constexpr (KIND == kDel) {
+            tmax_all = tmax_all > mq[0] ? tmax_all : mq[0];
+        } else if constexpr (KIND == kB128) {
+            const uint32_t m = warp_max_u32(mq[0]);
+            if (lane == 0) red[warp] = m;
+            __syncthreads();
+            uint32_t mm = 0;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) m = m > vmax[i] ? m : vmax[i];
-            if constexpr (KIND == kDel) {
-                tmax_all = tmax_all > m ? tmax_all : m;
-            } else {
-                m = warp_max_u32(m);
-                if (lane == 0) red[warp] = m;
-                __syncthreads();
-                uint32_t mm = 0;
-#pragma unroll
-                for (int w = 0; w < kThreads / 32; ++w) mm = mm > red[w] ? mm : red[w];
-                __syncthreads();
-                kd_tile = block_scale<FMT>(__uint_as_float(mm << 16));
-                if (t == 0) {
-                    if (ROW) ((float*)a.s_row)[tr * a.tiles_c + tc] = kd_tile;
-                    if (COL) ((float*)a.s_col)[tc * a.tiles_r + tr] = kd_tile;
-                }
+            for (int w = 0; w < kThreads / 32; ++w) mm = mm > red[w] ? mm : red[w];
+            __syncthreads();
+            kq[0] = kq[1] = block_scale<FMT>(__uint_as_float(mm << 16));
+            if (t == 0) {
+                if (ROW) ((float*)a.s_row)[tr * a.tiles_c + tc] = kq[0];
+                if (COL) ((float*)a.s_col)[tc * a.tiles_r + tr] = kq[0];
+            }
+        } else if constexpr (KIND == kB1) {
+            rowred[hh * kTile + rr] = mq[0];
+            __syncthreads();
+            const uint32_t m = max(rowred[rr], rowred[kTile + rr]);
+            mq[0] = mq[1] = m;
+            kq[0] = kq[1] = block_scale<FMT>(__uint_as_float(m << 16));
+            if (ROW && hh == 0) ((float*)a.s_row)[tc * (a.tiles_r * kTile) + r0 + rr] = kq[0];
+        } else if constexpr (KIND == kMX) {
+            const int e0 = mx_exponent<FMT>(mq[0] << 16), e1 = mx_exponent<FMT>(mq[1] << 16);
+            kq[0] = exp2_neg(e0);
+            kq[1] = exp2_neg(e1);
+            if (ROW) {
+                // this row's scale columns 4 tc + 2 hh + {0, 1} in the 128x4 tile (tr, tc)
+                uint8_t* tileb = (uint8_t*)a.s_row + (tr * a.tiles_c + tc) * 512;
+                *(uint16_t*)(tileb + (rr & 31) * 16 + (rr >> 5) * 4 + 2 * hh) =
+                    (uint16_t)((uint32_t)(e0 + 127) | ((uint32_t)(e1 + 127) << 8));
             }
         }
+
         // ---------------- row-wise copy
         if constexpr (ROW) {
+            const Factor f0 = make_factor<KIND>(kq[0]);
+            const Factor f1 = (KIND == kMX) ? make_factor<KIND>(kq[1]) : f0;
+            const bool s0 = may_saturate<KIND, FMT>(mq[0], f0);
+            const bool s1 = (KIND == kMX) ? may_saturate<KIND, FMT>(mq[1], f1) : s0;
+            uint2 q[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int64_t r = r0 + rsub + 16 * i;
-                float k;
-                if constexpr (kPerTensor) {
-                    k = ks;
-                } else if constexpr (KIND == kB128) {
-                    k = kd_tile;
-                } else if constexpr (KIND == kB1) {
-                    uint32_t m = vmax[i];
-                    m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
-                    m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
-                    m = max(m, __shfl_xor_sync(0xffffffffu, m, 4));
-                    m = max(m, __shfl_xor_sync(0xffffffffu, m, 8));
-                    k = block_scale<FMT>(__uint_as_float(m << 16));
-                    if (vcol == 0) {
-                        const int64_t Rp = a.tiles_r * kTile;
-                        ((float*)a.s_row)[tc * Rp + r] = k;
-                    }
-                } else {  // MXFP8
-                    uint32_t m = vmax[i];
-                    m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
-                    m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
-                    const int e = mx_exponent<FMT>(m << 16);
-                    k = exp2_neg(e);
-                    // gather the four block codes of this row segment into lane vcol == 0
-                    const uint32_t code = (uint32_t)(e + 127);
-                    const uint32_t c1 = __shfl_down_sync(0xffffffffu, code, 4);
-                    const uint32_t c2 = __shfl_down_sync(0xffffffffu, code, 8);
-                    const uint32_t c3 = __shfl_down_sync(0xffffffffu, code, 12);
-                    if (vcol == 0) {
-                        const int rr = (int)(r & 127);
-                        uint8_t* tileb = (uint8_t*)a.s_row + (tr * a.tiles_c + tc) * 512;
-                        *(uint32_t*)(tileb + (rr & 31) * 16 + (rr >> 5) * 4) = code | (c1 << 8) | (c2 << 16) | (c3 << 24);
-                    }
-                }
-                uint2 q;
-                if (!((vnf >> i) & 1u)) {
-                    const Factor f = make_factor<KIND>(k);
-                    q = convert8_fast<KIND, FMT>(v[i], f, nsat_row, may_saturate<KIND, FMT>(vmax[i], f));
-                } else {
-                    q = convert8<KIND, FMT>(v[i], k, nsat_row, true);
-                }
-                if (cin && r < a.R) *(uint2*)(a.q_row + r * a.C + c) = q;
+            for (int j = 0; j < 8; ++j) {
+                const Factor f = (j < 4) ? f0 : f1;
+                if (!((vnf >> j) & 1u))
+                    q[j] = convert8_fast<KIND, FMT>(v[j], f, nsat_row, (j < 4) ? s0 : s1);
+                else
+                    q[j] = convert8<KIND, FMT>(v[j], f.k, nsat_row, true);
+            }
+            const int64_t row = r0 + rr;
+            if (row < a.R) {
+                const int64_t col = c0 + 64 * hh;
+                uint8_t* dst = a.q_row + row * a.C + col;
+#pragma unroll
+                for (int j = 0; j < 8; j += 2)
+                    if (col + 8 * j < a.C) *(uint4*)(dst + 8 * j) = make_uint4(q[j].x, q[j].y, q[j + 1].x, q[j + 1].y);
             }
         }
 
@@ -333,15 +351,18 @@ __global__ void __launch_bounds__(kThreads, 2)
         if constexpr (COL) {
             const bool tile_nf = __syncthreads_or(vnf != 0) != 0;
             const int p = t & 63, qd = t >> 6;  // column pair, 32-row quarter
+            // columns 2p, 2p+1 sit in half p / 32, chunk (2p % 64) / 8, bytes (2p % 8) * 2
+            const uint8_t* chalf = stage + (p >> 5) * (kStageBytes / 2) + ((2 * p) & 7) * 2;
+            const int chunk = ((2 * p) & 63) >> 3;
             uint32_t w[32];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) w[j] = tile[(32 * qd + j) * (kTile / 2) + p];
+            for (int j = 0; j < 32; ++j) w[j] = *(const uint32_t*)(chalf + swz(32 * qd + j, chunk));
             float k0, k1;
             uint32_t cm0 = 0x7F7Fu, cm1 = 0x7F7Fu;  // column maxima (re-quantized kinds)
             if constexpr (kPerTensor) {
                 k0 = k1 = ks;
             } else if constexpr (KIND == kB128) {
-                k0 = k1 = kd_tile;
+                k0 = k1 = kq[0];
             } else {
                 uint32_t pm = 0;
 #pragma unroll
@@ -598,8 +619,8 @@ fp8q_status launch_tile(const QuantArgs& a, cudaStream_t s) {
     const int64_t ntiles = a.tiles_r * a.tiles_c;
     CUtensorMap tm;
     memset(&tm, 0, sizeof(tm));
-    if (ntiles > 0 && !make_map_2d(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.x, a.R, a.C, kTile, kTile,
-                                   CU_TENSOR_MAP_SWIZZLE_NONE))
+    if (ntiles > 0 && !make_map_2d(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.x, a.R, a.C, kTile / 2, kTile,
+                                   CU_TENSOR_MAP_SWIZZLE_128B))
         return FP8Q_ERR_CUDA;
     int64_t grid = (int64_t)num_sms() * 2;
     if (ntiles < grid) grid = ntiles;
