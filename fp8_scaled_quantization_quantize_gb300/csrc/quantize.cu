@@ -147,33 +147,38 @@ __device__ __forceinline__ float div_rn_recip(float x, float d, float r) {
     return __uint_as_float((__float_as_uint(q2) & 0x7FFFFFFFu) | (__float_as_uint(x) & 0x80000000u));
 }
 
-// The recipe's scaled value of a finite element.
-template <int KIND>
+// The recipe's scaled value of a finite element (FAST: the blockwise divisor
+// is in the reciprocal shortcut's range; the caller branches once per block).
+template <int KIND, bool FAST = true>
 __device__ __forceinline__ float apply(float x, const Factor& f) {
-    if constexpr (KIND == kB1 || KIND == kB128)
-        return f.fast ? div_rn_recip(x, f.k, f.r) : __fdiv_rn(x, f.k);
-    else
+    if constexpr (KIND == kB1 || KIND == kB128) {
+        if constexpr (FAST)
+            return div_rn_recip(x, f.k, f.r);
+        else
+            return __fdiv_rn(x, f.k);
+    } else {
         return __fmul_rn(x, f.k);
+    }
 }
 
 // Converts the 8 finite bf16 of v; counts saturation only when the caller
 // found that the vector's largest magnitude can exceed fmax once scaled
 // (the scaled value is monotone in |x|).
-template <int KIND, int FMT>
+template <int KIND, int FMT, bool FAST>
 __device__ __forceinline__ uint2 convert8_fast(const uint4& v, const Factor& f, uint32_t& nsat, bool count) {
-    float y[8] = {apply<KIND>(bf16_lo(v.x), f), apply<KIND>(bf16_hi(v.x), f), apply<KIND>(bf16_lo(v.y), f),
-                  apply<KIND>(bf16_hi(v.y), f), apply<KIND>(bf16_lo(v.z), f), apply<KIND>(bf16_hi(v.z), f),
-                  apply<KIND>(bf16_lo(v.w), f), apply<KIND>(bf16_hi(v.w), f)};
-    if (count) {
+    float y[8] = {apply<KIND, FAST>(bf16_lo(v.x), f), apply<KIND, FAST>(bf16_hi(v.x), f),
+                  apply<KIND, FAST>(bf16_lo(v.y), f), apply<KIND, FAST>(bf16_hi(v.y), f),
+                  apply<KIND, FAST>(bf16_lo(v.z), f), apply<KIND, FAST>(bf16_hi(v.z), f),
+                  apply<KIND, FAST>(bf16_lo(v.w), f), apply<KIND, FAST>(bf16_hi(v.w), f)};
 #pragma unroll
-        for (int j = 0; j < 8; ++j) nsat += fabsf(y[j]) > Fmt<FMT>::fmax ? 1u : 0u;
-    }
+    for (int j = 0; j < 8; ++j) nsat += (count && fabsf(y[j]) > Fmt<FMT>::fmax) ? 1u : 0u;  // predicated, no branch
     return make_uint2(cvt4<FMT>(y[0], y[1], y[2], y[3]), cvt4<FMT>(y[4], y[5], y[6], y[7]));
 }
 
 template <int KIND, int FMT>
 __device__ __forceinline__ bool may_saturate(uint32_t max_bits16, const Factor& f) {
-    return fabsf(apply<KIND>(__uint_as_float(max_bits16 << 16), f)) > Fmt<FMT>::fmax;
+    const float m = __uint_as_float(max_bits16 << 16);
+    return fabsf(f.fast ? apply<KIND, true>(m, f) : apply<KIND, false>(m, f)) > Fmt<FMT>::fmax;
 }
 
 template <int KIND, int FMT>
@@ -329,13 +334,19 @@ __global__ void __launch_bounds__(kThreads, 2)
             const bool s0 = may_saturate<KIND, FMT>(mq[0], f0);
             const bool s1 = (KIND == kMX) ? may_saturate<KIND, FMT>(mq[1], f1) : s0;
             uint2 q[8];
+            if (vnf == 0 && f0.fast && f1.fast) {  // the common case: one straight-line block
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const Factor f = (j < 4) ? f0 : f1;
-                if (!((vnf >> j) & 1u))
-                    q[j] = convert8_fast<KIND, FMT>(v[j], f, nsat_row, (j < 4) ? s0 : s1);
-                else
-                    q[j] = convert8<KIND, FMT>(v[j], f.k, nsat_row, true);
+                for (int j = 0; j < 8; ++j)
+                    q[j] = convert8_fast<KIND, FMT, true>(v[j], (j < 4) ? f0 : f1, nsat_row, (j < 4) ? s0 : s1);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const Factor f = (j < 4) ? f0 : f1;
+                    if ((vnf >> j) & 1u)
+                        q[j] = convert8<KIND, FMT>(v[j], f.k, nsat_row, true);
+                    else
+                        q[j] = convert8_fast<KIND, FMT, false>(v[j], f, nsat_row, (j < 4) ? s0 : s1);
+                }
             }
             const int64_t row = r0 + rr;
             if (row < a.R) {
@@ -412,22 +423,20 @@ __global__ void __launch_bounds__(kThreads, 2)
             // convert 32 rows of columns 2p, 2p+1
             uint32_t o0[8], o1[8];
             uint32_t ns = 0;
-            if (!tile_nf) {
-                const Factor f0 = make_factor<KIND>(k0), f1 = make_factor<KIND>(k1);
+            const Factor f0 = make_factor<KIND>(k0), f1 = make_factor<KIND>(k1);
+            if (!tile_nf && f0.fast && f1.fast) {
                 const bool req = (KIND == kB1 || KIND == kMX);
                 const bool c0s = req && may_saturate<KIND, FMT>(cm0, f0), c1s = req && may_saturate<KIND, FMT>(cm1, f1);
+                constexpr float fm = Fmt<FMT>::fmax;
 #pragma unroll
                 for (int j = 0; j < 32; j += 4) {
-                    const float ya0 = apply<KIND>(bf16_lo(w[j]), f0), ya1 = apply<KIND>(bf16_lo(w[j + 1]), f0);
-                    const float ya2 = apply<KIND>(bf16_lo(w[j + 2]), f0), ya3 = apply<KIND>(bf16_lo(w[j + 3]), f0);
-                    const float yb0 = apply<KIND>(bf16_hi(w[j]), f1), yb1 = apply<KIND>(bf16_hi(w[j + 1]), f1);
-                    const float yb2 = apply<KIND>(bf16_hi(w[j + 2]), f1), yb3 = apply<KIND>(bf16_hi(w[j + 3]), f1);
-                    if (c0s)
-                        ns += (fabsf(ya0) > Fmt<FMT>::fmax) + (fabsf(ya1) > Fmt<FMT>::fmax) +
-                              (fabsf(ya2) > Fmt<FMT>::fmax) + (fabsf(ya3) > Fmt<FMT>::fmax);
-                    if (c1s)
-                        ns += (fabsf(yb0) > Fmt<FMT>::fmax) + (fabsf(yb1) > Fmt<FMT>::fmax) +
-                              (fabsf(yb2) > Fmt<FMT>::fmax) + (fabsf(yb3) > Fmt<FMT>::fmax);
+                    const float ya0 = apply<KIND, true>(bf16_lo(w[j]), f0), ya1 = apply<KIND, true>(bf16_lo(w[j + 1]), f0);
+                    const float ya2 = apply<KIND, true>(bf16_lo(w[j + 2]), f0), ya3 = apply<KIND, true>(bf16_lo(w[j + 3]), f0);
+                    const float yb0 = apply<KIND, true>(bf16_hi(w[j]), f1), yb1 = apply<KIND, true>(bf16_hi(w[j + 1]), f1);
+                    const float yb2 = apply<KIND, true>(bf16_hi(w[j + 2]), f1), yb3 = apply<KIND, true>(bf16_hi(w[j + 3]), f1);
+                    ns += (c0s && fabsf(ya0) > fm) + (c0s && fabsf(ya1) > fm) + (c0s && fabsf(ya2) > fm) +
+                          (c0s && fabsf(ya3) > fm) + (c1s && fabsf(yb0) > fm) + (c1s && fabsf(yb1) > fm) +
+                          (c1s && fabsf(yb2) > fm) + (c1s && fabsf(yb3) > fm);
                     o0[j / 4] = cvt4<FMT>(ya0, ya1, ya2, ya3);
                     o1[j / 4] = cvt4<FMT>(yb0, yb1, yb2, yb3);
                 }
@@ -454,16 +463,16 @@ __global__ void __launch_bounds__(kThreads, 2)
                 }
             }
             nsat_col += ns;
-            const int64_t cc = c0 + 2 * p, rr = r0 + 32 * qd;
-            if (rr < a.R) {
-                const bool full = rr + 32 <= a.R;  // R % 16 == 0: else exactly 16 rows remain
+            const int64_t cc = c0 + 2 * p, rowc = r0 + 32 * qd;
+            if (rowc < a.R) {
+                const bool full = rowc + 32 <= a.R;  // R % 16 == 0: else exactly 16 rows remain
                 if (cc < a.C) {
-                    uint4* dst = (uint4*)(a.q_col + cc * a.R + rr);
+                    uint4* dst = (uint4*)(a.q_col + cc * a.R + rowc);
                     dst[0] = make_uint4(o0[0], o0[1], o0[2], o0[3]);
                     if (full) dst[1] = make_uint4(o0[4], o0[5], o0[6], o0[7]);
                 }
                 if (cc + 1 < a.C) {
-                    uint4* dst = (uint4*)(a.q_col + (cc + 1) * a.R + rr);
+                    uint4* dst = (uint4*)(a.q_col + (cc + 1) * a.R + rowc);
                     dst[0] = make_uint4(o1[0], o1[1], o1[2], o1[3]);
                     if (full) dst[1] = make_uint4(o1[4], o1[5], o1[6], o1[7]);
                 }
