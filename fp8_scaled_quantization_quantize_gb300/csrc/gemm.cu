@@ -13,12 +13,13 @@
 //                d_A[m][kb] * d_B[n(/128)][kb] and add it to fp32 register
 //                accumulators (sec. 2.2 1x128 x 128x128 tiles, or 1x128 x 1x128).
 //
-// Persistent kernel, one CTA per SM, 320 threads:
+// Persistent kernel, one CTA per SM, 576 threads:
 //   warp 0      TMA producer: A box 128x128 B, B box 256x128 B (128-byte
-//               swizzle) per stage, plus the MX scale tiles (bulk copies);
+//               swizzle) per stage (3 stages), plus the MX scale tiles (bulk copies);
 //   warp 1      TMEM allocator and single-thread MMA issuer (M128 N256 K32);
-//   warps 2-9   epilogue: warp w reads TMEM lanes 32 (w % 4) .. +31 (its rows)
-//               and columns 128 ((w - 2) / 4) .. +127.
+//   warps 2-17  epilogue: warp w reads TMEM lanes 32 (w % 4) .. +31 (its rows)
+//               and columns 64 ((w - 2) / 4) .. +63, and writes them through a
+//               swizzled shared-memory box and a TMA store.
 // Every mbarrier wait is bounded (about one second of %globaltimer); a wait
 // that gives up sets bit 0 of g_device_errors, raises a CTA-wide abort flag,
 // and the CTA drains its in-flight copies and MMAs (bounded) and frees TMEM.
@@ -33,7 +34,7 @@ __device__ unsigned int g_device_errors = 0;
 
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 128, STAGES = 4;
+constexpr int BM = 128, BN = 256, BK = 128, STAGES = 3;
 constexpr int kEpiWarps = 16;
 constexpr int kEpiCols = BN / (kEpiWarps / 4);  // accumulator columns per epilogue warp
 constexpr int kThreads = 64 + 32 * kEpiWarps;
@@ -44,10 +45,13 @@ constexpr uint32_t OFF_B = OFF_A + STAGES * A_STAGE;
 constexpr uint32_t OFF_SFA = OFF_B + STAGES * B_STAGE;
 constexpr uint32_t OFF_SFB = OFF_SFA + STAGES * SFA_STAGE;
 constexpr uint32_t OFF_SBW = OFF_SFB + STAGES * SFB_STAGE;      // per-epilogue-warp 1x128 B scales
-constexpr uint32_t OFF_BAR = OFF_SBW + kEpiWarps * kEpiCols * 4;
+constexpr uint32_t OFF_STG = (OFF_SBW + kEpiWarps * kEpiCols * 4 + 1023) / 1024 * 1024;
+constexpr uint32_t STG_WARP = 32 * 128;                          // one 32-row x 128-byte output box per warp
+constexpr uint32_t OFF_BAR = OFF_STG + kEpiWarps * STG_WARP;
 constexpr uint32_t NBARS = 2 * STAGES + 5;
 constexpr uint32_t OFF_MISC = OFF_BAR + 8 * NBARS;
 constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;            // + alignment slack
+static_assert(SMEM_BYTES <= 232448, "shared memory budget of one CTA");
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t SF_TMEM_COL = 256;                            // MX scale slots: 12 columns per stage
 constexpr uint64_t kWaitNs = 1000000000ull;
@@ -159,27 +163,66 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     return r;
 }
 
-// Writes 32 consecutive fp32 results of one output row (masked by N).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int x, int y, uint32_t src) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(map), "r"(x),
+                 "r"(y), "r"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// Stores this warp's 32 rows x 64 columns of D (v: the lane's row, scaled by
+// `scale`) through its shared-memory staging box and TMA: 128-byte rows in
+// the 128-byte swizzle (16-byte chunk c of row r at r*128 + (c ^ (r%8))*16),
+// so the lanes' writes do not conflict and the TMA clips rows / columns
+// outside D.  bf16: one 64-column box; fp32: two 32-column boxes.
 template <bool OUT_F32>
-__device__ __forceinline__ void store_row32(const Params& p, int64_t row, int64_t col, const float* v) {
-    if (OUT_F32) {
-        float* dst = (float*)p.D + row * p.N + col;
+__device__ __forceinline__ void store_slice(const CUtensorMap* mapD, uint8_t* stg, uint32_t stg_s, int lane, int x0,
+                                            int y0, int n_extent, int m_extent, const float* v, float scale) {
+    const int r = lane;
+    if (!OUT_F32) {
+        bulk_wait_read();  // lane 0's previous box has been read out of stg
+        __syncwarp();
 #pragma unroll
-        for (int j = 0; j < 32; j += 4)
-            if (col + j < p.N) *(float4*)(dst + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+        for (int c = 0; c < 8; ++c) {
+            const float* q = v + 8 * c;
+            const uint4 u = make_uint4(pack_bf16(q[0] * scale, q[1] * scale), pack_bf16(q[2] * scale, q[3] * scale),
+                                       pack_bf16(q[4] * scale, q[5] * scale), pack_bf16(q[6] * scale, q[7] * scale));
+            *(uint4*)(stg + r * 128 + ((c ^ (r & 7)) << 4)) = u;
+        }
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0 && x0 < n_extent && y0 < m_extent) {  // boxes wholly outside D are skipped
+            tma_store_2d(mapD, x0, y0, stg_s);
+            bulk_commit();
+        }
     } else {
-        uint16_t* dst = (uint16_t*)p.D + row * p.N + col;
 #pragma unroll
-        for (int j = 0; j < 32; j += 8)
-            if (col + j < p.N)
-                *(uint4*)(dst + j) = make_uint4(pack_bf16(v[j], v[j + 1]), pack_bf16(v[j + 2], v[j + 3]),
-                                                pack_bf16(v[j + 4], v[j + 5]), pack_bf16(v[j + 6], v[j + 7]));
+        for (int hx = 0; hx < 2; ++hx) {
+            bulk_wait_read();
+            __syncwarp();
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const float* q = v + 32 * hx + 4 * c;
+                *(float4*)(stg + r * 128 + ((c ^ (r & 7)) << 4)) =
+                    make_float4(q[0] * scale, q[1] * scale, q[2] * scale, q[3] * scale);
+            }
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0 && x0 + 32 * hx < n_extent && y0 < m_extent) {
+                tma_store_2d(mapD, x0 + 32 * hx, y0, stg_s);
+                bulk_commit();
+            }
+        }
     }
 }
 
 template <int REC, bool OUT_F32>
 __global__ void __launch_bounds__(kThreads, 1)
-    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Params p) {
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const __grid_constant__ CUtensorMap tmD, const Params p) {
     constexpr uint32_t kAcc = (REC == REC_PT) ? 2u : 1u;  // TMEM accumulator buffers of 256 columns
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -340,6 +383,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         float sab = 1.0f;
         if (REC == REC_PT) sab = __fmul_rn(*p.sa_inv, *p.sb_inv);
         float* sbw = (float*)(smem + OFF_SBW) + ew * kEpiCols;
+        uint8_t* stg = smem + OFF_STG + ew * STG_WARP;
+        const uint32_t stg_s = sb + OFF_STG + ew * STG_WARP;
         uint32_t tile_i = 0;
         uint64_t kbg = 0;
         for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++tile_i) {
@@ -362,15 +407,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(tempty(abuf));
-                if (row < p.M) {
+                float vf[64];
 #pragma unroll
-                    for (int c = 0; c < 2; ++c) {
-                        float v[32];
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[32 * c + i]) * sab;
-                        store_row32<OUT_F32>(p, row, col0 + 32 * c, v);
-                    }
-                }
+                for (int i = 0; i < 64; ++i) vf[i] = __uint_as_float(r[i]);
+                store_slice<OUT_F32>(&tmD, stg, stg_s, lane, (int)col0, (int)(mb * BM + 32 * q), (int)p.N, (int)p.M, vf,
+                                     sab);
             } else {
                 float acc[kEpiCols];
 #pragma unroll
@@ -447,14 +488,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (lane == 0) mbar_arrive(tempty(buf));
                 }
                 if (!ok) break;
-                if (row < p.M) {
-#pragma unroll
-                    for (int c = 0; c < kEpiCols / 32; ++c) store_row32<OUT_F32>(p, row, col0 + 32 * c, acc + 32 * c);
-                }
+                store_slice<OUT_F32>(&tmD, stg, stg_s, lane, (int)col0, (int)(mb * BM + 32 * q), (int)p.N, (int)p.M, acc,
+                                     1.0f);
             }
         }
     }
 
+    if (warp >= 2 && lane == 0) bulk_wait_all();  // this warp's output boxes are written
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
@@ -474,7 +514,8 @@ bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t K, uint32_
 int g_sms = 0;
 
 template <int REC, bool F32>
-fp8q_status launch_t(const CUtensorMap& ma, const CUtensorMap& mb, const Params& p, cudaStream_t s) {
+fp8q_status launch_t(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& md, const Params& p,
+                     cudaStream_t s) {
     auto kern = gemm_kernel<REC, F32>;
     static bool attr = false;
     if (!attr) {
@@ -490,13 +531,19 @@ fp8q_status launch_t(const CUtensorMap& ma, const CUtensorMap& mb, const Params&
     }
     const int64_t ntiles = p.tiles_m * p.tiles_n;
     const int grid = (int)(ntiles < g_sms ? ntiles : g_sms);
-    kern<<<grid, kThreads, SMEM_BYTES, s>>>(ma, mb, p);
+    kern<<<grid, kThreads, SMEM_BYTES, s>>>(ma, mb, md, p);
     return cudaGetLastError() == cudaSuccess ? FP8Q_OK : FP8Q_ERR_CUDA;
 }
 
 template <int REC>
 fp8q_status launch_rec(const CUtensorMap& ma, const CUtensorMap& mb, const Params& p, int out_dtype, cudaStream_t s) {
-    return out_dtype == 1 ? launch_t<REC, true>(ma, mb, p, s) : launch_t<REC, false>(ma, mb, p, s);
+    // D [M][N] row-major: 32-row boxes of 128 bytes (64 bf16 / 32 fp32) in the 128-byte swizzle
+    CUtensorMap md;
+    const bool f32 = out_dtype == 1;
+    if (!make_map_2d(&md, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, f32 ? 4 : 2, p.D,
+                     p.M, p.N, f32 ? 32 : 64, 32, CU_TENSOR_MAP_SWIZZLE_128B))
+        return FP8Q_ERR_CUDA;
+    return f32 ? launch_t<REC, true>(ma, mb, md, p, s) : launch_t<REC, false>(ma, mb, md, p, s);
 }
 
 }  // namespace
