@@ -15,7 +15,7 @@
 //
 // Persistent kernel, one CTA per SM, 576 threads:
 //   warp 0      TMA producer: A box 128x128 B, B box 256x128 B (128-byte
-//               swizzle) per stage (3 stages), plus the MX scale tiles (bulk copies);
+//               swizzle) per stage (4 stages), plus the MX scale tiles (bulk copies);
 //   warp 1      TMEM allocator and single-thread MMA issuer (M128 N256 K32);
 //   warps 2-17  epilogue: warp w reads TMEM lanes 32 (w % 4) .. +31 (its rows)
 //               and columns 64 ((w - 2) / 4) .. +63, and writes them through a
@@ -34,7 +34,7 @@ __device__ unsigned int g_device_errors = 0;
 
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 128, STAGES = 3;
+constexpr int BM = 128, BN = 256, BK = 128, STAGES = 4;
 constexpr int kEpiWarps = 16;
 constexpr int kEpiCols = BN / (kEpiWarps / 4);  // accumulator columns per epilogue warp
 constexpr int kThreads = 64 + 32 * kEpiWarps;
@@ -46,7 +46,7 @@ constexpr uint32_t OFF_SFA = OFF_B + STAGES * B_STAGE;
 constexpr uint32_t OFF_SFB = OFF_SFA + STAGES * SFA_STAGE;
 constexpr uint32_t OFF_SBW = OFF_SFB + STAGES * SFB_STAGE;      // per-epilogue-warp 1x128 B scales
 constexpr uint32_t OFF_STG = (OFF_SBW + kEpiWarps * kEpiCols * 4 + 1023) / 1024 * 1024;
-constexpr uint32_t STG_WARP = 32 * 128;                          // one 32-row x 128-byte output box per warp
+constexpr uint32_t STG_WARP = 32 * 32;                           // one 32-row x 32-byte output box per warp
 constexpr uint32_t OFF_BAR = OFF_STG + kEpiWarps * STG_WARP;
 constexpr uint32_t NBARS = 2 * STAGES + 5;
 constexpr uint32_t OFF_MISC = OFF_BAR + 8 * NBARS;
@@ -174,47 +174,41 @@ __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wa
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 // Stores this warp's 32 rows x 64 columns of D (v: the lane's row, scaled by
-// `scale`) through its shared-memory staging box and TMA: 128-byte rows in
-// the 128-byte swizzle (16-byte chunk c of row r at r*128 + (c ^ (r%8))*16),
-// so the lanes' writes do not conflict and the TMA clips rows / columns
-// outside D.  bf16: one 64-column box; fp32: two 32-column boxes.
+// `scale`) through its 1 KB shared-memory staging box and TMA stores, in
+// rounds of 32-byte row pieces (16 bf16 / 8 fp32) in the 32-byte swizzle
+// (16-byte chunk c of row r at r*32 + (c ^ ((r / 4) % 2))*16, so the lanes'
+// writes do not conflict).  The TMA clips rows / columns outside D; boxes
+// wholly outside D are skipped.
 template <bool OUT_F32>
 __device__ __forceinline__ void store_slice(const CUtensorMap* mapD, uint8_t* stg, uint32_t stg_s, int lane, int x0,
                                             int y0, int n_extent, int m_extent, const float* v, float scale) {
     const int r = lane;
-    if (!OUT_F32) {
-        bulk_wait_read();  // lane 0's previous box has been read out of stg
-        __syncwarp();
+    constexpr int kCols = OUT_F32 ? 8 : 16;  // columns per 32-byte piece
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-            const float* q = v + 8 * c;
-            const uint4 u = make_uint4(pack_bf16(q[0] * scale, q[1] * scale), pack_bf16(q[2] * scale, q[3] * scale),
-                                       pack_bf16(q[4] * scale, q[5] * scale), pack_bf16(q[6] * scale, q[7] * scale));
-            *(uint4*)(stg + r * 128 + ((c ^ (r & 7)) << 4)) = u;
+    for (int rd = 0; rd < 64 / kCols; ++rd) {
+        bulk_wait_read();  // the previous box has been read out of stg
+        __syncwarp();
+        const float* q = v + kCols * rd;
+        uint4 c0, c1;
+        if (!OUT_F32) {
+            c0 = make_uint4(pack_bf16(q[0] * scale, q[1] * scale), pack_bf16(q[2] * scale, q[3] * scale),
+                            pack_bf16(q[4] * scale, q[5] * scale), pack_bf16(q[6] * scale, q[7] * scale));
+            c1 = make_uint4(pack_bf16(q[8] * scale, q[9] * scale), pack_bf16(q[10] * scale, q[11] * scale),
+                            pack_bf16(q[12] * scale, q[13] * scale), pack_bf16(q[14] * scale, q[15] * scale));
+        } else {
+            c0 = make_uint4(__float_as_uint(q[0] * scale), __float_as_uint(q[1] * scale), __float_as_uint(q[2] * scale),
+                            __float_as_uint(q[3] * scale));
+            c1 = make_uint4(__float_as_uint(q[4] * scale), __float_as_uint(q[5] * scale), __float_as_uint(q[6] * scale),
+                            __float_as_uint(q[7] * scale));
         }
+        const int sw = (r >> 2) & 1;
+        *(uint4*)(stg + r * 32 + ((0 ^ sw) << 4)) = c0;
+        *(uint4*)(stg + r * 32 + ((1 ^ sw) << 4)) = c1;
         fence_async_smem();
         __syncwarp();
-        if (lane == 0 && x0 < n_extent && y0 < m_extent) {  // boxes wholly outside D are skipped
-            tma_store_2d(mapD, x0, y0, stg_s);
+        if (lane == 0 && x0 + kCols * rd < n_extent && y0 < m_extent) {
+            tma_store_2d(mapD, x0 + kCols * rd, y0, stg_s);
             bulk_commit();
-        }
-    } else {
-#pragma unroll
-        for (int hx = 0; hx < 2; ++hx) {
-            bulk_wait_read();
-            __syncwarp();
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const float* q = v + 32 * hx + 4 * c;
-                *(float4*)(stg + r * 128 + ((c ^ (r & 7)) << 4)) =
-                    make_float4(q[0] * scale, q[1] * scale, q[2] * scale, q[3] * scale);
-            }
-            fence_async_smem();
-            __syncwarp();
-            if (lane == 0 && x0 + 32 * hx < n_extent && y0 < m_extent) {
-                tma_store_2d(mapD, x0 + 32 * hx, y0, stg_s);
-                bulk_commit();
-            }
         }
     }
 }
@@ -537,11 +531,11 @@ fp8q_status launch_t(const CUtensorMap& ma, const CUtensorMap& mb, const CUtenso
 
 template <int REC>
 fp8q_status launch_rec(const CUtensorMap& ma, const CUtensorMap& mb, const Params& p, int out_dtype, cudaStream_t s) {
-    // D [M][N] row-major: 32-row boxes of 128 bytes (64 bf16 / 32 fp32) in the 128-byte swizzle
+    // D [M][N] row-major: 32-row boxes of 32 bytes (16 bf16 / 8 fp32) in the 32-byte swizzle
     CUtensorMap md;
     const bool f32 = out_dtype == 1;
     if (!make_map_2d(&md, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, f32 ? 4 : 2, p.D,
-                     p.M, p.N, f32 ? 32 : 64, 32, CU_TENSOR_MAP_SWIZZLE_128B))
+                     p.M, p.N, f32 ? 8 : 16, 32, CU_TENSOR_MAP_SWIZZLE_32B))
         return FP8Q_ERR_CUDA;
     return f32 ? launch_t<REC, true>(ma, mb, md, p, s) : launch_t<REC, false>(ma, mb, md, p, s);
 }
