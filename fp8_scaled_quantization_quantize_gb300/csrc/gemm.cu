@@ -27,6 +27,7 @@
 
 #include "fp8q_internal.cuh"
 #include "ptx.cuh"
+#include "umma.cuh"
 
 namespace fp8q {
 
@@ -74,25 +75,16 @@ struct Params {
 
 // ------------------------------------------------------------ PTX wrappers
 
+// The phase is usually complete already: test it inline (no call, so no
+// register save / restore around it) and only fall back to the bounded loop.
 __device__ __forceinline__ bool mbar_wait(uint32_t a, uint32_t parity, volatile int* abort_flag) {
+    if (mbar_try(a, parity)) return true;
     return mbar_wait_bounded(a, parity, abort_flag, &g_device_errors, 1u, kWaitNs);
 }
 
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_commit(uint32_t mbar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(mbar) : "memory");
 }
-
-// Shared-memory matrix descriptor: start >> 4, leading byte offset >> 4,
-// stride byte offset >> 4, fixed 0b001 at bit 46, swizzle mode at bit 61.
-__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo, uint32_t swz) {
-    return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
-           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | ((uint64_t)swz << 61);
-}
-// K-major operand tile, rows of 128 bytes in the 128-byte swizzle: 8-row
-// groups 1024 bytes apart.
-__device__ __forceinline__ uint64_t desc_sw128(uint32_t addr) { return smem_desc(addr, 16, 1024, 2); }
 
 __device__ __forceinline__ void mma_f8(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
     asm volatile(
@@ -110,107 +102,6 @@ __device__ __forceinline__ void mma_mx(uint32_t d, uint64_t a, uint64_t b, uint3
 }
 __device__ __forceinline__ void tc_cp_32x128b(uint32_t taddr, uint64_t desc) {
     asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc));
-}
-
-#define FP8Q_LD32(addr, r)                                                                                          \
-    asm volatile(                                                                                                   \
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18," \
-        "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"                                              \
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),         \
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),    \
-          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),  \
-          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])   \
-        : "r"(addr))
-
-#define FP8Q_LD16(addr, r)                                                                                     \
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, " \
-                 "[%16];"                                                                                      \
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),          \
-                   "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),      \
-                   "=r"(r[14]), "=r"(r[15])                                                                     \
-                 : "r"(addr))
-
-// Registers written by tcgen05.ld are valid only after tcgen05.wait::ld; this
-// empty asm, placed after the wait, keeps the compiler from hoisting their
-// uses above it.
-__device__ __forceinline__ void reg_fence16(uint32_t* r) {
-    asm volatile("" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
-                 "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
-                 "+r"(r[14]), "+r"(r[15]));
-}
-__device__ __forceinline__ void reg_fence32(uint32_t* r) {
-    reg_fence16(r);
-    reg_fence16(r + 16);
-}
-
-__device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-
-// Tile order: groups of 8 M-blocks, N-blocks outer inside a group, so the
-// CTAs working at one time share A and B panels in L2.
-__device__ __forceinline__ void tile_coords(int64_t t, int64_t tiles_m, int64_t tiles_n, int64_t& mb, int64_t& nb) {
-    const int64_t G = 8;
-    const int64_t group = t / (G * tiles_n);
-    const int64_t first = group * G;
-    const int64_t gs = (tiles_m - first) < G ? (tiles_m - first) : G;
-    const int64_t in = t - group * G * tiles_n;
-    mb = first + in % gs;
-    nb = in / gs;
-}
-
-__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
-    uint32_t r;
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));
-    return r;
-}
-
-__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int x, int y, uint32_t src) {
-    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(map), "r"(x),
-                 "r"(y), "r"(src)
-                 : "memory");
-}
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-
-// Stores this warp's 32 rows x 64 columns of D (v: the lane's row, scaled by
-// `scale`) through its 1 KB shared-memory staging box and TMA stores, in
-// rounds of 32-byte row pieces (16 bf16 / 8 fp32) in the 32-byte swizzle
-// (16-byte chunk c of row r at r*32 + (c ^ ((r / 4) % 2))*16, so the lanes'
-// writes do not conflict).  The TMA clips rows / columns outside D; boxes
-// wholly outside D are skipped.
-template <bool OUT_F32>
-__device__ __forceinline__ void store_slice(const CUtensorMap* mapD, uint8_t* stg, uint32_t stg_s, int lane, int x0,
-                                            int y0, int n_extent, int m_extent, const float* v, float scale) {
-    const int r = lane;
-    constexpr int kCols = OUT_F32 ? 8 : 16;  // columns per 32-byte piece
-#pragma unroll
-    for (int rd = 0; rd < 64 / kCols; ++rd) {
-        bulk_wait_read();  // the previous box has been read out of stg
-        __syncwarp();
-        const float* q = v + kCols * rd;
-        uint4 c0, c1;
-        if (!OUT_F32) {
-            c0 = make_uint4(pack_bf16(q[0] * scale, q[1] * scale), pack_bf16(q[2] * scale, q[3] * scale),
-                            pack_bf16(q[4] * scale, q[5] * scale), pack_bf16(q[6] * scale, q[7] * scale));
-            c1 = make_uint4(pack_bf16(q[8] * scale, q[9] * scale), pack_bf16(q[10] * scale, q[11] * scale),
-                            pack_bf16(q[12] * scale, q[13] * scale), pack_bf16(q[14] * scale, q[15] * scale));
-        } else {
-            c0 = make_uint4(__float_as_uint(q[0] * scale), __float_as_uint(q[1] * scale), __float_as_uint(q[2] * scale),
-                            __float_as_uint(q[3] * scale));
-            c1 = make_uint4(__float_as_uint(q[4] * scale), __float_as_uint(q[5] * scale), __float_as_uint(q[6] * scale),
-                            __float_as_uint(q[7] * scale));
-        }
-        const int sw = (r >> 2) & 1;
-        *(uint4*)(stg + r * 32 + ((0 ^ sw) << 4)) = c0;
-        *(uint4*)(stg + r * 32 + ((1 ^ sw) << 4)) = c1;
-        fence_async_smem();
-        __syncwarp();
-        if (lane == 0 && x0 + kCols * rd < n_extent && y0 < m_extent) {
-            tma_store_2d(mapD, x0 + kCols * rd, y0, stg_s);
-            bulk_commit();
-        }
-    }
 }
 
 template <int REC, bool OUT_F32>
@@ -380,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t* stg = smem + OFF_STG + ew * STG_WARP;
         const uint32_t stg_s = sb + OFF_STG + ew * STG_WARP;
         uint32_t tile_i = 0;
-        uint64_t kbg = 0;
+        uint32_t kbg = 0;
         for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++tile_i) {
             int64_t mb, nb;
             tile_coords(t, p.tiles_m, p.tiles_n, mb, nb);
@@ -411,33 +302,27 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int i = 0; i < kEpiCols; ++i) acc[i] = 0.0f;
                 const bool cvalid = (col0 < p.N);
-                // scales for the next two K blocks are loaded ahead of use
+                // the next K block's scales are loaded one iteration ahead (32-bit offsets:
+                // the host checks that the scale arrays index below 2^31)
                 const int nkb = (int)p.nkb;
-                const int64_t nblk = (nb * BN + kEpiCols * j) / 128;
-                const bool bvalid = nblk < p.nbn128;
-                const float* pa = p.bsa + row;                               // [kb][Mp]
-                const float* pb = p.bsb + (bvalid ? nblk * p.nkb : 0);       // 128x128: [nblk][kb]
-                const float* pv = p.bsb + (cvalid ? col0 : 0) + 2 * lane;    // 1x128: [kb][Np]
-                const int64_t Mp = p.Mp, Np = p.Np;
-                auto load_sa = [&](int kb) { return kb < nkb ? __ldg(pa + kb * Mp) : 0.0f; };
-                auto load_sb = [&](int kb) { return (REC == REC_B2D && bvalid && kb < nkb) ? __ldg(pb + kb) : 0.0f; };
-                auto load_sbv = [&](int kb) {
-                    float2 v = make_float2(0.f, 0.f);
-                    if (REC == REC_B1D && cvalid && kb < nkb) v = __ldg((const float2*)(pv + kb * Np));
-                    return v;
-                };
-                float sa0 = load_sa(0), sa1 = load_sa(1), sb0 = load_sb(0), sb1 = load_sb(1);
-                float2 sv0 = load_sbv(0), sv1 = load_sbv(1);
+                const int nblk = (int)((nb * BN + kEpiCols * j) / 128);
+                const bool bvalid = nblk < (int)p.nbn128;
+                const int Mp = (int)p.Mp, Np = (int)p.Np;
+                const float* pa = p.bsa + (int)row;                                   // [kb][Mp]
+                const float* pb = p.bsb + (bvalid ? nblk * nkb : 0);                  // 128x128: [nblk][kb]
+                const float* pv = p.bsb + (cvalid ? (int)col0 : 0) + 2 * lane;        // 1x128: [kb][Np]
+                float sa_n = __ldg(pa), sb_n = (REC == REC_B2D && bvalid) ? __ldg(pb) : 0.0f;
+                float2 sv_n = make_float2(0.f, 0.f);
+                if (REC == REC_B1D && cvalid) sv_n = __ldg((const float2*)pv);
                 bool ok = true;
                 for (int kb = 0; kb < nkb; ++kb, ++kbg) {
-                    const float sa = sa0, sbk = sb0;
-                    const float2 sv = sv0;
-                    sa0 = sa1;
-                    sb0 = sb1;
-                    sv0 = sv1;
-                    sa1 = load_sa(kb + 2);
-                    sb1 = load_sb(kb + 2);
-                    sv1 = load_sbv(kb + 2);
+                    const float sa = sa_n, sbk = sb_n;
+                    const float2 sv = sv_n;
+                    if (kb + 1 < nkb) {
+                        sa_n = __ldg(pa + (kb + 1) * Mp);
+                        if (REC == REC_B2D && bvalid) sb_n = __ldg(pb + kb + 1);
+                        if (REC == REC_B1D && cvalid) sv_n = __ldg((const float2*)(pv + (kb + 1) * Np));
+                    }
                     if (REC == REC_B1D) {
                         __syncwarp();
                         *(float2*)(sbw + 2 * lane) = sv;  // B scales of this warp's 64 columns
@@ -567,6 +452,8 @@ fp8q_status launch_gemm(const GemmOperand& A, const GemmOperand& B, void* D, int
     p.nkb = (K + BK - 1) / BK;
     p.D = D;
     p.Mp = p.tiles_m * BM;
+    if (p.Mp * p.nkb >= ((int64_t)1 << 31) || ((N + 127) / 128 * 128) * p.nkb >= ((int64_t)1 << 31))
+        return FP8Q_ERR_SHAPE;  // the blockwise epilogue indexes its scales with 32-bit offsets
     p.Np = (N + 127) / 128 * 128;
     p.nbn128 = (N + 127) / 128;
     const bool pt = A.kind == FP8Q_PERTENSOR_CURRENT || A.kind == FP8Q_PERTENSOR_DELAYED;
