@@ -477,7 +477,12 @@ def main():
     ap.add_argument("--K", type=int, default=8192)
     ap.add_argument("--out", choices=["bf16", "fp32"], default="bf16")
     ap.add_argument("--no-flush", action="store_true")
+    ap.add_argument("--gemm-variant", type=int, choices=[0, 1, 2], default=0,
+                    help="GEMM kernel: 0 automatic, 1 one SM per 128-row tile, 2 SM pairs (256-row tiles)")
     args = ap.parse_args()
+    if args.impl == "ours" and args.gemm_variant:
+        from fp8_scaled_quantization_quantize_gb300 import api as _api
+        _api.gemm_set_variant(args.gemm_variant)
     if args.mode != "step" and args.impl == "ours":
         run_modes(args)
         return

@@ -151,6 +151,11 @@ def scaled_gemm(A: QTensor, a_use_col: bool, B: QTensor, b_use_col: bool, out_dt
     return out
 
 
+def gemm_set_variant(variant: int):
+    """0 automatic, 1 one SM per tile, 2 SM pairs (see fp8q_gemm_set_variant)."""
+    L.check(L.load().fp8q_gemm_set_variant(int(variant)), "fp8q_gemm_set_variant")
+
+
 def cast_f32_bits(start: int, count: int, fmt: int, out: torch.Tensor, stream=None) -> torch.Tensor:
     L.check(L.load().fp8q_cast_f32_bits(start, count, fmt, _ptr(out), _stream(stream)), "fp8q_cast_f32_bits")
     return out

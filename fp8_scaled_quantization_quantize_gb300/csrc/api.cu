@@ -258,9 +258,17 @@ fp8q_status fp8q_scaled_gemm(const fp8q_tensor* A, int a_use_col, const fp8q_ten
     return launch_gemm(ga, gb, D, out_dtype, M, N, K, (cudaStream_t)stream);
 }
 
+fp8q_status fp8q_gemm_set_variant(int variant) {
+    if (variant < 0 || variant > 2) return FP8Q_ERR_ARG;
+    g_gemm_variant = variant;
+    return FP8Q_OK;
+}
+
 fp8q_status fp8q_device_errors(unsigned int* flags, void* stream) {
     if (!flags) return FP8Q_ERR_ARG;
     fp8q_status st = read_device_errors(flags, (cudaStream_t)stream);
+    if (st != FP8Q_OK) return st;
+    st = read_device_errors2(flags);
     if (st != FP8Q_OK) return st;
     return read_quant_errors(flags);
 }

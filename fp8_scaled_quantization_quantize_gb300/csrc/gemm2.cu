@@ -1,0 +1,561 @@
+// Scaled FP8 GEMM on SM pairs: tcgen05.mma.cta_group::2 (M = 256).
+//
+// Same arithmetic as gemm.cu ("2025 FP8 quantized-training guide", sec. 2.1-2.3
+// and 3.1): D = A_q . B_q^T with per-tensor, MXFP8 (block-scaled MMA) or
+// blockwise (per-128-K partials scaled in the epilogue) scales.  A cluster of
+// two CTAs on two SMs computes a 256 x BN tile: CTA r loads rows
+// 256 mp + 128 r of A and rows BN nb + (BN / 2) r of B, and the leader CTA
+// (r = 0) issues each MMA for both, so every SM streams half of the B panel
+// it would need alone and each shared-memory stage is a third smaller.
+//
+// Per CTA, 576 threads: warp 0 TMA producer (its halves, completing on the
+// leader's barriers), warp 1 TMEM allocation (with the peer) and, in the
+// leader, the single-thread MMA issuer; warps 2-17 the epilogue of the CTA's
+// own 128 rows (TMEM lanes 32 (w % 4) .., columns BN / 4 ((w - 2) / 4) ..),
+// which releases TMEM on the leader's barrier and stores D by TMA.
+// TMEM per CTA: per-tensor two 256-column accumulators; MXFP8 one accumulator
+// plus 12 scale columns per stage; blockwise (BN = 128) four 128-column
+// partial buffers, so the MMAs run up to three K blocks ahead of the epilogue.
+// All mbarrier waits are bounded as in gemm.cu; both CTAs always reach the
+// closing cluster barrier, so neither exits while its shared memory or TMEM
+// can still be used by the pair.
+#include <string.h>
+
+#include "fp8q_internal.cuh"
+#include "ptx.cuh"
+#include "umma.cuh"
+
+namespace fp8q {
+
+__device__ unsigned int g_device_errors2 = 0;
+
+namespace {
+
+constexpr int BM = 128, BK = 128;
+constexpr int kEpiWarps = 16;
+constexpr int kThreads = 64 + 32 * kEpiWarps;
+constexpr uint64_t kWaitNs = 1000000000ull;
+enum { REC_PT = 0, REC_MX = 1, REC_B2D = 2, REC_B1D = 3 };
+
+template <int REC>
+struct Cfg {
+    static constexpr int BN = (REC == REC_B2D || REC == REC_B1D) ? 128 : 256;  // pair tile columns
+    static constexpr int BH = BN / 2;                                           // B rows per CTA
+    static constexpr int STAGES = (BN == 256) ? 4 : 6;
+    static constexpr int NACC = (REC == REC_PT) ? 2 : (REC == REC_MX ? 1 : 4);  // TMEM buffers
+    static constexpr int EPI_COLS = BN / 4;
+    static constexpr uint32_t A_STAGE = BM * BK, B_STAGE = BH * BK;
+    static constexpr uint32_t OFF_A = 0;
+    static constexpr uint32_t OFF_B = OFF_A + STAGES * A_STAGE;
+    static constexpr uint32_t OFF_SFA = OFF_B + STAGES * B_STAGE;
+    static constexpr uint32_t OFF_SFB = OFF_SFA + (REC == REC_MX ? STAGES * 512 : 0);
+    static constexpr uint32_t OFF_SBW = OFF_SFB + (REC == REC_MX ? STAGES * 1024 : 0);
+    static constexpr uint32_t OFF_STG = (OFF_SBW + kEpiWarps * EPI_COLS * 4 + 1023) / 1024 * 1024;
+    static constexpr uint32_t STG_WARP = 4096;  // four 1 KB output boxes per epilogue warp
+    static constexpr uint32_t OFF_BAR = OFF_STG + kEpiWarps * STG_WARP;
+    static constexpr uint32_t NBARS = 2 * STAGES + 2 * NACC + 1;
+    static constexpr uint32_t OFF_MISC = OFF_BAR + 8 * NBARS;
+    static constexpr uint32_t SMEM = OFF_MISC + 16 + 1024;
+    static_assert(SMEM <= 232448, "shared memory budget of one CTA");
+};
+
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t SF_TMEM_COL = 256;
+
+struct Params2 {
+    int64_t M, N, K;
+    int64_t tiles_m2, tiles_n, nkb, tiles_m128, nbn128;
+    const float* sa_inv;
+    const float* sb_inv;
+    const float* bsa;
+    const float* bsb;
+    int64_t Mp, Np;
+    uint32_t idesc;
+};
+
+// ------------------------------------------------------------ PTX wrappers
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Address of the same shared variable in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+__device__ __forceinline__ bool mbar_wait2(uint32_t a, uint32_t parity, volatile int* abort_flag) {
+    if (mbar_try(a, parity)) return true;
+    return mbar_wait_bounded(a, parity, abort_flag, &g_device_errors2, 1u, kWaitNs);
+}
+// TMA load into this CTA's shared memory (its shared::cta address, which is
+// also its shared::cluster address) completing on an mbarrier given by a
+// shared::cluster address, here always the leader CTA's.
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t mbar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2 [%0], [%1, "
+        "{%2, %3}], [%4];" ::"r"(dst),
+        "l"(map), "r"(x), "r"(y), "r"(mbar)
+        : "memory");
+}
+__device__ __forceinline__ void tc2_commit_both(uint32_t mbar) {
+    const uint16_t mask = 3;
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            mbar),
+        "h"(mask)
+        : "memory");
+}
+__device__ __forceinline__ void tc2_commit_local(uint32_t mbar) {
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(mbar) : "memory");
+}
+__device__ __forceinline__ void mma2_f8(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc));
+}
+__device__ __forceinline__ void mma2_mx(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
+                                        uint32_t sfb, uint32_t acc) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
+        " tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n}\n" ::"r"(
+            d),
+        "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc));
+}
+__device__ __forceinline__ void tc2_cp_32x128b(uint32_t taddr, uint64_t desc) {
+    asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc));
+}
+
+// Stores this warp's 32 rows x COLS columns through its 4 KB staging area in
+// 1 KB boxes of 32-byte row pieces (32-byte swizzle: chunk c of row r at
+// r*32 + (c ^ ((r / 4) % 2))*16); waits for the staging to be read out only
+// when more than four boxes are needed.
+template <bool OUT_F32, int COLS>
+__device__ __forceinline__ void store_slice2(const CUtensorMap* mapD, uint8_t* stg, uint32_t stg_s, int lane, int x0,
+                                             int y0, int n_extent, int m_extent, const float* v, float scale) {
+    constexpr int kPiece = OUT_F32 ? 8 : 16;  // columns per 32-byte row piece
+    constexpr int kBoxes = COLS / kPiece;
+    const int r = lane, sw = (r >> 2) & 1;
+    bulk_wait_read();  // the previous tile's boxes have left the staging area
+    __syncwarp();
+#pragma unroll
+    for (int bx = 0; bx < kBoxes; ++bx) {
+        if (bx > 0 && (bx & 3) == 0) {
+            bulk_wait_read();
+            __syncwarp();
+        }
+        uint8_t* box = stg + (bx & 3) * 1024;
+        const float* q = v + kPiece * bx;
+        uint4 c0, c1;
+        if (!OUT_F32) {
+            c0 = make_uint4(pack_bf16(q[0] * scale, q[1] * scale), pack_bf16(q[2] * scale, q[3] * scale),
+                            pack_bf16(q[4] * scale, q[5] * scale), pack_bf16(q[6] * scale, q[7] * scale));
+            c1 = make_uint4(pack_bf16(q[8] * scale, q[9] * scale), pack_bf16(q[10] * scale, q[11] * scale),
+                            pack_bf16(q[12] * scale, q[13] * scale), pack_bf16(q[14] * scale, q[15] * scale));
+        } else {
+            c0 = make_uint4(__float_as_uint(q[0] * scale), __float_as_uint(q[1] * scale), __float_as_uint(q[2] * scale),
+                            __float_as_uint(q[3] * scale));
+            c1 = make_uint4(__float_as_uint(q[4] * scale), __float_as_uint(q[5] * scale), __float_as_uint(q[6] * scale),
+                            __float_as_uint(q[7] * scale));
+        }
+        *(uint4*)(box + r * 32 + ((0 ^ sw) << 4)) = c0;
+        *(uint4*)(box + r * 32 + ((1 ^ sw) << 4)) = c1;
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0 && x0 + kPiece * bx < n_extent && y0 < m_extent) {
+            tma_store_2d(mapD, x0 + kPiece * bx, y0, stg_s + (bx & 3) * 1024);
+            bulk_commit();
+        }
+    }
+}
+
+template <int REC, bool OUT_F32>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                 const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmSFA,
+                 const __grid_constant__ CUtensorMap tmSFB, const Params2 p) {
+    using C = Cfg<REC>;
+    constexpr int BN = C::BN, BH = C::BH, STAGES = C::STAGES, NACC = C::NACC, EC = C::EPI_COLS;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    const uint32_t sb = smem_u32(smem);
+    auto full = [&](int s) { return sb + C::OFF_BAR + 8u * s; };
+    auto empty = [&](int s) { return sb + C::OFF_BAR + 8u * (STAGES + s); };
+    auto tfull = [&](int b) { return sb + C::OFF_BAR + 8u * (2 * STAGES + b); };
+    auto tempty = [&](int b) { return sb + C::OFF_BAR + 8u * (2 * STAGES + NACC + b); };
+    const uint32_t mma_done = sb + C::OFF_BAR + 8u * (2 * STAGES + 2 * NACC);
+    uint32_t* tmem_slot = (uint32_t*)(smem + C::OFF_MISC);
+    volatile int* abort_flag = (volatile int*)(smem + C::OFF_MISC + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t cr = cluster_rank();
+    const bool leader = cr == 0;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full(s), 1);
+            mbar_init(empty(s), 1);
+        }
+        for (int b = 0; b < NACC; ++b) {
+            mbar_init(tfull(b), 1);
+            mbar_init(tempty(b), 2 * kEpiWarps);
+        }
+        mbar_init(mma_done, 1);
+        *abort_flag = 0;
+        mbar_fence_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_map(&tmA);
+        prefetch_map(&tmB);
+    }
+    if (warp == 1) {  // collective with the peer CTA's warp 1
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    __syncwarp();
+    cluster_sync();  // both CTAs' barriers exist before any remote arrive / complete_tx
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const int64_t npt = p.tiles_m2 * p.tiles_n;
+    const int64_t cid = blockIdx.x >> 1, ncl = gridDim.x >> 1;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer (both CTAs)
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            bool ok = true;
+            for (int64_t t = cid; t < npt && ok; t += ncl) {
+                int64_t mp, nb;
+                tile_coords(t, p.tiles_m2, p.tiles_n, mp, nb);
+                const bool b2 = (2 * nb + 1) < p.nbn128;  // MX: second 128-row scale tile of B exists
+                for (int64_t kb = 0; kb < p.nkb; ++kb) {
+                    if (!mbar_wait2(empty(s), ph ^ 1u, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fl = mapa(full(s), 0);
+                    if (leader) {
+                        uint32_t bytes = 2 * (C::A_STAGE + C::B_STAGE);
+                        if (REC == REC_MX) bytes += 2 * (512 + (b2 ? 1024u : 512u));
+                        mbar_expect_tx(full(s), bytes);
+                    }
+                    tma_load_2d_pair(sb + C::OFF_A + s * C::A_STAGE, &tmA, (int)(kb * BK), (int)(mp * 256 + BM * cr), fl);
+                    tma_load_2d_pair(sb + C::OFF_B + s * C::B_STAGE, &tmB, (int)(kb * BK), (int)(nb * BN + BH * cr), fl);
+                    if (REC == REC_MX) {
+                        tma_load_2d_pair(sb + C::OFF_SFA + s * 512, &tmSFA, 0, (int)((2 * mp + cr) * p.nkb + kb), fl);
+                        tma_load_2d_pair(sb + C::OFF_SFB + s * 1024, &tmSFB, 0, (int)((2 * nb) * p.nkb + kb), fl);
+                        if (b2)
+                            tma_load_2d_pair(sb + C::OFF_SFB + s * 1024 + 512, &tmSFB, 0,
+                                             (int)((2 * nb + 1) * p.nkb + kb), fl);
+                    }
+                    if (++s == STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer (leader only)
+        if (leader && lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            uint32_t tile_i = 0, kbg = 0;
+            bool ok = true;
+            for (int64_t t = cid; t < npt && ok; t += ncl, ++tile_i) {
+                const uint32_t abuf = tile_i % NACC;
+                if (REC == REC_PT || REC == REC_MX) {
+                    if (!mbar_wait2(tempty(abuf), ((tile_i / NACC) & 1u) ^ 1u, abort_flag)) break;
+                    tc_fence_after();
+                }
+                for (int64_t kb = 0; kb < p.nkb; ++kb) {
+                    uint32_t dcol = (REC == REC_PT) ? abuf * BN : 0;
+                    if (REC == REC_B2D || REC == REC_B1D) {
+                        const uint32_t buf = kbg % NACC;
+                        if (!mbar_wait2(tempty(buf), ((kbg / NACC) & 1u) ^ 1u, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        dcol = buf * BN;
+                    }
+                    if (!mbar_wait2(full(s), ph, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a0 = sb + C::OFF_A + s * C::A_STAGE, b0 = sb + C::OFF_B + s * C::B_STAGE;
+                    if (REC == REC_MX) {
+                        const uint32_t sft = tmem + SF_TMEM_COL + 12u * s;
+                        tc2_cp_32x128b(sft, smem_desc(sb + C::OFF_SFA + s * 512, 0, 128, 0));
+                        tc2_cp_32x128b(sft + 4, smem_desc(sb + C::OFF_SFB + s * 1024, 0, 128, 0));
+                        tc2_cp_32x128b(sft + 8, smem_desc(sb + C::OFF_SFB + s * 1024 + 512, 0, 128, 0));
+#pragma unroll
+                        for (int k = 0; k < BK / 32; ++k) {
+                            const uint32_t idesc = p.idesc | ((uint32_t)k << 4) | ((uint32_t)k << 29);
+                            mma2_mx(tmem, desc_sw128(a0 + 32 * k), desc_sw128(b0 + 32 * k), idesc, sft, sft + 4,
+                                    (kb > 0 || k > 0) ? 1u : 0u);
+                        }
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < BK / 32; ++k) {
+                            const uint32_t acc = (REC == REC_PT) ? ((kb > 0 || k > 0) ? 1u : 0u) : (k > 0 ? 1u : 0u);
+                            mma2_f8(tmem + dcol, desc_sw128(a0 + 32 * k), desc_sw128(b0 + 32 * k), p.idesc, acc);
+                        }
+                    }
+                    tc2_commit_both(empty(s));
+                    if (REC == REC_B2D || REC == REC_B1D) {
+                        tc2_commit_both(tfull(kbg % NACC));
+                        ++kbg;
+                    }
+                    if (++s == STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                if (REC == REC_PT || REC == REC_MX) tc2_commit_both(tfull(abuf));
+            }
+            tc2_commit_local(mma_done);
+            mbar_drain(mma_done, 0, kWaitNs);
+        }
+    } else {
+        // ------------------------------------------------ epilogue (both CTAs, own 128 rows)
+        const int ew = warp - 2, q = warp & 3, j = ew >> 2;
+        const uint32_t lane_base = (uint32_t)(32 * q) << 16;
+        const uint32_t tcol = (uint32_t)(EC * j);
+        float sab = 1.0f;
+        if (REC == REC_PT) sab = __fmul_rn(*p.sa_inv, *p.sb_inv);
+        float* sbw = (float*)(smem + C::OFF_SBW) + ew * EC;
+        uint8_t* stg = smem + C::OFF_STG + ew * C::STG_WARP;
+        const uint32_t stg_s = sb + C::OFF_STG + ew * C::STG_WARP;
+        auto release = [&](int b) {  // this warp is done with TMEM buffer b: tell the leader's MMA issuer
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_remote(mapa(tempty(b), 0));
+        };
+        uint32_t tile_i = 0, kbg = 0;
+        for (int64_t t = cid; t < npt; t += ncl, ++tile_i) {
+            int64_t mp, nb;
+            tile_coords(t, p.tiles_m2, p.tiles_n, mp, nb);
+            const int64_t row0 = mp * 256 + BM * cr + 32 * q;  // this warp's first row
+            const int64_t col0 = nb * BN + EC * j;
+            if (REC == REC_PT || REC == REC_MX) {
+                const uint32_t abuf = tile_i % NACC;
+                if (!mbar_wait2(tfull(abuf), (tile_i / NACC) & 1u, abort_flag)) break;
+                tc_fence_after();
+                uint32_t r[64];
+                FP8Q_LD32(tmem + lane_base + abuf * BN + tcol, r);
+                FP8Q_LD32(tmem + lane_base + abuf * BN + tcol + 32, (r + 32));
+                tc_wait_ld();
+                reg_fence32(r);
+                reg_fence32(r + 32);
+                release(abuf);
+                float vf[64];
+#pragma unroll
+                for (int i = 0; i < 64; ++i) vf[i] = __uint_as_float(r[i]);
+                store_slice2<OUT_F32, EC>(&tmD, stg, stg_s, lane, (int)col0, (int)row0, (int)p.N, (int)p.M, vf, sab);
+            } else {
+                float acc[EC];
+#pragma unroll
+                for (int i = 0; i < EC; ++i) acc[i] = 0.0f;
+                const int64_t row = row0 + lane;
+                const bool cvalid = col0 < p.N;
+                const int nkb = (int)p.nkb;
+                const int nblk = (int)(col0 / 128);
+                const bool bvalid = nblk < (int)p.nbn128;
+                const int Mp = (int)p.Mp, Np = (int)p.Np;
+                // rows past the last 128-row block (the pair tile's second half
+                // beyond M) read the last row's scales; their outputs are not stored
+                const float* pa = p.bsa + (row < Mp ? (int)row : Mp - 1);         // [kb][Mp]
+                const float* pb = p.bsb + (bvalid ? nblk * nkb : 0);              // 128x128: [nblk][kb]
+                const float* pv = p.bsb + (cvalid ? (int)col0 : 0) + lane;        // 1x128: [kb][Np]
+                float sa_n = __ldg(pa), sb_n = (REC == REC_B2D && bvalid) ? __ldg(pb) : 0.0f;
+                float sv_n = (REC == REC_B1D && cvalid) ? __ldg(pv) : 0.0f;
+                bool ok = true;
+                for (int kb = 0; kb < nkb; ++kb, ++kbg) {
+                    const float sa = sa_n, sbk = sb_n, sv = sv_n;
+                    if (kb + 1 < nkb) {
+                        sa_n = __ldg(pa + (kb + 1) * Mp);
+                        if (REC == REC_B2D && bvalid) sb_n = __ldg(pb + kb + 1);
+                        if (REC == REC_B1D && cvalid) sv_n = __ldg(pv + (kb + 1) * Np);
+                    }
+                    if (REC == REC_B1D) {
+                        __syncwarp();
+                        sbw[lane] = sv;  // B scales of this warp's 32 columns
+                        __syncwarp();
+                    }
+                    const float sc = __fmul_rn(sa, sbk);
+                    const uint32_t buf = kbg % NACC;
+                    if (!mbar_wait2(tfull(buf), (kbg / NACC) & 1u, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    uint32_t r[32];
+                    FP8Q_LD32(tmem + lane_base + buf * BN + tcol, r);
+                    tc_wait_ld();
+                    reg_fence32(r);
+                    release(buf);
+                    if (REC == REC_B2D) {
+#pragma unroll
+                        for (int i = 0; i < EC; ++i) acc[i] = fmaf(__uint_as_float(r[i]), sc, acc[i]);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < EC; i += 4) {
+                            const float4 s4 = *(const float4*)(sbw + i);
+                            acc[i] = fmaf(__uint_as_float(r[i]), __fmul_rn(sa, s4.x), acc[i]);
+                            acc[i + 1] = fmaf(__uint_as_float(r[i + 1]), __fmul_rn(sa, s4.y), acc[i + 1]);
+                            acc[i + 2] = fmaf(__uint_as_float(r[i + 2]), __fmul_rn(sa, s4.z), acc[i + 2]);
+                            acc[i + 3] = fmaf(__uint_as_float(r[i + 3]), __fmul_rn(sa, s4.w), acc[i + 3]);
+                        }
+                    }
+                }
+                if (!ok) break;
+                store_slice2<OUT_F32, EC>(&tmD, stg, stg_s, lane, (int)col0, (int)row0, (int)p.N, (int)p.M, acc, 1.0f);
+            }
+        }
+        if (lane == 0) bulk_wait_all();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    __syncwarp();
+    cluster_sync();  // the pair's MMAs, copies and remote arrivals are over
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
+    }
+}
+
+int g_sms2 = 0;
+
+template <int REC, bool F32>
+fp8q_status launch2_t(const CUtensorMap* maps, const Params2& p, cudaStream_t s) {
+    using C = Cfg<REC>;
+    auto kern = gemm2_kernel<REC, F32>;
+    static bool attr = false;
+    if (!attr) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
+            return FP8Q_ERR_CUDA;
+        attr = true;
+    }
+    if (g_sms2 == 0) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&g_sms2, cudaDevAttrMultiProcessorCount, dev);
+        if (g_sms2 < 2) g_sms2 = 2;
+    }
+    const int64_t npt = p.tiles_m2 * p.tiles_n;
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof(cfg));
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = s;
+    cudaLaunchAttribute la[1];
+    la[0].id = cudaLaunchAttributeClusterDimension;
+    la[0].val.clusterDim.x = 2;
+    la[0].val.clusterDim.y = 1;
+    la[0].val.clusterDim.z = 1;
+    cfg.attrs = la;
+    cfg.numAttrs = 1;
+    // as many persistent pairs as can be resident at once (SM pairs must sit
+    // in one GPC, so this can be below half the SM count)
+    static int max_clusters = 0;
+    if (max_clusters == 0) {
+        cfg.gridDim = dim3((unsigned)g_sms2, 1, 1);
+        if (cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg) != cudaSuccess || max_clusters < 1)
+            max_clusters = g_sms2 / 2;
+    }
+    const int64_t ncl = npt < max_clusters ? npt : max_clusters;
+    cfg.gridDim = dim3((unsigned)(2 * ncl), 1, 1);
+    if (cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], maps[4], p) != cudaSuccess)
+        return FP8Q_ERR_CUDA;
+    return cudaGetLastError() == cudaSuccess ? FP8Q_OK : FP8Q_ERR_CUDA;
+}
+
+template <int REC>
+fp8q_status launch2_rec(CUtensorMap* maps, const Params2& p, void* D, int out_dtype, cudaStream_t s) {
+    const bool f32 = out_dtype == 1;
+    if (!make_map_2d(&maps[2], f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, f32 ? 4 : 2,
+                     D, p.M, p.N, f32 ? 8 : 16, 32, CU_TENSOR_MAP_SWIZZLE_32B))
+        return FP8Q_ERR_CUDA;
+    return f32 ? launch2_t<REC, true>(maps, p, s) : launch2_t<REC, false>(maps, p, s);
+}
+
+}  // namespace
+
+fp8q_status read_device_errors2(unsigned int* flags) {
+    unsigned int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_device_errors2, sizeof(v)) != cudaSuccess) return FP8Q_ERR_CUDA;
+    const unsigned int zero = 0;
+    if (cudaMemcpyToSymbol(g_device_errors2, &zero, sizeof(zero)) != cudaSuccess) return FP8Q_ERR_CUDA;
+    *flags |= v;
+    return FP8Q_OK;
+}
+
+fp8q_status launch_gemm_pair(const GemmOperand& A, const GemmOperand& B, void* D, int out_dtype, int64_t M,
+                             int64_t N, int64_t K, cudaStream_t s) {
+    if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return FP8Q_ERR_SHAPE;
+    const bool mx = A.kind == FP8Q_MXFP8_1x32;
+    const bool pt = A.kind == FP8Q_PERTENSOR_CURRENT || A.kind == FP8Q_PERTENSOR_DELAYED;
+    const int bn = (mx || pt) ? 256 : 128;
+    CUtensorMap maps[5];
+    memset(maps, 0, sizeof(maps));
+    Params2 p;
+    memset(&p, 0, sizeof(p));
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.tiles_m2 = (M + 255) / 256;
+    p.tiles_n = (N + bn - 1) / bn;
+    p.nkb = (K + BK - 1) / BK;
+    p.tiles_m128 = (M + 127) / 128;
+    p.nbn128 = (N + 127) / 128;
+    p.Mp = p.tiles_m128 * 128;
+    p.Np = p.nbn128 * 128;
+    if (p.Mp * p.nkb >= ((int64_t)1 << 31) || p.Np * p.nkb >= ((int64_t)1 << 31)) return FP8Q_ERR_SHAPE;
+    if (!make_map_2d(&maps[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A.data, M, K, 128, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map_2d(&maps[1], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B.data, N, K, 128, bn / 2, CU_TENSOR_MAP_SWIZZLE_128B))
+        return FP8Q_ERR_CUDA;
+    const uint32_t shape = ((uint32_t)(bn >> 3) << 17) | ((uint32_t)(256 >> 4) << 24);
+    const uint32_t fmts = ((uint32_t)A.fmt << 7) | ((uint32_t)B.fmt << 10);
+    if (mx) {
+        // scale tiles as rows of 128 uint32 (512 bytes): [row tiles x K-block groups][128]
+        if (!make_map_2d(&maps[3], CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, A.scale, p.tiles_m128 * p.nkb, 128, 128, 1,
+                         CU_TENSOR_MAP_SWIZZLE_NONE) ||
+            !make_map_2d(&maps[4], CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, B.scale, p.nbn128 * p.nkb, 128, 128, 1,
+                         CU_TENSOR_MAP_SWIZZLE_NONE))
+            return FP8Q_ERR_CUDA;
+        p.idesc = shape | fmts | (1u << 23);
+        return launch2_rec<REC_MX>(maps, p, D, out_dtype, s);
+    }
+    maps[3] = maps[0];
+    maps[4] = maps[1];
+    p.idesc = shape | fmts | (1u << 4);
+    if (pt) {
+        p.sa_inv = A.scale_inv;
+        p.sb_inv = B.scale_inv;
+        return launch2_rec<REC_PT>(maps, p, D, out_dtype, s);
+    }
+    p.bsa = (const float*)A.scale;
+    p.bsb = (const float*)B.scale;
+    if (B.kind == FP8Q_BLOCK_128x128) return launch2_rec<REC_B2D>(maps, p, D, out_dtype, s);
+    return launch2_rec<REC_B1D>(maps, p, D, out_dtype, s);
+}
+
+}  // namespace fp8q

@@ -226,6 +226,17 @@ FP8Q_API fp8q_status fp8q_scaled_gemm(const fp8q_tensor* A, int a_use_col, const
                              void* D, int out_dtype, int64_t M, int64_t N, int64_t K, void* stream);
 
 /*
+ * Chooses the GEMM kernel for subsequent fp8q_scaled_gemm calls (process
+ * wide): 0 automatic (default: SM pairs for the per-tensor and MXFP8 recipes
+ * once the problem has at least 64 tiles of 256 x 256, else one SM per
+ * tile), 1 always one SM per 128-row tile
+ * (tcgen05.mma.cta_group::1, M = 128), 2 always SM pairs
+ * (tcgen05.mma.cta_group::2, M = 256, launched as clusters of two CTAs).
+ * Both compute the same D up to fp32 summation order.  Host only.
+ */
+FP8Q_API fp8q_status fp8q_gemm_set_variant(int variant);
+
+/*
  * Reads and clears the library's device error words on the current device
  * (bit 0: a GEMM pipeline wait timed out, bit 1: a quantize tile-load wait
  * timed out).  Synchronises `stream`.

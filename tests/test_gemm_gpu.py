@@ -88,10 +88,19 @@ RECIPES = [
 ]
 
 
+@pytest.fixture(params=[1, 2], ids=["sm1", "sm2"])
+def variant(request):
+    """Runs the test on the one-SM (M = 128) and the SM-pair (M = 256) kernel."""
+    api = _api()
+    api.gemm_set_variant(request.param)
+    yield request.param
+    api.gemm_set_variant(0)
+
+
 @pytest.mark.parametrize("name,kx,kw,kd,fx,fw,fd", RECIPES, ids=[r[0] for r in RECIPES])
 @pytest.mark.parametrize("T,H,F", [(256, 256, 512), (208, 272, 400), (384, 640, 528)])
 @pytest.mark.parametrize("out", [torch.bfloat16, torch.float32])
-def test_fprop_dgrad_wgrad(name, kx, kw, kd, fx, fw, fd, T, H, F, out):
+def test_fprop_dgrad_wgrad(name, kx, kw, kd, fx, fw, fd, T, H, F, out, variant):
     api = _api()
     X, W, dY = _layer(T, H, F, 40 + T)
     qx = api.quantize(X.cuda(), kx, fx, True, True)
@@ -105,7 +114,7 @@ def test_fprop_dgrad_wgrad(name, kx, kw, kd, fx, fw, fd, T, H, F, out):
         _check(api, qd, True, qx, True, out, ctx=f"{name} wgrad")    # dW = dY^T . X
 
 
-def test_gemm_k_sweep_and_ragged_k():
+def test_gemm_k_sweep_and_ragged_k(variant):
     api = _api()
     for K in (16, 48, 128, 144, 1040):
         a = inputs.normal_bf16((130, K), K)
@@ -119,7 +128,7 @@ def test_gemm_k_sweep_and_ragged_k():
         _check(api, qa, False, qb, False, ctx=f"K={K} block")
 
 
-def test_gemm_outlier_columns_blockwise():
+def test_gemm_outlier_columns_blockwise(variant):
     """1% outlier input channels x100 (the blockwise workload's activation)."""
     api = _api()
     x = inputs.to_bf16(inputs.with_outlier_columns(inputs.normal_f32((512, 1024), 3), 0.01, 100.0, 2))
@@ -148,7 +157,7 @@ def test_full_config_pertensor_256():
     _check(api, qa, False, qb, False, ctx="cfg1 full")
 
 
-def test_full_config_blockwise_llama8b_up_proj():
+def test_full_config_blockwise_llama8b_up_proj(variant):
     api = _api()
     X, W = inputs.llama8b_up_proj()
     qx = api.quantize(X.cuda(), 2, O.E4M3, True, False)
@@ -156,7 +165,7 @@ def test_full_config_blockwise_llama8b_up_proj():
     _check(api, qx, False, qw, False, sample=_edge_sample(14), ctx="cfg2 fprop (16 rows + 16 cols)")
 
 
-def test_full_config_mxfp8_llama8b_mlp():
+def test_full_config_mxfp8_llama8b_mlp(variant):
     api = _api()
     X, W, dY = inputs.llama8b_mlp()
     qx = api.quantize(X.cuda(), 4, O.E4M3, True, True)
