@@ -442,11 +442,13 @@ int g_gemm_variant = 0;
 fp8q_status launch_gemm(const GemmOperand& A, const GemmOperand& B, void* D, int out_dtype, int64_t M, int64_t N,
                         int64_t K, cudaStream_t s) {
     if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return FP8Q_ERR_SHAPE;
-    // SM pairs for per-tensor and MXFP8 once there are enough 256 x 256 tiles
-    // to occupy the GPU's SMs in pairs; blockwise stays on one SM per tile
-    const bool pt_or_mx = A.kind != FP8Q_BLOCK_1x128;
+    // SM pairs once there are enough 256 x 256 tiles to occupy the GPU's SMs
+    // in pairs (and, for blockwise scales, which the pair kernel fetches with
+    // bulk copies, 16-byte aligned scale arrays)
+    const bool scales_aligned =
+        A.kind != FP8Q_BLOCK_1x128 || ((((uintptr_t)A.scale) | ((uintptr_t)B.scale)) & 15) == 0;
     const int64_t pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
-    if (g_gemm_variant == 2 || (g_gemm_variant == 0 && pt_or_mx && pair_tiles >= 64))
+    if (g_gemm_variant == 2 || (g_gemm_variant == 0 && scales_aligned && pair_tiles >= 64))
         return launch_gemm_pair(A, B, D, out_dtype, M, N, K, s);
     CUtensorMap ma, mb;
     if (!make_map(&ma, A.data, M, K, BM) || !make_map(&mb, B.data, N, K, BN)) return FP8Q_ERR_CUDA;

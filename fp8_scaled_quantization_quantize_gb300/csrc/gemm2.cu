@@ -39,21 +39,27 @@ enum { REC_PT = 0, REC_MX = 1, REC_B2D = 2, REC_B1D = 3 };
 
 template <int REC>
 struct Cfg {
-    static constexpr int BN = (REC == REC_B2D || REC == REC_B1D) ? 128 : 256;  // pair tile columns
-    static constexpr int BH = BN / 2;                                           // B rows per CTA
-    static constexpr int STAGES = (BN == 256) ? 4 : 6;
-    static constexpr int NACC = (REC == REC_PT) ? 2 : (REC == REC_MX ? 1 : 4);  // TMEM buffers
+    static constexpr bool BLOCKWISE = REC == REC_B2D || REC == REC_B1D;
+    static constexpr int BN = 256;     // pair tile columns
+    static constexpr int BH = BN / 2;  // B rows per CTA
+    static constexpr int STAGES = BLOCKWISE ? 4 : 5;
+    static constexpr int NACC = (REC == REC_MX) ? 1 : 2;  // TMEM accumulators (blockwise: K-block partials)
     static constexpr int EPI_COLS = BN / 4;
+    // blockwise scales ring: per K block, this CTA's 128 A-row scales (512 B)
+    // and the tile's B scales (two floats for 128x128 blocks, 256 for 1x128);
+    // deep enough that the producer is never held back by the epilogue
+    static constexpr int SR = BLOCKWISE ? STAGES + NACC + 2 : 0;
+    static constexpr uint32_t SLOT = 512 + 4 * BN;
     static constexpr uint32_t A_STAGE = BM * BK, B_STAGE = BH * BK;
     static constexpr uint32_t OFF_A = 0;
     static constexpr uint32_t OFF_B = OFF_A + STAGES * A_STAGE;
     static constexpr uint32_t OFF_SFA = OFF_B + STAGES * B_STAGE;
     static constexpr uint32_t OFF_SFB = OFF_SFA + (REC == REC_MX ? STAGES * 512 : 0);
-    static constexpr uint32_t OFF_SBW = OFF_SFB + (REC == REC_MX ? STAGES * 1024 : 0);
-    static constexpr uint32_t OFF_STG = (OFF_SBW + kEpiWarps * EPI_COLS * 4 + 1023) / 1024 * 1024;
-    static constexpr uint32_t STG_WARP = 4096;  // four 1 KB output boxes per epilogue warp
+    static constexpr uint32_t OFF_SCL = OFF_SFB + (REC == REC_MX ? STAGES * 1024 : 0);
+    static constexpr uint32_t OFF_STG = OFF_SCL + SR * SLOT;
+    static constexpr uint32_t STG_WARP = BLOCKWISE ? 4096 : 2048;  // 1 KB output boxes per epilogue warp
     static constexpr uint32_t OFF_BAR = OFF_STG + kEpiWarps * STG_WARP;
-    static constexpr uint32_t NBARS = 2 * STAGES + 2 * NACC + 1;
+    static constexpr uint32_t NBARS = 2 * STAGES + 2 * NACC + 1 + 2 * SR;
     static constexpr uint32_t OFF_MISC = OFF_BAR + 8 * NBARS;
     static constexpr uint32_t SMEM = OFF_MISC + 16 + 1024;
     static_assert(SMEM <= 232448, "shared memory budget of one CTA");
@@ -89,8 +95,11 @@ __device__ __forceinline__ uint32_t mapa(uint32_t addr, uint32_t rank) {
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
     return r;
 }
+// Arrive on an mbarrier of a CTA of the cluster (default semantics: release
+// at CTA scope; a cluster-scope release costs about a microsecond per arrive).
+// The TMEM reads this signal covers have completed (tcgen05.wait::ld) before it.
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 __device__ __forceinline__ bool mbar_wait2(uint32_t a, uint32_t parity, volatile int* abort_flag) {
     if (mbar_try(a, parity)) return true;
@@ -105,6 +114,15 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
         "{%2, %3}], [%4];" ::"r"(dst),
         "l"(map), "r"(x), "r"(y), "r"(mbar)
         : "memory");
+}
+// 4-byte asynchronous copy whose completion is reported to an mbarrier by
+// cp_async_arrive (which does not raise the barrier's pending count: the
+// barrier's initial count includes it).
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_arrive(uint32_t mbar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(mbar) : "memory");
 }
 __device__ __forceinline__ void tc2_commit_both(uint32_t mbar) {
     const uint16_t mask = 3;
@@ -135,11 +153,11 @@ __device__ __forceinline__ void tc2_cp_32x128b(uint32_t taddr, uint64_t desc) {
     asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc));
 }
 
-// Stores this warp's 32 rows x COLS columns through its 4 KB staging area in
+// Stores this warp's 32 rows x COLS columns through its staging area of NBOX
 // 1 KB boxes of 32-byte row pieces (32-byte swizzle: chunk c of row r at
-// r*32 + (c ^ ((r / 4) % 2))*16); waits for the staging to be read out only
-// when more than four boxes are needed.
-template <bool OUT_F32, int COLS>
+// r*32 + (c ^ ((r / 4) % 2))*16); waits for the staging to be read out each
+// time all NBOX boxes are in flight.
+template <bool OUT_F32, int COLS, int NBOX>
 __device__ __forceinline__ void store_slice2(const CUtensorMap* mapD, uint8_t* stg, uint32_t stg_s, int lane, int x0,
                                              int y0, int n_extent, int m_extent, const float* v, float scale) {
     constexpr int kPiece = OUT_F32 ? 8 : 16;  // columns per 32-byte row piece
@@ -149,11 +167,11 @@ __device__ __forceinline__ void store_slice2(const CUtensorMap* mapD, uint8_t* s
     __syncwarp();
 #pragma unroll
     for (int bx = 0; bx < kBoxes; ++bx) {
-        if (bx > 0 && (bx & 3) == 0) {
+        if (bx > 0 && bx % NBOX == 0) {
             bulk_wait_read();
             __syncwarp();
         }
-        uint8_t* box = stg + (bx & 3) * 1024;
+        uint8_t* box = stg + (bx % NBOX) * 1024;
         const float* q = v + kPiece * bx;
         uint4 c0, c1;
         if (!OUT_F32) {
@@ -172,7 +190,7 @@ __device__ __forceinline__ void store_slice2(const CUtensorMap* mapD, uint8_t* s
         fence_async_smem();
         __syncwarp();
         if (lane == 0 && x0 + kPiece * bx < n_extent && y0 < m_extent) {
-            tma_store_2d(mapD, x0 + kPiece * bx, y0, stg_s + (bx & 3) * 1024);
+            tma_store_2d(mapD, x0 + kPiece * bx, y0, stg_s + (bx % NBOX) * 1024);
             bulk_commit();
         }
     }
@@ -193,6 +211,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto tfull = [&](int b) { return sb + C::OFF_BAR + 8u * (2 * STAGES + b); };
     auto tempty = [&](int b) { return sb + C::OFF_BAR + 8u * (2 * STAGES + NACC + b); };
     const uint32_t mma_done = sb + C::OFF_BAR + 8u * (2 * STAGES + 2 * NACC);
+    auto sfull = [&](int r) { return sb + C::OFF_BAR + 8u * (2 * STAGES + 2 * NACC + 1 + r); };
+    auto sempty = [&](int r) { return sb + C::OFF_BAR + 8u * (2 * STAGES + 2 * NACC + 1 + C::SR + r); };
     uint32_t* tmem_slot = (uint32_t*)(smem + C::OFF_MISC);
     volatile int* abort_flag = (volatile int*)(smem + C::OFF_MISC + 4);
 
@@ -209,6 +229,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(tempty(b), 2 * kEpiWarps);
         }
         mbar_init(mma_done, 1);
+        for (int r = 0; r < C::SR; ++r) {
+            mbar_init(sfull(r), REC == REC_B2D ? 2 : 1);
+            mbar_init(sempty(r), kEpiWarps);
+        }
         *abort_flag = 0;
         mbar_fence_init();
     }
@@ -235,12 +259,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------ TMA producer (both CTAs)
         if (lane == 0) {
             int s = 0;
-            uint32_t ph = 0;
+            uint32_t ph = 0, kbp = 0;
             bool ok = true;
             for (int64_t t = cid; t < npt && ok; t += ncl) {
                 int64_t mp, nb;
                 tile_coords(t, p.tiles_m2, p.tiles_n, mp, nb);
                 const bool b2 = (2 * nb + 1) < p.nbn128;  // MX: second 128-row scale tile of B exists
+                const int64_t rs = mp * 256 + BM * cr;    // this CTA's first row
+                const bool arow = rs < p.Mp;             // else all its rows are past M: no A scales
                 for (int64_t kb = 0; kb < p.nkb; ++kb) {
                     if (!mbar_wait2(empty(s), ph ^ 1u, abort_flag)) {
                         ok = false;
@@ -261,6 +287,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                             tma_load_2d_pair(sb + C::OFF_SFB + s * 1024 + 512, &tmSFB, 0,
                                              (int)((2 * nb + 1) * p.nkb + kb), fl);
                     }
+                    if constexpr (C::BLOCKWISE) {
+                        const uint32_t r = kbp % C::SR;
+                        if (!mbar_wait2(sempty(r), ((kbp / C::SR) & 1u) ^ 1u, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        const uint32_t dst = sb + C::OFF_SCL + r * C::SLOT;
+                        // 1x128 B scales of the tile's columns that exist (Np is a multiple of 128)
+                        const uint32_t bbytes = (p.Np - nb * BN >= BN) ? 4u * BN : 4u * (uint32_t)(p.Np - nb * BN);
+                        mbar_expect_tx(sfull(r), (arow ? 512u : 0u) + (REC == REC_B1D ? bbytes : 0u));
+                        if (arow) bulk_load(dst, p.bsa + kb * p.Mp + rs, 512, sfull(r));
+                        if (REC == REC_B1D) bulk_load(dst + 512, p.bsb + kb * p.Np + nb * BN, bbytes, sfull(r));
+                        if (REC == REC_B2D) {  // the scales of the tile's two 128-column B blocks
+                            cp_async_4(dst + 512, p.bsb + (2 * nb) * p.nkb + kb);
+                            if (2 * nb + 1 < p.nbn128) cp_async_4(dst + 516, p.bsb + (2 * nb + 1) * p.nkb + kb);
+                            cp_async_arrive(sfull(r));
+                        }
+                        ++kbp;
+                    }
                     if (++s == STAGES) {
                         s = 0;
                         ph ^= 1u;
@@ -275,6 +320,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t ph = 0;
             uint32_t tile_i = 0, kbg = 0;
             bool ok = true;
+            auto copy_sf = [&](int st) {
+                const uint32_t sft = tmem + SF_TMEM_COL + 12u * st;
+                tc2_cp_32x128b(sft, smem_desc(sb + C::OFF_SFA + st * 512, 0, 128, 0));
+                tc2_cp_32x128b(sft + 4, smem_desc(sb + C::OFF_SFB + st * 1024, 0, 128, 0));
+                tc2_cp_32x128b(sft + 8, smem_desc(sb + C::OFF_SFB + st * 1024 + 512, 0, 128, 0));
+            };
             for (int64_t t = cid; t < npt && ok; t += ncl, ++tile_i) {
                 const uint32_t abuf = tile_i % NACC;
                 if (REC == REC_PT || REC == REC_MX) {
@@ -297,12 +348,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     tc_fence_after();
+                    if (REC == REC_MX) copy_sf(s);
                     const uint32_t a0 = sb + C::OFF_A + s * C::A_STAGE, b0 = sb + C::OFF_B + s * C::B_STAGE;
                     if (REC == REC_MX) {
                         const uint32_t sft = tmem + SF_TMEM_COL + 12u * s;
-                        tc2_cp_32x128b(sft, smem_desc(sb + C::OFF_SFA + s * 512, 0, 128, 0));
-                        tc2_cp_32x128b(sft + 4, smem_desc(sb + C::OFF_SFB + s * 1024, 0, 128, 0));
-                        tc2_cp_32x128b(sft + 8, smem_desc(sb + C::OFF_SFB + s * 1024 + 512, 0, 128, 0));
 #pragma unroll
                         for (int k = 0; k < BK / 32; ++k) {
                             const uint32_t idesc = p.idesc | ((uint32_t)k << 4) | ((uint32_t)k << 29);
@@ -321,13 +370,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tc2_commit_both(tfull(kbg % NACC));
                         ++kbg;
                     }
+                    const bool last = kb + 1 == p.nkb;
+                    if ((REC == REC_PT || REC == REC_MX) && last) tc2_commit_both(tfull(abuf));
                     if (++s == STAGES) {
                         s = 0;
                         ph ^= 1u;
                     }
                 }
                 if (!ok) break;
-                if (REC == REC_PT || REC == REC_MX) tc2_commit_both(tfull(abuf));
             }
             tc2_commit_local(mma_done);
             mbar_drain(mma_done, 0, kWaitNs);
@@ -339,7 +389,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tcol = (uint32_t)(EC * j);
         float sab = 1.0f;
         if (REC == REC_PT) sab = __fmul_rn(*p.sa_inv, *p.sb_inv);
-        float* sbw = (float*)(smem + C::OFF_SBW) + ew * EC;
         uint8_t* stg = smem + C::OFF_STG + ew * C::STG_WARP;
         const uint32_t stg_s = sb + C::OFF_STG + ew * C::STG_WARP;
         auto release = [&](int b) {  // this warp is done with TMEM buffer b: tell the leader's MMA issuer
@@ -353,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tile_coords(t, p.tiles_m2, p.tiles_n, mp, nb);
             const int64_t row0 = mp * 256 + BM * cr + 32 * q;  // this warp's first row
             const int64_t col0 = nb * BN + EC * j;
-            if (REC == REC_PT || REC == REC_MX) {
+            if constexpr (!C::BLOCKWISE) {
                 const uint32_t abuf = tile_i % NACC;
                 if (!mbar_wait2(tfull(abuf), (tile_i / NACC) & 1u, abort_flag)) break;
                 tc_fence_after();
@@ -367,65 +416,56 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float vf[64];
 #pragma unroll
                 for (int i = 0; i < 64; ++i) vf[i] = __uint_as_float(r[i]);
-                store_slice2<OUT_F32, EC>(&tmD, stg, stg_s, lane, (int)col0, (int)row0, (int)p.N, (int)p.M, vf, sab);
+                store_slice2<OUT_F32, EC, C::STG_WARP / 1024>(&tmD, stg, stg_s, lane, (int)col0, (int)row0, (int)p.N, (int)p.M, vf, sab);
             } else {
-                float acc[EC];
+                float2 acc[EC / 2];  // packed pairs: Blackwell's two-lane FMA halves the promotion's instructions
 #pragma unroll
-                for (int i = 0; i < EC; ++i) acc[i] = 0.0f;
-                const int64_t row = row0 + lane;
-                const bool cvalid = col0 < p.N;
-                const int nkb = (int)p.nkb;
-                const int nblk = (int)(col0 / 128);
-                const bool bvalid = nblk < (int)p.nbn128;
-                const int Mp = (int)p.Mp, Np = (int)p.Np;
-                // rows past the last 128-row block (the pair tile's second half
-                // beyond M) read the last row's scales; their outputs are not stored
-                const float* pa = p.bsa + (row < Mp ? (int)row : Mp - 1);         // [kb][Mp]
-                const float* pb = p.bsb + (bvalid ? nblk * nkb : 0);              // 128x128: [nblk][kb]
-                const float* pv = p.bsb + (cvalid ? (int)col0 : 0) + lane;        // 1x128: [kb][Np]
-                float sa_n = __ldg(pa), sb_n = (REC == REC_B2D && bvalid) ? __ldg(pb) : 0.0f;
-                float sv_n = (REC == REC_B1D && cvalid) ? __ldg(pv) : 0.0f;
+                for (int i = 0; i < EC / 2; ++i) acc[i] = make_float2(0.0f, 0.0f);
                 bool ok = true;
-                for (int kb = 0; kb < nkb; ++kb, ++kbg) {
-                    const float sa = sa_n, sbk = sb_n, sv = sv_n;
-                    if (kb + 1 < nkb) {
-                        sa_n = __ldg(pa + (kb + 1) * Mp);
-                        if (REC == REC_B2D && bvalid) sb_n = __ldg(pb + kb + 1);
-                        if (REC == REC_B1D && cvalid) sv_n = __ldg(pv + (kb + 1) * Np);
+                for (int64_t kb = 0; kb < p.nkb; ++kb, ++kbg) {
+                    const uint32_t r = kbg % C::SR;
+                    if (!mbar_wait2(sfull(r), (kbg / C::SR) & 1u, abort_flag)) {
+                        ok = false;
+                        break;
                     }
-                    if (REC == REC_B1D) {
-                        __syncwarp();
-                        sbw[lane] = sv;  // B scales of this warp's 32 columns
-                        __syncwarp();
-                    }
-                    const float sc = __fmul_rn(sa, sbk);
+                    const float* scl = (const float*)(smem + C::OFF_SCL + r * C::SLOT);
+                    const float sa = scl[32 * q + lane];
+                    const float sc = (REC == REC_B2D) ? __fmul_rn(sa, scl[128 + (EC * j) / 128]) : 0.0f;
                     const uint32_t buf = kbg % NACC;
                     if (!mbar_wait2(tfull(buf), (kbg / NACC) & 1u, abort_flag)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    uint32_t r[32];
-                    FP8Q_LD32(tmem + lane_base + buf * BN + tcol, r);
-                    tc_wait_ld();
-                    reg_fence32(r);
-                    release(buf);
-                    if (REC == REC_B2D) {
+                    // four 16-column chunks: partial -> registers -> promoted into acc
 #pragma unroll
-                        for (int i = 0; i < EC; ++i) acc[i] = fmaf(__uint_as_float(r[i]), sc, acc[i]);
-                    } else {
+                    for (int c = 0; c < EC / 16; ++c) {
+                        uint64_t v[8];
+                        FP8Q_LD16_PAIRS(tmem + lane_base + buf * BN + tcol + 16 * c, v);
+                        if (c == EC / 16 - 1) release(buf);
+                        if (REC == REC_B2D) {
+                            const float2 sc2 = make_float2(sc, sc);
 #pragma unroll
-                        for (int i = 0; i < EC; i += 4) {
-                            const float4 s4 = *(const float4*)(sbw + i);
-                            acc[i] = fmaf(__uint_as_float(r[i]), __fmul_rn(sa, s4.x), acc[i]);
-                            acc[i + 1] = fmaf(__uint_as_float(r[i + 1]), __fmul_rn(sa, s4.y), acc[i + 1]);
-                            acc[i + 2] = fmaf(__uint_as_float(r[i + 2]), __fmul_rn(sa, s4.z), acc[i + 2]);
-                            acc[i + 3] = fmaf(__uint_as_float(r[i + 3]), __fmul_rn(sa, s4.w), acc[i + 3]);
+                            for (int i = 0; i < 8; ++i) acc[8 * c + i] = __ffma2_rn(u64_as_float2(v[i]), sc2, acc[8 * c + i]);
+                        } else {
+                            const float2 sa2 = make_float2(sa, sa);
+                            const float* sv = scl + 128 + EC * j + 16 * c;  // B scales of these columns
+#pragma unroll
+                            for (int i = 0; i < 8; i += 2) {
+                                const float4 s4 = *(const float4*)(sv + 2 * i);
+                                const float2 p0 = __fmul2_rn(sa2, make_float2(s4.x, s4.y));
+                                const float2 p1 = __fmul2_rn(sa2, make_float2(s4.z, s4.w));
+                                acc[8 * c + i] = __ffma2_rn(u64_as_float2(v[i]), p0, acc[8 * c + i]);
+                                acc[8 * c + i + 1] = __ffma2_rn(u64_as_float2(v[i + 1]), p1, acc[8 * c + i + 1]);
+                            }
                         }
                     }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(sempty(r));
                 }
                 if (!ok) break;
-                store_slice2<OUT_F32, EC>(&tmD, stg, stg_s, lane, (int)col0, (int)row0, (int)p.N, (int)p.M, acc, 1.0f);
+                store_slice2<OUT_F32, EC, C::STG_WARP / 1024>(&tmD, stg, stg_s, lane, (int)col0, (int)row0, (int)p.N, (int)p.M,
+                                          reinterpret_cast<const float*>(acc), 1.0f);
             }
         }
         if (lane == 0) bulk_wait_all();
@@ -513,7 +553,10 @@ fp8q_status launch_gemm_pair(const GemmOperand& A, const GemmOperand& B, void* D
     if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return FP8Q_ERR_SHAPE;
     const bool mx = A.kind == FP8Q_MXFP8_1x32;
     const bool pt = A.kind == FP8Q_PERTENSOR_CURRENT || A.kind == FP8Q_PERTENSOR_DELAYED;
-    const int bn = (mx || pt) ? 256 : 128;
+    static_assert(Cfg<REC_MX>::BN == Cfg<REC_PT>::BN && Cfg<REC_B2D>::BN == Cfg<REC_PT>::BN &&
+                      Cfg<REC_B1D>::BN == Cfg<REC_PT>::BN,
+                  "one tile width for every recipe");
+    const int bn = Cfg<REC_PT>::BN;
     CUtensorMap maps[5];
     memset(maps, 0, sizeof(maps));
     Params2 p;
@@ -552,6 +595,8 @@ fp8q_status launch_gemm_pair(const GemmOperand& A, const GemmOperand& B, void* D
         p.sb_inv = B.scale_inv;
         return launch2_rec<REC_PT>(maps, p, D, out_dtype, s);
     }
+    // blockwise scale rows are fetched by bulk copies: 16-byte aligned bases
+    if (((uintptr_t)A.scale | (uintptr_t)B.scale) & 15) return FP8Q_ERR_ARG;
     p.bsa = (const float*)A.scale;
     p.bsb = (const float*)B.scale;
     if (B.kind == FP8Q_BLOCK_128x128) return launch2_rec<REC_B2D>(maps, p, D, out_dtype, s);

@@ -36,6 +36,19 @@ __device__ __forceinline__ bool mbar_try(uint32_t a, uint32_t parity) {
     return ok != 0;
 }
 
+// try_wait that may suspend the thread for up to `hint_ns` (it resumes as
+// soon as the phase completes), so waiting warps take no issue slots from
+// the warps doing work on the same scheduler.
+__device__ __forceinline__ bool mbar_try_suspend(uint32_t a, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(a), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Bounded wait on an mbarrier phase (limit_ns of %globaltimer).  Returns false
 // when the CTA's abort flag is raised or the limit passes; in the latter case
 // it raises the flag and ORs `bit` into *err.
@@ -44,7 +57,7 @@ __device__ __noinline__ inline bool mbar_wait_bounded(uint32_t a, uint32_t parit
     if (mbar_try(a, parity)) return true;
     const uint64_t t0 = gtimer();
     while (true) {
-        if (mbar_try(a, parity)) return true;
+        if (mbar_try_suspend(a, parity, 20000u)) return true;
         if (*abort_flag) return false;
         if (gtimer() - t0 > limit_ns) {
             atomicOr(err, bit);

@@ -41,6 +41,29 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t addr) { return smem_desc
                    "=r"(r[14]), "=r"(r[15])                                                                     \
                  : "r"(addr))
 
+// 16 columns of TMEM, waited for, as 8 column pairs in 64-bit registers (the
+// operands of the two-lane fp32 instructions): the load, its wait and the
+// packing in one asm block, so the pairs are formed from completed registers.
+#define FP8Q_LD16_PAIRS(addr, d)                                                                                \
+    asm volatile(                                                                                               \
+        "{\n .reg .b32 t<16>;\n"                                                                                \
+        " tcgen05.ld.sync.aligned.32x32b.x16.b32 {t0,t1,t2,t3,t4,t5,t6,t7,t8,t9,t10,t11,t12,t13,t14,t15}, [%8];\n" \
+        " tcgen05.wait::ld.sync.aligned;\n"                                                                      \
+        " mov.b64 %0, {t0,t1};\n mov.b64 %1, {t2,t3};\n mov.b64 %2, {t4,t5};\n mov.b64 %3, {t6,t7};\n"            \
+        " mov.b64 %4, {t8,t9};\n mov.b64 %5, {t10,t11};\n mov.b64 %6, {t12,t13};\n mov.b64 %7, {t14,t15};\n}\n"  \
+        : "=l"(d[0]), "=l"(d[1]), "=l"(d[2]), "=l"(d[3]), "=l"(d[4]), "=l"(d[5]), "=l"(d[6]), "=l"(d[7])          \
+        : "r"(addr)                                                                                             \
+        : "memory")
+
+__device__ __forceinline__ float2 u64_as_float2(uint64_t u) {
+    union {
+        uint64_t u;
+        float2 f;
+    } x;
+    x.u = u;
+    return x.f;
+}
+
 // Registers written by tcgen05.ld are valid only after tcgen05.wait::ld; this
 // empty asm, placed after the wait, keeps the compiler from hoisting their
 // uses above it.

@@ -227,12 +227,14 @@ FP8Q_API fp8q_status fp8q_scaled_gemm(const fp8q_tensor* A, int a_use_col, const
 
 /*
  * Chooses the GEMM kernel for subsequent fp8q_scaled_gemm calls (process
- * wide): 0 automatic (default: SM pairs for the per-tensor and MXFP8 recipes
- * once the problem has at least 64 tiles of 256 x 256, else one SM per
- * tile), 1 always one SM per 128-row tile
+ * wide): 0 automatic (default: SM pairs once the problem has at least 64
+ * tiles of 256 x 256 and, for blockwise scales, both scale arrays are
+ * 16-byte aligned; else one SM per tile), 1 always one SM per 128-row tile
  * (tcgen05.mma.cta_group::1, M = 128), 2 always SM pairs
- * (tcgen05.mma.cta_group::2, M = 256, launched as clusters of two CTAs).
- * Both compute the same D up to fp32 summation order.  Host only.
+ * (tcgen05.mma.cta_group::2, M = 256, launched as clusters of two CTAs;
+ * blockwise scale arrays must then be 16-byte aligned, else the GEMM returns
+ * FP8Q_ERR_ARG).  Both compute the same D up to fp32 summation order.  Host
+ * only.
  */
 FP8Q_API fp8q_status fp8q_gemm_set_variant(int variant);
 
@@ -254,11 +256,15 @@ FP8Q_API fp8q_status fp8q_cast_f32_bits(uint32_t start, uint64_t count, int fmt,
  * Self-test of the blockwise recipes' division.  The quantize kernels compute
  * x / d (d = amax / fmax, [guide] sec. 2.2) as q = RN(x * r) with r = RN(1/d),
  * then one FMA residual correction, which yields the correctly rounded
- * quotient for d in [2^-80, 2^128) (smaller d takes the IEEE division).  This
- * entry point compares that computation with the IEEE quotient for every
- * finite bf16 x and every d[j] (device fp32 [nd]) and writes the mismatch
- * counts to mismatches (device uint64[2]: [0] FP8 codes of format fmt, [1]
- * fp32 bits).  Both must be 0.
+ * quotient for d in [2^-80, 2^128) and quotients in [2^-24, 2^126) (smaller d
+ * takes the IEEE division; quantization's quotients never exceed
+ * fmax (1 + 2^-23); below 2^-24, where the residual of a tiny x can leave the
+ * normal range, every quotient encodes to an FP8 zero).  This entry point
+ * compares that computation with the IEEE quotient for every finite bf16 x
+ * and every d[j] (device fp32 [nd]) whose quotient is below 2^126 and writes
+ * the mismatch counts to mismatches (device uint64[2]: [0] FP8 codes of
+ * format fmt over all those pairs, [1] fp32 bits where the IEEE quotient is
+ * at least 2^-24).  Both must be 0.
  */
 FP8Q_API fp8q_status fp8q_selftest_division(const float* d, int64_t nd, int fmt, unsigned long long* mismatches,
                                             void* stream);

@@ -1,9 +1,14 @@
 """The blockwise recipes divide by d = amax / fmax ("2025 FP8 quantized-training
 guide", sec. 2.2) through a correctly rounded reciprocal plus one FMA residual
 correction.  This checks that shortcut against IEEE division over its whole
-reachable domain: every finite bf16 x against every d = RN(a / fmax) for every
-positive finite bf16 a (the only divisors a bf16 tensor can produce), both
-formats, plus random fp32 divisors."""
+reachable domain and beyond: every finite bf16 x against every d = RN(a / fmax)
+for every positive finite bf16 a (the only divisors a bf16 tensor can
+produce), both formats, plus random fp32 divisors, for every pair whose
+quotient is below 2^126 (quantization's quotients never exceed
+fmax (1 + 2^-23), since it divides |x| <= amax by RN(amax / fmax)).  FP8
+codes must agree for all of them, fp32 bits wherever the quotient is at
+least 2^-24 (below that, where the residual of a tiny x can leave fp32's
+normal range, every quotient encodes to an FP8 zero)."""
 import numpy as np
 import pytest
 import torch
