@@ -4,18 +4,23 @@
 //
 // One tile kernel serves every recipe.  A persistent CTA of 256 threads walks
 // 128x128 tiles of x; TMA loads each tile (two 64-column boxes in the 128-byte
-// swizzle) into a 3-stage shared-memory ring.  Row path: thread t owns row
-// t % 128 and the 64-column half t / 128, i.e. two whole 1x32 blocks or half
-// of a 1x128 block, so block maxima are packed u16x2 maxima inside the thread
-// and each scale is computed once per 32 or 64 elements.  Column path: thread
-// t reads rows 32 (t / 64) .. +31 of columns 2 (t % 64), +1 from the same
-// swizzled tile (conflict-free), reduces the 1x32 / 1x128 column blocks and
-// stores 32-byte runs of the transposed copy.  The 128-aligned tiles make every
-// scale-layout pad entry the scale of an all-zero block (code 127 / 1.0).
+// swizzle) into a 3-stage shared-memory ring, two tiles ahead.  Row path:
+// thread t owns row t % 128 and the 64-column half t / 128, i.e. two whole
+// 1x32 blocks or half of a 1x128 block, so block maxima are packed u16x2
+// maxima inside the thread and each scale is computed once per 32 or 64
+// elements.  Column path (1x128, MXFP8): thread t reads rows 32 (t / 64) .. +31
+// of columns 2 (t % 64), +1 from the same swizzled tile (conflict-free) and
+// reduces the 1x32 / 1x128 column blocks; for per-tensor and 128x128 scales
+// the column copy is the byte transpose of the row codes.  Once the bf16 tile
+// is consumed, its stage takes the two 128x128 code tiles, which TMA stores
+// write out; the stage is reloaded after those stores have read it.  The
+// 128-aligned tiles make every scale-layout pad entry the scale of an all-zero
+// block (code 127 / 1.0).
 #include <string.h>
 
 #include "fp8q_internal.cuh"
 #include "ptx.cuh"
+#include "umma.cuh"
 
 namespace fp8q {
 
@@ -166,6 +171,53 @@ __device__ __forceinline__ float apply(float x, const Factor& f) {
     }
 }
 
+// Two elements at a time with Blackwell's two-lane fp32 instructions (each
+// lane an independent round-to-nearest operation, bit-identical to the
+// scalar forms).  Factor2 holds the factors of the two lanes.
+struct Factor2 {
+    float2 k, r, nk;  // multiplier or divisor, its reciprocal, minus the divisor
+};
+__device__ __forceinline__ Factor2 pair_factor(const Factor& a, const Factor& b) {
+    Factor2 f;
+    f.k = make_float2(a.k, b.k);
+    f.r = make_float2(a.r, b.r);
+    f.nk = make_float2(-a.k, -b.k);
+    return f;
+}
+__device__ __forceinline__ float2 bf16x2_f32(uint32_t w) { return make_float2(bf16_lo(w), bf16_hi(w)); }
+__device__ __forceinline__ float with_sign_of(float q, float x) {
+    return __uint_as_float((__float_as_uint(q) & 0x7FFFFFFFu) | (__float_as_uint(x) & 0x80000000u));
+}
+// apply<KIND, true> on both lanes: the blockwise quotient by the reciprocal
+// and one residual correction (div_rn_recip), else the product.
+template <int KIND>
+__device__ __forceinline__ float2 apply2(float2 x, const Factor2& f) {
+    if constexpr (KIND == kB1 || KIND == kB128) {
+        const float2 q = __fmul2_rn(x, f.r);
+        const float2 e = __ffma2_rn(q, f.nk, x);  // x - q d, exact
+        const float2 q2 = __ffma2_rn(e, f.r, q);
+        return make_float2(with_sign_of(q2.x, x.x), with_sign_of(q2.y, x.y));
+    } else {
+        return __fmul2_rn(x, f.k);
+    }
+}
+template <int FMT>
+__device__ __forceinline__ uint32_t sat2(float2 y, bool cx, bool cy) {
+    return (uint32_t)(cx && fabsf(y.x) > Fmt<FMT>::fmax) + (uint32_t)(cy && fabsf(y.y) > Fmt<FMT>::fmax);
+}
+
+// The 8 finite bf16 of v (one row) with one factor in both lanes of f; counts
+// saturation only when the caller found that the vector's largest magnitude
+// can exceed fmax once scaled (the scaled value is monotone in |x|).
+template <int KIND, int FMT>
+__device__ __forceinline__ uint2 convert8_packed(const uint4& v, const Factor2& f, uint32_t& nsat, bool count) {
+    const float2 y0 = apply2<KIND>(bf16x2_f32(v.x), f), y1 = apply2<KIND>(bf16x2_f32(v.y), f);
+    const float2 y2 = apply2<KIND>(bf16x2_f32(v.z), f), y3 = apply2<KIND>(bf16x2_f32(v.w), f);
+    if (count) nsat += sat2<FMT>(y0, true, true) + sat2<FMT>(y1, true, true) + sat2<FMT>(y2, true, true) +
+                       sat2<FMT>(y3, true, true);
+    return make_uint2(cvt4<FMT>(y0.x, y0.y, y1.x, y1.y), cvt4<FMT>(y2.x, y2.y, y3.x, y3.y));
+}
+
 // Converts the 8 finite bf16 of v; counts saturation only when the caller
 // found that the vector's largest magnitude can exceed fmax once scaled
 // (the scaled value is monotone in |x|).
@@ -213,10 +265,29 @@ __device__ __forceinline__ uint32_t exact_max(const uint4 (&v)[8], uint32_t& nnf
     return m;
 }
 
+// Two FP8 codes (low byte: column c, high byte: column c + 1) of row r of a
+// 128x128 code tile in the 128-byte swizzle.
+__device__ __forceinline__ uint32_t code_pair(const uint8_t* tile, int r, int c) {
+    return *(const uint16_t*)(tile + swz(r, c >> 4) + (c & 15));
+}
+// From the code pairs of rows j .. j + 3 (h0 .. h3), the four codes of the
+// low column (x) and of the high column (y), row j in the lowest byte.
+__device__ __forceinline__ void transpose4(uint32_t h0, uint32_t h1, uint32_t h2, uint32_t h3, uint32_t& x,
+                                           uint32_t& y) {
+    const uint32_t a = __byte_perm(h0, h1, 0x5140), b = __byte_perm(h2, h3, 0x5140);  // x0 x1 y0 y1 / x2 x3 y2 y3
+    x = __byte_perm(a, b, 0x5410);
+    y = __byte_perm(a, b, 0x7632);
+}
+
 template <int KIND, int FMT, bool ROW, bool COL>
 __global__ void __launch_bounds__(kThreads, 2)
-    quant_tile_kernel(const __grid_constant__ CUtensorMap tmx, QuantArgs a) {
+    quant_tile_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmrow,
+                      const __grid_constant__ CUtensorMap tmcol, QuantArgs a) {
     constexpr bool kPerTensor = (KIND == kCur || KIND == kDel);
+    // the column copy of a recipe whose scale does not depend on the copy's
+    // direction is the byte transpose of the row codes
+    constexpr bool kTranspose = COL && (kPerTensor || KIND == kB128);
+    constexpr bool kRowCodes = ROW || kTranspose;
     extern __shared__ uint8_t qsmem_raw[];
     uint8_t* qsmem = (uint8_t*)(((uintptr_t)qsmem_raw + 1023) & ~(uintptr_t)1023);
     const uint32_t sbase = smem_u32(qsmem);
@@ -227,17 +298,17 @@ __global__ void __launch_bounds__(kThreads, 2)
     __shared__ int abort_flag;
 
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-    const int rr = t & (kTile - 1), hh = t >> 7;  // row-path: row and 64-column half of the tile
-    const int64_t ntiles = a.tiles_r * a.tiles_c;
+    const int rr = t & (kTile - 1), hh = t >> 7;  // row path: row and 64-column half of the tile
+    const uint32_t ntiles = (uint32_t)(a.tiles_r * a.tiles_c), tiles_c = (uint32_t)a.tiles_c;
     auto bar = [&](int s) { return smem_u32(&bars[s]); };
 
-    // stage s: the tile's two 64-column halves, each [128 rows][128 bytes] in the
-    // 128-byte swizzle, loaded by two TMA boxes
-    auto issue = [&](int64_t it) {
-        const int64_t tileid = blockIdx.x + it * (int64_t)gridDim.x;
+    // the CTA's j-th tile into stage j % kStages: two 64-column boxes, each
+    // [128 rows][128 bytes] in the 128-byte swizzle
+    auto issue = [&](uint32_t j) {
+        const uint32_t tileid = blockIdx.x + j * gridDim.x;
         if (tileid >= ntiles) return;
-        const int s = (int)(it % kStages);
-        const int64_t tr = tileid / a.tiles_c, tc = tileid % a.tiles_c;
+        const uint32_t s = j % kStages;
+        const uint32_t tr = tileid / tiles_c, tc = tileid - tr * tiles_c;
         mbar_expect_tx(bar(s), kStageBytes);
         tma_load_2d(sbase + s * kStageBytes, &tmx, (int)(tc * kTile), (int)(tr * kTile), bar(s));
         tma_load_2d(sbase + s * kStageBytes + kStageBytes / 2, &tmx, (int)(tc * kTile + 64), (int)(tr * kTile), bar(s));
@@ -246,11 +317,19 @@ __global__ void __launch_bounds__(kThreads, 2)
         for (int s = 0; s < kStages; ++s) mbar_init(bar(s), 1);
         abort_flag = 0;
         mbar_fence_init();
-        if (ntiles > 0) prefetch_map(&tmx);
+        if (ntiles > 0) {
+            prefetch_map(&tmx);
+            if (ROW) prefetch_map(&tmrow);
+            if (COL) prefetch_map(&tmcol);
+        }
     }
     __syncthreads();
-    if (t == 0)
-        for (int j = 0; j < kStages; ++j) issue(j);
+    // two tiles in flight; the third stage holds the previous tile's codes
+    // until its stores have read them
+    if (t == 0) {
+        issue(0);
+        issue(1);
+    }
 
     float ks = 1.0f;
     if constexpr (kPerTensor) {
@@ -262,15 +341,13 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
 
     uint32_t nsat_row = 0, nsat_col = 0, nnf = 0, tmax_all = 0;
-    int64_t it = 0;
-    for (int64_t tileid = blockIdx.x; tileid < ntiles; tileid += gridDim.x, ++it) {
-        const int64_t tr = tileid / a.tiles_c, tc = tileid % a.tiles_c;
-        const int64_t r0 = tr * kTile, c0 = tc * kTile;
-        const int stg = (int)(it % kStages);
-        const bool ok = mbar_wait_bounded(bar(stg), (uint32_t)((it / kStages) & 1), &abort_flag, &g_quant_errors,
-                                          2u, kQuantWaitNs);
+    uint32_t it = 0, stg = 0, ph = 0;
+    for (uint32_t tileid = blockIdx.x; tileid < ntiles; tileid += gridDim.x, ++it) {
+        const uint32_t tr = tileid / tiles_c, tc = tileid - tr * tiles_c;
+        const int64_t r0 = (int64_t)tr * kTile, c0 = (int64_t)tc * kTile;
+        const bool ok = mbar_wait_bounded(bar(stg), ph, &abort_flag, &g_quant_errors, 2u, kQuantWaitNs);
         if (__syncthreads_or(!ok)) break;  // the whole CTA leaves together
-        const uint8_t* stage = qsmem + stg * kStageBytes;
+        uint8_t* stage = qsmem + stg * kStageBytes;
 
         // ---------------- analysis: row rr, columns 64 hh .. 64 hh + 63 of the tile
         const uint8_t* half = stage + hh * (kStageBytes / 2);
@@ -307,10 +384,9 @@ __global__ void __launch_bounds__(kThreads, 2)
             uint32_t mm = 0;
 #pragma unroll
             for (int w = 0; w < kThreads / 32; ++w) mm = mm > red[w] ? mm : red[w];
-            __syncthreads();
             kq[0] = kq[1] = block_scale<FMT>(__uint_as_float(mm << 16));
             if (t == 0) {
-                if (ROW) ((float*)a.s_row)[tr * a.tiles_c + tc] = kq[0];
+                if (ROW) ((float*)a.s_row)[tileid] = kq[0];
                 if (COL) ((float*)a.s_col)[tc * a.tiles_r + tr] = kq[0];
             }
         } else if constexpr (KIND == kB1) {
@@ -326,47 +402,43 @@ __global__ void __launch_bounds__(kThreads, 2)
             kq[1] = exp2_neg(e1);
             if (ROW) {
                 // this row's scale columns 4 tc + 2 hh + {0, 1} in the 128x4 tile (tr, tc)
-                uint8_t* tileb = (uint8_t*)a.s_row + (tr * a.tiles_c + tc) * 512;
+                uint8_t* tileb = (uint8_t*)a.s_row + (size_t)tileid * 512;
                 *(uint16_t*)(tileb + (rr & 31) * 16 + (rr >> 5) * 4 + 2 * hh) =
                     (uint16_t)((uint32_t)(e0 + 127) | ((uint32_t)(e1 + 127) << 8));
             }
         }
 
-        // ---------------- row-wise copy
-        if constexpr (ROW) {
+        // ---------------- row-wise codes
+        uint2 q[8];
+        uint32_t nsat_rc = 0;
+        if constexpr (kRowCodes) {
             const Factor f0 = make_factor<KIND>(kq[0]);
             const Factor f1 = (KIND == kMX) ? make_factor<KIND>(kq[1]) : f0;
             const bool s0 = may_saturate<KIND, FMT>(mq[0], f0);
             const bool s1 = (KIND == kMX) ? may_saturate<KIND, FMT>(mq[1], f1) : s0;
-            uint2 q[8];
             if (vnf == 0 && f0.fast && f1.fast) {  // the common case: one straight-line block
+                const Factor2 g0 = pair_factor(f0, f0), g1 = pair_factor(f1, f1);
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
-                    q[j] = convert8_fast<KIND, FMT, true>(v[j], (j < 4) ? f0 : f1, nsat_row, (j < 4) ? s0 : s1);
+                    q[j] = convert8_packed<KIND, FMT>(v[j], (j < 4) ? g0 : g1, nsat_rc, (j < 4) ? s0 : s1);
             } else {
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     const Factor f = (j < 4) ? f0 : f1;
                     if ((vnf >> j) & 1u)
-                        q[j] = convert8<KIND, FMT>(v[j], f.k, nsat_row, true);
+                        q[j] = convert8<KIND, FMT>(v[j], f.k, nsat_rc, true);
                     else
-                        q[j] = convert8_fast<KIND, FMT, false>(v[j], f, nsat_row, (j < 4) ? s0 : s1);
+                        q[j] = convert8_fast<KIND, FMT, false>(v[j], f, nsat_rc, (j < 4) ? s0 : s1);
                 }
             }
-            const int64_t row = r0 + rr;
-            if (row < a.R) {
-                const int64_t col = c0 + 64 * hh;
-                uint8_t* dst = a.q_row + row * a.C + col;
-#pragma unroll
-                for (int j = 0; j < 8; j += 2)
-                    if (col + 8 * j < a.C) *(uint4*)(dst + 8 * j) = make_uint4(q[j].x, q[j].y, q[j + 1].x, q[j + 1].y);
-            }
+            if (ROW) nsat_row += nsat_rc;  // a transposed column copy reports no count of its own
         }
 
-        // ---------------- column-wise copy
-        if constexpr (COL) {
+        // ---------------- column-wise codes re-quantized along the columns (1x128, MXFP8)
+        const int p = t & 63, qd = t >> 6;  // column pair 2p, 2p + 1; rows 32 qd .. 32 qd + 31
+        uint32_t o0[8], o1[8];
+        if constexpr (COL && !kTranspose) {
             const bool tile_nf = __syncthreads_or(vnf != 0) != 0;
-            const int p = t & 63, qd = t >> 6;  // column pair, 32-row quarter
             // columns 2p, 2p+1 sit in half p / 32, chunk (2p % 64) / 8, bytes (2p % 8) * 2
             const uint8_t* chalf = stage + (p >> 5) * (kStageBytes / 2) + ((2 * p) & 7) * 2;
             const int chunk = ((2 * p) & 63) >> 3;
@@ -374,16 +446,13 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
             for (int j = 0; j < 32; ++j) w[j] = *(const uint32_t*)(chalf + swz(32 * qd + j, chunk));
             float k0, k1;
-            uint32_t cm0 = 0x7F7Fu, cm1 = 0x7F7Fu;  // column maxima (re-quantized kinds)
-            if constexpr (kPerTensor) {
-                k0 = k1 = ks;
-            } else if constexpr (KIND == kB128) {
-                k0 = k1 = kq[0];
-            } else {
+            uint32_t m0, m1;
+            {
                 uint32_t pm = 0;
 #pragma unroll
                 for (int j = 0; j < 32; ++j) pm = max_u16x2(pm, w[j] & 0x7FFF7FFFu);
-                uint32_t m0 = pm & 0xFFFFu, m1 = pm >> 16;
+                m0 = pm & 0xFFFFu;
+                m1 = pm >> 16;
                 if (m0 >= 0x7F80u || m1 >= 0x7F80u) {  // NaN / Inf: exact finite maxima
                     m0 = m1 = 0;
 #pragma unroll
@@ -393,15 +462,13 @@ __global__ void __launch_bounds__(kThreads, 2)
                         m1 = (hi < 0x7F80u && hi > m1) ? hi : m1;
                     }
                 }
-                cm0 = m0;
-                cm1 = m1;
                 const int64_t cc = c0 + 2 * p;
                 if constexpr (KIND == kMX) {
                     const int e0 = mx_exponent<FMT>(m0 << 16), e1 = mx_exponent<FMT>(m1 << 16);
                     k0 = exp2_neg(e0);
                     k1 = exp2_neg(e1);
                     // column-wise scales: logical [C][ceil(R/32)], tiles over (c/128, kb/4)
-                    uint8_t* tileb = (uint8_t*)a.s_col + (tc * a.tiles_r + tr) * 512;
+                    uint8_t* tileb = (uint8_t*)a.s_col + ((size_t)tc * a.tiles_r + tr) * 512;
                     const int cr = 2 * p;
                     tileb[(cr & 31) * 16 + (cr >> 5) * 4 + qd] = (uint8_t)(e0 + 127);
                     tileb[((cr + 1) & 31) * 16 + ((cr + 1) >> 5) * 4 + qd] = (uint8_t)(e1 + 127);
@@ -415,8 +482,6 @@ __global__ void __launch_bounds__(kThreads, 2)
                              max(colred[2 * kTile + 2 * p + 1], colred[3 * kTile + 2 * p + 1]));
                     k0 = block_scale<FMT>(__uint_as_float(m0 << 16));
                     k1 = block_scale<FMT>(__uint_as_float(m1 << 16));
-                    cm0 = m0;
-                    cm1 = m1;
                     if (qd == 0) {
                         const int64_t Cp = a.tiles_c * kTile;
                         float* sc = (float*)a.s_col + tr * Cp + cc;
@@ -426,24 +491,20 @@ __global__ void __launch_bounds__(kThreads, 2)
                 }
             }
             // convert 32 rows of columns 2p, 2p+1
-            uint32_t o0[8], o1[8];
             uint32_t ns = 0;
             const Factor f0 = make_factor<KIND>(k0), f1 = make_factor<KIND>(k1);
             if (!tile_nf && f0.fast && f1.fast) {
-                const bool req = (KIND == kB1 || KIND == kMX);
-                const bool c0s = req && may_saturate<KIND, FMT>(cm0, f0), c1s = req && may_saturate<KIND, FMT>(cm1, f1);
-                constexpr float fm = Fmt<FMT>::fmax;
+                const bool c0s = may_saturate<KIND, FMT>(m0, f0), c1s = may_saturate<KIND, FMT>(m1, f1);
+                const Factor2 g = pair_factor(f0, f1);  // lanes: column 2p, column 2p + 1
 #pragma unroll
                 for (int j = 0; j < 32; j += 4) {
-                    const float ya0 = apply<KIND, true>(bf16_lo(w[j]), f0), ya1 = apply<KIND, true>(bf16_lo(w[j + 1]), f0);
-                    const float ya2 = apply<KIND, true>(bf16_lo(w[j + 2]), f0), ya3 = apply<KIND, true>(bf16_lo(w[j + 3]), f0);
-                    const float yb0 = apply<KIND, true>(bf16_hi(w[j]), f1), yb1 = apply<KIND, true>(bf16_hi(w[j + 1]), f1);
-                    const float yb2 = apply<KIND, true>(bf16_hi(w[j + 2]), f1), yb3 = apply<KIND, true>(bf16_hi(w[j + 3]), f1);
-                    ns += (c0s && fabsf(ya0) > fm) + (c0s && fabsf(ya1) > fm) + (c0s && fabsf(ya2) > fm) +
-                          (c0s && fabsf(ya3) > fm) + (c1s && fabsf(yb0) > fm) + (c1s && fabsf(yb1) > fm) +
-                          (c1s && fabsf(yb2) > fm) + (c1s && fabsf(yb3) > fm);
-                    o0[j / 4] = cvt4<FMT>(ya0, ya1, ya2, ya3);
-                    o1[j / 4] = cvt4<FMT>(yb0, yb1, yb2, yb3);
+                    const float2 y0 = apply2<KIND>(bf16x2_f32(w[j]), g), y1 = apply2<KIND>(bf16x2_f32(w[j + 1]), g);
+                    const float2 y2 = apply2<KIND>(bf16x2_f32(w[j + 2]), g), y3 = apply2<KIND>(bf16x2_f32(w[j + 3]), g);
+                    if (c0s || c1s)
+                        ns += sat2<FMT>(y0, c0s, c1s) + sat2<FMT>(y1, c0s, c1s) + sat2<FMT>(y2, c0s, c1s) +
+                              sat2<FMT>(y3, c0s, c1s);
+                    o0[j / 4] = cvt4<FMT>(y0.x, y1.x, y2.x, y3.x);
+                    o1[j / 4] = cvt4<FMT>(y0.y, y1.y, y2.y, y3.y);
                 }
             } else {
 #pragma unroll
@@ -454,11 +515,9 @@ __global__ void __launch_bounds__(kThreads, 2)
                           ya3 = scaled<KIND>(a3, k0);
                     float yb0 = scaled<KIND>(b0, k1), yb1 = scaled<KIND>(b1, k1), yb2 = scaled<KIND>(b2, k1),
                           yb3 = scaled<KIND>(b3, k1);
-                    if constexpr (KIND == kB1 || KIND == kMX) {
-                        ns += sat_count<FMT>(a0, ya0) + sat_count<FMT>(a1, ya1) + sat_count<FMT>(a2, ya2) +
-                              sat_count<FMT>(a3, ya3) + sat_count<FMT>(b0, yb0) + sat_count<FMT>(b1, yb1) +
-                              sat_count<FMT>(b2, yb2) + sat_count<FMT>(b3, yb3);
-                    }
+                    ns += sat_count<FMT>(a0, ya0) + sat_count<FMT>(a1, ya1) + sat_count<FMT>(a2, ya2) +
+                          sat_count<FMT>(a3, ya3) + sat_count<FMT>(b0, yb0) + sat_count<FMT>(b1, yb1) +
+                          sat_count<FMT>(b2, yb2) + sat_count<FMT>(b3, yb3);
                     // rebuild the bf16 pairs of each output column to reuse nan_sign2
                     const uint32_t a01 = (w[j] & 0xFFFFu) | (w[j + 1] << 16), a23 = (w[j + 2] & 0xFFFFu) | (w[j + 3] << 16);
                     const uint32_t b01 = (w[j] >> 16) | (w[j + 1] & 0xFFFF0000u), b23 = (w[j + 2] >> 16) | (w[j + 3] & 0xFFFF0000u);
@@ -468,29 +527,54 @@ __global__ void __launch_bounds__(kThreads, 2)
                 }
             }
             nsat_col += ns;
-            const int64_t cc = c0 + 2 * p, rowc = r0 + 32 * qd;
-            if (rowc < a.R) {
-                const bool full = rowc + 32 <= a.R;  // R % 16 == 0: else exactly 16 rows remain
-                if (cc < a.C) {
-                    uint4* dst = (uint4*)(a.q_col + cc * a.R + rowc);
-                    dst[0] = make_uint4(o0[0], o0[1], o0[2], o0[3]);
-                    if (full) dst[1] = make_uint4(o0[4], o0[5], o0[6], o0[7]);
-                }
-                if (cc + 1 < a.C) {
-                    uint4* dst = (uint4*)(a.q_col + (cc + 1) * a.R + rowc);
-                    dst[0] = make_uint4(o1[0], o1[1], o1[2], o1[3]);
-                    if (full) dst[1] = make_uint4(o1[4], o1[5], o1[6], o1[7]);
-                }
+        }
+
+        // ---------------- codes into the stage (its bf16 tile is consumed), then TMA stores
+        __syncthreads();
+        uint8_t* rowt = stage;                  // [128 rows][128 codes], 128-byte swizzle
+        uint8_t* colt = stage + kTile * kTile;  // [128 columns][128 codes], 128-byte swizzle
+        if constexpr (kRowCodes) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                *(uint4*)(rowt + swz(rr, 4 * hh + c)) = make_uint4(q[2 * c].x, q[2 * c].y, q[2 * c + 1].x, q[2 * c + 1].y);
+        }
+        if constexpr (kTranspose) {
+            __syncthreads();
+#pragma unroll
+            for (int j = 0; j < 32; j += 4) {
+                const int r = 32 * qd + j;
+                transpose4(code_pair(rowt, r, 2 * p), code_pair(rowt, r + 1, 2 * p), code_pair(rowt, r + 2, 2 * p),
+                           code_pair(rowt, r + 3, 2 * p), o0[j / 4], o1[j / 4]);
             }
         }
-        __syncthreads();  // stage and colred are free again: refill the stage
-        if (t == 0) issue(it + kStages);
+        if constexpr (COL) {
+            *(uint4*)(colt + swz(2 * p, 2 * qd)) = make_uint4(o0[0], o0[1], o0[2], o0[3]);
+            *(uint4*)(colt + swz(2 * p, 2 * qd + 1)) = make_uint4(o0[4], o0[5], o0[6], o0[7]);
+            *(uint4*)(colt + swz(2 * p + 1, 2 * qd)) = make_uint4(o1[0], o1[1], o1[2], o1[3]);
+            *(uint4*)(colt + swz(2 * p + 1, 2 * qd + 1)) = make_uint4(o1[4], o1[5], o1[6], o1[7]);
+        }
+        fence_async_smem();
+        __syncthreads();
+        if (t == 0) {
+            if (ROW) tma_store_2d(&tmrow, (int)c0, (int)r0, smem_u32(rowt));
+            if (COL) tma_store_2d(&tmcol, (int)r0, (int)c0, smem_u32(colt));
+            bulk_commit();
+            bulk_wait_read1();  // the previous tile's stores have read their stage ...
+            issue(it + 2);      // ... which now takes the tile after next
+        }
+        if (++stg == kStages) {
+            stg = 0;
+            ph ^= 1u;
+        }
     }
-    if (abort_flag && t == 0) {
-        // let the tile loads already issued land before the CTA exits (bounded)
-        for (int64_t j = it; j < it + kStages; ++j)
-            if (blockIdx.x + j * (int64_t)gridDim.x < ntiles)
-                mbar_drain(bar((int)(j % kStages)), (uint32_t)((j / kStages) & 1), kQuantWaitNs / 10);
+    if (t == 0) {
+        bulk_wait_all();  // the codes' stores are complete before the CTA's shared memory goes away
+        if (abort_flag) {
+            // let the tile loads already issued land before the CTA exits (bounded)
+            for (uint32_t j = it; j < it + 2; ++j)
+                if (blockIdx.x + j * gridDim.x < ntiles)
+                    mbar_drain(bar((int)(j % kStages)), (j / kStages) & 1u, kQuantWaitNs / 10);
+        }
     }
 
     // ---------------- counters (and the delayed recipe's tensor amax)
@@ -633,15 +717,27 @@ fp8q_status launch_tile(const QuantArgs& a, cudaStream_t s) {
         attr = true;
     }
     const int64_t ntiles = a.tiles_r * a.tiles_c;
-    CUtensorMap tm;
+    if (ntiles >= ((int64_t)1 << 31)) return FP8Q_ERR_SHAPE;  // the kernel counts tiles in 32 bits
+    CUtensorMap tm, trow, tcol;
     memset(&tm, 0, sizeof(tm));
-    if (ntiles > 0 && !make_map_2d(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.x, a.R, a.C, kTile / 2, kTile,
-                                   CU_TENSOR_MAP_SWIZZLE_128B))
-        return FP8Q_ERR_CUDA;
+    memset(&trow, 0, sizeof(trow));
+    memset(&tcol, 0, sizeof(tcol));
+    if (ntiles > 0) {
+        if (!make_map_2d(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.x, a.R, a.C, kTile / 2, kTile,
+                         CU_TENSOR_MAP_SWIZZLE_128B))
+            return FP8Q_ERR_CUDA;
+        // code tiles [128][128] in the 128-byte swizzle: row copy [R][C], column copy [C][R]
+        if (ROW && !make_map_2d(&trow, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.q_row, a.R, a.C, kTile, kTile,
+                                CU_TENSOR_MAP_SWIZZLE_128B))
+            return FP8Q_ERR_CUDA;
+        if (COL && !make_map_2d(&tcol, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.q_col, a.C, a.R, kTile, kTile,
+                                CU_TENSOR_MAP_SWIZZLE_128B))
+            return FP8Q_ERR_CUDA;
+    }
     int64_t grid = (int64_t)num_sms() * 2;
     if (ntiles < grid) grid = ntiles;
     if (grid < 1) grid = 1;
-    kern<<<(unsigned)grid, kThreads, kTileSmem, s>>>(tm, a);
+    kern<<<(unsigned)grid, kThreads, kTileSmem, s>>>(tm, trow, tcol, a);
     return cudaGetLastError() == cudaSuccess ? FP8Q_OK : FP8Q_ERR_CUDA;
 }
 
