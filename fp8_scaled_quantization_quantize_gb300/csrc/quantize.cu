@@ -143,18 +143,19 @@ __device__ __forceinline__ Factor make_factor(float k) {
 // x / d correctly rounded from r = RN(1 / d): q = RN(x r) lies within one ulp
 // of x / d, the residual x - d q is exactly representable and one FMA gives
 // it, and RN(q + residual * r) = RN(x / d) (Markstein's theorem on division
-// with a correctly rounded reciprocal).  Quotients that underflow keep the
-// sign of x (d > 0).  Valid for finite x, d in [2^-80, 2^128) and quotients in
-// [2^-24, 2^126): near overflow x r can round to infinity, and for tiny x the
-// residual can fall below the normal range; quotients under 2^-24 are below
-// half the smallest subnormal of either FP8 format and encode to zero
-// whatever their last bits, and quantization only divides |x| <= amax by
-// RN(amax / fmax), so its quotients stay below fmax (1 + 2^-23).
+// with a correctly rounded reciprocal).  The residual is formed negated,
+// t = RN(q d - x), and added back as -t r: the same values for x != 0, and the
+// sign of a zero x survives (-0: t = +0, -0 + -0 = -0), as it does for
+// quotients that underflow (d > 0).  Valid for finite x, d in [2^-80, 2^128)
+// and quotients in [2^-24, 2^126): near overflow x r can round to infinity,
+// and for tiny x the residual can fall below the normal range; quotients under
+// 2^-24 are below half the smallest subnormal of either FP8 format and encode
+// to zero whatever their last bits, and quantization only divides |x| <= amax
+// by RN(amax / fmax), so its quotients stay below fmax (1 + 2^-23).
 __device__ __forceinline__ float div_rn_recip(float x, float d, float r) {
     const float q = __fmul_rn(x, r);
-    const float e = __fmaf_rn(-q, d, x);
-    const float q2 = __fmaf_rn(e, r, q);
-    return __uint_as_float((__float_as_uint(q2) & 0x7FFFFFFFu) | (__float_as_uint(x) & 0x80000000u));
+    const float t = __fmaf_rn(q, d, -x);
+    return __fmaf_rn(-t, r, q);
 }
 
 // The recipe's scaled value of a finite element (FAST: the blockwise divisor
@@ -429,12 +430,23 @@ __global__ void __launch_bounds__(kThreads, 2)
             }
             if (ROW) nsat_row += nsat_rc;  // a transposed column copy reports no count of its own
         }
+        // the stage takes the codes once every thread has read its bf16 tile:
+        // after the block-maximum barrier (128x128; 1x128 without a column
+        // copy), after the column-block barrier (1x128), else after one more
+        uint8_t* rowt = stage;                  // [128 rows][128 codes], 128-byte swizzle
+        uint8_t* colt = stage + kTile * kTile;  // [128 columns][128 codes], 128-byte swizzle
+        auto put_row_codes = [&]() {
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                *(uint4*)(rowt + swz(rr, 4 * hh + c)) = make_uint4(q[2 * c].x, q[2 * c].y, q[2 * c + 1].x, q[2 * c + 1].y);
+        };
+        constexpr bool kCodesAfterBlockMax = KIND == kB128 || (KIND == kB1 && !COL);
+        if constexpr (kRowCodes && kCodesAfterBlockMax) put_row_codes();
 
         // ---------------- column-wise codes re-quantized along the columns (1x128, MXFP8)
         const int p = t & 63, qd = t >> 6;  // column pair 2p, 2p + 1; rows 32 qd .. 32 qd + 31
         uint32_t o0[8], o1[8];
         if constexpr (COL && !kTranspose) {
-            const bool tile_nf = __syncthreads_or(vnf != 0) != 0;
             // columns 2p, 2p+1 sit in half p / 32, chunk (2p % 64) / 8, bytes (2p % 8) * 2
             const uint8_t* chalf = stage + (p >> 5) * (kStageBytes / 2) + ((2 * p) & 7) * 2;
             const int chunk = ((2 * p) & 63) >> 3;
@@ -443,13 +455,15 @@ __global__ void __launch_bounds__(kThreads, 2)
             for (int j = 0; j < 32; ++j) w[j] = *(const uint32_t*)(chalf + swz(32 * qd + j, chunk));
             float k0, k1;
             uint32_t m0, m1;
+            bool col_nf;  // a NaN / Inf among these 64 elements
             {
                 uint32_t pm = 0;
 #pragma unroll
                 for (int j = 0; j < 32; ++j) pm = max_u16x2(pm, w[j] & 0x7FFF7FFFu);
                 m0 = pm & 0xFFFFu;
                 m1 = pm >> 16;
-                if (m0 >= 0x7F80u || m1 >= 0x7F80u) {  // NaN / Inf: exact finite maxima
+                col_nf = m0 >= 0x7F80u || m1 >= 0x7F80u;
+                if (col_nf) {  // NaN / Inf: exact finite maxima
                     m0 = m1 = 0;
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
@@ -471,7 +485,8 @@ __global__ void __launch_bounds__(kThreads, 2)
                 } else {  // 1x128 along the rows of x: reduce the four quarters
                     colred[qd * kTile + 2 * p] = m0;
                     colred[qd * kTile + 2 * p + 1] = m1;
-                    __syncthreads();
+                    __syncthreads();  // also: every bf16 read of the tile is done
+                    if constexpr (kRowCodes) put_row_codes();
                     m0 = max(max(colred[2 * p], colred[kTile + 2 * p]),
                              max(colred[2 * kTile + 2 * p], colred[3 * kTile + 2 * p]));
                     m1 = max(max(colred[2 * p + 1], colred[kTile + 2 * p + 1]),
@@ -489,7 +504,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             // convert 32 rows of columns 2p, 2p+1
             uint32_t ns = 0;
             const Factor f0 = make_factor<KIND>(k0), f1 = make_factor<KIND>(k1);
-            if (!tile_nf && f0.fast && f1.fast) {
+            if (!col_nf && f0.fast && f1.fast) {
                 const bool c0s = may_saturate<KIND, FMT>(m0, f0), c1s = may_saturate<KIND, FMT>(m1, f1);
                 const Factor2 g = pair_factor(f0, f1);  // lanes: column 2p, column 2p + 1
 #pragma unroll
@@ -526,13 +541,9 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
 
         // ---------------- codes into the stage (its bf16 tile is consumed), then TMA stores
-        __syncthreads();
-        uint8_t* rowt = stage;                  // [128 rows][128 codes], 128-byte swizzle
-        uint8_t* colt = stage + kTile * kTile;  // [128 columns][128 codes], 128-byte swizzle
-        if constexpr (kRowCodes) {
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-                *(uint4*)(rowt + swz(rr, 4 * hh + c)) = make_uint4(q[2 * c].x, q[2 * c].y, q[2 * c + 1].x, q[2 * c + 1].y);
+        if constexpr (!kCodesAfterBlockMax && KIND != kB1) {
+            __syncthreads();
+            if constexpr (kRowCodes) put_row_codes();
         }
         if constexpr (kTranspose) {
             __syncthreads();
