@@ -57,8 +57,47 @@ def peaks():
         return 6800.0, 1900.0, "fallback"
 
 
+class _Nvml:
+    """Read-only NVML queries through the driver's libnvidia-ml (ctypes): SM
+    clock, its maximum, power and the active clock-event (throttle) reasons."""
+
+    REASONS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown", 0x4: "sw_power_cap"}
+
+    def __init__(self, cuda_index: int):
+        import ctypes
+        self.c = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        import torch
+        props = torch.cuda.get_device_properties(cuda_index)
+        bus = getattr(props, "pci_bus_id", None)
+        dom = getattr(props, "pci_domain_id", 0)
+        dev = getattr(props, "pci_device_id", 0)
+        ok = False
+        if bus is not None:
+            pci = f"{dom:08x}:{bus:02x}:{dev:02x}.0".encode()
+            ok = self.lib.nvmlDeviceGetHandleByPciBusId_v2(ctypes.c_char_p(pci), ctypes.byref(self.h)) == 0
+        if not ok and self.lib.nvmlDeviceGetHandleByIndex_v2(cuda_index, ctypes.byref(self.h)) != 0:
+            raise RuntimeError("no NVML handle")
+        fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None)
+        self.reasons_fn = fn if fn is not None else self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    def sample(self):
+        c = self.c
+        sm, mx, pw, rs = c.c_uint(0), c.c_uint(0), c.c_uint(0), c.c_ulonglong(0)
+        self.lib.nvmlDeviceGetClockInfo(self.h, 1, c.byref(sm))      # NVML_CLOCK_SM
+        self.lib.nvmlDeviceGetMaxClockInfo(self.h, 1, c.byref(mx))
+        self.lib.nvmlDeviceGetPowerUsage(self.h, c.byref(pw))
+        self.reasons_fn(self.h, c.byref(rs))
+        return sm.value, mx.value, pw.value / 1000.0, [n for b, n in self.REASONS.items() if rs.value & b]
+
+
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
+    """SM clocks and throttle reasons sampled every 2 ms (NVML, in a thread)
+    while the timed region runs; nvidia-smi every 200 ms if NVML is not
+    reachable."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -67,9 +106,33 @@ class ClockSampler:
     def __init__(self, index: int):
         self.index = index
         self.proc = None
-        self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.rows = []
+        self.nvml = None
+        self.stop = None
+        self.thread = None
+        try:
+            self.nvml = _Nvml(index)
+        except Exception:
+            self.nvml = None
 
     def __enter__(self):
+        import threading
+        if self.nvml is not None:
+            self.stop = threading.Event()
+
+            def run():
+                while not self.stop.is_set():
+                    try:
+                        self.rows.append(self.nvml.sample())
+                    except Exception:
+                        pass
+                    time.sleep(0.002)
+
+            self.rows.append(self.nvml.sample())
+            self.thread = threading.Thread(target=run, daemon=True)
+            self.thread.start()
+            return self
+        self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
                                           "--format=csv,noheader,nounits", "-lms", "200"],
@@ -79,6 +142,10 @@ class ClockSampler:
         return self
 
     def __exit__(self, *exc):
+        if self.thread is not None:
+            self.rows.append(self.nvml.sample())
+            self.stop.set()
+            self.thread.join(timeout=5)
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -87,6 +154,13 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self):
+        if self.nvml is not None:
+            if not self.rows:
+                return None
+            sm = [r[0] for r in self.rows]
+            return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(r[1] for r in self.rows),
+                    "reasons": sorted({n for r in self.rows for n in r[3]}), "samples": len(self.rows),
+                    "power_w_max": round(max(r[2] for r in self.rows), 1), "source": "nvml, every 2 ms"}
         try:
             rows = [[c.strip() for c in r.split(",")] for r in open(self.tmp.name).read().strip().splitlines()
                     if r.strip()]
@@ -108,7 +182,7 @@ class ClockSampler:
         reasons = sorted({names[i] for r in rows for i in range(4)
                           if len(r) > 5 + i and r[5 + i].lower() == "active"})
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(rows)}
+                "reasons": reasons, "samples": len(rows), "source": "nvidia-smi, every 200 ms"}
 
 
 def dist_setup(n):
@@ -273,11 +347,12 @@ def run_ours(args):
         "gemm_tflops": round(gemm_tflops, 1),
         "quantize_gbs": round(qbytes / q_avg / 1e6, 1),
         "quantize_frac_of_hbm": round(qbytes / q_avg / 1e6 / hbm_peak, 3),
-        "roofline": {"kernel": "gemm_kernel<blockwise 1x128 x 128x128, bf16 out>", "bound": "tensor",
+        "roofline": {"kernel": gemm_kernel_name(T, F, "blockwise 1x128 x 128x128"), "bound": "tensor",
                      "achieved": round(gemm_tflops, 1), "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
                      "frac": round(gemm_tflops / fp8_peak, 3),
                      "peak_source": f"{peak_kind} bf16 burst x2 (dense FP8 / BF16 nominal ratio)",
-                     "traffic": None},
+                     "traffic": measured_traffic("gemm2_blockwise_llama8b_up_proj.md", GEMM2_SOURCES),
+                     "traffic_algorithmic": round(T * H + F * H + 2 * T * F + 4 * (T * H / 128 + F * H / 16384))},
         "e2e": {"value": round(world * flops / e2e_step / 1e9, 1), "unit": UNIT,
                 "h2d_bytes_per_step": X.numel() * 2 + W.numel() * 2, "d2h_bytes_per_step": Y.numel() * 2},
         "gpu_launches": launches,
@@ -292,6 +367,36 @@ def run_ours(args):
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def measured_traffic(profile: str, sources) -> float | None:
+    """dram read + write bytes per launch recorded in a profile summary, or
+    None once the kernel's sources have changed since that capture."""
+    import hashlib
+    try:
+        text = open(os.path.join(ROOT, "profiles", profile)).read()
+        rec = dict(line.split(": ", 1) for line in text.splitlines()
+                   if line.startswith(("traffic_bytes_per_launch: ", "sources_sha256: ")))
+        h = hashlib.sha256()
+        for src in sources:
+            with open(os.path.join(ROOT, "fp8_scaled_quantization_quantize_gb300", "csrc", src), "rb") as f:
+                h.update(f.read())
+        if h.hexdigest() != rec["sources_sha256"].strip():
+            return None
+        return float(rec["traffic_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+GEMM2_SOURCES = ("gemm2.cu", "umma.cuh", "ptx.cuh", "fp8q_internal.cuh")
+
+
+def gemm_kernel_name(M, N, recipe, out="bf16"):
+    """The kernel fp8q_scaled_gemm's automatic choice runs: SM pairs (gemm2_kernel,
+    256 x 256 tiles) once there are at least 64 such tiles, else gemm_kernel."""
+    if ((M + 255) // 256) * ((N + 255) // 256) >= 64:
+        return f"gemm2_kernel<{recipe}, {out} out> (SM pairs, 256x256 tiles)"
+    return f"gemm_kernel<{recipe}, {out} out> (one SM per 128x256 tile)"
 
 
 # ------------------------------------------------------- single-op modes

@@ -185,15 +185,17 @@ __device__ __forceinline__ Factor2 pair_factor(const Factor& a, const Factor& b)
     return f;
 }
 __device__ __forceinline__ float2 bf16x2_f32(uint32_t w) { return make_float2(bf16_lo(w), bf16_hi(w)); }
-// apply<KIND, true> on both lanes: the blockwise quotient by the reciprocal
-// and one residual correction (div_rn_recip, lane by lane: measured faster
-// than its two-lane form), else the two-lane product.
+// apply<KIND, true> on both lanes: div_rn_recip's three steps (the residual
+// formed negated) for the blockwise recipes, else the product.
 template <int KIND>
 __device__ __forceinline__ float2 apply2(float2 x, const Factor2& f) {
-    if constexpr (KIND == kB1 || KIND == kB128)
-        return make_float2(div_rn_recip(x.x, f.k.x, f.r.x), div_rn_recip(x.y, f.k.y, f.r.y));
-    else
+    if constexpr (KIND == kB1 || KIND == kB128) {
+        const float2 q = __fmul2_rn(x, f.r);
+        const float2 t = __ffma2_rn(q, f.k, make_float2(-x.x, -x.y));
+        return __ffma2_rn(make_float2(-t.x, -t.y), f.r, q);
+    } else {
         return __fmul2_rn(x, f.k);
+    }
 }
 template <int FMT>
 __device__ __forceinline__ uint32_t sat2(float2 y, bool cx, bool cy) {
