@@ -8,14 +8,17 @@
 // (r = 0) issues each MMA for both, so every SM streams half of the B panel
 // it would need alone and each shared-memory stage is a third smaller.
 //
-// Per CTA, 576 threads: warp 0 TMA producer (its halves, completing on the
+// Per CTA, 320 threads: warp 0 TMA producer (its halves, completing on the
 // leader's barriers), warp 1 TMEM allocation (with the peer) and, in the
-// leader, the single-thread MMA issuer; warps 2-17 the epilogue of the CTA's
-// own 128 rows (TMEM lanes 32 (w % 4) .., columns BN / 4 ((w - 2) / 4) ..),
-// which releases TMEM on the leader's barrier and stores D by TMA.
+// leader, the single-thread MMA issuer; warps 2-9 the epilogue of the CTA's
+// own 128 rows (TMEM lanes 32 (w % 4) .., columns 128 ((w - 2) / 4) ..),
+// which releases TMEM on the leader's barrier and stores D by TMA.  Eight
+// epilogue warps of 128 columns (not sixteen of 64) halve the per-K-block
+// handshakes the blockwise promotion issues on the schedulers it shares with
+// the MMA and TMA threads.
 // TMEM per CTA: per-tensor two 256-column accumulators; MXFP8 one accumulator
-// plus 12 scale columns per stage; blockwise (BN = 128) four 128-column
-// partial buffers, so the MMAs run up to three K blocks ahead of the epilogue.
+// plus 12 scale columns per stage; blockwise two 256-column partial buffers,
+// so the MMAs run one K block ahead of the epilogue.
 // All mbarrier waits are bounded as in gemm.cu; both CTAs always reach the
 // closing cluster barrier, so neither exits while its shared memory or TMEM
 // can still be used by the pair.
@@ -32,7 +35,7 @@ __device__ unsigned int g_device_errors2 = 0;
 namespace {
 
 constexpr int BM = 128, BK = 128;
-constexpr int kEpiWarps = 16;
+constexpr int kEpiWarps = 8;  // two per TMEM lane quarter, 128 columns each
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr uint64_t kWaitNs = 1000000000ull;
 enum { REC_PT = 0, REC_MX = 1, REC_B2D = 2, REC_B1D = 3 };
@@ -44,7 +47,7 @@ struct Cfg {
     static constexpr int BH = BN / 2;  // B rows per CTA
     static constexpr int STAGES = BLOCKWISE ? 4 : 5;
     static constexpr int NACC = (REC == REC_MX) ? 1 : 2;  // TMEM accumulators (blockwise: K-block partials)
-    static constexpr int EPI_COLS = BN / 4;
+    static constexpr int EPI_COLS = BN / (kEpiWarps / 4);
     // blockwise scales ring: per K block, this CTA's 128 A-row scales (512 B)
     // and the tile's B scales (two floats for 128x128 blocks, 256 for 1x128);
     // deep enough that the producer is never held back by the epilogue
@@ -57,7 +60,7 @@ struct Cfg {
     static constexpr uint32_t OFF_SFB = OFF_SFA + (REC == REC_MX ? STAGES * 512 : 0);
     static constexpr uint32_t OFF_SCL = OFF_SFB + (REC == REC_MX ? STAGES * 1024 : 0);
     static constexpr uint32_t OFF_STG = OFF_SCL + SR * SLOT;
-    static constexpr uint32_t STG_WARP = BLOCKWISE ? 4096 : 2048;  // 1 KB output boxes per epilogue warp
+    static constexpr uint32_t STG_WARP = 4096;  // four 1 KB output boxes per epilogue warp
     static constexpr uint32_t OFF_BAR = OFF_STG + kEpiWarps * STG_WARP;
     static constexpr uint32_t NBARS = 2 * STAGES + 2 * NACC + 1 + 2 * SR;
     static constexpr uint32_t OFF_MISC = OFF_BAR + 8 * NBARS;
@@ -406,16 +409,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t abuf = tile_i % NACC;
                 if (!mbar_wait2(tfull(abuf), (tile_i / NACC) & 1u, abort_flag)) break;
                 tc_fence_after();
-                uint32_t r[64];
-                FP8Q_LD32(tmem + lane_base + abuf * BN + tcol, r);
-                FP8Q_LD32(tmem + lane_base + abuf * BN + tcol + 32, (r + 32));
-                tc_wait_ld();
-                reg_fence32(r);
-                reg_fence32(r + 32);
-                release(abuf);
-                float vf[64];
+                uint32_t r[EC];
 #pragma unroll
-                for (int i = 0; i < 64; ++i) vf[i] = __uint_as_float(r[i]);
+                for (int c = 0; c < EC / 32; ++c) FP8Q_LD32(tmem + lane_base + abuf * BN + tcol + 32 * c, (r + 32 * c));
+                tc_wait_ld();
+#pragma unroll
+                for (int c = 0; c < EC / 32; ++c) reg_fence32(r + 32 * c);
+                release(abuf);
+                float vf[EC];
+#pragma unroll
+                for (int i = 0; i < EC; ++i) vf[i] = __uint_as_float(r[i]);
                 store_slice2<OUT_F32, EC, C::STG_WARP / 1024>(&tmD, stg, stg_s, lane, (int)col0, (int)row0, (int)p.N, (int)p.M, vf, sab);
             } else {
                 float2 acc[EC / 2];  // packed pairs: Blackwell's two-lane FMA halves the promotion's instructions
