@@ -62,7 +62,8 @@ struct Cfg {
     static constexpr uint32_t OFF_STG = OFF_SCL + SR * SLOT;
     static constexpr uint32_t STG_WARP = 4096;  // four 1 KB output boxes per epilogue warp
     static constexpr uint32_t OFF_BAR = OFF_STG + kEpiWarps * STG_WARP;
-    static constexpr uint32_t NBARS = 2 * STAGES + 2 * NACC + 1 + 2 * SR;
+    static constexpr int NSFB = (REC == REC_MX) ? STAGES : 0;  // MXFP8 scale-tile barriers per kind
+    static constexpr uint32_t NBARS = 2 * STAGES + 2 * NACC + 1 + 2 * SR + 2 * NSFB;
     static constexpr uint32_t OFF_MISC = OFF_BAR + 8 * NBARS;
     static constexpr uint32_t SMEM = OFF_MISC + 16 + 1024;
     static_assert(SMEM <= 232448, "shared memory budget of one CTA");
@@ -152,9 +153,14 @@ __device__ __forceinline__ void mma2_mx(uint32_t d, uint64_t a, uint64_t b, uint
             d),
         "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc));
 }
-__device__ __forceinline__ void tc2_cp_32x128b(uint32_t taddr, uint64_t desc) {
-    asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc));
+// Four TMEM columns of the warp's 32 lanes from registers, and the wait for
+// this thread's TMEM stores.
+__device__ __forceinline__ void tc_st_x4(uint32_t taddr, const uint4& v) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
 }
+__device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // Stores this warp's 32 rows x COLS columns through its staging area of NBOX
 // 1 KB boxes of 32-byte row pieces (32-byte swizzle: chunk c of row r at
@@ -216,6 +222,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t mma_done = sb + C::OFF_BAR + 8u * (2 * STAGES + 2 * NACC);
     auto sfull = [&](int r) { return sb + C::OFF_BAR + 8u * (2 * STAGES + 2 * NACC + 1 + r); };
     auto sempty = [&](int r) { return sb + C::OFF_BAR + 8u * (2 * STAGES + 2 * NACC + 1 + C::SR + r); };
+    // MXFP8: stage s's scale tiles have landed in this CTA (sfl) / are in both
+    // CTAs' TMEM (sfr, the leader's, one arrival per lane-quarter warp and CTA)
+    auto sfl = [&](int st) { return sb + C::OFF_BAR + 8u * (2 * STAGES + 2 * NACC + 1 + 2 * C::SR + st); };
+    auto sfr = [&](int st) { return sb + C::OFF_BAR + 8u * (2 * STAGES + 2 * NACC + 1 + 2 * C::SR + C::NSFB + st); };
     uint32_t* tmem_slot = (uint32_t*)(smem + C::OFF_MISC);
     volatile int* abort_flag = (volatile int*)(smem + C::OFF_MISC + 4);
 
@@ -235,6 +245,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int r = 0; r < C::SR; ++r) {
             mbar_init(sfull(r), REC == REC_B2D ? 2 : 1);
             mbar_init(sempty(r), kEpiWarps);
+        }
+        for (int st = 0; st < C::NSFB; ++st) {
+            mbar_init(sfl(st), 1);
+            mbar_init(sfr(st), 2 * 4);
         }
         *abort_flag = 0;
         mbar_fence_init();
@@ -276,19 +290,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     const uint32_t fl = mapa(full(s), 0);
-                    if (leader) {
-                        uint32_t bytes = 2 * (C::A_STAGE + C::B_STAGE);
-                        if (REC == REC_MX) bytes += 2 * (512 + (b2 ? 1024u : 512u));
-                        mbar_expect_tx(full(s), bytes);
-                    }
+                    if (leader) mbar_expect_tx(full(s), 2 * (C::A_STAGE + C::B_STAGE));
                     tma_load_2d_pair(sb + C::OFF_A + s * C::A_STAGE, &tmA, (int)(kb * BK), (int)(mp * 256 + BM * cr), fl);
                     tma_load_2d_pair(sb + C::OFF_B + s * C::B_STAGE, &tmB, (int)(kb * BK), (int)(nb * BN + BH * cr), fl);
-                    if (REC == REC_MX) {
-                        tma_load_2d_pair(sb + C::OFF_SFA + s * 512, &tmSFA, 0, (int)((2 * mp + cr) * p.nkb + kb), fl);
-                        tma_load_2d_pair(sb + C::OFF_SFB + s * 1024, &tmSFB, 0, (int)((2 * nb) * p.nkb + kb), fl);
+                    if (REC == REC_MX) {  // scale tiles into this CTA, for its epilogue warps to move to TMEM
+                        mbar_expect_tx(sfl(s), 512 + (b2 ? 1024u : 512u));
+                        tma_load_2d(sb + C::OFF_SFA + s * 512, &tmSFA, 0, (int)((2 * mp + cr) * p.nkb + kb), sfl(s));
+                        tma_load_2d(sb + C::OFF_SFB + s * 1024, &tmSFB, 0, (int)((2 * nb) * p.nkb + kb), sfl(s));
                         if (b2)
-                            tma_load_2d_pair(sb + C::OFF_SFB + s * 1024 + 512, &tmSFB, 0,
-                                             (int)((2 * nb + 1) * p.nkb + kb), fl);
+                            tma_load_2d(sb + C::OFF_SFB + s * 1024 + 512, &tmSFB, 0, (int)((2 * nb + 1) * p.nkb + kb),
+                                        sfl(s));
                     }
                     if constexpr (C::BLOCKWISE) {
                         const uint32_t r = kbp % C::SR;
@@ -323,12 +334,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t ph = 0;
             uint32_t tile_i = 0, kbg = 0;
             bool ok = true;
-            auto copy_sf = [&](int st) {
-                const uint32_t sft = tmem + SF_TMEM_COL + 12u * st;
-                tc2_cp_32x128b(sft, smem_desc(sb + C::OFF_SFA + st * 512, 0, 128, 0));
-                tc2_cp_32x128b(sft + 4, smem_desc(sb + C::OFF_SFB + st * 1024, 0, 128, 0));
-                tc2_cp_32x128b(sft + 8, smem_desc(sb + C::OFF_SFB + st * 1024 + 512, 0, 128, 0));
-            };
             for (int64_t t = cid; t < npt && ok; t += ncl, ++tile_i) {
                 const uint32_t abuf = tile_i % NACC;
                 if (REC == REC_PT || REC == REC_MX) {
@@ -346,12 +351,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tc_fence_after();
                         dcol = buf * BN;
                     }
-                    if (!mbar_wait2(full(s), ph, abort_flag)) {
+                    if (!mbar_wait2(full(s), ph, abort_flag) || (REC == REC_MX && !mbar_wait2(sfr(s), ph, abort_flag))) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    if (REC == REC_MX) copy_sf(s);
                     const uint32_t a0 = sb + C::OFF_A + s * C::A_STAGE, b0 = sb + C::OFF_B + s * C::B_STAGE;
                     if (REC == REC_MX) {
                         const uint32_t sft = tmem + SF_TMEM_COL + 12u * s;
@@ -399,10 +403,48 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive_remote(mapa(tempty(b), 0));
         };
+        // MXFP8: these warps also move each K block's scale tiles from shared
+        // memory into TMEM with tcgen05.st (keeping the copies off the MMA
+        // issue stream): every lane quarter gets the tile's 32 rows of 16 bytes,
+        // the replicated layout the block-scaled MMA reads.  The two warps of a
+        // lane quarter take alternate K blocks, running up to STAGES - 1 K
+        // blocks past the tile being drained (further would wait on MMAs that
+        // wait on this warp's release of the accumulator).
+        uint64_t g_sf = (uint64_t)j;
+        const uint64_t my_tiles = npt > cid ? (uint64_t)((npt - cid + ncl - 1) / ncl) : 0;
+        const uint64_t total_kb = my_tiles * (uint64_t)p.nkb;
+        bool sf_ok = true;
+        auto move_sf_upto = [&](uint64_t limit) {
+            if constexpr (REC == REC_MX) {
+                while (sf_ok && g_sf < limit) {
+                    const int st = (int)(g_sf % STAGES);
+                    if (!mbar_wait2(sfl(st), (uint32_t)((g_sf / STAGES) & 1u), abort_flag)) {
+                        sf_ok = false;
+                        break;
+                    }
+                    const uint4 sa4 = *(const uint4*)(smem + C::OFF_SFA + st * 512 + lane * 16);
+                    const uint4 sb0 = *(const uint4*)(smem + C::OFF_SFB + st * 1024 + lane * 16);
+                    const uint4 sb1 = *(const uint4*)(smem + C::OFF_SFB + st * 1024 + 512 + lane * 16);
+                    const uint32_t sft = tmem + lane_base + SF_TMEM_COL + 12u * st;
+                    tc_st_x4(sft, sa4);
+                    tc_st_x4(sft + 4, sb0);
+                    tc_st_x4(sft + 8, sb1);
+                    tc_wait_st();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_remote(mapa(sfr(st), 0));
+                    g_sf += 2;
+                }
+            }
+        };
         uint32_t tile_i = 0, kbg = 0;
         for (int64_t t = cid; t < npt; t += ncl, ++tile_i) {
             int64_t mp, nb;
             tile_coords(t, p.tiles_m2, p.tiles_n, mp, nb);
+            if constexpr (REC == REC_MX) {
+                const uint64_t lim = (uint64_t)(tile_i + 1) * (uint64_t)p.nkb + (uint64_t)(STAGES - 1);
+                move_sf_upto(lim < total_kb ? lim : total_kb);
+            }
             const int64_t row0 = mp * 256 + BM * cr + 32 * q;  // this warp's first row
             const int64_t col0 = nb * BN + EC * j;
             if constexpr (!C::BLOCKWISE) {
