@@ -176,26 +176,38 @@ __device__ __forceinline__ float apply(float x, const Factor& f) {
 // lane an independent round-to-nearest operation, bit-identical to the
 // scalar forms).  Factor2 holds the factors of the two lanes.
 struct Factor2 {
-    float2 k, r;  // multiplier or divisor, its reciprocal
+    float2 k, nr;  // multiplier or divisor; minus the divisor's reciprocal
 };
 __device__ __forceinline__ Factor2 pair_factor(const Factor& a, const Factor& b) {
     Factor2 f;
     f.k = make_float2(a.k, b.k);
-    f.r = make_float2(a.r, b.r);
+    f.nr = make_float2(-a.r, -b.r);
     return f;
 }
 __device__ __forceinline__ float2 bf16x2_f32(uint32_t w) { return make_float2(bf16_lo(w), bf16_hi(w)); }
-// apply<KIND, true> on both lanes: div_rn_recip's three steps (the residual
-// formed negated) for the blockwise recipes, else the product.
+// The blockwise recipes' lanes come out negated: with nr = -RN(1/d),
+// -q = RN(x nr), e = RN(x - q d) = RN(-q d + x) (exact), -q2 = RN(e nr - q)
+// = -RN(q + e r) -- Markstein's three steps with no negation at run time, and
+// a zero x gives -q2 = -0 * sign(x), so the codes of -q2 with their sign bits
+// flipped (kNegated) are the codes of RN(x / d) with the sign of a zero kept.
+// Other recipes: the product.
+template <int KIND>
+constexpr bool kNegated = KIND == kB1 || KIND == kB128;
 template <int KIND>
 __device__ __forceinline__ float2 apply2(float2 x, const Factor2& f) {
-    if constexpr (KIND == kB1 || KIND == kB128) {
-        const float2 q = __fmul2_rn(x, f.r);
-        const float2 t = __ffma2_rn(q, f.k, make_float2(-x.x, -x.y));
-        return __ffma2_rn(make_float2(-t.x, -t.y), f.r, q);
+    if constexpr (kNegated<KIND>) {
+        const float2 nq = __fmul2_rn(x, f.nr);
+        const float2 e = __ffma2_rn(nq, f.k, x);
+        return __ffma2_rn(e, f.nr, nq);
     } else {
         return __fmul2_rn(x, f.k);
     }
+}
+// cvt4 of apply2's lanes, sign bits restored for the negated recipes.
+template <int KIND, int FMT>
+__device__ __forceinline__ uint32_t cvt4_applied(float a, float b, float c, float d) {
+    const uint32_t q = cvt4<FMT>(a, b, c, d);
+    return kNegated<KIND> ? q ^ 0x80808080u : q;
 }
 template <int FMT>
 __device__ __forceinline__ uint32_t sat2(float2 y, bool cx, bool cy) {
@@ -214,7 +226,7 @@ __device__ __forceinline__ uint2 convert8_packed(const uint4& v, const Factor2& 
     if (KIND != kB1 && KIND != kB128 || count)
         nsat += sat2<FMT>(y0, count, count) + sat2<FMT>(y1, count, count) + sat2<FMT>(y2, count, count) +
                 sat2<FMT>(y3, count, count);
-    return make_uint2(cvt4<FMT>(y0.x, y0.y, y1.x, y1.y), cvt4<FMT>(y2.x, y2.y, y3.x, y3.y));
+    return make_uint2(cvt4_applied<KIND, FMT>(y0.x, y0.y, y1.x, y1.y), cvt4_applied<KIND, FMT>(y2.x, y2.y, y3.x, y3.y));
 }
 
 // Converts the 8 finite bf16 of v; counts saturation only when the caller
@@ -516,8 +528,8 @@ __global__ void __launch_bounds__(kThreads, 2)
                     if (KIND != kB1 || c0s || c1s)
                         ns += sat2<FMT>(y0, c0s, c1s) + sat2<FMT>(y1, c0s, c1s) + sat2<FMT>(y2, c0s, c1s) +
                               sat2<FMT>(y3, c0s, c1s);
-                    o0[j / 4] = cvt4<FMT>(y0.x, y1.x, y2.x, y3.x);
-                    o1[j / 4] = cvt4<FMT>(y0.y, y1.y, y2.y, y3.y);
+                    o0[j / 4] = cvt4_applied<KIND, FMT>(y0.x, y1.x, y2.x, y3.x);
+                    o1[j / 4] = cvt4_applied<KIND, FMT>(y0.y, y1.y, y2.y, y3.y);
                 }
             } else {
 #pragma unroll
@@ -679,8 +691,9 @@ __global__ void cast_bits_kernel(uint32_t start, uint64_t count, uint8_t* out) {
 
 // For every finite bf16 x and each divisor d[j] in the fast range whose
 // quotient is below 2^126 in magnitude, compares div_rn_recip(x, d, RN(1/d))
-// with the IEEE quotient: [0] counts FP8 codes that differ (all such pairs),
-// [1] fp32 results that differ where the IEEE quotient is at least 2^-24.
+// and the tile kernel's two-lane negated form (on x and -x) with the IEEE
+// quotient: [0] counts FP8 codes that differ (all such pairs), [1] fp32
+// results that differ where the IEEE quotient is at least 2^-24.
 template <int FMT>
 __global__ void div_selftest_kernel(const float* d, int64_t nd, unsigned long long* mismatch) {
     const uint32_t xb = blockIdx.x * blockDim.x + threadIdx.x;  // bf16 pattern
@@ -692,9 +705,21 @@ __global__ void div_selftest_kernel(const float* d, int64_t nd, unsigned long lo
         if (!xfin || !(dj >= 0x1p-80f) || !(dj < 0x1p+128f)) continue;
         const float exact = __fdiv_rn(x, dj);
         if (!(fabsf(exact) < 0x1p+126f)) continue;
-        const float fast = div_rn_recip(x, dj, __frcp_rn(dj));
-        bad_bits += fabsf(exact) >= 0x1p-24f && __float_as_uint(exact) != __float_as_uint(fast);
-        bad_code += (cvt2<FMT>(exact, 0.0f) & 0xFFu) != (cvt2<FMT>(fast, 0.0f) & 0xFFu);
+        const float r = __frcp_rn(dj);
+        const float fast = div_rn_recip(x, dj, r);
+        // the two-lane, negated form the tile kernel runs (lane x: this pair)
+        Factor f;
+        f.k = dj;
+        f.r = r;
+        f.fast = true;
+        const float2 ny = apply2<kB1>(make_float2(x, -x), pair_factor(f, f));
+        const uint32_t ce = cvt2<FMT>(exact, -exact);
+        const bool big = fabsf(exact) >= 0x1p-24f;
+        bad_bits += big && __float_as_uint(exact) != __float_as_uint(fast);
+        bad_bits += big && (__float_as_uint(exact) != __float_as_uint(-ny.x) ||
+                            __float_as_uint(-exact) != __float_as_uint(-ny.y));
+        bad_code += (ce & 0xFFu) != (cvt2<FMT>(fast, 0.0f) & 0xFFu);
+        bad_code += ce != ((cvt2<FMT>(ny.x, ny.y) ^ 0x8080u) & 0xFFFFu);
     }
     bad_code = warp_sum_u32(bad_code);
     bad_bits = warp_sum_u32(bad_bits);

@@ -260,7 +260,8 @@ FP8Q_API fp8q_status fp8q_cast_f32_bits(uint32_t start, uint64_t count, int fmt,
  * takes the IEEE division; quantization's quotients never exceed
  * fmax (1 + 2^-23); below 2^-24, where the residual of a tiny x can leave the
  * normal range, every quotient encodes to an FP8 zero).  This entry point
- * compares that computation with the IEEE quotient for every finite bf16 x
+ * compares that computation (scalar, and the two-lane form with negated
+ * lanes the tile kernel runs, on x and -x) with the IEEE quotient for every finite bf16 x
  * and every d[j] (device fp32 [nd]) whose quotient is below 2^126 and writes
  * the mismatch counts to mismatches (device uint64[2]: [0] FP8 codes of
  * format fmt over all those pairs, [1] fp32 bits where the IEEE quotient is
