@@ -131,7 +131,7 @@ __device__ __forceinline__ Factor make_factor(float k) {
     Factor f;
     f.k = k;
     if constexpr (KIND == kB1 || KIND == kB128) {
-        f.r = __frcp_rn(k);
+        f.r = k >= 0x1p-80f ? rcp_rn(k) : 0.0f;  // the reciprocal serves the shortcut only
         f.fast = k >= 0x1p-80f;  // keeps the residual below exact in fp32
     } else {
         f.r = 0.0f;
@@ -693,19 +693,26 @@ __global__ void cast_bits_kernel(uint32_t start, uint64_t count, uint8_t* out) {
 // quotient is below 2^126 in magnitude, compares div_rn_recip(x, d, RN(1/d))
 // and the tile kernel's two-lane negated form (on x and -x) with the IEEE
 // quotient: [0] counts FP8 codes that differ (all such pairs), [1] fp32
-// results that differ where the IEEE quotient is at least 2^-24.
+// results that differ where the IEEE quotient is at least 2^-24, plus the
+// kernels' rcp_rn(d) against the IEEE reciprocal and their block_scale(x)
+// against IEEE amax / fmax for every positive bf16 x.
 template <int FMT>
 __global__ void div_selftest_kernel(const float* d, int64_t nd, unsigned long long* mismatch) {
     const uint32_t xb = blockIdx.x * blockDim.x + threadIdx.x;  // bf16 pattern
     const float x = __uint_as_float(xb << 16);
     const bool xfin = (xb & 0x7F80u) != 0x7F80u;
     uint32_t bad_code = 0, bad_bits = 0;
+    if (blockIdx.y == 0 && xfin && x > 0.0f &&  // the kernels' block divisor, every positive bf16 amax
+        __float_as_uint(block_scale<FMT>(x)) != __float_as_uint(__fdiv_rn(x, Fmt<FMT>::fmax)))
+        ++bad_bits;
     for (int64_t j = blockIdx.y; j < nd; j += gridDim.y) {
         const float dj = d[j];
         if (!xfin || !(dj >= 0x1p-80f) || !(dj < 0x1p+128f)) continue;
         const float exact = __fdiv_rn(x, dj);
         if (!(fabsf(exact) < 0x1p+126f)) continue;
         const float r = __frcp_rn(dj);
+        if (xb == 0 && dj <= 0x1p+120f && __float_as_uint(rcp_rn(dj)) != __float_as_uint(r))
+            ++bad_bits;  // the kernels' reciprocal, on its domain (a bf16 amax gives d < 2^120)
         const float fast = div_rn_recip(x, dj, r);
         // the two-lane, negated form the tile kernel runs (lane x: this pair)
         Factor f;
