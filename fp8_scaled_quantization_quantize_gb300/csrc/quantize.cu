@@ -290,6 +290,28 @@ __device__ __forceinline__ void transpose4(uint32_t h0, uint32_t h1, uint32_t h2
     y = __byte_perm(a, b, 0x7632);
 }
 
+// Number of the bf16 of v whose magnitude bits equal m.
+__device__ __forceinline__ uint32_t count_equal8(const uint4& v, uint32_t m) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t c = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) c += ((w[i] & 0x7FFFu) == m) + (((w[i] >> 16) & 0x7FFFu) == m);
+    return c;
+}
+// Saturated elements of a per-tensor-current or blockwise block whose maximum
+// m can saturate.  Those scales are one correctly rounded division of fmax and
+// amax (relative error <= 2^-24) and the next bf16 below m is at least 2^-8
+// smaller, so only elements equal to m in magnitude can exceed fmax once
+// scaled: count those, looking only inside the vectors whose maximum is m.
+template <int J0, int J1>
+__device__ __forceinline__ uint32_t count_at_max(const uint4 (&v)[8], uint32_t m) {
+    uint32_t c = 0;
+#pragma unroll
+    for (int j = J0; j < J1; ++j)
+        if (fold16(vec_pmax(v[j])) == m) c += count_equal8(v[j], m);
+    return c;
+}
+
 template <int KIND, int FMT, bool ROW, bool COL>
 __global__ void __launch_bounds__(kThreads, 2)
     quant_tile_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmrow,
@@ -367,11 +389,14 @@ __global__ void __launch_bounds__(kThreads, 2)
         for (int j = 0; j < 8; ++j) v[j] = *(const uint4*)(half + swz(rr, j));
         uint32_t vnf = 0;       // bit j: vector j holds a NaN / Inf
         uint32_t mq[2];         // MX: the two 1x32 blocks' maxima; else mq[0] = the half-row maximum
+        uint32_t mh[2];         // the maxima of vectors 0-3 and 4-7 (NaN / Inf-free halves)
         {
             const uint32_t p0 = max_u16x2(max_u16x2(vec_pmax(v[0]), vec_pmax(v[1])),
                                           max_u16x2(vec_pmax(v[2]), vec_pmax(v[3])));
             const uint32_t p1 = max_u16x2(max_u16x2(vec_pmax(v[4]), vec_pmax(v[5])),
                                           max_u16x2(vec_pmax(v[6]), vec_pmax(v[7])));
+            mh[0] = fold16(p0);
+            mh[1] = fold16(p1);
             if constexpr (KIND == kMX) {
                 mq[0] = fold16(p0);
                 mq[1] = fold16(p1);
@@ -429,9 +454,15 @@ __global__ void __launch_bounds__(kThreads, 2)
             const bool s1 = (KIND == kMX) ? may_saturate<KIND, FMT>(mq[1], f1) : s0;
             if (vnf == 0 && f0.fast && f1.fast) {  // the common case: one straight-line block
                 const Factor2 g0 = pair_factor(f0, f0), g1 = pair_factor(f1, f1);
+                constexpr bool kAtMax = KIND == kCur || KIND == kB1 || KIND == kB128;
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
-                    q[j] = convert8_packed<KIND, FMT>(v[j], (j < 4) ? g0 : g1, nsat_rc, (j < 4) ? s0 : s1);
+                    q[j] = convert8_packed<KIND, FMT>(v[j], (j < 4) ? g0 : g1, nsat_rc,
+                                                      kAtMax ? false : ((j < 4) ? s0 : s1));
+                if (kAtMax && s0) {  // only elements equal to the block maximum can saturate
+                    if (mh[0] == mq[0]) nsat_rc += count_at_max<0, 4>(v, mq[0]);
+                    if (mh[1] == mq[0]) nsat_rc += count_at_max<4, 8>(v, mq[0]);
+                }
             } else {
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
@@ -468,14 +499,22 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
             for (int j = 0; j < 32; ++j) w[j] = *(const uint32_t*)(chalf + swz(32 * qd + j, chunk));
             float k0, k1;
-            uint32_t m0, m1;
-            bool col_nf;  // a NaN / Inf among these 64 elements
+            uint32_t m0, m1, own0, own1;  // column block maxima; this thread's 32-row maxima
+            bool col_nf;                   // a NaN / Inf among these 64 elements
+            uint32_t pmg[4];               // packed maxima of rows 8g .. 8g + 7
             {
-                uint32_t pm = 0;
 #pragma unroll
-                for (int j = 0; j < 32; ++j) pm = max_u16x2(pm, w[j] & 0x7FFF7FFFu);
+                for (int g = 0; g < 4; ++g) {
+                    uint32_t x = w[8 * g] & 0x7FFF7FFFu;
+#pragma unroll
+                    for (int i = 1; i < 8; ++i) x = max_u16x2(x, w[8 * g + i] & 0x7FFF7FFFu);
+                    pmg[g] = x;
+                }
+                const uint32_t pm = max_u16x2(max_u16x2(pmg[0], pmg[1]), max_u16x2(pmg[2], pmg[3]));
                 m0 = pm & 0xFFFFu;
                 m1 = pm >> 16;
+                own0 = m0;
+                own1 = m1;
                 col_nf = m0 >= 0x7F80u || m1 >= 0x7F80u;
                 if (col_nf) {  // NaN / Inf: exact finite maxima
                     m0 = m1 = 0;
@@ -525,11 +564,24 @@ __global__ void __launch_bounds__(kThreads, 2)
                 for (int j = 0; j < 32; j += 4) {
                     const float2 y0 = apply2<KIND>(bf16x2_f32(w[j]), g), y1 = apply2<KIND>(bf16x2_f32(w[j + 1]), g);
                     const float2 y2 = apply2<KIND>(bf16x2_f32(w[j + 2]), g), y3 = apply2<KIND>(bf16x2_f32(w[j + 3]), g);
-                    if (KIND != kB1 || c0s || c1s)
+                    if (KIND != kB1)
                         ns += sat2<FMT>(y0, c0s, c1s) + sat2<FMT>(y1, c0s, c1s) + sat2<FMT>(y2, c0s, c1s) +
                               sat2<FMT>(y3, c0s, c1s);
                     o0[j / 4] = cvt4_applied<KIND, FMT>(y0.x, y1.x, y2.x, y3.x);
                     o1[j / 4] = cvt4_applied<KIND, FMT>(y0.y, y1.y, y2.y, y3.y);
+                }
+                if (KIND == kB1 && ((c0s && own0 == m0) || (c1s && own1 == m1))) {
+                    // only elements equal to the block maximum can saturate (count_at_max),
+                    // looked for in the 8-row groups whose maximum it is
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) {
+                        const bool lo = c0s && (pmg[g] & 0xFFFFu) == m0, hi = c1s && (pmg[g] >> 16) == m1;
+                        if (lo || hi) {
+#pragma unroll
+                            for (int i = 0; i < 8; ++i)
+                                ns += (lo && (w[8 * g + i] & 0x7FFFu) == m0) + (hi && ((w[8 * g + i] >> 16) & 0x7FFFu) == m1);
+                        }
+                    }
                 }
             } else {
 #pragma unroll
