@@ -494,7 +494,7 @@ def run_modes(args):
         for mib in (16, 32, 64, 128, 256, 512, 1024, 2048):
             rows = mib * 2 ** 20 // 2 // 4096
             x = _device_tensor(rows, 4096, 5)
-            for kind in (0, 2, 3, 4):
+            for kind in (0, 1, 2, 3, 4):
                 print(json.dumps(quantize_point(kind, rows, 4096, True, True, args.steps, args.warmup, flush, x)),
                       flush=True)
             del x
