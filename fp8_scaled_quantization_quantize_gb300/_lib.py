@@ -17,7 +17,7 @@ PERTENSOR_CURRENT, PERTENSOR_DELAYED, BLOCK_1x128, BLOCK_128x128, MXFP8_1x32 = r
 EXPORTS = ("fp8q_version", "fp8q_status_str", "fp8q_scale_bytes", "fp8q_quantize", "fp8q_delayed_create",
            "fp8q_delayed_update", "fp8q_delayed_get", "fp8q_delayed_set", "fp8q_delayed_history_len",
            "fp8q_delayed_destroy", "fp8q_scaled_gemm", "fp8q_device_errors", "fp8q_cast_f32_bits", "fp8q_selftest_division",
-           "fp8q_gemm_set_variant")
+           "fp8q_gemm_set_variant", "fp8q_scaled_gemm_mxq")
 
 
 class Recipe(ctypes.Structure):
@@ -78,6 +78,9 @@ def load(path: str = LIB_PATH):
                                    i64, P]
     L.fp8q_device_errors.restype = i32
     L.fp8q_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint), P]
+    L.fp8q_scaled_gemm_mxq.restype = i32
+    L.fp8q_scaled_gemm_mxq.argtypes = [ctypes.POINTER(Tensor), i32, ctypes.POINTER(Tensor), i32, P, i32,
+                                       ctypes.POINTER(Tensor), i64, i64, i64, P]
     L.fp8q_gemm_set_variant.restype = i32
     L.fp8q_gemm_set_variant.argtypes = [i32]
     L.fp8q_selftest_division.restype = i32

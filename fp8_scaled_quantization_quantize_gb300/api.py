@@ -151,6 +151,26 @@ def scaled_gemm(A: QTensor, a_use_col: bool, B: QTensor, b_use_col: bool, out_dt
     return out
 
 
+def scaled_gemm_mxq(A: QTensor, a_use_col: bool, B: QTensor, b_use_col: bool, fmt: int = E4M3,
+                    want_d: bool = True, out: QTensor | None = None, d_out: torch.Tensor | None = None,
+                    stream=None):
+    """The GEMM with its bf16 output also quantized MXFP8 1x32 row-wise in the
+    epilogue (fp8q_scaled_gemm_mxq): returns (D bf16 or None, QTensor)."""
+    M = A.cols if a_use_col else A.rows
+    K = A.rows if a_use_col else A.cols
+    N = B.cols if b_use_col else B.rows
+    dev = (A.data_col if a_use_col else A.data_row).device
+    if out is None:
+        out = alloc(MXFP8_1x32, fmt, M, N, True, False, dev)
+    if want_d and d_out is None:
+        d_out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    ca, cb, cq = A.c_struct(), B.c_struct(), out.c_struct()
+    L.check(L.load().fp8q_scaled_gemm_mxq(ctypes.byref(ca), int(a_use_col), ctypes.byref(cb), int(b_use_col),
+                                          _ptr(d_out) if want_d else None, fmt, ctypes.byref(cq), M, N, K,
+                                          _stream(stream)), "fp8q_scaled_gemm_mxq")
+    return (d_out if want_d else None), out
+
+
 def gemm_set_variant(variant: int):
     """0 automatic, 1 one SM per tile, 2 SM pairs (see fp8q_gemm_set_variant)."""
     L.check(L.load().fp8q_gemm_set_variant(int(variant)), "fp8q_gemm_set_variant")

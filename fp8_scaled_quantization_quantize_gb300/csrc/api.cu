@@ -258,6 +258,52 @@ fp8q_status fp8q_scaled_gemm(const fp8q_tensor* A, int a_use_col, const fp8q_ten
     return launch_gemm(ga, gb, D, out_dtype, M, N, K, (cudaStream_t)stream);
 }
 
+fp8q_status fp8q_scaled_gemm_mxq(const fp8q_tensor* A, int a_use_col, const fp8q_tensor* B, int b_use_col, void* D,
+                                 int fmt, fp8q_tensor* Dq, int64_t M, int64_t N, int64_t K, void* stream) {
+    if (!A || !B || !Dq || !valid_fmt(fmt)) return FP8Q_ERR_ARG;
+    if (M < 1 || N < 1 || K < 1) return FP8Q_ERR_SHAPE;
+    if (K % 16 != 0 || N % 32 != 0) return FP8Q_ERR_SHAPE;
+    if (!Dq->data_row || !Dq->scale_row || !Dq->counters) return FP8Q_ERR_ARG;
+    if (!aligned16(Dq->data_row) || !aligned16(Dq->scale_row) || (D && !aligned16(D))) return FP8Q_ERR_ALIGN;
+    if (!valid_kind(A->kind) || !valid_kind(B->kind) || !valid_fmt(A->fmt) || !valid_fmt(B->fmt)) return FP8Q_ERR_ARG;
+    const int64_t am = a_use_col ? A->cols : A->rows, ak = a_use_col ? A->rows : A->cols;
+    const int64_t bn = b_use_col ? B->cols : B->rows, bk = b_use_col ? B->rows : B->cols;
+    if (am != M || ak != K || bn != N || bk != K) return FP8Q_ERR_SHAPE;
+    const bool a_pt = A->kind == FP8Q_PERTENSOR_CURRENT || A->kind == FP8Q_PERTENSOR_DELAYED;
+    const bool b_pt = B->kind == FP8Q_PERTENSOR_CURRENT || B->kind == FP8Q_PERTENSOR_DELAYED;
+    if (a_pt != b_pt) return FP8Q_ERR_DTYPE;
+    if (!a_pt) {
+        if (A->kind == FP8Q_MXFP8_1x32 || B->kind == FP8Q_MXFP8_1x32) {
+            if (A->kind != B->kind) return FP8Q_ERR_DTYPE;
+        } else if (A->kind != FP8Q_BLOCK_1x128) {
+            return FP8Q_ERR_DTYPE;
+        }
+    }
+    GemmOperand ga, gb;
+    ga.data = (const uint8_t*)(a_use_col ? A->data_col : A->data_row);
+    ga.scale = a_use_col ? A->scale_col : A->scale_row;
+    ga.scale_inv = A->scale_inv;
+    ga.rows = M;
+    ga.kind = A->kind;
+    ga.fmt = A->fmt;
+    gb.data = (const uint8_t*)(b_use_col ? B->data_col : B->data_row);
+    gb.scale = b_use_col ? B->scale_col : B->scale_row;
+    gb.scale_inv = B->scale_inv;
+    gb.rows = N;
+    gb.kind = B->kind;
+    gb.fmt = B->fmt;
+    if (!ga.data || !gb.data) return FP8Q_ERR_ARG;
+    if (a_pt ? !ga.scale_inv || !gb.scale_inv : !ga.scale || !gb.scale) return FP8Q_ERR_ARG;
+    if (!aligned16(ga.data) || !aligned16(gb.data)) return FP8Q_ERR_ALIGN;
+    if (!a_pt && (!aligned16(ga.scale) || !aligned16(gb.scale))) return FP8Q_ERR_ALIGN;
+    Dq->rows = M;
+    Dq->cols = N;
+    Dq->fmt = fmt;
+    Dq->kind = FP8Q_MXFP8_1x32;
+    return launch_gemm_pair(ga, gb, D, 0, M, N, K, (cudaStream_t)stream, fmt, Dq->data_row, Dq->scale_row,
+                            Dq->counters);
+}
+
 fp8q_status fp8q_gemm_set_variant(int variant) {
     if (variant < 0 || variant > 2) return FP8Q_ERR_ARG;
     g_gemm_variant = variant;

@@ -81,6 +81,10 @@ struct Params2 {
     const float* bsb;
     int64_t Mp, Np;
     uint32_t idesc;
+    // fused MXFP8 row-wise quantization of the bf16 output (QF != 0)
+    uint8_t* qscale;                 // packed 128x4 E8M0 tiles of the [M][N] row copy
+    unsigned long long* qcounters;   // [0] saturated, [2] NaN / Inf elements
+    int hasD;                        // also store the bf16 D
 };
 
 // ------------------------------------------------------------ PTX wrappers
@@ -205,11 +209,101 @@ __device__ __forceinline__ void store_slice2(const CUtensorMap* mapD, uint8_t* s
     }
 }
 
-template <int REC, bool OUT_F32>
+// MXFP8 (1x32 along N) quantization of this warp's 32 rows x COLS columns of
+// D as stored in bf16 (RN(v scale), as store_slice2 writes it): per 32-column
+// block the amax over finite |x|, e = floor(log2 amax) - emax_elem clamped to
+// [-127, 127] (E8M0 e + 127), codes sat_rne(x 2^-e) with a NaN keeping its
+// sign, saturated / NaN-Inf elements counted -- the quantize kernel's MXFP8
+// row path ("2025 FP8 quantized-training guide", sec. 2.3) on these values.
+// Codes leave through the staging boxes by TMA (uint8 32 x 32 boxes, 32-byte
+// swizzle); each row's four scale bytes of a 128-column group go to the packed
+// 128x4 tile layout.  Blocks past N and rows past M are not counted; scale
+// rows up to Mp are written (rows past M hold zeros: code 127, the pad).
+template <int QFMT, int COLS, int NBOX>
+__device__ __forceinline__ void store_q(const CUtensorMap* mapQ, uint8_t* stg, uint32_t stg_s, int lane, int x0, int y0,
+                                        const Params2& p, const float* v, float scale, uint32_t& nsat, uint32_t& nnf) {
+    static_assert(COLS == 128, "one 128-column scale group per warp slice");
+    const int r = lane, sw = (r >> 2) & 1;
+    const int64_t row = (int64_t)y0 + r;
+    const bool row_live = row < p.M;
+    uint32_t ebytes = 0;
+    bulk_wait_read();  // the D boxes have left the staging area
+    __syncwarp();
+#pragma unroll
+    for (int b = 0; b < COLS / 32; ++b) {
+        uint32_t h[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) h[i] = pack_bf16(v[32 * b + 2 * i] * scale, v[32 * b + 2 * i + 1] * scale);
+        const bool live = row_live && (int64_t)x0 + 32 * b < p.N;
+        uint32_t pm = 0;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) pm = max_u16x2(pm, h[i] & 0x7FFF7FFFu);
+        uint32_t m = max(pm & 0xFFFFu, pm >> 16);
+        const bool nf = m >= 0x7F80u;
+        if (nf) {  // exact finite maximum; NaN / Inf counted
+            m = 0;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const uint32_t a = (h[i / 2] >> (16 * (i & 1))) & 0x7FFFu;
+                if (a < 0x7F80u)
+                    m = a > m ? a : m;
+                else if (live)
+                    ++nnf;
+            }
+        }
+        if (!live) m = 0;
+        const int e = mx_exponent<QFMT>(m << 16);
+        const float k = exp2_neg(e);
+        ebytes |= (uint32_t)(e + 127) << (8 * b);
+        const float2 k2 = make_float2(k, k);
+        const bool sat = live && __uint_as_float(m << 16) * k > Fmt<QFMT>::fmax;
+        uint32_t c[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float2 y0 = __fmul2_rn(make_float2(__uint_as_float(h[2 * i] << 16), __uint_as_float(h[2 * i] & 0xFFFF0000u)), k2);
+            const float2 y1 = __fmul2_rn(
+                make_float2(__uint_as_float(h[2 * i + 1] << 16), __uint_as_float(h[2 * i + 1] & 0xFFFF0000u)), k2);
+            c[i] = cvt4<QFMT>(y0.x, y0.y, y1.x, y1.y);
+            if (sat)
+                nsat += (fabsf(y0.x) <= 3.402823466e38f && fabsf(y0.x) > Fmt<QFMT>::fmax) +
+                        (fabsf(y0.y) <= 3.402823466e38f && fabsf(y0.y) > Fmt<QFMT>::fmax) +
+                        (fabsf(y1.x) <= 3.402823466e38f && fabsf(y1.x) > Fmt<QFMT>::fmax) +
+                        (fabsf(y1.y) <= 3.402823466e38f && fabsf(y1.y) > Fmt<QFMT>::fmax);
+            if (nf) {  // the hardware's NaN code is 0x7F whatever the sign
+                uint32_t lo = c[i] & 0xFFFFu, hi = c[i] >> 16;
+                if ((h[2 * i] & 0x7FFFu) > 0x7F80u) lo = (lo & ~0xFFu) | ((h[2 * i] >> 8) & 0x80u) | 0x7Fu;
+                if ((h[2 * i] & 0x7FFF0000u) > 0x7F800000u) lo = (lo & ~0xFF00u) | ((h[2 * i] >> 16) & 0x8000u) | 0x7F00u;
+                if ((h[2 * i + 1] & 0x7FFFu) > 0x7F80u) hi = (hi & ~0xFFu) | ((h[2 * i + 1] >> 8) & 0x80u) | 0x7Fu;
+                if ((h[2 * i + 1] & 0x7FFF0000u) > 0x7F800000u)
+                    hi = (hi & ~0xFF00u) | ((h[2 * i + 1] >> 16) & 0x8000u) | 0x7F00u;
+                c[i] = lo | (hi << 16);
+            }
+        }
+        if (b > 0 && b % NBOX == 0) {
+            bulk_wait_read();
+            __syncwarp();
+        }
+        uint8_t* box = stg + (b % NBOX) * 1024;
+        *(uint4*)(box + r * 32 + ((0 ^ sw) << 4)) = make_uint4(c[0], c[1], c[2], c[3]);
+        *(uint4*)(box + r * 32 + ((1 ^ sw) << 4)) = make_uint4(c[4], c[5], c[6], c[7]);
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0 && (int64_t)x0 + 32 * b < p.N && (int64_t)y0 < p.M) {
+            tma_store_2d(mapQ, x0 + 32 * b, y0, stg_s + (b % NBOX) * 1024);
+            bulk_commit();
+        }
+    }
+    if (row < p.Mp && (int64_t)x0 < p.N) {
+        const int64_t tile = (row / 128) * p.nbn128 + x0 / 128;
+        *(uint32_t*)(p.qscale + tile * 512 + (row % 32) * 16 + ((row % 128) / 32) * 4) = ebytes;
+    }
+}
+
+template <int REC, bool OUT_F32, int QF>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmSFA,
-                 const __grid_constant__ CUtensorMap tmSFB, const Params2 p) {
+                 const __grid_constant__ CUtensorMap tmSFB, const __grid_constant__ CUtensorMap tmQ, const Params2 p) {
     using C = Cfg<REC>;
     constexpr int BN = C::BN, BH = C::BH, STAGES = C::STAGES, NACC = C::NACC, EC = C::EPI_COLS;
     extern __shared__ uint8_t smem_raw[];
@@ -410,6 +504,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // lane quarter take alternate K blocks, running up to STAGES - 1 K
         // blocks past the tile being drained (further would wait on MMAs that
         // wait on this warp's release of the accumulator).
+        uint32_t q_sat = 0, q_nf = 0;  // fused output quantization's counters
         uint64_t g_sf = (uint64_t)j;
         const uint64_t my_tiles = npt > cid ? (uint64_t)((npt - cid + ncl - 1) / ncl) : 0;
         const uint64_t total_kb = my_tiles * (uint64_t)p.nkb;
@@ -461,7 +556,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float vf[EC];
 #pragma unroll
                 for (int i = 0; i < EC; ++i) vf[i] = __uint_as_float(r[i]);
-                store_slice2<OUT_F32, EC, C::STG_WARP / 1024>(&tmD, stg, stg_s, lane, (int)col0, (int)row0, (int)p.N, (int)p.M, vf, sab);
+                if (QF == 0 || p.hasD)
+                    store_slice2<OUT_F32, EC, C::STG_WARP / 1024>(&tmD, stg, stg_s, lane, (int)col0, (int)row0, (int)p.N,
+                                                                  (int)p.M, vf, sab);
+                if constexpr (QF != 0)
+                    store_q<QF - 1, EC, C::STG_WARP / 1024>(&tmQ, stg, stg_s, lane, (int)col0, (int)row0, p, vf, sab,
+                                                            q_sat, q_nf);
             } else {
                 float2 acc[EC / 2];  // packed pairs: Blackwell's two-lane FMA halves the promotion's instructions
 #pragma unroll
@@ -509,11 +609,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (lane == 0) mbar_arrive(sempty(r));
                 }
                 if (!ok) break;
-                store_slice2<OUT_F32, EC, C::STG_WARP / 1024>(&tmD, stg, stg_s, lane, (int)col0, (int)row0, (int)p.N, (int)p.M,
-                                          reinterpret_cast<const float*>(acc), 1.0f);
+                if (QF == 0 || p.hasD)
+                    store_slice2<OUT_F32, EC, C::STG_WARP / 1024>(&tmD, stg, stg_s, lane, (int)col0, (int)row0, (int)p.N,
+                                                                  (int)p.M, reinterpret_cast<const float*>(acc), 1.0f);
+                if constexpr (QF != 0)
+                    store_q<QF - 1, EC, C::STG_WARP / 1024>(&tmQ, stg, stg_s, lane, (int)col0, (int)row0, p,
+                                                            reinterpret_cast<const float*>(acc), 1.0f, q_sat, q_nf);
             }
         }
         if (lane == 0) bulk_wait_all();
+        if constexpr (QF != 0) {
+            q_sat = warp_sum_u32(q_sat);
+            q_nf = warp_sum_u32(q_nf);
+            if (lane == 0) {
+                if (q_sat) atomicAdd(&p.qcounters[0], (unsigned long long)q_sat);
+                if (q_nf) atomicAdd(&p.qcounters[2], (unsigned long long)q_nf);
+            }
+        }
     }
 
     tc_fence_before();
@@ -529,10 +641,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 int g_sms2 = 0;
 
-template <int REC, bool F32>
+template <int REC, bool F32, int QF>
 fp8q_status launch2_t(const CUtensorMap* maps, const Params2& p, cudaStream_t s) {
     using C = Cfg<REC>;
-    auto kern = gemm2_kernel<REC, F32>;
+    auto kern = gemm2_kernel<REC, F32, QF>;
     static bool attr = false;
     if (!attr) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
@@ -568,18 +680,25 @@ fp8q_status launch2_t(const CUtensorMap* maps, const Params2& p, cudaStream_t s)
     }
     const int64_t ncl = npt < max_clusters ? npt : max_clusters;
     cfg.gridDim = dim3((unsigned)(2 * ncl), 1, 1);
-    if (cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], maps[4], p) != cudaSuccess)
+    if (cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p) != cudaSuccess)
         return FP8Q_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? FP8Q_OK : FP8Q_ERR_CUDA;
 }
 
 template <int REC>
-fp8q_status launch2_rec(CUtensorMap* maps, const Params2& p, void* D, int out_dtype, cudaStream_t s) {
+fp8q_status launch2_rec(CUtensorMap* maps, const Params2& p, void* D, int out_dtype, int qfmt, void* qdata,
+                        cudaStream_t s) {
     const bool f32 = out_dtype == 1;
-    if (!make_map_2d(&maps[2], f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, f32 ? 4 : 2,
-                     D, p.M, p.N, f32 ? 8 : 16, 32, CU_TENSOR_MAP_SWIZZLE_32B))
+    if (D != nullptr && !make_map_2d(&maps[2], f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                                     f32 ? 4 : 2, D, p.M, p.N, f32 ? 8 : 16, 32, CU_TENSOR_MAP_SWIZZLE_32B))
         return FP8Q_ERR_CUDA;
-    return f32 ? launch2_t<REC, true>(maps, p, s) : launch2_t<REC, false>(maps, p, s);
+    if (qfmt < 0) return f32 ? launch2_t<REC, true, 0>(maps, p, s) : launch2_t<REC, false, 0>(maps, p, s);
+    // fused MXFP8 output codes: uint8 [M][N] in 32 x 32 boxes (32-byte swizzle)
+    if (f32 || !make_map_2d(&maps[5], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, qdata, p.M, p.N, 32, 32,
+                            CU_TENSOR_MAP_SWIZZLE_32B))
+        return f32 ? FP8Q_ERR_ARG : FP8Q_ERR_CUDA;
+    return qfmt == FP8Q_E4M3 ? launch2_t<REC, false, 1 + FP8Q_E4M3>(maps, p, s)
+                             : launch2_t<REC, false, 1 + FP8Q_E5M2>(maps, p, s);
 }
 
 }  // namespace
@@ -594,7 +713,8 @@ fp8q_status read_device_errors2(unsigned int* flags) {
 }
 
 fp8q_status launch_gemm_pair(const GemmOperand& A, const GemmOperand& B, void* D, int out_dtype, int64_t M,
-                             int64_t N, int64_t K, cudaStream_t s) {
+                             int64_t N, int64_t K, cudaStream_t s, int qfmt, void* qdata, void* qscale,
+                             unsigned long long* qcounters) {
     if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return FP8Q_ERR_SHAPE;
     const bool mx = A.kind == FP8Q_MXFP8_1x32;
     const bool pt = A.kind == FP8Q_PERTENSOR_CURRENT || A.kind == FP8Q_PERTENSOR_DELAYED;
@@ -602,10 +722,15 @@ fp8q_status launch_gemm_pair(const GemmOperand& A, const GemmOperand& B, void* D
                       Cfg<REC_B1D>::BN == Cfg<REC_PT>::BN,
                   "one tile width for every recipe");
     const int bn = Cfg<REC_PT>::BN;
-    CUtensorMap maps[5];
+    CUtensorMap maps[6];
     memset(maps, 0, sizeof(maps));
     Params2 p;
     memset(&p, 0, sizeof(p));
+    p.hasD = D != nullptr;
+    p.qscale = (uint8_t*)qscale;
+    p.qcounters = qcounters;
+    if (qfmt >= 0 && qcounters != nullptr && cudaMemsetAsync(qcounters, 0, 3 * sizeof(unsigned long long), s) != cudaSuccess)
+        return FP8Q_ERR_CUDA;
     p.M = M;
     p.N = N;
     p.K = K;
@@ -630,7 +755,7 @@ fp8q_status launch_gemm_pair(const GemmOperand& A, const GemmOperand& B, void* D
                          CU_TENSOR_MAP_SWIZZLE_NONE))
             return FP8Q_ERR_CUDA;
         p.idesc = shape | fmts | (1u << 23);
-        return launch2_rec<REC_MX>(maps, p, D, out_dtype, s);
+        return launch2_rec<REC_MX>(maps, p, D, out_dtype, qfmt, qdata, s);
     }
     maps[3] = maps[0];
     maps[4] = maps[1];
@@ -638,14 +763,14 @@ fp8q_status launch_gemm_pair(const GemmOperand& A, const GemmOperand& B, void* D
     if (pt) {
         p.sa_inv = A.scale_inv;
         p.sb_inv = B.scale_inv;
-        return launch2_rec<REC_PT>(maps, p, D, out_dtype, s);
+        return launch2_rec<REC_PT>(maps, p, D, out_dtype, qfmt, qdata, s);
     }
     // blockwise scale rows are fetched by bulk copies: 16-byte aligned bases
     if (((uintptr_t)A.scale | (uintptr_t)B.scale) & 15) return FP8Q_ERR_ARG;
     p.bsa = (const float*)A.scale;
     p.bsb = (const float*)B.scale;
-    if (B.kind == FP8Q_BLOCK_128x128) return launch2_rec<REC_B2D>(maps, p, D, out_dtype, s);
-    return launch2_rec<REC_B1D>(maps, p, D, out_dtype, s);
+    if (B.kind == FP8Q_BLOCK_128x128) return launch2_rec<REC_B2D>(maps, p, D, out_dtype, qfmt, qdata, s);
+    return launch2_rec<REC_B1D>(maps, p, D, out_dtype, qfmt, qdata, s);
 }
 
 }  // namespace fp8q

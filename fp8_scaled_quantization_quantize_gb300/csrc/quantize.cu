@@ -105,11 +105,6 @@ __device__ __forceinline__ uint2 convert8(const uint4& v, float k, uint32_t& nsa
     return q;
 }
 
-__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
-    uint32_t r;
-    asm("max.u16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-    return r;
-}
 
 // Per-half maxima of |x| over the 8 bf16 of v, NaN / Inf included (their
 // magnitude bits are >= 0x7F80, so a fold of 0x7F80 or more flags them).

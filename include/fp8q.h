@@ -226,6 +226,26 @@ FP8Q_API fp8q_status fp8q_scaled_gemm(const fp8q_tensor* A, int a_use_col, const
                              void* D, int out_dtype, int64_t M, int64_t N, int64_t K, void* stream);
 
 /*
+ * fp8q_scaled_gemm with the next quantize fused into its epilogue: the GEMM's
+ * bf16 output (as fp8q_scaled_gemm would store it) is also quantized with the
+ * MXFP8 1x32 recipe along its rows ([guide] sec. 2.3 and 3.1: a GEMM's output
+ * is the next layer's input; [nemo] strategy 4), so that Dq->data_row,
+ * Dq->scale_row and Dq->counters ([0] saturated, [1] 0, [2] NaN / Inf) equal
+ * what fp8q_quantize(MXFP8_1x32, fmt, row-wise only) of that bf16 D writes.
+ * D (bf16 [M][N]) may be NULL: then only the quantized output is written.
+ * Dq is caller-owned: data_row uint8 [M][N], scale_row of
+ * fp8q_scale_bytes(MXFP8_1x32, M, N) bytes, counters uint64[3]; its rows /
+ * cols / fmt / kind are filled in (data_col / scale_col / amax / scale /
+ * scale_inv are not used).  Constraints as fp8q_scaled_gemm plus N % 32 == 0
+ * and 16-byte aligned Dq buffers.  Runs on the SM-pair kernel whatever
+ * fp8q_gemm_set_variant chose.  This entry point has no counterpart on the
+ * pages: they describe the quantize and the GEMM as separate steps.
+ */
+FP8Q_API fp8q_status fp8q_scaled_gemm_mxq(const fp8q_tensor* A, int a_use_col, const fp8q_tensor* B, int b_use_col,
+                                 void* D, int fmt, fp8q_tensor* Dq, int64_t M, int64_t N, int64_t K,
+                                 void* stream);
+
+/*
  * Chooses the GEMM kernel for subsequent fp8q_scaled_gemm calls (process
  * wide): 0 automatic (default: SM pairs once the problem has at least 64
  * tiles of 256 x 256 and, for blockwise scales, both scale arrays are

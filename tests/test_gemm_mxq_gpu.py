@@ -1,0 +1,122 @@
+"""GEMM with the next quantize fused into its epilogue (fp8q_scaled_gemm_mxq).
+
+The fused output must be exactly what the quantize step would make of the
+GEMM's bf16 output: the oracle quantizes the kernel's own bf16 D with the
+MXFP8 1x32 recipe ("2025 FP8 quantized-training guide", sec. 2.3) and every
+code, packed E8M0 scale byte and counter must match.  D itself is the plain
+SM-pair GEMM's D bit for bit, and without D the quantized output is the same.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from fp8_scaled_quantization_quantize_gb300 import inputs
+from _helpers import assert_quant_equal, gpu_outputs
+
+pytestmark = pytest.mark.gpu
+
+
+def _api():
+    from fp8_scaled_quantization_quantize_gb300 import api
+    return api
+
+
+# name, kind A, kind B, format A, format B
+RECIPES = [
+    ("pertensor", 0, 0, O.E4M3, O.E4M3),
+    ("mxfp8", 4, 4, O.E4M3, O.E4M3),
+    ("block_1x128_128x128", 2, 3, O.E4M3, O.E4M3),
+    ("block_1x128_1x128", 2, 2, O.E4M3, O.E4M3),
+]
+
+
+def _operands(api, kA, kB, fA, fB, M, N, K, seed):
+    a = inputs.normal_bf16((M, K), seed)
+    b = inputs.normal_bf16((N, K), seed + 1, 0.02)
+    qa = api.quantize(a.cuda(), kA, fA, True, False)
+    qb = api.quantize(b.cuda(), kB, fB, True, False)
+    return qa, qb
+
+
+def _check_fused(api, qa, qb, fmt, ctx):
+    D, Dq = api.scaled_gemm_mxq(qa, False, qb, False, fmt, want_d=True)
+    torch.cuda.synchronize()
+    got = gpu_outputs(Dq)
+    ref = O.quantize(O.MXFP8_1x32, fmt, inputs.bf16_bits(D.cpu()), True, False)
+    assert_quant_equal(O.MXFP8_1x32, got, ref, True, False, ctx)
+    return D, Dq, got
+
+
+@pytest.mark.parametrize("name,kA,kB,fA,fB", RECIPES, ids=[r[0] for r in RECIPES])
+@pytest.mark.parametrize("M,N,K", [(256, 512, 256), (208, 288, 400), (384, 800, 528), (640, 1024, 1040)])
+@pytest.mark.parametrize("fmt", [O.E4M3, O.E5M2])
+def test_fused_output_quantize_matches_quantize_of_d(name, kA, kB, fA, fB, M, N, K, fmt):
+    api = _api()
+    qa, qb = _operands(api, kA, kB, fA, fB, M, N, K, 60 + M)
+    D, Dq, got = _check_fused(api, qa, qb, fmt, f"{name} {M}x{N}x{K} fmt={fmt}")
+    # D is the plain SM-pair GEMM's D
+    api.gemm_set_variant(2)
+    try:
+        D2 = api.scaled_gemm(qa, False, qb, False)
+        torch.cuda.synchronize()
+    finally:
+        api.gemm_set_variant(0)
+    assert torch.equal(D.view(torch.int16), D2.view(torch.int16)), "fused D differs from the GEMM's D"
+    # and without D the quantized output is the same
+    none, Dq2 = api.scaled_gemm_mxq(qa, False, qb, False, fmt, want_d=False)
+    torch.cuda.synchronize()
+    assert none is None
+    got2 = gpu_outputs(Dq2)
+    assert np.array_equal(got2["data_row"], got["data_row"])
+    assert np.array_equal(got2["scale_row_bytes"], got["scale_row_bytes"])
+    assert (got2["sat_row"], got2["nonfinite"]) == (got["sat_row"], got["nonfinite"])
+    assert api.device_errors() == 0
+
+
+def test_fused_output_counts_saturation():
+    """MXFP8 blocks whose scaled maximum lands in (448, 512) saturate: a
+    typical N(0,1) product has many; the count must equal the oracle's."""
+    api = _api()
+    qa, qb = _operands(api, 4, 4, O.E4M3, O.E4M3, 512, 1024, 512, 5)
+    _, _, got = _check_fused(api, qa, qb, O.E4M3, "saturation")
+    assert got["sat_row"] > 0
+
+
+def test_fused_output_of_overflowing_d():
+    """A per-tensor GEMM whose fp32 result overflows: D is +-Inf in bf16, every
+    element is counted as nonfinite and encodes to +-448 (satfinite), and the
+    blocks' finite maximum is 0 (E8M0 127)."""
+    api = _api()
+    M, N, K = 256, 256, 128
+    big = torch.full((M, K), 1e30, dtype=torch.bfloat16)
+    qa = api.quantize(big.cuda(), 0, O.E4M3, True, False)
+    qb = api.quantize(big[:N].clone().cuda(), 0, O.E4M3, True, False)
+    D, Dq, got = _check_fused(api, qa, qb, O.E4M3, "overflow")
+    assert torch.isinf(D.float()).all()
+    assert got["nonfinite"] == M * N
+
+
+def test_fused_output_llama8b_fprop_sampled_rows():
+    """The Llama-3-8B MLP fprop shape (MXFP8 X [8192x4096] . W^T [14336x4096]):
+    the fused codes and scales of 64 sampled rows against the oracle's quantize
+    of those rows of the kernel's D."""
+    api = _api()
+    X, W, _ = inputs.llama8b_mlp()
+    qx = api.quantize(X.cuda(), 4, O.E4M3, True, False)
+    qw = api.quantize(W.cuda(), 4, O.E4M3, True, False)
+    D, Dq = api.scaled_gemm_mxq(qx, False, qw, False, O.E4M3, want_d=True)
+    torch.cuda.synchronize()
+    rows = np.sort(np.random.default_rng(3).choice(8192, 64, replace=False))
+    Dr = D[torch.as_tensor(rows, device=D.device)].cpu()
+    ref = O.quantize(O.MXFP8_1x32, O.E4M3, inputs.bf16_bits(Dr), True, False)
+    assert np.array_equal(Dq.data_row[torch.as_tensor(rows, device=D.device)].cpu().numpy(), ref["data_row"])
+    # scale bytes of the sampled rows from the packed tiles: row r, scale column k
+    sb = Dq.scale_row.cpu().numpy()
+    S = 14336 // 32
+    tiles_c = 14336 // 128
+    k = np.arange(S)[None, :]
+    r = rows[:, None]
+    off = ((r // 128) * tiles_c + k // 4) * 512 + (r % 32) * 16 + ((r % 128) // 32) * 4 + k % 4
+    assert np.array_equal(sb[off], ref["scale_row"])
+    assert api.device_errors() == 0
