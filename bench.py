@@ -332,8 +332,36 @@ def run_ours(args):
               "quantize_gbs": round(qb3 / qms / 1e6, 1),
               "quantize_frac_of_hbm": round(qb3 / qms / 1e6 / hbm_peak, 3),
               "ms_per_step": round(sms, 4)}
+        # the fprop with the next layer's MXFP8 quantize of Y fused into its
+        # epilogue, against the GEMM followed by the quantize kernel on Y
+        qy = api.alloc(api.MXFP8_1x32, api.E4M3, T3, F, True, False, dev)
+
+        def sep():
+            api.scaled_gemm(q3[0], False, q3[1], False, out=outs[0], stream=stream)
+            api.quantize_into(outs[0], qy, stream=stream)
+
+        def fused(with_d):
+            api.scaled_gemm_mxq(q3[0], False, q3[1], False, api.E4M3, want_d=with_d, out=qy,
+                                d_out=outs[0] if with_d else None, stream=stream)
+
+        fus = {}
+        for name, fn in (("gemm_then_quantize", sep), ("fused_with_bf16_y", lambda: fused(True)),
+                         ("fused_fp8_only", lambda: fused(False))):
+            for _ in range(args.warmup):
+                flush.zero_()
+                fn()
+            evs_f = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+            for i in range(args.steps):
+                flush.zero_()
+                evs_f[i][0].record()
+                fn()
+                evs_f[i][1].record()
+            torch.cuda.synchronize()
+            fus[name] = round(statistics.mean(e[0].elapsed_time(e[1]) for e in evs_f), 4)
+        mx["fprop_next_quantize_ms"] = fus
+        mx["fprop_fused_tflops"] = round(f3 / fus["fused_fp8_only"] / 1e9, 1)
         errs |= api.device_errors()
-        launches += 6 * args.steps
+        launches += 6 * args.steps + 4 * args.steps
 
     value = world * flops / ms_step / 1e9
     gemm_tflops = flops / g_avg / 1e9

@@ -3,19 +3,20 @@
 // Same arithmetic as gemm.cu ("2025 FP8 quantized-training guide", sec. 2.1-2.3
 // and 3.1): D = A_q . B_q^T with per-tensor, MXFP8 (block-scaled MMA) or
 // blockwise (per-128-K partials scaled in the epilogue) scales.  A cluster of
-// two CTAs on two SMs computes a 256 x BN tile: CTA r loads rows
-// 256 mp + 128 r of A and rows BN nb + (BN / 2) r of B, and the leader CTA
-// (r = 0) issues each MMA for both, so every SM streams half of the B panel
-// it would need alone and each shared-memory stage is a third smaller.
+// two CTAs on two SMs computes a 256 x BN tile (BN = 256): CTA r
+// loads rows 256 mp + 128 r of A and rows BN nb + (BN / 2) r of B, and the
+// leader CTA (r = 0) issues each MMA for both, so every SM streams half of the
+// B panel it would need alone and each shared-memory stage is a third smaller.
 //
-// Per CTA, 320 threads: warp 0 TMA producer (its halves, completing on the
-// leader's barriers), warp 1 TMEM allocation (with the peer) and, in the
-// leader, the single-thread MMA issuer; warps 2-9 the epilogue of the CTA's
-// own 128 rows (TMEM lanes 32 (w % 4) .., columns 128 ((w - 2) / 4) ..),
-// which releases TMEM on the leader's barrier and stores D by TMA.  Eight
-// epilogue warps of 128 columns (not sixteen of 64) halve the per-K-block
-// handshakes the blockwise promotion issues on the schedulers it shares with
-// the MMA and TMA threads.
+// Per CTA: warp 0 TMA producer (its halves, completing on the leader's
+// barriers), warp 1 TMEM allocation (with the peer) and, in the leader, the
+// single-thread MMA issuer; then the epilogue warps for the CTA's own 128
+// rows (TMEM lanes 32 (w % 4) .., columns EC ((w - 2) / 4) ..), which release
+// TMEM on the leader's barrier and store D by TMA: eight warps of 128
+// columns (320 threads).  Blockwise: with two K-block partial buffers the
+// MMAs of K block g + 2 wait for the epilogue to release block g, which is
+// what limits this recipe (measured: about 445 cycles from a partial's
+// arrival to its release against about 600 cycles of MMAs per K block).
 // TMEM per CTA: per-tensor two 256-column accumulators; MXFP8 one accumulator
 // plus 12 scale columns per stage; blockwise two 256-column partial buffers,
 // so the MMAs run one K block ahead of the epilogue.
@@ -35,21 +36,25 @@ __device__ unsigned int g_device_errors2 = 0;
 namespace {
 
 constexpr int BM = 128, BK = 128;
-constexpr int kEpiWarps = 8;  // two per TMEM lane quarter, 128 columns each
-constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr uint64_t kWaitNs = 1000000000ull;
 enum { REC_PT = 0, REC_MX = 1, REC_B2D = 2, REC_B1D = 3 };
 
 template <int REC>
 struct Cfg {
     static constexpr bool BLOCKWISE = REC == REC_B2D || REC == REC_B1D;
-    static constexpr int BN = 256;     // pair tile columns
+    // pair tile columns and epilogue warps (two per TMEM lane quarter).  The
+    // code also runs blockwise tiles of 192 columns with twelve warps of 64
+    // columns, which measured slower (0.50 vs 0.63 of peak at the Llama-3-8B
+    // up-projection)
+    static constexpr int BN = 256;
     static constexpr int BH = BN / 2;  // B rows per CTA
+    static constexpr int EPI_WARPS = 8;
+    static constexpr int THREADS = 64 + 32 * EPI_WARPS;
     static constexpr int STAGES = BLOCKWISE ? 4 : 5;
     static constexpr int NACC = (REC == REC_MX) ? 1 : 2;  // TMEM accumulators (blockwise: K-block partials)
-    static constexpr int EPI_COLS = BN / (kEpiWarps / 4);
+    static constexpr int EPI_COLS = BN / (EPI_WARPS / 4);
     // blockwise scales ring: per K block, this CTA's 128 A-row scales (512 B)
-    // and the tile's B scales (two floats for 128x128 blocks, 256 for 1x128);
+    // and the tile's B scales (two floats for 128x128 blocks, BN for 1x128);
     // deep enough that the producer is never held back by the epilogue
     static constexpr int SR = BLOCKWISE ? STAGES + NACC + 2 : 0;
     static constexpr uint32_t SLOT = 512 + 4 * BN;
@@ -61,7 +66,7 @@ struct Cfg {
     static constexpr uint32_t OFF_SCL = OFF_SFB + (REC == REC_MX ? STAGES * 1024 : 0);
     static constexpr uint32_t OFF_STG = OFF_SCL + SR * SLOT;
     static constexpr uint32_t STG_WARP = 4096;  // four 1 KB output boxes per epilogue warp
-    static constexpr uint32_t OFF_BAR = OFF_STG + kEpiWarps * STG_WARP;
+    static constexpr uint32_t OFF_BAR = OFF_STG + EPI_WARPS * STG_WARP;
     static constexpr int NSFB = (REC == REC_MX) ? STAGES : 0;  // MXFP8 scale-tile barriers per kind
     static constexpr uint32_t NBARS = 2 * STAGES + 2 * NACC + 1 + 2 * SR + 2 * NSFB;
     static constexpr uint32_t OFF_MISC = OFF_BAR + 8 * NBARS;
@@ -217,12 +222,13 @@ __device__ __forceinline__ void store_slice2(const CUtensorMap* mapD, uint8_t* s
 // row path ("2025 FP8 quantized-training guide", sec. 2.3) on these values.
 // Codes leave through the staging boxes by TMA (uint8 32 x 32 boxes, 32-byte
 // swizzle); each row's four scale bytes of a 128-column group go to the packed
-// 128x4 tile layout.  Blocks past N and rows past M are not counted; scale
-// rows up to Mp are written (rows past M hold zeros: code 127, the pad).
+// 128x4 tile layout.  Blocks past N and rows past M are not counted; scales
+// are written for rows up to Mp and columns up to Np (blocks past M or N get
+// code 127, the pad).
 template <int QFMT, int COLS, int NBOX>
 __device__ __forceinline__ void store_q(const CUtensorMap* mapQ, uint8_t* stg, uint32_t stg_s, int lane, int x0, int y0,
                                         const Params2& p, const float* v, float scale, uint32_t& nsat, uint32_t& nnf) {
-    static_assert(COLS == 128, "one 128-column scale group per warp slice");
+    static_assert(COLS == 128 || COLS == 64, "a slice is all or half of one 128-column scale group");
     const int r = lane, sw = (r >> 2) & 1;
     const int64_t row = (int64_t)y0 + r;
     const bool row_live = row < p.M;
@@ -293,14 +299,18 @@ __device__ __forceinline__ void store_q(const CUtensorMap* mapQ, uint8_t* stg, u
             bulk_commit();
         }
     }
-    if (row < p.Mp && (int64_t)x0 < p.N) {
+    if (row < p.Mp && (int64_t)x0 < p.Np) {  // pads of the last 128-column group included (code 127)
         const int64_t tile = (row / 128) * p.nbn128 + x0 / 128;
-        *(uint32_t*)(p.qscale + tile * 512 + (row % 32) * 16 + ((row % 128) / 32) * 4) = ebytes;
+        uint8_t* dst = p.qscale + tile * 512 + (row % 32) * 16 + ((row % 128) / 32) * 4 + (x0 % 128) / 32;
+        if (COLS == 128)
+            *(uint32_t*)dst = ebytes;
+        else
+            *(uint16_t*)dst = (uint16_t)ebytes;
     }
 }
 
 template <int REC, bool OUT_F32, int QF>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<REC>::THREADS, 1)
     gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmSFA,
                  const __grid_constant__ CUtensorMap tmSFB, const __grid_constant__ CUtensorMap tmQ, const Params2 p) {
@@ -333,12 +343,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int b = 0; b < NACC; ++b) {
             mbar_init(tfull(b), 1);
-            mbar_init(tempty(b), 2 * kEpiWarps);
+            mbar_init(tempty(b), 2 * C::EPI_WARPS);
         }
         mbar_init(mma_done, 1);
         for (int r = 0; r < C::SR; ++r) {
             mbar_init(sfull(r), REC == REC_B2D ? 2 : 1);
-            mbar_init(sempty(r), kEpiWarps);
+            mbar_init(sempty(r), C::EPI_WARPS);
         }
         for (int st = 0; st < C::NSFB; ++st) {
             mbar_init(sfl(st), 1);
@@ -407,9 +417,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mbar_expect_tx(sfull(r), (arow ? 512u : 0u) + (REC == REC_B1D ? bbytes : 0u));
                         if (arow) bulk_load(dst, p.bsa + kb * p.Mp + rs, 512, sfull(r));
                         if (REC == REC_B1D) bulk_load(dst + 512, p.bsb + kb * p.Np + nb * BN, bbytes, sfull(r));
-                        if (REC == REC_B2D) {  // the scales of the tile's two 128-column B blocks
-                            cp_async_4(dst + 512, p.bsb + (2 * nb) * p.nkb + kb);
-                            if (2 * nb + 1 < p.nbn128) cp_async_4(dst + 516, p.bsb + (2 * nb + 1) * p.nkb + kb);
+                        if (REC == REC_B2D) {  // the scales of the (at most two) 128-column B blocks of the tile
+                            const int64_t b0 = (nb * BN) / 128;
+                            cp_async_4(dst + 512, p.bsb + b0 * p.nkb + kb);
+                            if (b0 + 1 < p.nbn128) cp_async_4(dst + 516, p.bsb + (b0 + 1) * p.nkb + kb);
                             cp_async_arrive(sfull(r));
                         }
                         ++kbp;
@@ -575,7 +586,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     const float* scl = (const float*)(smem + C::OFF_SCL + r * C::SLOT);
                     const float sa = scl[32 * q + lane];
-                    const float sc = (REC == REC_B2D) ? __fmul_rn(sa, scl[128 + (EC * j) / 128]) : 0.0f;
+                    // this warp's 64-column slice lies in one 128-column B block
+                    const float sc = (REC == REC_B2D) ? __fmul_rn(sa, scl[128 + (int)((nb * BN + EC * j) / 128 - (nb * BN) / 128)]) : 0.0f;
                     const uint32_t buf = kbg % NACC;
                     if (!mbar_wait2(tfull(buf), (kbg / NACC) & 1u, abort_flag)) {
                         ok = false;
@@ -660,7 +672,7 @@ fp8q_status launch2_t(const CUtensorMap* maps, const Params2& p, cudaStream_t s)
     const int64_t npt = p.tiles_m2 * p.tiles_n;
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof(cfg));
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3(C::THREADS, 1, 1);
     cfg.dynamicSmemBytes = C::SMEM;
     cfg.stream = s;
     cudaLaunchAttribute la[1];
@@ -718,10 +730,8 @@ fp8q_status launch_gemm_pair(const GemmOperand& A, const GemmOperand& B, void* D
     if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return FP8Q_ERR_SHAPE;
     const bool mx = A.kind == FP8Q_MXFP8_1x32;
     const bool pt = A.kind == FP8Q_PERTENSOR_CURRENT || A.kind == FP8Q_PERTENSOR_DELAYED;
-    static_assert(Cfg<REC_MX>::BN == Cfg<REC_PT>::BN && Cfg<REC_B2D>::BN == Cfg<REC_PT>::BN &&
-                      Cfg<REC_B1D>::BN == Cfg<REC_PT>::BN,
-                  "one tile width for every recipe");
-    const int bn = Cfg<REC_PT>::BN;
+    static_assert(Cfg<REC_MX>::BN == Cfg<REC_PT>::BN && Cfg<REC_B2D>::BN == Cfg<REC_B1D>::BN, "tile widths");
+    const int bn = (mx || pt) ? Cfg<REC_PT>::BN : Cfg<REC_B2D>::BN;
     CUtensorMap maps[6];
     memset(maps, 0, sizeof(maps));
     Params2 p;
