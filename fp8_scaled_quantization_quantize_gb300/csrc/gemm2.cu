@@ -175,9 +175,14 @@ __device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sy
 // 1 KB boxes of 32-byte row pieces (32-byte swizzle: chunk c of row r at
 // r*32 + (c ^ ((r / 4) % 2))*16); waits for the staging to be read out each
 // time all NBOX boxes are in flight.
-template <bool OUT_F32, int COLS, int NBOX>
+struct NoPoll {
+    __device__ __forceinline__ void operator()() const {}
+};
+
+template <bool OUT_F32, int COLS, int NBOX, typename Poll = NoPoll>
 __device__ __forceinline__ void store_slice2(const CUtensorMap* mapD, uint8_t* stg, uint32_t stg_s, int lane, int x0,
-                                             int y0, int n_extent, int m_extent, const float* v, float scale) {
+                                             int y0, int n_extent, int m_extent, const float* v, float scale,
+                                             const Poll& poll = Poll()) {
     constexpr int kPiece = OUT_F32 ? 8 : 16;  // columns per 32-byte row piece
     constexpr int kBoxes = COLS / kPiece;
     const int r = lane, sw = (r >> 2) & 1;
@@ -211,6 +216,7 @@ __device__ __forceinline__ void store_slice2(const CUtensorMap* mapD, uint8_t* s
             tma_store_2d(mapD, x0 + kPiece * bx, y0, stg_s + (bx % NBOX) * 1024);
             bulk_commit();
         }
+        poll();
     }
 }
 
@@ -225,9 +231,10 @@ __device__ __forceinline__ void store_slice2(const CUtensorMap* mapD, uint8_t* s
 // 128x4 tile layout.  Blocks past N and rows past M are not counted; scales
 // are written for rows up to Mp and columns up to Np (blocks past M or N get
 // code 127, the pad).
-template <int QFMT, int COLS, int NBOX>
+template <int QFMT, int COLS, int NBOX, typename Poll = NoPoll>
 __device__ __forceinline__ void store_q(const CUtensorMap* mapQ, uint8_t* stg, uint32_t stg_s, int lane, int x0, int y0,
-                                        const Params2& p, const float* v, float scale, uint32_t& nsat, uint32_t& nnf) {
+                                        const Params2& p, const float* v, float scale, uint32_t& nsat, uint32_t& nnf,
+                                        const Poll& poll = Poll()) {
     static_assert(COLS == 128 || COLS == 64, "a slice is all or half of one 128-column scale group");
     const int r = lane, sw = (r >> 2) & 1;
     const int64_t row = (int64_t)y0 + r;
@@ -298,6 +305,7 @@ __device__ __forceinline__ void store_q(const CUtensorMap* mapQ, uint8_t* stg, u
             tma_store_2d(mapQ, x0 + 32 * b, y0, stg_s + (b % NBOX) * 1024);
             bulk_commit();
         }
+        poll();
     }
     if (row < p.Mp && (int64_t)x0 < p.Np) {  // pads of the last 128-column group included (code 127)
         const int64_t tile = (row / 128) * p.nbn128 + x0 / 128;
@@ -520,6 +528,20 @@ __global__ void __launch_bounds__(Cfg<REC>::THREADS, 1)
         const uint64_t my_tiles = npt > cid ? (uint64_t)((npt - cid + ncl - 1) / ncl) : 0;
         const uint64_t total_kb = my_tiles * (uint64_t)p.nkb;
         bool sf_ok = true;
+        auto move_one_sf = [&](int st) {  // stage st's scale tiles have landed: into TMEM
+            const uint4 sa4 = *(const uint4*)(smem + C::OFF_SFA + st * 512 + lane * 16);
+            const uint4 sb0 = *(const uint4*)(smem + C::OFF_SFB + st * 1024 + lane * 16);
+            const uint4 sb1 = *(const uint4*)(smem + C::OFF_SFB + st * 1024 + 512 + lane * 16);
+            const uint32_t sft = tmem + lane_base + SF_TMEM_COL + 12u * st;
+            tc_st_x4(sft, sa4);
+            tc_st_x4(sft + 4, sb0);
+            tc_st_x4(sft + 8, sb1);
+            tc_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_remote(mapa(sfr(st), 0));
+            g_sf += 2;
+        };
         auto move_sf_upto = [&](uint64_t limit) {
             if constexpr (REC == REC_MX) {
                 while (sf_ok && g_sf < limit) {
@@ -528,18 +550,18 @@ __global__ void __launch_bounds__(Cfg<REC>::THREADS, 1)
                         sf_ok = false;
                         break;
                     }
-                    const uint4 sa4 = *(const uint4*)(smem + C::OFF_SFA + st * 512 + lane * 16);
-                    const uint4 sb0 = *(const uint4*)(smem + C::OFF_SFB + st * 1024 + lane * 16);
-                    const uint4 sb1 = *(const uint4*)(smem + C::OFF_SFB + st * 1024 + 512 + lane * 16);
-                    const uint32_t sft = tmem + lane_base + SF_TMEM_COL + 12u * st;
-                    tc_st_x4(sft, sa4);
-                    tc_st_x4(sft + 4, sb0);
-                    tc_st_x4(sft + 8, sb1);
-                    tc_wait_st();
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive_remote(mapa(sfr(st), 0));
-                    g_sf += 2;
+                    move_one_sf(st);
+                }
+            }
+        };
+        // while the warp drains and stores a tile: move the next K block's
+        // scale tiles if they have landed (never waits), so the MMAs of the
+        // next tile do not stall on them behind this tile's stores
+        auto poll_sf = [&]() {
+            if constexpr (REC == REC_MX) {
+                if (sf_ok && g_sf < total_kb) {
+                    const int st = (int)(g_sf % STAGES);
+                    if (__all_sync(0xffffffffu, mbar_try(sfl(st), (uint32_t)((g_sf / STAGES) & 1u)))) move_one_sf(st);
                 }
             }
         };
@@ -569,10 +591,10 @@ __global__ void __launch_bounds__(Cfg<REC>::THREADS, 1)
                 for (int i = 0; i < EC; ++i) vf[i] = __uint_as_float(r[i]);
                 if (QF == 0 || p.hasD)
                     store_slice2<OUT_F32, EC, C::STG_WARP / 1024>(&tmD, stg, stg_s, lane, (int)col0, (int)row0, (int)p.N,
-                                                                  (int)p.M, vf, sab);
+                                                                  (int)p.M, vf, sab, poll_sf);
                 if constexpr (QF != 0)
                     store_q<QF - 1, EC, C::STG_WARP / 1024>(&tmQ, stg, stg_s, lane, (int)col0, (int)row0, p, vf, sab,
-                                                            q_sat, q_nf);
+                                                            q_sat, q_nf, poll_sf);
             } else {
                 float2 acc[EC / 2];  // packed pairs: Blackwell's two-lane FMA halves the promotion's instructions
 #pragma unroll
