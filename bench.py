@@ -518,6 +518,26 @@ def run_modes(args):
     elif args.mode == "gemm":
         print(json.dumps(gemm_point(KINDS[args.kind], args.M, args.N, args.K, args.steps, args.warmup, flush,
                                     args.out)), flush=True)
+    elif args.mode == "qerror":  # quantization error per recipe (analysis, not timed)
+        from fp8_scaled_quantization_quantize_gb300 import api, inputs, qerror
+        X, W = inputs.llama8b_up_proj()
+        data = [("cfg2 X 4096x4096, 1% columns x100", X, api.E4M3), ("cfg2 W 14336x4096 N(0,0.02^2)", W, api.E4M3),
+                ("cfg5 64 MiB N(0,1), 0.1% elements x1000", inputs.sweep_tensor(64), api.E4M3),
+                ("cfg3 dY 8192x14336 N(0,1e-4^2)", inputs.normal_bf16((8192, 14336), 2, 1e-4), api.E4M3),
+                ("cfg3 dY 8192x14336 N(0,1e-4^2)", inputs.normal_bf16((8192, 14336), 2, 1e-4), api.E5M2)]
+        for name, x, fmt in data:
+            xd = x.cuda()
+            base = None
+            for kind in (0, 2, 3, 4):
+                qt = api.quantize(xd, kind, fmt, True, False)
+                e = qerror.error(xd.float(), qerror.dequantize_rowwise(qt))
+                base = e["rel_err"] if kind == 0 else base
+                print(json.dumps({"mode": "qerror", "data": name, "fmt": "e4m3" if fmt == api.E4M3 else "e5m2",
+                                  "recipe": [k for k, v in KINDS.items() if v == kind][0],
+                                  "rel_err": round(e["rel_err"], 6), "sqnr_db": round(e["sqnr_db"], 2),
+                                  "vs_pertensor": round(e["rel_err"] / base, 3),
+                                  "saturated": int(qt.counters[0].item())}), flush=True)
+            del xd
     else:  # sweep: the roofline sweep workload
         for mib in (16, 32, 64, 128, 256, 512, 1024, 2048):
             rows = mib * 2 ** 20 // 2 // 4096
@@ -598,8 +618,9 @@ def main():
     ap.add_argument("--skip-mx", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
-    ap.add_argument("--mode", choices=["step", "quantize", "gemm", "sweep"], default="step",
-                    help="step: the benchmark line (default); quantize / gemm: one kernel; sweep: roofline sweep")
+    ap.add_argument("--mode", choices=["step", "quantize", "gemm", "sweep", "qerror"], default="step",
+                    help="step: the benchmark line (default); quantize / gemm: one kernel; sweep: roofline sweep; "
+                         "qerror: quantization error per recipe")
     ap.add_argument("--kind", choices=list(KINDS), default="mx")
     ap.add_argument("--rows", type=int, default=16384)
     ap.add_argument("--cols", type=int, default=8192)
