@@ -518,6 +518,44 @@ def run_modes(args):
     elif args.mode == "gemm":
         print(json.dumps(gemm_point(KINDS[args.kind], args.M, args.N, args.K, args.steps, args.warmup, flush,
                                     args.out)), flush=True)
+    elif args.mode == "delayed70b":  # cfg 4: delayed hybrid scaling, Llama-3-70B FFN, 3 GEMMs per step
+        from fp8_scaled_quantization_quantize_gb300 import api, inputs
+        bases = inputs.llama70b_ffn_bases()
+        mags = inputs.delayed_magnitudes()
+        steps_t = [tuple(t.cuda() for t in inputs.llama70b_ffn_step(t, bases, mags)) for t in range(4)]
+        T4, H4 = steps_t[0][0].shape
+        F4 = steps_t[0][1].shape[0]
+        fmts = (api.E4M3, api.E4M3, api.E5M2)
+        states = [api.DelayedState(16, f, 0) for f in fmts]
+        qs = [api.alloc(api.PERTENSOR_DELAYED, f, *steps_t[0][i].shape, True, True, "cuda") for i, f in enumerate(fmts)]
+        outs = [torch.empty(sh, dtype=torch.bfloat16, device="cuda") for sh in ((T4, F4), (T4, H4), (F4, H4))]
+        stream = torch.cuda.current_stream()
+
+        def one(t):
+            for x, q, st in zip(steps_t[t % 4], qs, states):
+                api.quantize_into(x, q, st, stream=stream)   # casts with the history's scale, then updates it
+            api.scaled_gemm(qs[0], False, qs[1], False, out=outs[0], stream=stream)   # fprop
+            api.scaled_gemm(qs[2], False, qs[1], True, out=outs[1], stream=stream)    # dgrad
+            api.scaled_gemm(qs[2], True, qs[0], True, out=outs[2], stream=stream)     # wgrad
+
+        for i in range(args.warmup):
+            flush.zero_()
+            one(i)
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+        for i in range(args.steps):
+            flush.zero_()
+            ev[i][0].record()
+            one(i)
+            ev[i][1].record()
+        torch.cuda.synchronize()
+        ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+        flops = 3 * 2.0 * T4 * F4 * H4
+        print(json.dumps({"mode": "delayed70b", "workload": "per-tensor delayed, E4M3 X/W + E5M2 dY, Llama-3-70B "
+                          "FFN (tokens 4096, hidden 8192, ffn 28672): quantize + history update of X, W, dY (both "
+                          "copies) + fprop, dgrad, wgrad", "ms_per_step": round(ms, 4),
+                          "tflops": round(flops / ms / 1e9, 1),
+                          "frac_of_fp8_peak": round(flops / ms / 1e9 / (2.0 * peaks()[1]), 3),
+                          "device_errors": api.device_errors()}), flush=True)
     elif args.mode == "qerror":  # quantization error per recipe (analysis, not timed)
         from fp8_scaled_quantization_quantize_gb300 import api, inputs, qerror
         X, W = inputs.llama8b_up_proj()
@@ -618,9 +656,9 @@ def main():
     ap.add_argument("--skip-mx", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
-    ap.add_argument("--mode", choices=["step", "quantize", "gemm", "sweep", "qerror"], default="step",
+    ap.add_argument("--mode", choices=["step", "quantize", "gemm", "sweep", "qerror", "delayed70b"], default="step",
                     help="step: the benchmark line (default); quantize / gemm: one kernel; sweep: roofline sweep; "
-                         "qerror: quantization error per recipe")
+                         "qerror: quantization error per recipe; delayed70b: the delayed-scaling 70B FFN step")
     ap.add_argument("--kind", choices=list(KINDS), default="mx")
     ap.add_argument("--rows", type=int, default=16384)
     ap.add_argument("--cols", type=int, default=8192)
