@@ -12,6 +12,14 @@ The recipes follow the four web pages on FP8 training:
   * "mastering FP8 LLM training 1.5x speedup", scaling strategies 1-4;
   * bjdmk.com.cn/news/5220490, sec. 3.3 (DelayedScaling margin / interval).
 
+Per-channel current scaling ("mastering FP8 LLM training 1.5x speedup",
+Figure 1 and its discussion: one scaling factor per channel, i.e. per row or
+column, between per-tensor and 2D blocks in granularity) is read as the
+per-tensor current rule applied to each row of x (row-wise copy) and to each
+column of x (column-wise copy), so that a copy's factor is constant along the
+contraction dimension of the GEMM it feeds.  Its stored dequantization factor
+is RN(1 / s), the per-tensor recipe's scale_inv, one per row of the copy.
+
 The column-wise copy is the quantized transpose: for per-tensor and 128x128
 tiles it is the byte transpose of the row-wise copy (same scales, transposed
 for tiles); for 1x128 and 1x32 blocks it is a re-quantization of x^T with the
@@ -33,7 +41,7 @@ E4M3, E5M2 = 0, 1
 FMAX = {E4M3: 448.0, E5M2: 57344.0}
 
 # recipe kinds (the oracle's own numbering)
-PERTENSOR_CURRENT, PERTENSOR_DELAYED, BLOCK_1x128, BLOCK_128x128, MXFP8_1x32 = range(5)
+PERTENSOR_CURRENT, PERTENSOR_DELAYED, BLOCK_1x128, BLOCK_128x128, MXFP8_1x32, PERCHANNEL_CURRENT = range(6)
 KIND_MULT, KIND_DIV, KIND_POW2 = 0, 1, 2
 
 
@@ -234,6 +242,15 @@ def pack_block1x128(d: np.ndarray) -> np.ndarray:
     return out
 
 
+def pad128(v: np.ndarray) -> np.ndarray:
+    """A per-channel copy's factors as stored for the GEMM: fp32, one per row
+    of the copy, zero-padded to a multiple of 128 entries."""
+    v = np.asarray(v, dtype=np.float32)
+    out = np.zeros(-(-v.size // 128) * 128, dtype=np.float32)
+    out[:v.size] = v
+    return out
+
+
 # --------------------------------------------------------------- recipes
 
 def quantize(kind: int, fmt: int, x_bits: np.ndarray, rowwise: bool = True, colwise: bool = False,
@@ -245,6 +262,8 @@ def quantize(kind: int, fmt: int, x_bits: np.ndarray, rowwise: bool = True, colw
     1x128: [R, C/128] / [C, R/128] fp32 d; 128x128: [R/128, C/128] / its
     transpose; MXFP8: [R, C/32] / [C, R/32] E8M0 codes) and, for 1x128 and
     MXFP8, *_packed in the GEMM layout; amax, scale, scale_inv (per-tensor);
+    per-channel: scale_row [R] / scale_col [C] fp32 RN(1 / s), *_packed
+    zero-padded to 128, and mult_* (s) and amax_* per row / column;
     sat_row, sat_col, nonfinite counts.
     """
     x = np.ascontiguousarray(x_bits, dtype=np.uint16)
@@ -278,6 +297,29 @@ def quantize(kind: int, fmt: int, x_bits: np.ndarray, rowwise: bool = True, colw
             out.update(data_col=np.ascontiguousarray(q.T), scale_col=np.ascontiguousarray(d.T))
         if not rowwise:
             out["sat_row"] = 0
+        return out
+
+    if kind == PERCHANNEL_CURRENT:
+        # one block per row (row copy) / per column (column copy), multiply rule
+        out.update(sat_row=0, sat_col=0, nonfinite=0)
+        if R == 0 or C == 0:
+            if rowwise:
+                out.update(data_row=np.zeros((R, C), np.uint8), scale_row=np.zeros(R, np.float32),
+                           scale_row_packed=pad128(np.zeros(R, np.float32)))
+            if colwise:
+                out.update(data_col=np.zeros((C, R), np.uint8), scale_col=np.zeros(C, np.float32),
+                           scale_col_packed=pad128(np.zeros(C, np.float32)))
+            return out
+        if rowwise:
+            q, sm, _, am, sat, nf = quant_blocks(x, 1, C, KIND_MULT, fmt)
+            inv = (np.float32(1.0) / sm[:, 0]).astype(np.float32)
+            out.update(data_row=q, scale_row=inv, scale_row_packed=pad128(inv), mult_row=sm[:, 0],
+                       amax_row=am[:, 0], sat_row=sat, nonfinite=nf)
+        if colwise:
+            q, sm, _, am, sat, nf = quant_blocks(x, R, 1, KIND_MULT, fmt)
+            inv = (np.float32(1.0) / sm[0, :]).astype(np.float32)
+            out.update(data_col=np.ascontiguousarray(q.T), scale_col=inv, scale_col_packed=pad128(inv),
+                       mult_col=sm[0, :], amax_col=am[0, :], sat_col=sat, nonfinite=nf)
         return out
 
     if kind == BLOCK_1x128:
@@ -344,4 +386,6 @@ def dequant_scales(kind: int, q: dict, which: str, rows: int, cols: int):
         return s, 1, 128
     if kind == MXFP8_1x32:
         return np.ldexp(np.float32(1.0), s.astype(np.int32) - 127).astype(np.float32), 1, 32
+    if kind == PERCHANNEL_CURRENT:
+        return np.ascontiguousarray(s.reshape(rows, 1)), 1, max(cols, 1)
     raise ValueError(kind)

@@ -37,11 +37,13 @@ def _exact(A, tabA, sA, a_bm, a_bk, B, tabB, sB, b_bn, b_bk):
 
 
 CASES = [
-    # name, (a_bm, a_bk), (b_bn, b_bk): per-tensor, 1x128 x 128x128, 1x128 x 1x128, MX 1x32
+    # name, (a_bm, a_bk), (b_bn, b_bk): per-tensor, 1x128 x 128x128, 1x128 x 1x128, MX 1x32,
+    # per-channel
     ("pertensor", None, None),
     ("block_1d2d", (1, 128), (128, 128)),
     ("block_1d1d", (1, 128), (1, 128)),
     ("mx", (1, 32), (1, 32)),
+    ("perchannel", (1, 300), (1, 300)),     # one factor per row of A and of B
 ]
 
 

@@ -64,6 +64,52 @@ def test_hand_block_pertensor():
     assert np.array_equal(res["data_col"], exp.T)
 
 
+def test_hand_perchannel():
+    """Rows k, 2k, k/2 of k = (c % 29) - 14: row maxima 14, 28, 7 give s = 32,
+    16, 64 (RN(448 / amax), exact) and every row the codes of k x 32.  Column
+    c holds k, 2k, k/2 with maximum 2|k|: s = 224 / |k| maps the rows to
+    +-224, +-448, +-112 (E4M3 0x76, 0x7E, 0x6E); all-zero columns keep s = 1."""
+    k = np.array([(c % 29) - 14 for c in range(48)], dtype=np.float64)
+    x = np.stack([k, 2 * k, k / 2])
+    res = O.quantize(O.PERCHANNEL_CURRENT, O.E4M3, _bits(x), True, True)
+    assert list(res["mult_row"]) == [32.0, 16.0, 64.0]
+    assert list(res["scale_row"]) == [np.float32(1 / 32), np.float32(1 / 16), np.float32(1 / 64)]
+    exp = _k32_expected(k.astype(int))
+    for r in range(3):
+        assert np.array_equal(res["data_row"][r], exp)
+    mag = {0: 0x76, 1: 0x7E, 2: 0x6E}
+    for c in range(48):
+        kc = int(k[c])
+        if kc == 0:
+            assert res["mult_col"][c] == 1.0 and not res["data_col"][c].any()
+            continue
+        assert res["mult_col"][c] == np.float32(448.0 / (2 * abs(kc)))
+        sign = 0x80 if kc < 0 else 0
+        assert list(res["data_col"][c]) == [mag[r] | sign for r in range(3)], c
+    # saturated before the cast: where RN(224 / |k|) rounded up, 2|k| s lands
+    # just above 448 (and still encodes to 448)
+    s32 = np.float32(448.0) / np.float32(2 * np.abs(k[k != 0]))
+    over = int(np.count_nonzero(np.float32(2 * np.abs(k[k != 0])) * s32 > np.float32(448.0)))
+    assert res["sat_row"] == 0 and res["sat_col"] == over and res["nonfinite"] == 0
+    assert res["scale_row_packed"].size == 128 and not res["scale_row_packed"][3:].any()
+
+
+def test_perchannel_rows_are_pertensor():
+    """Each row of a per-channel copy is the per-tensor current quantization of
+    that row alone: codes, multiplier, dequantization factor, saturation."""
+    x = _rand_bits((37, 208), 11)
+    x[5, 7] = 0x7F80                   # an Inf in one row: excluded from its amax, counted
+    res = O.quantize(O.PERCHANNEL_CURRENT, O.E5M2, x, True, False)
+    sat = 0
+    for r in range(37):
+        one = O.quantize(O.PERTENSOR_CURRENT, O.E5M2, x[r:r + 1], True, False)
+        assert np.array_equal(res["data_row"][r], one["data_row"][0]), r
+        assert res["mult_row"][r] == one["scale"] and res["scale_row"][r] == one["scale_inv"]
+        assert res["amax_row"][r] == one["amax"]
+        sat += one["sat_row"]
+    assert res["sat_row"] == sat and res["nonfinite"] == 1
+
+
 def test_e8m0_closed_form():
     fmts = {"e4m3": O.E4M3, "e5m2": O.E5M2}
     n = 0
@@ -134,7 +180,7 @@ def test_pertensor_amax_maps_to_fmax():
     assert np.all((res["data_row"][xf == xf.max()] & 0x7F) == 0x7E)
 
 
-@pytest.mark.parametrize("kind", [O.BLOCK_1x128, O.MXFP8_1x32])
+@pytest.mark.parametrize("kind", [O.BLOCK_1x128, O.MXFP8_1x32, O.PERCHANNEL_CURRENT])
 def test_colwise_is_rowwise_of_transpose(kind):
     x = _rand_bits((200, 176), 4)
     res = O.quantize(kind, O.E4M3, x, True, True)
