@@ -12,7 +12,7 @@ from dataclasses import dataclass
 import torch
 
 from . import _lib as L
-from ._lib import (BLOCK_1x128, BLOCK_128x128, E4M3, E5M2, MXFP8_1x32, PERTENSOR_CURRENT,  # noqa: F401
+from ._lib import (BLOCK_1x128, BLOCK_128x128, E4M3, E5M2, MXFP8_1x32, PERCHANNEL_CURRENT, PERTENSOR_CURRENT,  # noqa: F401
                    PERTENSOR_DELAYED, Fp8qError)
 
 

@@ -23,9 +23,21 @@ bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
 bool valid_fmt(int f) { return f == FP8Q_E4M3 || f == FP8Q_E5M2; }
 
-bool valid_kind(int k) { return k >= FP8Q_PERTENSOR_CURRENT && k <= FP8Q_MXFP8_1x32; }
+bool valid_kind(int k) { return k >= FP8Q_PERTENSOR_CURRENT && k <= FP8Q_PERCHANNEL_CURRENT; }
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+bool is_pertensor(int k) { return k == FP8Q_PERTENSOR_CURRENT || k == FP8Q_PERTENSOR_DELAYED; }
+
+// Recipe pairs of the scaled GEMM: both per-tensor (current / delayed in any
+// mix), both MXFP8, both per-channel, or A 1x128 with B 1x128 or 128x128.
+bool gemm_kinds_ok(int ka, int kb) {
+    if (is_pertensor(ka) || is_pertensor(kb)) return is_pertensor(ka) && is_pertensor(kb);
+    if (ka == FP8Q_MXFP8_1x32 || kb == FP8Q_MXFP8_1x32 || ka == FP8Q_PERCHANNEL_CURRENT ||
+        kb == FP8Q_PERCHANNEL_CURRENT)
+        return ka == kb;
+    return ka == FP8Q_BLOCK_1x128 && (kb == FP8Q_BLOCK_1x128 || kb == FP8Q_BLOCK_128x128);
+}
 
 // Scale bytes of one copy with logical shape [R][C] (blocks along C).
 size_t copy_scale_bytes(int kind, int64_t R, int64_t C) {
@@ -36,6 +48,8 @@ size_t copy_scale_bytes(int kind, int64_t R, int64_t C) {
             return (size_t)(cdiv(R, 128) * cdiv(C, 128)) * sizeof(float);
         case FP8Q_MXFP8_1x32:
             return (size_t)(cdiv(R, 128) * cdiv(C, 128)) * 512u;
+        case FP8Q_PERCHANNEL_CURRENT:
+            return (size_t)(cdiv(R, 128) * 128) * sizeof(float);
         default:
             return 0;
     }
@@ -82,7 +96,7 @@ fp8q_status fp8q_quantize(const fp8q_recipe* rc, const void* x, int64_t rows, in
     if (cols % 16 != 0) return FP8Q_ERR_SHAPE;
     if (col && rows % 16 != 0) return FP8Q_ERR_SHAPE;
     const bool empty = rows == 0 || cols == 0;
-    const bool per_tensor = rc->kind == FP8Q_PERTENSOR_CURRENT || rc->kind == FP8Q_PERTENSOR_DELAYED;
+    const bool per_tensor = is_pertensor(rc->kind);
     if (!out->counters) return FP8Q_ERR_ARG;
     if (((uintptr_t)out->counters & 7u) != 0) return FP8Q_ERR_ALIGN;
     if (!empty) {
@@ -228,16 +242,8 @@ fp8q_status fp8q_scaled_gemm(const fp8q_tensor* A, int a_use_col, const fp8q_ten
     const int64_t am = a_use_col ? A->cols : A->rows, ak = a_use_col ? A->rows : A->cols;
     const int64_t bn = b_use_col ? B->cols : B->rows, bk = b_use_col ? B->rows : B->cols;
     if (am != M || ak != K || bn != N || bk != K) return FP8Q_ERR_SHAPE;
-    const bool a_pt = A->kind == FP8Q_PERTENSOR_CURRENT || A->kind == FP8Q_PERTENSOR_DELAYED;
-    const bool b_pt = B->kind == FP8Q_PERTENSOR_CURRENT || B->kind == FP8Q_PERTENSOR_DELAYED;
-    if (a_pt != b_pt) return FP8Q_ERR_DTYPE;
-    if (!a_pt) {
-        if (A->kind == FP8Q_MXFP8_1x32 || B->kind == FP8Q_MXFP8_1x32) {
-            if (A->kind != B->kind) return FP8Q_ERR_DTYPE;
-        } else if (A->kind != FP8Q_BLOCK_1x128) {
-            return FP8Q_ERR_DTYPE;  // blockwise: A must be 1x128, B 1x128 or 128x128
-        }
-    }
+    const bool a_pt = is_pertensor(A->kind);
+    if (!gemm_kinds_ok(A->kind, B->kind)) return FP8Q_ERR_DTYPE;
     GemmOperand ga, gb;
     ga.data = (const uint8_t*)(a_use_col ? A->data_col : A->data_row);
     ga.scale = a_use_col ? A->scale_col : A->scale_row;
@@ -269,16 +275,8 @@ fp8q_status fp8q_scaled_gemm_mxq(const fp8q_tensor* A, int a_use_col, const fp8q
     const int64_t am = a_use_col ? A->cols : A->rows, ak = a_use_col ? A->rows : A->cols;
     const int64_t bn = b_use_col ? B->cols : B->rows, bk = b_use_col ? B->rows : B->cols;
     if (am != M || ak != K || bn != N || bk != K) return FP8Q_ERR_SHAPE;
-    const bool a_pt = A->kind == FP8Q_PERTENSOR_CURRENT || A->kind == FP8Q_PERTENSOR_DELAYED;
-    const bool b_pt = B->kind == FP8Q_PERTENSOR_CURRENT || B->kind == FP8Q_PERTENSOR_DELAYED;
-    if (a_pt != b_pt) return FP8Q_ERR_DTYPE;
-    if (!a_pt) {
-        if (A->kind == FP8Q_MXFP8_1x32 || B->kind == FP8Q_MXFP8_1x32) {
-            if (A->kind != B->kind) return FP8Q_ERR_DTYPE;
-        } else if (A->kind != FP8Q_BLOCK_1x128) {
-            return FP8Q_ERR_DTYPE;
-        }
-    }
+    const bool a_pt = is_pertensor(A->kind);
+    if (!gemm_kinds_ok(A->kind, B->kind)) return FP8Q_ERR_DTYPE;
     GemmOperand ga, gb;
     ga.data = (const uint8_t*)(a_use_col ? A->data_col : A->data_row);
     ga.scale = a_use_col ? A->scale_col : A->scale_row;

@@ -37,7 +37,8 @@ namespace {
 
 constexpr int BM = 128, BK = 128;
 constexpr uint64_t kWaitNs = 1000000000ull;
-enum { REC_PT = 0, REC_MX = 1, REC_B2D = 2, REC_B1D = 3 };
+// recipes: per-tensor, MXFP8, blockwise 1x128 x 128x128 / 1x128 x 1x128, per-channel
+enum { REC_PT = 0, REC_MX = 1, REC_B2D = 2, REC_B1D = 3, REC_PC = 4 };
 
 template <int REC>
 struct Cfg {
@@ -449,12 +450,12 @@ __global__ void __launch_bounds__(Cfg<REC>::THREADS, 1)
             bool ok = true;
             for (int64_t t = cid; t < npt && ok; t += ncl, ++tile_i) {
                 const uint32_t abuf = tile_i % NACC;
-                if (REC == REC_PT || REC == REC_MX) {
+                if (REC == REC_PT || REC == REC_PC || REC == REC_MX) {
                     if (!mbar_wait2(tempty(abuf), ((tile_i / NACC) & 1u) ^ 1u, abort_flag)) break;
                     tc_fence_after();
                 }
                 for (int64_t kb = 0; kb < p.nkb; ++kb) {
-                    uint32_t dcol = (REC == REC_PT) ? abuf * BN : 0;
+                    uint32_t dcol = (REC == REC_PT || REC == REC_PC) ? abuf * BN : 0;
                     if (REC == REC_B2D || REC == REC_B1D) {
                         const uint32_t buf = kbg % NACC;
                         if (!mbar_wait2(tempty(buf), ((kbg / NACC) & 1u) ^ 1u, abort_flag)) {
@@ -481,7 +482,8 @@ __global__ void __launch_bounds__(Cfg<REC>::THREADS, 1)
                     } else {
 #pragma unroll
                         for (int k = 0; k < BK / 32; ++k) {
-                            const uint32_t acc = (REC == REC_PT) ? ((kb > 0 || k > 0) ? 1u : 0u) : (k > 0 ? 1u : 0u);
+                            const uint32_t acc =
+                                (REC == REC_PT || REC == REC_PC) ? ((kb > 0 || k > 0) ? 1u : 0u) : (k > 0 ? 1u : 0u);
                             mma2_f8(tmem + dcol, desc_sw128(a0 + 32 * k), desc_sw128(b0 + 32 * k), p.idesc, acc);
                         }
                     }
@@ -491,7 +493,7 @@ __global__ void __launch_bounds__(Cfg<REC>::THREADS, 1)
                         ++kbg;
                     }
                     const bool last = kb + 1 == p.nkb;
-                    if ((REC == REC_PT || REC == REC_MX) && last) tc2_commit_both(tfull(abuf));
+                    if ((REC == REC_PT || REC == REC_PC || REC == REC_MX) && last) tc2_commit_both(tfull(abuf));
                     if (++s == STAGES) {
                         s = 0;
                         ph ^= 1u;
@@ -589,11 +591,30 @@ __global__ void __launch_bounds__(Cfg<REC>::THREADS, 1)
                 float vf[EC];
 #pragma unroll
                 for (int i = 0; i < EC; ++i) vf[i] = __uint_as_float(r[i]);
+                if constexpr (REC == REC_PC) {
+                    // per channel: D = fp32(s_inv_A[m] s_inv_B[n]) x acc; the factor
+                    // vectors are padded to 128 entries, and a warp's 128 columns lie
+                    // wholly inside or past them
+                    const int64_t m = row0 + lane;
+                    const float ia = m < p.Mp ? p.bsa[m] : 0.0f;
+                    if (col0 < p.Np) {
+                        const float4* ib = (const float4*)(p.bsb + col0);
+#pragma unroll
+                        for (int i = 0; i < EC / 4; ++i) {
+                            const float4 b = ib[i];
+                            vf[4 * i] = __fmul_rn(vf[4 * i], __fmul_rn(ia, b.x));
+                            vf[4 * i + 1] = __fmul_rn(vf[4 * i + 1], __fmul_rn(ia, b.y));
+                            vf[4 * i + 2] = __fmul_rn(vf[4 * i + 2], __fmul_rn(ia, b.z));
+                            vf[4 * i + 3] = __fmul_rn(vf[4 * i + 3], __fmul_rn(ia, b.w));
+                        }
+                    }
+                }
+                const float osc = (REC == REC_PC) ? 1.0f : sab;
                 if (QF == 0 || p.hasD)
                     store_slice2<OUT_F32, EC, C::STG_WARP / 1024>(&tmD, stg, stg_s, lane, (int)col0, (int)row0, (int)p.N,
-                                                                  (int)p.M, vf, sab, poll_sf);
+                                                                  (int)p.M, vf, osc, poll_sf);
                 if constexpr (QF != 0)
-                    store_q<QF - 1, EC, C::STG_WARP / 1024>(&tmQ, stg, stg_s, lane, (int)col0, (int)row0, p, vf, sab,
+                    store_q<QF - 1, EC, C::STG_WARP / 1024>(&tmQ, stg, stg_s, lane, (int)col0, (int)row0, p, vf, osc,
                                                             q_sat, q_nf, poll_sf);
             } else {
                 float2 acc[EC / 2];  // packed pairs: Blackwell's two-lane FMA halves the promotion's instructions
@@ -752,8 +773,9 @@ fp8q_status launch_gemm_pair(const GemmOperand& A, const GemmOperand& B, void* D
     if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return FP8Q_ERR_SHAPE;
     const bool mx = A.kind == FP8Q_MXFP8_1x32;
     const bool pt = A.kind == FP8Q_PERTENSOR_CURRENT || A.kind == FP8Q_PERTENSOR_DELAYED;
+    const bool pc = A.kind == FP8Q_PERCHANNEL_CURRENT;
     static_assert(Cfg<REC_MX>::BN == Cfg<REC_PT>::BN && Cfg<REC_B2D>::BN == Cfg<REC_B1D>::BN, "tile widths");
-    const int bn = (mx || pt) ? Cfg<REC_PT>::BN : Cfg<REC_B2D>::BN;
+    const int bn = (mx || pt || pc) ? Cfg<REC_PT>::BN : Cfg<REC_B2D>::BN;
     CUtensorMap maps[6];
     memset(maps, 0, sizeof(maps));
     Params2 p;
@@ -796,6 +818,12 @@ fp8q_status launch_gemm_pair(const GemmOperand& A, const GemmOperand& B, void* D
         p.sa_inv = A.scale_inv;
         p.sb_inv = B.scale_inv;
         return launch2_rec<REC_PT>(maps, p, D, out_dtype, qfmt, qdata, s);
+    }
+    if (pc) {  // the copies' per-row factors, fp32 padded to 128 entries
+        if (((uintptr_t)A.scale | (uintptr_t)B.scale) & 15) return FP8Q_ERR_ARG;
+        p.bsa = (const float*)A.scale;
+        p.bsb = (const float*)B.scale;
+        return launch2_rec<REC_PC>(maps, p, D, out_dtype, qfmt, qdata, s);
     }
     // blockwise scale rows are fetched by bulk copies: 16-byte aligned bases
     if (((uintptr_t)A.scale | (uintptr_t)B.scale) & 15) return FP8Q_ERR_ARG;

@@ -293,7 +293,7 @@ __device__ __forceinline__ uint32_t count_equal8(const uint4& v, uint32_t m) {
     for (int i = 0; i < 4; ++i) c += ((w[i] & 0x7FFFu) == m) + (((w[i] >> 16) & 0x7FFFu) == m);
     return c;
 }
-// Saturated elements of a per-tensor-current or blockwise block whose maximum
+// Saturated elements of a per-tensor-current, per-channel or blockwise block whose maximum
 // m can saturate.  Those scales are one correctly rounded division of fmax and
 // amax (relative error <= 2^-24) and the next bf16 below m is at least 2^-8
 // smaller, so only elements equal to m in magnitude can exceed fmax once
@@ -427,6 +427,14 @@ __global__ void __launch_bounds__(kThreads, 2)
             mq[0] = mq[1] = m;
             kq[0] = kq[1] = block_scale<FMT>(__uint_as_float(m << 16));
             if (ROW && hh == 0) ((float*)a.s_row)[tc * (a.tiles_r * kTile) + r0 + rr] = kq[0];
+        } else if constexpr (KIND == kPC) {
+            // the row's maximum over all of x (the amax pass left it in s_row as
+            // bf16 magnitude bits): s = fmax / amax, the per-tensor current rule
+            if constexpr (ROW) {
+                const uint32_t m = ((const uint32_t*)a.s_row)[r0 + rr];
+                mq[0] = mq[1] = m;
+                kq[0] = kq[1] = pertensor_scale<FMT>(__uint_as_float(m << 16));
+            }
         } else if constexpr (KIND == kMX) {
             const int e0 = mx_exponent<FMT>(mq[0] << 16), e1 = mx_exponent<FMT>(mq[1] << 16);
             kq[0] = exp2_neg(e0);
@@ -449,7 +457,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             const bool s1 = (KIND == kMX) ? may_saturate<KIND, FMT>(mq[1], f1) : s0;
             if (vnf == 0 && f0.fast && f1.fast) {  // the common case: one straight-line block
                 const Factor2 g0 = pair_factor(f0, f0), g1 = pair_factor(f1, f1);
-                constexpr bool kAtMax = KIND == kCur || KIND == kB1 || KIND == kB128;
+                constexpr bool kAtMax = KIND == kCur || KIND == kB1 || KIND == kB128 || KIND == kPC;
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
                     q[j] = convert8_packed<KIND, FMT>(v[j], (j < 4) ? g0 : g1, nsat_rc,
@@ -483,7 +491,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         constexpr bool kCodesAfterBlockMax = KIND == kB128 || (KIND == kB1 && !COL);
         if constexpr (kRowCodes && kCodesAfterBlockMax) put_row_codes();
 
-        // ---------------- column-wise codes re-quantized along the columns (1x128, MXFP8)
+        // ---------------- column-wise codes re-quantized along the columns (1x128, MXFP8, per channel)
         const int p = t & 63, qd = t >> 6;  // column pair 2p, 2p + 1; rows 32 qd .. 32 qd + 31
         uint32_t o0[8], o1[8];
         if constexpr (COL && !kTranspose) {
@@ -530,6 +538,12 @@ __global__ void __launch_bounds__(kThreads, 2)
                     const int cr = 2 * p;
                     tileb[(cr & 31) * 16 + (cr >> 5) * 4 + qd] = (uint8_t)(e0 + 127);
                     tileb[((cr + 1) & 31) * 16 + ((cr + 1) >> 5) * 4 + qd] = (uint8_t)(e1 + 127);
+                } else if constexpr (KIND == kPC) {
+                    // the columns' maxima over all of x (from the amax pass, in s_col)
+                    m0 = ((const uint32_t*)a.s_col)[cc];
+                    m1 = ((const uint32_t*)a.s_col)[cc + 1];
+                    k0 = pertensor_scale<FMT>(__uint_as_float(m0 << 16));
+                    k1 = pertensor_scale<FMT>(__uint_as_float(m1 << 16));
                 } else {  // 1x128 along the rows of x: reduce the four quarters
                     colred[qd * kTile + 2 * p] = m0;
                     colred[qd * kTile + 2 * p + 1] = m1;
@@ -559,13 +573,13 @@ __global__ void __launch_bounds__(kThreads, 2)
                 for (int j = 0; j < 32; j += 4) {
                     const float2 y0 = apply2<KIND>(bf16x2_f32(w[j]), g), y1 = apply2<KIND>(bf16x2_f32(w[j + 1]), g);
                     const float2 y2 = apply2<KIND>(bf16x2_f32(w[j + 2]), g), y3 = apply2<KIND>(bf16x2_f32(w[j + 3]), g);
-                    if (KIND != kB1)
+                    if (KIND != kB1 && KIND != kPC)
                         ns += sat2<FMT>(y0, c0s, c1s) + sat2<FMT>(y1, c0s, c1s) + sat2<FMT>(y2, c0s, c1s) +
                               sat2<FMT>(y3, c0s, c1s);
                     o0[j / 4] = cvt4_applied<KIND, FMT>(y0.x, y1.x, y2.x, y3.x);
                     o1[j / 4] = cvt4_applied<KIND, FMT>(y0.y, y1.y, y2.y, y3.y);
                 }
-                if (KIND == kB1 && ((c0s && own0 == m0) || (c1s && own1 == m1))) {
+                if ((KIND == kB1 || KIND == kPC) && ((c0s && own0 == m0) || (c1s && own1 == m1))) {
                     // only elements equal to the block maximum can saturate (count_at_max),
                     // looked for in the 8-row groups whose maximum it is
 #pragma unroll
@@ -652,7 +666,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (lane == 0) {
         if (nsat_row) atomicAdd(&a.counters[0], (unsigned long long)nsat_row);
         if (nsat_col) atomicAdd(&a.counters[1], (unsigned long long)nsat_col);
-        if (KIND != kCur && nnf) atomicAdd(&a.counters[2], (unsigned long long)nnf);
+        if (KIND != kCur && KIND != kPC && nnf) atomicAdd(&a.counters[2], (unsigned long long)nnf);  // else the amax pass
     }
     if constexpr (KIND == kDel) {
         tmax_all = warp_max_u32(tmax_all);
@@ -692,6 +706,80 @@ __global__ void __launch_bounds__(kThreads) amax_kernel(const uint16_t* x, int64
         if (mm) atomicMax((unsigned int*)amax, mm << 16);
         if (nn) atomicAdd(&counters[2], (unsigned long long)nn);
     }
+}
+
+// The two bf16 of w as magnitude bits, a NaN / Inf half replaced by 0.
+__device__ __forceinline__ uint32_t finite_mag2(uint32_t w) {
+    const uint32_t lo = w & 0x7FFFu, hi = (w >> 16) & 0x7FFFu;
+    return (lo < 0x7F80u ? lo : 0u) | ((hi < 0x7F80u ? hi : 0u) << 16);
+}
+__device__ __forceinline__ uint32_t nonfinite2(uint32_t w) {
+    return (uint32_t)((w & 0x7FFFu) >= 0x7F80u) + (uint32_t)(((w >> 16) & 0x7FFFu) >= 0x7F80u);
+}
+
+// Per-channel current scaling, pass 1: the largest finite |x| of every row
+// (rowmax[r]) and of every column (colmax[c]) of x, as bf16 magnitude bits in
+// uint32 words of the zeroed scale buffers (atomicMax merges the strips), and
+// the NaN / Inf count.  A CTA takes strips of 64 rows x 256 columns: warp w
+// rows 8w .. 8w + 7, lane l columns 8l .. 8l + 7 (one 16-byte load a row).
+template <bool ROW, bool COL>
+__global__ void __launch_bounds__(256) pc_amax_kernel(const uint16_t* x, int64_t R, int64_t C, uint32_t* rowmax,
+                                                      uint32_t* colmax, unsigned long long* counters) {
+    __shared__ uint32_t cred[8][128];  // per warp: column-pair maxima of its 8 rows
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t strips_c = (C + 255) / 256, strips = ((R + 63) / 64) * strips_c;
+    uint32_t nf = 0;
+    for (int64_t sidx = blockIdx.x; sidx < strips; sidx += gridDim.x) {
+        const int64_t r0 = (sidx / strips_c) * 64 + 8 * warp, cs = (sidx % strips_c) * 256, c = cs + 8 * lane;
+        uint4 v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)  // C % 8 == 0: a vector is wholly inside or outside
+            v[i] = (c < C && r0 + i < R) ? ld_nc_v4(x + (r0 + i) * C + c) : make_uint4(0u, 0u, 0u, 0u);
+        uint32_t cm[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+            uint32_t rm = 0;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const uint32_t f = finite_mag2(w[k]);
+                nf += nonfinite2(w[k]);
+                cm[k] = max_u16x2(cm[k], f);
+                rm = max_u16x2(rm, f);
+            }
+            if constexpr (ROW) {
+                const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, fold16(rm));
+                if (lane == 0 && m != 0u && r0 + i < R) atomicMax(rowmax + r0 + i, m);
+            }
+        }
+        if constexpr (COL) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) cred[warp][4 * lane + k] = cm[k];
+            __syncthreads();
+            if (threadIdx.x < 128) {
+                uint32_t m = 0;
+#pragma unroll
+                for (int w = 0; w < 8; ++w) m = max_u16x2(m, cred[w][threadIdx.x]);
+                const int64_t cc = cs + 2 * threadIdx.x;
+                if (cc < C) {
+                    if (m & 0xFFFFu) atomicMax(colmax + cc, m & 0xFFFFu);
+                    if (m >> 16) atomicMax(colmax + cc + 1, m >> 16);
+                }
+            }
+            __syncthreads();  // cred is rewritten by the next strip
+        }
+    }
+    nf = warp_sum_u32(nf);
+    if (lane == 0 && nf) atomicAdd(&counters[2], (unsigned long long)nf);
+}
+
+// Per-channel current scaling, last pass: each entry of a scale buffer (a
+// row's or column's amax bits, 0 past the copy's rows) becomes the
+// dequantization factor fp32(1 / s), s = fmax / amax (amax 0 -> s = 1).
+template <int FMT>
+__global__ void pc_finalize_kernel(uint32_t* m, int64_t n) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+        ((float*)m)[i] = __fdiv_rn(1.0f, pertensor_scale<FMT>(__uint_as_float(m[i] << 16)));
 }
 
 __global__ void delayed_update_kernel(DelayedDev* st, const float* amax, const unsigned long long* nonfinite) {
@@ -842,6 +930,41 @@ fp8q_status launch_tile_fmt(const QuantArgs& a, int fmt, bool row, bool col, cud
                             : launch_tile_rc<KIND, FP8Q_E5M2>(a, row, col, s);
 }
 
+// Per-channel current: zero the scale buffers, the amax pass into them, the
+// tile pass (reads them), then the buffers' amax bits become fp32(1 / s).
+fp8q_status launch_perchannel(const QuantArgs& a, int fmt, bool row, bool col, cudaStream_t s) {
+    const int64_t Rp = a.tiles_r * 128, Cp = a.tiles_c * 128;
+    if (Rp == 0 || Cp == 0) return FP8Q_OK;  // empty x: nothing to write
+    if (row && cudaMemsetAsync(a.s_row, 0, (size_t)Rp * sizeof(float), s) != cudaSuccess) return FP8Q_ERR_CUDA;
+    if (col && cudaMemsetAsync(a.s_col, 0, (size_t)Cp * sizeof(float), s) != cudaSuccess) return FP8Q_ERR_CUDA;
+    const int64_t strips = ((a.R + 63) / 64) * ((a.C + 255) / 256);
+    int64_t grid = (int64_t)num_sms() * 8;
+    if (strips < grid) grid = strips;
+    uint32_t* rm = (uint32_t*)a.s_row;
+    uint32_t* cm = (uint32_t*)a.s_col;
+    if (row && col)
+        pc_amax_kernel<true, true><<<(unsigned)grid, 256, 0, s>>>(a.x, a.R, a.C, rm, cm, a.counters);
+    else if (row)
+        pc_amax_kernel<true, false><<<(unsigned)grid, 256, 0, s>>>(a.x, a.R, a.C, rm, cm, a.counters);
+    else
+        pc_amax_kernel<false, true><<<(unsigned)grid, 256, 0, s>>>(a.x, a.R, a.C, rm, cm, a.counters);
+    if (cudaGetLastError() != cudaSuccess) return FP8Q_ERR_CUDA;
+    const fp8q_status r = launch_tile_fmt<kPC>(a, fmt, row, col, s);
+    if (r != FP8Q_OK) return r;
+    for (int w = 0; w < 2; ++w) {
+        if (w == 0 ? !row : !col) continue;
+        uint32_t* m = w == 0 ? rm : cm;
+        const int64_t n = w == 0 ? Rp : Cp;
+        const unsigned blocks = (unsigned)((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
+        if (fmt == FP8Q_E4M3)
+            pc_finalize_kernel<FP8Q_E4M3><<<blocks, 256, 0, s>>>(m, n);
+        else
+            pc_finalize_kernel<FP8Q_E5M2><<<blocks, 256, 0, s>>>(m, n);
+        if (cudaGetLastError() != cudaSuccess) return FP8Q_ERR_CUDA;
+    }
+    return FP8Q_OK;
+}
+
 }  // namespace
 
 fp8q_status launch_quantize(const fp8q_recipe* rc, const QuantArgs& a, DelayedDev* st, cudaStream_t s) {
@@ -872,6 +995,8 @@ fp8q_status launch_quantize(const fp8q_recipe* rc, const QuantArgs& a, DelayedDe
             return launch_tile_fmt<kB128>(a, rc->fmt, row, col, s);
         case kMX:
             return launch_tile_fmt<kMX>(a, rc->fmt, row, col, s);
+        case kPC:
+            return launch_perchannel(a, rc->fmt, row, col, s);
         default:
             return FP8Q_ERR_ARG;
     }

@@ -19,7 +19,7 @@ import math
 
 import torch
 
-from ._lib import BLOCK_1x128, BLOCK_128x128, E4M3, MXFP8_1x32, PERTENSOR_CURRENT, PERTENSOR_DELAYED
+from ._lib import BLOCK_1x128, BLOCK_128x128, E4M3, MXFP8_1x32, PERCHANNEL_CURRENT, PERTENSOR_CURRENT, PERTENSOR_DELAYED
 
 
 def _cdiv(a: int, b: int) -> int:
@@ -40,6 +40,8 @@ def row_scales(qt) -> torch.Tensor:
     if qt.kind in (PERTENSOR_CURRENT, PERTENSOR_DELAYED):
         return qt.scale_inv.to(dev).float().reshape(1, 1).expand(R, C)
     buf = qt.scale_row
+    if qt.kind == PERCHANNEL_CURRENT:
+        return buf.view(torch.float32)[:R].reshape(R, 1).expand(R, C)
     if qt.kind == BLOCK_128x128:
         s = buf.view(torch.float32)[: _cdiv(R, 128) * _cdiv(C, 128)].reshape(_cdiv(R, 128), _cdiv(C, 128))
         return s.repeat_interleave(128, 0)[:R].repeat_interleave(128, 1)[:, :C]

@@ -38,11 +38,15 @@
  *                            rows 128i.., scale columns 4j..; row r,
  *                            column k at (r%32)*16 + (r%128/32)*4 + k%4;
  *                            pad entries 127
+ *   PERCHANNEL_CURRENT       fp32 [Rp], Rp = R up to 128: row r's       s_inv[r]
+ *                            fp32(1 / s_r); pad entries 1.0 (the rule
+ *                            for an all-zero row)
  *
- * The column-wise copy of BLOCK_1x128 and MXFP8_1x32 re-quantizes x^T with
- * its blocks along the rows of x (the contraction dimension of the wgrad
- * GEMM); for per-tensor and 128x128 kinds it is the byte transpose of the
- * row-wise copy with the same (transposed) scales.
+ * The column-wise copy of BLOCK_1x128, MXFP8_1x32 and PERCHANNEL_CURRENT
+ * re-quantizes x^T with its blocks along the rows of x (the contraction
+ * dimension of the wgrad GEMM; per channel: one factor per column of x); for
+ * per-tensor and 128x128 kinds it is the byte transpose of the row-wise copy
+ * with the same (transposed) scales.
  */
 #ifndef FP8Q_H
 #define FP8Q_H
@@ -80,8 +84,12 @@ typedef enum {
     FP8Q_PERTENSOR_DELAYED = 1,  /* s from the max of an amax history of past steps */
     FP8Q_BLOCK_1x128 = 2,        /* d = amax / fmax per 1x128 block; q = sat_rne(x / d) */
     FP8Q_BLOCK_128x128 = 3,      /* same per 128x128 tile (weights) */
-    FP8Q_MXFP8_1x32 = 4          /* e = floor(log2 amax) - emax_elem per 1x32 block,
+    FP8Q_MXFP8_1x32 = 4,         /* e = floor(log2 amax) - emax_elem per 1x32 block,
                                     E8M0 code e + 127, q = sat_rne(x * 2^-e) */
+    FP8Q_PERCHANNEL_CURRENT = 5  /* [nemo] Figure 1 (channel-wise scaling, one factor
+                                    per row / column): the per-tensor current rule
+                                    per row of the copy, s_r = fmax / amax(row r),
+                                    q = sat_rne(x * s_r) */
 } fp8q_recipe_kind;
 
 typedef struct {
@@ -157,7 +165,11 @@ FP8Q_API fp8q_status fp8q_scale_bytes(const fp8q_recipe* recipe, int64_t rows, i
  * same fmt) supplies s; the call writes amax / scale / scale_inv / counters,
  * then records amax in st's history and derives the next step's scale
  * (st is left unchanged when x held a NaN / Inf).  Blockwise d = amax / fmax
- * (amax 0 -> 1).  Amax always excludes NaN / Inf.  Counters are overwritten.
+ * (amax 0 -> 1).  Per-channel current: a pass over x first takes every
+ * row's and every column's amax (into the scale buffers, as scratch), then
+ * s = fmax / amax per row (row-wise copy) or per column (column-wise copy)
+ * as for per-tensor current, and the scale buffers end holding fp32(1 / s).
+ * Amax always excludes NaN / Inf.  Counters are overwritten.
  */
 FP8Q_API fp8q_status fp8q_quantize(const fp8q_recipe* recipe, const void* x, int64_t rows, int64_t cols,
                           fp8q_delayed_state* st, fp8q_tensor* out, void* stream);
@@ -216,7 +228,9 @@ FP8Q_API void fp8q_delayed_destroy(fp8q_delayed_state* st);
  * BLOCK_128x128 or BLOCK_1x128 (E4M3 or E5M2): partial sums over each
  * 128-wide K block are scaled by d_A[m][kb] * d_B[n(/128)][kb] and summed in
  * fp32.  Both MXFP8_1x32: every 32-wide K block scaled by 2^(eA + eB) in the
- * tensor core.
+ * tensor core.  Both PERCHANNEL_CURRENT: D[m][n] = fp32(s_inv_A[m] *
+ * s_inv_B[n]) * (q_A . q_B^T)[m][n] (runs on the SM-pair kernel whatever
+ * fp8q_gemm_set_variant selects).
  * out_dtype 0 = bf16 (RNE), 1 = fp32; D is device [M][N] row-major, 16-byte
  * aligned, N % 8 == 0.  M, N, K >= 1; K % 16 == 0.  D is fully overwritten.
  * A bounded wait inside the kernel that gives up records FP8Q_ERR_TIMEOUT in

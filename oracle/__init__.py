@@ -244,9 +244,10 @@ def pack_block1x128(d: np.ndarray) -> np.ndarray:
 
 def pad128(v: np.ndarray) -> np.ndarray:
     """A per-channel copy's factors as stored for the GEMM: fp32, one per row
-    of the copy, zero-padded to a multiple of 128 entries."""
+    of the copy, padded to a multiple of 128 entries with 1.0, the factor the
+    rule gives an all-zero row (amax 0 -> s = 1), as the 1x128 layout pads."""
     v = np.asarray(v, dtype=np.float32)
-    out = np.zeros(-(-v.size // 128) * 128, dtype=np.float32)
+    out = np.ones(-(-v.size // 128) * 128, dtype=np.float32)
     out[:v.size] = v
     return out
 
@@ -263,7 +264,7 @@ def quantize(kind: int, fmt: int, x_bits: np.ndarray, rowwise: bool = True, colw
     transpose; MXFP8: [R, C/32] / [C, R/32] E8M0 codes) and, for 1x128 and
     MXFP8, *_packed in the GEMM layout; amax, scale, scale_inv (per-tensor);
     per-channel: scale_row [R] / scale_col [C] fp32 RN(1 / s), *_packed
-    zero-padded to 128, and mult_* (s) and amax_* per row / column;
+    padded to 128 entries with 1.0, and mult_* (s) and amax_* per row / column;
     sat_row, sat_col, nonfinite counts.
     """
     x = np.ascontiguousarray(x_bits, dtype=np.uint16)
@@ -304,11 +305,11 @@ def quantize(kind: int, fmt: int, x_bits: np.ndarray, rowwise: bool = True, colw
         out.update(sat_row=0, sat_col=0, nonfinite=0)
         if R == 0 or C == 0:
             if rowwise:
-                out.update(data_row=np.zeros((R, C), np.uint8), scale_row=np.zeros(R, np.float32),
-                           scale_row_packed=pad128(np.zeros(R, np.float32)))
+                out.update(data_row=np.zeros((R, C), np.uint8), scale_row=np.ones(R, np.float32),
+                           scale_row_packed=pad128(np.ones(R, np.float32)))
             if colwise:
-                out.update(data_col=np.zeros((C, R), np.uint8), scale_col=np.zeros(C, np.float32),
-                           scale_col_packed=pad128(np.zeros(C, np.float32)))
+                out.update(data_col=np.zeros((C, R), np.uint8), scale_col=np.ones(C, np.float32),
+                           scale_col_packed=pad128(np.ones(C, np.float32)))
             return out
         if rowwise:
             q, sm, _, am, sat, nf = quant_blocks(x, 1, C, KIND_MULT, fmt)

@@ -8,7 +8,8 @@ import torch
 import oracle as O
 from fp8_scaled_quantization_quantize_gb300 import inputs
 
-KIND_NAMES = {0: "pertensor_current", 1: "pertensor_delayed", 2: "block_1x128", 3: "block_128x128", 4: "mxfp8_1x32"}
+KIND_NAMES = {0: "pertensor_current", 1: "pertensor_delayed", 2: "block_1x128", 3: "block_128x128", 4: "mxfp8_1x32",
+              5: "perchannel_current"}
 
 
 def bits_of(x: torch.Tensor) -> np.ndarray:
@@ -45,6 +46,8 @@ def expected_scale_bytes(kind: int, ref: dict, which: str) -> np.ndarray | None:
         return np.ascontiguousarray(ref["scale_" + which], dtype=np.float32).view(np.uint8).ravel()
     if kind == O.MXFP8_1x32:
         return ref["scale_" + which + "_packed"].ravel()
+    if kind == O.PERCHANNEL_CURRENT:
+        return ref["scale_" + which + "_packed"].astype(np.float32).view(np.uint8).ravel()
     return None
 
 

@@ -41,6 +41,8 @@ def _host_scales(api, qt, use_col):
         off = ((r // 128) * tiles_c + c // 4) * 512 + (r % 32) * 16 + ((r % 128) // 32) * 4 + c % 4
         codes = buf[off].astype(np.int32)
         return np.ldexp(np.float32(1), codes - 127).astype(np.float32), 1, 32
+    if qt.kind == api.PERCHANNEL_CURRENT:
+        return np.ascontiguousarray(buf.view(np.float32)[:R].reshape(R, 1)), 1, max(C, 1)
     raise ValueError(qt.kind)
 
 
@@ -85,6 +87,7 @@ RECIPES = [
     ("pertensor_hybrid", 0, 0, 0, O.E4M3, O.E4M3, O.E5M2),
     ("mxfp8", 4, 4, 4, O.E4M3, O.E4M3, O.E4M3),
     ("block_1x128_128x128", 2, 3, 2, O.E4M3, O.E4M3, O.E4M3),
+    ("perchannel_hybrid", 5, 5, 5, O.E4M3, O.E4M3, O.E5M2),
 ]
 
 
@@ -119,7 +122,7 @@ def test_gemm_k_sweep_and_ragged_k(variant):
     for K in (16, 48, 128, 144, 1040):
         a = inputs.normal_bf16((130, K), K)
         b = inputs.normal_bf16((264, K), K + 1)
-        for kind in (0, 4):
+        for kind in (0, 4, 5):
             qa = api.quantize(a.cuda(), kind, O.E4M3, True, False)
             qb = api.quantize(b.cuda(), kind, O.E4M3, True, False)
             _check(api, qa, False, qb, False, ctx=f"K={K} kind={kind}")
@@ -163,6 +166,20 @@ def test_full_config_blockwise_llama8b_up_proj(variant):
     qx = api.quantize(X.cuda(), 2, O.E4M3, True, False)
     qw = api.quantize(W.cuda(), 3, O.E4M3, True, False)
     _check(api, qx, False, qw, False, sample=_edge_sample(14), ctx="cfg2 fprop (16 rows + 16 cols)")
+
+
+def test_full_config_perchannel_llama8b_up_proj():
+    """Per-channel current scaling at the Llama-3-8B up-projection (X with its
+    1% outlier columns): fprop, and GEMMs through both column copies."""
+    api = _api()
+    X, W = inputs.llama8b_up_proj()
+    qx = api.quantize(X.cuda(), 5, O.E4M3, True, True)
+    qw = api.quantize(W.cuda(), 5, O.E4M3, True, True)
+    s = _edge_sample(10)
+    _check(api, qx, False, qw, False, sample=s, ctx="perchannel fprop")
+    # the column copies (per-column factors): W^T W (K = 14336) and X^T X (K = 4096)
+    _check(api, qw, True, qw, True, sample=s, ctx="perchannel W^T . W")
+    _check(api, qx, True, qx, True, sample=s, ctx="perchannel X^T . X")
 
 
 def test_full_config_mxfp8_llama8b_mlp(variant):

@@ -28,6 +28,7 @@ RECIPES = [
     ("mxfp8", 4, 4, O.E4M3, O.E4M3),
     ("block_1x128_128x128", 2, 3, O.E4M3, O.E4M3),
     ("block_1x128_1x128", 2, 2, O.E4M3, O.E4M3),
+    ("perchannel", 5, 5, O.E4M3, O.E4M3),
 ]
 
 

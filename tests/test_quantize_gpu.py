@@ -13,7 +13,7 @@ from tests._helpers import assert_quant_equal, bits_of, gpu_outputs
 
 pytestmark = pytest.mark.gpu
 
-KINDS = [O.PERTENSOR_CURRENT, O.BLOCK_1x128, O.BLOCK_128x128, O.MXFP8_1x32]
+KINDS = [O.PERTENSOR_CURRENT, O.BLOCK_1x128, O.BLOCK_128x128, O.MXFP8_1x32, O.PERCHANNEL_CURRENT]
 COPIES = [(True, False), (False, True), (True, True)]
 
 
@@ -137,6 +137,8 @@ CONFIG_SHAPES = [
     ("cfg2 X", O.BLOCK_1x128, O.E4M3, None, True, True, lambda: inputs.llama8b_up_proj()[0]),
     ("cfg2 W", O.BLOCK_128x128, O.E4M3, None, True, True, lambda: inputs.llama8b_up_proj()[1]),
     ("cfg3 X", O.MXFP8_1x32, O.E4M3, None, True, True, lambda: inputs.llama8b_mlp()[0]),
+    ("perchannel X", O.PERCHANNEL_CURRENT, O.E4M3, None, True, True, lambda: inputs.llama8b_up_proj()[0]),
+    ("perchannel W", O.PERCHANNEL_CURRENT, O.E4M3, None, True, True, lambda: inputs.llama8b_up_proj()[1]),
 ]
 
 
