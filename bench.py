@@ -363,6 +363,32 @@ def run_ours(args):
         errs |= api.device_errors()
         launches += 6 * args.steps + 4 * args.steps
 
+    # ---- scaling granularity at the bench shape ("mastering FP8 LLM training
+    # 1.5x speedup", Figure 1: per-tensor fastest, per-channel between, 2D
+    # blocks slowest): the fprop GEMM with each, and the per-channel quantize
+    qpt = [api.quantize(t, api.PERTENSOR_CURRENT, api.E4M3, True, False) for t in (X, W)]
+    qpc = [api.alloc(api.PERCHANNEL_CURRENT, api.E4M3, *t.shape, True, True, dev) for t in (X, W)]
+
+    def pc_quantize():
+        for t, q in zip((X, W), qpc):
+            api.quantize_into(t, q, stream=stream)
+
+    pcq_ms = _time_ms(pc_quantize, args.steps, args.warmup, flush)
+    gran = {}
+    for name, (qa_, qb_) in (("pertensor", qpt), ("perchannel", qpc), ("blockwise", (qx, qw))):
+        ms = _time_ms(lambda a=qa_, b=qb_: api.scaled_gemm(a, False, b, False, out=Y, stream=stream),
+                      args.steps, args.warmup, flush)
+        gran[name] = round(flops / ms / 1e9, 1)
+    pc_bytes = (T * H + F * H) * (2 + 2 + 2)   # the amax pass and the cast read x; two FP8 copies
+    granularity = {"workload": "fprop GEMM of the bench shape by scaling granularity; per-channel quantize of X "
+                               "and W (both copies)",
+                   "gemm_tflops": gran,
+                   "gemm_frac_of_fp8_peak": {k: round(v / fp8_peak, 3) for k, v in gran.items()},
+                   "perchannel_quantize_gbs": round(pc_bytes / pcq_ms / 1e6, 1),
+                   "perchannel_quantize_frac_of_hbm": round(pc_bytes / pcq_ms / 1e6 / hbm_peak, 3)}
+    launches += 8 * args.steps + 3 * args.steps   # per-channel: amax, cast, two finalizes per tensor
+    errs |= api.device_errors()
+
     value = world * flops / ms_step / 1e9
     gemm_tflops = flops / g_avg / 1e9
     line = {
@@ -387,6 +413,7 @@ def run_ours(args):
         "clocks": clocks,
         "device_errors": errs,
         "mxfp8": mx,
+        "granularity": granularity,
     }
     if rank == 0 and not args.skip_cpu:
         line["cpu_baseline"] = cpu_baseline(args.cpu_budget)
@@ -429,8 +456,8 @@ def gemm_kernel_name(M, N, recipe, out="bf16"):
 
 # ------------------------------------------------------- single-op modes
 
-KINDS = {"current": 0, "delayed": 1, "1x128": 2, "128x128": 3, "mx": 4}
-QBYTES_SCALE = {0: 0.0, 1: 0.0, 2: 4 / 128, 3: 4 / (128 * 128), 4: 1 / 32}
+KINDS = {"current": 0, "delayed": 1, "1x128": 2, "128x128": 3, "mx": 4, "perchannel": 5}
+QBYTES_SCALE = {0: 0.0, 1: 0.0, 2: 4 / 128, 3: 4 / (128 * 128), 4: 1 / 32, 5: 0.0}
 
 
 def _device_tensor(rows, cols, seed, outlier_frac=0.001, factor=1000.0):
@@ -477,7 +504,8 @@ def quantize_point(kind, rows, cols, rowwise, colwise, steps, warmup, flush, x=N
     qt = api.alloc(kind, api.E4M3, rows, cols, rowwise, colwise, "cuda")
     ms = _time_ms(lambda: api.quantize_into(x, qt, st), steps, warmup, flush)
     copies = int(rowwise) + int(colwise)
-    per_elem = 2 + copies * (1 + QBYTES_SCALE[kind]) + (2 if kind == 0 else 0)
+    # the current-scaling kinds read x twice (the amax pass, then the cast)
+    per_elem = 2 + copies * (1 + QBYTES_SCALE[kind]) + (2 if kind in (0, 5) else 0)
     gbs = rows * cols * per_elem / ms / 1e6
     del qt
     torch.cuda.synchronize()
@@ -501,7 +529,7 @@ def gemm_point(kind, M, N, K, steps, warmup, flush, out="bf16"):
     D = torch.empty((M, N), dtype=torch.bfloat16 if out == "bf16" else torch.float32, device="cuda")
     ms = _time_ms(lambda: api.scaled_gemm(qa, False, qb, False, out=D), steps, warmup, flush)
     tf = 2.0 * M * N * K / ms / 1e9
-    name = {0: "pertensor", 2: "blockwise 1x128 x 128x128", 4: "mxfp8"}[kind]
+    name = {0: "pertensor", 2: "blockwise 1x128 x 128x128", 4: "mxfp8", 5: "perchannel"}[kind]
     del qa, qb, D
     torch.cuda.synchronize()
     return {"mode": "gemm", "recipe": name, "M": M, "N": N, "K": K, "out": out, "ms": round(ms, 4),
@@ -566,7 +594,7 @@ def run_modes(args):
         for name, x, fmt in data:
             xd = x.cuda()
             base = None
-            for kind in (0, 2, 3, 4):
+            for kind in (0, 5, 2, 3, 4):
                 qt = api.quantize(xd, kind, fmt, True, False)
                 e = qerror.error(xd.float(), qerror.dequantize_rowwise(qt))
                 base = e["rel_err"] if kind == 0 else base
@@ -580,14 +608,14 @@ def run_modes(args):
         for mib in (16, 32, 64, 128, 256, 512, 1024, 2048):
             rows = mib * 2 ** 20 // 2 // 4096
             x = _device_tensor(rows, 4096, 5)
-            for kind in (0, 1, 2, 3, 4):
+            for kind in (0, 1, 2, 3, 4, 5):
                 print(json.dumps(quantize_point(kind, rows, 4096, True, True, args.steps, args.warmup, flush, x)),
                       flush=True)
             del x
-        for kind in (4, 2, 0):
+        for kind in (4, 2, 0, 5):
             for K in (1024, 2048, 4096, 8192, 16384):
                 print(json.dumps(gemm_point(kind, 8192, 8192, K, args.steps, args.warmup, flush)), flush=True)
-        for kind in (4, 2, 0):
+        for kind in (4, 2, 0, 5):
             print(json.dumps(gemm_point(kind, 8192, 53248, 16384, args.steps, args.warmup, flush)), flush=True)
 
 
