@@ -363,6 +363,11 @@ def run_ours(args):
         errs |= api.device_errors()
         launches += 6 * args.steps + 4 * args.steps
 
+    # ---- the same quantize phase as one fp8q_quantize_multi call
+    multi_ms = _time_ms(lambda: api.quantize_multi([(X, qx), (W, qw)], stream=stream), args.steps, args.warmup,
+                        flush)
+    launches += 2 * args.steps
+
     # ---- scaling granularity at the bench shape ("mastering FP8 LLM training
     # 1.5x speedup", Figure 1: per-tensor fastest, per-channel between, 2D
     # blocks slowest): the fprop GEMM with each, and the per-channel quantize
@@ -401,6 +406,7 @@ def run_ours(args):
         "gemm_tflops": round(gemm_tflops, 1),
         "quantize_gbs": round(qbytes / q_avg / 1e6, 1),
         "quantize_frac_of_hbm": round(qbytes / q_avg / 1e6 / hbm_peak, 3),
+        "quantize_ms": {"two_calls": round(q_avg, 4), "one_multi_call": round(multi_ms, 4)},
         "roofline": {"kernel": gemm_kernel_name(T, F, "blockwise 1x128 x 128x128"), "bound": "tensor",
                      "achieved": round(gemm_tflops, 1), "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
                      "frac": round(gemm_tflops / fp8_peak, 3),
@@ -546,6 +552,20 @@ def run_modes(args):
     elif args.mode == "gemm":
         print(json.dumps(gemm_point(KINDS[args.kind], args.M, args.N, args.K, args.steps, args.warmup, flush,
                                     args.out)), flush=True)
+    elif args.mode == "multi":  # n small tensors: n quantize calls against one fp8q_quantize_multi
+        from fp8_scaled_quantization_quantize_gb300 import api
+        n, rows, cols = 8, args.rows, args.cols
+        xs = [_device_tensor(rows, cols, 40 + i) for i in range(n)]
+        kind = KINDS[args.kind]
+        qs = [api.alloc(kind, api.E4M3, rows, cols, True, True, "cuda") for _ in range(n)]
+        sep = _time_ms(lambda: [api.quantize_into(x, q) for x, q in zip(xs, qs)], args.steps, args.warmup, flush)
+        mul = _time_ms(lambda: api.quantize_multi(list(zip(xs, qs))), args.steps, args.warmup, flush)
+        per_elem = 2 + 2 * (1 + QBYTES_SCALE[kind]) + (2 if kind in (0, 5) else 0)
+        byts = n * rows * cols * per_elem
+        print(json.dumps({"mode": "multi", "kind": args.kind, "tensors": n, "rows": rows, "cols": cols,
+                          "separate_ms": round(sep, 4), "multi_ms": round(mul, 4),
+                          "separate_frac_of_hbm": round(byts / sep / 1e6 / peaks()[0], 3),
+                          "multi_frac_of_hbm": round(byts / mul / 1e6 / peaks()[0], 3)}), flush=True)
     elif args.mode == "delayed70b":  # cfg 4: delayed hybrid scaling, Llama-3-70B FFN, 3 GEMMs per step
         from fp8_scaled_quantization_quantize_gb300 import api, inputs
         bases = inputs.llama70b_ffn_bases()
@@ -684,9 +704,11 @@ def main():
     ap.add_argument("--skip-mx", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
-    ap.add_argument("--mode", choices=["step", "quantize", "gemm", "sweep", "qerror", "delayed70b"], default="step",
+    ap.add_argument("--mode", choices=["step", "quantize", "gemm", "sweep", "qerror", "delayed70b", "multi"],
+                    default="step",
                     help="step: the benchmark line (default); quantize / gemm: one kernel; sweep: roofline sweep; "
-                         "qerror: quantization error per recipe; delayed70b: the delayed-scaling 70B FFN step")
+                         "qerror: quantization error per recipe; delayed70b: the delayed-scaling 70B FFN step; "
+                         "multi: 8 small tensors, separate quantize calls against one fp8q_quantize_multi")
     ap.add_argument("--kind", choices=list(KINDS), default="mx")
     ap.add_argument("--rows", type=int, default=16384)
     ap.add_argument("--cols", type=int, default=8192)

@@ -129,6 +129,29 @@ def quantize_into(x: torch.Tensor, qt: QTensor, state: DelayedState | None = Non
     return qt
 
 
+def quantize_multi(jobs, stream=None):
+    """Quantizes several tensors in one call (fp8q_quantize_multi): jobs is a
+    sequence of (x, qt) or (x, qt, state) with qt preallocated as for
+    quantize_into; the outputs equal those of quantize_into on each."""
+    jobs = list(jobs)
+    arr = (L.QuantizeJob * max(len(jobs), 1))()
+    keep = []
+    for i, job in enumerate(jobs):
+        x, qt = job[0], job[1]
+        state = job[2] if len(job) > 2 else None
+        if x.dtype != torch.bfloat16 or x.dim() != 2 or not x.is_contiguous():
+            raise ValueError("x must be a contiguous 2-D bf16 tensor")
+        ct = qt.c_struct()
+        keep.append(ct)
+        arr[i].recipe = L.Recipe(qt.kind, qt.fmt, int(qt.rowwise), int(qt.colwise))
+        arr[i].x = x.data_ptr()
+        arr[i].rows, arr[i].cols = x.shape[0], x.shape[1]
+        arr[i].state = state.handle if state is not None else None
+        arr[i].out = ctypes.pointer(ct)
+    L.check(L.load().fp8q_quantize_multi(arr, len(jobs), _stream(stream)), "fp8q_quantize_multi")
+    return [job[1] for job in jobs]
+
+
 def quantize(x: torch.Tensor, kind: int, fmt: int = E4M3, rowwise: bool = True, colwise: bool = False,
              state: DelayedState | None = None, stream=None) -> QTensor:
     qt = alloc(kind, fmt, x.shape[0], x.shape[1], rowwise, colwise, device=x.device)

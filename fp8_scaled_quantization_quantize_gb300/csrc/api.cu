@@ -55,6 +55,66 @@ size_t copy_scale_bytes(int kind, int64_t R, int64_t C) {
     }
 }
 
+// Checks one quantize call's arguments (fp8q_quantize's contract) and fills
+// the kernels' arguments; writes nothing.
+fp8q_status prepare_quantize(const fp8q_recipe* rc, const void* x, int64_t rows, int64_t cols,
+                             const fp8q_delayed_state* st, const fp8q_tensor* out, QuantArgs& a) {
+    if (!rc || !out) return FP8Q_ERR_ARG;
+    if (!valid_kind(rc->kind) || !valid_fmt(rc->fmt)) return FP8Q_ERR_ARG;
+    const bool row = rc->want_rowwise != 0, col = rc->want_colwise != 0;
+    if (!row && !col) return FP8Q_ERR_ARG;
+    if (rows < 0 || cols < 0) return FP8Q_ERR_SHAPE;
+    if (rows > 0 && cols > 0 && rows > kMaxElems / cols) return FP8Q_ERR_SHAPE;
+    if (cols % 16 != 0) return FP8Q_ERR_SHAPE;
+    if (col && rows % 16 != 0) return FP8Q_ERR_SHAPE;
+    const bool empty = rows == 0 || cols == 0;
+    const bool per_tensor = is_pertensor(rc->kind);
+    if (!out->counters) return FP8Q_ERR_ARG;
+    if (((uintptr_t)out->counters & 7u) != 0) return FP8Q_ERR_ALIGN;
+    if (!empty) {
+        if (!x || (row && !out->data_row) || (col && !out->data_col)) return FP8Q_ERR_ARG;
+        if (!aligned16(x) || (row && !aligned16(out->data_row)) || (col && !aligned16(out->data_col)))
+            return FP8Q_ERR_ALIGN;
+    }
+    if (per_tensor) {
+        if (!out->amax || !out->scale || !out->scale_inv) return FP8Q_ERR_ARG;
+        if (((uintptr_t)out->amax | (uintptr_t)out->scale | (uintptr_t)out->scale_inv) & 3u) return FP8Q_ERR_ALIGN;
+    } else if (!empty) {
+        if ((row && !out->scale_row) || (col && !out->scale_col)) return FP8Q_ERR_ARG;
+        if ((row && !aligned16(out->scale_row)) || (col && !aligned16(out->scale_col))) return FP8Q_ERR_ALIGN;
+    }
+    if (rc->kind == FP8Q_PERTENSOR_DELAYED) {
+        if (!st) return FP8Q_ERR_ARG;
+        if (st->fmt != rc->fmt) return FP8Q_ERR_DTYPE;
+        int dev = -1;
+        cudaGetDevice(&dev);
+        if (dev != st->device) return FP8Q_ERR_ARG;
+    }
+    memset(&a, 0, sizeof(a));
+    a.x = (const uint16_t*)x;
+    a.R = rows;
+    a.C = cols;
+    a.q_row = row ? (uint8_t*)out->data_row : nullptr;
+    a.q_col = col ? (uint8_t*)out->data_col : nullptr;
+    a.s_row = row ? out->scale_row : nullptr;
+    a.s_col = col ? out->scale_col : nullptr;
+    a.amax = out->amax;
+    a.scale = out->scale;
+    a.scale_inv = out->scale_inv;
+    a.counters = out->counters;
+    a.st = (rc->kind == FP8Q_PERTENSOR_DELAYED && st) ? st->dev : nullptr;
+    a.tiles_r = empty ? 0 : cdiv(rows, 128);
+    a.tiles_c = empty ? 0 : cdiv(cols, 128);
+    return FP8Q_OK;
+}
+
+void set_meta(const fp8q_recipe* rc, int64_t rows, int64_t cols, fp8q_tensor* out) {
+    out->rows = rows;
+    out->cols = cols;
+    out->fmt = rc->fmt;
+    out->kind = rc->kind;
+}
+
 }  // namespace
 
 extern "C" {
@@ -87,59 +147,29 @@ fp8q_status fp8q_scale_bytes(const fp8q_recipe* rc, int64_t rows, int64_t cols, 
 
 fp8q_status fp8q_quantize(const fp8q_recipe* rc, const void* x, int64_t rows, int64_t cols,
                           fp8q_delayed_state* st, fp8q_tensor* out, void* stream) {
-    if (!rc || !out) return FP8Q_ERR_ARG;
-    if (!valid_kind(rc->kind) || !valid_fmt(rc->fmt)) return FP8Q_ERR_ARG;
-    const bool row = rc->want_rowwise != 0, col = rc->want_colwise != 0;
-    if (!row && !col) return FP8Q_ERR_ARG;
-    if (rows < 0 || cols < 0) return FP8Q_ERR_SHAPE;
-    if (rows > 0 && cols > 0 && rows > kMaxElems / cols) return FP8Q_ERR_SHAPE;
-    if (cols % 16 != 0) return FP8Q_ERR_SHAPE;
-    if (col && rows % 16 != 0) return FP8Q_ERR_SHAPE;
-    const bool empty = rows == 0 || cols == 0;
-    const bool per_tensor = is_pertensor(rc->kind);
-    if (!out->counters) return FP8Q_ERR_ARG;
-    if (((uintptr_t)out->counters & 7u) != 0) return FP8Q_ERR_ALIGN;
-    if (!empty) {
-        if (!x || (row && !out->data_row) || (col && !out->data_col)) return FP8Q_ERR_ARG;
-        if (!aligned16(x) || (row && !aligned16(out->data_row)) || (col && !aligned16(out->data_col)))
-            return FP8Q_ERR_ALIGN;
-    }
-    if (per_tensor) {
-        if (!out->amax || !out->scale || !out->scale_inv) return FP8Q_ERR_ARG;
-        if (((uintptr_t)out->amax | (uintptr_t)out->scale | (uintptr_t)out->scale_inv) & 3u) return FP8Q_ERR_ALIGN;
-    } else if (!empty) {
-        if ((row && !out->scale_row) || (col && !out->scale_col)) return FP8Q_ERR_ARG;
-        if ((row && !aligned16(out->scale_row)) || (col && !aligned16(out->scale_col))) return FP8Q_ERR_ALIGN;
-    }
-    if (rc->kind == FP8Q_PERTENSOR_DELAYED) {
-        if (!st) return FP8Q_ERR_ARG;
-        if (st->fmt != rc->fmt) return FP8Q_ERR_DTYPE;
-        int dev = -1;
-        cudaGetDevice(&dev);
-        if (dev != st->device) return FP8Q_ERR_ARG;
-    }
-
     QuantArgs a;
-    memset(&a, 0, sizeof(a));
-    a.x = (const uint16_t*)x;
-    a.R = rows;
-    a.C = cols;
-    a.q_row = row ? (uint8_t*)out->data_row : nullptr;
-    a.q_col = col ? (uint8_t*)out->data_col : nullptr;
-    a.s_row = row ? out->scale_row : nullptr;
-    a.s_col = col ? out->scale_col : nullptr;
-    a.amax = out->amax;
-    a.scale = out->scale;
-    a.scale_inv = out->scale_inv;
-    a.counters = out->counters;
-    a.st = st ? st->dev : nullptr;
-    a.tiles_r = empty ? 0 : cdiv(rows, 128);
-    a.tiles_c = empty ? 0 : cdiv(cols, 128);
-    out->rows = rows;
-    out->cols = cols;
-    out->fmt = rc->fmt;
-    out->kind = rc->kind;
+    const fp8q_status v = prepare_quantize(rc, x, rows, cols, st, out, a);
+    if (v != FP8Q_OK) return v;
+    set_meta(rc, rows, cols, out);
     return launch_quantize(rc, a, st ? st->dev : nullptr, (cudaStream_t)stream);
+}
+
+fp8q_status fp8q_quantize_multi(const fp8q_quantize_job* jobs, int n, void* stream) {
+    if (n < 0 || n > FP8Q_MULTI_MAX || (n > 0 && !jobs)) return FP8Q_ERR_ARG;
+    QuantArgs a[FP8Q_MULTI_MAX];
+    const fp8q_recipe* rcs[FP8Q_MULTI_MAX];
+    DelayedDev* sts[FP8Q_MULTI_MAX];
+    for (int i = 0; i < n; ++i) {  // every job is checked before anything is enqueued
+        const fp8q_quantize_job& j = jobs[i];
+        const fp8q_status v = prepare_quantize(&j.recipe, j.x, j.rows, j.cols, j.state, j.out, a[i]);
+        if (v != FP8Q_OK) return v;
+        for (int k = 0; k < i; ++k)
+            if (jobs[k].out == j.out || (jobs[k].state && jobs[k].state == j.state)) return FP8Q_ERR_ARG;
+        rcs[i] = &j.recipe;
+        sts[i] = j.state ? j.state->dev : nullptr;
+    }
+    for (int i = 0; i < n; ++i) set_meta(&jobs[i].recipe, jobs[i].rows, jobs[i].cols, jobs[i].out);
+    return launch_quantize_multi(n, rcs, a, sts, (cudaStream_t)stream);
 }
 
 fp8q_status fp8q_delayed_create(int history_len, int fmt, int margin, fp8q_delayed_state** out) {

@@ -18,6 +18,8 @@
 // block (code 127 / 1.0).
 #include <string.h>
 
+#include <mutex>
+
 #include "fp8q_internal.cuh"
 #include "ptx.cuh"
 #include "umma.cuh"
@@ -307,6 +309,93 @@ __device__ __forceinline__ uint32_t count_at_max(const uint4 (&v)[8], uint32_t m
     return c;
 }
 
+// The rare paths of a tile -- a NaN / Inf in the data, or a blockwise divisor
+// below the reciprocal shortcut's range -- out of line, so that the loop's
+// common path stays compact in the instruction cache.  Arrays travel by value
+// in small structs: the common path never takes their address, so they stay
+// in registers there.
+struct Row8 {
+    uint4 v[8];
+};
+struct RowCodes {
+    uint2 q[8];
+    uint32_t nsat;
+};
+struct MaxNf {
+    uint32_t m, nnf, vnf;
+};
+struct Col32 {
+    uint32_t w[32];
+};
+struct ColCodes {
+    uint32_t o0[8], o1[8];
+    uint32_t ns;
+};
+
+template <int J0, int J1>
+__device__ __noinline__ MaxNf exact_max_rare(Row8 r) {
+    MaxNf e;
+    e.nnf = 0;
+    e.vnf = 0;
+    e.m = exact_max<J0, J1>(r.v, e.nnf, e.vnf);
+    return e;
+}
+
+template <int KIND, int FMT>
+__device__ __noinline__ RowCodes row_codes_rare(Row8 r, uint32_t vnf, Factor f0, Factor f1, bool s0, bool s1) {
+    RowCodes out;
+    out.nsat = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const Factor f = (j < 4) ? f0 : f1;
+        if ((vnf >> j) & 1u)
+            out.q[j] = convert8<KIND, FMT>(r.v[j], f.k, out.nsat, true);
+        else
+            out.q[j] = convert8_fast<KIND, FMT, false>(r.v[j], f, out.nsat, (j < 4) ? s0 : s1);
+    }
+    return out;
+}
+
+// Largest finite magnitudes of the two columns of c (NaN / Inf excluded).
+__device__ __noinline__ uint2 col_exact_max_rare(Col32 c) {
+    uint32_t m0 = 0, m1 = 0;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        const uint32_t lo = c.w[j] & 0x7FFFu, hi = (c.w[j] >> 16) & 0x7FFFu;
+        m0 = (lo < 0x7F80u && lo > m0) ? lo : m0;
+        m1 = (hi < 0x7F80u && hi > m1) ? hi : m1;
+    }
+    return make_uint2(m0, m1);
+}
+
+// Codes of 32 rows of two columns element by element (exact saturation
+// counts, NaN signs kept).
+template <int KIND, int FMT>
+__device__ __noinline__ ColCodes col_codes_rare(Col32 c, float k0, float k1) {
+    ColCodes out;
+    out.ns = 0;
+    const uint32_t* w = c.w;
+#pragma unroll
+    for (int j = 0; j < 32; j += 4) {
+        float a0 = bf16_lo(w[j]), a1 = bf16_lo(w[j + 1]), a2 = bf16_lo(w[j + 2]), a3 = bf16_lo(w[j + 3]);
+        float b0 = bf16_hi(w[j]), b1 = bf16_hi(w[j + 1]), b2 = bf16_hi(w[j + 2]), b3 = bf16_hi(w[j + 3]);
+        float ya0 = scaled<KIND>(a0, k0), ya1 = scaled<KIND>(a1, k0), ya2 = scaled<KIND>(a2, k0),
+              ya3 = scaled<KIND>(a3, k0);
+        float yb0 = scaled<KIND>(b0, k1), yb1 = scaled<KIND>(b1, k1), yb2 = scaled<KIND>(b2, k1),
+              yb3 = scaled<KIND>(b3, k1);
+        out.ns += sat_count<FMT>(a0, ya0) + sat_count<FMT>(a1, ya1) + sat_count<FMT>(a2, ya2) +
+                  sat_count<FMT>(a3, ya3) + sat_count<FMT>(b0, yb0) + sat_count<FMT>(b1, yb1) +
+                  sat_count<FMT>(b2, yb2) + sat_count<FMT>(b3, yb3);
+        // rebuild the bf16 pairs of each output column to reuse nan_sign2
+        const uint32_t a01 = (w[j] & 0xFFFFu) | (w[j + 1] << 16), a23 = (w[j + 2] & 0xFFFFu) | (w[j + 3] << 16);
+        const uint32_t b01 = (w[j] >> 16) | (w[j + 1] & 0xFFFF0000u), b23 = (w[j + 2] >> 16) | (w[j + 3] & 0xFFFF0000u);
+        const uint32_t qa = cvt4<FMT>(ya0, ya1, ya2, ya3), qb = cvt4<FMT>(yb0, yb1, yb2, yb3);
+        out.o0[j / 4] = nan_sign2(qa & 0xFFFFu, a01) | (nan_sign2(qa >> 16, a23) << 16);
+        out.o1[j / 4] = nan_sign2(qb & 0xFFFFu, b01) | (nan_sign2(qb >> 16, b23) << 16);
+    }
+    return out;
+}
+
 template <int KIND, int FMT, bool ROW, bool COL>
 __global__ void __launch_bounds__(kThreads, 2)
     quant_tile_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmrow,
@@ -395,11 +484,34 @@ __global__ void __launch_bounds__(kThreads, 2)
             if constexpr (KIND == kMX) {
                 mq[0] = fold16(p0);
                 mq[1] = fold16(p1);
-                if (mq[0] >= 0x7F80u) mq[0] = exact_max<0, 4>(v, nnf, vnf);
-                if (mq[1] >= 0x7F80u) mq[1] = exact_max<4, 8>(v, nnf, vnf);
+                if (mq[0] >= 0x7F80u || mq[1] >= 0x7F80u) {
+                    Row8 r;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) r.v[j] = v[j];
+                    if (mq[0] >= 0x7F80u) {
+                        const MaxNf e = exact_max_rare<0, 4>(r);
+                        mq[0] = e.m;
+                        nnf += e.nnf;
+                        vnf |= e.vnf;
+                    }
+                    if (mq[1] >= 0x7F80u) {
+                        const MaxNf e = exact_max_rare<4, 8>(r);
+                        mq[1] = e.m;
+                        nnf += e.nnf;
+                        vnf |= e.vnf;
+                    }
+                }
             } else {
                 mq[0] = fold16(max_u16x2(p0, p1));
-                if (mq[0] >= 0x7F80u) mq[0] = exact_max<0, 8>(v, nnf, vnf);
+                if (mq[0] >= 0x7F80u) {
+                    Row8 r;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) r.v[j] = v[j];
+                    const MaxNf e = exact_max_rare<0, 8>(r);
+                    mq[0] = e.m;
+                    nnf += e.nnf;
+                    vnf |= e.vnf;
+                }
                 mq[1] = mq[0];
             }
         }
@@ -467,14 +579,13 @@ __global__ void __launch_bounds__(kThreads, 2)
                     if (mh[1] == mq[0]) nsat_rc += count_at_max<4, 8>(v, mq[0]);
                 }
             } else {
+                Row8 r;
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const Factor f = (j < 4) ? f0 : f1;
-                    if ((vnf >> j) & 1u)
-                        q[j] = convert8<KIND, FMT>(v[j], f.k, nsat_rc, true);
-                    else
-                        q[j] = convert8_fast<KIND, FMT, false>(v[j], f, nsat_rc, (j < 4) ? s0 : s1);
-                }
+                for (int j = 0; j < 8; ++j) r.v[j] = v[j];
+                const RowCodes rc = row_codes_rare<KIND, FMT>(r, vnf, f0, f1, s0, s1);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) q[j] = rc.q[j];
+                nsat_rc += rc.nsat;
             }
             if (ROW) nsat_row += nsat_rc;  // a transposed column copy reports no count of its own
         }
@@ -520,13 +631,12 @@ __global__ void __launch_bounds__(kThreads, 2)
                 own1 = m1;
                 col_nf = m0 >= 0x7F80u || m1 >= 0x7F80u;
                 if (col_nf) {  // NaN / Inf: exact finite maxima
-                    m0 = m1 = 0;
+                    Col32 cw;
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const uint32_t lo = w[j] & 0x7FFFu, hi = (w[j] >> 16) & 0x7FFFu;
-                        m0 = (lo < 0x7F80u && lo > m0) ? lo : m0;
-                        m1 = (hi < 0x7F80u && hi > m1) ? hi : m1;
-                    }
+                    for (int j = 0; j < 32; ++j) cw.w[j] = w[j];
+                    const uint2 m = col_exact_max_rare(cw);
+                    m0 = m.x;
+                    m1 = m.y;
                 }
                 const int64_t cc = c0 + 2 * p;
                 if constexpr (KIND == kMX) {
@@ -593,24 +703,16 @@ __global__ void __launch_bounds__(kThreads, 2)
                     }
                 }
             } else {
+                Col32 cw;
 #pragma unroll
-                for (int j = 0; j < 32; j += 4) {
-                    float a0 = bf16_lo(w[j]), a1 = bf16_lo(w[j + 1]), a2 = bf16_lo(w[j + 2]), a3 = bf16_lo(w[j + 3]);
-                    float b0 = bf16_hi(w[j]), b1 = bf16_hi(w[j + 1]), b2 = bf16_hi(w[j + 2]), b3 = bf16_hi(w[j + 3]);
-                    float ya0 = scaled<KIND>(a0, k0), ya1 = scaled<KIND>(a1, k0), ya2 = scaled<KIND>(a2, k0),
-                          ya3 = scaled<KIND>(a3, k0);
-                    float yb0 = scaled<KIND>(b0, k1), yb1 = scaled<KIND>(b1, k1), yb2 = scaled<KIND>(b2, k1),
-                          yb3 = scaled<KIND>(b3, k1);
-                    ns += sat_count<FMT>(a0, ya0) + sat_count<FMT>(a1, ya1) + sat_count<FMT>(a2, ya2) +
-                          sat_count<FMT>(a3, ya3) + sat_count<FMT>(b0, yb0) + sat_count<FMT>(b1, yb1) +
-                          sat_count<FMT>(b2, yb2) + sat_count<FMT>(b3, yb3);
-                    // rebuild the bf16 pairs of each output column to reuse nan_sign2
-                    const uint32_t a01 = (w[j] & 0xFFFFu) | (w[j + 1] << 16), a23 = (w[j + 2] & 0xFFFFu) | (w[j + 3] << 16);
-                    const uint32_t b01 = (w[j] >> 16) | (w[j + 1] & 0xFFFF0000u), b23 = (w[j + 2] >> 16) | (w[j + 3] & 0xFFFF0000u);
-                    const uint32_t qa = cvt4<FMT>(ya0, ya1, ya2, ya3), qb = cvt4<FMT>(yb0, yb1, yb2, yb3);
-                    o0[j / 4] = nan_sign2(qa & 0xFFFFu, a01) | (nan_sign2(qa >> 16, a23) << 16);
-                    o1[j / 4] = nan_sign2(qb & 0xFFFFu, b01) | (nan_sign2(qb >> 16, b23) << 16);
+                for (int j = 0; j < 32; ++j) cw.w[j] = w[j];
+                const ColCodes cc2 = col_codes_rare<KIND, FMT>(cw, k0, k1);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    o0[j] = cc2.o0[j];
+                    o1[j] = cc2.o1[j];
                 }
+                ns += cc2.ns;
             }
             nsat_col += ns;
         }
@@ -911,6 +1013,7 @@ fp8q_status launch_tile(const QuantArgs& a, cudaStream_t s) {
             return FP8Q_ERR_CUDA;
     }
     int64_t grid = (int64_t)num_sms() * 2;
+    if (a.grid_cap > 0 && a.grid_cap < grid) grid = a.grid_cap;
     if (ntiles < grid) grid = ntiles;
     if (grid < 1) grid = 1;
     kern<<<(unsigned)grid, kThreads, kTileSmem, s>>>(tm, trow, tcol, a);
@@ -1000,6 +1103,55 @@ fp8q_status launch_quantize(const fp8q_recipe* rc, const QuantArgs& a, DelayedDe
         default:
             return FP8Q_ERR_ARG;
     }
+}
+
+// Fork / join of fp8q_quantize_multi: one library-owned stream per job
+// (created once per device), the tile passes' two resident CTAs per SM
+// shared out by the jobs' tile counts.
+namespace {
+std::mutex g_multi_mu;
+struct MultiStreams {
+    cudaStream_t s[FP8Q_MULTI_MAX];
+    cudaEvent_t fork, join[FP8Q_MULTI_MAX];
+    bool ready;
+};
+MultiStreams g_multi[64];
+}  // namespace
+
+fp8q_status launch_quantize_multi(int n, const fp8q_recipe* const* rcs, QuantArgs* a, DelayedDev* const* sts,
+                                  cudaStream_t s) {
+    if (n == 0) return FP8Q_OK;
+    if (n == 1) return launch_quantize(rcs[0], a[0], sts[0], s);
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FP8Q_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_multi_mu);
+    MultiStreams& m = g_multi[dev];
+    if (!m.ready) {
+        for (int i = 0; i < FP8Q_MULTI_MAX; ++i) {
+            if (cudaStreamCreateWithFlags(&m.s[i], cudaStreamNonBlocking) != cudaSuccess ||
+                cudaEventCreateWithFlags(&m.join[i], cudaEventDisableTiming) != cudaSuccess)
+                return FP8Q_ERR_CUDA;
+        }
+        if (cudaEventCreateWithFlags(&m.fork, cudaEventDisableTiming) != cudaSuccess) return FP8Q_ERR_CUDA;
+        m.ready = true;
+    }
+    int64_t total = 0;
+    for (int i = 0; i < n; ++i) total += a[i].tiles_r * a[i].tiles_c;
+    const int64_t budget = (int64_t)num_sms() * 2;
+    if (cudaEventRecord(m.fork, s) != cudaSuccess) return FP8Q_ERR_CUDA;
+    fp8q_status r = FP8Q_OK;
+    for (int i = 0; i < n; ++i) {
+        const int64_t tiles = a[i].tiles_r * a[i].tiles_c;
+        a[i].grid_cap = total > 0 ? (budget * tiles / total > 0 ? budget * tiles / total : 1) : 0;
+        if (cudaStreamWaitEvent(m.s[i], m.fork, 0) != cudaSuccess) return FP8Q_ERR_CUDA;
+        const fp8q_status ri = launch_quantize(rcs[i], a[i], sts[i], m.s[i]);
+        if (ri != FP8Q_OK && r == FP8Q_OK) r = ri;
+        // join even after a failed launch: the caller's stream never waits on a
+        // job that was not enqueued behind the fork
+        if (cudaEventRecord(m.join[i], m.s[i]) != cudaSuccess || cudaStreamWaitEvent(s, m.join[i], 0) != cudaSuccess)
+            return FP8Q_ERR_CUDA;
+    }
+    return r;
 }
 
 fp8q_status launch_div_selftest(const float* d, int64_t nd, int fmt, unsigned long long* mismatch, cudaStream_t s) {

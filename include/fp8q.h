@@ -175,6 +175,32 @@ FP8Q_API fp8q_status fp8q_quantize(const fp8q_recipe* recipe, const void* x, int
                           fp8q_delayed_state* st, fp8q_tensor* out, void* stream);
 
 /*
+ * Several quantize calls as one: the same outputs as fp8q_quantize on each
+ * job in order (no counterpart on the pages; a launch arrangement), but the
+ * jobs' tile passes run side by side, their resident CTAs shared out in
+ * proportion to each job's 128x128 tiles, so that a small tensor does not
+ * leave SMs idle while its kernel fills and drains (the Llama-3-8B
+ * up-projection quantizes X of 1024 tiles and W of 3584).  Every job is
+ * checked as fp8q_quantize checks its arguments before anything is enqueued;
+ * 1 <= n <= FP8Q_MULTI_MAX (n = 0 does nothing); no two jobs may share an
+ * output struct or a delayed state.  The work is ordered after what `stream`
+ * holds and before what is enqueued on it later: the call records an event on
+ * `stream`, runs each job on a library-owned stream of the current device
+ * that waits for it, and makes `stream` wait for each job's end (so a CUDA
+ * graph capture of `stream` takes the fork and join in).  Calls from several
+ * host threads are serialised.
+ */
+#define FP8Q_MULTI_MAX 16
+typedef struct {
+    fp8q_recipe recipe;
+    const void* x;             /* bf16 [rows][cols], device */
+    int64_t rows, cols;
+    fp8q_delayed_state* state; /* delayed recipe only, else NULL */
+    fp8q_tensor* out;          /* host struct of device buffers, as for fp8q_quantize */
+} fp8q_quantize_job;
+FP8Q_API fp8q_status fp8q_quantize_multi(const fp8q_quantize_job* jobs, int n, void* stream);
+
+/*
  * Creates a delayed-scaling state on the current device: history_len in
  * [1, 4096] (the [guide] sec. 2.1 history; 16 by default in the tests),
  * margin in [0, 64] (s = fmax / max(history) * 2^-margin; [essay] sec. 3.3

@@ -60,6 +60,9 @@ def test_scale_bytes(lib):
     # MX: 512-byte tiles of 128 rows x 4 scale columns
     assert _sb(lib, L.MXFP8_1x32, 8192, 4096) == (L.OK, 64 * 32 * 512, 32 * 64 * 512)
     assert _sb(lib, L.MXFP8_1x32, 130, 48, True, False) == (L.OK, 2 * 1 * 512, 0)
+    # per-channel: one fp32 per row of the copy, padded to 128
+    assert _sb(lib, L.PERCHANNEL_CURRENT, 4096, 14336) == (L.OK, 4096 * 4, 14336 * 4)
+    assert _sb(lib, L.PERCHANNEL_CURRENT, 200, 272) == (L.OK, 256 * 4, 384 * 4)
     assert _sb(lib, 9, 16, 16)[0] == L.ERR_ARG
     assert _sb(lib, L.MXFP8_1x32, -1, 16)[0] == L.ERR_SHAPE
 
@@ -86,6 +89,30 @@ def test_quantize_validation_without_gpu(lib):
     assert _q(lib, t=t) == L.ERR_ALIGN                      # misaligned scale buffer
     assert _q(lib, kind=L.PERTENSOR_DELAYED) == L.ERR_ARG   # delayed needs a state
     assert _q(lib, rows=1 << 30, cols=1 << 11) == L.ERR_SHAPE
+
+
+def test_quantize_multi_validation_without_gpu(lib):
+    """Every job is checked before anything is enqueued; the same checks as
+    fp8q_quantize, plus the job count and no shared outputs or states."""
+    t1 = L.Tensor(16, 32, 64, 128, 256, 272, 288, 512, 0, 0, 0, 0)
+    t2 = L.Tensor(16, 32, 64, 128, 256, 272, 288, 512, 0, 0, 0, 0)
+
+    def jobs(*specs):
+        arr = (L.QuantizeJob * max(len(specs), 1))()
+        for i, (kind, rows, cols, x, t) in enumerate(specs):
+            arr[i].recipe = L.Recipe(kind, L.E4M3, 1, 0)
+            arr[i].x, arr[i].rows, arr[i].cols, arr[i].state = x, rows, cols, None
+            arr[i].out = ctypes.pointer(t)
+        return arr
+
+    m = lambda arr, n: lib.fp8q_quantize_multi(arr, n, None)
+    assert m(jobs(), 0) == L.OK                                              # nothing to do
+    assert m(jobs(), -1) == L.ERR_ARG
+    assert m(jobs(), L.MULTI_MAX + 1) == L.ERR_ARG
+    assert m(jobs((L.MXFP8_1x32, 32, 32, 16, t1), (L.MXFP8_1x32, 32, 40, 16, t2)), 2) == L.ERR_SHAPE
+    assert m(jobs((L.MXFP8_1x32, 32, 32, 16, t1), (L.BLOCK_1x128, 32, 32, 24, t2)), 2) == L.ERR_ALIGN
+    assert m(jobs((L.MXFP8_1x32, 32, 32, 16, t1), (L.PERTENSOR_DELAYED, 32, 32, 16, t2)), 2) == L.ERR_ARG
+    assert m(jobs((L.MXFP8_1x32, 32, 32, 16, t1), (L.BLOCK_1x128, 32, 32, 16, t1)), 2) == L.ERR_ARG  # same out
 
 
 def test_gemm_validation_without_gpu(lib):

@@ -211,3 +211,69 @@ def test_delayed_llama70b_32_steps():
             assert np.array_equal(np.float32(hist), ostates[i].hist), ctx
         if t == 20:
             assert any(ostates[i].scale < np.float32(448.0) for i in range(2))
+
+
+def test_quantize_multi_matches_separate_calls_and_oracle():
+    """fp8q_quantize_multi over one job of every recipe (mixed shapes, both
+    formats, a delayed state): every output equals the oracle's and what
+    separate fp8q_quantize calls write, and the delayed state advances once."""
+    api = _api()
+    specs = [  # kind, fmt, shape, rowwise, colwise
+        (O.BLOCK_1x128, O.E4M3, (400, 1040), True, True),
+        (O.BLOCK_128x128, O.E4M3, (1040, 400), True, True),
+        (O.PERTENSOR_CURRENT, O.E5M2, (272, 400), True, True),
+        (O.PERTENSOR_DELAYED, O.E4M3, (256, 384), True, True),
+        (O.MXFP8_1x32, O.E4M3, (208, 288), True, True),
+        (O.PERCHANNEL_CURRENT, O.E5M2, (336, 528), True, False),
+    ]
+    xs = [_mixed(sh, 90 + i) for i, (_, _, sh, _, _) in enumerate(specs)]
+    st, st2 = api.DelayedState(16, O.E4M3, 0), api.DelayedState(16, O.E4M3, 0)
+    ost = O.Delayed(16, O.E4M3, 0)
+    for s in (st, st2):     # one earlier step, so the multi call casts with a real history scale
+        s.update(torch.tensor([3.5], dtype=torch.float32, device="cuda"))
+    ost.update(3.5)
+    qts = [api.alloc(k, f, *sh, r, c, "cuda") for k, f, sh, r, c in specs]
+    xd = [x.cuda() for x in xs]
+    jobs = [(x, q, st) if k == O.PERTENSOR_DELAYED else (x, q) for x, q, (k, *_) in zip(xd, qts, specs)]
+    api.quantize_multi(jobs)
+    for (k, f, sh, r, c), x, q, xdev in zip(specs, xs, qts, xd):
+        got = gpu_outputs(q)
+        ref = O.quantize(k, f, bits_of(x), r, c, state=ost if k == O.PERTENSOR_DELAYED else None)
+        assert_quant_equal(k, got, ref, r, c, ctx=f"multi kind {k}")
+        one = gpu_outputs(api.quantize(xdev, k, f, r, c, state=st2 if k == O.PERTENSOR_DELAYED else None))
+        assert [got[kk] for kk in ("sat_row", "sat_col", "nonfinite")] == \
+            [one[kk] for kk in ("sat_row", "sat_col", "nonfinite")], k
+        for key in ("data_row", "data_col", "scale_row_bytes", "scale_col_bytes"):
+            if key in one:
+                assert np.array_equal(got[key], one[key]), (k, key)
+    h, head, s, si = st.get()
+    assert head == ost.head and np.float32(s) == ost.scale
+    assert api.device_errors() == 0
+
+
+def test_quantize_multi_in_a_cuda_graph():
+    """The multi call's fork and join are captured into a CUDA graph with the
+    stream: replays on new inputs give the outputs of direct calls."""
+    api = _api()
+    X = inputs.normal_bf16((512, 1024), 7).cuda()
+    W = inputs.normal_bf16((1536, 1024), 8, 0.02).cuda()
+    qx = api.alloc(O.BLOCK_1x128, O.E4M3, 512, 1024, True, True, "cuda")
+    qw = api.alloc(O.BLOCK_128x128, O.E4M3, 1536, 1024, True, True, "cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        api.quantize_multi([(X, qx), (W, qw)])      # warm-up: creates the library's streams
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        api.quantize_multi([(X, qx), (W, qw)])
+    X.copy_(inputs.normal_bf16((512, 1024), 17).cuda())
+    W.copy_(inputs.normal_bf16((1536, 1024), 18, 0.02).cuda())
+    g.replay()
+    torch.cuda.synchronize()
+    gx, gw = gpu_outputs(qx), gpu_outputs(qw)
+    rx = gpu_outputs(api.quantize(X, O.BLOCK_1x128, O.E4M3, True, True))
+    rw = gpu_outputs(api.quantize(W, O.BLOCK_128x128, O.E4M3, True, True))
+    for got, ref in ((gx, rx), (gw, rw)):
+        for key in ("data_row", "data_col", "scale_row_bytes", "scale_col_bytes"):
+            assert np.array_equal(got[key], ref[key]), key
+    assert api.device_errors() == 0
