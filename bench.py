@@ -266,23 +266,47 @@ def run_ours(args):
     ms_step = max_over_ranks(statistics.mean(e[0].elapsed_time(e[2]) for e in evs), world)
     errs = api.device_errors()
 
-    # ---- end to end through the C ABI with host buffers
+    # ---- end to end through the C ABI with host buffers.  The host link (about
+    # 200 GB/s each way, measured) dominates, so the step overlaps what it can:
+    # X's quantize runs while W is still crossing, and the GEMM runs in four
+    # column blocks of Y (api.row_block of W), each copied back while the next
+    # one computes.  Every byte of X, W and Y crosses inside the timed region.
+    NC = 4
+    Nc = F // NC
     Xp, Wp = Xh.pin_memory(), Wh.pin_memory()
-    Yp = torch.empty((T, F), dtype=torch.bfloat16).pin_memory()
+    Yps = [torch.empty((T, Nc), dtype=torch.bfloat16).pin_memory() for _ in range(NC)]
+    Ycs = [torch.empty((T, Nc), dtype=torch.bfloat16, device=dev) for _ in range(NC)]
+    qw_blocks = [api.row_block(qw, c * Nc, (c + 1) * Nc) for c in range(NC)]
+    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+
+    def e2e_step():
+        s_in.wait_stream(stream)
+        X.copy_(Xp, non_blocking=True)
+        with torch.cuda.stream(s_in):
+            W.copy_(Wp, non_blocking=True)
+        api.quantize_into(X, qx, stream=stream)
+        stream.wait_stream(s_in)
+        api.quantize_into(W, qw, stream=stream)
+        for c in range(NC):
+            api.scaled_gemm(qx, False, qw_blocks[c], False, out=Ycs[c], stream=stream)
+            s_out.wait_stream(stream)
+            with torch.cuda.stream(s_out):
+                Yps[c].copy_(Ycs[c], non_blocking=True)
+        stream.wait_stream(s_out)
+
     e2e_ms = []
     for i in range(args.warmup + args.steps):
         flush.zero_()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
-        X.copy_(Xp, non_blocking=True)
-        W.copy_(Wp, non_blocking=True)
-        step()
-        Yp.copy_(Y, non_blocking=True)
+        e2e_step()
         e1.record()
         torch.cuda.synchronize()
         if i >= args.warmup:
             e2e_ms.append(e0.elapsed_time(e1))
-    e2e_step = max_over_ranks(statistics.mean(e2e_ms), world)
+    e2e_step_ms = max_over_ranks(statistics.mean(e2e_ms), world)
+    Yh = torch.cat(Yps, dim=1)
+    e2e_ok = bool(torch.equal(Yh.view(torch.int16), Y.cpu().view(torch.int16)))
 
     # ---- MXFP8 Llama-3-8B MLP layer: quantize (both copies) + fprop / dgrad / wgrad
     mx = None
@@ -413,8 +437,11 @@ def run_ours(args):
                      "peak_source": f"{peak_kind} bf16 burst x2 (dense FP8 / BF16 nominal ratio)",
                      "traffic": measured_traffic("gemm2_blockwise_llama8b_up_proj.md", GEMM2_SOURCES),
                      "traffic_algorithmic": round(T * H + F * H + 2 * T * F + 4 * (T * H / 128 + F * H / 16384))},
-        "e2e": {"value": round(world * flops / e2e_step / 1e9, 1), "unit": UNIT,
-                "h2d_bytes_per_step": X.numel() * 2 + W.numel() * 2, "d2h_bytes_per_step": Y.numel() * 2},
+        "e2e": {"value": round(world * flops / e2e_step_ms / 1e9, 1), "unit": UNIT,
+                "h2d_bytes_per_step": X.numel() * 2 + W.numel() * 2,
+                "d2h_bytes_per_step": sum(y.numel() for y in Yps) * 2, "ms_per_step": round(e2e_step_ms, 4),
+                "result_equals_device_step": e2e_ok,
+                "overlap": "X quantize under W's copy; GEMM in 4 column blocks of Y, each copied back under the next"},
         "gpu_launches": launches,
         "clocks": clocks,
         "device_errors": errs,

@@ -66,6 +66,33 @@ class QTensor:
         return self.data_col is not None
 
 
+def row_block(qt: QTensor, r0: int, r1: int) -> QTensor:
+    """Rows [r0, r1) of a quantized tensor's row-wise copy as a QTensor of its
+    own (views of qt's buffers, nothing copied): a GEMM operand for a block of
+    output columns, e.g. one shard of a weight.  r0 and r1 are multiples of
+    128 (r1 may be qt.rows).  Per-tensor, 128x128, MXFP8 and per-channel
+    copies: their scales of a 128-row block are contiguous; a 1x128 copy's
+    are K-block-major, so it raises."""
+    if qt.data_row is None:
+        raise ValueError("row_block needs the row-wise copy")
+    if not (0 <= r0 < r1 <= qt.rows) or r0 % 128 or (r1 % 128 and r1 != qt.rows):
+        raise ValueError("row block bounds must be multiples of 128 inside the tensor")
+    C = qt.cols
+    sr = None
+    if qt.kind == BLOCK_128x128:
+        per = -(-C // 128) * 4                       # bytes of one 128-row block of scales
+        sr = qt.scale_row[(r0 // 128) * per:(-(-r1 // 128)) * per]
+    elif qt.kind == MXFP8_1x32:
+        per = -(-C // 128) * 512
+        sr = qt.scale_row[(r0 // 128) * per:(-(-r1 // 128)) * per]
+    elif qt.kind == PERCHANNEL_CURRENT:
+        sr = qt.scale_row[r0 * 4:(-(-r1 // 128)) * 128 * 4]
+    elif qt.kind not in (PERTENSOR_CURRENT, PERTENSOR_DELAYED):
+        raise ValueError("row_block: the 1x128 scale layout is not row-contiguous")
+    return QTensor(qt.kind, qt.fmt, r1 - r0, C, qt.data_row[r0:r1], None, sr, None,
+                   qt.amax, qt.scale, qt.scale_inv, qt.counters)
+
+
 def alloc(kind: int, fmt: int, rows: int, cols: int, rowwise: bool = True, colwise: bool = False,
           device="cuda") -> QTensor:
     rb, cb = scale_bytes(kind, rows, cols, rowwise, colwise)

@@ -138,3 +138,27 @@ def test_delayed_validation_without_gpu(lib):
     assert lib.fp8q_delayed_create(16, L.E4M3, -1, ctypes.byref(h)) == L.ERR_ARG
     assert lib.fp8q_delayed_update(None, None, None, None) == L.ERR_ARG
     assert lib.fp8q_cast_f32_bits(0, 16, 9, 16, None) == L.ERR_ARG
+
+
+def test_row_block_views():
+    """api.row_block: views of the row copy and of its scales for a block of
+    128-row groups (host buffers; no GPU needed)."""
+    torch = pytest.importorskip("torch")
+    from fp8_scaled_quantization_quantize_gb300 import api
+    R, C = 1000, 384
+    for kind, per_block in ((L.BLOCK_128x128, 3 * 4), (L.MXFP8_1x32, 3 * 512), (L.PERCHANNEL_CURRENT, 128 * 4)):
+        qt = api.alloc(kind, L.E4M3, R, C, True, False, device="cpu")
+        qt.data_row.copy_(torch.arange(R * C, dtype=torch.int64).reshape(R, C).to(torch.uint8))
+        qt.scale_row.copy_(torch.arange(qt.scale_row.numel(), dtype=torch.int64).to(torch.uint8))
+        b = api.row_block(qt, 256, 1000)
+        assert (b.rows, b.cols, b.kind) == (744, C, kind)
+        assert torch.equal(b.data_row, qt.data_row[256:1000])
+        assert b.scale_row.numel() == 6 * per_block             # 128-row groups 2..7 (the last one partial)
+        assert torch.equal(b.scale_row, qt.scale_row[2 * per_block:8 * per_block])
+    qt = api.alloc(L.BLOCK_1x128, L.E4M3, R, C, True, False, device="cpu")
+    with pytest.raises(ValueError):
+        api.row_block(qt, 0, 128)                                # K-block-major scales
+    qt = api.alloc(L.PERTENSOR_CURRENT, L.E4M3, R, C, True, False, device="cpu")
+    with pytest.raises(ValueError):
+        api.row_block(qt, 64, 512)                               # not a 128-row boundary
+    assert api.row_block(qt, 896, 1000).rows == 104

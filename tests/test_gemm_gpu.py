@@ -192,3 +192,29 @@ def test_full_config_mxfp8_llama8b_mlp(variant):
     _check(api, qx, False, qw, False, sample=s, ctx="cfg3 fprop")
     _check(api, qd, False, qw, True, sample=s, ctx="cfg3 dgrad")
     _check(api, qd, True, qx, True, sample=s, ctx="cfg3 wgrad")
+
+
+@pytest.mark.parametrize("ka,kb", [(2, 3), (4, 4), (0, 0), (5, 5)], ids=["blockwise", "mxfp8", "pertensor", "perchannel"])
+def test_gemm_on_row_blocks_of_b(ka, kb):
+    """D = A . B^T computed on row blocks of B (api.row_block: the weight in
+    column shards of D) equals the matching columns of the whole GEMM bit for
+    bit on the same kernel, and the oracle."""
+    api = _api()
+    # K = 512: a 128-row block of 128x128 scales is 16 bytes, so every block's
+    # scales start 16-byte aligned, as the SM-pair kernel's bulk copies need
+    a = inputs.normal_bf16((512, 512), 31)
+    b = inputs.normal_bf16((1152, 512), 32, 0.02)
+    qa = api.quantize(a.cuda(), ka, O.E4M3, True, False)
+    qb = api.quantize(b.cuda(), kb, O.E4M3, True, False)
+    api.gemm_set_variant(2)
+    try:
+        D = api.scaled_gemm(qa, False, qb, False)
+        for r0, r1 in ((0, 384), (384, 1024), (1024, 1152)):
+            blk = api.row_block(qb, r0, r1)
+            Dc = api.scaled_gemm(qa, False, blk, False)
+            torch.cuda.synchronize()
+            assert torch.equal(Dc.view(torch.int16), D[:, r0:r1].contiguous().view(torch.int16)), (r0, r1)
+            _check(api, qa, False, blk, False, ctx=f"row block {r0}:{r1}")
+    finally:
+        api.gemm_set_variant(0)
+    assert api.device_errors() == 0
