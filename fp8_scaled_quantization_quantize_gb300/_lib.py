@@ -17,7 +17,7 @@ PERTENSOR_CURRENT, PERTENSOR_DELAYED, BLOCK_1x128, BLOCK_128x128, MXFP8_1x32, PE
 EXPORTS = ("fp8q_version", "fp8q_status_str", "fp8q_scale_bytes", "fp8q_quantize", "fp8q_delayed_create",
            "fp8q_delayed_update", "fp8q_delayed_get", "fp8q_delayed_set", "fp8q_delayed_history_len",
            "fp8q_delayed_destroy", "fp8q_scaled_gemm", "fp8q_device_errors", "fp8q_cast_f32_bits", "fp8q_selftest_division",
-           "fp8q_gemm_set_variant", "fp8q_scaled_gemm_mxq", "fp8q_quantize_multi")
+           "fp8q_gemm_set_variant", "fp8q_scaled_gemm_mxq", "fp8q_quantize_multi", "fp8q_quantize_rows")
 MULTI_MAX = 16  # FP8Q_MULTI_MAX
 
 
@@ -66,6 +66,8 @@ def load(path: str = LIB_PATH):
                                    ctypes.POINTER(ctypes.c_size_t)]
     L.fp8q_quantize.restype = i32
     L.fp8q_quantize.argtypes = [ctypes.POINTER(Recipe), P, i64, i64, P, ctypes.POINTER(Tensor), P]
+    L.fp8q_quantize_rows.restype = i32
+    L.fp8q_quantize_rows.argtypes = [ctypes.POINTER(Recipe), P, i64, i64, i64, i64, ctypes.POINTER(Tensor), P]
     L.fp8q_quantize_multi.restype = i32
     L.fp8q_quantize_multi.argtypes = [ctypes.POINTER(QuantizeJob), i32, P]
     L.fp8q_delayed_create.restype = i32

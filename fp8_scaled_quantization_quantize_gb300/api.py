@@ -156,6 +156,18 @@ def quantize_into(x: torch.Tensor, qt: QTensor, state: DelayedState | None = Non
     return qt
 
 
+def quantize_rows_into(x_block: torch.Tensor, qt: QTensor, row0: int, stream=None) -> QTensor:
+    """Quantizes rows row0 .. row0 + len(x_block) - 1 of the tensor whose
+    buffers qt holds (fp8q_quantize_rows); qt.counters are added to."""
+    if x_block.dtype != torch.bfloat16 or x_block.dim() != 2 or not x_block.is_contiguous():
+        raise ValueError("x_block must be a contiguous 2-D bf16 tensor")
+    rc = L.Recipe(qt.kind, qt.fmt, int(qt.rowwise), int(qt.colwise))
+    ct = qt.c_struct()
+    L.check(L.load().fp8q_quantize_rows(ctypes.byref(rc), _ptr(x_block), row0, x_block.shape[0], qt.rows,
+                                        x_block.shape[1], ctypes.byref(ct), _stream(stream)), "fp8q_quantize_rows")
+    return qt
+
+
 def quantize_multi(jobs, stream=None):
     """Quantizes several tensors in one call (fp8q_quantize_multi): jobs is a
     sequence of (x, qt) or (x, qt, state) with qt preallocated as for

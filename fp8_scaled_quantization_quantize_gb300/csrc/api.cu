@@ -105,6 +105,9 @@ fp8q_status prepare_quantize(const fp8q_recipe* rc, const void* x, int64_t rows,
     a.st = (rc->kind == FP8Q_PERTENSOR_DELAYED && st) ? st->dev : nullptr;
     a.tiles_r = empty ? 0 : cdiv(rows, 128);
     a.tiles_c = empty ? 0 : cdiv(cols, 128);
+    a.row0 = 0;  // the whole tensor
+    a.R_total = rows;
+    a.tiles_r_total = a.tiles_r;
     return FP8Q_OK;
 }
 
@@ -152,6 +155,27 @@ fp8q_status fp8q_quantize(const fp8q_recipe* rc, const void* x, int64_t rows, in
     if (v != FP8Q_OK) return v;
     set_meta(rc, rows, cols, out);
     return launch_quantize(rc, a, st ? st->dev : nullptr, (cudaStream_t)stream);
+}
+
+fp8q_status fp8q_quantize_rows(const fp8q_recipe* rc, const void* x, int64_t row0, int64_t rows, int64_t total_rows,
+                               int64_t cols, fp8q_tensor* out, void* stream) {
+    if (!rc || !out) return FP8Q_ERR_ARG;
+    if (is_pertensor(rc->kind) || (rc->kind == FP8Q_PERCHANNEL_CURRENT && rc->want_colwise))
+        return FP8Q_ERR_DTYPE;  // their scales need the whole tensor (or whole columns)
+    if (row0 < 0 || rows < 0 || total_rows < 0 || row0 + rows > total_rows) return FP8Q_ERR_SHAPE;
+    if (row0 % 128 != 0 || (rows % 128 != 0 && row0 + rows != total_rows)) return FP8Q_ERR_SHAPE;
+    if (rc->want_colwise && total_rows % 16 != 0) return FP8Q_ERR_SHAPE;
+    if (total_rows > 0 && cols > 0 && total_rows > kMaxElems / cols) return FP8Q_ERR_SHAPE;
+    QuantArgs a;
+    const fp8q_status v = prepare_quantize(rc, x, rows, cols, nullptr, out, a);
+    if (v != FP8Q_OK) return v;
+    set_meta(rc, total_rows, cols, out);
+    if (rows == 0 || cols == 0) return FP8Q_OK;
+    a.row0 = row0;
+    a.R_total = total_rows;
+    a.tiles_r_total = cdiv(total_rows, 128);
+    a.add_counters = 1;
+    return launch_quantize(rc, a, nullptr, (cudaStream_t)stream);
 }
 
 fp8q_status fp8q_quantize_multi(const fp8q_quantize_job* jobs, int n, void* stream) {

@@ -462,6 +462,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (uint32_t tileid = blockIdx.x; tileid < ntiles; tileid += gridDim.x, ++it) {
         const uint32_t tr = tileid / tiles_c, tc = tileid - tr * tiles_c;
         const int64_t r0 = (int64_t)tr * kTile, c0 = (int64_t)tc * kTile;
+        // the tile's place in the whole tensor (a block of rows starts at row0)
+        const int64_t trg = (int64_t)tr + a.row0 / kTile, r0g = a.row0 + r0;
+        const int64_t tileg = trg * (int64_t)tiles_c + tc;
         const bool ok = mbar_wait_bounded(bar(stg), ph, &abort_flag, &g_quant_errors, 2u, kQuantWaitNs);
         if (__syncthreads_or(!ok)) break;  // the whole CTA leaves together
         uint8_t* stage = qsmem + stg * kStageBytes;
@@ -529,8 +532,8 @@ __global__ void __launch_bounds__(kThreads, 2)
             for (int w = 0; w < kThreads / 32; ++w) mm = mm > red[w] ? mm : red[w];
             kq[0] = kq[1] = block_scale<FMT>(__uint_as_float(mm << 16));
             if (t == 0) {
-                if (ROW) ((float*)a.s_row)[tileid] = kq[0];
-                if (COL) ((float*)a.s_col)[tc * a.tiles_r + tr] = kq[0];
+                if (ROW) ((float*)a.s_row)[tileg] = kq[0];
+                if (COL) ((float*)a.s_col)[tc * a.tiles_r_total + trg] = kq[0];
             }
         } else if constexpr (KIND == kB1) {
             rowred[hh * kTile + rr] = mq[0];
@@ -538,12 +541,12 @@ __global__ void __launch_bounds__(kThreads, 2)
             const uint32_t m = max(rowred[rr], rowred[kTile + rr]);
             mq[0] = mq[1] = m;
             kq[0] = kq[1] = block_scale<FMT>(__uint_as_float(m << 16));
-            if (ROW && hh == 0) ((float*)a.s_row)[tc * (a.tiles_r * kTile) + r0 + rr] = kq[0];
+            if (ROW && hh == 0) ((float*)a.s_row)[tc * (a.tiles_r_total * kTile) + r0g + rr] = kq[0];
         } else if constexpr (KIND == kPC) {
             // the row's maximum over all of x (the amax pass left it in s_row as
             // bf16 magnitude bits): s = fmax / amax, the per-tensor current rule
             if constexpr (ROW) {
-                const uint32_t m = ((const uint32_t*)a.s_row)[r0 + rr];
+                const uint32_t m = ((const uint32_t*)a.s_row)[r0g + rr];
                 mq[0] = mq[1] = m;
                 kq[0] = kq[1] = pertensor_scale<FMT>(__uint_as_float(m << 16));
             }
@@ -553,7 +556,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             kq[1] = exp2_neg(e1);
             if (ROW) {
                 // this row's scale columns 4 tc + 2 hh + {0, 1} in the 128x4 tile (tr, tc)
-                uint8_t* tileb = (uint8_t*)a.s_row + (size_t)tileid * 512;
+                uint8_t* tileb = (uint8_t*)a.s_row + (size_t)tileg * 512;
                 *(uint16_t*)(tileb + (rr & 31) * 16 + (rr >> 5) * 4 + 2 * hh) =
                     (uint16_t)((uint32_t)(e0 + 127) | ((uint32_t)(e1 + 127) << 8));
             }
@@ -644,7 +647,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                     k0 = exp2_neg(e0);
                     k1 = exp2_neg(e1);
                     // column-wise scales: logical [C][ceil(R/32)], tiles over (c/128, kb/4)
-                    uint8_t* tileb = (uint8_t*)a.s_col + ((size_t)tc * a.tiles_r + tr) * 512;
+                    uint8_t* tileb = (uint8_t*)a.s_col + ((size_t)tc * a.tiles_r_total + trg) * 512;
                     const int cr = 2 * p;
                     tileb[(cr & 31) * 16 + (cr >> 5) * 4 + qd] = (uint8_t)(e0 + 127);
                     tileb[((cr + 1) & 31) * 16 + ((cr + 1) >> 5) * 4 + qd] = (uint8_t)(e1 + 127);
@@ -667,7 +670,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                     k1 = block_scale<FMT>(__uint_as_float(m1 << 16));
                     if (qd == 0) {
                         const int64_t Cp = a.tiles_c * kTile;
-                        float* sc = (float*)a.s_col + tr * Cp + cc;
+                        float* sc = (float*)a.s_col + trg * Cp + cc;
                         sc[0] = k0;
                         sc[1] = k1;
                     }
@@ -740,8 +743,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         fence_async_smem();
         __syncthreads();
         if (t == 0) {
-            if (ROW) tma_store_2d(&tmrow, (int)c0, (int)r0, smem_u32(rowt));
-            if (COL) tma_store_2d(&tmcol, (int)r0, (int)c0, smem_u32(colt));
+            if (ROW) tma_store_2d(&tmrow, (int)c0, (int)r0g, smem_u32(rowt));
+            if (COL) tma_store_2d(&tmcol, (int)r0g, (int)c0, smem_u32(colt));
             bulk_commit();
             bulk_wait_read1();  // the previous tile's stores have read their stage ...
             issue(it + 2);      // ... which now takes the tile after next
@@ -995,7 +998,7 @@ fp8q_status launch_tile(const QuantArgs& a, cudaStream_t s) {
         attr = true;
     }
     const int64_t ntiles = a.tiles_r * a.tiles_c;
-    if (ntiles >= ((int64_t)1 << 31)) return FP8Q_ERR_SHAPE;  // the kernel counts tiles in 32 bits
+    if (a.tiles_r_total * a.tiles_c >= ((int64_t)1 << 31)) return FP8Q_ERR_SHAPE;  // tiles counted in 32 bits
     CUtensorMap tm, trow, tcol;
     memset(&tm, 0, sizeof(tm));
     memset(&trow, 0, sizeof(trow));
@@ -1005,10 +1008,10 @@ fp8q_status launch_tile(const QuantArgs& a, cudaStream_t s) {
                          CU_TENSOR_MAP_SWIZZLE_128B))
             return FP8Q_ERR_CUDA;
         // code tiles [128][128] in the 128-byte swizzle: row copy [R][C], column copy [C][R]
-        if (ROW && !make_map_2d(&trow, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.q_row, a.R, a.C, kTile, kTile,
+        if (ROW && !make_map_2d(&trow, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.q_row, a.R_total, a.C, kTile, kTile,
                                 CU_TENSOR_MAP_SWIZZLE_128B))
             return FP8Q_ERR_CUDA;
-        if (COL && !make_map_2d(&tcol, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.q_col, a.C, a.R, kTile, kTile,
+        if (COL && !make_map_2d(&tcol, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.q_col, a.C, a.R_total, kTile, kTile,
                                 CU_TENSOR_MAP_SWIZZLE_128B))
             return FP8Q_ERR_CUDA;
     }
@@ -1038,12 +1041,13 @@ fp8q_status launch_tile_fmt(const QuantArgs& a, int fmt, bool row, bool col, cud
 fp8q_status launch_perchannel(const QuantArgs& a, int fmt, bool row, bool col, cudaStream_t s) {
     const int64_t Rp = a.tiles_r * 128, Cp = a.tiles_c * 128;
     if (Rp == 0 || Cp == 0) return FP8Q_OK;  // empty x: nothing to write
-    if (row && cudaMemsetAsync(a.s_row, 0, (size_t)Rp * sizeof(float), s) != cudaSuccess) return FP8Q_ERR_CUDA;
+    // a block of rows (fp8q_quantize_rows) owns entries row0 .. row0 + Rp - 1
+    uint32_t* rm = a.s_row ? (uint32_t*)a.s_row + a.row0 : nullptr;
+    if (row && cudaMemsetAsync(rm, 0, (size_t)Rp * sizeof(float), s) != cudaSuccess) return FP8Q_ERR_CUDA;
     if (col && cudaMemsetAsync(a.s_col, 0, (size_t)Cp * sizeof(float), s) != cudaSuccess) return FP8Q_ERR_CUDA;
     const int64_t strips = ((a.R + 63) / 64) * ((a.C + 255) / 256);
     int64_t grid = (int64_t)num_sms() * 8;
     if (strips < grid) grid = strips;
-    uint32_t* rm = (uint32_t*)a.s_row;
     uint32_t* cm = (uint32_t*)a.s_col;
     if (row && col)
         pc_amax_kernel<true, true><<<(unsigned)grid, 256, 0, s>>>(a.x, a.R, a.C, rm, cm, a.counters);
@@ -1072,7 +1076,8 @@ fp8q_status launch_perchannel(const QuantArgs& a, int fmt, bool row, bool col, c
 
 fp8q_status launch_quantize(const fp8q_recipe* rc, const QuantArgs& a, DelayedDev* st, cudaStream_t s) {
     const bool row = rc->want_rowwise != 0, col = rc->want_colwise != 0;
-    if (cudaMemsetAsync(a.counters, 0, 3 * sizeof(unsigned long long), s) != cudaSuccess) return FP8Q_ERR_CUDA;
+    if (!a.add_counters && cudaMemsetAsync(a.counters, 0, 3 * sizeof(unsigned long long), s) != cudaSuccess)
+        return FP8Q_ERR_CUDA;
     switch (rc->kind) {
         case kCur: {
             if (cudaMemsetAsync(a.amax, 0, sizeof(float), s) != cudaSuccess) return FP8Q_ERR_CUDA;

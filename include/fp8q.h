@@ -175,6 +175,25 @@ FP8Q_API fp8q_status fp8q_quantize(const fp8q_recipe* recipe, const void* x, int
                           fp8q_delayed_state* st, fp8q_tensor* out, void* stream);
 
 /*
+ * Quantizes rows row0 .. row0 + rows - 1 of a tensor of total_rows x cols
+ * whose rows arrive in blocks (a weight streamed in from the host, say): x is
+ * the block (device bf16 [rows][cols]); out describes the WHOLE tensor's
+ * buffers as fp8q_quantize would fill them for [total_rows][cols], and the
+ * call writes the block's part: its rows of data_row, its columns of data_col,
+ * and the scales of its 128-row groups.  Quantizing every block once gives
+ * exactly what fp8q_quantize on the whole tensor writes, because these
+ * recipes' scales never span two 128-row groups (no counterpart on the pages;
+ * their block recipes read tile by tile).  Kinds: BLOCK_1x128, BLOCK_128x128,
+ * MXFP8_1x32 (either copy), PERCHANNEL_CURRENT (row-wise copy only); others
+ * FP8Q_ERR_DTYPE.  row0 % 128 == 0, and rows % 128 == 0 unless the block
+ * ends the tensor; total_rows % 16 == 0 with a column copy; cols % 16 == 0.
+ * Counters are ADDED to (zero them before the first block); out->rows is set
+ * to total_rows.
+ */
+FP8Q_API fp8q_status fp8q_quantize_rows(const fp8q_recipe* recipe, const void* x, int64_t row0, int64_t rows,
+                               int64_t total_rows, int64_t cols, fp8q_tensor* out, void* stream);
+
+/*
  * Several quantize calls as one: the same outputs as fp8q_quantize on each
  * job in order (no counterpart on the pages; a launch arrangement), but the
  * jobs' tile passes run side by side, their resident CTAs shared out in

@@ -115,6 +115,23 @@ def test_quantize_multi_validation_without_gpu(lib):
     assert m(jobs((L.MXFP8_1x32, 32, 32, 16, t1), (L.BLOCK_1x128, 32, 32, 16, t1)), 2) == L.ERR_ARG  # same out
 
 
+def test_quantize_rows_validation_without_gpu(lib):
+    t = L.Tensor(16, 32, 64, 128, 256, 272, 288, 512, 0, 0, 0, 0)
+
+    def qr(kind, row0, rows, total, cols=32, col=False, x=16):
+        rc = L.Recipe(kind, L.E4M3, 1, int(col))
+        return lib.fp8q_quantize_rows(ctypes.byref(rc), x, row0, rows, total, cols, ctypes.byref(t), None)
+
+    assert qr(L.PERTENSOR_CURRENT, 0, 128, 256) == L.ERR_DTYPE        # the scale needs the whole tensor
+    assert qr(L.PERCHANNEL_CURRENT, 0, 128, 256, col=True) == L.ERR_DTYPE
+    assert qr(L.BLOCK_128x128, 64, 128, 256) == L.ERR_SHAPE            # row0 off a 128-row group
+    assert qr(L.BLOCK_128x128, 0, 100, 256) == L.ERR_SHAPE             # a partial block that does not end it
+    assert qr(L.BLOCK_128x128, 128, 256, 256) == L.ERR_SHAPE           # past the end
+    assert qr(L.MXFP8_1x32, 0, 128, 200, col=True) == L.ERR_SHAPE      # total rows % 16 with a column copy
+    assert qr(L.BLOCK_1x128, 0, 128, 256, cols=40) == L.ERR_SHAPE
+    assert qr(L.BLOCK_1x128, 0, 128, 256, x=24) == L.ERR_ALIGN
+
+
 def test_gemm_validation_without_gpu(lib):
     a = L.Tensor(16, 32, 64, 128, 256, 272, 288, 512, 64, 128, L.E4M3, L.MXFP8_1x32)
     b = L.Tensor(16, 32, 64, 128, 256, 272, 288, 512, 96, 128, L.E4M3, L.MXFP8_1x32)

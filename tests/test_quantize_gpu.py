@@ -277,3 +277,33 @@ def test_quantize_multi_in_a_cuda_graph():
         for key in ("data_row", "data_col", "scale_row_bytes", "scale_col_bytes"):
             assert np.array_equal(got[key], ref[key]), key
     assert api.device_errors() == 0
+
+
+@pytest.mark.parametrize("kind,fmt,rowwise,colwise", [
+    (O.BLOCK_1x128, O.E4M3, True, True), (O.BLOCK_128x128, O.E5M2, True, True),
+    (O.MXFP8_1x32, O.E4M3, True, True), (O.MXFP8_1x32, O.E4M3, False, True),
+    (O.PERCHANNEL_CURRENT, O.E4M3, True, False)])
+def test_quantize_rows_blocks_equal_whole(kind, fmt, rowwise, colwise):
+    """fp8q_quantize_rows over blocks [0, 256), [256, 640), [640, 720) of a
+    720-row tensor writes every byte the whole-tensor call writes (buffers
+    poisoned first), the counters add up to its counters, and both match the
+    oracle."""
+    api = _api()
+    x = _mixed((720, 400), 123)
+    xd = x.cuda()
+    whole = gpu_outputs(api.quantize(xd, kind, fmt, rowwise, colwise))
+    qt = api.alloc(kind, fmt, 720, 400, rowwise, colwise, "cuda")
+    for t in (qt.data_row, qt.data_col, qt.scale_row, qt.scale_col):
+        if t is not None:
+            t.fill_(0xA5)
+    qt.counters.zero_()
+    for r0, r1 in ((0, 256), (256, 640), (640, 720)):
+        api.quantize_rows_into(xd[r0:r1].contiguous(), qt, r0)
+    got = gpu_outputs(qt)
+    for key in ("data_row", "data_col", "scale_row_bytes", "scale_col_bytes"):
+        if key in whole:
+            assert np.array_equal(got[key], whole[key]), key
+    assert [got[k] for k in ("sat_row", "sat_col", "nonfinite")] == [whole[k] for k in ("sat_row", "sat_col", "nonfinite")]
+    ref = O.quantize(kind, fmt, bits_of(x), rowwise, colwise)
+    assert_quant_equal(kind, got, ref, rowwise, colwise, ctx="rows")
+    assert api.device_errors() == 0
