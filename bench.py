@@ -273,7 +273,7 @@ def run_ours(args):
     # column block of Y (api.row_block of W) runs at once, its result copied
     # back on a third stream while later blocks still arrive.  Every byte of X,
     # W and Y crosses inside the timed region.
-    NC = 8
+    NC = args.e2e_blocks
     Nc = F // NC
     Xp, Wp = Xh.pin_memory(), Wh.pin_memory()
     Yps = [torch.empty((T, Nc), dtype=torch.bfloat16).pin_memory() for _ in range(NC)]
@@ -450,8 +450,8 @@ def run_ours(args):
                 "h2d_bytes_per_step": X.numel() * 2 + W.numel() * 2,
                 "d2h_bytes_per_step": sum(y.numel() for y in Yps) * 2, "ms_per_step": round(e2e_step_ms, 4),
                 "result_equals_device_step": e2e_ok,
-                "overlap": "W crosses in 8 row blocks, each quantized on arrival (fp8q_quantize_rows) and its column "
-                           "block of Y computed and copied back while later blocks still cross"},
+                "overlap": f"W crosses in {NC} row blocks, each quantized on arrival (fp8q_quantize_rows) and its "
+                           "column block of Y computed and copied back while later blocks still cross"},
         "gpu_launches": launches,
         "clocks": clocks,
         "device_errors": errs,
@@ -747,6 +747,8 @@ def main():
                          "qerror: quantization error per recipe; delayed70b: the delayed-scaling 70B FFN step; "
                          "multi: 8 small tensors, separate quantize calls against one fp8q_quantize_multi")
     ap.add_argument("--kind", choices=list(KINDS), default="mx")
+    ap.add_argument("--e2e-blocks", type=int, choices=[1, 2, 4, 7, 8, 14, 16], default=8,
+                    help="row blocks of W in the end-to-end pipeline (F = 14336 = 112 x 128)")
     ap.add_argument("--rows", type=int, default=16384)
     ap.add_argument("--cols", type=int, default=8192)
     ap.add_argument("--no-rowwise", action="store_true")
