@@ -239,8 +239,9 @@ def run_ours(args):
     def step(ev=None):
         if ev:
             ev[0].record()
-        api.quantize_into(X, qx, stream=stream)
-        api.quantize_into(W, qw, stream=stream)
+        # X and W in one call: their tile passes share the SMs (a few percent
+        # faster than two calls here: 0.066 against 0.068 ms)
+        api.quantize_multi([(X, qx), (W, qw)], stream=stream)
         if ev:
             ev[1].record()
         api.scaled_gemm(qx, False, qw, False, out=Y, stream=stream)
@@ -396,9 +397,12 @@ def run_ours(args):
         errs |= api.device_errors()
         launches += 6 * args.steps + 4 * args.steps
 
-    # ---- the same quantize phase as one fp8q_quantize_multi call
-    multi_ms = _time_ms(lambda: api.quantize_multi([(X, qx), (W, qw)], stream=stream), args.steps, args.warmup,
-                        flush)
+    # ---- the same quantize phase as two separate calls
+    def two_calls():
+        api.quantize_into(X, qx, stream=stream)
+        api.quantize_into(W, qw, stream=stream)
+
+    two_ms = _time_ms(two_calls, args.steps, args.warmup, flush)
     launches += 2 * args.steps
 
     # ---- scaling granularity at the bench shape ("mastering FP8 LLM training
@@ -439,7 +443,7 @@ def run_ours(args):
         "gemm_tflops": round(gemm_tflops, 1),
         "quantize_gbs": round(qbytes / q_avg / 1e6, 1),
         "quantize_frac_of_hbm": round(qbytes / q_avg / 1e6 / hbm_peak, 3),
-        "quantize_ms": {"two_calls": round(q_avg, 4), "one_multi_call": round(multi_ms, 4)},
+        "quantize_ms": {"one_multi_call": round(q_avg, 4), "two_calls": round(two_ms, 4)},
         "roofline": {"kernel": gemm_kernel_name(T, F, "blockwise 1x128 x 128x128"), "bound": "tensor",
                      "achieved": round(gemm_tflops, 1), "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
                      "frac": round(gemm_tflops / fp8_peak, 3),
