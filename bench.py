@@ -284,8 +284,8 @@ def run_ours(args):
     ev_x = torch.cuda.Event()
     ev_w = [torch.cuda.Event() for _ in range(NC)]
 
-    def e2e_step():
-        s_in.wait_stream(stream)
+    def e2e_step(st):
+        s_in.wait_stream(st)
         with torch.cuda.stream(s_in):
             X.copy_(Xp, non_blocking=True)
             ev_x.record(s_in)
@@ -293,28 +293,47 @@ def run_ours(args):
                 W[c * Nc:(c + 1) * Nc].copy_(Wp[c * Nc:(c + 1) * Nc], non_blocking=True)
                 ev_w[c].record(s_in)
         qw.counters.zero_()
-        stream.wait_event(ev_x)
-        api.quantize_into(X, qx, stream=stream)
+        st.wait_event(ev_x)
+        api.quantize_into(X, qx, stream=st)
         for c in range(NC):
-            stream.wait_event(ev_w[c])
-            api.quantize_rows_into(W[c * Nc:(c + 1) * Nc], qw, c * Nc, stream=stream)
-            api.scaled_gemm(qx, False, qw_blocks[c], False, out=Ycs[c], stream=stream)
-            s_out.wait_stream(stream)
+            st.wait_event(ev_w[c])
+            api.quantize_rows_into(W[c * Nc:(c + 1) * Nc], qw, c * Nc, stream=st)
+            api.scaled_gemm(qx, False, qw_blocks[c], False, out=Ycs[c], stream=st)
+            s_out.wait_stream(st)
             with torch.cuda.stream(s_out):
                 Yps[c].copy_(Ycs[c], non_blocking=True)
-        stream.wait_stream(s_out)
+        st.wait_stream(s_out)
 
-    e2e_ms = []
-    for i in range(args.warmup + args.steps):
-        flush.zero_()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        e2e_step()
-        e1.record()
+    def time_e2e(run):
+        ms = []
+        for i in range(args.warmup + args.steps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            run()
+            e1.record()
+            torch.cuda.synchronize()
+            if i >= args.warmup:
+                ms.append(e0.elapsed_time(e1))
+        return statistics.mean(ms)
+
+    # eagerly, then as one CUDA graph (the library's calls, copies and the
+    # fork / join of the three streams captured together; host launch work
+    # leaves the timed region)
+    e2e_eager = time_e2e(lambda: e2e_step(stream))
+    e2e_graph_ms = None
+    try:
+        cap = torch.cuda.Stream(device=dev)
+        cap.wait_stream(stream)
+        g_e2e = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_e2e, stream=cap):
+            e2e_step(cap)
         torch.cuda.synchronize()
-        if i >= args.warmup:
-            e2e_ms.append(e0.elapsed_time(e1))
-    e2e_step_ms = max_over_ranks(statistics.mean(e2e_ms), world)
+        e2e_graph_ms = time_e2e(g_e2e.replay)
+    except Exception as exc:  # capture not possible here: the eager number stands
+        print(f"e2e graph capture failed: {exc}", file=sys.stderr)
+    e2e_best = min(e2e_eager, e2e_graph_ms) if e2e_graph_ms else e2e_eager
+    e2e_step_ms = max_over_ranks(e2e_best, world)
     Yh = torch.cat(Yps, dim=1)
     e2e_ok = bool(torch.equal(Yh.view(torch.int16), Y.cpu().view(torch.int16)))
 
@@ -453,6 +472,8 @@ def run_ours(args):
         "e2e": {"value": round(world * flops / e2e_step_ms / 1e9, 1), "unit": UNIT,
                 "h2d_bytes_per_step": X.numel() * 2 + W.numel() * 2,
                 "d2h_bytes_per_step": sum(y.numel() for y in Yps) * 2, "ms_per_step": round(e2e_step_ms, 4),
+                "ms_per_step_eager": round(e2e_eager, 4),
+                "ms_per_step_graph": round(e2e_graph_ms, 4) if e2e_graph_ms else None,
                 "result_equals_device_step": e2e_ok,
                 "overlap": f"W crosses in {NC} row blocks, each quantized on arrival (fp8q_quantize_rows) and its "
                            "column block of Y computed and copied back while later blocks still cross"},
