@@ -628,7 +628,7 @@ def run_modes(args):
                           "separate_ms": round(sep, 4), "multi_ms": round(mul, 4),
                           "separate_frac_of_hbm": round(byts / sep / 1e6 / peaks()[0], 3),
                           "multi_frac_of_hbm": round(byts / mul / 1e6 / peaks()[0], 3)}), flush=True)
-    elif args.mode == "delayed70b":  # cfg 4: delayed hybrid scaling, Llama-3-70B FFN, 3 GEMMs per step
+    elif args.mode == "delayed70b":  # delayed hybrid scaling, Llama-3-70B FFN, 3 GEMMs per step
         from fp8_scaled_quantization_quantize_gb300 import api, inputs
         bases = inputs.llama70b_ffn_bases()
         mags = inputs.delayed_magnitudes()
@@ -669,10 +669,10 @@ def run_modes(args):
     elif args.mode == "qerror":  # quantization error per recipe (analysis, not timed)
         from fp8_scaled_quantization_quantize_gb300 import api, inputs, qerror
         X, W = inputs.llama8b_up_proj()
-        data = [("cfg2 X 4096x4096, 1% columns x100", X, api.E4M3), ("cfg2 W 14336x4096 N(0,0.02^2)", W, api.E4M3),
-                ("cfg5 64 MiB N(0,1), 0.1% elements x1000", inputs.sweep_tensor(64), api.E4M3),
-                ("cfg3 dY 8192x14336 N(0,1e-4^2)", inputs.normal_bf16((8192, 14336), 2, 1e-4), api.E4M3),
-                ("cfg3 dY 8192x14336 N(0,1e-4^2)", inputs.normal_bf16((8192, 14336), 2, 1e-4), api.E5M2)]
+        data = [("Llama-3-8B up-proj X 4096x4096, 1% columns x100", X, api.E4M3), ("Llama-3-8B up-proj W 14336x4096 N(0,0.02^2)", W, api.E4M3),
+                ("sweep tensor 64 MiB N(0,1), 0.1% elements x1000", inputs.sweep_tensor(64), api.E4M3),
+                ("Llama-3-8B MLP dY 8192x14336 N(0,1e-4^2)", inputs.normal_bf16((8192, 14336), 2, 1e-4), api.E4M3),
+                ("Llama-3-8B MLP dY 8192x14336 N(0,1e-4^2)", inputs.normal_bf16((8192, 14336), 2, 1e-4), api.E5M2)]
         for name, x, fmt in data:
             xd = x.cuda()
             base = None

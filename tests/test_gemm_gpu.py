@@ -157,7 +157,7 @@ def test_full_config_pertensor_256():
     A, B = inputs.pertensor_256()
     qa = api.quantize(A.cuda(), 0, O.E4M3, True, False)
     qb = api.quantize(B.cuda(), 0, O.E4M3, True, False)
-    _check(api, qa, False, qb, False, ctx="cfg1 full")
+    _check(api, qa, False, qb, False, ctx="per-tensor 256 full")
 
 
 def test_full_config_blockwise_llama8b_up_proj(variant):
@@ -165,7 +165,7 @@ def test_full_config_blockwise_llama8b_up_proj(variant):
     X, W = inputs.llama8b_up_proj()
     qx = api.quantize(X.cuda(), 2, O.E4M3, True, False)
     qw = api.quantize(W.cuda(), 3, O.E4M3, True, False)
-    _check(api, qx, False, qw, False, sample=_edge_sample(14), ctx="cfg2 fprop (16 rows + 16 cols)")
+    _check(api, qx, False, qw, False, sample=_edge_sample(14), ctx="up-proj fprop (16 rows + 16 cols)")
 
 
 def test_full_config_perchannel_llama8b_up_proj():
@@ -189,9 +189,9 @@ def test_full_config_mxfp8_llama8b_mlp(variant):
     qw = api.quantize(W.cuda(), 4, O.E4M3, True, True)
     qd = api.quantize(dY.cuda(), 4, O.E4M3, True, True)
     s = _edge_sample(6)
-    _check(api, qx, False, qw, False, sample=s, ctx="cfg3 fprop")
-    _check(api, qd, False, qw, True, sample=s, ctx="cfg3 dgrad")
-    _check(api, qd, True, qx, True, sample=s, ctx="cfg3 wgrad")
+    _check(api, qx, False, qw, False, sample=s, ctx="MXFP8 MLP fprop")
+    _check(api, qd, False, qw, True, sample=s, ctx="MXFP8 MLP dgrad")
+    _check(api, qd, True, qx, True, sample=s, ctx="MXFP8 MLP wgrad")
 
 
 @pytest.mark.parametrize("ka,kb", [(2, 3), (4, 4), (0, 0), (5, 5)], ids=["blockwise", "mxfp8", "pertensor", "perchannel"])

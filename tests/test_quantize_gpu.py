@@ -133,10 +133,10 @@ def test_delayed_update_entry_point():
 
 CONFIG_SHAPES = [
     # (name, kind, fmt, shape, rowwise, colwise, maker)
-    ("cfg1 A", O.PERTENSOR_CURRENT, O.E4M3, None, True, True, lambda: inputs.pertensor_256()[0]),
-    ("cfg2 X", O.BLOCK_1x128, O.E4M3, None, True, True, lambda: inputs.llama8b_up_proj()[0]),
-    ("cfg2 W", O.BLOCK_128x128, O.E4M3, None, True, True, lambda: inputs.llama8b_up_proj()[1]),
-    ("cfg3 X", O.MXFP8_1x32, O.E4M3, None, True, True, lambda: inputs.llama8b_mlp()[0]),
+    ("per-tensor 256 A", O.PERTENSOR_CURRENT, O.E4M3, None, True, True, lambda: inputs.pertensor_256()[0]),
+    ("up-proj X", O.BLOCK_1x128, O.E4M3, None, True, True, lambda: inputs.llama8b_up_proj()[0]),
+    ("up-proj W", O.BLOCK_128x128, O.E4M3, None, True, True, lambda: inputs.llama8b_up_proj()[1]),
+    ("MXFP8 MLP X", O.MXFP8_1x32, O.E4M3, None, True, True, lambda: inputs.llama8b_mlp()[0]),
     ("perchannel X", O.PERCHANNEL_CURRENT, O.E4M3, None, True, True, lambda: inputs.llama8b_up_proj()[0]),
     ("perchannel W", O.PERCHANNEL_CURRENT, O.E4M3, None, True, True, lambda: inputs.llama8b_up_proj()[1]),
 ]
@@ -150,8 +150,8 @@ def test_quantize_full_config_shapes(name, kind, fmt, shape, rowwise, colwise, m
 def test_quantize_full_mx_dy_and_w():
     X, W, dY = inputs.llama8b_mlp()
     del X
-    _run(O.MXFP8_1x32, O.E4M3, W, True, True, ctx="cfg3 W")
-    _run(O.MXFP8_1x32, O.E4M3, dY, True, True, ctx="cfg3 dY")
+    _run(O.MXFP8_1x32, O.E4M3, W, True, True, ctx="MXFP8 MLP W")
+    _run(O.MXFP8_1x32, O.E4M3, dY, True, True, ctx="MXFP8 MLP dY")
 
 
 def test_quantize_sweep_tensor_pertensor_and_mx():
