@@ -307,3 +307,40 @@ def test_quantize_rows_blocks_equal_whole(kind, fmt, rowwise, colwise):
     ref = O.quantize(kind, fmt, bits_of(x), rowwise, colwise)
     assert_quant_equal(kind, got, ref, rowwise, colwise, ctx="rows")
     assert api.device_errors() == 0
+
+
+def test_quantize_multi_and_rows_edge_cases():
+    """An empty job among others, a single job, an empty block: the same bytes
+    as the plain calls, nothing written for the empty ones."""
+    api = _api()
+    x = _mixed((272, 400), 5).cuda()
+    empty = torch.zeros((0, 64), dtype=torch.bfloat16, device="cuda")
+    q1 = api.alloc(O.MXFP8_1x32, O.E4M3, 272, 400, True, True, "cuda")
+    q0 = api.alloc(O.BLOCK_1x128, O.E4M3, 0, 64, True, True, "cuda")
+    api.quantize_multi([(x, q1), (empty, q0)])
+    ref = gpu_outputs(api.quantize(x, O.MXFP8_1x32, O.E4M3, True, True))
+    got = gpu_outputs(q1)
+    for key in ("data_row", "data_col", "scale_row_bytes", "scale_col_bytes"):
+        assert np.array_equal(got[key], ref[key]), key
+    assert gpu_outputs(q0)["nonfinite"] == 0
+    q2 = api.alloc(O.BLOCK_128x128, O.E5M2, 272, 400, True, True, "cuda")
+    api.quantize_multi([(x, q2)])                        # one job: the plain path
+    one = gpu_outputs(api.quantize(x, O.BLOCK_128x128, O.E5M2, True, True))
+    g2 = gpu_outputs(q2)
+    for key in ("data_row", "data_col", "scale_row_bytes", "scale_col_bytes"):
+        assert np.array_equal(g2[key], one[key]), key
+    # an empty block of rows writes nothing, and E5M2 1x128 row-only blocks match the whole call
+    q3 = api.alloc(O.BLOCK_1x128, O.E5M2, 272, 400, True, False, "cuda")
+    q3.data_row.fill_(0x5A)
+    q3.counters.zero_()
+    api.quantize_rows_into(x[256:256].contiguous(), q3, 256)
+    torch.cuda.synchronize()
+    assert bool((q3.data_row == 0x5A).all())
+    for r0, r1 in ((0, 128), (128, 272)):
+        api.quantize_rows_into(x[r0:r1].contiguous(), q3, r0)
+    whole = gpu_outputs(api.quantize(x, O.BLOCK_1x128, O.E5M2, True, False))
+    g3 = gpu_outputs(q3)
+    assert np.array_equal(g3["data_row"], whole["data_row"])
+    assert np.array_equal(g3["scale_row_bytes"], whole["scale_row_bytes"])
+    assert g3["sat_row"] == whole["sat_row"]
+    assert api.device_errors() == 0
