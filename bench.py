@@ -333,6 +333,7 @@ def run_ours(args):
     except Exception as exc:  # capture not possible here: the eager number stands
         print(f"e2e graph capture failed: {exc}", file=sys.stderr)
     e2e_best = min(e2e_eager, e2e_graph_ms) if e2e_graph_ms else e2e_eager
+    e2e_launches = (1 + 2 * NC) * args.steps * (2 if e2e_graph_ms else 1)   # X, then per block: quantize + GEMM
     e2e_step_ms = max_over_ranks(e2e_best, world)
     Yh = torch.cat(Yps, dim=1)
     e2e_ok = bool(torch.equal(Yh.view(torch.int16), Y.cpu().view(torch.int16)))
@@ -475,7 +476,7 @@ def run_ours(args):
                 "result_equals_device_step": e2e_ok,
                 "overlap": f"W crosses in {NC} row blocks, each quantized on arrival (fp8q_quantize_rows) and its "
                            "column block of Y computed and copied back while later blocks still cross"},
-        "gpu_launches": launches,
+        "gpu_launches": launches + e2e_launches,
         "clocks": clocks,
         "device_errors": errs,
         "mxfp8": mx,
