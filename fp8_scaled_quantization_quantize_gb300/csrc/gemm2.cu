@@ -629,7 +629,8 @@ __global__ void __launch_bounds__(Cfg<REC>::THREADS, 1)
                     }
                     const float* scl = (const float*)(smem + C::OFF_SCL + r * C::SLOT);
                     const float sa = scl[32 * q + lane];
-                    // this warp's 64-column slice lies in one 128-column B block
+                    // this warp's EC columns lie in one 128-column B block (tiles start on
+                    // 256-column boundaries)
                     const float sc = (REC == REC_B2D) ? __fmul_rn(sa, scl[128 + (int)((nb * BN + EC * j) / 128 - (nb * BN) / 128)]) : 0.0f;
                     const uint32_t buf = kbg % NACC;
                     if (!mbar_wait2(tfull(buf), (kbg / NACC) & 1u, abort_flag)) {
