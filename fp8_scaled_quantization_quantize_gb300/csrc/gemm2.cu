@@ -557,13 +557,15 @@ __global__ void __launch_bounds__(Cfg<REC>::THREADS, 1)
             }
         };
         // while the warp drains and stores a tile: move the next K block's
-        // scale tiles if they have landed (never waits), so the MMAs of the
-        // next tile do not stall on them behind this tile's stores
+        // scale tiles if they have landed (a non-blocking test: a try_wait here
+        // held each of a tile's eight store boxes while the scales were still
+        // in flight, about 15 us a tile at K = 1024), so the MMAs of the next
+        // tile do not stall on them behind this tile's stores
         auto poll_sf = [&]() {
             if constexpr (REC == REC_MX) {
                 if (sf_ok && g_sf < total_kb) {
                     const int st = (int)(g_sf % STAGES);
-                    if (__all_sync(0xffffffffu, mbar_try(sfl(st), (uint32_t)((g_sf / STAGES) & 1u)))) move_one_sf(st);
+                    if (__all_sync(0xffffffffu, mbar_test(sfl(st), (uint32_t)((g_sf / STAGES) & 1u)))) move_one_sf(st);
                 }
             }
         };

@@ -218,3 +218,22 @@ def test_gemm_on_row_blocks_of_b(ka, kb):
     finally:
         api.gemm_set_variant(0)
     assert api.device_errors() == 0
+
+
+@pytest.mark.parametrize("M,N,K", [(4096, 4096, 640), (4096, 4096, 1024), (4096, 4096, 1152), (8192, 8192, 1024)])
+def test_mxfp8_short_k_many_tiles_per_pair(M, N, K):
+    """MXFP8 on the SM-pair kernel with few K blocks (5 to 9) and several
+    tiles per SM pair: the scale-tile movers run up to four K blocks into
+    the next tile, past the stage ring's length, so every landing-barrier wait
+    must be exact (sampled rows and columns against the oracle)."""
+    api = _api()
+    a = inputs.normal_bf16((M, K), 70 + K)
+    b = inputs.normal_bf16((N, K), 71 + K, 0.02)
+    qa = api.quantize(a.cuda(), 4, O.E4M3, True, False)
+    qb = api.quantize(b.cuda(), 4, O.E4M3, True, False)
+    api.gemm_set_variant(2)
+    try:
+        _check(api, qa, False, qb, False, sample=_edge_sample(12), ctx=f"mx {M}x{N}x{K}")
+    finally:
+        api.gemm_set_variant(0)
+    assert api.device_errors() == 0
