@@ -23,3 +23,24 @@ def test_reference_arm_prints_the_contract_line():
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
     assert d["config"]["M"] == 4096 and d["config"]["N"] == 14336 and d["config"]["K"] == 4096
+
+
+def test_profile_traffic_follows_the_kernel_sources(tmp_path, monkeypatch):
+    """bench.py reports a profile's dram traffic only while the hash of the
+    kernel's sources recorded with it matches the sources (else null)."""
+    import hashlib
+    sys.path.insert(0, ROOT)
+    import bench
+    src = tmp_path / "fp8_scaled_quantization_quantize_gb300" / "csrc"
+    src.mkdir(parents=True)
+    (src / "k.cu").write_text("// kernel v1\n")
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    digest = hashlib.sha256(b"// kernel v1\n").hexdigest()
+    (prof / "p.md").write_text(f"# p\n\ntraffic_bytes_per_launch: 12345\nsources_sha256: {digest}\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.measured_traffic("p.md", ("k.cu",)) == 12345.0
+    (src / "k.cu").write_text("// kernel v2\n")
+    assert bench.measured_traffic("p.md", ("k.cu",)) is None
+    assert bench.measured_traffic("missing.md", ("k.cu",)) is None
+
