@@ -111,6 +111,37 @@ fp8q_status prepare_quantize(const fp8q_recipe* rc, const void* x, int64_t rows,
     return FP8Q_OK;
 }
 
+// The two GEMM operands of D[M][N] = A_q . B_q^T from the chosen copies:
+// recipes, formats and the copies' logical shapes checked, the data and the
+// scales each recipe needs present and 16-byte aligned.
+fp8q_status prepare_operands(const fp8q_tensor* A, int a_use_col, const fp8q_tensor* B, int b_use_col, int64_t M,
+                             int64_t N, int64_t K, GemmOperand& ga, GemmOperand& gb) {
+    if (!valid_kind(A->kind) || !valid_kind(B->kind) || !valid_fmt(A->fmt) || !valid_fmt(B->fmt)) return FP8Q_ERR_ARG;
+    // logical shapes of the chosen copies
+    const int64_t am = a_use_col ? A->cols : A->rows, ak = a_use_col ? A->rows : A->cols;
+    const int64_t bn = b_use_col ? B->cols : B->rows, bk = b_use_col ? B->rows : B->cols;
+    if (am != M || ak != K || bn != N || bk != K) return FP8Q_ERR_SHAPE;
+    if (!gemm_kinds_ok(A->kind, B->kind)) return FP8Q_ERR_DTYPE;
+    const bool pt = is_pertensor(A->kind);
+    ga.data = (const uint8_t*)(a_use_col ? A->data_col : A->data_row);
+    ga.scale = a_use_col ? A->scale_col : A->scale_row;
+    ga.scale_inv = A->scale_inv;
+    ga.rows = M;
+    ga.kind = A->kind;
+    ga.fmt = A->fmt;
+    gb.data = (const uint8_t*)(b_use_col ? B->data_col : B->data_row);
+    gb.scale = b_use_col ? B->scale_col : B->scale_row;
+    gb.scale_inv = B->scale_inv;
+    gb.rows = N;
+    gb.kind = B->kind;
+    gb.fmt = B->fmt;
+    if (!ga.data || !gb.data) return FP8Q_ERR_ARG;
+    if (pt ? !ga.scale_inv || !gb.scale_inv : !ga.scale || !gb.scale) return FP8Q_ERR_ARG;
+    if (!aligned16(ga.data) || !aligned16(gb.data)) return FP8Q_ERR_ALIGN;
+    if (!pt && (!aligned16(ga.scale) || !aligned16(gb.scale))) return FP8Q_ERR_ALIGN;
+    return FP8Q_OK;
+}
+
 void set_meta(const fp8q_recipe* rc, int64_t rows, int64_t cols, fp8q_tensor* out) {
     out->rows = rows;
     out->cols = cols;
@@ -291,30 +322,10 @@ fp8q_status fp8q_scaled_gemm(const fp8q_tensor* A, int a_use_col, const fp8q_ten
     if (out_dtype != 0 && out_dtype != 1) return FP8Q_ERR_ARG;
     if (M < 1 || N < 1 || K < 1) return FP8Q_ERR_SHAPE;
     if (K % 16 != 0 || N % 8 != 0) return FP8Q_ERR_SHAPE;
-    if (!valid_kind(A->kind) || !valid_kind(B->kind) || !valid_fmt(A->fmt) || !valid_fmt(B->fmt)) return FP8Q_ERR_ARG;
-    // logical shapes of the chosen copies
-    const int64_t am = a_use_col ? A->cols : A->rows, ak = a_use_col ? A->rows : A->cols;
-    const int64_t bn = b_use_col ? B->cols : B->rows, bk = b_use_col ? B->rows : B->cols;
-    if (am != M || ak != K || bn != N || bk != K) return FP8Q_ERR_SHAPE;
-    const bool a_pt = is_pertensor(A->kind);
-    if (!gemm_kinds_ok(A->kind, B->kind)) return FP8Q_ERR_DTYPE;
     GemmOperand ga, gb;
-    ga.data = (const uint8_t*)(a_use_col ? A->data_col : A->data_row);
-    ga.scale = a_use_col ? A->scale_col : A->scale_row;
-    ga.scale_inv = A->scale_inv;
-    ga.rows = M;
-    ga.kind = A->kind;
-    ga.fmt = A->fmt;
-    gb.data = (const uint8_t*)(b_use_col ? B->data_col : B->data_row);
-    gb.scale = b_use_col ? B->scale_col : B->scale_row;
-    gb.scale_inv = B->scale_inv;
-    gb.rows = N;
-    gb.kind = B->kind;
-    gb.fmt = B->fmt;
-    if (!ga.data || !gb.data) return FP8Q_ERR_ARG;
-    if (a_pt ? !ga.scale_inv || !gb.scale_inv : !ga.scale || !gb.scale) return FP8Q_ERR_ARG;
-    if (!aligned16(ga.data) || !aligned16(gb.data) || !aligned16(D)) return FP8Q_ERR_ALIGN;
-    if (!a_pt && (!aligned16(ga.scale) || !aligned16(gb.scale))) return FP8Q_ERR_ALIGN;
+    const fp8q_status v = prepare_operands(A, a_use_col, B, b_use_col, M, N, K, ga, gb);
+    if (v != FP8Q_OK) return v;
+    if (!aligned16(D)) return FP8Q_ERR_ALIGN;
     return launch_gemm(ga, gb, D, out_dtype, M, N, K, (cudaStream_t)stream);
 }
 
@@ -325,29 +336,9 @@ fp8q_status fp8q_scaled_gemm_mxq(const fp8q_tensor* A, int a_use_col, const fp8q
     if (K % 16 != 0 || N % 32 != 0) return FP8Q_ERR_SHAPE;
     if (!Dq->data_row || !Dq->scale_row || !Dq->counters) return FP8Q_ERR_ARG;
     if (!aligned16(Dq->data_row) || !aligned16(Dq->scale_row) || (D && !aligned16(D))) return FP8Q_ERR_ALIGN;
-    if (!valid_kind(A->kind) || !valid_kind(B->kind) || !valid_fmt(A->fmt) || !valid_fmt(B->fmt)) return FP8Q_ERR_ARG;
-    const int64_t am = a_use_col ? A->cols : A->rows, ak = a_use_col ? A->rows : A->cols;
-    const int64_t bn = b_use_col ? B->cols : B->rows, bk = b_use_col ? B->rows : B->cols;
-    if (am != M || ak != K || bn != N || bk != K) return FP8Q_ERR_SHAPE;
-    const bool a_pt = is_pertensor(A->kind);
-    if (!gemm_kinds_ok(A->kind, B->kind)) return FP8Q_ERR_DTYPE;
     GemmOperand ga, gb;
-    ga.data = (const uint8_t*)(a_use_col ? A->data_col : A->data_row);
-    ga.scale = a_use_col ? A->scale_col : A->scale_row;
-    ga.scale_inv = A->scale_inv;
-    ga.rows = M;
-    ga.kind = A->kind;
-    ga.fmt = A->fmt;
-    gb.data = (const uint8_t*)(b_use_col ? B->data_col : B->data_row);
-    gb.scale = b_use_col ? B->scale_col : B->scale_row;
-    gb.scale_inv = B->scale_inv;
-    gb.rows = N;
-    gb.kind = B->kind;
-    gb.fmt = B->fmt;
-    if (!ga.data || !gb.data) return FP8Q_ERR_ARG;
-    if (a_pt ? !ga.scale_inv || !gb.scale_inv : !ga.scale || !gb.scale) return FP8Q_ERR_ARG;
-    if (!aligned16(ga.data) || !aligned16(gb.data)) return FP8Q_ERR_ALIGN;
-    if (!a_pt && (!aligned16(ga.scale) || !aligned16(gb.scale))) return FP8Q_ERR_ALIGN;
+    const fp8q_status v = prepare_operands(A, a_use_col, B, b_use_col, M, N, K, ga, gb);
+    if (v != FP8Q_OK) return v;
     Dq->rows = M;
     Dq->cols = N;
     Dq->fmt = fmt;
