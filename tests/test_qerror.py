@@ -22,7 +22,7 @@ def test_error_formula_hand_example():
     assert e["sqnr_db"] == pytest.approx(20.0, abs=1e-12)
 
 
-@pytest.mark.parametrize("kind", [0, 2, 3, 4])
+@pytest.mark.parametrize("kind", [0, 2, 3, 4, 5])
 @pytest.mark.parametrize("fmt", [O.E4M3, O.E5M2])
 def test_dequantize_layouts_match_the_oracle(kind, fmt):
     R, C = 200, 272
