@@ -17,7 +17,7 @@ def test_errors_on_gpu_outputs_equal_the_oracles_and_order_as_reported():
     from fp8_scaled_quantization_quantize_gb300 import api
     x = inputs.to_bf16(inputs.with_outlier_columns(inputs.normal_f32((1024, 4096), 0), 0.01, 100.0, 2))
     errs = {}
-    for kind in (0, 2, 3, 4):
+    for kind in (0, 2, 3, 4, 5):
         qt = api.quantize(x.cuda(), kind, O.E4M3, True, False)
         e_gpu = qerror.error(x.float().cuda(), qerror.dequantize_rowwise(qt))
         ref = O.quantize(kind, O.E4M3, inputs.bf16_bits(x), True, False)
