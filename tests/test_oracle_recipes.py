@@ -146,7 +146,7 @@ def _rand_bits(shape, seed, outliers=True):
     return _bits(x)
 
 
-@pytest.mark.parametrize("br,bc", [(1, 128), (128, 128)])
+@pytest.mark.parametrize("br,bc", [(1, 128), (128, 128), (1, 64), (64, 64), (32, 32), (1, 256), (256, 256)])
 def test_blockwise_block_max_hits_fmax(br, bc):
     x = _rand_bits((300, 390), 1)
     q, d, _, am, sat, nf = O.quant_blocks(x, br, bc, O.KIND_DIV, O.E4M3)
@@ -191,7 +191,8 @@ def test_colwise_is_rowwise_of_transpose(kind):
 
 
 @pytest.mark.parametrize("br,bc,kind", [(1, 128, O.KIND_DIV), (128, 128, O.KIND_DIV), (1, 32, O.KIND_POW2),
-                                        (32, 1, O.KIND_POW2), (128, 1, O.KIND_DIV)])
+                                        (32, 1, O.KIND_POW2), (128, 1, O.KIND_DIV), (1, 64, O.KIND_DIV),
+                                        (64, 64, O.KIND_DIV), (256, 256, O.KIND_DIV)])
 def test_ragged_edges_equal_zero_padding(br, bc, kind):
     """A partial edge block takes the elements present: zero padding to full
     blocks (zeros never change an amax) must give the same codes and scales."""
@@ -204,6 +205,20 @@ def test_ragged_edges_equal_zero_padding(br, bc, kind):
     qp, sp, e8p, amp, *_ = O.quant_blocks(xp, br, bc, kind, O.E4M3)
     assert np.array_equal(q, qp[:133, :272])
     assert np.array_equal(s, sp) and np.array_equal(am, amp)
+
+
+@pytest.mark.parametrize("br,bc,kind", [(1, 128, O.KIND_DIV), (64, 64, O.KIND_DIV), (32, 128, O.KIND_DIV),
+                                        (1, 32, O.KIND_POW2), (1, 256, O.KIND_MULT)])
+def test_block_shape_transposes_with_the_matrix(br, bc, kind):
+    """Generic sub-channel blocks: quantizing x^T with br x bc blocks gives the
+    transpose of quantizing x with bc x br blocks (codes, scales, maxima), so
+    no row / column index is swapped anywhere in the block loop."""
+    x = _rand_bits((200, 330), 21)
+    xt = np.ascontiguousarray(x.T)
+    q, sc, _, am, sat, nf = O.quant_blocks(x, bc, br, kind, O.E4M3)
+    qt, sct, _, amt, satt, nft = O.quant_blocks(xt, br, bc, kind, O.E4M3)
+    assert np.array_equal(qt, q.T) and np.array_equal(sct, sc.T) and np.array_equal(amt, am.T)
+    assert (satt, nft) == (sat, nf)
 
 
 def test_nonfinite_inputs():
