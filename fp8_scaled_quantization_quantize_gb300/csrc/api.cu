@@ -162,7 +162,7 @@ const char* fp8q_status_str(fp8q_status s) {
         case FP8Q_ERR_SHAPE: return "invalid shape";
         case FP8Q_ERR_ALIGN: return "misaligned pointer or row pitch";
         case FP8Q_ERR_DTYPE: return "format / recipe combination not allowed";
-        case FP8Q_ERR_UNSUPPORTED: return "not supported by this build";
+        case FP8Q_ERR_UNSUPPORTED: return "not supported by this library";
         case FP8Q_ERR_CUDA: return "CUDA error";
         case FP8Q_ERR_TIMEOUT: return "device wait timed out";
         case FP8Q_WARN_NONFINITE: return "nonfinite input";

@@ -70,7 +70,7 @@ typedef enum {
     FP8Q_ERR_SHAPE = 2,        /* negative or inconsistent sizes, size limits */
     FP8Q_ERR_ALIGN = 3,        /* pointer or row pitch not 16-byte aligned */
     FP8Q_ERR_DTYPE = 4,        /* format / recipe combination not allowed */
-    FP8Q_ERR_UNSUPPORTED = 5,  /* valid request this build does not implement */
+    FP8Q_ERR_UNSUPPORTED = 5,  /* valid request this library does not implement */
     FP8Q_ERR_CUDA = 6,         /* a CUDA call or kernel launch failed */
     FP8Q_ERR_TIMEOUT = 7,      /* a bounded device wait gave up (see fp8q_device_errors) */
     FP8Q_WARN_NONFINITE = 8    /* reserved: nonfinite inputs are reported via counters */

@@ -16,7 +16,7 @@ def pytest_configure(config):
 @pytest.fixture(autouse=True)
 def _gpu_guard(request):
     """A gpu-marked test fails (never skips) when no GPU is visible, so a run
-    on a GPU machine cannot pass by silently not running the CUDA path."""
+    that expects a GPU cannot pass by silently not running the CUDA path."""
     if request.node.get_closest_marker("gpu") is not None:
         import torch
         assert torch.cuda.is_available(), "gpu test run without a visible CUDA device"
