@@ -154,3 +154,42 @@ def test_f64_to_bf16():
     assert O.f64_to_bf16([1 + 2 ** -8])[0] == 0x3F80
     assert O.f64_to_bf16([3.5e38])[0] == 0x7F80
     assert O.f64_to_bf16([-0.0])[0] == 0x8000
+
+
+def _pattern_windows(fmt):
+    """Windows of 2^17 consecutive fp32 bit patterns (both signs) around the
+    places a cast can go wrong: fp32 subnormals and zero, the format's
+    smallest subnormal, 1.0, its largest finite value, and Inf / NaN."""
+    fmax = O.FMAX[fmt]
+    smallest = 2.0 ** -9 if fmt == O.E4M3 else 2.0 ** -16
+    centres = [0, int(np.float32(smallest).view(np.uint32)), int(np.float32(1.0).view(np.uint32)),
+               int(np.float32(fmax).view(np.uint32)), 0x7F800000]
+    half = 1 << 16
+    out = []
+    for c in centres:
+        lo = max(0, c - half)
+        hi = min(0x80000000, c + half)
+        out += [(lo, hi - lo), (0x80000000 + lo, hi - lo)]
+    return out
+
+
+@pytest.mark.parametrize("fmt", [O.E4M3, O.E5M2])
+def test_encode_bits_range_over_fp32_patterns(fmt):
+    """The encoder over a range of fp32 bit patterns (the expected side of
+    the exhaustive GPU cast check): PyTorch's float8 cast below the largest
+    finite value, saturation to it at and above (Inf included), and the
+    format's NaN code (S.1111.111 / S.11111.11) for NaN."""
+    fmax = O.FMAX[fmt]
+    fmax_code = 0x7E if fmt == O.E4M3 else 0x7B
+    for start, count in _pattern_windows(fmt):
+        bits = np.arange(start, start + count, dtype=np.uint64).astype(np.uint32)
+        v = bits.view(np.float32)
+        got = O.encode_bits_range(start, count, fmt)
+        sign = (bits >> 31).astype(np.uint8) << 7
+        nan = np.isnan(v)
+        big = ~nan & ((bits & 0x7FFFFFFF) >= np.float32(fmax).view(np.uint32))   # |v| >= fmax, by bits
+        small = ~nan & ~big
+        assert np.all(got[nan] & 0x7F == 0x7F)
+        assert np.array_equal(got[big], fmax_code | sign[big])
+        ref = torch.from_numpy(v[small].copy()).to(TORCH_DT[fmt]).view(torch.uint8).numpy()
+        assert np.array_equal(got[small], ref), hex(start)

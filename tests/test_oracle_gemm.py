@@ -103,3 +103,26 @@ def test_bf16_output_rounding_is_within_normwise_bound():
     # round-to-nearest to 8 significant bits: relative error <= 2^-8 per element
     assert np.all(np.abs(Db - D) <= np.abs(D) * 2.0 ** -8)
     assert rel < 2e-3
+
+
+def test_gemm_points_at_scattered_points():
+    """The point-wise entry (what the full-size parity tests sample) at
+    out-of-order and repeated output points, with 128x128 tiles on B and 1x128
+    blocks on A at a ragged M, N, K: each point equals the exact rational sum
+    of its own row of A and row of B."""
+    rng = np.random.default_rng(31)
+    M, N, K = 9, 260, 300
+    A, tabA = _finite_codes(rng, (M, K), O.E4M3, narrow=True)
+    B, tabB = _finite_codes(rng, (N, K), O.E4M3, narrow=True)
+    sA = np.ldexp(np.float32(1), rng.integers(-3, 4, (M, 3))).astype(np.float32)
+    sB = np.ldexp(np.float32(1), rng.integers(-3, 4, (3, 3))).astype(np.float32)
+    pm = rng.integers(0, M, 200)
+    pn = rng.integers(0, N, 200)
+    pm[:3], pn[:3] = [M - 1, 0, M - 1], [N - 1, N - 1, N - 1]     # corners, one repeated
+    got = O.gemm_points(A, O.E4M3, sA, 1, 128, B, O.E4M3, sB, 128, 128, pm, pn)
+    for i, (m, n) in enumerate(zip(pm, pn)):
+        acc = Fraction(0)
+        for k in range(K):
+            acc += (Fraction(float(tabA[A[m, k]])) * Fraction(float(sA[m, k // 128]))
+                    * Fraction(float(tabB[B[n, k]])) * Fraction(float(sB[n // 128, k // 128])))
+        assert Fraction(got[i]) == acc, (i, m, n)
