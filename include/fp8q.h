@@ -145,7 +145,9 @@ FP8Q_API const char* fp8q_status_str(fp8q_status s);
 /*
  * Bytes of the scale buffers of a quantize call with this recipe and x shape
  * [rows][cols]: *row_bytes for scale_row, *col_bytes for scale_col (0 for
- * per-tensor kinds).  Either output pointer may be NULL.  Host only.
+ * per-tensor kinds).  Either output pointer may be NULL.  Host only.  The
+ * sizes are those of the layouts above, one scale per block of [guide]
+ * sec. 2.2-2.3 or per channel of [nemo] Figure 1.
  */
 FP8Q_API fp8q_status fp8q_scale_bytes(const fp8q_recipe* recipe, int64_t rows, int64_t cols,
                              size_t* row_bytes, size_t* col_bytes);
@@ -242,7 +244,8 @@ FP8Q_API fp8q_status fp8q_delayed_update(fp8q_delayed_state* st, const float* am
 /*
  * Checkpoint: copies the state to host memory.  hist (host fp32
  * [history_len]), head, scale and scale_inv may each be NULL.  Synchronises
- * the device.
+ * the device.  (The state is [guide] sec. 2.1's history; saving and restoring
+ * it has no counterpart on the pages.)
  */
 FP8Q_API fp8q_status fp8q_delayed_get(const fp8q_delayed_state* st, float* hist, int* head,
                              float* scale, float* scale_inv);
@@ -313,21 +316,24 @@ FP8Q_API fp8q_status fp8q_scaled_gemm_mxq(const fp8q_tensor* A, int a_use_col, c
  * (tcgen05.mma.cta_group::2, M = 256, launched as clusters of two CTAs;
  * blockwise scale arrays must then be 16-byte aligned, else the GEMM returns
  * FP8Q_ERR_ARG).  Both compute the same D up to fp32 summation order.  Host
- * only.
+ * only.  No counterpart on the pages: a choice between two tilings of the
+ * same GEMM.
  */
 FP8Q_API fp8q_status fp8q_gemm_set_variant(int variant);
 
 /*
  * Reads and clears the library's device error words on the current device
  * (bit 0: a GEMM pipeline wait timed out, bit 1: a quantize tile-load wait
- * timed out).  Synchronises `stream`.
+ * timed out).  Synchronises `stream`.  No counterpart on the pages: the
+ * library's own failure detection.
  */
 FP8Q_API fp8q_status fp8q_device_errors(unsigned int* flags, void* stream);
 
 /*
- * The saturating RNE cast on its own: out[i] = cast(float with bit pattern
- * start + i) for i < count (device uint8 out).  Serves exhaustive checks of
- * the device conversion over all 2^32 fp32 inputs.
+ * The saturating RNE cast on its own ([guide] sec. 1.1 formats, the cast
+ * rule stated at the top of this header): out[i] = cast(float with bit
+ * pattern start + i) for i < count (device uint8 out).  Serves exhaustive
+ * checks of the device conversion over all 2^32 fp32 inputs.
  */
 FP8Q_API fp8q_status fp8q_cast_f32_bits(uint32_t start, uint64_t count, int fmt, void* out, void* stream);
 
