@@ -179,3 +179,16 @@ def test_row_block_views():
     with pytest.raises(ValueError):
         api.row_block(qt, 64, 512)                               # not a 128-row boundary
     assert api.row_block(qt, 896, 1000).rows == 104
+
+
+def test_missing_library_raises(monkeypatch, tmp_path):
+    """Without the built library the binding raises at the first call; there
+    is no other implementation to fall back on."""
+    from fp8_scaled_quantization_quantize_gb300 import _lib, api
+    missing = str(tmp_path / "libfp8q.so")
+    monkeypatch.setattr(_lib, "_lib", None)
+    monkeypatch.setattr(_lib.load, "__defaults__", (missing,))
+    with pytest.raises(ImportError, match="not built"):
+        _lib.load()
+    with pytest.raises(ImportError, match="not built"):
+        api.scale_bytes(api.BLOCK_1x128, 256, 256, True, True)
