@@ -344,3 +344,40 @@ def test_quantize_multi_and_rows_edge_cases():
     assert np.array_equal(g3["scale_row_bytes"], whole["scale_row_bytes"])
     assert g3["sat_row"] == whole["sat_row"]
     assert api.device_errors() == 0
+
+
+def test_bench_step_as_timed_matches_oracle():
+    """The benchmark's step in the launch arrangement it is timed in: X
+    (1x128) and W (128x128) of the Llama-3-8B up-projection, both copies, in
+    one fp8q_quantize_multi call, then the fprop GEMM with the automatic
+    kernel choice.  Every byte, scale and counter of both tensors equals the
+    oracle's; the GEMM matches the oracle's fp64 sum on every output of 8
+    rows and of 8 columns (the first and last of each among them)."""
+    api = _api()
+    X, W = inputs.llama8b_up_proj()
+    T, H = X.shape
+    F = W.shape[0]
+    qx = api.alloc(O.BLOCK_1x128, O.E4M3, T, H, True, True, "cuda")
+    qw = api.alloc(O.BLOCK_128x128, O.E4M3, F, H, True, True, "cuda")
+    Xd, Wd = X.cuda(), W.cuda()
+    api.quantize_multi([(Xd, qx), (Wd, qw)])
+    refs = {}
+    for name, kind, x, q in (("X", O.BLOCK_1x128, X, qx), ("W", O.BLOCK_128x128, W, qw)):
+        refs[name] = O.quantize(kind, O.E4M3, bits_of(x), True, True)
+        assert_quant_equal(kind, gpu_outputs(q), refs[name], True, True, ctx=f"bench step {name}")
+    Y = api.scaled_gemm(qx, False, qw, False)
+    torch.cuda.synchronize()
+    g = np.random.default_rng(2024)
+    rows = np.unique(np.concatenate([[0, T - 1], g.choice(T, 6, replace=False)]))
+    cols = np.unique(np.concatenate([[0, F - 1], g.choice(F, 6, replace=False)]))
+    pm1, pn1 = [a.ravel() for a in np.meshgrid(rows, np.arange(F), indexing="ij")]
+    pm2, pn2 = [a.ravel() for a in np.meshgrid(np.arange(T), cols, indexing="ij")]
+    pm, pn = np.concatenate([pm1, pm2]), np.concatenate([pn1, pn2])
+    sx, xbm, xbk = O.dequant_scales(O.BLOCK_1x128, refs["X"], "row", T, H)
+    sw, wbn, wbk = O.dequant_scales(O.BLOCK_128x128, refs["W"], "row", F, H)
+    ref = O.gemm_points(refs["X"]["data_row"], O.E4M3, sx, xbm, xbk, refs["W"]["data_row"], O.E4M3, sw, wbn, wbk,
+                        pm, pn)
+    got = Y.float().cpu().numpy()[pm, pn].astype(np.float64)
+    rel = np.linalg.norm(got - ref) / np.linalg.norm(ref)
+    assert np.all(np.isfinite(got)) and rel <= 2e-3, rel
+    assert api.device_errors() == 0
