@@ -28,6 +28,27 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
+# The library takes plain pointers and cannot see a buffer's size or where it
+# lives: a tensor of another shape than the buffers it pairs with, or one in
+# host memory, would reach the kernels as an out-of-range or host address.
+# These checks stop that here.
+
+def _check_device(t: torch.Tensor, ref: torch.Tensor, name: str):
+    if not t.is_cuda or t.device != ref.device:
+        raise ValueError(f"{name} must be on the CUDA device of the buffers it pairs with ({ref.device})")
+
+
+def _check_input(x: torch.Tensor, qt: QTensor, name: str = "x", any_rows: bool = False):
+    """x is contiguous 2-D bf16 of qt's shape (any row count with any_rows:
+    a block of qt's rows) on qt's CUDA device."""
+    if x.dtype != torch.bfloat16 or x.dim() != 2 or not x.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous 2-D bf16 tensor")
+    want = (x.shape[0] if any_rows else qt.rows, qt.cols)
+    if tuple(x.shape) != want:
+        raise ValueError(f"{name} has shape {tuple(x.shape)}; the output buffers hold {(qt.rows, qt.cols)}")
+    _check_device(x, qt.counters, name)
+
+
 def scale_bytes(kind: int, rows: int, cols: int, rowwise: bool, colwise: bool):
     rb, cb = ctypes.c_size_t(0), ctypes.c_size_t(0)
     rc = L.Recipe(kind, E4M3, int(rowwise), int(colwise))
@@ -117,6 +138,11 @@ class DelayedState:
         self.history_len, self.fmt, self.margin = history_len, fmt, margin
 
     def update(self, amax: torch.Tensor, nonfinite: torch.Tensor | None = None, stream=None):
+        if amax.dtype != torch.float32 or amax.numel() < 1 or not amax.is_cuda:
+            raise ValueError("amax must be a CUDA fp32 tensor")
+        if nonfinite is not None and (nonfinite.dtype != torch.int64 or nonfinite.numel() < 1
+                                      or nonfinite.device != amax.device):
+            raise ValueError("nonfinite must be an int64 tensor on amax's device")
         L.check(L.load().fp8q_delayed_update(self.handle, _ptr(amax), _ptr(nonfinite), _stream(stream)),
                 "fp8q_delayed_update")
 
@@ -146,8 +172,7 @@ class DelayedState:
 
 def quantize_into(x: torch.Tensor, qt: QTensor, state: DelayedState | None = None, stream=None) -> QTensor:
     """Quantizes bf16 x [rows, cols] into preallocated qt (same kind / fmt / copies)."""
-    if x.dtype != torch.bfloat16 or x.dim() != 2 or not x.is_contiguous():
-        raise ValueError("x must be a contiguous 2-D bf16 tensor")
+    _check_input(x, qt)
     rc = L.Recipe(qt.kind, qt.fmt, int(qt.rowwise), int(qt.colwise))
     ct = qt.c_struct()
     L.check(L.load().fp8q_quantize(ctypes.byref(rc), _ptr(x), x.shape[0], x.shape[1],
@@ -159,8 +184,7 @@ def quantize_into(x: torch.Tensor, qt: QTensor, state: DelayedState | None = Non
 def quantize_rows_into(x_block: torch.Tensor, qt: QTensor, row0: int, stream=None) -> QTensor:
     """Quantizes rows row0 .. row0 + len(x_block) - 1 of the tensor whose
     buffers qt holds (fp8q_quantize_rows); qt.counters are added to."""
-    if x_block.dtype != torch.bfloat16 or x_block.dim() != 2 or not x_block.is_contiguous():
-        raise ValueError("x_block must be a contiguous 2-D bf16 tensor")
+    _check_input(x_block, qt, "x_block", any_rows=True)
     rc = L.Recipe(qt.kind, qt.fmt, int(qt.rowwise), int(qt.colwise))
     ct = qt.c_struct()
     L.check(L.load().fp8q_quantize_rows(ctypes.byref(rc), _ptr(x_block), row0, x_block.shape[0], qt.rows,
@@ -178,8 +202,7 @@ def quantize_multi(jobs, stream=None):
     for i, job in enumerate(jobs):
         x, qt = job[0], job[1]
         state = job[2] if len(job) > 2 else None
-        if x.dtype != torch.bfloat16 or x.dim() != 2 or not x.is_contiguous():
-            raise ValueError("x must be a contiguous 2-D bf16 tensor")
+        _check_input(x, qt, f"x of job {i}")
         ct = qt.c_struct()
         keep.append(ct)
         arr[i].recipe = L.Recipe(qt.kind, qt.fmt, int(qt.rowwise), int(qt.colwise))
@@ -197,15 +220,28 @@ def quantize(x: torch.Tensor, kind: int, fmt: int = E4M3, rowwise: bool = True, 
     return quantize_into(x, qt, state, stream)
 
 
+def _check_operands(A: QTensor, a_use_col: bool, B: QTensor, b_use_col: bool) -> torch.Tensor:
+    """The chosen copies' data on one CUDA device (a missing copy is left to
+    the library, which rejects it); returns a tensor on that device."""
+    ref = A.counters
+    for name, qt, use_col in (("A", A, a_use_col), ("B", B, b_use_col)):
+        data = qt.data_col if use_col else qt.data_row
+        _check_device(data if data is not None else qt.counters, ref, f"{name}'s buffers")
+    return ref
+
+
 def scaled_gemm(A: QTensor, a_use_col: bool, B: QTensor, b_use_col: bool, out_dtype=torch.bfloat16,
                 out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """D = A_q . B_q^T (fp32 accumulate) with the recipes' scales applied."""
     M = A.cols if a_use_col else A.rows
     K = A.rows if a_use_col else A.cols
     N = B.cols if b_use_col else B.rows
+    ref = _check_operands(A, a_use_col, B, b_use_col)
     if out is None:
-        dev = (A.data_col if a_use_col else A.data_row).device
-        out = torch.empty((M, N), dtype=out_dtype, device=dev)
+        out = torch.empty((M, N), dtype=out_dtype, device=ref.device)
+    if out.dtype not in (torch.bfloat16, torch.float32) or tuple(out.shape) != (M, N) or not out.is_contiguous():
+        raise ValueError(f"out must be a contiguous bf16 or fp32 tensor of shape {(M, N)}")
+    _check_device(out, ref, "out")
     od = {torch.bfloat16: 0, torch.float32: 1}[out.dtype]
     ca, cb = A.c_struct(), B.c_struct()
     L.check(L.load().fp8q_scaled_gemm(ctypes.byref(ca), int(a_use_col), ctypes.byref(cb), int(b_use_col), _ptr(out),
@@ -221,11 +257,19 @@ def scaled_gemm_mxq(A: QTensor, a_use_col: bool, B: QTensor, b_use_col: bool, fm
     M = A.cols if a_use_col else A.rows
     K = A.rows if a_use_col else A.cols
     N = B.cols if b_use_col else B.rows
-    dev = (A.data_col if a_use_col else A.data_row).device
+    dev = _check_operands(A, a_use_col, B, b_use_col).device
     if out is None:
         out = alloc(MXFP8_1x32, fmt, M, N, True, False, dev)
+    if (out.rows, out.cols) != (M, N) or out.data_row is None or out.scale_row is None:
+        raise ValueError(f"out must hold a row-wise MXFP8 copy of shape {(M, N)}")
+    _check_device(out.data_row, out.counters, "out's buffers")
+    _check_device(out.counters, A.counters, "out's buffers")
     if want_d and d_out is None:
         d_out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    if want_d:
+        if d_out.dtype != torch.bfloat16 or tuple(d_out.shape) != (M, N) or not d_out.is_contiguous():
+            raise ValueError(f"d_out must be a contiguous bf16 tensor of shape {(M, N)}")
+        _check_device(d_out, A.counters, "d_out")
     ca, cb, cq = A.c_struct(), B.c_struct(), out.c_struct()
     L.check(L.load().fp8q_scaled_gemm_mxq(ctypes.byref(ca), int(a_use_col), ctypes.byref(cb), int(b_use_col),
                                           _ptr(d_out) if want_d else None, fmt, ctypes.byref(cq), M, N, K,
@@ -239,6 +283,8 @@ def gemm_set_variant(variant: int):
 
 
 def cast_f32_bits(start: int, count: int, fmt: int, out: torch.Tensor, stream=None) -> torch.Tensor:
+    if out.dtype != torch.uint8 or not out.is_cuda or out.numel() < count or not out.is_contiguous():
+        raise ValueError("out must be a contiguous CUDA uint8 tensor of at least count elements")
     L.check(L.load().fp8q_cast_f32_bits(start, count, fmt, _ptr(out), _stream(stream)), "fp8q_cast_f32_bits")
     return out
 
@@ -246,6 +292,8 @@ def cast_f32_bits(start: int, count: int, fmt: int, out: torch.Tensor, stream=No
 def selftest_division(d: torch.Tensor, fmt: int, stream=None):
     """(FP8 code mismatches, fp32 mismatches) of the blockwise division shortcut
     against IEEE division over every finite bf16 x and every divisor in d."""
+    if d.dtype != torch.float32 or not d.is_cuda or not d.is_contiguous():
+        raise ValueError("d must be a contiguous CUDA fp32 tensor")
     out = torch.zeros(2, dtype=torch.int64, device=d.device)
     L.check(L.load().fp8q_selftest_division(_ptr(d), d.numel(), fmt, _ptr(out), _stream(stream)),
             "fp8q_selftest_division")

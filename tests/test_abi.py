@@ -192,3 +192,36 @@ def test_missing_library_raises(monkeypatch, tmp_path):
         _lib.load()
     with pytest.raises(ImportError, match="not built"):
         api.scale_bytes(api.BLOCK_1x128, 256, 256, True, True)
+
+
+def test_binding_rejects_mismatched_or_host_buffers():
+    """The binding refuses, before the library is called, tensors that would
+    reach the kernels as out-of-range or host addresses: an input of another
+    shape than its output buffers, host tensors, a wrong GEMM output."""
+    torch = pytest.importorskip("torch")
+    from fp8_scaled_quantization_quantize_gb300 import api
+    qt = api.alloc(L.BLOCK_1x128, L.E4M3, 256, 128, True, True, device="cpu")
+    x = torch.zeros((256, 128), dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="shape"):
+        api.quantize_into(torch.zeros((512, 128), dtype=torch.bfloat16), qt)
+    with pytest.raises(ValueError, match="shape"):
+        api.quantize_multi([(torch.zeros((256, 256), dtype=torch.bfloat16), qt)])
+    with pytest.raises(ValueError, match="shape"):
+        api.quantize_rows_into(torch.zeros((128, 64), dtype=torch.bfloat16), qt, 0)
+    with pytest.raises(ValueError, match="CUDA device"):
+        api.quantize_into(x, qt)
+    with pytest.raises(ValueError, match="CUDA device"):
+        api.quantize_multi([(x, qt)])
+    with pytest.raises(ValueError, match="CUDA device"):
+        api.quantize_rows_into(x[:128], qt, 0)
+    with pytest.raises(ValueError, match="contiguous 2-D bf16"):
+        api.quantize_into(x.float(), qt)
+    qb = api.alloc(L.BLOCK_128x128, L.E4M3, 384, 128, True, False, device="cpu")
+    with pytest.raises(ValueError, match="CUDA device"):
+        api.scaled_gemm(qt, False, qb, False)
+    with pytest.raises(ValueError, match="CUDA device"):
+        api.scaled_gemm_mxq(qt, False, qb, False)
+    with pytest.raises(ValueError, match="uint8"):
+        api.cast_f32_bits(0, 16, L.E4M3, torch.empty(16, dtype=torch.uint8))
+    with pytest.raises(ValueError, match="fp32"):
+        api.selftest_division(torch.ones(4), L.E4M3)
