@@ -1,4 +1,4 @@
-"""The path's one cross-replica exchange, on CPU ranks (gloo, world size 2).
+"""The path's cross-replica exchanges, on CPU ranks (gloo, world size 2).
 
 When a per-tensor recipe's tensor is sharded across data-parallel ranks
 (rows split), every rank must quantize with the same scale: the shard amaxes
@@ -8,7 +8,10 @@ amax history of the tensor).  Each rank computes its shard's amax with the
 oracle, all-reduces the max, updates its own copy of the state, and casts its
 shard; the states and the concatenated codes must equal the single-process
 oracle run on the whole tensor.  Blockwise / MX recipes need no exchange:
-their blocks never straddle a row split at a multiple of the block height.
+their blocks never straddle a row split at a multiple of the block height,
+so ranks that quantize row shards and all-gather the FP8 codes and scales
+(tensor parallelism's gather, in FP8) hold what one process quantizing the
+whole tensor would.
 """
 import os
 import socket
@@ -78,3 +81,54 @@ def test_sharded_delayed_scaling_matches_single_process():
         assert np.array_equal(np.concatenate([gathered[r][0][t] for r in range(world)]), qfull)
     for r in range(world):
         assert gathered[r][2] == ref.hist.tolist() and gathered[r][3] == ref.head
+
+
+def _gather_worker(rank, world, port, out):
+    """Each rank quantizes its row shard (row-wise copy; shard edges on
+    128-row boundaries) and the ranks all-gather the FP8 codes and their
+    block scales: the exchange a tensor-parallel layer makes when it gathers
+    an activation or a gradient in FP8 instead of bf16."""
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    x = inputs.bf16_bits(inputs.normal_bf16((512, 384), 900, 1e-3))
+    shard = np.ascontiguousarray(np.split(x, world, axis=0)[rank])
+    mine = {}
+    for name, kind, fmt in (("activation mx e4m3", O.MXFP8_1x32, O.E4M3),
+                            ("gradient 1x128 e5m2", O.BLOCK_1x128, O.E5M2)):
+        q = O.quantize(kind, fmt, shard, True, False)
+        mine[name] = (q["data_row"], q["scale_row"], q["sat_row"])
+    gathered = [None] * world
+    dist.all_gather_object(gathered, mine)
+    if rank == 0:
+        out.put(gathered)
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_fp8_allgather_of_row_shards_equals_whole_tensor_quantize():
+    """Gathering per-rank FP8 shards (codes + 1x32 / 1x128 scales) gives what
+    quantizing the whole tensor gives: these blocks never cross a row
+    boundary, so sharding rows needs no scale exchange ("2025 FP8
+    quantized-training guide", sec. 4.1: quantize locally, then all-gather the
+    FP8 bytes; E5M2 for the gradients)."""
+    world = 2
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_gather_worker, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    gathered = q.get(timeout=120)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    x = inputs.bf16_bits(inputs.normal_bf16((512, 384), 900, 1e-3))
+    for name, kind, fmt in (("activation mx e4m3", O.MXFP8_1x32, O.E4M3),
+                            ("gradient 1x128 e5m2", O.BLOCK_1x128, O.E5M2)):
+        whole = O.quantize(kind, fmt, x, True, False)
+        codes = np.concatenate([g[name][0] for g in gathered])
+        scales = np.concatenate([g[name][1] for g in gathered])
+        assert np.array_equal(codes, whole["data_row"]), name
+        assert np.array_equal(scales, whole["scale_row"]), name
+        assert sum(g[name][2] for g in gathered) == whole["sat_row"], name
