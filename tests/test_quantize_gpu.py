@@ -381,3 +381,80 @@ def test_bench_step_as_timed_matches_oracle():
     rel = np.linalg.norm(got - ref) / np.linalg.norm(ref)
     assert np.all(np.isfinite(got)) and rel <= 2e-3, rel
     assert api.device_errors() == 0
+
+
+BAND = 256          # canary bytes on each side of every output buffer (keeps 16-byte alignment)
+CANARY = 0xA5
+
+
+def _guarded(nbytes, device):
+    """nbytes of uint8 inside a buffer with BAND canary bytes on each side:
+    (the inner view, the whole buffer)."""
+    whole = torch.full((BAND + nbytes + BAND,), CANARY, dtype=torch.uint8, device=device)
+    return whole[BAND:BAND + nbytes], whole
+
+
+def _guarded_qtensor(api, kind, fmt, rows, cols, rowwise, colwise, device):
+    """A QTensor whose every buffer sits between canary bands, sized as
+    api.alloc sizes them."""
+    rb, cb = api.scale_bytes(kind, rows, cols, rowwise, colwise)
+    wholes = []
+
+    def buf(n):
+        v, w = _guarded(n, device)
+        wholes.append((w, n))
+        return v
+
+    data_row = buf(rows * cols).view(rows, cols) if rowwise else None
+    data_col = buf(rows * cols).view(cols, rows) if colwise else None
+    scale_row = buf(max(rb, 16)) if rowwise and rb else None
+    scale_col = buf(max(cb, 16)) if colwise and cb else None
+    amax, scale, scale_inv = (buf(4).view(torch.float32) for _ in range(3))
+    counters = buf(24).view(torch.int64)
+    scale.fill_(1.0)
+    scale_inv.fill_(1.0)
+    counters.zero_()
+    qt = api.QTensor(kind, fmt, rows, cols, data_row, data_col, scale_row, scale_col, amax, scale, scale_inv,
+                     counters)
+    return qt, wholes
+
+
+def _bands_intact(wholes):
+    for w, n in wholes:
+        h = w.cpu().numpy()
+        if not (np.all(h[:BAND] == CANARY) and np.all(h[BAND + n:] == CANARY)):
+            return False
+    return True
+
+
+@pytest.mark.parametrize("kind", KINDS)
+def test_outputs_stay_inside_their_buffers(kind):
+    """Guard bands: every quantize output buffer (codes, scales, scalars,
+    counters), the GEMM's D and the fused quantize's outputs are placed
+    between canary bytes at ragged shapes (288 x 400: 128-row and 128-column
+    tails); after the calls the canaries are intact and the quantize outputs
+    still equal the oracle's."""
+    api = _api()
+    rows, cols = 288, 400
+    x = _mixed((rows, cols), 77)
+    qt, wholes = _guarded_qtensor(api, kind, O.E4M3, rows, cols, True, True, "cuda")
+    api.quantize_into(x.cuda(), qt)
+    ref = O.quantize(kind, O.E4M3, bits_of(x), True, True)
+    assert_quant_equal(kind, gpu_outputs(qt), ref, True, True, ctx=f"guarded {kind}")
+    assert _bands_intact(wholes), f"quantize kind {kind} wrote outside a buffer"
+    # D = A . qt^T (M = N = 288, K = 400) into a guarded bf16 buffer; a 128x128
+    # copy pairs with a 1x128 A operand, every other kind with itself
+    qa = api.quantize(x.cuda(), O.BLOCK_1x128, O.E4M3, True, False) if kind == O.BLOCK_128x128 else qt
+    d, dw = _guarded(rows * rows * 2, "cuda")
+    api.scaled_gemm(qa, False, qt, False, out=d.view(torch.bfloat16).view(rows, rows))
+    torch.cuda.synchronize()
+    assert _bands_intact([(dw, rows * rows * 2)]), f"GEMM kind {kind} wrote outside D"
+    if kind == O.MXFP8_1x32:
+        # the fused MXFP8 quantize of D (N = 288, a multiple of 32)
+        qy, yw = _guarded_qtensor(api, O.MXFP8_1x32, O.E4M3, rows, rows, True, False, "cuda")
+        dy, dyw = _guarded(rows * rows * 2, "cuda")
+        api.scaled_gemm_mxq(qt, False, qt, False, O.E4M3, want_d=True, out=qy,
+                            d_out=dy.view(torch.bfloat16).view(rows, rows))
+        torch.cuda.synchronize()
+        assert _bands_intact(yw + [(dyw, rows * rows * 2)]), "fused quantize wrote outside its buffers"
+    assert api.device_errors() == 0
