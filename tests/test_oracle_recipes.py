@@ -146,38 +146,48 @@ def _rand_bits(shape, seed, outliers=True):
     return _bits(x)
 
 
+# code of the largest finite magnitude: E4M3 0.1111.110 = 448, E5M2 0.11110.11 = 57344
+FMAX_CODE = {O.E4M3: 0x7E, O.E5M2: 0x7B}
+
+
+@pytest.mark.parametrize("fmt", [O.E4M3, O.E5M2])
 @pytest.mark.parametrize("br,bc", [(1, 128), (128, 128), (1, 64), (64, 64), (32, 32), (1, 256), (256, 256)])
-def test_blockwise_block_max_hits_fmax(br, bc):
+def test_blockwise_block_max_hits_fmax(br, bc, fmt):
     x = _rand_bits((300, 390), 1)
-    q, d, _, am, sat, nf = O.quant_blocks(x, br, bc, O.KIND_DIV, O.E4M3)
+    q, d, _, am, sat, nf = O.quant_blocks(x, br, bc, O.KIND_DIV, fmt)
     xf = np.abs(O.bf16_to_f32(x))
     for bi in range(am.shape[0]):
         for bj in range(am.shape[1]):
             blk = xf[bi * br:(bi + 1) * br, bj * bc:(bj + 1) * bc]
             qb = q[bi * br:(bi + 1) * br, bj * bc:(bj + 1) * bc]
             assert am[bi, bj] == blk.max()
-            assert np.all((qb[blk == blk.max()] & 0x7F) == 0x7E)
-            assert np.all((qb & 0x7F) <= 0x7E)
+            assert np.all((qb[blk == blk.max()] & 0x7F) == FMAX_CODE[fmt])
+            assert np.all((qb & 0x7F) <= FMAX_CODE[fmt])
 
 
-def test_mx_scaled_block_max_in_top_binade():
+@pytest.mark.parametrize("fmt,emax,top_lo", [(O.E4M3, 8, 0x78), (O.E5M2, 15, 0x78)])
+def test_mx_scaled_block_max_in_top_binade(fmt, emax, top_lo):
+    """e = floor(log2 amax) - emax puts the scaled block maximum in
+    [2^(emax), 2^(emax + 1)): E4M3 [256, 512) (codes 0x78 = 256 .. 0x7E = 448,
+    saturating above), E5M2 [32768, 65536) (0x78 = 32768 .. 0x7B = 57344)."""
     x = _rand_bits((64, 320), 2)
-    q, sc, e8, am, sat, nf = O.quant_blocks(x, 1, 32, O.KIND_POW2, O.E4M3)
+    q, sc, e8, am, sat, nf = O.quant_blocks(x, 1, 32, O.KIND_POW2, fmt)
     for r in range(64):
         for b in range(10):
             e = int(e8[r, b]) - 127
             scaled = float(am[r, b]) * 2.0 ** -e
-            assert 256.0 <= scaled < 512.0
+            assert 2.0 ** emax <= scaled < 2.0 ** (emax + 1)
             top = (q[r, b * 32:(b + 1) * 32] & 0x7F).max()
-            assert 0x78 <= top <= 0x7E
+            assert top_lo <= top <= FMAX_CODE[fmt]
 
 
-def test_pertensor_amax_maps_to_fmax():
+@pytest.mark.parametrize("fmt", [O.E4M3, O.E5M2])
+def test_pertensor_amax_maps_to_fmax(fmt):
     x = _rand_bits((200, 160), 3)
-    res = O.quantize(O.PERTENSOR_CURRENT, O.E4M3, x, True, False)
+    res = O.quantize(O.PERTENSOR_CURRENT, fmt, x, True, False)
     xf = np.abs(O.bf16_to_f32(x))
     assert res["amax"] == xf.max()
-    assert np.all((res["data_row"][xf == xf.max()] & 0x7F) == 0x7E)
+    assert np.all((res["data_row"][xf == xf.max()] & 0x7F) == FMAX_CODE[fmt])
 
 
 @pytest.mark.parametrize("kind", [O.BLOCK_1x128, O.MXFP8_1x32, O.PERCHANNEL_CURRENT])
