@@ -64,6 +64,33 @@ def test_hand_block_pertensor():
     assert np.array_equal(res["data_col"], exp.T)
 
 
+def _k4096_e5m2_expected(ks):
+    tab = {}
+    with open(os.path.join(GOLD, "block_k_times_4096_e5m2.txt")) as f:
+        for line in f:
+            if line.strip() and not line.startswith("#"):
+                k, code = line.split()[:2]
+                tab[int(k)] = int(code, 16)
+    assert len(tab) == 15
+    return np.array([tab[abs(k)] | (0x80 if k < 0 else 0) for k in ks], dtype=np.uint8)
+
+
+def test_hand_block_e5m2_all_recipes():
+    """The same block in E5M2: 1x128 and 128x128 (d = 2^-12), MX (E8M0 115)
+    and per-tensor (s = 4096) all cast 4096 k, three of them ties."""
+    ks = np.array([(i % 29) - 14 for i in range(128)])
+    exp = _k4096_e5m2_expected(ks)
+    for br, bc in ((1, 128), (128, 128)):
+        q, d, _, am, sat, nf = O.quant_blocks(_bits(ks[None, :]), br, bc, O.KIND_DIV, O.E5M2)
+        assert d[0, 0] == np.float32(2.0 ** -12) and am[0, 0] == 14.0
+        assert np.array_equal(q[0], exp) and sat == 0 and nf == 0
+    q, sc, e8, am, sat, nf = O.quant_blocks(_bits(ks[None, :]), 1, 32, O.KIND_POW2, O.E5M2)
+    assert e8.shape == (1, 4) and np.all(e8 == 115) and np.array_equal(q[0], exp) and sat == 0
+    res = O.quantize(O.PERTENSOR_CURRENT, O.E5M2, _bits(ks[None, :]), True, False)
+    assert res["scale"] == np.float32(4096.0) and res["scale_inv"] == np.float32(2.0 ** -12)
+    assert np.array_equal(res["data_row"][0], exp) and res["sat_row"] == 0
+
+
 def test_hand_perchannel():
     """Rows k, 2k, k/2 of k = (c % 29) - 14: row maxima 14, 28, 7 give s = 32,
     16, 64 (RN(448 / amax), exact) and every row the codes of k x 32.  Column
