@@ -58,7 +58,7 @@ def peaks():
 
 
 class _Nvml:
-    """Read-only NVML queries through the driver's libnvidia-ml (ctypes): SM
+    """Read-only NVML queries through the NVIDIA driver's libnvidia-ml (ctypes): SM
     clock, its maximum, power and the active clock-event (throttle) reasons."""
 
     REASONS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown", 0x4: "sw_power_cap"}
