@@ -40,14 +40,24 @@
  *     nonfinite.  Saturated = finite x whose scaled fp32 value exceeds fmax.
  *   - Delayed: step t casts with the scale from the history of steps < t,
  *     then records amax_t, rolls the ring and sets
- *     s = fmax / max(history) * 2^-margin (amax 0 -> 1); a step with a
- *     nonfinite input leaves the state unchanged.
+ *     s = fmax / max(history) * 2^-margin (amax 0 -> 1; a product below
+ *     the smallest normal fp32 is raised to it, so 1 / s stays finite); a
+ *     step with a nonfinite input leaves the state unchanged.
  *
- * Build: gcc -O2 -std=c11 -ffp-contract=off -fPIC -shared (no fused
- * multiply-add contraction, so every fp32 operation rounds on its own).
+ * Build: gcc -O2 -std=c11 -ffp-contract=off -fopenmp -fPIC -shared (no
+ * fused multiply-add contraction, so every fp32 operation rounds on its own).
+ * OpenMP only splits independent work across host threads: blocks of a
+ * quantizer, elements of a per-tensor cast, output points of the GEMM.  Each
+ * block, element and point is computed exactly as in a serial loop (a GEMM
+ * point still sums k = 0..K-1 in order), and what is combined across threads
+ * is a maximum or a count, so the results do not depend on the thread count
+ * (orc_set_threads(1) gives the single-core oracle).
  */
 #include <float.h>
 #include <math.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
@@ -203,6 +213,22 @@ int orc_mx_exponent(float amax, int fmt)
     return e;
 }
 
+/* ------------------------------------------------------------- threads */
+
+/* Host threads the oracle's loops may use (n >= 1); returns the count now in
+ * force.  Without OpenMP everything runs on one thread. */
+int orc_set_threads(int n)
+{
+#ifdef _OPENMP
+    if (n >= 1)
+        omp_set_num_threads(n);
+    return omp_get_max_threads();
+#else
+    (void)n;
+    return 1;
+#endif
+}
+
 /* ------------------------------------------------------------- quantizers */
 
 #define ORC_KIND_MULT 0  /* per-tensor: y = x * s,  s = fmax / amax */
@@ -226,11 +252,16 @@ void orc_quant_blocks(const uint16_t* x, int64_t R, int64_t C, int64_t br, int64
     int64_t nbc = (C + bc - 1) / bc;
     double fmax = orc_fmax(fmt);
     uint64_t nsat = 0, nnf = 0;
+    /* one block (a per-tensor scope): its rows are split across threads;
+     * several blocks: the blocks are */
+    const int one = nbr * nbc == 1;
+#pragma omp parallel for collapse(2) reduction(+ : nsat, nnf) schedule(dynamic, 16) if (!one)
     for (int64_t bi = 0; bi < nbr; ++bi) {
         for (int64_t bj = 0; bj < nbc; ++bj) {
             int64_t r0 = bi * br, r1 = r0 + br < R ? r0 + br : R;
             int64_t c0 = bj * bc, c1 = c0 + bc < C ? c0 + bc : C;
             float amax = 0.0f;
+#pragma omp parallel for reduction(max : amax) if (one)
             for (int64_t r = r0; r < r1; ++r)
                 for (int64_t c = c0; c < c1; ++c) {
                     float f = orc_bf16_to_f32(x[r * C + c]);
@@ -248,16 +279,20 @@ void orc_quant_blocks(const uint16_t* x, int64_t R, int64_t C, int64_t br, int64
                 sc = ldexpf(1.0f, e);
             }
             float mul = (kind == ORC_KIND_POW2) ? ldexpf(1.0f, -e) : sc;
+            uint64_t bsat = 0, bnf = 0;
+#pragma omp parallel for reduction(+ : bsat, bnf) if (one)
             for (int64_t r = r0; r < r1; ++r)
                 for (int64_t c = c0; c < c1; ++c) {
                     float f = orc_bf16_to_f32(x[r * C + c]);
                     float y = (kind == ORC_KIND_DIV) ? f / sc : f * mul;
                     if (!isfinite(f))
-                        ++nnf;
+                        ++bnf;
                     else if (fabs((double)y) > fmax)
-                        ++nsat;
+                        ++bsat;
                     q[r * C + c] = orc_fp8_encode(y, fmt);
                 }
+            nsat += bsat;
+            nnf += bnf;
             if (scale)
                 scale[bi * nbc + bj] = sc;
             if (e8m0)
@@ -280,6 +315,7 @@ void orc_cast_scaled(const uint16_t* x, int64_t n, float s, int fmt, uint8_t* q,
     double fmax = orc_fmax(fmt);
     float amax = 0.0f;
     uint64_t nsat = 0, nnf = 0;
+#pragma omp parallel for reduction(max : amax) reduction(+ : nsat, nnf) schedule(static)
     for (int64_t i = 0; i < n; ++i) {
         float f = orc_bf16_to_f32(x[i]);
         float y = f * s;
@@ -310,6 +346,7 @@ void orc_amax_sat(const uint16_t* x, int64_t n, float s, int fmt, float* amax_ou
     double fmax = orc_fmax(fmt);
     float amax = 0.0f;
     uint64_t nsat = 0, nnf = 0;
+#pragma omp parallel for reduction(max : amax) reduction(+ : nsat, nnf) schedule(static)
     for (int64_t i = 0; i < n; ++i) {
         float f = orc_bf16_to_f32(x[i]);
         if (!isfinite(f)) {
@@ -376,6 +413,11 @@ void orc_delayed_update(orc_delayed* st, float amax, uint64_t nonfinite)
         s = s * ldexpf(1.0f, -st->margin);
         if (isinf(s))
             s = FLT_MAX;
+        /* a margin can push s below the normal range (margin 64 with a
+         * history max near the bf16 maximum): raise it to the smallest
+         * normal fp32, so that 1 / s stays finite */
+        if (s < FLT_MIN)
+            s = FLT_MIN;
     }
     st->scale = s;
     st->scale_inv = 1.0f / s;
@@ -440,6 +482,7 @@ void orc_gemm_points(const uint8_t* A, int fmtA, const float* sA, int64_t a_bm, 
         tabA[c] = orc_fp8_decode((uint8_t)c, fmtA);
         tabB[c] = orc_fp8_decode((uint8_t)c, fmtB);
     }
+#pragma omp parallel for schedule(dynamic, 64)
     for (int64_t p = 0; p < npts; ++p) {
         int64_t m = pm[p], n = pn[p];
         double acc = 0.0;

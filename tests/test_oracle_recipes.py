@@ -305,10 +305,33 @@ def test_delayed_spike_leaves_after_history_length():
 
 
 def test_delayed_margin():
-    st = O.Delayed(4, O.E5M2, 2)
+    """Margins worked by hand: E4M3, margin 1, amax 7: 448 / 7 = 64 exactly,
+    times 2^-1 gives s = 32, and x = 7 scales to 224 = 1.75 * 2^7, the E4M3
+    code 0 1110 110 = 0x76.  E5M2, margin 2, amax 7: 57344 / 7 = 8192 exactly,
+    s = 2048 = 2^11, scale_inv = 2^-11."""
+    st = O.Delayed(4, O.E4M3, 1)
     st.update(7.0)
-    assert st.scale == np.float32(np.float32(57344.0) / np.float32(7.0) * np.float32(0.25))
-    assert st.scale_inv == np.float32(1.0) / st.scale
+    assert st.scale == 32.0 and st.scale_inv == 1.0 / 32.0
+    q, amax, sat, nf = O.cast_scaled(np.array([0x40E0, 0xC0E0], dtype=np.uint16), st.scale, O.E4M3)  # +-7.0
+    assert list(q) == [0x76, 0xF6] and amax == 7.0 and sat == 0 and nf == 0
+    st5 = O.Delayed(4, O.E5M2, 2)
+    st5.update(7.0)
+    assert st5.scale == 2048.0 and st5.scale_inv == 2.0 ** -11
+
+
+def test_delayed_margin_underflow_is_clamped():
+    """A margin large enough to push s below the normal fp32 range (margin
+    64 with history max 2^127: 448 / 2^127 * 2^-64 = 1.75 * 2^-183, below the
+    smallest subnormal) raises s to the smallest normal, 2^-126, so scale_inv
+    = 2^126 stays finite; a subnormal product (margin 20: 1.75 * 2^-139) is
+    raised the same way, and margin 5 on amax 2^120 (s = 1.75 * 2^(8 - 120 - 5) = 1.75 * 2^-117, a
+    normal number) is left alone."""
+    for margin, amax, want in ((64, 2.0 ** 127, 2.0 ** -126), (20, 2.0 ** 127, 2.0 ** -126),
+                               (5, 2.0 ** 120, 1.75 * 2.0 ** -117)):
+        st = O.Delayed(16, O.E4M3, margin)
+        st.update(amax)
+        assert st.scale == np.float32(want), (margin, st.scale)
+        assert np.isfinite(st.scale_inv) and st.scale_inv == np.float32(1.0 / want)
 
 
 def test_pack_mx_positions_and_padding():
