@@ -49,7 +49,7 @@ def build(force: bool = False) -> str:
     """Compiles the oracle with gcc (no FMA contraction) if it is stale."""
     if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
         tmp = _LIB + f".tmp{os.getpid()}"
-        subprocess.check_call(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math",
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fopenmp",
                                "-fPIC", "-shared", _SRC, "-o", tmp, "-lm"])
         os.replace(tmp, _LIB)
     return _LIB
@@ -90,10 +90,18 @@ def lib():
         L.orc_pack_block1x128.argtypes = [P, i64, i64, P]
         L.orc_gemm_points.argtypes = [P, i32, P, i64, i64, i64, P, i32, P, i64, i64, i64,
                                       i64, i64, i64, P, P, i64, P]
+        L.orc_set_threads.restype = i32
+        L.orc_set_threads.argtypes = [i32]
         L.orc_f64_to_bf16.restype = ctypes.c_uint16
         L.orc_f64_to_bf16.argtypes = [ctypes.c_double]
         _lib = L
     return _lib
+
+
+def set_threads(n: int = 0) -> int:
+    """Host threads the oracle's loops use (0: leave as is); returns the count
+    in force.  Results do not depend on it (see the C file's header)."""
+    return int(lib().orc_set_threads(int(n)))
 
 
 def _p(a: np.ndarray):
