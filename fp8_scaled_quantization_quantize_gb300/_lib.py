@@ -17,7 +17,8 @@ PERTENSOR_CURRENT, PERTENSOR_DELAYED, BLOCK_1x128, BLOCK_128x128, MXFP8_1x32, PE
 EXPORTS = ("fp8q_version", "fp8q_status_str", "fp8q_scale_bytes", "fp8q_quantize", "fp8q_delayed_create",
            "fp8q_delayed_update", "fp8q_delayed_get", "fp8q_delayed_set", "fp8q_delayed_history_len",
            "fp8q_delayed_destroy", "fp8q_scaled_gemm", "fp8q_device_errors", "fp8q_cast_f32_bits", "fp8q_selftest_division",
-           "fp8q_gemm_set_variant", "fp8q_scaled_gemm_mxq", "fp8q_quantize_multi", "fp8q_quantize_rows")
+           "fp8q_gemm_set_variant", "fp8q_scaled_gemm_mxq", "fp8q_quantize_multi", "fp8q_quantize_rows",
+           "fp8q_set_wait_limit", "fp8q_stall_next")
 MULTI_MAX = 16  # FP8Q_MULTI_MAX
 
 
@@ -95,6 +96,10 @@ def load(path: str = LIB_PATH):
     L.fp8q_gemm_set_variant.argtypes = [i32]
     L.fp8q_selftest_division.restype = i32
     L.fp8q_selftest_division.argtypes = [P, i64, i32, P, P]
+    L.fp8q_set_wait_limit.restype = i32
+    L.fp8q_set_wait_limit.argtypes = [u64]
+    L.fp8q_stall_next.restype = i32
+    L.fp8q_stall_next.argtypes = [i32]
     L.fp8q_cast_f32_bits.restype = i32
     L.fp8q_cast_f32_bits.argtypes = [u32, u64, i32, P, P]
     _lib = L

@@ -36,6 +36,16 @@ def _ptr(t):
 def _check_device(t: torch.Tensor, ref: torch.Tensor, name: str):
     if not t.is_cuda or t.device != ref.device:
         raise ValueError(f"{name} must be on the CUDA device of the buffers it pairs with ({ref.device})")
+    _check_current(t.device, name)
+
+
+def _check_current(dev: torch.device, name: str):
+    """The library launches on the current CUDA device: buffers of another
+    device would reach its kernels as foreign addresses."""
+    cur = torch.cuda.current_device()
+    if dev.index is not None and dev.index != cur:
+        raise ValueError(f"{name} is on {dev} but cuda:{cur} is the current device; "
+                         f"call inside `with torch.cuda.device({dev.index}):`")
 
 
 def _check_input(x: torch.Tensor, qt: QTensor, name: str = "x", any_rows: bool = False):
@@ -140,6 +150,7 @@ class DelayedState:
     def update(self, amax: torch.Tensor, nonfinite: torch.Tensor | None = None, stream=None):
         if amax.dtype != torch.float32 or amax.numel() < 1 or not amax.is_cuda:
             raise ValueError("amax must be a CUDA fp32 tensor")
+        _check_current(amax.device, "amax")
         if nonfinite is not None and (nonfinite.dtype != torch.int64 or nonfinite.numel() < 1
                                       or nonfinite.device != amax.device):
             raise ValueError("nonfinite must be an int64 tensor on amax's device")
@@ -285,6 +296,7 @@ def gemm_set_variant(variant: int):
 def cast_f32_bits(start: int, count: int, fmt: int, out: torch.Tensor, stream=None) -> torch.Tensor:
     if out.dtype != torch.uint8 or not out.is_cuda or out.numel() < count or not out.is_contiguous():
         raise ValueError("out must be a contiguous CUDA uint8 tensor of at least count elements")
+    _check_current(out.device, "out")
     L.check(L.load().fp8q_cast_f32_bits(start, count, fmt, _ptr(out), _stream(stream)), "fp8q_cast_f32_bits")
     return out
 
@@ -294,6 +306,7 @@ def selftest_division(d: torch.Tensor, fmt: int, stream=None):
     against IEEE division over every finite bf16 x and every divisor in d."""
     if d.dtype != torch.float32 or not d.is_cuda or not d.is_contiguous():
         raise ValueError("d must be a contiguous CUDA fp32 tensor")
+    _check_current(d.device, "d")
     out = torch.zeros(2, dtype=torch.int64, device=d.device)
     L.check(L.load().fp8q_selftest_division(_ptr(d), d.numel(), fmt, _ptr(out), _stream(stream)),
             "fp8q_selftest_division")
@@ -302,6 +315,22 @@ def selftest_division(d: torch.Tensor, fmt: int, stream=None):
 
 
 def device_errors(stream=None) -> int:
+    """Reads and clears the device error words (fp8q_device_errors): bit 0 a
+    GEMM wait timed out, bit 1 a quantize wait timed out; 0 when none did."""
     v = ctypes.c_uint(0)
-    L.check(L.load().fp8q_device_errors(ctypes.byref(v), _stream(stream)), "fp8q_device_errors")
+    st = L.load().fp8q_device_errors(ctypes.byref(v), _stream(stream))
+    if st not in (L.OK, L.ERR_TIMEOUT):
+        L.check(st, "fp8q_device_errors")
     return v.value
+
+
+def set_wait_limit(ns: int):
+    """Limit of every bounded device wait for later launches, in ns (0: the
+    default, one second); see fp8q_set_wait_limit."""
+    L.check(L.load().fp8q_set_wait_limit(int(ns)), "fp8q_set_wait_limit")
+
+
+def stall_next(n: int):
+    """The next n quantize-tile / GEMM launches run with no loads, so their
+    waits run out (a test of the failure path; fp8q_stall_next)."""
+    L.check(L.load().fp8q_stall_next(int(n)), "fp8q_stall_next")

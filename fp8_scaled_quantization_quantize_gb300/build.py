@@ -38,7 +38,7 @@ def _sources():
 
 
 def _deps():
-    return _sources() + sorted(glob.glob(os.path.join(CSRC, "*.cuh"))) + [os.path.join(INCLUDE, "fp8q.h"),
+    return _sources() + sorted(glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(CSRC, "*.h"))) + [os.path.join(INCLUDE, "fp8q.h"),
                                                                            os.path.abspath(__file__)]
 
 

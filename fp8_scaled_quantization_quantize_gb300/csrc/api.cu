@@ -3,6 +3,8 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <atomic>
+
 #include "fp8q_internal.cuh"
 
 struct fp8q_delayed_state {
@@ -14,6 +16,27 @@ struct fp8q_delayed_state {
 };
 
 using namespace fp8q;
+
+namespace {
+
+constexpr uint64_t kDefaultWaitNs = 1000000000ull;  // one second
+std::atomic<uint64_t> g_wait_ns{kDefaultWaitNs};
+std::atomic<int> g_stall{0};
+
+}  // namespace
+
+namespace fp8q {
+
+uint64_t wait_limit_ns() { return g_wait_ns.load(std::memory_order_relaxed); }
+
+int take_stall() {
+    int n = g_stall.load(std::memory_order_relaxed);
+    while (n > 0 && !g_stall.compare_exchange_weak(n, n - 1, std::memory_order_relaxed)) {
+    }
+    return n > 0 ? 1 : 0;
+}
+
+}  // namespace fp8q
 
 namespace {
 
@@ -108,6 +131,7 @@ fp8q_status prepare_quantize(const fp8q_recipe* rc, const void* x, int64_t rows,
     a.row0 = 0;  // the whole tensor
     a.R_total = rows;
     a.tiles_r_total = a.tiles_r;
+    a.wait_ns = wait_limit_ns();
     return FP8Q_OK;
 }
 
@@ -140,6 +164,13 @@ fp8q_status prepare_operands(const fp8q_tensor* A, int a_use_col, const fp8q_ten
     if (!aligned16(ga.data) || !aligned16(gb.data)) return FP8Q_ERR_ALIGN;
     if (!pt && (!aligned16(ga.scale) || !aligned16(gb.scale))) return FP8Q_ERR_ALIGN;
     return FP8Q_OK;
+}
+
+// The state's memory and its kernels belong to the device it was created on;
+// a call made while another device is current would run them there.
+bool on_state_device(const fp8q_delayed_state* st) {
+    int dev = -1;
+    return cudaGetDevice(&dev) == cudaSuccess && dev == st->device;
 }
 
 void set_meta(const fp8q_recipe* rc, int64_t rows, int64_t cols, fp8q_tensor* out) {
@@ -268,12 +299,14 @@ fp8q_status fp8q_delayed_create(int history_len, int fmt, int margin, fp8q_delay
 fp8q_status fp8q_delayed_update(fp8q_delayed_state* st, const float* amax, const unsigned long long* nonfinite,
                                 void* stream) {
     if (!st || !amax) return FP8Q_ERR_ARG;
+    if (!on_state_device(st)) return FP8Q_ERR_ARG;
     return launch_delayed_update(st->dev, amax, nonfinite, (cudaStream_t)stream);
 }
 
 fp8q_status fp8q_delayed_get(const fp8q_delayed_state* st, float* hist, int* head, float* scale,
                              float* scale_inv) {
     if (!st) return FP8Q_ERR_ARG;
+    if (!on_state_device(st)) return FP8Q_ERR_ARG;
     const size_t bytes = sizeof(DelayedDev) + sizeof(float) * (size_t)st->H;
     DelayedDev* host = (DelayedDev*)malloc(bytes);
     if (!host) return FP8Q_ERR_ARG;
@@ -292,6 +325,7 @@ fp8q_status fp8q_delayed_get(const fp8q_delayed_state* st, float* hist, int* hea
 fp8q_status fp8q_delayed_set(fp8q_delayed_state* st, const float* hist, int head, float scale, float scale_inv) {
     if (!st || !hist) return FP8Q_ERR_ARG;
     if (head < 0 || head >= st->H) return FP8Q_ERR_ARG;
+    if (!on_state_device(st)) return FP8Q_ERR_ARG;
     const size_t bytes = sizeof(DelayedDev) + sizeof(float) * (size_t)st->H;
     DelayedDev* host = (DelayedDev*)calloc(1, bytes);
     if (!host) return FP8Q_ERR_ARG;
@@ -359,7 +393,20 @@ fp8q_status fp8q_device_errors(unsigned int* flags, void* stream) {
     if (st != FP8Q_OK) return st;
     st = read_device_errors2(flags);
     if (st != FP8Q_OK) return st;
-    return read_quant_errors(flags);
+    st = read_quant_errors(flags);
+    if (st != FP8Q_OK) return st;
+    return *flags ? FP8Q_ERR_TIMEOUT : FP8Q_OK;
+}
+
+fp8q_status fp8q_set_wait_limit(uint64_t ns) {
+    g_wait_ns.store(ns ? ns : kDefaultWaitNs, std::memory_order_relaxed);
+    return FP8Q_OK;
+}
+
+fp8q_status fp8q_stall_next(int n) {
+    if (n < 0) return FP8Q_ERR_ARG;
+    g_stall.store(n, std::memory_order_relaxed);
+    return FP8Q_OK;
 }
 
 fp8q_status fp8q_selftest_division(const float* d, int64_t nd, int fmt, unsigned long long* mismatches,

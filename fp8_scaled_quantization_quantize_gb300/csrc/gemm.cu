@@ -55,7 +55,6 @@ constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;            // + alignment 
 static_assert(SMEM_BYTES <= 232448, "shared memory budget of one CTA");
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t SF_TMEM_COL = 256;                            // MX scale slots: 12 columns per stage
-constexpr uint64_t kWaitNs = 1000000000ull;
 
 enum { REC_PT = 0, REC_MX = 1, REC_B2D = 2, REC_B1D = 3 };
 
@@ -71,15 +70,17 @@ struct Params {
     const float* bsb;       // [nkb][Np] (1x128) or [ceil(N/128)][nkb] (128x128)
     int64_t Mp, Np, nbn128;
     uint32_t idesc;
+    uint64_t wait_ns;  // bounded-wait limit
+    int stall;         // 1: the producer issues no loads (diagnostic)
 };
 
 // ------------------------------------------------------------ PTX wrappers
 
 // The phase is usually complete already: test it inline (no call, so no
 // register save / restore around it) and only fall back to the bounded loop.
-__device__ __forceinline__ bool mbar_wait(uint32_t a, uint32_t parity, volatile int* abort_flag) {
+__device__ __forceinline__ bool mbar_wait(uint32_t a, uint32_t parity, volatile int* abort_flag, uint64_t limit_ns) {
     if (mbar_try(a, parity)) return true;
-    return mbar_wait_bounded(a, parity, abort_flag, &g_device_errors, 1u, kWaitNs);
+    return mbar_wait_bounded(a, parity, abort_flag, &g_device_errors, 1u, limit_ns);
 }
 
 __device__ __forceinline__ void tc_commit(uint32_t mbar) {
@@ -152,7 +153,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
-        if (lane == 0) {
+        if (lane == 0 && !p.stall) {  // a stalled launch (diagnostic) loads nothing
             int s = 0;
             uint32_t ph = 0;
             uint32_t filled = 0, fill_par = 0;  // per-stage bits for the abort drain
@@ -162,7 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tile_coords(t, p.tiles_m, p.tiles_n, mb, nb);
                 const bool b2 = (2 * nb + 1) < p.nbn128;  // second 128-row scale tile of B exists
                 for (int64_t kb = 0; kb < p.nkb; ++kb) {
-                    if (!mbar_wait(empty(s), ph ^ 1u, abort_flag)) {
+                    if (!mbar_wait(empty(s), ph ^ 1u, abort_flag, p.wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -189,7 +190,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (*abort_flag) {
                 // let copies already issued land before the CTA exits (bounded)
                 for (int i = 0; i < STAGES; ++i)
-                    if (filled >> i & 1u) mbar_drain(full(i), (fill_par >> i) & 1u, kWaitNs / 10);
+                    if (filled >> i & 1u) mbar_drain(full(i), (fill_par >> i) & 1u, p.wait_ns / 10);
             }
         }
     } else if (warp == 1) {
@@ -204,21 +205,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (REC == REC_PT || REC == REC_MX) {
                     // per-tensor: two accumulator buffers, so the epilogue of tile i
                     // overlaps the MMAs of tile i + 1; MX: one (its scale slots use the rest)
-                    if (!mbar_wait(tempty(tile_i % kAcc), ((tile_i / kAcc) & 1u) ^ 1u, abort_flag)) break;
+                    if (!mbar_wait(tempty(tile_i % kAcc), ((tile_i / kAcc) & 1u) ^ 1u, abort_flag, p.wait_ns)) break;
                     tc_fence_after();
                 }
                 for (int64_t kb = 0; kb < p.nkb; ++kb) {
                     uint32_t dcol = (REC == REC_PT) ? (tile_i % kAcc) * BN : 0;
                     if (REC == REC_B2D || REC == REC_B1D) {
                         const uint32_t buf = (uint32_t)(kbg & 1u);
-                        if (!mbar_wait(tempty(buf), (uint32_t)((kbg >> 1) & 1u) ^ 1u, abort_flag)) {
+                        if (!mbar_wait(tempty(buf), (uint32_t)((kbg >> 1) & 1u) ^ 1u, abort_flag, p.wait_ns)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
                         dcol = buf * BN;
                     }
-                    if (!mbar_wait(full(s), ph, abort_flag)) {
+                    if (!mbar_wait(full(s), ph, abort_flag, p.wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -257,7 +258,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // every MMA / copy this thread issued has completed once mma_done fires
             tc_commit(mma_done);
-            mbar_drain(mma_done, 0, kWaitNs);
+            mbar_drain(mma_done, 0, p.wait_ns);
         }
     } else {
         // ------------------------------------------------ epilogue warps
@@ -280,7 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t tcol = (uint32_t)(kEpiCols * j);
             if (REC == REC_PT || REC == REC_MX) {
                 const uint32_t abuf = tile_i % kAcc;
-                if (!mbar_wait(tfull(abuf), (tile_i / kAcc) & 1u, abort_flag)) break;
+                if (!mbar_wait(tfull(abuf), (tile_i / kAcc) & 1u, abort_flag, p.wait_ns)) break;
                 tc_fence_after();
                 // drain this warp's 64 columns into registers, hand TMEM back, then store
                 uint32_t r[64];
@@ -330,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     const float sc = __fmul_rn(sa, sbk);
                     const uint32_t buf = (uint32_t)(kbg & 1u);
-                    if (!mbar_wait(tfull(buf), (uint32_t)((kbg >> 1) & 1u), abort_flag)) {
+                    if (!mbar_wait(tfull(buf), (uint32_t)((kbg >> 1) & 1u), abort_flag, p.wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -390,26 +391,16 @@ bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t K, uint32_
     return make_map_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, base, rows, K, 128, box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-int g_sms = 0;
-
 template <int REC, bool F32>
 fp8q_status launch_t(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& md, const Params& p,
                      cudaStream_t s) {
     auto kern = gemm_kernel<REC, F32>;
-    static bool attr = false;
-    if (!attr) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) != cudaSuccess)
-            return FP8Q_ERR_CUDA;
-        attr = true;
-    }
-    if (g_sms == 0) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&g_sms, cudaDevAttrMultiProcessorCount, dev);
-        if (g_sms < 1) g_sms = 1;
-    }
+    static PerDevice<bool> attr;
+    if (!smem_opt_in(attr, kern, SMEM_BYTES)) return FP8Q_ERR_CUDA;
+    const int sms = sm_count();
+    if (sms < 1) return FP8Q_ERR_CUDA;
     const int64_t ntiles = p.tiles_m * p.tiles_n;
-    const int grid = (int)(ntiles < g_sms ? ntiles : g_sms);
+    const int grid = (int)(ntiles < sms ? ntiles : sms);
     kern<<<grid, kThreads, SMEM_BYTES, s>>>(ma, mb, md, p);
     return cudaGetLastError() == cudaSuccess ? FP8Q_OK : FP8Q_ERR_CUDA;
 }
@@ -463,6 +454,8 @@ fp8q_status launch_gemm(const GemmOperand& A, const GemmOperand& B, void* D, int
     p.tiles_n = (N + BN - 1) / BN;
     p.nkb = (K + BK - 1) / BK;
     p.D = D;
+    p.wait_ns = wait_limit_ns();
+    p.stall = take_stall();
     p.Mp = p.tiles_m * BM;
     if (p.Mp * p.nkb >= ((int64_t)1 << 31) || ((N + 127) / 128 * 128) * p.nkb >= ((int64_t)1 << 31))
         return FP8Q_ERR_SHAPE;  // the blockwise epilogue indexes its scales with 32-bit offsets

@@ -36,7 +36,6 @@ __device__ unsigned int g_device_errors2 = 0;
 namespace {
 
 constexpr int BM = 128, BK = 128;
-constexpr uint64_t kWaitNs = 1000000000ull;
 // recipes: per-tensor, MXFP8, blockwise 1x128 x 128x128 / 1x128 x 1x128, per-channel
 enum { REC_PT = 0, REC_MX = 1, REC_B2D = 2, REC_B1D = 3, REC_PC = 4 };
 
@@ -91,6 +90,8 @@ struct Params2 {
     uint8_t* qscale;                 // packed 128x4 E8M0 tiles of the [M][N] row copy
     unsigned long long* qcounters;   // [0] saturated, [2] NaN / Inf elements
     int hasD;                        // also store the bf16 D
+    uint64_t wait_ns;                // bounded-wait limit
+    int stall;                       // 1: the producers issue no loads (diagnostic)
 };
 
 // ------------------------------------------------------------ PTX wrappers
@@ -115,9 +116,9 @@ __device__ __forceinline__ uint32_t mapa(uint32_t addr, uint32_t rank) {
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
-__device__ __forceinline__ bool mbar_wait2(uint32_t a, uint32_t parity, volatile int* abort_flag) {
+__device__ __forceinline__ bool mbar_wait2(uint32_t a, uint32_t parity, volatile int* abort_flag, uint64_t limit_ns) {
     if (mbar_try(a, parity)) return true;
-    return mbar_wait_bounded(a, parity, abort_flag, &g_device_errors2, 1u, kWaitNs);
+    return mbar_wait_bounded(a, parity, abort_flag, &g_device_errors2, 1u, limit_ns);
 }
 // TMA load into this CTA's shared memory (its shared::cta address, which is
 // also its shared::cluster address) completing on an mbarrier given by a
@@ -387,7 +388,7 @@ __global__ void __launch_bounds__(Cfg<REC>::THREADS, 1)
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer (both CTAs)
-        if (lane == 0) {
+        if (lane == 0 && !p.stall) {  // a stalled launch (diagnostic) loads nothing
             int s = 0;
             uint32_t ph = 0, kbp = 0;
             bool ok = true;
@@ -398,7 +399,7 @@ __global__ void __launch_bounds__(Cfg<REC>::THREADS, 1)
                 const int64_t rs = mp * 256 + BM * cr;    // this CTA's first row
                 const bool arow = rs < p.Mp;             // else all its rows are past M: no A scales
                 for (int64_t kb = 0; kb < p.nkb; ++kb) {
-                    if (!mbar_wait2(empty(s), ph ^ 1u, abort_flag)) {
+                    if (!mbar_wait2(empty(s), ph ^ 1u, abort_flag, p.wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -416,7 +417,7 @@ __global__ void __launch_bounds__(Cfg<REC>::THREADS, 1)
                     }
                     if constexpr (C::BLOCKWISE) {
                         const uint32_t r = kbp % C::SR;
-                        if (!mbar_wait2(sempty(r), ((kbp / C::SR) & 1u) ^ 1u, abort_flag)) {
+                        if (!mbar_wait2(sempty(r), ((kbp / C::SR) & 1u) ^ 1u, abort_flag, p.wait_ns)) {
                             ok = false;
                             break;
                         }
@@ -451,21 +452,21 @@ __global__ void __launch_bounds__(Cfg<REC>::THREADS, 1)
             for (int64_t t = cid; t < npt && ok; t += ncl, ++tile_i) {
                 const uint32_t abuf = tile_i % NACC;
                 if (REC == REC_PT || REC == REC_PC || REC == REC_MX) {
-                    if (!mbar_wait2(tempty(abuf), ((tile_i / NACC) & 1u) ^ 1u, abort_flag)) break;
+                    if (!mbar_wait2(tempty(abuf), ((tile_i / NACC) & 1u) ^ 1u, abort_flag, p.wait_ns)) break;
                     tc_fence_after();
                 }
                 for (int64_t kb = 0; kb < p.nkb; ++kb) {
                     uint32_t dcol = (REC == REC_PT || REC == REC_PC) ? abuf * BN : 0;
                     if (REC == REC_B2D || REC == REC_B1D) {
                         const uint32_t buf = kbg % NACC;
-                        if (!mbar_wait2(tempty(buf), ((kbg / NACC) & 1u) ^ 1u, abort_flag)) {
+                        if (!mbar_wait2(tempty(buf), ((kbg / NACC) & 1u) ^ 1u, abort_flag, p.wait_ns)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
                         dcol = buf * BN;
                     }
-                    if (!mbar_wait2(full(s), ph, abort_flag) || (REC == REC_MX && !mbar_wait2(sfr(s), ph, abort_flag))) {
+                    if (!mbar_wait2(full(s), ph, abort_flag, p.wait_ns) || (REC == REC_MX && !mbar_wait2(sfr(s), ph, abort_flag, p.wait_ns))) {
                         ok = false;
                         break;
                     }
@@ -502,7 +503,7 @@ __global__ void __launch_bounds__(Cfg<REC>::THREADS, 1)
                 if (!ok) break;
             }
             tc2_commit_local(mma_done);
-            mbar_drain(mma_done, 0, kWaitNs);
+            mbar_drain(mma_done, 0, p.wait_ns);
         }
     } else {
         // ------------------------------------------------ epilogue (both CTAs, own 128 rows)
@@ -548,7 +549,7 @@ __global__ void __launch_bounds__(Cfg<REC>::THREADS, 1)
             if constexpr (REC == REC_MX) {
                 while (sf_ok && g_sf < limit) {
                     const int st = (int)(g_sf % STAGES);
-                    if (!mbar_wait2(sfl(st), (uint32_t)((g_sf / STAGES) & 1u), abort_flag)) {
+                    if (!mbar_wait2(sfl(st), (uint32_t)((g_sf / STAGES) & 1u), abort_flag, p.wait_ns)) {
                         sf_ok = false;
                         break;
                     }
@@ -581,7 +582,7 @@ __global__ void __launch_bounds__(Cfg<REC>::THREADS, 1)
             const int64_t col0 = nb * BN + EC * j;
             if constexpr (!C::BLOCKWISE) {
                 const uint32_t abuf = tile_i % NACC;
-                if (!mbar_wait2(tfull(abuf), (tile_i / NACC) & 1u, abort_flag)) break;
+                if (!mbar_wait2(tfull(abuf), (tile_i / NACC) & 1u, abort_flag, p.wait_ns)) break;
                 tc_fence_after();
                 uint32_t r[EC];
 #pragma unroll
@@ -625,7 +626,7 @@ __global__ void __launch_bounds__(Cfg<REC>::THREADS, 1)
                 bool ok = true;
                 for (int64_t kb = 0; kb < p.nkb; ++kb, ++kbg) {
                     const uint32_t r = kbg % C::SR;
-                    if (!mbar_wait2(sfull(r), (kbg / C::SR) & 1u, abort_flag)) {
+                    if (!mbar_wait2(sfull(r), (kbg / C::SR) & 1u, abort_flag, p.wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -635,7 +636,7 @@ __global__ void __launch_bounds__(Cfg<REC>::THREADS, 1)
                     // 256-column boundaries)
                     const float sc = (REC == REC_B2D) ? __fmul_rn(sa, scl[128 + (int)((nb * BN + EC * j) / 128 - (nb * BN) / 128)]) : 0.0f;
                     const uint32_t buf = kbg % NACC;
-                    if (!mbar_wait2(tfull(buf), (kbg / NACC) & 1u, abort_flag)) {
+                    if (!mbar_wait2(tfull(buf), (kbg / NACC) & 1u, abort_flag, p.wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -697,24 +698,14 @@ __global__ void __launch_bounds__(Cfg<REC>::THREADS, 1)
     }
 }
 
-int g_sms2 = 0;
-
 template <int REC, bool F32, int QF>
 fp8q_status launch2_t(const CUtensorMap* maps, const Params2& p, cudaStream_t s) {
     using C = Cfg<REC>;
     auto kern = gemm2_kernel<REC, F32, QF>;
-    static bool attr = false;
-    if (!attr) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
-            return FP8Q_ERR_CUDA;
-        attr = true;
-    }
-    if (g_sms2 == 0) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&g_sms2, cudaDevAttrMultiProcessorCount, dev);
-        if (g_sms2 < 2) g_sms2 = 2;
-    }
+    static PerDevice<bool> attr;
+    if (!smem_opt_in(attr, kern, C::SMEM)) return FP8Q_ERR_CUDA;
+    const int sms = sm_count();
+    if (sms < 2) return FP8Q_ERR_CUDA;
     const int64_t npt = p.tiles_m2 * p.tiles_n;
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof(cfg));
@@ -729,13 +720,15 @@ fp8q_status launch2_t(const CUtensorMap* maps, const Params2& p, cudaStream_t s)
     cfg.attrs = la;
     cfg.numAttrs = 1;
     // as many persistent pairs as can be resident at once (SM pairs must sit
-    // in one GPC, so this can be below half the SM count)
-    static int max_clusters = 0;
-    if (max_clusters == 0) {
-        cfg.gridDim = dim3((unsigned)g_sms2, 1, 1);
-        if (cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg) != cudaSuccess || max_clusters < 1)
-            max_clusters = g_sms2 / 2;
-    }
+    // in one GPC, so this can be below half the SM count), once per device
+    static PerDevice<int> resident;
+    int max_clusters = 0;
+    resident.get(current_device(), max_clusters, [&](int& v) {
+        cfg.gridDim = dim3((unsigned)sms, 1, 1);
+        if (cudaOccupancyMaxActiveClusters(&v, kern, &cfg) != cudaSuccess || v < 1) v = sms / 2;
+        return true;
+    });
+    if (max_clusters < 1) max_clusters = sms / 2;
     const int64_t ncl = npt < max_clusters ? npt : max_clusters;
     cfg.gridDim = dim3((unsigned)(2 * ncl), 1, 1);
     if (cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p) != cudaSuccess)
@@ -784,6 +777,8 @@ fp8q_status launch_gemm_pair(const GemmOperand& A, const GemmOperand& B, void* D
     Params2 p;
     memset(&p, 0, sizeof(p));
     p.hasD = D != nullptr;
+    p.wait_ns = wait_limit_ns();
+    p.stall = take_stall();
     p.qscale = (uint8_t*)qscale;
     p.qcounters = qcounters;
     if (qfmt >= 0 && qcounters != nullptr && cudaMemsetAsync(qcounters, 0, 3 * sizeof(unsigned long long), s) != cudaSuccess)

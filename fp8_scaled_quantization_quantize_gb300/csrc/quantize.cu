@@ -36,7 +36,6 @@ constexpr int kTile = 128;
 constexpr int kStages = 3;
 constexpr uint32_t kStageBytes = kTile * kTile * 2;  // one bf16 tile
 constexpr uint32_t kTileSmem = kStages * kStageBytes + 1024;
-constexpr uint64_t kQuantWaitNs = 1000000000ull;
 
 __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
     uint4 v;
@@ -423,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     // [128 rows][128 bytes] in the 128-byte swizzle
     auto issue = [&](uint32_t j) {
         const uint32_t tileid = blockIdx.x + j * gridDim.x;
-        if (tileid >= ntiles) return;
+        if (tileid >= ntiles || a.stall) return;  // a stalled launch (diagnostic) loads nothing
         const uint32_t s = j % kStages;
         const uint32_t tr = tileid / tiles_c, tc = tileid - tr * tiles_c;
         mbar_expect_tx(bar(s), kStageBytes);
@@ -465,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         // the tile's place in the whole tensor (a block of rows starts at row0)
         const int64_t trg = (int64_t)tr + a.row0 / kTile, r0g = a.row0 + r0;
         const int64_t tileg = trg * (int64_t)tiles_c + tc;
-        const bool ok = mbar_wait_bounded(bar(stg), ph, &abort_flag, &g_quant_errors, 2u, kQuantWaitNs);
+        const bool ok = mbar_wait_bounded(bar(stg), ph, &abort_flag, &g_quant_errors, 2u, a.wait_ns);
         if (__syncthreads_or(!ok)) break;  // the whole CTA leaves together
         uint8_t* stage = qsmem + stg * kStageBytes;
 
@@ -756,11 +755,11 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     if (t == 0) {
         bulk_wait_all();  // the codes' stores are complete before the CTA's shared memory goes away
-        if (abort_flag) {
+        if (abort_flag && !a.stall) {
             // let the tile loads already issued land before the CTA exits (bounded)
             for (uint32_t j = it; j < it + 2; ++j)
                 if (blockIdx.x + j * gridDim.x < ntiles)
-                    mbar_drain(bar((int)(j % kStages)), (j / kStages) & 1u, kQuantWaitNs / 10);
+                    mbar_drain(bar((int)(j % kStages)), (j / kStages) & 1u, a.wait_ns / 10);
         }
     }
 
@@ -904,6 +903,9 @@ __global__ void delayed_update_kernel(DelayedDev* st, const float* amax, const u
         s = __fdiv_rn(st->fmt == FP8Q_E4M3 ? 448.0f : 57344.0f, m);
         s = __fmul_rn(s, exp2_neg(st->margin));
         if (isinf(s)) s = 3.402823466e38f;
+        // a large margin can push s below the normal range: the smallest
+        // normal fp32 keeps 1 / s finite
+        if (s < 1.175494351e-38f) s = 1.175494351e-38f;
     }
     st->scale = s;
     st->scale_inv = __fdiv_rn(1.0f, s);
@@ -976,27 +978,20 @@ __global__ void div_selftest_kernel(const float* d, int64_t nd, unsigned long lo
     }
 }
 
-int g_num_sms = 0;
-
+// SMs of the current device (at least 1, so that a grid size stays valid; a
+// device that cannot be queried fails at the launch instead).
 int num_sms() {
-    if (g_num_sms == 0) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
-        if (g_num_sms <= 0) g_num_sms = 1;
-    }
-    return g_num_sms;
+    const int n = sm_count();
+    return n > 0 ? n : 1;
 }
 
 template <int KIND, int FMT, bool ROW, bool COL>
-fp8q_status launch_tile(const QuantArgs& a, cudaStream_t s) {
-    static bool attr = false;
+fp8q_status launch_tile(const QuantArgs& args, cudaStream_t s) {
+    QuantArgs a = args;
+    a.stall = take_stall();
+    static PerDevice<bool> attr;
     auto kern = quant_tile_kernel<KIND, FMT, ROW, COL>;
-    if (!attr) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kTileSmem) != cudaSuccess)
-            return FP8Q_ERR_CUDA;
-        attr = true;
-    }
+    if (!smem_opt_in(attr, kern, kTileSmem)) return FP8Q_ERR_CUDA;
     const int64_t ntiles = a.tiles_r * a.tiles_c;
     if (a.tiles_r_total * a.tiles_c >= ((int64_t)1 << 31)) return FP8Q_ERR_SHAPE;  // tiles counted in 32 bits
     CUtensorMap tm, trow, tcol;

@@ -225,9 +225,11 @@ FP8Q_API fp8q_status fp8q_quantize_multi(const fp8q_quantize_job* jobs, int n, v
  * Creates a delayed-scaling state on the current device: history_len in
  * [1, 4096] (the [guide] sec. 2.1 history; 16 by default in the tests),
  * margin in [0, 64] (s = fmax / max(history) * 2^-margin; [essay] sec. 3.3
- * uses 0).  The history starts all zero, so the first step casts with s = 1.
- * Allocates device memory (cudaMalloc) and synchronises.  *out receives the
- * handle; free it with fp8q_delayed_destroy.
+ * uses 0; an s below the smallest normal fp32, which a large margin on a
+ * large history maximum can give, is raised to it so that scale_inv = 1 / s
+ * stays finite).  The history starts all zero, so the first step casts with
+ * s = 1.  Allocates device memory (cudaMalloc) and synchronises.  *out
+ * receives the handle; free it with fp8q_delayed_destroy.
  */
 FP8Q_API fp8q_status fp8q_delayed_create(int history_len, int fmt, int margin, fp8q_delayed_state** out);
 
@@ -236,7 +238,8 @@ FP8Q_API fp8q_status fp8q_delayed_create(int history_len, int fmt, int margin, f
  * scale, on `stream`.  nonfinite (device uint64[1], may be NULL) nonzero
  * leaves the state unchanged.  fp8q_quantize does this itself for the
  * delayed kind; this entry point serves callers that combine amax values
- * from elsewhere (e.g. a max over data-parallel replicas).
+ * from elsewhere (e.g. a max over data-parallel replicas).  FP8Q_ERR_ARG when
+ * the current device is not the one the state was created on.
  */
 FP8Q_API fp8q_status fp8q_delayed_update(fp8q_delayed_state* st, const float* amax,
                                 const unsigned long long* nonfinite, void* stream);
@@ -245,13 +248,15 @@ FP8Q_API fp8q_status fp8q_delayed_update(fp8q_delayed_state* st, const float* am
  * Checkpoint: copies the state to host memory.  hist (host fp32
  * [history_len]), head, scale and scale_inv may each be NULL.  Synchronises
  * the device.  (The state is [guide] sec. 2.1's history; saving and restoring
- * it has no counterpart on the pages.)
+ * it has no counterpart on the pages.)  FP8Q_ERR_ARG when the current device
+ * is not the state's.
  */
 FP8Q_API fp8q_status fp8q_delayed_get(const fp8q_delayed_state* st, float* hist, int* head,
                              float* scale, float* scale_inv);
 
 /* Restore: overwrites history (host fp32 [history_len]), head, and the scale
- * pair from host memory.  Synchronises the device. */
+ * pair from host memory.  Synchronises the device.  FP8Q_ERR_ARG when the
+ * current device is not the state's. */
 FP8Q_API fp8q_status fp8q_delayed_set(fp8q_delayed_state* st, const float* hist, int head,
                              float scale, float scale_inv);
 
@@ -324,10 +329,27 @@ FP8Q_API fp8q_status fp8q_gemm_set_variant(int variant);
 /*
  * Reads and clears the library's device error words on the current device
  * (bit 0: a GEMM pipeline wait timed out, bit 1: a quantize tile-load wait
- * timed out).  Synchronises `stream`.  No counterpart on the pages: the
- * library's own failure detection.
+ * timed out) into *flags.  Synchronises `stream`.  Returns FP8Q_ERR_TIMEOUT
+ * when a bit was set, FP8Q_OK when none was.  No counterpart on the pages:
+ * the library's own failure detection.
  */
 FP8Q_API fp8q_status fp8q_device_errors(unsigned int* flags, void* stream);
+
+/*
+ * Failure-detection settings (host only, process wide; no counterpart on the
+ * pages).  Every wait inside the quantize tile kernel and the GEMM kernels
+ * (on a pipeline stage, an accumulator, a scale tile) is bounded: past the
+ * limit it sets the error word that fp8q_device_errors reads, the CTA drains
+ * what it has in flight (bounded), frees its TMEM and exits, and the device
+ * stays usable.  fp8q_set_wait_limit sets that limit in nanoseconds for
+ * launches made afterwards (0 restores the default, one second).
+ * fp8q_stall_next(n) makes the next n quantize-tile or GEMM launches run
+ * stalled: their producers issue no loads, so their first pipeline waits run
+ * out and the launches end through the path above (their outputs are left
+ * unwritten).  It exists to test that path; n = 0 cancels.
+ */
+FP8Q_API fp8q_status fp8q_set_wait_limit(uint64_t ns);
+FP8Q_API fp8q_status fp8q_stall_next(int n);
 
 /*
  * The saturating RNE cast on its own ([guide] sec. 1.1 formats, the cast
