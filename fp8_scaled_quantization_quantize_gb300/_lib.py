@@ -18,7 +18,7 @@ EXPORTS = ("fp8q_version", "fp8q_status_str", "fp8q_scale_bytes", "fp8q_quantize
            "fp8q_delayed_update", "fp8q_delayed_get", "fp8q_delayed_set", "fp8q_delayed_history_len",
            "fp8q_delayed_destroy", "fp8q_scaled_gemm", "fp8q_device_errors", "fp8q_cast_f32_bits", "fp8q_selftest_division",
            "fp8q_gemm_set_variant", "fp8q_scaled_gemm_mxq", "fp8q_quantize_multi", "fp8q_quantize_rows",
-           "fp8q_set_wait_limit", "fp8q_stall_next")
+           "fp8q_set_wait_limit", "fp8q_stall_next", "fp8q_scaled_gemm_q")
 MULTI_MAX = 16  # FP8Q_MULTI_MAX
 
 
@@ -92,6 +92,9 @@ def load(path: str = LIB_PATH):
     L.fp8q_scaled_gemm_mxq.restype = i32
     L.fp8q_scaled_gemm_mxq.argtypes = [ctypes.POINTER(Tensor), i32, ctypes.POINTER(Tensor), i32, P, i32,
                                        ctypes.POINTER(Tensor), i64, i64, i64, P]
+    L.fp8q_scaled_gemm_q.restype = i32
+    L.fp8q_scaled_gemm_q.argtypes = [ctypes.POINTER(Tensor), i32, ctypes.POINTER(Tensor), i32, P, i32, i32,
+                                     ctypes.POINTER(Tensor), i64, i64, i64, P]
     L.fp8q_gemm_set_variant.restype = i32
     L.fp8q_gemm_set_variant.argtypes = [i32]
     L.fp8q_selftest_division.restype = i32

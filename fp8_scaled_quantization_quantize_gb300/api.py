@@ -260,19 +260,24 @@ def scaled_gemm(A: QTensor, a_use_col: bool, B: QTensor, b_use_col: bool, out_dt
     return out
 
 
-def scaled_gemm_mxq(A: QTensor, a_use_col: bool, B: QTensor, b_use_col: bool, fmt: int = E4M3,
-                    want_d: bool = True, out: QTensor | None = None, d_out: torch.Tensor | None = None,
-                    stream=None):
-    """The GEMM with its bf16 output also quantized MXFP8 1x32 row-wise in the
-    epilogue (fp8q_scaled_gemm_mxq): returns (D bf16 or None, QTensor)."""
+def scaled_gemm_q(A: QTensor, a_use_col: bool, B: QTensor, b_use_col: bool, kind: int = MXFP8_1x32,
+                  fmt: int = E4M3, want_d: bool = True, out: QTensor | None = None,
+                  d_out: torch.Tensor | None = None, stream=None):
+    """The GEMM with its bf16 output also quantized row-wise in the epilogue
+    (fp8q_scaled_gemm_q), kind MXFP8_1x32 or BLOCK_1x128: returns
+    (D bf16 or None, QTensor)."""
     M = A.cols if a_use_col else A.rows
     K = A.rows if a_use_col else A.cols
     N = B.cols if b_use_col else B.rows
     dev = _check_operands(A, a_use_col, B, b_use_col).device
+    if kind not in (MXFP8_1x32, BLOCK_1x128):
+        raise ValueError("kind must be MXFP8_1x32 or BLOCK_1x128")
     if out is None:
-        out = alloc(MXFP8_1x32, fmt, M, N, True, False, dev)
-    if (out.rows, out.cols) != (M, N) or out.data_row is None or out.scale_row is None:
-        raise ValueError(f"out must hold a row-wise MXFP8 copy of shape {(M, N)}")
+        out = alloc(kind, fmt, M, N, True, False, dev)
+    if (out.rows, out.cols) != (M, N) or out.data_row is None or out.scale_row is None or out.kind != kind:
+        raise ValueError(f"out must hold a row-wise copy of kind {kind} and shape {(M, N)}")
+    if out.scale_row.numel() < scale_bytes(kind, M, N, True, False)[0]:
+        raise ValueError("out.scale_row is smaller than the recipe's scale bytes")
     _check_device(out.data_row, out.counters, "out's buffers")
     _check_device(out.counters, A.counters, "out's buffers")
     if want_d and d_out is None:
@@ -282,10 +287,18 @@ def scaled_gemm_mxq(A: QTensor, a_use_col: bool, B: QTensor, b_use_col: bool, fm
             raise ValueError(f"d_out must be a contiguous bf16 tensor of shape {(M, N)}")
         _check_device(d_out, A.counters, "d_out")
     ca, cb, cq = A.c_struct(), B.c_struct(), out.c_struct()
-    L.check(L.load().fp8q_scaled_gemm_mxq(ctypes.byref(ca), int(a_use_col), ctypes.byref(cb), int(b_use_col),
-                                          _ptr(d_out) if want_d else None, fmt, ctypes.byref(cq), M, N, K,
-                                          _stream(stream)), "fp8q_scaled_gemm_mxq")
+    L.check(L.load().fp8q_scaled_gemm_q(ctypes.byref(ca), int(a_use_col), ctypes.byref(cb), int(b_use_col),
+                                        _ptr(d_out) if want_d else None, kind, fmt, ctypes.byref(cq), M, N, K,
+                                        _stream(stream)), "fp8q_scaled_gemm_q")
     return (d_out if want_d else None), out
+
+
+def scaled_gemm_mxq(A: QTensor, a_use_col: bool, B: QTensor, b_use_col: bool, fmt: int = E4M3,
+                    want_d: bool = True, out: QTensor | None = None, d_out: torch.Tensor | None = None,
+                    stream=None):
+    """The GEMM with its bf16 output also quantized MXFP8 1x32 row-wise in the
+    epilogue (fp8q_scaled_gemm_mxq): returns (D bf16 or None, QTensor)."""
+    return scaled_gemm_q(A, a_use_col, B, b_use_col, MXFP8_1x32, fmt, want_d, out, d_out, stream)
 
 
 def gemm_set_variant(variant: int):

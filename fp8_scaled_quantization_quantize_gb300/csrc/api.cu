@@ -363,22 +363,30 @@ fp8q_status fp8q_scaled_gemm(const fp8q_tensor* A, int a_use_col, const fp8q_ten
     return launch_gemm(ga, gb, D, out_dtype, M, N, K, (cudaStream_t)stream);
 }
 
-fp8q_status fp8q_scaled_gemm_mxq(const fp8q_tensor* A, int a_use_col, const fp8q_tensor* B, int b_use_col, void* D,
-                                 int fmt, fp8q_tensor* Dq, int64_t M, int64_t N, int64_t K, void* stream) {
+fp8q_status fp8q_scaled_gemm_q(const fp8q_tensor* A, int a_use_col, const fp8q_tensor* B, int b_use_col, void* D,
+                               int out_kind, int fmt, fp8q_tensor* Dq, int64_t M, int64_t N, int64_t K,
+                               void* stream) {
     if (!A || !B || !Dq || !valid_fmt(fmt)) return FP8Q_ERR_ARG;
+    if (out_kind != FP8Q_MXFP8_1x32 && out_kind != FP8Q_BLOCK_1x128) return FP8Q_ERR_UNSUPPORTED;
     if (M < 1 || N < 1 || K < 1) return FP8Q_ERR_SHAPE;
-    if (K % 16 != 0 || N % 32 != 0) return FP8Q_ERR_SHAPE;
+    if (K % 16 != 0 || N % (out_kind == FP8Q_MXFP8_1x32 ? 32 : 16) != 0) return FP8Q_ERR_SHAPE;
     if (!Dq->data_row || !Dq->scale_row || !Dq->counters) return FP8Q_ERR_ARG;
     if (!aligned16(Dq->data_row) || !aligned16(Dq->scale_row) || (D && !aligned16(D))) return FP8Q_ERR_ALIGN;
+    if (((uintptr_t)Dq->counters & 7u) != 0) return FP8Q_ERR_ALIGN;
     GemmOperand ga, gb;
     const fp8q_status v = prepare_operands(A, a_use_col, B, b_use_col, M, N, K, ga, gb);
     if (v != FP8Q_OK) return v;
     Dq->rows = M;
     Dq->cols = N;
     Dq->fmt = fmt;
-    Dq->kind = FP8Q_MXFP8_1x32;
-    return launch_gemm_pair(ga, gb, D, 0, M, N, K, (cudaStream_t)stream, fmt, Dq->data_row, Dq->scale_row,
+    Dq->kind = out_kind;
+    return launch_gemm_pair(ga, gb, D, 0, M, N, K, (cudaStream_t)stream, out_kind, fmt, Dq->data_row, Dq->scale_row,
                             Dq->counters);
+}
+
+fp8q_status fp8q_scaled_gemm_mxq(const fp8q_tensor* A, int a_use_col, const fp8q_tensor* B, int b_use_col, void* D,
+                                 int fmt, fp8q_tensor* Dq, int64_t M, int64_t N, int64_t K, void* stream) {
+    return fp8q_scaled_gemm_q(A, a_use_col, B, b_use_col, D, FP8Q_MXFP8_1x32, fmt, Dq, M, N, K, stream);
 }
 
 fp8q_status fp8q_gemm_set_variant(int variant) {

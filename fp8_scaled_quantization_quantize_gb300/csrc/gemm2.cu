@@ -86,8 +86,9 @@ struct Params2 {
     const float* bsb;
     int64_t Mp, Np;
     uint32_t idesc;
-    // fused MXFP8 row-wise quantization of the bf16 output (QF != 0)
-    uint8_t* qscale;                 // packed 128x4 E8M0 tiles of the [M][N] row copy
+    // fused row-wise quantization of the bf16 output (QF != 0: MXFP8 for
+    // QF 1, 2, 1x128 for QF 3, 4)
+    uint8_t* qscale;                 // MXFP8: packed 128x4 E8M0 tiles; 1x128: fp32 [ceil(N/128)][Mp]
     unsigned long long* qcounters;   // [0] saturated, [2] NaN / Inf elements
     int hasD;                        // also store the bf16 D
     uint64_t wait_ns;                // bounded-wait limit
@@ -317,6 +318,115 @@ __device__ __forceinline__ void store_q(const CUtensorMap* mapQ, uint8_t* stg, u
         else
             *(uint16_t*)dst = (uint16_t)ebytes;
     }
+}
+
+// The exact finite maximum of 128 bf16 (two to a word) and the NaN / Inf
+// count among the first `live` of them: the rare path of store_q128, out of
+// line so that the common path stays compact.
+struct Bf16x128 {
+    uint32_t w[64];
+};
+struct MaxCount {
+    uint32_t m, n;
+};
+__device__ __noinline__ MaxCount exact_max128(Bf16x128 h, int live) {
+    MaxCount r = {0u, 0u};
+    for (int i = 0; i < 128; ++i) {
+        const uint32_t a = (h.w[i / 2] >> (16 * (i & 1))) & 0x7FFFu;
+        if (a < 0x7F80u)
+            r.m = a > r.m ? a : r.m;
+        else if (i < live)
+            ++r.n;
+    }
+    return r;
+}
+
+// 1x128 (along N) quantization of this warp's 32 rows x 128 columns of D as
+// stored in bf16 (RN(v scale), as store_slice2 writes it): per row the amax of
+// the 128 bf16 over the finite ones (NaN / Inf counted), d = RN(amax / fmax)
+// (block_scale: 1 for amax 0), codes sat_rne(x / d) correctly rounded
+// (Markstein's division from RN(1 / d), two lanes, negated; IEEE division for
+// d below 2^-80 or a block holding NaN / Inf) with a NaN keeping its sign --
+// the quantize kernel's 1x128 row path ("2025 FP8 quantized-training guide",
+// sec. 2.2) on these values.  Saturation: d is one correctly rounded division
+// and the next bf16 below the block maximum is at least 2^-8 smaller, so only
+// elements equal to the maximum can exceed fmax; they are counted when the
+// maximum does.  Codes leave through the staging boxes by TMA (uint8 32 x 32
+// boxes, 32-byte swizzle); each row's d goes to the K-block-major scale array
+// at (x0 / 128) Mp + row (rows past M, up to Mp, get the pad 1.0).
+template <int QFMT, int NBOX>
+__device__ __forceinline__ void store_q128(const CUtensorMap* mapQ, uint8_t* stg, uint32_t stg_s, int lane, int x0,
+                                           int y0, const Params2& p, const float* v, float scale, uint32_t& nsat,
+                                           uint32_t& nnf) {
+    static_assert(NBOX >= 4, "a warp's 128 code columns fill four staging boxes");
+    const int r = lane, sw = (r >> 2) & 1;
+    const int64_t row = (int64_t)y0 + r;
+    const bool row_live = row < p.M;
+    const int live = !row_live ? 0 : ((int64_t)x0 + 128 <= p.N ? 128 : (int)(p.N - x0));  // columns inside D
+    uint32_t h[64];
+#pragma unroll
+    for (int i = 0; i < 64; ++i) h[i] = pack_bf16(v[2 * i] * scale, v[2 * i + 1] * scale);
+    uint32_t pm = 0;
+#pragma unroll
+    for (int i = 0; i < 64; ++i) pm = max_u16x2(pm, h[i] & 0x7FFF7FFFu);
+    uint32_t m = max(pm & 0xFFFFu, pm >> 16);
+    const bool nf = m >= 0x7F80u;
+    if (nf) {
+        Bf16x128 hb;
+#pragma unroll
+        for (int i = 0; i < 64; ++i) hb.w[i] = h[i];
+        const MaxCount e = exact_max128(hb, live);
+        m = e.m;
+        nnf += e.n;
+    }
+    if (!row_live) m = 0;
+    const float d = block_scale<QFMT>(__uint_as_float(m << 16));
+    const bool fast = !nf && d >= 0x1p-80f;
+    const float rd = fast ? rcp_rn(d) : 1.0f;
+    const float2 d2 = make_float2(d, d), nr2 = make_float2(-rd, -rd);
+    // only elements equal to the block maximum can saturate
+    const bool may_sat = row_live && fabsf(__fdiv_rn(__uint_as_float(m << 16), d)) > Fmt<QFMT>::fmax;
+    if (may_sat) {
+#pragma unroll
+        for (int i = 0; i < 64; ++i)
+            nsat += (2 * i < live && (h[i] & 0x7FFFu) == m) + (2 * i + 1 < live && ((h[i] >> 16) & 0x7FFFu) == m);
+    }
+    bulk_wait_read();  // the D boxes have left the staging area
+    __syncwarp();
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+        uint32_t c[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t w0 = h[16 * b + 2 * i], w1 = h[16 * b + 2 * i + 1];
+            const float2 a0 = make_float2(__uint_as_float(w0 << 16), __uint_as_float(w0 & 0xFFFF0000u));
+            const float2 a1 = make_float2(__uint_as_float(w1 << 16), __uint_as_float(w1 & 0xFFFF0000u));
+            if (fast) {
+                const float2 y0 = div2_neg(a0, d2, nr2), y1 = div2_neg(a1, d2, nr2);
+                c[i] = cvt4<QFMT>(y0.x, y0.y, y1.x, y1.y) ^ 0x80808080u;
+            } else {
+                c[i] = cvt4<QFMT>(__fdiv_rn(a0.x, d), __fdiv_rn(a0.y, d), __fdiv_rn(a1.x, d), __fdiv_rn(a1.y, d));
+                if (nf) {  // the hardware's NaN code is 0x7F whatever the sign
+                    uint32_t lo = c[i] & 0xFFFFu, hi = c[i] >> 16;
+                    if ((w0 & 0x7FFFu) > 0x7F80u) lo = (lo & ~0xFFu) | ((w0 >> 8) & 0x80u) | 0x7Fu;
+                    if ((w0 & 0x7FFF0000u) > 0x7F800000u) lo = (lo & ~0xFF00u) | ((w0 >> 16) & 0x8000u) | 0x7F00u;
+                    if ((w1 & 0x7FFFu) > 0x7F80u) hi = (hi & ~0xFFu) | ((w1 >> 8) & 0x80u) | 0x7Fu;
+                    if ((w1 & 0x7FFF0000u) > 0x7F800000u) hi = (hi & ~0xFF00u) | ((w1 >> 16) & 0x8000u) | 0x7F00u;
+                    c[i] = lo | (hi << 16);
+                }
+            }
+        }
+        uint8_t* box = stg + b * 1024;
+        *(uint4*)(box + r * 32 + ((0 ^ sw) << 4)) = make_uint4(c[0], c[1], c[2], c[3]);
+        *(uint4*)(box + r * 32 + ((1 ^ sw) << 4)) = make_uint4(c[4], c[5], c[6], c[7]);
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0 && (int64_t)x0 + 32 * b < p.N && (int64_t)y0 < p.M) {
+            tma_store_2d(mapQ, x0 + 32 * b, y0, stg_s + b * 1024);
+            bulk_commit();
+        }
+    }
+    if (row < p.Mp && (int64_t)x0 < p.N) ((float*)p.qscale)[(int64_t)(x0 / 128) * p.Mp + row] = d;
 }
 
 template <int REC, bool OUT_F32, int QF>
@@ -616,9 +726,12 @@ __global__ void __launch_bounds__(Cfg<REC>::THREADS, 1)
                 if (QF == 0 || p.hasD)
                     store_slice2<OUT_F32, EC, C::STG_WARP / 1024>(&tmD, stg, stg_s, lane, (int)col0, (int)row0, (int)p.N,
                                                                   (int)p.M, vf, osc, poll_sf);
-                if constexpr (QF != 0)
+                if constexpr (QF == 1 || QF == 2)
                     store_q<QF - 1, EC, C::STG_WARP / 1024>(&tmQ, stg, stg_s, lane, (int)col0, (int)row0, p, vf, osc,
                                                             q_sat, q_nf, poll_sf);
+                if constexpr (QF == 3 || QF == 4)
+                    store_q128<QF - 3, C::STG_WARP / 1024>(&tmQ, stg, stg_s, lane, (int)col0, (int)row0, p, vf, osc,
+                                                           q_sat, q_nf);
             } else {
                 float2 acc[EC / 2];  // packed pairs: Blackwell's two-lane FMA halves the promotion's instructions
 #pragma unroll
@@ -671,9 +784,12 @@ __global__ void __launch_bounds__(Cfg<REC>::THREADS, 1)
                 if (QF == 0 || p.hasD)
                     store_slice2<OUT_F32, EC, C::STG_WARP / 1024>(&tmD, stg, stg_s, lane, (int)col0, (int)row0, (int)p.N,
                                                                   (int)p.M, reinterpret_cast<const float*>(acc), 1.0f);
-                if constexpr (QF != 0)
+                if constexpr (QF == 1 || QF == 2)
                     store_q<QF - 1, EC, C::STG_WARP / 1024>(&tmQ, stg, stg_s, lane, (int)col0, (int)row0, p,
                                                             reinterpret_cast<const float*>(acc), 1.0f, q_sat, q_nf);
+                if constexpr (QF == 3 || QF == 4)
+                    store_q128<QF - 3, C::STG_WARP / 1024>(&tmQ, stg, stg_s, lane, (int)col0, (int)row0, p,
+                                                           reinterpret_cast<const float*>(acc), 1.0f, q_sat, q_nf);
             }
         }
         if (lane == 0) bulk_wait_all();
@@ -737,17 +853,20 @@ fp8q_status launch2_t(const CUtensorMap* maps, const Params2& p, cudaStream_t s)
 }
 
 template <int REC>
-fp8q_status launch2_rec(CUtensorMap* maps, const Params2& p, void* D, int out_dtype, int qfmt, void* qdata,
-                        cudaStream_t s) {
+fp8q_status launch2_rec(CUtensorMap* maps, const Params2& p, void* D, int out_dtype, int qkind, int qfmt,
+                        void* qdata, cudaStream_t s) {
     const bool f32 = out_dtype == 1;
     if (D != nullptr && !make_map_2d(&maps[2], f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                                      f32 ? 4 : 2, D, p.M, p.N, f32 ? 8 : 16, 32, CU_TENSOR_MAP_SWIZZLE_32B))
         return FP8Q_ERR_CUDA;
-    if (qfmt < 0) return f32 ? launch2_t<REC, true, 0>(maps, p, s) : launch2_t<REC, false, 0>(maps, p, s);
-    // fused MXFP8 output codes: uint8 [M][N] in 32 x 32 boxes (32-byte swizzle)
+    if (qkind < 0) return f32 ? launch2_t<REC, true, 0>(maps, p, s) : launch2_t<REC, false, 0>(maps, p, s);
+    // fused output codes: uint8 [M][N] in 32 x 32 boxes (32-byte swizzle)
     if (f32 || !make_map_2d(&maps[5], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, qdata, p.M, p.N, 32, 32,
                             CU_TENSOR_MAP_SWIZZLE_32B))
         return f32 ? FP8Q_ERR_ARG : FP8Q_ERR_CUDA;
+    if (qkind == FP8Q_BLOCK_1x128)
+        return qfmt == FP8Q_E4M3 ? launch2_t<REC, false, 3 + FP8Q_E4M3>(maps, p, s)
+                                 : launch2_t<REC, false, 3 + FP8Q_E5M2>(maps, p, s);
     return qfmt == FP8Q_E4M3 ? launch2_t<REC, false, 1 + FP8Q_E4M3>(maps, p, s)
                              : launch2_t<REC, false, 1 + FP8Q_E5M2>(maps, p, s);
 }
@@ -764,7 +883,7 @@ fp8q_status read_device_errors2(unsigned int* flags) {
 }
 
 fp8q_status launch_gemm_pair(const GemmOperand& A, const GemmOperand& B, void* D, int out_dtype, int64_t M,
-                             int64_t N, int64_t K, cudaStream_t s, int qfmt, void* qdata, void* qscale,
+                             int64_t N, int64_t K, cudaStream_t s, int qkind, int qfmt, void* qdata, void* qscale,
                              unsigned long long* qcounters) {
     if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return FP8Q_ERR_SHAPE;
     const bool mx = A.kind == FP8Q_MXFP8_1x32;
@@ -781,7 +900,7 @@ fp8q_status launch_gemm_pair(const GemmOperand& A, const GemmOperand& B, void* D
     p.stall = take_stall();
     p.qscale = (uint8_t*)qscale;
     p.qcounters = qcounters;
-    if (qfmt >= 0 && qcounters != nullptr && cudaMemsetAsync(qcounters, 0, 3 * sizeof(unsigned long long), s) != cudaSuccess)
+    if (qkind >= 0 && qcounters != nullptr && cudaMemsetAsync(qcounters, 0, 3 * sizeof(unsigned long long), s) != cudaSuccess)
         return FP8Q_ERR_CUDA;
     p.M = M;
     p.N = N;
@@ -807,7 +926,7 @@ fp8q_status launch_gemm_pair(const GemmOperand& A, const GemmOperand& B, void* D
                          CU_TENSOR_MAP_SWIZZLE_NONE))
             return FP8Q_ERR_CUDA;
         p.idesc = shape | fmts | (1u << 23);
-        return launch2_rec<REC_MX>(maps, p, D, out_dtype, qfmt, qdata, s);
+        return launch2_rec<REC_MX>(maps, p, D, out_dtype, qkind, qfmt, qdata, s);
     }
     maps[3] = maps[0];
     maps[4] = maps[1];
@@ -815,20 +934,20 @@ fp8q_status launch_gemm_pair(const GemmOperand& A, const GemmOperand& B, void* D
     if (pt) {
         p.sa_inv = A.scale_inv;
         p.sb_inv = B.scale_inv;
-        return launch2_rec<REC_PT>(maps, p, D, out_dtype, qfmt, qdata, s);
+        return launch2_rec<REC_PT>(maps, p, D, out_dtype, qkind, qfmt, qdata, s);
     }
     if (pc) {  // the copies' per-row factors, fp32 padded to 128 entries
         if (((uintptr_t)A.scale | (uintptr_t)B.scale) & 15) return FP8Q_ERR_ARG;
         p.bsa = (const float*)A.scale;
         p.bsb = (const float*)B.scale;
-        return launch2_rec<REC_PC>(maps, p, D, out_dtype, qfmt, qdata, s);
+        return launch2_rec<REC_PC>(maps, p, D, out_dtype, qkind, qfmt, qdata, s);
     }
     // blockwise scale rows are fetched by bulk copies: 16-byte aligned bases
     if (((uintptr_t)A.scale | (uintptr_t)B.scale) & 15) return FP8Q_ERR_ARG;
     p.bsa = (const float*)A.scale;
     p.bsb = (const float*)B.scale;
-    if (B.kind == FP8Q_BLOCK_128x128) return launch2_rec<REC_B2D>(maps, p, D, out_dtype, qfmt, qdata, s);
-    return launch2_rec<REC_B1D>(maps, p, D, out_dtype, qfmt, qdata, s);
+    if (B.kind == FP8Q_BLOCK_128x128) return launch2_rec<REC_B2D>(maps, p, D, out_dtype, qkind, qfmt, qdata, s);
+    return launch2_rec<REC_B1D>(maps, p, D, out_dtype, qkind, qfmt, qdata, s);
 }
 
 }  // namespace fp8q

@@ -192,9 +192,7 @@ constexpr bool kNegated = KIND == kB1 || KIND == kB128;
 template <int KIND>
 __device__ __forceinline__ float2 apply2(float2 x, const Factor2& f) {
     if constexpr (kNegated<KIND>) {
-        const float2 nq = __fmul2_rn(x, f.nr);
-        const float2 e = __ffma2_rn(nq, f.k, x);
-        return __ffma2_rn(e, f.nr, nq);
+        return div2_neg(x, f.k, f.nr);
     } else {
         return __fmul2_rn(x, f.k);
     }

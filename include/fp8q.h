@@ -313,6 +313,21 @@ FP8Q_API fp8q_status fp8q_scaled_gemm_mxq(const fp8q_tensor* A, int a_use_col, c
                                  void* stream);
 
 /*
+ * The same fusion for either row-wise recipe the next GEMM takes: out_kind
+ * FP8Q_MXFP8_1x32 (exactly fp8q_scaled_gemm_mxq) or FP8Q_BLOCK_1x128 ([guide]
+ * sec. 2.2: activations and gradients in 1x128 blocks; here blocks of 128
+ * columns of D).  For 1x128, Dq->data_row, Dq->scale_row (fp32
+ * [ceil(N/128)][ceil(M/128) * 128], K-block-major, pads 1.0) and Dq->counters
+ * equal what fp8q_quantize(BLOCK_1x128, fmt, row-wise only) of the bf16 D
+ * writes; N % 16 == 0.  Other kinds: FP8Q_ERR_UNSUPPORTED.  Same buffers,
+ * constraints and kernel otherwise.  No counterpart on the pages (a fusion of
+ * two steps they describe separately).
+ */
+FP8Q_API fp8q_status fp8q_scaled_gemm_q(const fp8q_tensor* A, int a_use_col, const fp8q_tensor* B, int b_use_col,
+                                        void* D, int out_kind, int fmt, fp8q_tensor* Dq, int64_t M, int64_t N,
+                                        int64_t K, void* stream);
+
+/*
  * Chooses the GEMM kernel for subsequent fp8q_scaled_gemm calls (process
  * wide): 0 automatic (default: SM pairs once the problem has at least 64
  * tiles of 256 x 256 and, for blockwise scales, both scale arrays are

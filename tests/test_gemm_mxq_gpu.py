@@ -1,10 +1,12 @@
-"""GEMM with the next quantize fused into its epilogue (fp8q_scaled_gemm_mxq).
+"""GEMM with the next quantize fused into its epilogue (fp8q_scaled_gemm_q,
+fp8q_scaled_gemm_mxq).
 
 The fused output must be exactly what the quantize step would make of the
 GEMM's bf16 output: the oracle quantizes the kernel's own bf16 D with the
-MXFP8 1x32 recipe ("2025 FP8 quantized-training guide", sec. 2.3) and every
-code, packed E8M0 scale byte and counter must match.  D itself is the plain
-SM-pair GEMM's D bit for bit, and without D the quantized output is the same.
+MXFP8 1x32 recipe ("2025 FP8 quantized-training guide", sec. 2.3) or the
+1x128 recipe (sec. 2.2), and every code, scale byte (in the library's
+layout) and counter must match.  D itself is the plain SM-pair GEMM's D bit
+for bit, and without D the quantized output is the same.
 """
 import numpy as np
 import pytest
@@ -40,22 +42,32 @@ def _operands(api, kA, kB, fA, fB, M, N, K, seed):
     return qa, qb
 
 
-def _check_fused(api, qa, qb, fmt, ctx):
-    D, Dq = api.scaled_gemm_mxq(qa, False, qb, False, fmt, want_d=True)
+OUT_KINDS = {"mxfp8": O.MXFP8_1x32, "1x128": O.BLOCK_1x128}
+
+
+def _check_fused(api, qa, qb, fmt, ctx, kind=O.MXFP8_1x32):
+    D, Dq = api.scaled_gemm_q(qa, False, qb, False, kind, fmt, want_d=True)
     torch.cuda.synchronize()
     got = gpu_outputs(Dq)
-    ref = O.quantize(O.MXFP8_1x32, fmt, inputs.bf16_bits(D.cpu()), True, False)
-    assert_quant_equal(O.MXFP8_1x32, got, ref, True, False, ctx)
+    ref = O.quantize(kind, fmt, inputs.bf16_bits(D.cpu()), True, False)
+    assert_quant_equal(kind, got, ref, True, False, ctx)
     return D, Dq, got
 
 
+SHAPES = [(256, 512, 256), (208, 288, 400), (384, 800, 528), (640, 1024, 1040), (208, 272, 400)]
+
+
 @pytest.mark.parametrize("name,kA,kB,fA,fB", RECIPES, ids=[r[0] for r in RECIPES])
-@pytest.mark.parametrize("M,N,K", [(256, 512, 256), (208, 288, 400), (384, 800, 528), (640, 1024, 1040)])
+@pytest.mark.parametrize("M,N,K", SHAPES)
 @pytest.mark.parametrize("fmt", [O.E4M3, O.E5M2])
-def test_fused_output_quantize_matches_quantize_of_d(name, kA, kB, fA, fB, M, N, K, fmt):
+@pytest.mark.parametrize("out_kind", list(OUT_KINDS))
+def test_fused_output_quantize_matches_quantize_of_d(name, kA, kB, fA, fB, M, N, K, fmt, out_kind):
+    kind = OUT_KINDS[out_kind]
+    if kind == O.MXFP8_1x32 and N % 32:
+        pytest.skip("the MXFP8 output takes N % 32 == 0")
     api = _api()
     qa, qb = _operands(api, kA, kB, fA, fB, M, N, K, 60 + M)
-    D, Dq, got = _check_fused(api, qa, qb, fmt, f"{name} {M}x{N}x{K} fmt={fmt}")
+    D, Dq, got = _check_fused(api, qa, qb, fmt, f"{name} {M}x{N}x{K} fmt={fmt} out={out_kind}", kind)
     # D is the plain SM-pair GEMM's D
     api.gemm_set_variant(2)
     try:
@@ -65,7 +77,7 @@ def test_fused_output_quantize_matches_quantize_of_d(name, kA, kB, fA, fB, M, N,
         api.gemm_set_variant(0)
     assert torch.equal(D.view(torch.int16), D2.view(torch.int16)), "fused D differs from the GEMM's D"
     # and without D the quantized output is the same
-    none, Dq2 = api.scaled_gemm_mxq(qa, False, qb, False, fmt, want_d=False)
+    none, Dq2 = api.scaled_gemm_q(qa, False, qb, False, kind, fmt, want_d=False)
     torch.cuda.synchronize()
     assert none is None
     got2 = gpu_outputs(Dq2)
@@ -75,27 +87,47 @@ def test_fused_output_quantize_matches_quantize_of_d(name, kA, kB, fA, fB, M, N,
     assert api.device_errors() == 0
 
 
-def test_fused_output_counts_saturation():
+@pytest.mark.parametrize("out_kind", list(OUT_KINDS))
+def test_fused_output_counts_saturation(out_kind):
     """MXFP8 blocks whose scaled maximum lands in (448, 512) saturate: a
-    typical N(0,1) product has many; the count must equal the oracle's."""
+    typical N(0,1) product has many.  A 1x128 block saturates when d =
+    RN(amax / 448) rounds below amax / 448, so its maximum divides to just
+    above 448.  Both counts must equal the oracle's."""
     api = _api()
     qa, qb = _operands(api, 4, 4, O.E4M3, O.E4M3, 512, 1024, 512, 5)
-    _, _, got = _check_fused(api, qa, qb, O.E4M3, "saturation")
+    _, _, got = _check_fused(api, qa, qb, O.E4M3, "saturation", OUT_KINDS[out_kind])
     assert got["sat_row"] > 0
 
 
-def test_fused_output_of_overflowing_d():
+@pytest.mark.parametrize("out_kind", list(OUT_KINDS))
+def test_fused_output_of_overflowing_d(out_kind):
     """A per-tensor GEMM whose fp32 result overflows: D is +-Inf in bf16, every
     element is counted as nonfinite and encodes to +-448 (satfinite), and the
-    blocks' finite maximum is 0 (E8M0 127)."""
+    blocks' finite maximum is 0 (E8M0 127, 1x128 d = 1)."""
     api = _api()
     M, N, K = 256, 256, 128
     big = torch.full((M, K), 1e30, dtype=torch.bfloat16)
     qa = api.quantize(big.cuda(), 0, O.E4M3, True, False)
     qb = api.quantize(big[:N].clone().cuda(), 0, O.E4M3, True, False)
-    D, Dq, got = _check_fused(api, qa, qb, O.E4M3, "overflow")
+    D, Dq, got = _check_fused(api, qa, qb, O.E4M3, "overflow", OUT_KINDS[out_kind])
     assert torch.isinf(D.float()).all()
     assert got["nonfinite"] == M * N
+
+
+def test_fused_1x128_output_of_d_with_nan_and_tiny_blocks():
+    """1x128 output blocks holding NaN (a NaN operand row), and blocks whose
+    maximum is tiny (d below the reciprocal shortcut's range, IEEE division):
+    codes, scales and counters equal the oracle's quantize of D."""
+    api = _api()
+    M, N, K = 256, 384, 256
+    a = inputs.normal_f32((M, K), 91)
+    a[7, 3] = np.nan
+    a[100:140, :] *= np.float32(2.0 ** -80)   # rows of D near 2^-76: d near 2^-84, the IEEE-division path
+    b = inputs.normal_f32((N, K), 92)
+    qa = api.quantize(inputs.to_bf16(a).cuda(), O.BLOCK_1x128, O.E4M3, True, False)
+    qb = api.quantize(inputs.to_bf16(b).cuda(), O.BLOCK_128x128, O.E4M3, True, False)
+    D, Dq, got = _check_fused(api, qa, qb, O.E4M3, "nan / tiny", O.BLOCK_1x128)
+    assert got["nonfinite"] > 0
 
 
 def test_fused_output_llama8b_fprop_sampled_rows():
@@ -120,4 +152,24 @@ def test_fused_output_llama8b_fprop_sampled_rows():
     r = rows[:, None]
     off = ((r // 128) * tiles_c + k // 4) * 512 + (r % 32) * 16 + ((r % 128) // 32) * 4 + k % 4
     assert np.array_equal(sb[off], ref["scale_row"])
+    assert api.device_errors() == 0
+
+
+def test_fused_1x128_output_llama8b_up_proj_sampled_rows():
+    """The blockwise Llama-3-8B up-projection (X 1x128 [4096x4096] . W^T
+    128x128 [14336x4096]) with the next layer's 1x128 quantize of Y fused:
+    64 sampled rows' codes and fp32 scales (K-block-major [112][4096]) against
+    the oracle's quantize of those rows of the kernel's own bf16 Y."""
+    api = _api()
+    X, W = inputs.llama8b_up_proj()
+    qx = api.quantize(X.cuda(), O.BLOCK_1x128, O.E4M3, True, False)
+    qw = api.quantize(W.cuda(), O.BLOCK_128x128, O.E4M3, True, False)
+    D, Dq = api.scaled_gemm_q(qx, False, qw, False, O.BLOCK_1x128, O.E4M3, want_d=True)
+    torch.cuda.synchronize()
+    rows = np.sort(np.random.default_rng(4).choice(4096, 64, replace=False))
+    idx = torch.as_tensor(rows, device=D.device)
+    ref = O.quantize(O.BLOCK_1x128, O.E4M3, inputs.bf16_bits(D[idx].cpu()), True, False)
+    assert np.array_equal(Dq.data_row[idx].cpu().numpy(), ref["data_row"])
+    sc = Dq.scale_row.cpu().numpy().view(np.float32).reshape(14336 // 128, 4096)
+    assert np.array_equal(sc[:, rows].T, ref["scale_row"])
     assert api.device_errors() == 0
