@@ -431,6 +431,24 @@ def run_ours(args):
     two_ms = _time_ms(two_calls, args.steps, args.warmup, flush)
     launches += 2 * args.steps
 
+    # ---- the bench fprop with the next layer's 1x128 quantize of Y fused into
+    # its epilogue, against the GEMM followed by the quantize kernel on Y
+    qy1 = api.alloc(api.BLOCK_1x128, api.E4M3, T, F, True, False, dev)
+
+    def gemm_then_quantize():
+        api.scaled_gemm(qx, False, qw, False, out=Y, stream=stream)
+        api.quantize_into(Y, qy1, stream=stream)
+
+    def fused_next(with_d):
+        api.scaled_gemm_q(qx, False, qw, False, api.BLOCK_1x128, api.E4M3, want_d=with_d, out=qy1,
+                          d_out=Y if with_d else None, stream=stream)
+
+    bfus = {name: round(_time_ms(fn, args.steps, args.warmup, flush), 4)
+            for name, fn in (("gemm_then_quantize", gemm_then_quantize), ("fused_with_bf16_y", lambda: fused_next(True)),
+                             ("fused_fp8_only", lambda: fused_next(False)))}
+    launches += 4 * args.steps
+    errs |= api.device_errors()
+
     # ---- scaling granularity at the bench shape ("mastering FP8 LLM training
     # 1.5x speedup", Figure 1: per-tensor fastest, per-channel between, 2D
     # blocks slowest): the fprop GEMM with each, and the per-channel quantize
@@ -463,8 +481,7 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "fp8e4m3 x fp8e4m3 -> fp32 accumulate (quantize in fp32)",
         "data": "synthetic (seeded N(0,1) with 1% outlier columns x100; W N(0,0.02^2))",
-        "config": {"workload": WORKLOAD, "M": T, "N": F, "K": H, "recipe": "blockwise 1x128 / 128x128",
-                   "l2": "flushed (512 MiB write) before every timed step", "parallelism": f"replicas x{world}"},
+        "config": bench_config(world),
         "gemm_tflops": round(gemm_tflops, 1),
         "quantize_gbs": round(qbytes / q_avg / 1e6, 1),
         "quantize_frac_of_hbm": round(qbytes / q_avg / 1e6 / hbm_peak, 3),
@@ -473,7 +490,7 @@ def run_ours(args):
                      "achieved": round(gemm_tflops, 1), "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
                      "frac": round(gemm_tflops / fp8_peak, 3),
                      "peak_source": f"{peak_kind} bf16 burst x2 (dense FP8 / BF16 nominal ratio)",
-                     "traffic": measured_traffic("gemm2_blockwise_llama8b_up_proj.md", GEMM2_SOURCES),
+                     "traffic": measured_traffic("gemm2_blockwise_llama8b_up_proj.json", GEMM2_SOURCES),
                      "traffic_algorithmic": round(T * H + F * H + 2 * T * F + 4 * (T * H / 128 + F * H / 16384))},
         "e2e": {"value": round(whole_job_tflops(flops, e2e_step_ms, world), 1), "unit": UNIT,
                 "h2d_bytes_per_step": X.numel() * 2 + W.numel() * 2,
@@ -487,10 +504,14 @@ def run_ours(args):
         "clocks": clocks,
         "device_errors": errs,
         "mxfp8": mx,
+        "blockwise_fprop_next_quantize_ms": bfus,
         "granularity": granularity,
     }
     if rank == 0 and not args.skip_cpu:
-        line["cpu_baseline"] = cpu_baseline(args.cpu_budget)
+        # every host core on the whole quantize and a GEMM sample; one core on
+        # a row sample of the quantize and a GEMM sample
+        line["cpu_baseline"] = cpu_baseline(args.cpu_budget, 0)
+        line["cpu_baseline"]["single_core"] = cpu_baseline(args.cpu_budget / 2, 1, 128, 1024)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -499,25 +520,30 @@ def run_ours(args):
 
 
 def measured_traffic(profile: str, sources) -> float | None:
-    """dram read + write bytes per launch recorded in a profile summary, or
-    None once the kernel's sources have changed since that capture."""
-    import hashlib
+    """dram read + write bytes per launch recorded with an ncu profile
+    (profiles/<name>.json: traffic_bytes_per_launch, sources_sha256), or None
+    once the kernel's sources have changed since that capture."""
     try:
-        text = open(os.path.join(ROOT, "profiles", profile)).read()
-        rec = dict(line.split(": ", 1) for line in text.splitlines()
-                   if line.startswith(("traffic_bytes_per_launch: ", "sources_sha256: ")))
-        h = hashlib.sha256()
-        for src in sources:
-            with open(os.path.join(ROOT, "fp8_scaled_quantization_quantize_gb300", "csrc", src), "rb") as f:
-                h.update(f.read())
-        if h.hexdigest() != rec["sources_sha256"].strip():
+        with open(os.path.join(ROOT, "profiles", profile)) as f:
+            rec = json.load(f)
+        if sources_sha256(sources) != rec["sources_sha256"]:
             return None
         return float(rec["traffic_bytes_per_launch"])
     except Exception:
         return None
 
 
-GEMM2_SOURCES = ("gemm2.cu", "umma.cuh", "ptx.cuh", "fp8q_internal.cuh")
+def sources_sha256(sources) -> str:
+    """The hash measured_traffic compares (the kernel's sources in order)."""
+    import hashlib
+    h = hashlib.sha256()
+    for src in sources:
+        with open(os.path.join(ROOT, "fp8_scaled_quantization_quantize_gb300", "csrc", src), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+GEMM2_SOURCES = ("gemm2.cu", "umma.cuh", "ptx.cuh", "fp8q_internal.cuh", "per_device.h")
 
 
 def gemm_kernel_name(M, N, recipe, out="bf16"):
@@ -711,56 +737,101 @@ def run_modes(args):
 
 # -------------------------------------------------------------- oracle arm
 
-def cpu_baseline(budget_s: float = 15.0) -> dict:
-    """The oracle timed on a bounded sample of the step, extrapolated to the
-    full step: quantize 128 rows of X (1x128, both copies) and 1024 rows of W
-    (128x128, both copies), and fprop GEMM output points until the budget."""
+def host_cores() -> int:
+    """Host cores this process may run on (the affinity mask, else the count)."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+_HOST_BITS = None
+
+
+def _host_bits():
+    """The step's X and W as bf16 bit patterns in host memory (drawn once)."""
+    global _HOST_BITS
+    if _HOST_BITS is None:
+        from fp8_scaled_quantization_quantize_gb300 import inputs
+        Xh, Wh = inputs.llama8b_up_proj(T, H, F)
+        _HOST_BITS = (inputs.bf16_bits(Xh), inputs.bf16_bits(Wh))
+    return _HOST_BITS
+
+
+def cpu_baseline(budget_s: float = 10.0, threads: int = 0, x_rows: int = T, w_rows: int = F) -> dict:
+    """The oracle (plain C, OpenMP over independent blocks and output points)
+    timed on `threads` host cores (0: all of them) on the step: quantize the
+    first x_rows rows of X (1x128) and w_rows rows of W (128x128), both
+    copies (the whole tensors by default), then fprop GEMM output points,
+    doubling their number until the budget is spent; the step's time is
+    extrapolated from the per-element and per-point times."""
     import numpy as np
 
     import oracle as O
-    from fp8_scaled_quantization_quantize_gb300 import inputs
 
-    Xh, Wh = inputs.llama8b_up_proj(T, H, F)
-    xb, wb = inputs.bf16_bits(Xh), inputs.bf16_bits(Wh)
+    cores = O.set_threads(threads if threads > 0 else host_cores())
+    xb, wb = _host_bits()
     t0 = time.perf_counter()
-    qx = O.quantize(O.BLOCK_1x128, O.E4M3, xb[:128], True, True)
+    qx = O.quantize(O.BLOCK_1x128, O.E4M3, xb[:x_rows], True, True)
     t1 = time.perf_counter()
-    qw = O.quantize(O.BLOCK_128x128, O.E4M3, wb[:128 * 8], True, True)
+    qw = O.quantize(O.BLOCK_128x128, O.E4M3, wb[:w_rows], True, True)
     t2 = time.perf_counter()
-    per_x = (t1 - t0) / (128 * H)
-    per_w = (t2 - t1) / (128 * 8 * H)
+    per_x = (t1 - t0) / (x_rows * H)
+    per_w = (t2 - t1) / (w_rows * H)
     A, sA = qx["data_row"], qx["scale_row"]
     B, sB = qw["data_row"], qw["scale_row"]
-    n, pts, tg = 256, 0, 0.0
+    n, pts, tg = 256 * cores, 0, 0.0
     while True:
-        pm = np.zeros(n, dtype=np.int64)
+        pm = np.arange(n, dtype=np.int64) // B.shape[0] % A.shape[0]
         pn = np.arange(n, dtype=np.int64) % B.shape[0]
         g0 = time.perf_counter()
         O.gemm_points(A, O.E4M3, sA, 1, 128, B, O.E4M3, sB, 128, 128, pm, pn)
-        tg += time.perf_counter() - g0
+        dt = time.perf_counter() - g0
+        tg += dt
         pts += n
-        if tg + (t2 - t0) > budget_s or n >= 1 << 16:
+        # stop when the next, twice as large, chunk would overrun the budget
+        if tg + (t2 - t0) + 2 * dt > budget_s or n >= 1 << 22:
             break
         n *= 2
     per_point = tg / pts
     full_s = per_x * T * H + per_w * F * H + per_point * T * F
-    return {"value": round(2.0 * T * F * H / full_s / 1e12, 6), "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"quantize 128 rows of X and 1024 rows of W, {pts} GEMM output points (K={H}); "
-                      f"extrapolated to the full step ({full_s:.1f} s)"}
+    quant = ("all of X and W" if (x_rows, w_rows) == (T, F) else f"{x_rows} rows of X and {w_rows} rows of W")
+    return {"value": round(2.0 * T * F * H / full_s / 1e12, 6), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"quantize {quant} (both copies), {pts} fprop GEMM output points (K={H}) on {cores} "
+                      f"thread(s); extrapolated to the full step ({full_s:.1f} s)",
+            "seconds": round(time.perf_counter() - t0, 2), "full_step_s": round(full_s, 2)}
+
+
+def bench_config(world: int) -> dict:
+    """The `config` of both arms' lines."""
+    return {"workload": WORKLOAD, "M": T, "N": F, "K": H, "recipe": "blockwise 1x128 / 128x128",
+            "l2": "flushed (512 MiB write) before every timed step", "parallelism": f"replicas x{world}"}
 
 
 def run_reference(args):
+    """The reference arm: the oracle on every host core, each step a bounded
+    sample of the step (quantize 512 rows of X and 2048 rows of W, then GEMM
+    output points for the rest of the step's budget), extrapolated."""
     if int(os.environ.get("RANK", "0")) != 0:
         return
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    budget = min(5.0, max(0.5, 90.0 / max(1, args.steps + args.warmup)))
+    _host_bits()
     for _ in range(args.warmup):
-        cpu_baseline(min(2.0, args.cpu_budget))
-    vals = [cpu_baseline(args.cpu_budget / max(1, args.steps)) for _ in range(args.steps)]
+        cpu_baseline(budget, 0, 512, 2048)
+    vals, walls = [], []
+    for _ in range(args.steps):
+        w0 = time.perf_counter()
+        vals.append(cpu_baseline(budget, 0, 512, 2048))
+        walls.append(time.perf_counter() - w0)
     v = statistics.mean(x["value"] for x in vals)
-    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT,
-            "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps, "warmup": args.warmup,
+    cores = vals[-1]["cores"]
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * statistics.mean(walls), 1),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
-            "data": "synthetic", "config": {"workload": WORKLOAD, "M": T, "N": F, "K": H},
-            "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": vals[-1]["sample"]},
+            "data": "synthetic (the same seeded X and W)", "config": bench_config(world),
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": vals[-1]["sample"] + "; ms_per_step is the sample's wall time"},
             "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -773,7 +844,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--skip-mx", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
-    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--mode", choices=["step", "quantize", "gemm", "sweep", "qerror", "delayed70b", "multi"],
                     default="step",
                     help="step: the benchmark line (default); quantize / gemm: one kernel; sweep: roofline sweep; "

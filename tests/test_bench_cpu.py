@@ -37,10 +37,11 @@ def test_profile_traffic_follows_the_kernel_sources(tmp_path, monkeypatch):
     prof = tmp_path / "profiles"
     prof.mkdir()
     digest = hashlib.sha256(b"// kernel v1\n").hexdigest()
-    (prof / "p.md").write_text(f"# p\n\ntraffic_bytes_per_launch: 12345\nsources_sha256: {digest}\n")
+    (prof / "p.json").write_text(json.dumps({"traffic_bytes_per_launch": 12345, "sources_sha256": digest}))
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
-    assert bench.measured_traffic("p.md", ("k.cu",)) == 12345.0
+    assert bench.sources_sha256(("k.cu",)) == digest
+    assert bench.measured_traffic("p.json", ("k.cu",)) == 12345.0
     (src / "k.cu").write_text("// kernel v2\n")
-    assert bench.measured_traffic("p.md", ("k.cu",)) is None
-    assert bench.measured_traffic("missing.md", ("k.cu",)) is None
+    assert bench.measured_traffic("p.json", ("k.cu",)) is None
+    assert bench.measured_traffic("missing.json", ("k.cu",)) is None
 
