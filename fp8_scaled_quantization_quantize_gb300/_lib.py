@@ -12,7 +12,7 @@ OK, ERR_ARG, ERR_SHAPE, ERR_ALIGN, ERR_DTYPE, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIM
 # fp8q_format
 E4M3, E5M2 = 0, 1
 # fp8q_recipe_kind
-PERTENSOR_CURRENT, PERTENSOR_DELAYED, BLOCK_1x128, BLOCK_128x128, MXFP8_1x32, PERCHANNEL_CURRENT = range(6)
+PERTENSOR_CURRENT, PERTENSOR_DELAYED, BLOCK_1x128, BLOCK_128x128, MXFP8_1x32, PERCHANNEL_CURRENT, BLOCK_GENERIC = range(7)
 
 EXPORTS = ("fp8q_version", "fp8q_status_str", "fp8q_scale_bytes", "fp8q_quantize", "fp8q_delayed_create",
            "fp8q_delayed_update", "fp8q_delayed_get", "fp8q_delayed_set", "fp8q_delayed_history_len",
@@ -24,14 +24,15 @@ MULTI_MAX = 16  # FP8Q_MULTI_MAX
 
 class Recipe(ctypes.Structure):
     _fields_ = [("kind", ctypes.c_int), ("fmt", ctypes.c_int), ("want_rowwise", ctypes.c_int),
-                ("want_colwise", ctypes.c_int)]
+                ("want_colwise", ctypes.c_int), ("block_rows", ctypes.c_int), ("block_cols", ctypes.c_int)]
 
 
 class Tensor(ctypes.Structure):
     _fields_ = [("data_row", ctypes.c_void_p), ("data_col", ctypes.c_void_p), ("scale_row", ctypes.c_void_p),
                 ("scale_col", ctypes.c_void_p), ("amax", ctypes.c_void_p), ("scale", ctypes.c_void_p),
                 ("scale_inv", ctypes.c_void_p), ("counters", ctypes.c_void_p), ("rows", ctypes.c_int64),
-                ("cols", ctypes.c_int64), ("fmt", ctypes.c_int), ("kind", ctypes.c_int)]
+                ("cols", ctypes.c_int64), ("fmt", ctypes.c_int), ("kind", ctypes.c_int),
+                ("block_rows", ctypes.c_int), ("block_cols", ctypes.c_int)]
 
 
 class QuantizeJob(ctypes.Structure):

@@ -12,8 +12,8 @@ from dataclasses import dataclass
 import torch
 
 from . import _lib as L
-from ._lib import (BLOCK_1x128, BLOCK_128x128, E4M3, E5M2, MXFP8_1x32, PERCHANNEL_CURRENT, PERTENSOR_CURRENT,  # noqa: F401
-                   PERTENSOR_DELAYED, Fp8qError)
+from ._lib import (BLOCK_1x128, BLOCK_128x128, BLOCK_GENERIC, E4M3, E5M2, MXFP8_1x32, PERCHANNEL_CURRENT,  # noqa: F401
+                   PERTENSOR_CURRENT, PERTENSOR_DELAYED, Fp8qError)
 
 
 def _stream(stream) -> int:
@@ -59,9 +59,11 @@ def _check_input(x: torch.Tensor, qt: QTensor, name: str = "x", any_rows: bool =
     _check_device(x, qt.counters, name)
 
 
-def scale_bytes(kind: int, rows: int, cols: int, rowwise: bool, colwise: bool):
+def scale_bytes(kind: int, rows: int, cols: int, rowwise: bool, colwise: bool, block=(0, 0)):
+    """Bytes of the scale buffers (fp8q_scale_bytes); block = (rows, cols) of a
+    BLOCK_GENERIC recipe's blocks."""
     rb, cb = ctypes.c_size_t(0), ctypes.c_size_t(0)
-    rc = L.Recipe(kind, E4M3, int(rowwise), int(colwise))
+    rc = L.Recipe(kind, E4M3, int(rowwise), int(colwise), *block)
     L.check(L.load().fp8q_scale_bytes(ctypes.byref(rc), rows, cols, ctypes.byref(rb), ctypes.byref(cb)),
             "fp8q_scale_bytes")
     return rb.value, cb.value
@@ -82,11 +84,15 @@ class QTensor:
     scale: torch.Tensor              # fp32[1]
     scale_inv: torch.Tensor          # fp32[1]
     counters: torch.Tensor           # int64[3]: sat_row, sat_col, nonfinite
+    block: tuple = (0, 0)            # BLOCK_GENERIC: (block rows, block cols)
 
     def c_struct(self) -> L.Tensor:
         return L.Tensor(_ptr(self.data_row), _ptr(self.data_col), _ptr(self.scale_row), _ptr(self.scale_col),
                         _ptr(self.amax), _ptr(self.scale), _ptr(self.scale_inv), _ptr(self.counters),
-                        self.rows, self.cols, self.fmt, self.kind)
+                        self.rows, self.cols, self.fmt, self.kind, *self.block)
+
+    def recipe(self) -> L.Recipe:
+        return L.Recipe(self.kind, self.fmt, int(self.rowwise), int(self.colwise), *self.block)
 
     @property
     def rowwise(self) -> bool:
@@ -120,13 +126,18 @@ def row_block(qt: QTensor, r0: int, r1: int) -> QTensor:
         sr = qt.scale_row[r0 * 4:(-(-r1 // 128)) * 128 * 4]
     elif qt.kind not in (PERTENSOR_CURRENT, PERTENSOR_DELAYED):
         raise ValueError("row_block: the 1x128 scale layout is not row-contiguous")
+    if qt.kind == BLOCK_GENERIC:
+        raise ValueError("row_block: generic block scales are not taken apart by rows")
     return QTensor(qt.kind, qt.fmt, r1 - r0, C, qt.data_row[r0:r1], None, sr, None,
                    qt.amax, qt.scale, qt.scale_inv, qt.counters)
 
 
 def alloc(kind: int, fmt: int, rows: int, cols: int, rowwise: bool = True, colwise: bool = False,
-          device="cuda") -> QTensor:
-    rb, cb = scale_bytes(kind, rows, cols, rowwise, colwise)
+          device="cuda", block=(0, 0)) -> QTensor:
+    """Device buffers for one quantize call; block = (rows, cols) of the
+    blocks of a BLOCK_GENERIC recipe (1 x b or b x b, b in 32, 64, 128, 256)."""
+    block = tuple(int(v) for v in block) if kind == BLOCK_GENERIC else (0, 0)
+    rb, cb = scale_bytes(kind, rows, cols, rowwise, colwise, block)
     u8 = dict(dtype=torch.uint8, device=device)
     f32 = dict(dtype=torch.float32, device=device)
     return QTensor(kind, fmt, rows, cols,
@@ -135,7 +146,7 @@ def alloc(kind: int, fmt: int, rows: int, cols: int, rowwise: bool = True, colwi
                    torch.empty(max(rb, 16), **u8) if rowwise and rb else None,
                    torch.empty(max(cb, 16), **u8) if colwise and cb else None,
                    torch.zeros(1, **f32), torch.ones(1, **f32), torch.ones(1, **f32),
-                   torch.zeros(3, dtype=torch.int64, device=device))
+                   torch.zeros(3, dtype=torch.int64, device=device), block)
 
 
 class DelayedState:
@@ -184,7 +195,7 @@ class DelayedState:
 def quantize_into(x: torch.Tensor, qt: QTensor, state: DelayedState | None = None, stream=None) -> QTensor:
     """Quantizes bf16 x [rows, cols] into preallocated qt (same kind / fmt / copies)."""
     _check_input(x, qt)
-    rc = L.Recipe(qt.kind, qt.fmt, int(qt.rowwise), int(qt.colwise))
+    rc = qt.recipe()
     ct = qt.c_struct()
     L.check(L.load().fp8q_quantize(ctypes.byref(rc), _ptr(x), x.shape[0], x.shape[1],
                                    state.handle if state is not None else None, ctypes.byref(ct), _stream(stream)),
@@ -196,7 +207,7 @@ def quantize_rows_into(x_block: torch.Tensor, qt: QTensor, row0: int, stream=Non
     """Quantizes rows row0 .. row0 + len(x_block) - 1 of the tensor whose
     buffers qt holds (fp8q_quantize_rows); qt.counters are added to."""
     _check_input(x_block, qt, "x_block", any_rows=True)
-    rc = L.Recipe(qt.kind, qt.fmt, int(qt.rowwise), int(qt.colwise))
+    rc = qt.recipe()
     ct = qt.c_struct()
     L.check(L.load().fp8q_quantize_rows(ctypes.byref(rc), _ptr(x_block), row0, x_block.shape[0], qt.rows,
                                         x_block.shape[1], ctypes.byref(ct), _stream(stream)), "fp8q_quantize_rows")
@@ -216,7 +227,7 @@ def quantize_multi(jobs, stream=None):
         _check_input(x, qt, f"x of job {i}")
         ct = qt.c_struct()
         keep.append(ct)
-        arr[i].recipe = L.Recipe(qt.kind, qt.fmt, int(qt.rowwise), int(qt.colwise))
+        arr[i].recipe = qt.recipe()
         arr[i].x = x.data_ptr()
         arr[i].rows, arr[i].cols = x.shape[0], x.shape[1]
         arr[i].state = state.handle if state is not None else None
@@ -226,8 +237,8 @@ def quantize_multi(jobs, stream=None):
 
 
 def quantize(x: torch.Tensor, kind: int, fmt: int = E4M3, rowwise: bool = True, colwise: bool = False,
-             state: DelayedState | None = None, stream=None) -> QTensor:
-    qt = alloc(kind, fmt, x.shape[0], x.shape[1], rowwise, colwise, device=x.device)
+             state: DelayedState | None = None, stream=None, block=(0, 0)) -> QTensor:
+    qt = alloc(kind, fmt, x.shape[0], x.shape[1], rowwise, colwise, device=x.device, block=block)
     return quantize_into(x, qt, state, stream)
 
 

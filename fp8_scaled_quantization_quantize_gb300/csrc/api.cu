@@ -46,25 +46,48 @@ bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
 bool valid_fmt(int f) { return f == FP8Q_E4M3 || f == FP8Q_E5M2; }
 
-bool valid_kind(int k) { return k >= FP8Q_PERTENSOR_CURRENT && k <= FP8Q_PERCHANNEL_CURRENT; }
+bool valid_kind(int k) { return k >= FP8Q_PERTENSOR_CURRENT && k <= FP8Q_BLOCK_GENERIC; }
+
+// Block shapes of the generic kind: 1 x b or b x b, b in {32, 64, 128, 256}.
+bool valid_generic(int br, int bc) {
+    return (bc == 32 || bc == 64 || bc == 128 || bc == 256) && (br == 1 || br == bc);
+}
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 bool is_pertensor(int k) { return k == FP8Q_PERTENSOR_CURRENT || k == FP8Q_PERTENSOR_DELAYED; }
 
+// A blockwise copy as (block rows, block cols): 1x128 / 128x128 kinds and
+// the generic kind's shape; (0, 0) for other kinds.
+void block_shape(const fp8q_tensor* t, int& br, int& bc) {
+    br = bc = 0;
+    if (t->kind == FP8Q_BLOCK_1x128) br = 1, bc = 128;
+    if (t->kind == FP8Q_BLOCK_128x128) br = bc = 128;
+    if (t->kind == FP8Q_BLOCK_GENERIC) br = t->block_rows, bc = t->block_cols;
+}
+
 // Recipe pairs of the scaled GEMM: both per-tensor (current / delayed in any
-// mix), both MXFP8, both per-channel, or A 1x128 with B 1x128 or 128x128.
-bool gemm_kinds_ok(int ka, int kb) {
+// mix), both MXFP8, both per-channel, or blockwise A of 1 x b blocks with B of
+// 1 x b or b x b blocks (b the same: the K block of the promotion).
+bool gemm_kinds_ok(const fp8q_tensor* A, const fp8q_tensor* B) {
+    const int ka = A->kind, kb = B->kind;
     if (is_pertensor(ka) || is_pertensor(kb)) return is_pertensor(ka) && is_pertensor(kb);
     if (ka == FP8Q_MXFP8_1x32 || kb == FP8Q_MXFP8_1x32 || ka == FP8Q_PERCHANNEL_CURRENT ||
         kb == FP8Q_PERCHANNEL_CURRENT)
         return ka == kb;
-    return ka == FP8Q_BLOCK_1x128 && (kb == FP8Q_BLOCK_1x128 || kb == FP8Q_BLOCK_128x128);
+    int abr, abc, bbr, bbc;
+    block_shape(A, abr, abc);
+    block_shape(B, bbr, bbc);
+    return abr == 1 && abc > 0 && bbc == abc && (bbr == 1 || bbr == bbc);
 }
 
-// Scale bytes of one copy with logical shape [R][C] (blocks along C).
-size_t copy_scale_bytes(int kind, int64_t R, int64_t C) {
+// Scale bytes of one copy with logical shape [R][C] (blocks along C; br x bc
+// blocks for the generic kind).
+size_t copy_scale_bytes(int kind, int64_t R, int64_t C, int br = 0, int bc = 0) {
     switch (kind) {
+        case FP8Q_BLOCK_GENERIC:
+            if (br == 1) return (size_t)(cdiv(C, bc) * cdiv(R, 128) * 128) * sizeof(float);
+            return (size_t)(cdiv(R, br) * cdiv(C, bc)) * sizeof(float);
         case FP8Q_BLOCK_1x128:
             return (size_t)(cdiv(C, 128) * cdiv(R, 128) * 128) * sizeof(float);
         case FP8Q_BLOCK_128x128:
@@ -84,6 +107,8 @@ fp8q_status prepare_quantize(const fp8q_recipe* rc, const void* x, int64_t rows,
                              const fp8q_delayed_state* st, const fp8q_tensor* out, QuantArgs& a) {
     if (!rc || !out) return FP8Q_ERR_ARG;
     if (!valid_kind(rc->kind) || !valid_fmt(rc->fmt)) return FP8Q_ERR_ARG;
+    if (rc->kind == FP8Q_BLOCK_GENERIC && !valid_generic(rc->block_rows, rc->block_cols))
+        return FP8Q_ERR_UNSUPPORTED;
     const bool row = rc->want_rowwise != 0, col = rc->want_colwise != 0;
     if (!row && !col) return FP8Q_ERR_ARG;
     if (rows < 0 || cols < 0) return FP8Q_ERR_SHAPE;
@@ -132,6 +157,8 @@ fp8q_status prepare_quantize(const fp8q_recipe* rc, const void* x, int64_t rows,
     a.R_total = rows;
     a.tiles_r_total = a.tiles_r;
     a.wait_ns = wait_limit_ns();
+    a.br = rc->kind == FP8Q_BLOCK_GENERIC ? rc->block_rows : 0;
+    a.bc = rc->kind == FP8Q_BLOCK_GENERIC ? rc->block_cols : 0;
     return FP8Q_OK;
 }
 
@@ -145,7 +172,7 @@ fp8q_status prepare_operands(const fp8q_tensor* A, int a_use_col, const fp8q_ten
     const int64_t am = a_use_col ? A->cols : A->rows, ak = a_use_col ? A->rows : A->cols;
     const int64_t bn = b_use_col ? B->cols : B->rows, bk = b_use_col ? B->rows : B->cols;
     if (am != M || ak != K || bn != N || bk != K) return FP8Q_ERR_SHAPE;
-    if (!gemm_kinds_ok(A->kind, B->kind)) return FP8Q_ERR_DTYPE;
+    if (!gemm_kinds_ok(A, B)) return FP8Q_ERR_DTYPE;
     const bool pt = is_pertensor(A->kind);
     ga.data = (const uint8_t*)(a_use_col ? A->data_col : A->data_row);
     ga.scale = a_use_col ? A->scale_col : A->scale_row;
@@ -159,6 +186,16 @@ fp8q_status prepare_operands(const fp8q_tensor* A, int a_use_col, const fp8q_ten
     gb.rows = N;
     gb.kind = B->kind;
     gb.fmt = B->fmt;
+    // blockwise operands by block shape: the specialised kinds and the
+    // generic 1 x 128 / 128 x 128 shapes are the same GEMM
+    int abr, abc, bbr, bbc;
+    block_shape(A, abr, abc);
+    block_shape(B, bbr, bbc);
+    ga.kblock = gb.kblock = abc;
+    if (abc > 0) {
+        ga.kind = FP8Q_BLOCK_1x128;
+        gb.kind = bbr == 1 ? FP8Q_BLOCK_1x128 : FP8Q_BLOCK_128x128;
+    }
     if (!ga.data || !gb.data) return FP8Q_ERR_ARG;
     if (pt ? !ga.scale_inv || !gb.scale_inv : !ga.scale || !gb.scale) return FP8Q_ERR_ARG;
     if (!aligned16(ga.data) || !aligned16(gb.data)) return FP8Q_ERR_ALIGN;
@@ -178,6 +215,8 @@ void set_meta(const fp8q_recipe* rc, int64_t rows, int64_t cols, fp8q_tensor* ou
     out->cols = cols;
     out->fmt = rc->fmt;
     out->kind = rc->kind;
+    out->block_rows = rc->kind == FP8Q_BLOCK_GENERIC ? rc->block_rows : 0;
+    out->block_cols = rc->kind == FP8Q_BLOCK_GENERIC ? rc->block_cols : 0;
 }
 
 }  // namespace
@@ -204,9 +243,12 @@ const char* fp8q_status_str(fp8q_status s) {
 fp8q_status fp8q_scale_bytes(const fp8q_recipe* rc, int64_t rows, int64_t cols, size_t* row_bytes,
                              size_t* col_bytes) {
     if (!rc || !valid_kind(rc->kind)) return FP8Q_ERR_ARG;
+    if (rc->kind == FP8Q_BLOCK_GENERIC && !valid_generic(rc->block_rows, rc->block_cols))
+        return FP8Q_ERR_UNSUPPORTED;
     if (rows < 0 || cols < 0) return FP8Q_ERR_SHAPE;
-    if (row_bytes) *row_bytes = rc->want_rowwise ? copy_scale_bytes(rc->kind, rows, cols) : 0;
-    if (col_bytes) *col_bytes = rc->want_colwise ? copy_scale_bytes(rc->kind, cols, rows) : 0;
+    const int br = rc->block_rows, bc = rc->block_cols;
+    if (row_bytes) *row_bytes = rc->want_rowwise ? copy_scale_bytes(rc->kind, rows, cols, br, bc) : 0;
+    if (col_bytes) *col_bytes = rc->want_colwise ? copy_scale_bytes(rc->kind, cols, rows, br, bc) : 0;
     return FP8Q_OK;
 }
 
@@ -222,8 +264,9 @@ fp8q_status fp8q_quantize(const fp8q_recipe* rc, const void* x, int64_t rows, in
 fp8q_status fp8q_quantize_rows(const fp8q_recipe* rc, const void* x, int64_t row0, int64_t rows, int64_t total_rows,
                                int64_t cols, fp8q_tensor* out, void* stream) {
     if (!rc || !out) return FP8Q_ERR_ARG;
-    if (is_pertensor(rc->kind) || (rc->kind == FP8Q_PERCHANNEL_CURRENT && rc->want_colwise))
-        return FP8Q_ERR_DTYPE;  // their scales need the whole tensor (or whole columns)
+    if (is_pertensor(rc->kind) || (rc->kind == FP8Q_PERCHANNEL_CURRENT && rc->want_colwise) ||
+        rc->kind == FP8Q_BLOCK_GENERIC)
+        return FP8Q_ERR_DTYPE;  // their scales need the whole tensor (or whole columns / other row groups)
     if (row0 < 0 || rows < 0 || total_rows < 0 || row0 + rows > total_rows) return FP8Q_ERR_SHAPE;
     if (row0 % 128 != 0 || (rows % 128 != 0 && row0 + rows != total_rows)) return FP8Q_ERR_SHAPE;
     if (rc->want_colwise && total_rows % 16 != 0) return FP8Q_ERR_SHAPE;

@@ -440,7 +440,8 @@ fp8q_status launch_gemm(const GemmOperand& A, const GemmOperand& B, void* D, int
         A.kind != FP8Q_BLOCK_1x128 || ((((uintptr_t)A.scale) | ((uintptr_t)B.scale)) & 15) == 0;
     const int64_t pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
     // per-channel scales only on SM pairs
-    if (A.kind == FP8Q_PERCHANNEL_CURRENT || g_gemm_variant == 2 ||
+    // per-channel scales and K blocks other than 128 only on SM pairs
+    if (A.kind == FP8Q_PERCHANNEL_CURRENT || (A.kblock != 0 && A.kblock != 128) || g_gemm_variant == 2 ||
         (g_gemm_variant == 0 && scales_aligned && pair_tiles >= 64))
         return launch_gemm_pair(A, B, D, out_dtype, M, N, K, s);
     CUtensorMap ma, mb;

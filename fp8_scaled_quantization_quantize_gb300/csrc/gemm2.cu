@@ -80,6 +80,7 @@ constexpr uint32_t SF_TMEM_COL = 256;
 struct Params2 {
     int64_t M, N, K;
     int64_t tiles_m2, tiles_n, nkb, tiles_m128, nbn128;
+    int64_t nkbq, nbnq;              // blockwise: K blocks of the scales (KB wide), B's KB-row blocks
     const float* sa_inv;
     const float* sb_inv;
     const float* bsa;
@@ -429,7 +430,12 @@ __device__ __forceinline__ void store_q128(const CUtensorMap* mapQ, uint8_t* stg
     if (row < p.Mp && (int64_t)x0 < p.N) ((float*)p.qscale)[(int64_t)(x0 / 128) * p.Mp + row] = d;
 }
 
-template <int REC, bool OUT_F32, int QF>
+// KB (blockwise recipes): the K block of the scales, i.e. of the partial sums
+// the epilogue promotes -- 128 for the 1x128 / 128x128 recipes, 32, 64 or 256
+// for the generic sub-channel blocks ("mastering FP8 LLM training 1.5x
+// speedup", scaling strategy 3).  A 128-wide pipeline stage then holds
+// 128 / KB partials (KB <= 128) or half of one (KB = 256).
+template <int REC, bool OUT_F32, int QF, int KB = 128>
 __global__ void __launch_bounds__(Cfg<REC>::THREADS, 1)
     gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmSFA,
@@ -526,24 +532,35 @@ __global__ void __launch_bounds__(Cfg<REC>::THREADS, 1)
                                         sfl(s));
                     }
                     if constexpr (C::BLOCKWISE) {
-                        const uint32_t r = kbp % C::SR;
-                        if (!mbar_wait2(sempty(r), ((kbp / C::SR) & 1u) ^ 1u, abort_flag, p.wait_ns)) {
-                            ok = false;
-                            break;
+                        // the scales of each K block (partial) that starts in this stage
+                        constexpr int PPS = KB <= 128 ? 128 / KB : 1;
+#pragma unroll
+                        for (int i = 0; i < PPS; ++i) {
+                            if (KB > 128 && (kb & 1)) break;  // a 256-wide block started in the previous stage
+                            const int64_t kq = KB > 128 ? kb / 2 : kb * PPS + i;
+                            if (kq >= p.nkbq) break;
+                            const uint32_t r = kbp % C::SR;
+                            if (!mbar_wait2(sempty(r), ((kbp / C::SR) & 1u) ^ 1u, abort_flag, p.wait_ns)) {
+                                ok = false;
+                                break;
+                            }
+                            const uint32_t dst = sb + C::OFF_SCL + r * C::SLOT;
+                            // 1 x KB B scales of the tile's columns that exist (Np is a multiple of 128)
+                            const uint32_t bbytes =
+                                (p.Np - nb * BN >= BN) ? 4u * BN : 4u * (uint32_t)(p.Np - nb * BN);
+                            mbar_expect_tx(sfull(r), (arow ? 512u : 0u) + (REC == REC_B1D ? bbytes : 0u));
+                            if (arow) bulk_load(dst, p.bsa + kq * p.Mp + rs, 512, sfull(r));
+                            if (REC == REC_B1D) bulk_load(dst + 512, p.bsb + kq * p.Np + nb * BN, bbytes, sfull(r));
+                            if (REC == REC_B2D) {  // the scales of the tile's KB-row B blocks (BN / KB, at least one)
+                                const int64_t b0 = (nb * BN) / KB;
+#pragma unroll
+                                for (int t = 0; t < (BN >= KB ? BN / KB : 1); ++t)
+                                    if (b0 + t < p.nbnq) cp_async_4(dst + 512 + 4 * t, p.bsb + (b0 + t) * p.nkbq + kq);
+                                cp_async_arrive(sfull(r));
+                            }
+                            ++kbp;
                         }
-                        const uint32_t dst = sb + C::OFF_SCL + r * C::SLOT;
-                        // 1x128 B scales of the tile's columns that exist (Np is a multiple of 128)
-                        const uint32_t bbytes = (p.Np - nb * BN >= BN) ? 4u * BN : 4u * (uint32_t)(p.Np - nb * BN);
-                        mbar_expect_tx(sfull(r), (arow ? 512u : 0u) + (REC == REC_B1D ? bbytes : 0u));
-                        if (arow) bulk_load(dst, p.bsa + kb * p.Mp + rs, 512, sfull(r));
-                        if (REC == REC_B1D) bulk_load(dst + 512, p.bsb + kb * p.Np + nb * BN, bbytes, sfull(r));
-                        if (REC == REC_B2D) {  // the scales of the (at most two) 128-column B blocks of the tile
-                            const int64_t b0 = (nb * BN) / 128;
-                            cp_async_4(dst + 512, p.bsb + b0 * p.nkb + kb);
-                            if (b0 + 1 < p.nbn128) cp_async_4(dst + 516, p.bsb + (b0 + 1) * p.nkb + kb);
-                            cp_async_arrive(sfull(r));
-                        }
-                        ++kbp;
+                        if (!ok) break;
                     }
                     if (++s == STAGES) {
                         s = 0;
@@ -567,7 +584,7 @@ __global__ void __launch_bounds__(Cfg<REC>::THREADS, 1)
                 }
                 for (int64_t kb = 0; kb < p.nkb; ++kb) {
                     uint32_t dcol = (REC == REC_PT || REC == REC_PC) ? abuf * BN : 0;
-                    if (REC == REC_B2D || REC == REC_B1D) {
+                    if ((REC == REC_B2D || REC == REC_B1D) && KB == 128) {
                         const uint32_t buf = kbg % NACC;
                         if (!mbar_wait2(tempty(buf), ((kbg / NACC) & 1u) ^ 1u, abort_flag, p.wait_ns)) {
                             ok = false;
@@ -590,6 +607,32 @@ __global__ void __launch_bounds__(Cfg<REC>::THREADS, 1)
                             mma2_mx(tmem, desc_sw128(a0 + 32 * k), desc_sw128(b0 + 32 * k), idesc, sft, sft + 4,
                                     (kb > 0 || k > 0) ? 1u : 0u);
                         }
+                    } else if ((REC == REC_B2D || REC == REC_B1D) && KB != 128) {
+                        // K blocks of KB: each partial takes a free TMEM buffer before its
+                        // first MMA and is handed to the epilogue after its last
+                        constexpr int MPB = KB / 32;  // MMAs of K = 32 per partial
+#pragma unroll
+                        for (int k = 0; k < BK / 32; ++k) {
+                            const int64_t kq = KB > 128 ? kb / 2 : (kb * BK + 32 * k) / KB;  // this MMA's partial
+                            if (kq >= p.nkbq) break;
+                            const bool first = KB > 128 ? ((kb & 1) == 0 && k == 0) : (k % MPB == 0);
+                            const bool last = KB > 128 ? (((kb & 1) == 1 || kb + 1 == p.nkb) && k == BK / 32 - 1)
+                                                       : (k % MPB == MPB - 1);
+                            if (first) {
+                                if (!mbar_wait2(tempty(kbg % NACC), ((kbg / NACC) & 1u) ^ 1u, abort_flag, p.wait_ns)) {
+                                    ok = false;
+                                    break;
+                                }
+                                tc_fence_after();
+                            }
+                            mma2_f8(tmem + (kbg % NACC) * BN, desc_sw128(a0 + 32 * k), desc_sw128(b0 + 32 * k), p.idesc,
+                                    first ? 0u : 1u);
+                            if (last) {
+                                tc2_commit_both(tfull(kbg % NACC));
+                                ++kbg;
+                            }
+                        }
+                        if (!ok) break;
                     } else {
 #pragma unroll
                         for (int k = 0; k < BK / 32; ++k) {
@@ -599,7 +642,7 @@ __global__ void __launch_bounds__(Cfg<REC>::THREADS, 1)
                         }
                     }
                     tc2_commit_both(empty(s));
-                    if (REC == REC_B2D || REC == REC_B1D) {
+                    if ((REC == REC_B2D || REC == REC_B1D) && KB == 128) {
                         tc2_commit_both(tfull(kbg % NACC));
                         ++kbg;
                     }
@@ -737,7 +780,7 @@ __global__ void __launch_bounds__(Cfg<REC>::THREADS, 1)
 #pragma unroll
                 for (int i = 0; i < EC / 2; ++i) acc[i] = make_float2(0.0f, 0.0f);
                 bool ok = true;
-                for (int64_t kb = 0; kb < p.nkb; ++kb, ++kbg) {
+                for (int64_t kb = 0; kb < p.nkbq; ++kb, ++kbg) {
                     const uint32_t r = kbg % C::SR;
                     if (!mbar_wait2(sfull(r), (kbg / C::SR) & 1u, abort_flag, p.wait_ns)) {
                         ok = false;
@@ -745,9 +788,9 @@ __global__ void __launch_bounds__(Cfg<REC>::THREADS, 1)
                     }
                     const float* scl = (const float*)(smem + C::OFF_SCL + r * C::SLOT);
                     const float sa = scl[32 * q + lane];
-                    // this warp's EC columns lie in one 128-column B block (tiles start on
-                    // 256-column boundaries)
-                    const float sc = (REC == REC_B2D) ? __fmul_rn(sa, scl[128 + (int)((nb * BN + EC * j) / 128 - (nb * BN) / 128)]) : 0.0f;
+                    // KB >= 128: this warp's EC columns lie in one KB-row B block (tiles
+                    // start on 256-column boundaries); smaller KB: one per chunk, below
+                    const float sc = (REC == REC_B2D && KB >= 128) ? __fmul_rn(sa, scl[128 + (EC * j) / KB]) : 0.0f;
                     const uint32_t buf = kbg % NACC;
                     if (!mbar_wait2(tfull(buf), (kbg / NACC) & 1u, abort_flag, p.wait_ns)) {
                         ok = false;
@@ -761,7 +804,8 @@ __global__ void __launch_bounds__(Cfg<REC>::THREADS, 1)
                         FP8Q_LD16_PAIRS(tmem + lane_base + buf * BN + tcol + 16 * c, v);
                         if (c == EC / 16 - 1) release(buf);
                         if (REC == REC_B2D) {
-                            const float2 sc2 = make_float2(sc, sc);
+                            const float scc = KB >= 128 ? sc : __fmul_rn(sa, scl[128 + (EC * j + 16 * c) / KB]);
+                            const float2 sc2 = make_float2(scc, scc);
 #pragma unroll
                             for (int i = 0; i < 8; ++i) acc[8 * c + i] = __ffma2_rn(u64_as_float2(v[i]), sc2, acc[8 * c + i]);
                         } else {
@@ -814,10 +858,10 @@ __global__ void __launch_bounds__(Cfg<REC>::THREADS, 1)
     }
 }
 
-template <int REC, bool F32, int QF>
+template <int REC, bool F32, int QF, int KB = 128>
 fp8q_status launch2_t(const CUtensorMap* maps, const Params2& p, cudaStream_t s) {
     using C = Cfg<REC>;
-    auto kern = gemm2_kernel<REC, F32, QF>;
+    auto kern = gemm2_kernel<REC, F32, QF, KB>;
     static PerDevice<bool> attr;
     if (!smem_opt_in(attr, kern, C::SMEM)) return FP8Q_ERR_CUDA;
     const int sms = sm_count();
@@ -908,6 +952,8 @@ fp8q_status launch_gemm_pair(const GemmOperand& A, const GemmOperand& B, void* D
     p.tiles_m2 = (M + 255) / 256;
     p.tiles_n = (N + bn - 1) / bn;
     p.nkb = (K + BK - 1) / BK;
+    p.nkbq = p.nkb;
+    p.nbnq = (N + 127) / 128;
     p.tiles_m128 = (M + 127) / 128;
     p.nbn128 = (N + 127) / 128;
     p.Mp = p.tiles_m128 * 128;
@@ -946,8 +992,33 @@ fp8q_status launch_gemm_pair(const GemmOperand& A, const GemmOperand& B, void* D
     if (((uintptr_t)A.scale | (uintptr_t)B.scale) & 15) return FP8Q_ERR_ARG;
     p.bsa = (const float*)A.scale;
     p.bsb = (const float*)B.scale;
-    if (B.kind == FP8Q_BLOCK_128x128) return launch2_rec<REC_B2D>(maps, p, D, out_dtype, qkind, qfmt, qdata, s);
-    return launch2_rec<REC_B1D>(maps, p, D, out_dtype, qkind, qfmt, qdata, s);
+    const int kbs = A.kblock;  // the scales' K block: 128, or a generic 32, 64, 256
+    p.nkbq = (K + kbs - 1) / kbs;
+    p.nbnq = (N + kbs - 1) / kbs;
+    if (p.Mp * p.nkbq >= ((int64_t)1 << 31) || p.Np * p.nkbq >= ((int64_t)1 << 31)) return FP8Q_ERR_SHAPE;
+    const bool b2 = B.kind == FP8Q_BLOCK_128x128;
+    if (kbs == 128)
+        return b2 ? launch2_rec<REC_B2D>(maps, p, D, out_dtype, qkind, qfmt, qdata, s)
+                  : launch2_rec<REC_B1D>(maps, p, D, out_dtype, qkind, qfmt, qdata, s);
+    if (qkind >= 0) return FP8Q_ERR_UNSUPPORTED;  // the fused output quantize takes 128-wide K blocks
+    if (D == nullptr) return FP8Q_ERR_ARG;
+    const bool f32 = out_dtype == 1;
+    if (!make_map_2d(&maps[2], f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, f32 ? 4 : 2,
+                     D, p.M, p.N, f32 ? 8 : 16, 32, CU_TENSOR_MAP_SWIZZLE_32B))
+        return FP8Q_ERR_CUDA;
+    switch (kbs * 2 + (b2 ? 1 : 0)) {
+#define FP8Q_KB_CASE(KBV)                                                                                     \
+    case KBV * 2 + 1:                                                                                         \
+        return f32 ? launch2_t<REC_B2D, true, 0, KBV>(maps, p, s) : launch2_t<REC_B2D, false, 0, KBV>(maps, p, s); \
+    case KBV * 2:                                                                                             \
+        return f32 ? launch2_t<REC_B1D, true, 0, KBV>(maps, p, s) : launch2_t<REC_B1D, false, 0, KBV>(maps, p, s);
+        FP8Q_KB_CASE(32)
+        FP8Q_KB_CASE(64)
+        FP8Q_KB_CASE(256)
+#undef FP8Q_KB_CASE
+        default:
+            return FP8Q_ERR_UNSUPPORTED;
+    }
 }
 
 }  // namespace fp8q

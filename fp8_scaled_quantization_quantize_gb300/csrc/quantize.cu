@@ -76,7 +76,7 @@ __device__ __forceinline__ uint32_t nan_sign2(uint32_t q, uint32_t w) {
 // Scaled value of one element for the recipe's scale rule.
 template <int KIND>
 __device__ __forceinline__ float scaled(float x, float k) {
-    if constexpr (KIND == kB1 || KIND == kB128)
+    if constexpr (KIND == kB1 || KIND == kB128 || KIND == kGen)
         return __fdiv_rn(x, k);  // blockwise: x / d
     else
         return __fmul_rn(x, k);  // per-tensor x * s, MXFP8 x * 2^-e (exact)
@@ -126,7 +126,7 @@ template <int KIND>
 __device__ __forceinline__ Factor make_factor(float k) {
     Factor f;
     f.k = k;
-    if constexpr (KIND == kB1 || KIND == kB128) {
+    if constexpr (KIND == kB1 || KIND == kB128 || KIND == kGen) {
         f.r = k >= 0x1p-80f ? rcp_rn(k) : 0.0f;  // the reciprocal serves the shortcut only
         f.fast = k >= 0x1p-80f;  // keeps the residual below exact in fp32
     } else {
@@ -158,7 +158,7 @@ __device__ __forceinline__ float div_rn_recip(float x, float d, float r) {
 // is in the reciprocal shortcut's range; the caller branches once per block).
 template <int KIND, bool FAST = true>
 __device__ __forceinline__ float apply(float x, const Factor& f) {
-    if constexpr (KIND == kB1 || KIND == kB128) {
+    if constexpr (KIND == kB1 || KIND == kB128 || KIND == kGen) {
         if constexpr (FAST)
             return div_rn_recip(x, f.k, f.r);
         else
@@ -188,7 +188,7 @@ __device__ __forceinline__ float2 bf16x2_f32(uint32_t w) { return make_float2(bf
 // flipped (kNegated) are the codes of RN(x / d) with the sign of a zero kept.
 // Other recipes: the product.
 template <int KIND>
-constexpr bool kNegated = KIND == kB1 || KIND == kB128;
+constexpr bool kNegated = KIND == kB1 || KIND == kB128 || KIND == kGen;
 template <int KIND>
 __device__ __forceinline__ float2 apply2(float2 x, const Factor2& f) {
     if constexpr (kNegated<KIND>) {
@@ -217,7 +217,7 @@ __device__ __forceinline__ uint2 convert8_packed(const uint4& v, const Factor2& 
     const float2 y2 = apply2<KIND>(bf16x2_f32(v.z), f), y3 = apply2<KIND>(bf16x2_f32(v.w), f);
     // blockwise scales almost never saturate (a uniform, untaken branch);
     // MXFP8 and per-tensor blocks often can: count without branching
-    if (KIND != kB1 && KIND != kB128 || count)
+    if (KIND != kB1 && KIND != kB128 && KIND != kGen || count)
         nsat += sat2<FMT>(y0, count, count) + sat2<FMT>(y1, count, count) + sat2<FMT>(y2, count, count) +
                 sat2<FMT>(y3, count, count);
     return make_uint2(cvt4_applied<KIND, FMT>(y0.x, y0.y, y1.x, y1.y), cvt4_applied<KIND, FMT>(y2.x, y2.y, y3.x, y3.y));
@@ -393,14 +393,16 @@ __device__ __noinline__ ColCodes col_codes_rare(Col32 c, float k0, float k1) {
     return out;
 }
 
-template <int KIND, int FMT, bool ROW, bool COL>
+// GSQ (generic blocks only): the blocks are square (b x b), else 1 x b; the
+// block width b is a.bc, read at run time.
+template <int KIND, int FMT, bool ROW, bool COL, bool GSQ = false>
 __global__ void __launch_bounds__(kThreads, 2)
     quant_tile_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmrow,
                       const __grid_constant__ CUtensorMap tmcol, QuantArgs a) {
     constexpr bool kPerTensor = (KIND == kCur || KIND == kDel);
     // the column copy of a recipe whose scale does not depend on the copy's
     // direction is the byte transpose of the row codes
-    constexpr bool kTranspose = COL && (kPerTensor || KIND == kB128);
+    constexpr bool kTranspose = COL && (kPerTensor || KIND == kB128 || (KIND == kGen && GSQ));
     constexpr bool kRowCodes = ROW || kTranspose;
     extern __shared__ uint8_t qsmem_raw[];
     uint8_t* qsmem = (uint8_t*)(((uintptr_t)qsmem_raw + 1023) & ~(uintptr_t)1023);
@@ -481,7 +483,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                                           max_u16x2(vec_pmax(v[6]), vec_pmax(v[7])));
             mh[0] = fold16(p0);
             mh[1] = fold16(p1);
-            if constexpr (KIND == kMX) {
+            if (KIND == kMX || (KIND == kGen && a.bc == 32)) {
                 mq[0] = fold16(p0);
                 mq[1] = fold16(p1);
                 if (mq[0] >= 0x7F80u || mq[1] >= 0x7F80u) {
@@ -547,6 +549,33 @@ __global__ void __launch_bounds__(kThreads, 2)
                 mq[0] = mq[1] = m;
                 kq[0] = kq[1] = pertensor_scale<FMT>(__uint_as_float(m << 16));
             }
+        } else if constexpr (KIND == kGen) {
+            // the blocks' maxima over all of x (the amax pass left them in the
+            // scale buffers as bf16 magnitude bits); rows and columns past x read 0
+            if constexpr (kRowCodes) {
+                const int64_t rg = r0g + rr, cf = c0 + 64 * hh;  // row; first column of this half
+                const int bc = a.bc;
+                const int64_t nbc = (a.C + bc - 1) / bc;
+                uint32_t m2[2] = {0u, 0u};
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    const int64_t cc = cf + 32 * i;
+                    if (rg < a.R_total && cc < a.C && (i == 0 || bc == 32)) {
+                        const int64_t bj = cc / bc;
+                        if constexpr (GSQ) {
+                            const int64_t nbr = (a.R_total + bc - 1) / bc, bi = rg / bc;
+                            m2[i] = ROW ? ((const uint32_t*)a.s_row)[bi * nbc + bj] : ((const uint32_t*)a.s_col)[bj * nbr + bi];
+                        } else {
+                            m2[i] = ((const uint32_t*)a.s_row)[bj * (a.tiles_r_total * kTile) + rg];
+                        }
+                    }
+                }
+                if (bc != 32) m2[1] = m2[0];
+                mq[0] = m2[0];
+                mq[1] = m2[1];
+                kq[0] = block_scale<FMT>(__uint_as_float(m2[0] << 16));
+                kq[1] = block_scale<FMT>(__uint_as_float(m2[1] << 16));
+            }
         } else if constexpr (KIND == kMX) {
             const int e0 = mx_exponent<FMT>(mq[0] << 16), e1 = mx_exponent<FMT>(mq[1] << 16);
             kq[0] = exp2_neg(e0);
@@ -563,20 +592,21 @@ __global__ void __launch_bounds__(kThreads, 2)
         uint2 q[8];
         uint32_t nsat_rc = 0;
         if constexpr (kRowCodes) {
+            const bool two = KIND == kMX || (KIND == kGen && a.bc == 32);  // two blocks in this half row
             const Factor f0 = make_factor<KIND>(kq[0]);
-            const Factor f1 = (KIND == kMX) ? make_factor<KIND>(kq[1]) : f0;
+            const Factor f1 = two ? make_factor<KIND>(kq[1]) : f0;
             const bool s0 = may_saturate<KIND, FMT>(mq[0], f0);
-            const bool s1 = (KIND == kMX) ? may_saturate<KIND, FMT>(mq[1], f1) : s0;
+            const bool s1 = two ? may_saturate<KIND, FMT>(mq[1], f1) : s0;
             if (vnf == 0 && f0.fast && f1.fast) {  // the common case: one straight-line block
                 const Factor2 g0 = pair_factor(f0, f0), g1 = pair_factor(f1, f1);
-                constexpr bool kAtMax = KIND == kCur || KIND == kB1 || KIND == kB128 || KIND == kPC;
+                constexpr bool kAtMax = KIND == kCur || KIND == kB1 || KIND == kB128 || KIND == kPC || KIND == kGen;
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
                     q[j] = convert8_packed<KIND, FMT>(v[j], (j < 4) ? g0 : g1, nsat_rc,
                                                       kAtMax ? false : ((j < 4) ? s0 : s1));
-                if (kAtMax && s0) {  // only elements equal to the block maximum can saturate
-                    if (mh[0] == mq[0]) nsat_rc += count_at_max<0, 4>(v, mq[0]);
-                    if (mh[1] == mq[0]) nsat_rc += count_at_max<4, 8>(v, mq[0]);
+                if (kAtMax) {  // only elements equal to the block maximum can saturate
+                    if (s0 && mh[0] == mq[0]) nsat_rc += count_at_max<0, 4>(v, mq[0]);
+                    if (s1 && mh[1] == mq[1]) nsat_rc += count_at_max<4, 8>(v, mq[1]);
                 }
             } else {
                 Row8 r;
@@ -648,6 +678,18 @@ __global__ void __launch_bounds__(kThreads, 2)
                     const int cr = 2 * p;
                     tileb[(cr & 31) * 16 + (cr >> 5) * 4 + qd] = (uint8_t)(e0 + 127);
                     tileb[((cr + 1) & 31) * 16 + ((cr + 1) >> 5) * 4 + qd] = (uint8_t)(e1 + 127);
+                } else if constexpr (KIND == kGen) {
+                    // blocks of bc rows of one column (1 x bc blocks of x^T): their maxima
+                    // from the amax pass, in s_col [ceil(R/bc)][Cp]; rows past x read 0
+                    const int64_t rq = r0g + 32 * qd;
+                    m0 = m1 = 0u;
+                    if (rq < a.R_total) {
+                        const uint32_t* sc = (const uint32_t*)a.s_col + (rq / a.bc) * (a.tiles_c * kTile) + cc;
+                        m0 = sc[0];
+                        m1 = sc[1];
+                    }
+                    k0 = block_scale<FMT>(__uint_as_float(m0 << 16));
+                    k1 = block_scale<FMT>(__uint_as_float(m1 << 16));
                 } else if constexpr (KIND == kPC) {
                     // the columns' maxima over all of x (from the amax pass, in s_col)
                     m0 = ((const uint32_t*)a.s_col)[cc];
@@ -683,13 +725,13 @@ __global__ void __launch_bounds__(kThreads, 2)
                 for (int j = 0; j < 32; j += 4) {
                     const float2 y0 = apply2<KIND>(bf16x2_f32(w[j]), g), y1 = apply2<KIND>(bf16x2_f32(w[j + 1]), g);
                     const float2 y2 = apply2<KIND>(bf16x2_f32(w[j + 2]), g), y3 = apply2<KIND>(bf16x2_f32(w[j + 3]), g);
-                    if (KIND != kB1 && KIND != kPC)
+                    if (KIND != kB1 && KIND != kPC && KIND != kGen)
                         ns += sat2<FMT>(y0, c0s, c1s) + sat2<FMT>(y1, c0s, c1s) + sat2<FMT>(y2, c0s, c1s) +
                               sat2<FMT>(y3, c0s, c1s);
                     o0[j / 4] = cvt4_applied<KIND, FMT>(y0.x, y1.x, y2.x, y3.x);
                     o1[j / 4] = cvt4_applied<KIND, FMT>(y0.y, y1.y, y2.y, y3.y);
                 }
-                if ((KIND == kB1 || KIND == kPC) && ((c0s && own0 == m0) || (c1s && own1 == m1))) {
+                if ((KIND == kB1 || KIND == kPC || KIND == kGen) && ((c0s && own0 == m0) || (c1s && own1 == m1))) {
                     // only elements equal to the block maximum can saturate (count_at_max),
                     // looked for in the 8-row groups whose maximum it is
 #pragma unroll
@@ -768,7 +810,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (lane == 0) {
         if (nsat_row) atomicAdd(&a.counters[0], (unsigned long long)nsat_row);
         if (nsat_col) atomicAdd(&a.counters[1], (unsigned long long)nsat_col);
-        if (KIND != kCur && KIND != kPC && nnf) atomicAdd(&a.counters[2], (unsigned long long)nnf);  // else the amax pass
+        if (KIND != kCur && KIND != kPC && KIND != kGen && nnf)
+            atomicAdd(&a.counters[2], (unsigned long long)nnf);  // else the amax pass
     }
     if constexpr (KIND == kDel) {
         tmax_all = warp_max_u32(tmax_all);
@@ -873,6 +916,107 @@ __global__ void __launch_bounds__(256) pc_amax_kernel(const uint16_t* x, int64_t
     }
     nf = warp_sum_u32(nf);
     if (lane == 0 && nf) atomicAdd(&counters[2], (unsigned long long)nf);
+}
+
+// Generic blockwise scaling (1 x b or b x b blocks, b = bc), pass 1: the
+// largest finite |x| of every block, as bf16 magnitude bits in uint32 words of
+// the zeroed scale buffers (atomicMax merges the strips), at the position the
+// block's scale takes: 1 x b blocks in the row copy's [ceil(C/b)][Rp] and, for
+// the column copy, the blocks of b rows of one column in [ceil(R/b)][Cp];
+// b x b blocks in the row copy's [ceil(R/b)][ceil(C/b)], or without a row
+// copy at the transposed position of the column copy's buffer.  NaN / Inf
+// counted.  A CTA takes strips of 64 rows x 256 columns: warp w rows 8w ..
+// 8w + 7, lane l columns 8l .. 8l + 7 (one 16-byte load a row); the bc / 8
+// lanes of a block column meet by shuffles, the warps of a block of rows of
+// one column through shared memory.
+template <bool SQ, bool ROW, bool COL>
+__global__ void __launch_bounds__(256) gen_amax_kernel(const uint16_t* x, int64_t R, int64_t C, int bc,
+                                                       uint32_t* srow, uint32_t* scol,
+                                                       unsigned long long* counters) {
+    __shared__ uint32_t cred[8][128];  // per warp: column-pair maxima of its 8 rows
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int lg = bc / 8 < 32 ? bc / 8 : 32;  // lanes per block column
+    const int64_t strips_c = (C + 255) / 256, strips = ((R + 63) / 64) * strips_c;
+    const int64_t Rp = (R + 127) / 128 * 128, Cp = (C + 127) / 128 * 128;
+    const int64_t nbc = (C + bc - 1) / bc, nbr = (R + bc - 1) / bc;
+    uint32_t nf = 0;
+    for (int64_t sidx = blockIdx.x; sidx < strips; sidx += gridDim.x) {
+        const int64_t rs = (sidx / strips_c) * 64, r0 = rs + 8 * warp, cs = (sidx % strips_c) * 256, c = cs + 8 * lane;
+        uint4 v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)  // C % 8 == 0: a vector is wholly inside or outside
+            v[i] = (c < C && r0 + i < R) ? ld_nc_v4(x + (r0 + i) * C + c) : make_uint4(0u, 0u, 0u, 0u);
+        uint32_t cm[4] = {0u, 0u, 0u, 0u};
+        uint32_t sq = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+            uint32_t rm = 0;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const uint32_t f = finite_mag2(w[k]);
+                nf += nonfinite2(w[k]);
+                cm[k] = max_u16x2(cm[k], f);
+                rm = max_u16x2(rm, f);
+            }
+            uint32_t m = fold16(rm);
+            if constexpr (!SQ && ROW) {
+                for (int o = 1; o < lg; o <<= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+                if (lane % lg == 0 && m != 0u && r0 + i < R && c < C) atomicMax(srow + (c / bc) * Rp + r0 + i, m);
+            }
+            sq = max(sq, m);
+        }
+        if constexpr (SQ) {  // the warp's 8 rows lie in one block row (b >= 32)
+            for (int o = 1; o < lg; o <<= 1) sq = max(sq, __shfl_xor_sync(0xFFFFFFFFu, sq, o));
+            if (lane % lg == 0 && sq != 0u && c < C) {
+                const int64_t bi = r0 / bc, bj = c / bc;
+                if (ROW)
+                    atomicMax(srow + bi * nbc + bj, sq);
+                else
+                    atomicMax(scol + bj * nbr + bi, sq);
+            }
+        }
+        if constexpr (!SQ && COL) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) cred[warp][4 * lane + k] = cm[k];
+            __syncthreads();
+            if (threadIdx.x < 128) {
+                // the warps of one block of b rows: all eight (b >= 64; strips start
+                // at multiples of 64) or four (b = 32)
+                const int g = bc >= 64 ? 8 : 4;
+                for (int g0 = 0; g0 < 8; g0 += g) {
+                    uint32_t m = 0;
+                    for (int w = g0; w < g0 + g; ++w) m = max_u16x2(m, cred[w][threadIdx.x]);
+                    const int64_t cc = cs + 2 * threadIdx.x, rb = (rs + 8 * g0) / bc;
+                    if (cc < C && rs + 8 * g0 < R) {
+                        if (m & 0xFFFFu) atomicMax(scol + rb * Cp + cc, m & 0xFFFFu);
+                        if (m >> 16) atomicMax(scol + rb * Cp + cc + 1, m >> 16);
+                    }
+                }
+            }
+            __syncthreads();  // cred is rewritten by the next strip
+        }
+    }
+    nf = warp_sum_u32(nf);
+    if (lane == 0 && nf) atomicAdd(&counters[2], (unsigned long long)nf);
+}
+
+// Generic blockwise scaling, last pass: each entry of a scale buffer (a
+// block's amax bits; 0 in pad entries) becomes d = RN(amax / fmax), amax 0 -> 1.
+template <int FMT>
+__global__ void gen_finalize_kernel(uint32_t* m, int64_t n) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+        ((float*)m)[i] = block_scale<FMT>(__uint_as_float(m[i] << 16));
+}
+
+// Square blocks with both copies: the column copy's scales are the row copy's
+// transposed, d of the amax bits [nbr][nbc] into [nbc][nbr] (run before the row
+// buffer is finalized in place).
+template <int FMT>
+__global__ void gen_transpose_scales_kernel(const uint32_t* rowm, float* cold, int64_t nbr, int64_t nbc) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nbr * nbc;
+         i += (int64_t)gridDim.x * blockDim.x)
+        cold[(i % nbc) * nbr + i / nbc] = block_scale<FMT>(__uint_as_float(rowm[i] << 16));
 }
 
 // Per-channel current scaling, last pass: each entry of a scale buffer (a
@@ -983,12 +1127,12 @@ int num_sms() {
     return n > 0 ? n : 1;
 }
 
-template <int KIND, int FMT, bool ROW, bool COL>
+template <int KIND, int FMT, bool ROW, bool COL, bool GSQ = false>
 fp8q_status launch_tile(const QuantArgs& args, cudaStream_t s) {
     QuantArgs a = args;
     a.stall = take_stall();
     static PerDevice<bool> attr;
-    auto kern = quant_tile_kernel<KIND, FMT, ROW, COL>;
+    auto kern = quant_tile_kernel<KIND, FMT, ROW, COL, GSQ>;
     if (!smem_opt_in(attr, kern, kTileSmem)) return FP8Q_ERR_CUDA;
     const int64_t ntiles = a.tiles_r * a.tiles_c;
     if (a.tiles_r_total * a.tiles_c >= ((int64_t)1 << 31)) return FP8Q_ERR_SHAPE;  // tiles counted in 32 bits
@@ -1016,17 +1160,74 @@ fp8q_status launch_tile(const QuantArgs& args, cudaStream_t s) {
     return cudaGetLastError() == cudaSuccess ? FP8Q_OK : FP8Q_ERR_CUDA;
 }
 
-template <int KIND, int FMT>
+template <int KIND, int FMT, bool GSQ = false>
 fp8q_status launch_tile_rc(const QuantArgs& a, bool row, bool col, cudaStream_t s) {
-    if (row && col) return launch_tile<KIND, FMT, true, true>(a, s);
-    if (row) return launch_tile<KIND, FMT, true, false>(a, s);
-    return launch_tile<KIND, FMT, false, true>(a, s);
+    if (row && col) return launch_tile<KIND, FMT, true, true, GSQ>(a, s);
+    if (row) return launch_tile<KIND, FMT, true, false, GSQ>(a, s);
+    return launch_tile<KIND, FMT, false, true, GSQ>(a, s);
 }
 
-template <int KIND>
+template <int KIND, bool GSQ = false>
 fp8q_status launch_tile_fmt(const QuantArgs& a, int fmt, bool row, bool col, cudaStream_t s) {
-    return fmt == FP8Q_E4M3 ? launch_tile_rc<KIND, FP8Q_E4M3>(a, row, col, s)
-                            : launch_tile_rc<KIND, FP8Q_E5M2>(a, row, col, s);
+    return fmt == FP8Q_E4M3 ? launch_tile_rc<KIND, FP8Q_E4M3, GSQ>(a, row, col, s)
+                            : launch_tile_rc<KIND, FP8Q_E5M2, GSQ>(a, row, col, s);
+}
+
+// Generic blockwise scaling of shapes other than 1 x 128 / 128 x 128: zero the
+// scale buffers, the block-amax pass into them, the tile pass (reads them),
+// then the buffers' amax bits become d (for square blocks with both copies the
+// column copy's scales are the row copy's transposed).
+fp8q_status launch_generic(const QuantArgs& a, int fmt, bool row, bool col, cudaStream_t s) {
+    const int64_t Rp = a.tiles_r * 128, Cp = a.tiles_c * 128;
+    if (Rp == 0 || Cp == 0) return FP8Q_OK;  // empty x: nothing to write
+    const int bc = a.bc;
+    const bool sq = a.br == a.bc;
+    const int64_t nbr = (a.R + bc - 1) / bc, nbc = (a.C + bc - 1) / bc;
+    const int64_t row_n = sq ? nbr * nbc : nbc * Rp, col_n = sq ? nbr * nbc : nbr * Cp;
+    uint32_t* rm = (uint32_t*)a.s_row;
+    uint32_t* cm = (uint32_t*)a.s_col;
+    if (row && cudaMemsetAsync(rm, 0, (size_t)row_n * 4, s) != cudaSuccess) return FP8Q_ERR_CUDA;
+    if (col && cudaMemsetAsync(cm, 0, (size_t)col_n * 4, s) != cudaSuccess) return FP8Q_ERR_CUDA;
+    const int64_t strips = ((a.R + 63) / 64) * ((a.C + 255) / 256);
+    int64_t grid = (int64_t)num_sms() * 8;
+    if (strips < grid) grid = strips;
+    const unsigned g = (unsigned)grid;
+    if (sq) {
+        if (row)
+            gen_amax_kernel<true, true, false><<<g, 256, 0, s>>>(a.x, a.R, a.C, bc, rm, cm, a.counters);
+        else
+            gen_amax_kernel<true, false, true><<<g, 256, 0, s>>>(a.x, a.R, a.C, bc, rm, cm, a.counters);
+    } else if (row && col) {
+        gen_amax_kernel<false, true, true><<<g, 256, 0, s>>>(a.x, a.R, a.C, bc, rm, cm, a.counters);
+    } else if (row) {
+        gen_amax_kernel<false, true, false><<<g, 256, 0, s>>>(a.x, a.R, a.C, bc, rm, cm, a.counters);
+    } else {
+        gen_amax_kernel<false, false, true><<<g, 256, 0, s>>>(a.x, a.R, a.C, bc, rm, cm, a.counters);
+    }
+    if (cudaGetLastError() != cudaSuccess) return FP8Q_ERR_CUDA;
+    const fp8q_status r = sq ? launch_tile_fmt<kGen, true>(a, fmt, row, col, s) : launch_tile_fmt<kGen, false>(a, fmt, row, col, s);
+    if (r != FP8Q_OK) return r;
+    auto blocks = [](int64_t n) { return (unsigned)((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096); };
+    const bool e4 = fmt == FP8Q_E4M3;
+    if (sq && row && col) {
+        if (e4)
+            gen_transpose_scales_kernel<FP8Q_E4M3><<<blocks(row_n), 256, 0, s>>>(rm, (float*)cm, nbr, nbc);
+        else
+            gen_transpose_scales_kernel<FP8Q_E5M2><<<blocks(row_n), 256, 0, s>>>(rm, (float*)cm, nbr, nbc);
+        if (cudaGetLastError() != cudaSuccess) return FP8Q_ERR_CUDA;
+    }
+    for (int w = 0; w < 2; ++w) {
+        // in place: the row buffer; the column buffer unless it was filled above
+        if (w == 0 ? !row : (!col || (sq && row))) continue;
+        uint32_t* m = w == 0 ? rm : cm;
+        const int64_t n = w == 0 ? row_n : col_n;
+        if (e4)
+            gen_finalize_kernel<FP8Q_E4M3><<<blocks(n), 256, 0, s>>>(m, n);
+        else
+            gen_finalize_kernel<FP8Q_E5M2><<<blocks(n), 256, 0, s>>>(m, n);
+        if (cudaGetLastError() != cudaSuccess) return FP8Q_ERR_CUDA;
+    }
+    return FP8Q_OK;
 }
 
 // Per-channel current: zero the scale buffers, the amax pass into them, the
@@ -1098,6 +1299,10 @@ fp8q_status launch_quantize(const fp8q_recipe* rc, const QuantArgs& a, DelayedDe
             return launch_tile_fmt<kMX>(a, rc->fmt, row, col, s);
         case kPC:
             return launch_perchannel(a, rc->fmt, row, col, s);
+        case kGen:  // 1 x 128 and 128 x 128 are the specialised kinds' kernels
+            if (a.br == 1 && a.bc == 128) return launch_tile_fmt<kB1>(a, rc->fmt, row, col, s);
+            if (a.br == 128 && a.bc == 128) return launch_tile_fmt<kB128>(a, rc->fmt, row, col, s);
+            return launch_generic(a, rc->fmt, row, col, s);
         default:
             return FP8Q_ERR_ARG;
     }

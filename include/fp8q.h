@@ -41,12 +41,14 @@
  *   PERCHANNEL_CURRENT       fp32 [Rp], Rp = R up to 128: row r's       s_inv[r]
  *                            fp32(1 / s_r); pad entries 1.0 (the rule
  *                            for an all-zero row)
+ *   BLOCK_GENERIC 1 x b      fp32 [ceil(C/b)][Rp], as BLOCK_1x128       d
+ *   BLOCK_GENERIC b x b      fp32 [ceil(R/b)][ceil(C/b)], as 128x128    d
  *
- * The column-wise copy of BLOCK_1x128, MXFP8_1x32 and PERCHANNEL_CURRENT
- * re-quantizes x^T with its blocks along the rows of x (the contraction
- * dimension of the wgrad GEMM; per channel: one factor per column of x); for
- * per-tensor and 128x128 kinds it is the byte transpose of the row-wise copy
- * with the same (transposed) scales.
+ * The column-wise copy of BLOCK_1x128, MXFP8_1x32, PERCHANNEL_CURRENT and a
+ * 1 x b BLOCK_GENERIC re-quantizes x^T with its blocks along the rows of x
+ * (the contraction dimension of the wgrad GEMM; per channel: one factor per
+ * column of x); for per-tensor, 128x128 and b x b kinds it is the byte
+ * transpose of the row-wise copy with the same (transposed) scales.
  */
 #ifndef FP8Q_H
 #define FP8Q_H
@@ -86,10 +88,14 @@ typedef enum {
     FP8Q_BLOCK_128x128 = 3,      /* same per 128x128 tile (weights) */
     FP8Q_MXFP8_1x32 = 4,         /* e = floor(log2 amax) - emax_elem per 1x32 block,
                                     E8M0 code e + 127, q = sat_rne(x * 2^-e) */
-    FP8Q_PERCHANNEL_CURRENT = 5  /* [nemo] Figure 1 (channel-wise scaling, one factor
+    FP8Q_PERCHANNEL_CURRENT = 5, /* [nemo] Figure 1 (channel-wise scaling, one factor
                                     per row / column): the per-tensor current rule
                                     per row of the copy, s_r = fmax / amax(row r),
                                     q = sat_rne(x * s_r) */
+    FP8Q_BLOCK_GENERIC = 6       /* [nemo] scaling strategy 3 (sub-channel blocks of
+                                    user-set dimensions): the blockwise rule of
+                                    BLOCK_1x128 on blocks of block_rows x block_cols,
+                                    either 1 x b or b x b with b in {32, 64, 128, 256} */
 } fp8q_recipe_kind;
 
 typedef struct {
@@ -97,6 +103,8 @@ typedef struct {
     int fmt;            /* fp8q_format of the quantized data */
     int want_rowwise;   /* 1: write data_row (+ scale_row) */
     int want_colwise;   /* 1: write data_col (+ scale_col) */
+    int block_rows;     /* BLOCK_GENERIC only: 1 or b */
+    int block_cols;     /* BLOCK_GENERIC only: b in {32, 64, 128, 256} */
 } fp8q_recipe;
 
 /*
@@ -113,8 +121,8 @@ typedef struct {
  *              whose scaled fp32 value exceeded fmax (saturated), [1] the same
  *              for a re-quantized column-wise copy (0 when the column-wise
  *              copy is a byte transpose), [2] NaN / Inf elements of x.
- * rows / cols / fmt / kind are filled in by fp8q_quantize and read by
- * fp8q_scaled_gemm.
+ * rows / cols / fmt / kind (and, for BLOCK_GENERIC, block_rows / block_cols)
+ * are filled in by fp8q_quantize and read by fp8q_scaled_gemm.
  */
 typedef struct {
     void* data_row;
@@ -129,6 +137,8 @@ typedef struct {
     int64_t cols;
     int fmt;
     int kind;
+    int block_rows;   /* BLOCK_GENERIC: the recipe's block shape (else 0) */
+    int block_cols;
 } fp8q_tensor;
 
 /* Opaque per-tensor delayed-scaling state, owned by the library: an amax ring
@@ -171,7 +181,12 @@ FP8Q_API fp8q_status fp8q_scale_bytes(const fp8q_recipe* recipe, int64_t rows, i
  * row's and every column's amax (into the scale buffers, as scratch), then
  * s = fmax / amax per row (row-wise copy) or per column (column-wise copy)
  * as for per-tensor current, and the scale buffers end holding fp32(1 / s).
- * Amax always excludes NaN / Inf.  Counters are overwritten.
+ * Amax always excludes NaN / Inf.  Counters are overwritten.  BLOCK_GENERIC:
+ * recipe->block_rows x block_cols must be 1 x b or b x b, b in {32, 64, 128,
+ * 256} (else FP8Q_ERR_UNSUPPORTED); 1 x 128 and 128 x 128 run exactly as
+ * BLOCK_1x128 and BLOCK_128x128; other shapes take a pass over x that leaves
+ * every block's amax in the scale buffers (as scratch), then the cast, and the
+ * scale buffers end holding d.
  */
 FP8Q_API fp8q_status fp8q_quantize(const fp8q_recipe* recipe, const void* x, int64_t rows, int64_t cols,
                           fp8q_delayed_state* st, fp8q_tensor* out, void* stream);

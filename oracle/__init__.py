@@ -41,7 +41,7 @@ E4M3, E5M2 = 0, 1
 FMAX = {E4M3: 448.0, E5M2: 57344.0}
 
 # recipe kinds (the oracle's own numbering)
-PERTENSOR_CURRENT, PERTENSOR_DELAYED, BLOCK_1x128, BLOCK_128x128, MXFP8_1x32, PERCHANNEL_CURRENT = range(6)
+PERTENSOR_CURRENT, PERTENSOR_DELAYED, BLOCK_1x128, BLOCK_128x128, MXFP8_1x32, PERCHANNEL_CURRENT, BLOCK_GENERIC = range(7)
 KIND_MULT, KIND_DIV, KIND_POW2 = 0, 1, 2
 
 
@@ -262,6 +262,29 @@ def pad128(v: np.ndarray) -> np.ndarray:
 
 # --------------------------------------------------------------- recipes
 
+def quantize_generic(fmt: int, x_bits: np.ndarray, br: int, bc: int, rowwise: bool = True,
+                     colwise: bool = False) -> dict:
+    """Sub-channel blocks of user-set dimensions ("mastering FP8 LLM training
+    1.5x speedup", scaling strategy 3), the blockwise rule of sec. 2.2 of the
+    2025 guide on br x bc blocks (1 x b or b x b): the row copy quantizes x,
+    the column copy quantizes x^T, each with br x bc blocks (for square blocks
+    that is the transpose of the row copy).  scale_row / scale_col are the
+    plain [ceil(R/br)][ceil(C/bc)] d of each copy; *_packed the library's
+    layout (1 x b: K-block-major [ceil(C/b)][Rp], pads 1.0; b x b: plain)."""
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    out: dict = {"sat_row": 0, "sat_col": 0, "nonfinite": 0}
+    for which, on, m in (("row", rowwise, x), ("col", colwise, np.ascontiguousarray(x.T))):
+        if not on:
+            continue
+        q, d, _, am, sat, nf = quant_blocks(m, br, bc, KIND_DIV, fmt)
+        packed = pack_block1x128(d) if br == 1 else d
+        out.update({"data_" + which: q, "scale_" + which: d, "scale_" + which + "_packed": packed,
+                    "sat_" + which: sat, "nonfinite": nf})
+    if br == bc:
+        out["sat_col"] = 0  # the column copy of square blocks is the row copy's transpose: no count of its own
+    return out
+
+
 def quantize(kind: int, fmt: int, x_bits: np.ndarray, rowwise: bool = True, colwise: bool = False,
              state: Delayed | None = None) -> dict:
     """One quantize call of a recipe, returning what the product writes:
@@ -383,9 +406,11 @@ def gemm_full(A, fmtA, sA, a_bm, a_bk, B, fmtB, sB, b_bn, b_bk) -> np.ndarray:
     return gemm_points(A, fmtA, sA, a_bm, a_bk, B, fmtB, sB, b_bn, b_bk, mm.ravel(), nn.ravel()).reshape(M, N)
 
 
-def dequant_scales(kind: int, q: dict, which: str, rows: int, cols: int):
+def dequant_scales(kind: int, q: dict, which: str, rows: int, cols: int, block=(0, 0)):
     """(scale array, block rows, block cols) of a quantized copy for
-    gemm_points: which = 'row' or 'col'."""
+    gemm_points: which = 'row' or 'col'; block = (br, bc) of a generic kind."""
+    if kind == BLOCK_GENERIC:
+        return q["scale_" + which], block[0], block[1]
     if kind in (PERTENSOR_CURRENT, PERTENSOR_DELAYED):
         return np.array([[q["scale_inv"]]], dtype=np.float32), rows, cols
     s = q["scale_" + which]

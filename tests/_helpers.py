@@ -46,8 +46,8 @@ def expected_scale_bytes(kind: int, ref: dict, which: str) -> np.ndarray | None:
         return np.ascontiguousarray(ref["scale_" + which], dtype=np.float32).view(np.uint8).ravel()
     if kind == O.MXFP8_1x32:
         return ref["scale_" + which + "_packed"].ravel()
-    if kind == O.PERCHANNEL_CURRENT:
-        return ref["scale_" + which + "_packed"].astype(np.float32).view(np.uint8).ravel()
+    if kind in (O.PERCHANNEL_CURRENT, O.BLOCK_GENERIC):
+        return np.ascontiguousarray(ref["scale_" + which + "_packed"], dtype=np.float32).view(np.uint8).ravel()
     return None
 
 

@@ -366,3 +366,20 @@ def test_amax_sat_matches_cast_scaled():
         for fmt in (O.E4M3, O.E5M2):
             q, amax, sat, nf = O.cast_scaled(x, s, fmt)
             assert O.amax_sat(x, s, fmt) == (amax, sat, nf)
+
+
+def test_generic_128_blocks_are_the_specialised_recipes():
+    """The generic sub-channel recipe at 1 x 128 and 128 x 128 is exactly the
+    guide's sec. 2.2 recipes (codes, packed scales, counters), and its square
+    blocks' column copy is the transpose of the row copy."""
+    x = _rand_bits((272, 400), 41)
+    for (br, bc), kind in (((1, 128), O.BLOCK_1x128), ((128, 128), O.BLOCK_128x128)):
+        g = O.quantize_generic(O.E4M3, x, br, bc, True, True)
+        s = O.quantize(kind, O.E4M3, x, True, True)
+        for key in ("data_row", "data_col", "sat_row", "sat_col", "nonfinite"):
+            assert np.array_equal(g[key], s[key]), (kind, key)
+        for which in ("row", "col"):
+            sp = s.get("scale_" + which + "_packed", s["scale_" + which])
+            assert np.array_equal(g["scale_" + which + "_packed"], sp), (kind, which)
+    g = O.quantize_generic(O.E5M2, x, 64, 64, True, True)
+    assert np.array_equal(g["data_col"], g["data_row"].T) and np.array_equal(g["scale_col"], g["scale_row"].T)
