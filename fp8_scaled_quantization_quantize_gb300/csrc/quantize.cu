@@ -1338,13 +1338,23 @@ fp8q_status launch_quantize_multi(int n, const fp8q_recipe* const* rcs, QuantArg
         if (cudaEventCreateWithFlags(&m.fork, cudaEventDisableTiming) != cudaSuccess) return FP8Q_ERR_CUDA;
         m.ready = true;
     }
+    // each job's share of the resident CTAs follows its tiles weighted by
+    // their cost: a re-quantized column copy (1 x 128 blocks, MXFP8) takes a
+    // second conversion per element, the byte transposes do not (measured on
+    // the Llama-3-8B up-projection's X 1 x 128 + W 128 x 128, both copies:
+    // 66.5 us with equal weights, 60 us with 1.3 - 1.6 for X's tiles)
+    auto weight = [&](int i) -> int64_t {
+        if (!rcs[i]->want_colwise) return 100;
+        if (rcs[i]->kind == kB1 || (rcs[i]->kind == kGen && rcs[i]->block_rows == 1)) return 145;
+        return rcs[i]->kind == kMX ? 120 : 100;
+    };
     int64_t total = 0;
-    for (int i = 0; i < n; ++i) total += a[i].tiles_r * a[i].tiles_c;
+    for (int i = 0; i < n; ++i) total += a[i].tiles_r * a[i].tiles_c * weight(i);
     const int64_t budget = (int64_t)num_sms() * 2;
     if (cudaEventRecord(m.fork, s) != cudaSuccess) return FP8Q_ERR_CUDA;
     fp8q_status r = FP8Q_OK;
     for (int i = 0; i < n; ++i) {
-        const int64_t tiles = a[i].tiles_r * a[i].tiles_c;
+        const int64_t tiles = a[i].tiles_r * a[i].tiles_c * weight(i);
         a[i].grid_cap = total > 0 ? (budget * tiles / total > 0 ? budget * tiles / total : 1) : 0;
         if (cudaStreamWaitEvent(m.s[i], m.fork, 0) != cudaSuccess) return FP8Q_ERR_CUDA;
         const fp8q_status ri = launch_quantize(rcs[i], a[i], sts[i], m.s[i]);
