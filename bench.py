@@ -556,8 +556,8 @@ def gemm_kernel_name(M, N, recipe, out="bf16"):
 
 # ------------------------------------------------------- single-op modes
 
-KINDS = {"current": 0, "delayed": 1, "1x128": 2, "128x128": 3, "mx": 4, "perchannel": 5}
-QBYTES_SCALE = {0: 0.0, 1: 0.0, 2: 4 / 128, 3: 4 / (128 * 128), 4: 1 / 32, 5: 0.0}
+KINDS = {"current": 0, "delayed": 1, "1x128": 2, "128x128": 3, "mx": 4, "perchannel": 5, "generic": 6}
+QBYTES_SCALE = {0: 0.0, 1: 0.0, 2: 4 / 128, 3: 4 / (128 * 128), 4: 1 / 32, 5: 0.0, 6: 0.0}
 
 
 def _device_tensor(rows, cols, seed, outlier_frac=0.001, factor=1000.0):
@@ -593,7 +593,7 @@ def _time_ms(fn, steps, warmup, flush=None):
     return statistics.mean(a.elapsed_time(b) for a, b in ms)
 
 
-def quantize_point(kind, rows, cols, rowwise, colwise, steps, warmup, flush, x=None):
+def quantize_point(kind, rows, cols, rowwise, colwise, steps, warmup, flush, x=None, block=(0, 0)):
     import torch
 
     from fp8_scaled_quantization_quantize_gb300 import api
@@ -601,21 +601,27 @@ def quantize_point(kind, rows, cols, rowwise, colwise, steps, warmup, flush, x=N
     if x is None:
         x = _device_tensor(rows, cols, 5)
     st = api.DelayedState(16, api.E4M3, 0) if kind == 1 else None
-    qt = api.alloc(kind, api.E4M3, rows, cols, rowwise, colwise, "cuda")
+    qt = api.alloc(kind, api.E4M3, rows, cols, rowwise, colwise, "cuda", block=block)
     ms = _time_ms(lambda: api.quantize_into(x, qt, st), steps, warmup, flush)
     copies = int(rowwise) + int(colwise)
-    # the current-scaling kinds read x twice (the amax pass, then the cast)
-    per_elem = 2 + copies * (1 + QBYTES_SCALE[kind]) + (2 if kind in (0, 5) else 0)
+    # the current-scaling kinds read x twice (the amax pass, then the cast), and
+    # so do generic blocks other than 1 x 128 / 128 x 128 (the block-amax pass)
+    two_pass = kind in (0, 5) or (kind == 6 and tuple(block) not in ((1, 128), (128, 128)))
+    qscale = 4 / (block[0] * block[1]) if kind == 6 else QBYTES_SCALE[kind]
+    per_elem = 2 + copies * (1 + qscale) + (2 if two_pass else 0)
     gbs = rows * cols * per_elem / ms / 1e6
     del qt
     torch.cuda.synchronize()
-    return {"mode": "quantize", "kind": [k for k, v in KINDS.items() if v == kind][0], "rows": rows, "cols": cols,
+    return {"mode": "quantize", "kind": [k for k, v in KINDS.items() if v == kind][0] +
+            (f" {block[0]}x{block[1]}" if kind == 6 else ""), "rows": rows, "cols": cols,
             "mib": rows * cols * 2 / 2 ** 20, "rowwise": rowwise, "colwise": colwise, "ms": round(ms, 4),
             "gbs": round(gbs, 1), "frac_of_hbm": round(gbs / hbm_peak, 3),
             "algorithmic_bytes_per_elem": round(per_elem, 4)}
 
 
-def gemm_point(kind, M, N, K, steps, warmup, flush, out="bf16"):
+def gemm_point(kind, M, N, K, steps, warmup, flush, out="bf16", block=0, b2d=True):
+    """One GEMM timed; kind 6 (generic blocks): A 1 x block, B block x block
+    (b2d) or 1 x block."""
     import torch
 
     from fp8_scaled_quantization_quantize_gb300 import api
@@ -623,13 +629,15 @@ def gemm_point(kind, M, N, K, steps, warmup, flush, out="bf16"):
     a = _device_tensor(M, K, 11)
     b = _device_tensor(N, K, 12)
     kb = 3 if kind == 2 else kind
-    qa = api.quantize(a, kind, api.E4M3, True, False)
-    qb = api.quantize(b, kb, api.E4M3, True, False)
+    ba, bb = ((1, block), ((block, block) if b2d else (1, block))) if kind == 6 else ((0, 0), (0, 0))
+    qa = api.quantize(a, kind, api.E4M3, True, False, block=ba)
+    qb = api.quantize(b, kb, api.E4M3, True, False, block=bb)
     del a, b
     D = torch.empty((M, N), dtype=torch.bfloat16 if out == "bf16" else torch.float32, device="cuda")
     ms = _time_ms(lambda: api.scaled_gemm(qa, False, qb, False, out=D), steps, warmup, flush)
     tf = 2.0 * M * N * K / ms / 1e9
-    name = {0: "pertensor", 2: "blockwise 1x128 x 128x128", 4: "mxfp8", 5: "perchannel"}[kind]
+    name = {0: "pertensor", 2: "blockwise 1x128 x 128x128", 4: "mxfp8", 5: "perchannel"}.get(
+        kind, f"generic 1x{block} x {bb[0]}x{bb[1]}")
     del qa, qb, D
     torch.cuda.synchronize()
     return {"mode": "gemm", "recipe": name, "M": M, "N": N, "K": K, "out": out, "ms": round(ms, 4),
@@ -640,12 +648,13 @@ def run_modes(args):
     import torch
     torch.cuda.set_device(0)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda") if not args.no_flush else None
+    blk = (1 if args.block_1d else args.block, args.block)
     if args.mode == "quantize":
         print(json.dumps(quantize_point(KINDS[args.kind], args.rows, args.cols, not args.no_rowwise, args.colwise,
-                                        args.steps, args.warmup, flush)), flush=True)
+                                        args.steps, args.warmup, flush, block=blk)), flush=True)
     elif args.mode == "gemm":
         print(json.dumps(gemm_point(KINDS[args.kind], args.M, args.N, args.K, args.steps, args.warmup, flush,
-                                    args.out)), flush=True)
+                                    args.out, args.block, not args.block_1d)), flush=True)
     elif args.mode == "multi":  # n small tensors: n quantize calls against one fp8q_quantize_multi
         from fp8_scaled_quantization_quantize_gb300 import api
         n, rows, cols = 8, args.rows, args.cols
@@ -733,6 +742,17 @@ def run_modes(args):
                 print(json.dumps(gemm_point(kind, 8192, 8192, K, args.steps, args.warmup, flush)), flush=True)
         for kind in (4, 2, 0, 5):
             print(json.dumps(gemm_point(kind, 8192, 53248, 16384, args.steps, args.warmup, flush)), flush=True)
+        # generic sub-channel blocks: quantize (both copies, 256 MiB) and the GEMM
+        # at 8192^2 x 4096 for each K block, 1D2D and 1D1D
+        x = _device_tensor(32768, 4096, 5)
+        for blk in ((1, 32), (1, 64), (1, 256), (32, 32), (64, 64), (256, 256)):
+            print(json.dumps(quantize_point(6, 32768, 4096, True, True, args.steps, args.warmup, flush, x, blk)),
+                  flush=True)
+        del x
+        for b in (32, 64, 128, 256):
+            for b2d in (True, False):
+                print(json.dumps(gemm_point(6, 8192, 8192, 4096, args.steps, args.warmup, flush, "bf16", b, b2d)),
+                      flush=True)
 
 
 # -------------------------------------------------------------- oracle arm
@@ -851,6 +871,9 @@ def main():
                          "qerror: quantization error per recipe; delayed70b: the delayed-scaling 70B FFN step; "
                          "multi: 8 small tensors, separate quantize calls against one fp8q_quantize_multi")
     ap.add_argument("--kind", choices=list(KINDS), default="mx")
+    ap.add_argument("--block", type=int, choices=[32, 64, 128, 256], default=128,
+                    help="generic kind: block width b (quantize b x b unless --block-1d; GEMM A 1 x b, B b x b)")
+    ap.add_argument("--block-1d", action="store_true", help="generic kind: 1 x b blocks (GEMM: B 1 x b too)")
     ap.add_argument("--e2e-blocks", type=int, choices=[1, 2, 4, 7, 8, 14, 16], default=8,
                     help="row blocks of W in the end-to-end pipeline (F = 14336 = 112 x 128)")
     ap.add_argument("--rows", type=int, default=16384)
