@@ -367,9 +367,16 @@ __device__ __forceinline__ void store_q128(const CUtensorMap* mapQ, uint8_t* stg
     uint32_t h[64];
 #pragma unroll
     for (int i = 0; i < 64; ++i) h[i] = pack_bf16(v[2 * i] * scale, v[2 * i + 1] * scale);
-    uint32_t pm = 0;
+    uint32_t cm[8];  // packed maxima of each 16-column chunk
 #pragma unroll
-    for (int i = 0; i < 64; ++i) pm = max_u16x2(pm, h[i] & 0x7FFF7FFFu);
+    for (int c = 0; c < 8; ++c) {
+        uint32_t x = h[8 * c] & 0x7FFF7FFFu;
+#pragma unroll
+        for (int i = 1; i < 8; ++i) x = max_u16x2(x, h[8 * c + i] & 0x7FFF7FFFu);
+        cm[c] = x;
+    }
+    const uint32_t pm = max_u16x2(max_u16x2(max_u16x2(cm[0], cm[1]), max_u16x2(cm[2], cm[3])),
+                                  max_u16x2(max_u16x2(cm[4], cm[5]), max_u16x2(cm[6], cm[7])));
     uint32_t m = max(pm & 0xFFFFu, pm >> 16);
     const bool nf = m >= 0x7F80u;
     if (nf) {
@@ -387,10 +394,14 @@ __device__ __forceinline__ void store_q128(const CUtensorMap* mapQ, uint8_t* stg
     const float2 d2 = make_float2(d, d), nr2 = make_float2(-rd, -rd);
     // only elements equal to the block maximum can saturate
     const bool may_sat = row_live && fabsf(__fdiv_rn(__uint_as_float(m << 16), d)) > Fmt<QFMT>::fmax;
-    if (may_sat) {
+    if (may_sat) {  // look only inside the chunks whose maximum it is (all of them when NaN / Inf hide it)
 #pragma unroll
-        for (int i = 0; i < 64; ++i)
-            nsat += (2 * i < live && (h[i] & 0x7FFFu) == m) + (2 * i + 1 < live && ((h[i] >> 16) & 0x7FFFu) == m);
+        for (int c = 0; c < 8; ++c) {
+            if (!nf && max(cm[c] & 0xFFFFu, cm[c] >> 16) != m) continue;
+#pragma unroll
+            for (int i = 8 * c; i < 8 * c + 8; ++i)
+                nsat += (2 * i < live && (h[i] & 0x7FFFu) == m) + (2 * i + 1 < live && ((h[i] >> 16) & 0x7FFFu) == m);
+        }
     }
     bulk_wait_read();  // the D boxes have left the staging area
     __syncwarp();

@@ -464,6 +464,48 @@ __global__ void __launch_bounds__(kThreads, 2)
         // the tile's place in the whole tensor (a block of rows starts at row0)
         const int64_t trg = (int64_t)tr + a.row0 / kTile, r0g = a.row0 + r0;
         const int64_t tileg = trg * (int64_t)tiles_c + tc;
+        // per-channel and generic blocks: the maxima the amax pass left in the
+        // scale buffers, loaded before the tile's wait so that their latency
+        // overlaps it (pre_r: this thread's row path, two 32-column blocks;
+        // pre_c: its column pair); rows and columns past x read 0
+        uint32_t pre_r[2] = {0u, 0u}, pre_c[2] = {0u, 0u};
+        if constexpr (KIND == kPC) {
+            if constexpr (ROW) pre_r[0] = pre_r[1] = ((const uint32_t*)a.s_row)[r0g + rr];
+            if constexpr (COL && !kTranspose) {
+                const int64_t cc = c0 + 2 * (t & 63);
+                pre_c[0] = ((const uint32_t*)a.s_col)[cc];
+                pre_c[1] = ((const uint32_t*)a.s_col)[cc + 1];
+            }
+        } else if constexpr (KIND == kGen) {
+            const int bc = a.bc;
+            if constexpr (kRowCodes) {
+                const int64_t rg = r0g + rr, cf = c0 + 64 * hh;  // row; first column of this half
+                const int64_t nbc = (a.C + bc - 1) / bc;
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    const int64_t cc = cf + 32 * i;
+                    if (rg < a.R_total && cc < a.C && (i == 0 || bc == 32)) {
+                        const int64_t bj = cc / bc;
+                        if constexpr (GSQ) {
+                            const int64_t nbr = (a.R_total + bc - 1) / bc, bi = rg / bc;
+                            pre_r[i] = ROW ? ((const uint32_t*)a.s_row)[bi * nbc + bj]
+                                           : ((const uint32_t*)a.s_col)[bj * nbr + bi];
+                        } else {
+                            pre_r[i] = ((const uint32_t*)a.s_row)[bj * (a.tiles_r_total * kTile) + rg];
+                        }
+                    }
+                }
+                if (bc != 32) pre_r[1] = pre_r[0];
+            }
+            if constexpr (COL && !kTranspose) {
+                const int64_t rq = r0g + 32 * (t >> 6), cc = c0 + 2 * (t & 63);
+                if (rq < a.R_total) {
+                    const uint32_t* sc = (const uint32_t*)a.s_col + (rq / bc) * (a.tiles_c * kTile) + cc;
+                    pre_c[0] = sc[0];
+                    pre_c[1] = sc[1];
+                }
+            }
+        }
         const bool ok = mbar_wait_bounded(bar(stg), ph, &abort_flag, &g_quant_errors, 2u, a.wait_ns);
         if (__syncthreads_or(!ok)) break;  // the whole CTA leaves together
         uint8_t* stage = qsmem + stg * kStageBytes;
@@ -545,7 +587,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             // the row's maximum over all of x (the amax pass left it in s_row as
             // bf16 magnitude bits): s = fmax / amax, the per-tensor current rule
             if constexpr (ROW) {
-                const uint32_t m = ((const uint32_t*)a.s_row)[r0g + rr];
+                const uint32_t m = pre_r[0];
                 mq[0] = mq[1] = m;
                 kq[0] = kq[1] = pertensor_scale<FMT>(__uint_as_float(m << 16));
             }
@@ -553,28 +595,10 @@ __global__ void __launch_bounds__(kThreads, 2)
             // the blocks' maxima over all of x (the amax pass left them in the
             // scale buffers as bf16 magnitude bits); rows and columns past x read 0
             if constexpr (kRowCodes) {
-                const int64_t rg = r0g + rr, cf = c0 + 64 * hh;  // row; first column of this half
-                const int bc = a.bc;
-                const int64_t nbc = (a.C + bc - 1) / bc;
-                uint32_t m2[2] = {0u, 0u};
-#pragma unroll
-                for (int i = 0; i < 2; ++i) {
-                    const int64_t cc = cf + 32 * i;
-                    if (rg < a.R_total && cc < a.C && (i == 0 || bc == 32)) {
-                        const int64_t bj = cc / bc;
-                        if constexpr (GSQ) {
-                            const int64_t nbr = (a.R_total + bc - 1) / bc, bi = rg / bc;
-                            m2[i] = ROW ? ((const uint32_t*)a.s_row)[bi * nbc + bj] : ((const uint32_t*)a.s_col)[bj * nbr + bi];
-                        } else {
-                            m2[i] = ((const uint32_t*)a.s_row)[bj * (a.tiles_r_total * kTile) + rg];
-                        }
-                    }
-                }
-                if (bc != 32) m2[1] = m2[0];
-                mq[0] = m2[0];
-                mq[1] = m2[1];
-                kq[0] = block_scale<FMT>(__uint_as_float(m2[0] << 16));
-                kq[1] = block_scale<FMT>(__uint_as_float(m2[1] << 16));
+                mq[0] = pre_r[0];
+                mq[1] = pre_r[1];
+                kq[0] = block_scale<FMT>(__uint_as_float(pre_r[0] << 16));
+                kq[1] = block_scale<FMT>(__uint_as_float(pre_r[1] << 16));
             }
         } else if constexpr (KIND == kMX) {
             const int e0 = mx_exponent<FMT>(mq[0] << 16), e1 = mx_exponent<FMT>(mq[1] << 16);
@@ -681,19 +705,14 @@ __global__ void __launch_bounds__(kThreads, 2)
                 } else if constexpr (KIND == kGen) {
                     // blocks of bc rows of one column (1 x bc blocks of x^T): their maxima
                     // from the amax pass, in s_col [ceil(R/bc)][Cp]; rows past x read 0
-                    const int64_t rq = r0g + 32 * qd;
-                    m0 = m1 = 0u;
-                    if (rq < a.R_total) {
-                        const uint32_t* sc = (const uint32_t*)a.s_col + (rq / a.bc) * (a.tiles_c * kTile) + cc;
-                        m0 = sc[0];
-                        m1 = sc[1];
-                    }
+                    m0 = pre_c[0];
+                    m1 = pre_c[1];
                     k0 = block_scale<FMT>(__uint_as_float(m0 << 16));
                     k1 = block_scale<FMT>(__uint_as_float(m1 << 16));
                 } else if constexpr (KIND == kPC) {
                     // the columns' maxima over all of x (from the amax pass, in s_col)
-                    m0 = ((const uint32_t*)a.s_col)[cc];
-                    m1 = ((const uint32_t*)a.s_col)[cc + 1];
+                    m0 = pre_c[0];
+                    m1 = pre_c[1];
                     k0 = pertensor_scale<FMT>(__uint_as_float(m0 << 16));
                     k1 = pertensor_scale<FMT>(__uint_as_float(m1 << 16));
                 } else {  // 1x128 along the rows of x: reduce the four quarters
