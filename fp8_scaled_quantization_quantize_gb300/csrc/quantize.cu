@@ -393,17 +393,422 @@ __device__ __noinline__ ColCodes col_codes_rare(Col32 c, float k0, float k1) {
     return out;
 }
 
+// Per-thread counters of a tile pass: saturated elements of the row-wise and
+// of a re-quantized column-wise copy, NaN / Inf elements, and (delayed
+// scaling) the largest finite magnitude seen, as bf16 bits.
+struct TileCounts {
+    uint32_t sat_row, sat_col, nonfinite, tmax;
+};
+
+template <int KIND, bool COL, bool GSQ>
+struct TileTraits {
+    static constexpr bool kPerTensor = (KIND == kCur || KIND == kDel);
+    // the column copy of a recipe whose scale does not depend on the copy's
+    // direction is the byte transpose of the row codes
+    static constexpr bool kTranspose = COL && (kPerTensor || KIND == kB128 || (KIND == kGen && GSQ));
+};
+
+// Per-channel and generic blocks: the maxima that the amax pass left in the
+// scale buffers for this thread's part of tile `tileid`, loaded before the
+// tile's wait so that their latency overlaps it (pre_r: the row path's two
+// 32-column blocks; pre_c: the column path's column pair).  Nothing for the
+// other recipes.
+template <int KIND, bool ROW, bool COL, bool GSQ>
+__device__ __forceinline__ void tile_maxima(const QuantArgs& a, uint32_t tileid, uint32_t tiles_c,
+                                            uint32_t (&pre_r)[2], uint32_t (&pre_c)[2]) {
+    constexpr bool kTranspose = TileTraits<KIND, COL, GSQ>::kTranspose;
+    constexpr bool kRowCodes = ROW || kTranspose;
+    const int t = threadIdx.x, rr = t & (kTile - 1), hh = t >> 7;
+    const uint32_t tr = tileid / tiles_c, tc = tileid - tr * tiles_c;
+    const int64_t r0g = a.row0 + (int64_t)tr * kTile, c0 = (int64_t)tc * kTile;
+    (void)rr;
+    (void)hh;
+    (void)r0g;
+    (void)c0;
+    (void)kRowCodes;
+    // per-channel and generic blocks: the maxima the amax pass left in the
+    // scale buffers, loaded before the tile's wait so that their latency
+    // overlaps it (pre_r: this thread's row path, two 32-column blocks;
+    // pre_c: its column pair); rows and columns past x read 0
+    if constexpr (KIND == kPC) {
+        if constexpr (ROW) pre_r[0] = pre_r[1] = ((const uint32_t*)a.s_row)[r0g + rr];
+        if constexpr (COL && !kTranspose) {
+            const int64_t cc = c0 + 2 * (t & 63);
+            pre_c[0] = ((const uint32_t*)a.s_col)[cc];
+            pre_c[1] = ((const uint32_t*)a.s_col)[cc + 1];
+        }
+    } else if constexpr (KIND == kGen) {
+        const int bc = a.bc;
+        if constexpr (kRowCodes) {
+            const int64_t rg = r0g + rr, cf = c0 + 64 * hh;  // row; first column of this half
+            const int64_t nbc = (a.C + bc - 1) / bc;
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const int64_t cc = cf + 32 * i;
+                if (rg < a.R_total && cc < a.C && (i == 0 || bc == 32)) {
+                    const int64_t bj = cc / bc;
+                    if constexpr (GSQ) {
+                        const int64_t nbr = (a.R_total + bc - 1) / bc, bi = rg / bc;
+                        pre_r[i] = ROW ? ((const uint32_t*)a.s_row)[bi * nbc + bj]
+                                       : ((const uint32_t*)a.s_col)[bj * nbr + bi];
+                    } else {
+                        pre_r[i] = ((const uint32_t*)a.s_row)[bj * (a.tiles_r_total * kTile) + rg];
+                    }
+                }
+            }
+            if (bc != 32) pre_r[1] = pre_r[0];
+        }
+        if constexpr (COL && !kTranspose) {
+            const int64_t rq = r0g + 32 * (t >> 6), cc = c0 + 2 * (t & 63);
+            if (rq < a.R_total) {
+                const uint32_t* sc = (const uint32_t*)a.s_col + (rq / bc) * (a.tiles_c * kTile) + cc;
+                pre_c[0] = sc[0];
+                pre_c[1] = sc[1];
+            }
+        }
+    }
+}
+
+// One 128 x 128 tile (`tileid` of a tensor of tiles_c tile columns) whose
+// bf16 values sit in `stage` as TMA loaded them (two 64-column halves,
+// 128-byte swizzle): its row-wise and / or column-wise codes and scales; the
+// codes replace the bf16 tile in the stage and thread 0 issues their TMA
+// stores (the caller commits them).  Called by every thread of the CTA.
+template <int KIND, int FMT, bool ROW, bool COL, bool GSQ>
+__device__ __forceinline__ void tile_body(const QuantArgs& a, const CUtensorMap* tmrow, const CUtensorMap* tmcol,
+                                          uint8_t* stage, uint32_t tileid, uint32_t tiles_c, float ks,
+                                          const uint32_t (&pre_r)[2], const uint32_t (&pre_c)[2], uint32_t* colred,
+                                          uint32_t* rowred, uint32_t* red, TileCounts& cnt) {
+    constexpr bool kPerTensor = TileTraits<KIND, COL, GSQ>::kPerTensor;
+    constexpr bool kTranspose = TileTraits<KIND, COL, GSQ>::kTranspose;
+    constexpr bool kRowCodes = ROW || kTranspose;
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const int rr = t & (kTile - 1), hh = t >> 7;  // row path: row and 64-column half of the tile
+    const uint32_t tr = tileid / tiles_c, tc = tileid - tr * tiles_c;
+    const int64_t r0 = (int64_t)tr * kTile, c0 = (int64_t)tc * kTile;
+    // the tile's place in the whole tensor (a block of rows starts at row0)
+    const int64_t trg = (int64_t)tr + a.row0 / kTile, r0g = a.row0 + r0;
+    const int64_t tileg = trg * (int64_t)tiles_c + tc;
+    uint32_t& nsat_row = cnt.sat_row;
+    uint32_t& nsat_col = cnt.sat_col;
+    uint32_t& nnf = cnt.nonfinite;
+    uint32_t& tmax_all = cnt.tmax;
+    (void)kPerTensor;
+    (void)lane;
+    (void)warp;
+    (void)r0;
+    (void)tileg;
+    (void)ks;
+    (void)pre_r;
+    (void)pre_c;
+    (void)tmax_all;
+    (void)nsat_col;
+    (void)red;
+    (void)rowred;
+    (void)colred;
+    // ---------------- analysis: row rr, columns 64 hh .. 64 hh + 63 of the tile
+    const uint8_t* half = stage + hh * (kStageBytes / 2);
+    uint4 v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = *(const uint4*)(half + swz(rr, j));
+    uint32_t vnf = 0;       // bit j: vector j holds a NaN / Inf
+    uint32_t mq[2];         // MX: the two 1x32 blocks' maxima; else mq[0] = the half-row maximum
+    uint32_t mh[2];         // the maxima of vectors 0-3 and 4-7 (NaN / Inf-free halves)
+    {
+        const uint32_t p0 = max_u16x2(max_u16x2(vec_pmax(v[0]), vec_pmax(v[1])),
+                                      max_u16x2(vec_pmax(v[2]), vec_pmax(v[3])));
+        const uint32_t p1 = max_u16x2(max_u16x2(vec_pmax(v[4]), vec_pmax(v[5])),
+                                      max_u16x2(vec_pmax(v[6]), vec_pmax(v[7])));
+        mh[0] = fold16(p0);
+        mh[1] = fold16(p1);
+        if (KIND == kMX || (KIND == kGen && a.bc == 32)) {
+            mq[0] = fold16(p0);
+            mq[1] = fold16(p1);
+            if (mq[0] >= 0x7F80u || mq[1] >= 0x7F80u) {
+                Row8 r;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) r.v[j] = v[j];
+                if (mq[0] >= 0x7F80u) {
+                    const MaxNf e = exact_max_rare<0, 4>(r);
+                    mq[0] = e.m;
+                    nnf += e.nnf;
+                    vnf |= e.vnf;
+                }
+                if (mq[1] >= 0x7F80u) {
+                    const MaxNf e = exact_max_rare<4, 8>(r);
+                    mq[1] = e.m;
+                    nnf += e.nnf;
+                    vnf |= e.vnf;
+                }
+            }
+        } else {
+            mq[0] = fold16(max_u16x2(p0, p1));
+            if (mq[0] >= 0x7F80u) {
+                Row8 r;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) r.v[j] = v[j];
+                const MaxNf e = exact_max_rare<0, 8>(r);
+                mq[0] = e.m;
+                nnf += e.nnf;
+                vnf |= e.vnf;
+            }
+            mq[1] = mq[0];
+        }
+    }
+
+    // ---------------- block scales
+    float kq[2] = {ks, ks};
+    if constexpr (KIND == kDel) {
+        tmax_all = tmax_all > mq[0] ? tmax_all : mq[0];
+    } else if constexpr (KIND == kB128) {
+        const uint32_t m = warp_max_u32(mq[0]);
+        if (lane == 0) red[warp] = m;
+        __syncthreads();
+        uint32_t mm = 0;
+#pragma unroll
+        for (int w = 0; w < kThreads / 32; ++w) mm = mm > red[w] ? mm : red[w];
+        kq[0] = kq[1] = block_scale<FMT>(__uint_as_float(mm << 16));
+        if (t == 0) {
+            if (ROW) ((float*)a.s_row)[tileg] = kq[0];
+            if (COL) ((float*)a.s_col)[tc * a.tiles_r_total + trg] = kq[0];
+        }
+    } else if constexpr (KIND == kB1) {
+        rowred[hh * kTile + rr] = mq[0];
+        __syncthreads();
+        const uint32_t m = max(rowred[rr], rowred[kTile + rr]);
+        mq[0] = mq[1] = m;
+        kq[0] = kq[1] = block_scale<FMT>(__uint_as_float(m << 16));
+        if (ROW && hh == 0) ((float*)a.s_row)[tc * (a.tiles_r_total * kTile) + r0g + rr] = kq[0];
+    } else if constexpr (KIND == kPC) {
+        // the row's maximum over all of x (the amax pass left it in s_row as
+        // bf16 magnitude bits): s = fmax / amax, the per-tensor current rule
+        if constexpr (ROW) {
+            const uint32_t m = pre_r[0];
+            mq[0] = mq[1] = m;
+            kq[0] = kq[1] = pertensor_scale<FMT>(__uint_as_float(m << 16));
+        }
+    } else if constexpr (KIND == kGen) {
+        // the blocks' maxima over all of x (the amax pass left them in the
+        // scale buffers as bf16 magnitude bits); rows and columns past x read 0
+        if constexpr (kRowCodes) {
+            mq[0] = pre_r[0];
+            mq[1] = pre_r[1];
+            kq[0] = block_scale<FMT>(__uint_as_float(pre_r[0] << 16));
+            kq[1] = block_scale<FMT>(__uint_as_float(pre_r[1] << 16));
+        }
+    } else if constexpr (KIND == kMX) {
+        const int e0 = mx_exponent<FMT>(mq[0] << 16), e1 = mx_exponent<FMT>(mq[1] << 16);
+        kq[0] = exp2_neg(e0);
+        kq[1] = exp2_neg(e1);
+        if (ROW) {
+            // this row's scale columns 4 tc + 2 hh + {0, 1} in the 128x4 tile (tr, tc)
+            uint8_t* tileb = (uint8_t*)a.s_row + (size_t)tileg * 512;
+            *(uint16_t*)(tileb + (rr & 31) * 16 + (rr >> 5) * 4 + 2 * hh) =
+                (uint16_t)((uint32_t)(e0 + 127) | ((uint32_t)(e1 + 127) << 8));
+        }
+    }
+
+    // ---------------- row-wise codes
+    uint2 q[8];
+    uint32_t nsat_rc = 0;
+    if constexpr (kRowCodes) {
+        const bool two = KIND == kMX || (KIND == kGen && a.bc == 32);  // two blocks in this half row
+        const Factor f0 = make_factor<KIND>(kq[0]);
+        const Factor f1 = two ? make_factor<KIND>(kq[1]) : f0;
+        const bool s0 = may_saturate<KIND, FMT>(mq[0], f0);
+        const bool s1 = two ? may_saturate<KIND, FMT>(mq[1], f1) : s0;
+        if (vnf == 0 && f0.fast && f1.fast) {  // the common case: one straight-line block
+            const Factor2 g0 = pair_factor(f0, f0), g1 = pair_factor(f1, f1);
+            constexpr bool kAtMax = KIND == kCur || KIND == kB1 || KIND == kB128 || KIND == kPC || KIND == kGen;
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                q[j] = convert8_packed<KIND, FMT>(v[j], (j < 4) ? g0 : g1, nsat_rc,
+                                                  kAtMax ? false : ((j < 4) ? s0 : s1));
+            if (kAtMax) {  // only elements equal to the block maximum can saturate
+                if (s0 && mh[0] == mq[0]) nsat_rc += count_at_max<0, 4>(v, mq[0]);
+                if (s1 && mh[1] == mq[1]) nsat_rc += count_at_max<4, 8>(v, mq[1]);
+            }
+        } else {
+            Row8 r;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) r.v[j] = v[j];
+            const RowCodes rc = row_codes_rare<KIND, FMT>(r, vnf, f0, f1, s0, s1);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) q[j] = rc.q[j];
+            nsat_rc += rc.nsat;
+        }
+        if (ROW) nsat_row += nsat_rc;  // a transposed column copy reports no count of its own
+    }
+    // the stage takes the codes once every thread has read its bf16 tile:
+    // after the block-maximum barrier (128x128; 1x128 without a column
+    // copy), after the column-block barrier (1x128), else after one more
+    uint8_t* rowt = stage;                  // [128 rows][128 codes], 128-byte swizzle
+    uint8_t* colt = stage + kTile * kTile;  // [128 columns][128 codes], 128-byte swizzle
+    auto put_row_codes = [&]() {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+            *(uint4*)(rowt + swz(rr, 4 * hh + c)) = make_uint4(q[2 * c].x, q[2 * c].y, q[2 * c + 1].x, q[2 * c + 1].y);
+    };
+    constexpr bool kCodesAfterBlockMax = KIND == kB128 || (KIND == kB1 && !COL);
+    if constexpr (kRowCodes && kCodesAfterBlockMax) put_row_codes();
+
+    // ---------------- column-wise codes re-quantized along the columns (1x128, MXFP8, per channel)
+    const int p = t & 63, qd = t >> 6;  // column pair 2p, 2p + 1; rows 32 qd .. 32 qd + 31
+    uint32_t o0[8], o1[8];
+    if constexpr (COL && !kTranspose) {
+        // columns 2p, 2p+1 sit in half p / 32, chunk (2p % 64) / 8, bytes (2p % 8) * 2
+        const uint8_t* chalf = stage + (p >> 5) * (kStageBytes / 2) + ((2 * p) & 7) * 2;
+        const int chunk = ((2 * p) & 63) >> 3;
+        uint32_t w[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) w[j] = *(const uint32_t*)(chalf + swz(32 * qd + j, chunk));
+        float k0, k1;
+        uint32_t m0, m1, own0, own1;  // column block maxima; this thread's 32-row maxima
+        bool col_nf;                   // a NaN / Inf among these 64 elements
+        uint32_t pmg[4];               // packed maxima of rows 8g .. 8g + 7
+        {
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                uint32_t x = w[8 * g] & 0x7FFF7FFFu;
+#pragma unroll
+                for (int i = 1; i < 8; ++i) x = max_u16x2(x, w[8 * g + i] & 0x7FFF7FFFu);
+                pmg[g] = x;
+            }
+            const uint32_t pm = max_u16x2(max_u16x2(pmg[0], pmg[1]), max_u16x2(pmg[2], pmg[3]));
+            m0 = pm & 0xFFFFu;
+            m1 = pm >> 16;
+            own0 = m0;
+            own1 = m1;
+            col_nf = m0 >= 0x7F80u || m1 >= 0x7F80u;
+            if (col_nf) {  // NaN / Inf: exact finite maxima
+                Col32 cw;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) cw.w[j] = w[j];
+                const uint2 m = col_exact_max_rare(cw);
+                m0 = m.x;
+                m1 = m.y;
+            }
+            const int64_t cc = c0 + 2 * p;
+            if constexpr (KIND == kMX) {
+                const int e0 = mx_exponent<FMT>(m0 << 16), e1 = mx_exponent<FMT>(m1 << 16);
+                k0 = exp2_neg(e0);
+                k1 = exp2_neg(e1);
+                // column-wise scales: logical [C][ceil(R/32)], tiles over (c/128, kb/4)
+                uint8_t* tileb = (uint8_t*)a.s_col + ((size_t)tc * a.tiles_r_total + trg) * 512;
+                const int cr = 2 * p;
+                tileb[(cr & 31) * 16 + (cr >> 5) * 4 + qd] = (uint8_t)(e0 + 127);
+                tileb[((cr + 1) & 31) * 16 + ((cr + 1) >> 5) * 4 + qd] = (uint8_t)(e1 + 127);
+            } else if constexpr (KIND == kGen) {
+                // blocks of bc rows of one column (1 x bc blocks of x^T): their maxima
+                // from the amax pass, in s_col [ceil(R/bc)][Cp]; rows past x read 0
+                m0 = pre_c[0];
+                m1 = pre_c[1];
+                k0 = block_scale<FMT>(__uint_as_float(m0 << 16));
+                k1 = block_scale<FMT>(__uint_as_float(m1 << 16));
+            } else if constexpr (KIND == kPC) {
+                // the columns' maxima over all of x (from the amax pass, in s_col)
+                m0 = pre_c[0];
+                m1 = pre_c[1];
+                k0 = pertensor_scale<FMT>(__uint_as_float(m0 << 16));
+                k1 = pertensor_scale<FMT>(__uint_as_float(m1 << 16));
+            } else {  // 1x128 along the rows of x: reduce the four quarters
+                colred[qd * kTile + 2 * p] = m0;
+                colred[qd * kTile + 2 * p + 1] = m1;
+                __syncthreads();  // also: every bf16 read of the tile is done
+                if constexpr (kRowCodes) put_row_codes();
+                m0 = max(max(colred[2 * p], colred[kTile + 2 * p]),
+                         max(colred[2 * kTile + 2 * p], colred[3 * kTile + 2 * p]));
+                m1 = max(max(colred[2 * p + 1], colred[kTile + 2 * p + 1]),
+                         max(colred[2 * kTile + 2 * p + 1], colred[3 * kTile + 2 * p + 1]));
+                k0 = block_scale<FMT>(__uint_as_float(m0 << 16));
+                k1 = block_scale<FMT>(__uint_as_float(m1 << 16));
+                if (qd == 0) {
+                    const int64_t Cp = a.tiles_c * kTile;
+                    float* sc = (float*)a.s_col + trg * Cp + cc;
+                    sc[0] = k0;
+                    sc[1] = k1;
+                }
+            }
+        }
+        // convert 32 rows of columns 2p, 2p+1
+        uint32_t ns = 0;
+        const Factor f0 = make_factor<KIND>(k0), f1 = make_factor<KIND>(k1);
+        if (!col_nf && f0.fast && f1.fast) {
+            const bool c0s = may_saturate<KIND, FMT>(m0, f0), c1s = may_saturate<KIND, FMT>(m1, f1);
+            const Factor2 g = pair_factor(f0, f1);  // lanes: column 2p, column 2p + 1
+#pragma unroll
+            for (int j = 0; j < 32; j += 4) {
+                const float2 y0 = apply2<KIND>(bf16x2_f32(w[j]), g), y1 = apply2<KIND>(bf16x2_f32(w[j + 1]), g);
+                const float2 y2 = apply2<KIND>(bf16x2_f32(w[j + 2]), g), y3 = apply2<KIND>(bf16x2_f32(w[j + 3]), g);
+                if (KIND != kB1 && KIND != kPC && KIND != kGen)
+                    ns += sat2<FMT>(y0, c0s, c1s) + sat2<FMT>(y1, c0s, c1s) + sat2<FMT>(y2, c0s, c1s) +
+                          sat2<FMT>(y3, c0s, c1s);
+                o0[j / 4] = cvt4_applied<KIND, FMT>(y0.x, y1.x, y2.x, y3.x);
+                o1[j / 4] = cvt4_applied<KIND, FMT>(y0.y, y1.y, y2.y, y3.y);
+            }
+            if ((KIND == kB1 || KIND == kPC || KIND == kGen) && ((c0s && own0 == m0) || (c1s && own1 == m1))) {
+                // only elements equal to the block maximum can saturate (count_at_max),
+                // looked for in the 8-row groups whose maximum it is
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    const bool lo = c0s && (pmg[g] & 0xFFFFu) == m0, hi = c1s && (pmg[g] >> 16) == m1;
+                    if (lo || hi) {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            ns += (lo && (w[8 * g + i] & 0x7FFFu) == m0) + (hi && ((w[8 * g + i] >> 16) & 0x7FFFu) == m1);
+                    }
+                }
+            }
+        } else {
+            Col32 cw;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) cw.w[j] = w[j];
+            const ColCodes cc2 = col_codes_rare<KIND, FMT>(cw, k0, k1);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                o0[j] = cc2.o0[j];
+                o1[j] = cc2.o1[j];
+            }
+            ns += cc2.ns;
+        }
+        nsat_col += ns;
+    }
+
+    // ---------------- codes into the stage (its bf16 tile is consumed), then TMA stores
+    if constexpr (!kCodesAfterBlockMax && KIND != kB1) {
+        __syncthreads();
+        if constexpr (kRowCodes) put_row_codes();
+    }
+    if constexpr (kTranspose) {
+        __syncthreads();
+#pragma unroll
+        for (int j = 0; j < 32; j += 4) {
+            const int r = 32 * qd + j;
+            transpose4(code_pair(rowt, r, 2 * p), code_pair(rowt, r + 1, 2 * p), code_pair(rowt, r + 2, 2 * p),
+                       code_pair(rowt, r + 3, 2 * p), o0[j / 4], o1[j / 4]);
+        }
+    }
+    if constexpr (COL) {
+        *(uint4*)(colt + swz(2 * p, 2 * qd)) = make_uint4(o0[0], o0[1], o0[2], o0[3]);
+        *(uint4*)(colt + swz(2 * p, 2 * qd + 1)) = make_uint4(o0[4], o0[5], o0[6], o0[7]);
+        *(uint4*)(colt + swz(2 * p + 1, 2 * qd)) = make_uint4(o1[0], o1[1], o1[2], o1[3]);
+        *(uint4*)(colt + swz(2 * p + 1, 2 * qd + 1)) = make_uint4(o1[4], o1[5], o1[6], o1[7]);
+    }
+    fence_async_smem();
+    __syncthreads();
+    if (t == 0) {
+        if (ROW) tma_store_2d(tmrow, (int)c0, (int)r0g, smem_u32(rowt));
+        if (COL) tma_store_2d(tmcol, (int)r0g, (int)c0, smem_u32(colt));
+    }
+}
+
 // GSQ (generic blocks only): the blocks are square (b x b), else 1 x b; the
 // block width b is a.bc, read at run time.
 template <int KIND, int FMT, bool ROW, bool COL, bool GSQ = false>
 __global__ void __launch_bounds__(kThreads, 2)
     quant_tile_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmrow,
                       const __grid_constant__ CUtensorMap tmcol, QuantArgs a) {
-    constexpr bool kPerTensor = (KIND == kCur || KIND == kDel);
-    // the column copy of a recipe whose scale does not depend on the copy's
-    // direction is the byte transpose of the row codes
-    constexpr bool kTranspose = COL && (kPerTensor || KIND == kB128 || (KIND == kGen && GSQ));
-    constexpr bool kRowCodes = ROW || kTranspose;
+    constexpr bool kPerTensor = TileTraits<KIND, COL, GSQ>::kPerTensor;
     extern __shared__ uint8_t qsmem_raw[];
     uint8_t* qsmem = (uint8_t*)(((uintptr_t)qsmem_raw + 1023) & ~(uintptr_t)1023);
     const uint32_t sbase = smem_u32(qsmem);
@@ -413,8 +818,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     __shared__ __align__(8) uint64_t bars[kStages];
     __shared__ int abort_flag;
 
-    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-    const int rr = t & (kTile - 1), hh = t >> 7;  // row path: row and 64-column half of the tile
+    const int t = threadIdx.x, lane = t & 31;
     const uint32_t ntiles = (uint32_t)(a.tiles_r * a.tiles_c), tiles_c = (uint32_t)a.tiles_c;
     auto bar = [&](int s) { return smem_u32(&bars[s]); };
 
@@ -456,353 +860,16 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
     }
 
-    uint32_t nsat_row = 0, nsat_col = 0, nnf = 0, tmax_all = 0;
+    TileCounts cnt = {0u, 0u, 0u, 0u};
     uint32_t it = 0, stg = 0, ph = 0;
     for (uint32_t tileid = blockIdx.x; tileid < ntiles; tileid += gridDim.x, ++it) {
-        const uint32_t tr = tileid / tiles_c, tc = tileid - tr * tiles_c;
-        const int64_t r0 = (int64_t)tr * kTile, c0 = (int64_t)tc * kTile;
-        // the tile's place in the whole tensor (a block of rows starts at row0)
-        const int64_t trg = (int64_t)tr + a.row0 / kTile, r0g = a.row0 + r0;
-        const int64_t tileg = trg * (int64_t)tiles_c + tc;
-        // per-channel and generic blocks: the maxima the amax pass left in the
-        // scale buffers, loaded before the tile's wait so that their latency
-        // overlaps it (pre_r: this thread's row path, two 32-column blocks;
-        // pre_c: its column pair); rows and columns past x read 0
         uint32_t pre_r[2] = {0u, 0u}, pre_c[2] = {0u, 0u};
-        if constexpr (KIND == kPC) {
-            if constexpr (ROW) pre_r[0] = pre_r[1] = ((const uint32_t*)a.s_row)[r0g + rr];
-            if constexpr (COL && !kTranspose) {
-                const int64_t cc = c0 + 2 * (t & 63);
-                pre_c[0] = ((const uint32_t*)a.s_col)[cc];
-                pre_c[1] = ((const uint32_t*)a.s_col)[cc + 1];
-            }
-        } else if constexpr (KIND == kGen) {
-            const int bc = a.bc;
-            if constexpr (kRowCodes) {
-                const int64_t rg = r0g + rr, cf = c0 + 64 * hh;  // row; first column of this half
-                const int64_t nbc = (a.C + bc - 1) / bc;
-#pragma unroll
-                for (int i = 0; i < 2; ++i) {
-                    const int64_t cc = cf + 32 * i;
-                    if (rg < a.R_total && cc < a.C && (i == 0 || bc == 32)) {
-                        const int64_t bj = cc / bc;
-                        if constexpr (GSQ) {
-                            const int64_t nbr = (a.R_total + bc - 1) / bc, bi = rg / bc;
-                            pre_r[i] = ROW ? ((const uint32_t*)a.s_row)[bi * nbc + bj]
-                                           : ((const uint32_t*)a.s_col)[bj * nbr + bi];
-                        } else {
-                            pre_r[i] = ((const uint32_t*)a.s_row)[bj * (a.tiles_r_total * kTile) + rg];
-                        }
-                    }
-                }
-                if (bc != 32) pre_r[1] = pre_r[0];
-            }
-            if constexpr (COL && !kTranspose) {
-                const int64_t rq = r0g + 32 * (t >> 6), cc = c0 + 2 * (t & 63);
-                if (rq < a.R_total) {
-                    const uint32_t* sc = (const uint32_t*)a.s_col + (rq / bc) * (a.tiles_c * kTile) + cc;
-                    pre_c[0] = sc[0];
-                    pre_c[1] = sc[1];
-                }
-            }
-        }
+        tile_maxima<KIND, ROW, COL, GSQ>(a, tileid, tiles_c, pre_r, pre_c);
         const bool ok = mbar_wait_bounded(bar(stg), ph, &abort_flag, &g_quant_errors, 2u, a.wait_ns);
         if (__syncthreads_or(!ok)) break;  // the whole CTA leaves together
-        uint8_t* stage = qsmem + stg * kStageBytes;
-
-        // ---------------- analysis: row rr, columns 64 hh .. 64 hh + 63 of the tile
-        const uint8_t* half = stage + hh * (kStageBytes / 2);
-        uint4 v[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) v[j] = *(const uint4*)(half + swz(rr, j));
-        uint32_t vnf = 0;       // bit j: vector j holds a NaN / Inf
-        uint32_t mq[2];         // MX: the two 1x32 blocks' maxima; else mq[0] = the half-row maximum
-        uint32_t mh[2];         // the maxima of vectors 0-3 and 4-7 (NaN / Inf-free halves)
-        {
-            const uint32_t p0 = max_u16x2(max_u16x2(vec_pmax(v[0]), vec_pmax(v[1])),
-                                          max_u16x2(vec_pmax(v[2]), vec_pmax(v[3])));
-            const uint32_t p1 = max_u16x2(max_u16x2(vec_pmax(v[4]), vec_pmax(v[5])),
-                                          max_u16x2(vec_pmax(v[6]), vec_pmax(v[7])));
-            mh[0] = fold16(p0);
-            mh[1] = fold16(p1);
-            if (KIND == kMX || (KIND == kGen && a.bc == 32)) {
-                mq[0] = fold16(p0);
-                mq[1] = fold16(p1);
-                if (mq[0] >= 0x7F80u || mq[1] >= 0x7F80u) {
-                    Row8 r;
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) r.v[j] = v[j];
-                    if (mq[0] >= 0x7F80u) {
-                        const MaxNf e = exact_max_rare<0, 4>(r);
-                        mq[0] = e.m;
-                        nnf += e.nnf;
-                        vnf |= e.vnf;
-                    }
-                    if (mq[1] >= 0x7F80u) {
-                        const MaxNf e = exact_max_rare<4, 8>(r);
-                        mq[1] = e.m;
-                        nnf += e.nnf;
-                        vnf |= e.vnf;
-                    }
-                }
-            } else {
-                mq[0] = fold16(max_u16x2(p0, p1));
-                if (mq[0] >= 0x7F80u) {
-                    Row8 r;
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) r.v[j] = v[j];
-                    const MaxNf e = exact_max_rare<0, 8>(r);
-                    mq[0] = e.m;
-                    nnf += e.nnf;
-                    vnf |= e.vnf;
-                }
-                mq[1] = mq[0];
-            }
-        }
-
-        // ---------------- block scales
-        float kq[2] = {ks, ks};
-        if constexpr (KIND == kDel) {
-            tmax_all = tmax_all > mq[0] ? tmax_all : mq[0];
-        } else if constexpr (KIND == kB128) {
-            const uint32_t m = warp_max_u32(mq[0]);
-            if (lane == 0) red[warp] = m;
-            __syncthreads();
-            uint32_t mm = 0;
-#pragma unroll
-            for (int w = 0; w < kThreads / 32; ++w) mm = mm > red[w] ? mm : red[w];
-            kq[0] = kq[1] = block_scale<FMT>(__uint_as_float(mm << 16));
-            if (t == 0) {
-                if (ROW) ((float*)a.s_row)[tileg] = kq[0];
-                if (COL) ((float*)a.s_col)[tc * a.tiles_r_total + trg] = kq[0];
-            }
-        } else if constexpr (KIND == kB1) {
-            rowred[hh * kTile + rr] = mq[0];
-            __syncthreads();
-            const uint32_t m = max(rowred[rr], rowred[kTile + rr]);
-            mq[0] = mq[1] = m;
-            kq[0] = kq[1] = block_scale<FMT>(__uint_as_float(m << 16));
-            if (ROW && hh == 0) ((float*)a.s_row)[tc * (a.tiles_r_total * kTile) + r0g + rr] = kq[0];
-        } else if constexpr (KIND == kPC) {
-            // the row's maximum over all of x (the amax pass left it in s_row as
-            // bf16 magnitude bits): s = fmax / amax, the per-tensor current rule
-            if constexpr (ROW) {
-                const uint32_t m = pre_r[0];
-                mq[0] = mq[1] = m;
-                kq[0] = kq[1] = pertensor_scale<FMT>(__uint_as_float(m << 16));
-            }
-        } else if constexpr (KIND == kGen) {
-            // the blocks' maxima over all of x (the amax pass left them in the
-            // scale buffers as bf16 magnitude bits); rows and columns past x read 0
-            if constexpr (kRowCodes) {
-                mq[0] = pre_r[0];
-                mq[1] = pre_r[1];
-                kq[0] = block_scale<FMT>(__uint_as_float(pre_r[0] << 16));
-                kq[1] = block_scale<FMT>(__uint_as_float(pre_r[1] << 16));
-            }
-        } else if constexpr (KIND == kMX) {
-            const int e0 = mx_exponent<FMT>(mq[0] << 16), e1 = mx_exponent<FMT>(mq[1] << 16);
-            kq[0] = exp2_neg(e0);
-            kq[1] = exp2_neg(e1);
-            if (ROW) {
-                // this row's scale columns 4 tc + 2 hh + {0, 1} in the 128x4 tile (tr, tc)
-                uint8_t* tileb = (uint8_t*)a.s_row + (size_t)tileg * 512;
-                *(uint16_t*)(tileb + (rr & 31) * 16 + (rr >> 5) * 4 + 2 * hh) =
-                    (uint16_t)((uint32_t)(e0 + 127) | ((uint32_t)(e1 + 127) << 8));
-            }
-        }
-
-        // ---------------- row-wise codes
-        uint2 q[8];
-        uint32_t nsat_rc = 0;
-        if constexpr (kRowCodes) {
-            const bool two = KIND == kMX || (KIND == kGen && a.bc == 32);  // two blocks in this half row
-            const Factor f0 = make_factor<KIND>(kq[0]);
-            const Factor f1 = two ? make_factor<KIND>(kq[1]) : f0;
-            const bool s0 = may_saturate<KIND, FMT>(mq[0], f0);
-            const bool s1 = two ? may_saturate<KIND, FMT>(mq[1], f1) : s0;
-            if (vnf == 0 && f0.fast && f1.fast) {  // the common case: one straight-line block
-                const Factor2 g0 = pair_factor(f0, f0), g1 = pair_factor(f1, f1);
-                constexpr bool kAtMax = KIND == kCur || KIND == kB1 || KIND == kB128 || KIND == kPC || KIND == kGen;
-#pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    q[j] = convert8_packed<KIND, FMT>(v[j], (j < 4) ? g0 : g1, nsat_rc,
-                                                      kAtMax ? false : ((j < 4) ? s0 : s1));
-                if (kAtMax) {  // only elements equal to the block maximum can saturate
-                    if (s0 && mh[0] == mq[0]) nsat_rc += count_at_max<0, 4>(v, mq[0]);
-                    if (s1 && mh[1] == mq[1]) nsat_rc += count_at_max<4, 8>(v, mq[1]);
-                }
-            } else {
-                Row8 r;
-#pragma unroll
-                for (int j = 0; j < 8; ++j) r.v[j] = v[j];
-                const RowCodes rc = row_codes_rare<KIND, FMT>(r, vnf, f0, f1, s0, s1);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) q[j] = rc.q[j];
-                nsat_rc += rc.nsat;
-            }
-            if (ROW) nsat_row += nsat_rc;  // a transposed column copy reports no count of its own
-        }
-        // the stage takes the codes once every thread has read its bf16 tile:
-        // after the block-maximum barrier (128x128; 1x128 without a column
-        // copy), after the column-block barrier (1x128), else after one more
-        uint8_t* rowt = stage;                  // [128 rows][128 codes], 128-byte swizzle
-        uint8_t* colt = stage + kTile * kTile;  // [128 columns][128 codes], 128-byte swizzle
-        auto put_row_codes = [&]() {
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-                *(uint4*)(rowt + swz(rr, 4 * hh + c)) = make_uint4(q[2 * c].x, q[2 * c].y, q[2 * c + 1].x, q[2 * c + 1].y);
-        };
-        constexpr bool kCodesAfterBlockMax = KIND == kB128 || (KIND == kB1 && !COL);
-        if constexpr (kRowCodes && kCodesAfterBlockMax) put_row_codes();
-
-        // ---------------- column-wise codes re-quantized along the columns (1x128, MXFP8, per channel)
-        const int p = t & 63, qd = t >> 6;  // column pair 2p, 2p + 1; rows 32 qd .. 32 qd + 31
-        uint32_t o0[8], o1[8];
-        if constexpr (COL && !kTranspose) {
-            // columns 2p, 2p+1 sit in half p / 32, chunk (2p % 64) / 8, bytes (2p % 8) * 2
-            const uint8_t* chalf = stage + (p >> 5) * (kStageBytes / 2) + ((2 * p) & 7) * 2;
-            const int chunk = ((2 * p) & 63) >> 3;
-            uint32_t w[32];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) w[j] = *(const uint32_t*)(chalf + swz(32 * qd + j, chunk));
-            float k0, k1;
-            uint32_t m0, m1, own0, own1;  // column block maxima; this thread's 32-row maxima
-            bool col_nf;                   // a NaN / Inf among these 64 elements
-            uint32_t pmg[4];               // packed maxima of rows 8g .. 8g + 7
-            {
-#pragma unroll
-                for (int g = 0; g < 4; ++g) {
-                    uint32_t x = w[8 * g] & 0x7FFF7FFFu;
-#pragma unroll
-                    for (int i = 1; i < 8; ++i) x = max_u16x2(x, w[8 * g + i] & 0x7FFF7FFFu);
-                    pmg[g] = x;
-                }
-                const uint32_t pm = max_u16x2(max_u16x2(pmg[0], pmg[1]), max_u16x2(pmg[2], pmg[3]));
-                m0 = pm & 0xFFFFu;
-                m1 = pm >> 16;
-                own0 = m0;
-                own1 = m1;
-                col_nf = m0 >= 0x7F80u || m1 >= 0x7F80u;
-                if (col_nf) {  // NaN / Inf: exact finite maxima
-                    Col32 cw;
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) cw.w[j] = w[j];
-                    const uint2 m = col_exact_max_rare(cw);
-                    m0 = m.x;
-                    m1 = m.y;
-                }
-                const int64_t cc = c0 + 2 * p;
-                if constexpr (KIND == kMX) {
-                    const int e0 = mx_exponent<FMT>(m0 << 16), e1 = mx_exponent<FMT>(m1 << 16);
-                    k0 = exp2_neg(e0);
-                    k1 = exp2_neg(e1);
-                    // column-wise scales: logical [C][ceil(R/32)], tiles over (c/128, kb/4)
-                    uint8_t* tileb = (uint8_t*)a.s_col + ((size_t)tc * a.tiles_r_total + trg) * 512;
-                    const int cr = 2 * p;
-                    tileb[(cr & 31) * 16 + (cr >> 5) * 4 + qd] = (uint8_t)(e0 + 127);
-                    tileb[((cr + 1) & 31) * 16 + ((cr + 1) >> 5) * 4 + qd] = (uint8_t)(e1 + 127);
-                } else if constexpr (KIND == kGen) {
-                    // blocks of bc rows of one column (1 x bc blocks of x^T): their maxima
-                    // from the amax pass, in s_col [ceil(R/bc)][Cp]; rows past x read 0
-                    m0 = pre_c[0];
-                    m1 = pre_c[1];
-                    k0 = block_scale<FMT>(__uint_as_float(m0 << 16));
-                    k1 = block_scale<FMT>(__uint_as_float(m1 << 16));
-                } else if constexpr (KIND == kPC) {
-                    // the columns' maxima over all of x (from the amax pass, in s_col)
-                    m0 = pre_c[0];
-                    m1 = pre_c[1];
-                    k0 = pertensor_scale<FMT>(__uint_as_float(m0 << 16));
-                    k1 = pertensor_scale<FMT>(__uint_as_float(m1 << 16));
-                } else {  // 1x128 along the rows of x: reduce the four quarters
-                    colred[qd * kTile + 2 * p] = m0;
-                    colred[qd * kTile + 2 * p + 1] = m1;
-                    __syncthreads();  // also: every bf16 read of the tile is done
-                    if constexpr (kRowCodes) put_row_codes();
-                    m0 = max(max(colred[2 * p], colred[kTile + 2 * p]),
-                             max(colred[2 * kTile + 2 * p], colred[3 * kTile + 2 * p]));
-                    m1 = max(max(colred[2 * p + 1], colred[kTile + 2 * p + 1]),
-                             max(colred[2 * kTile + 2 * p + 1], colred[3 * kTile + 2 * p + 1]));
-                    k0 = block_scale<FMT>(__uint_as_float(m0 << 16));
-                    k1 = block_scale<FMT>(__uint_as_float(m1 << 16));
-                    if (qd == 0) {
-                        const int64_t Cp = a.tiles_c * kTile;
-                        float* sc = (float*)a.s_col + trg * Cp + cc;
-                        sc[0] = k0;
-                        sc[1] = k1;
-                    }
-                }
-            }
-            // convert 32 rows of columns 2p, 2p+1
-            uint32_t ns = 0;
-            const Factor f0 = make_factor<KIND>(k0), f1 = make_factor<KIND>(k1);
-            if (!col_nf && f0.fast && f1.fast) {
-                const bool c0s = may_saturate<KIND, FMT>(m0, f0), c1s = may_saturate<KIND, FMT>(m1, f1);
-                const Factor2 g = pair_factor(f0, f1);  // lanes: column 2p, column 2p + 1
-#pragma unroll
-                for (int j = 0; j < 32; j += 4) {
-                    const float2 y0 = apply2<KIND>(bf16x2_f32(w[j]), g), y1 = apply2<KIND>(bf16x2_f32(w[j + 1]), g);
-                    const float2 y2 = apply2<KIND>(bf16x2_f32(w[j + 2]), g), y3 = apply2<KIND>(bf16x2_f32(w[j + 3]), g);
-                    if (KIND != kB1 && KIND != kPC && KIND != kGen)
-                        ns += sat2<FMT>(y0, c0s, c1s) + sat2<FMT>(y1, c0s, c1s) + sat2<FMT>(y2, c0s, c1s) +
-                              sat2<FMT>(y3, c0s, c1s);
-                    o0[j / 4] = cvt4_applied<KIND, FMT>(y0.x, y1.x, y2.x, y3.x);
-                    o1[j / 4] = cvt4_applied<KIND, FMT>(y0.y, y1.y, y2.y, y3.y);
-                }
-                if ((KIND == kB1 || KIND == kPC || KIND == kGen) && ((c0s && own0 == m0) || (c1s && own1 == m1))) {
-                    // only elements equal to the block maximum can saturate (count_at_max),
-                    // looked for in the 8-row groups whose maximum it is
-#pragma unroll
-                    for (int g = 0; g < 4; ++g) {
-                        const bool lo = c0s && (pmg[g] & 0xFFFFu) == m0, hi = c1s && (pmg[g] >> 16) == m1;
-                        if (lo || hi) {
-#pragma unroll
-                            for (int i = 0; i < 8; ++i)
-                                ns += (lo && (w[8 * g + i] & 0x7FFFu) == m0) + (hi && ((w[8 * g + i] >> 16) & 0x7FFFu) == m1);
-                        }
-                    }
-                }
-            } else {
-                Col32 cw;
-#pragma unroll
-                for (int j = 0; j < 32; ++j) cw.w[j] = w[j];
-                const ColCodes cc2 = col_codes_rare<KIND, FMT>(cw, k0, k1);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    o0[j] = cc2.o0[j];
-                    o1[j] = cc2.o1[j];
-                }
-                ns += cc2.ns;
-            }
-            nsat_col += ns;
-        }
-
-        // ---------------- codes into the stage (its bf16 tile is consumed), then TMA stores
-        if constexpr (!kCodesAfterBlockMax && KIND != kB1) {
-            __syncthreads();
-            if constexpr (kRowCodes) put_row_codes();
-        }
-        if constexpr (kTranspose) {
-            __syncthreads();
-#pragma unroll
-            for (int j = 0; j < 32; j += 4) {
-                const int r = 32 * qd + j;
-                transpose4(code_pair(rowt, r, 2 * p), code_pair(rowt, r + 1, 2 * p), code_pair(rowt, r + 2, 2 * p),
-                           code_pair(rowt, r + 3, 2 * p), o0[j / 4], o1[j / 4]);
-            }
-        }
-        if constexpr (COL) {
-            *(uint4*)(colt + swz(2 * p, 2 * qd)) = make_uint4(o0[0], o0[1], o0[2], o0[3]);
-            *(uint4*)(colt + swz(2 * p, 2 * qd + 1)) = make_uint4(o0[4], o0[5], o0[6], o0[7]);
-            *(uint4*)(colt + swz(2 * p + 1, 2 * qd)) = make_uint4(o1[0], o1[1], o1[2], o1[3]);
-            *(uint4*)(colt + swz(2 * p + 1, 2 * qd + 1)) = make_uint4(o1[4], o1[5], o1[6], o1[7]);
-        }
-        fence_async_smem();
-        __syncthreads();
+        tile_body<KIND, FMT, ROW, COL, GSQ>(a, &tmrow, &tmcol, qsmem + stg * kStageBytes, tileid, tiles_c, ks, pre_r,
+                                            pre_c, colred, rowred, red, cnt);
         if (t == 0) {
-            if (ROW) tma_store_2d(&tmrow, (int)c0, (int)r0g, smem_u32(rowt));
-            if (COL) tma_store_2d(&tmcol, (int)r0g, (int)c0, smem_u32(colt));
             bulk_commit();
             bulk_wait_read1();  // the previous tile's stores have read their stage ...
             issue(it + 2);      // ... which now takes the tile after next
@@ -823,9 +890,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
 
     // ---------------- counters (and the delayed recipe's tensor amax)
-    nsat_row = warp_sum_u32(nsat_row);
-    nsat_col = warp_sum_u32(nsat_col);
-    nnf = warp_sum_u32(nnf);
+    const uint32_t nsat_row = warp_sum_u32(cnt.sat_row);
+    const uint32_t nsat_col = warp_sum_u32(cnt.sat_col);
+    const uint32_t nnf = warp_sum_u32(cnt.nonfinite);
     if (lane == 0) {
         if (nsat_row) atomicAdd(&a.counters[0], (unsigned long long)nsat_row);
         if (nsat_col) atomicAdd(&a.counters[1], (unsigned long long)nsat_col);
@@ -833,7 +900,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             atomicAdd(&a.counters[2], (unsigned long long)nnf);  // else the amax pass
     }
     if constexpr (KIND == kDel) {
-        tmax_all = warp_max_u32(tmax_all);
+        const uint32_t tmax_all = warp_max_u32(cnt.tmax);
         if (lane == 0 && tmax_all) atomicMax((unsigned int*)a.amax, tmax_all << 16);
     }
 }
@@ -1326,6 +1393,7 @@ fp8q_status launch_quantize(const fp8q_recipe* rc, const QuantArgs& a, DelayedDe
             return FP8Q_ERR_ARG;
     }
 }
+
 
 // Fork / join of fp8q_quantize_multi: one library-owned stream per job
 // (created once per device), the tile passes' two resident CTAs per SM
