@@ -400,12 +400,22 @@ struct TileCounts {
     uint32_t sat_row, sat_col, nonfinite, tmax;
 };
 
-template <int KIND, bool COL, bool GSQ>
+// Generic blocks (KIND kGen): where the block maxima come from and the
+// blocks' shape.  Blocks of 32 or 64 lie inside a 128 x 128 tile, so the tile
+// pass finds their maxima itself (as for 1 x 128 and MXFP8); 256-wide blocks
+// span tiles and take a pass over x first, whose maxima the tile pass loads.
+enum { kGenNone = 0, kGenPass1D = 1, kGenPassSq = 2, kGenTile1D = 3, kGenTileSq = 4 };
+template <int GEN>
+constexpr bool kGenSquare = GEN == kGenPassSq || GEN == kGenTileSq;
+template <int GEN>
+constexpr bool kGenPass = GEN == kGenPass1D || GEN == kGenPassSq;
+
+template <int KIND, bool COL, int GEN>
 struct TileTraits {
     static constexpr bool kPerTensor = (KIND == kCur || KIND == kDel);
     // the column copy of a recipe whose scale does not depend on the copy's
     // direction is the byte transpose of the row codes
-    static constexpr bool kTranspose = COL && (kPerTensor || KIND == kB128 || (KIND == kGen && GSQ));
+    static constexpr bool kTranspose = COL && (kPerTensor || KIND == kB128 || (KIND == kGen && kGenSquare<GEN>));
 };
 
 // Per-channel and generic blocks: the maxima that the amax pass left in the
@@ -413,10 +423,10 @@ struct TileTraits {
 // tile's wait so that their latency overlaps it (pre_r: the row path's two
 // 32-column blocks; pre_c: the column path's column pair).  Nothing for the
 // other recipes.
-template <int KIND, bool ROW, bool COL, bool GSQ>
+template <int KIND, bool ROW, bool COL, int GEN>
 __device__ __forceinline__ void tile_maxima(const QuantArgs& a, uint32_t tileid, uint32_t tiles_c,
                                             uint32_t (&pre_r)[2], uint32_t (&pre_c)[2]) {
-    constexpr bool kTranspose = TileTraits<KIND, COL, GSQ>::kTranspose;
+    constexpr bool kTranspose = TileTraits<KIND, COL, GEN>::kTranspose;
     constexpr bool kRowCodes = ROW || kTranspose;
     const int t = threadIdx.x, rr = t & (kTile - 1), hh = t >> 7;
     const uint32_t tr = tileid / tiles_c, tc = tileid - tr * tiles_c;
@@ -437,18 +447,18 @@ __device__ __forceinline__ void tile_maxima(const QuantArgs& a, uint32_t tileid,
             pre_c[0] = ((const uint32_t*)a.s_col)[cc];
             pre_c[1] = ((const uint32_t*)a.s_col)[cc + 1];
         }
-    } else if constexpr (KIND == kGen) {
-        const int bc = a.bc;
+    } else if constexpr (KIND == kGen && kGenPass<GEN>) {
+        const int bc = a.bc, sh = __ffs(bc) - 1;  // b is a power of two
         if constexpr (kRowCodes) {
             const int64_t rg = r0g + rr, cf = c0 + 64 * hh;  // row; first column of this half
-            const int64_t nbc = (a.C + bc - 1) / bc;
+            const int64_t nbc = (a.C + bc - 1) >> sh;
 #pragma unroll
             for (int i = 0; i < 2; ++i) {
                 const int64_t cc = cf + 32 * i;
                 if (rg < a.R_total && cc < a.C && (i == 0 || bc == 32)) {
-                    const int64_t bj = cc / bc;
-                    if constexpr (GSQ) {
-                        const int64_t nbr = (a.R_total + bc - 1) / bc, bi = rg / bc;
+                    const int64_t bj = cc >> sh;
+                    if constexpr (kGenSquare<GEN>) {
+                        const int64_t nbr = (a.R_total + bc - 1) >> sh, bi = rg >> sh;
                         pre_r[i] = ROW ? ((const uint32_t*)a.s_row)[bi * nbc + bj]
                                        : ((const uint32_t*)a.s_col)[bj * nbr + bi];
                     } else {
@@ -461,7 +471,7 @@ __device__ __forceinline__ void tile_maxima(const QuantArgs& a, uint32_t tileid,
         if constexpr (COL && !kTranspose) {
             const int64_t rq = r0g + 32 * (t >> 6), cc = c0 + 2 * (t & 63);
             if (rq < a.R_total) {
-                const uint32_t* sc = (const uint32_t*)a.s_col + (rq / bc) * (a.tiles_c * kTile) + cc;
+                const uint32_t* sc = (const uint32_t*)a.s_col + (rq >> sh) * (a.tiles_c * kTile) + cc;
                 pre_c[0] = sc[0];
                 pre_c[1] = sc[1];
             }
@@ -474,13 +484,13 @@ __device__ __forceinline__ void tile_maxima(const QuantArgs& a, uint32_t tileid,
 // 128-byte swizzle): its row-wise and / or column-wise codes and scales; the
 // codes replace the bf16 tile in the stage and thread 0 issues their TMA
 // stores (the caller commits them).  Called by every thread of the CTA.
-template <int KIND, int FMT, bool ROW, bool COL, bool GSQ>
+template <int KIND, int FMT, bool ROW, bool COL, int GEN>
 __device__ __forceinline__ void tile_body(const QuantArgs& a, const CUtensorMap* tmrow, const CUtensorMap* tmcol,
                                           uint8_t* stage, uint32_t tileid, uint32_t tiles_c, float ks,
                                           const uint32_t (&pre_r)[2], const uint32_t (&pre_c)[2], uint32_t* colred,
                                           uint32_t* rowred, uint32_t* red, TileCounts& cnt) {
-    constexpr bool kPerTensor = TileTraits<KIND, COL, GSQ>::kPerTensor;
-    constexpr bool kTranspose = TileTraits<KIND, COL, GSQ>::kTranspose;
+    constexpr bool kPerTensor = TileTraits<KIND, COL, GEN>::kPerTensor;
+    constexpr bool kTranspose = TileTraits<KIND, COL, GEN>::kTranspose;
     constexpr bool kRowCodes = ROW || kTranspose;
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
     const int rr = t & (kTile - 1), hh = t >> 7;  // row path: row and 64-column half of the tile
@@ -587,7 +597,7 @@ __device__ __forceinline__ void tile_body(const QuantArgs& a, const CUtensorMap*
             mq[0] = mq[1] = m;
             kq[0] = kq[1] = pertensor_scale<FMT>(__uint_as_float(m << 16));
         }
-    } else if constexpr (KIND == kGen) {
+    } else if constexpr (KIND == kGen && kGenPass<GEN>) {
         // the blocks' maxima over all of x (the amax pass left them in the
         // scale buffers as bf16 magnitude bits); rows and columns past x read 0
         if constexpr (kRowCodes) {
@@ -595,6 +605,49 @@ __device__ __forceinline__ void tile_body(const QuantArgs& a, const CUtensorMap*
             mq[1] = pre_r[1];
             kq[0] = block_scale<FMT>(__uint_as_float(pre_r[0] << 16));
             kq[1] = block_scale<FMT>(__uint_as_float(pre_r[1] << 16));
+        }
+    } else if constexpr (KIND == kGen) {
+        // blocks of b = 32 or 64 inside the tile (tiles start on multiples of
+        // 128): 1 x b blocks are this half row's two 32-column pieces or all
+        // of it; b x b blocks gather the half rows of one warp (b = 32: rows
+        // 32 (warp % 4) ..) or of two (b = 64: warps w and w ^ 1)
+        const int bc = a.bc, sh = __ffs(bc) - 1;  // b is a power of two
+        if constexpr (GEN == kGenTileSq) {
+            if (bc == 32) {
+                mq[0] = warp_max_u32(mq[0]);
+                mq[1] = warp_max_u32(mq[1]);
+            } else {
+                const uint32_t m = warp_max_u32(mq[0]);
+                if (lane == 0) red[warp] = m;
+                __syncthreads();
+                mq[0] = mq[1] = max(red[warp], red[warp ^ 1]);
+            }
+        }
+        kq[0] = block_scale<FMT>(__uint_as_float(mq[0] << 16));
+        kq[1] = bc == 32 ? block_scale<FMT>(__uint_as_float(mq[1] << 16)) : kq[0];
+        const int64_t nbc = (a.C + bc - 1) >> sh, bj0 = (c0 + 64 * hh) >> sh;
+        if constexpr (GEN == kGenTile1D) {
+            // row copy's scales [ceil(C / b)][Rp]: every row of the tile, pad rows included
+            if (ROW) {
+                float* sr = (float*)a.s_row + r0g + rr;
+                const int64_t rp = a.tiles_r_total * kTile;
+                if (bj0 < nbc) sr[bj0 * rp] = kq[0];
+                if (bc == 32 && bj0 + 1 < nbc) sr[(bj0 + 1) * rp] = kq[1];
+            }
+        } else {
+            // [ceil(R / b)][ceil(C / b)] and, for the transposed column copy,
+            // [ceil(C / b)][ceil(R / b)]: one lane per block writes
+            const int64_t nbr = (a.R_total + bc - 1) >> sh, bi = (r0g + rr) >> sh;
+            if (lane == 0 && (bc == 32 || (warp & 1) == 0) && bi < nbr) {
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    if (i == 1 && bc != 32) break;
+                    if (bj0 + i < nbc) {
+                        if (ROW) ((float*)a.s_row)[bi * nbc + bj0 + i] = kq[i];
+                        if (COL) ((float*)a.s_col)[(bj0 + i) * nbr + bi] = kq[i];
+                    }
+                }
+            }
         }
     } else if constexpr (KIND == kMX) {
         const int e0 = mx_exponent<FMT>(mq[0] << 16), e1 = mx_exponent<FMT>(mq[1] << 16);
@@ -698,13 +751,33 @@ __device__ __forceinline__ void tile_body(const QuantArgs& a, const CUtensorMap*
                 const int cr = 2 * p;
                 tileb[(cr & 31) * 16 + (cr >> 5) * 4 + qd] = (uint8_t)(e0 + 127);
                 tileb[((cr + 1) & 31) * 16 + ((cr + 1) >> 5) * 4 + qd] = (uint8_t)(e1 + 127);
-            } else if constexpr (KIND == kGen) {
+            } else if constexpr (KIND == kGen && kGenPass<GEN>) {
                 // blocks of bc rows of one column (1 x bc blocks of x^T): their maxima
                 // from the amax pass, in s_col [ceil(R/bc)][Cp]; rows past x read 0
                 m0 = pre_c[0];
                 m1 = pre_c[1];
                 k0 = block_scale<FMT>(__uint_as_float(m0 << 16));
                 k1 = block_scale<FMT>(__uint_as_float(m1 << 16));
+            } else if constexpr (KIND == kGen) {
+                // blocks of b = 32 rows of one column are this thread's rows; b = 64
+                // joins the row quarters 2i, 2i + 1; scales [ceil(R / b)][Cp]
+                const int bc = a.bc, sh = __ffs(bc) - 1;  // b is a power of two
+                if (bc == 64) {
+                    colred[qd * kTile + 2 * p] = m0;
+                    colred[qd * kTile + 2 * p + 1] = m1;
+                    __syncthreads();
+                    const int q0 = qd & ~1;
+                    m0 = max(colred[q0 * kTile + 2 * p], colred[(q0 + 1) * kTile + 2 * p]);
+                    m1 = max(colred[q0 * kTile + 2 * p + 1], colred[(q0 + 1) * kTile + 2 * p + 1]);
+                }
+                k0 = block_scale<FMT>(__uint_as_float(m0 << 16));
+                k1 = block_scale<FMT>(__uint_as_float(m1 << 16));
+                const int64_t nbr = (a.R_total + bc - 1) >> sh, bi = (r0g + 32 * qd) >> sh;
+                if ((bc == 32 || (qd & 1) == 0) && bi < nbr) {
+                    float* sc = (float*)a.s_col + bi * (a.tiles_c * kTile) + cc;
+                    sc[0] = k0;
+                    sc[1] = k1;
+                }
             } else if constexpr (KIND == kPC) {
                 // the columns' maxima over all of x (from the amax pass, in s_col)
                 m0 = pre_c[0];
@@ -802,17 +875,17 @@ __device__ __forceinline__ void tile_body(const QuantArgs& a, const CUtensorMap*
     }
 }
 
-// GSQ (generic blocks only): the blocks are square (b x b), else 1 x b; the
-// block width b is a.bc, read at run time.
-template <int KIND, int FMT, bool ROW, bool COL, bool GSQ = false>
+// GEN (generic blocks only): the blocks' shape and the source of their
+// maxima (kGen* above); the block width b is a.bc, read at run time.
+template <int KIND, int FMT, bool ROW, bool COL, int GEN = kGenNone>
 __global__ void __launch_bounds__(kThreads, 2)
     quant_tile_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmrow,
                       const __grid_constant__ CUtensorMap tmcol, QuantArgs a) {
-    constexpr bool kPerTensor = TileTraits<KIND, COL, GSQ>::kPerTensor;
+    constexpr bool kPerTensor = TileTraits<KIND, COL, GEN>::kPerTensor;
     extern __shared__ uint8_t qsmem_raw[];
     uint8_t* qsmem = (uint8_t*)(((uintptr_t)qsmem_raw + 1023) & ~(uintptr_t)1023);
     const uint32_t sbase = smem_u32(qsmem);
-    __shared__ uint32_t colred[COL && KIND == kB1 ? 4 * kTile : 1];
+    __shared__ uint32_t colred[COL && (KIND == kB1 || (KIND == kGen && GEN == kGenTile1D)) ? 4 * kTile : 1];
     __shared__ uint32_t rowred[KIND == kB1 ? 2 * kTile : 1];
     __shared__ uint32_t red[kThreads / 32];
     __shared__ __align__(8) uint64_t bars[kStages];
@@ -864,10 +937,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     uint32_t it = 0, stg = 0, ph = 0;
     for (uint32_t tileid = blockIdx.x; tileid < ntiles; tileid += gridDim.x, ++it) {
         uint32_t pre_r[2] = {0u, 0u}, pre_c[2] = {0u, 0u};
-        tile_maxima<KIND, ROW, COL, GSQ>(a, tileid, tiles_c, pre_r, pre_c);
+        tile_maxima<KIND, ROW, COL, GEN>(a, tileid, tiles_c, pre_r, pre_c);
         const bool ok = mbar_wait_bounded(bar(stg), ph, &abort_flag, &g_quant_errors, 2u, a.wait_ns);
         if (__syncthreads_or(!ok)) break;  // the whole CTA leaves together
-        tile_body<KIND, FMT, ROW, COL, GSQ>(a, &tmrow, &tmcol, qsmem + stg * kStageBytes, tileid, tiles_c, ks, pre_r,
+        tile_body<KIND, FMT, ROW, COL, GEN>(a, &tmrow, &tmcol, qsmem + stg * kStageBytes, tileid, tiles_c, ks, pre_r,
                                             pre_c, colred, rowred, red, cnt);
         if (t == 0) {
             bulk_commit();
@@ -896,7 +969,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (lane == 0) {
         if (nsat_row) atomicAdd(&a.counters[0], (unsigned long long)nsat_row);
         if (nsat_col) atomicAdd(&a.counters[1], (unsigned long long)nsat_col);
-        if (KIND != kCur && KIND != kPC && KIND != kGen && nnf)
+        if (KIND != kCur && KIND != kPC && !(KIND == kGen && kGenPass<GEN>) && nnf)
             atomicAdd(&a.counters[2], (unsigned long long)nnf);  // else the amax pass
     }
     if constexpr (KIND == kDel) {
@@ -1024,7 +1097,8 @@ __global__ void __launch_bounds__(256) gen_amax_kernel(const uint16_t* x, int64_
     const int lg = bc / 8 < 32 ? bc / 8 : 32;  // lanes per block column
     const int64_t strips_c = (C + 255) / 256, strips = ((R + 63) / 64) * strips_c;
     const int64_t Rp = (R + 127) / 128 * 128, Cp = (C + 127) / 128 * 128;
-    const int64_t nbc = (C + bc - 1) / bc, nbr = (R + bc - 1) / bc;
+    const int sh = __ffs(bc) - 1;  // b is a power of two
+    const int64_t nbc = (C + bc - 1) >> sh, nbr = (R + bc - 1) >> sh;
     uint32_t nf = 0;
     for (int64_t sidx = blockIdx.x; sidx < strips; sidx += gridDim.x) {
         const int64_t rs = (sidx / strips_c) * 64, r0 = rs + 8 * warp, cs = (sidx % strips_c) * 256, c = cs + 8 * lane;
@@ -1048,14 +1122,14 @@ __global__ void __launch_bounds__(256) gen_amax_kernel(const uint16_t* x, int64_
             uint32_t m = fold16(rm);
             if constexpr (!SQ && ROW) {
                 for (int o = 1; o < lg; o <<= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-                if (lane % lg == 0 && m != 0u && r0 + i < R && c < C) atomicMax(srow + (c / bc) * Rp + r0 + i, m);
+                if (lane % lg == 0 && m != 0u && r0 + i < R && c < C) atomicMax(srow + (c >> sh) * Rp + r0 + i, m);
             }
             sq = max(sq, m);
         }
         if constexpr (SQ) {  // the warp's 8 rows lie in one block row (b >= 32)
             for (int o = 1; o < lg; o <<= 1) sq = max(sq, __shfl_xor_sync(0xFFFFFFFFu, sq, o));
             if (lane % lg == 0 && sq != 0u && c < C) {
-                const int64_t bi = r0 / bc, bj = c / bc;
+                const int64_t bi = r0 >> sh, bj = c >> sh;
                 if (ROW)
                     atomicMax(srow + bi * nbc + bj, sq);
                 else
@@ -1073,7 +1147,7 @@ __global__ void __launch_bounds__(256) gen_amax_kernel(const uint16_t* x, int64_
                 for (int g0 = 0; g0 < 8; g0 += g) {
                     uint32_t m = 0;
                     for (int w = g0; w < g0 + g; ++w) m = max_u16x2(m, cred[w][threadIdx.x]);
-                    const int64_t cc = cs + 2 * threadIdx.x, rb = (rs + 8 * g0) / bc;
+                    const int64_t cc = cs + 2 * threadIdx.x, rb = (rs + 8 * g0) >> sh;
                     if (cc < C && rs + 8 * g0 < R) {
                         if (m & 0xFFFFu) atomicMax(scol + rb * Cp + cc, m & 0xFFFFu);
                         if (m >> 16) atomicMax(scol + rb * Cp + cc + 1, m >> 16);
@@ -1213,12 +1287,12 @@ int num_sms() {
     return n > 0 ? n : 1;
 }
 
-template <int KIND, int FMT, bool ROW, bool COL, bool GSQ = false>
+template <int KIND, int FMT, bool ROW, bool COL, int GEN = kGenNone>
 fp8q_status launch_tile(const QuantArgs& args, cudaStream_t s) {
     QuantArgs a = args;
     a.stall = take_stall();
     static PerDevice<bool> attr;
-    auto kern = quant_tile_kernel<KIND, FMT, ROW, COL, GSQ>;
+    auto kern = quant_tile_kernel<KIND, FMT, ROW, COL, GEN>;
     if (!smem_opt_in(attr, kern, kTileSmem)) return FP8Q_ERR_CUDA;
     const int64_t ntiles = a.tiles_r * a.tiles_c;
     if (a.tiles_r_total * a.tiles_c >= ((int64_t)1 << 31)) return FP8Q_ERR_SHAPE;  // tiles counted in 32 bits
@@ -1246,28 +1320,32 @@ fp8q_status launch_tile(const QuantArgs& args, cudaStream_t s) {
     return cudaGetLastError() == cudaSuccess ? FP8Q_OK : FP8Q_ERR_CUDA;
 }
 
-template <int KIND, int FMT, bool GSQ = false>
+template <int KIND, int FMT, int GEN = kGenNone>
 fp8q_status launch_tile_rc(const QuantArgs& a, bool row, bool col, cudaStream_t s) {
-    if (row && col) return launch_tile<KIND, FMT, true, true, GSQ>(a, s);
-    if (row) return launch_tile<KIND, FMT, true, false, GSQ>(a, s);
-    return launch_tile<KIND, FMT, false, true, GSQ>(a, s);
+    if (row && col) return launch_tile<KIND, FMT, true, true, GEN>(a, s);
+    if (row) return launch_tile<KIND, FMT, true, false, GEN>(a, s);
+    return launch_tile<KIND, FMT, false, true, GEN>(a, s);
 }
 
-template <int KIND, bool GSQ = false>
+template <int KIND, int GEN = kGenNone>
 fp8q_status launch_tile_fmt(const QuantArgs& a, int fmt, bool row, bool col, cudaStream_t s) {
-    return fmt == FP8Q_E4M3 ? launch_tile_rc<KIND, FP8Q_E4M3, GSQ>(a, row, col, s)
-                            : launch_tile_rc<KIND, FP8Q_E5M2, GSQ>(a, row, col, s);
+    return fmt == FP8Q_E4M3 ? launch_tile_rc<KIND, FP8Q_E4M3, GEN>(a, row, col, s)
+                            : launch_tile_rc<KIND, FP8Q_E5M2, GEN>(a, row, col, s);
 }
 
-// Generic blockwise scaling of shapes other than 1 x 128 / 128 x 128: zero the
-// scale buffers, the block-amax pass into them, the tile pass (reads them),
-// then the buffers' amax bits become d (for square blocks with both copies the
-// column copy's scales are the row copy's transposed).
+// Generic blockwise scaling of shapes other than 1 x 128 / 128 x 128.  Blocks
+// of 32 or 64: the tile pass alone (block maxima inside each tile).  Blocks
+// of 256: zero the scale buffers, the block-amax pass into them, the tile
+// pass (reads them), then the buffers' amax bits become d (for square blocks
+// with both copies the column copy's scales are the row copy's transposed).
 fp8q_status launch_generic(const QuantArgs& a, int fmt, bool row, bool col, cudaStream_t s) {
     const int64_t Rp = a.tiles_r * 128, Cp = a.tiles_c * 128;
     if (Rp == 0 || Cp == 0) return FP8Q_OK;  // empty x: nothing to write
     const int bc = a.bc;
     const bool sq = a.br == a.bc;
+    if (bc <= 64)
+        return sq ? launch_tile_fmt<kGen, kGenTileSq>(a, fmt, row, col, s)
+                  : launch_tile_fmt<kGen, kGenTile1D>(a, fmt, row, col, s);
     const int64_t nbr = (a.R + bc - 1) / bc, nbc = (a.C + bc - 1) / bc;
     const int64_t row_n = sq ? nbr * nbc : nbc * Rp, col_n = sq ? nbr * nbc : nbr * Cp;
     uint32_t* rm = (uint32_t*)a.s_row;
@@ -1291,7 +1369,8 @@ fp8q_status launch_generic(const QuantArgs& a, int fmt, bool row, bool col, cuda
         gen_amax_kernel<false, false, true><<<g, 256, 0, s>>>(a.x, a.R, a.C, bc, rm, cm, a.counters);
     }
     if (cudaGetLastError() != cudaSuccess) return FP8Q_ERR_CUDA;
-    const fp8q_status r = sq ? launch_tile_fmt<kGen, true>(a, fmt, row, col, s) : launch_tile_fmt<kGen, false>(a, fmt, row, col, s);
+    const fp8q_status r = sq ? launch_tile_fmt<kGen, kGenPassSq>(a, fmt, row, col, s)
+                             : launch_tile_fmt<kGen, kGenPass1D>(a, fmt, row, col, s);
     if (r != FP8Q_OK) return r;
     auto blocks = [](int64_t n) { return (unsigned)((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096); };
     const bool e4 = fmt == FP8Q_E4M3;

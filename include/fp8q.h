@@ -184,9 +184,9 @@ FP8Q_API fp8q_status fp8q_scale_bytes(const fp8q_recipe* recipe, int64_t rows, i
  * Amax always excludes NaN / Inf.  Counters are overwritten.  BLOCK_GENERIC:
  * recipe->block_rows x block_cols must be 1 x b or b x b, b in {32, 64, 128,
  * 256} (else FP8Q_ERR_UNSUPPORTED); 1 x 128 and 128 x 128 run exactly as
- * BLOCK_1x128 and BLOCK_128x128; other shapes take a pass over x that leaves
- * every block's amax in the scale buffers (as scratch), then the cast, and the
- * scale buffers end holding d.
+ * BLOCK_1x128 and BLOCK_128x128; b = 32 and 64 take one pass over x; b = 256
+ * takes a pass over x that leaves every block's amax in the scale buffers (as
+ * scratch), then the cast.  The scale buffers end holding d.
  */
 FP8Q_API fp8q_status fp8q_quantize(const fp8q_recipe* recipe, const void* x, int64_t rows, int64_t cols,
                           fp8q_delayed_state* st, fp8q_tensor* out, void* stream);
