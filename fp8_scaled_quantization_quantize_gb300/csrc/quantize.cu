@@ -1021,56 +1021,105 @@ __device__ __forceinline__ uint32_t nonfinite2(uint32_t w) {
     return (uint32_t)((w & 0x7FFFu) >= 0x7F80u) + (uint32_t)(((w >> 16) & 0x7FFFu) >= 0x7F80u);
 }
 
+// The exact finite maxima of a thread's 8 x 8 elements of a strip (rows r0 ..
+// r0 + 7, columns c .. c + 7; column pairs cm, rows rm) and its NaN / Inf
+// count: the rare path of the per-channel amax pass, taken when a warp's
+// packed maxima flag a NaN / Inf; it loads the elements again.
+struct StripMax {
+    uint32_t cm[4], rm[8], nf;
+};
+__device__ __noinline__ StripMax strip_exact(const uint16_t* x, int64_t R, int64_t C, int64_t r0, int64_t c) {
+    StripMax e;
+    e.nf = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) e.cm[k] = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint4 v = (c < C && r0 + i < R) ? ld_nc_v4(x + (r0 + i) * C + c) : make_uint4(0u, 0u, 0u, 0u);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t rm = 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const uint32_t f = finite_mag2(w[k]);
+            e.nf += nonfinite2(w[k]);
+            e.cm[k] = max_u16x2(e.cm[k], f);
+            rm = max_u16x2(rm, f);
+        }
+        e.rm[i] = rm;
+    }
+    return e;
+}
+
 // Per-channel current scaling, pass 1: the largest finite |x| of every row
 // (rowmax[r]) and of every column (colmax[c]) of x, as bf16 magnitude bits in
 // uint32 words of the zeroed scale buffers (atomicMax merges the strips), and
-// the NaN / Inf count.  A CTA takes strips of 64 rows x 256 columns: warp w
-// rows 8w .. 8w + 7, lane l columns 8l .. 8l + 7 (one 16-byte load a row).
+// the NaN / Inf count.  CTA i walks the strips of 64 rows x 256 columns of
+// column band i % bands, rows i / bands, + the grid's CTAs per band ...:
+// warp w rows 8w .. 8w + 7, lane l columns 8l .. 8l + 7 (one 16-byte load a
+// row); the column maxima stay in registers across the walk and meet in
+// shared memory once at its end.  The common path takes the packed maxima of
+// the magnitude bits (one AND and the u16x2 maxima a word) and leaves NaN /
+// Inf to a rare exact path.
 template <bool ROW, bool COL>
-__global__ void __launch_bounds__(256) pc_amax_kernel(const uint16_t* x, int64_t R, int64_t C, uint32_t* rowmax,
-                                                      uint32_t* colmax, unsigned long long* counters) {
-    __shared__ uint32_t cred[8][128];  // per warp: column-pair maxima of its 8 rows
+__global__ void __launch_bounds__(256, 4) pc_amax_kernel(const uint16_t* x, int64_t R, int64_t C, uint32_t* rowmax,
+                                                         uint32_t* colmax, unsigned long long* counters) {
+    __shared__ uint32_t cred[8][128];  // per warp: column-pair maxima of its rows
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int64_t strips_c = (C + 255) / 256, strips = ((R + 63) / 64) * strips_c;
-    uint32_t nf = 0;
-    for (int64_t sidx = blockIdx.x; sidx < strips; sidx += gridDim.x) {
-        const int64_t r0 = (sidx / strips_c) * 64 + 8 * warp, cs = (sidx % strips_c) * 256, c = cs + 8 * lane;
+    // strips counted in 32 bits (the host refuses more than 2^31); the grid
+    // is a multiple of the band count
+    const uint32_t bands = (uint32_t)((C + 255) / 256), strips_r = (uint32_t)((R + 63) / 64);
+    const uint32_t per_band = gridDim.x / bands, band = blockIdx.x % bands;
+    const int64_t cs = (int64_t)band * 256, c = cs + 8 * lane;
+    uint32_t nf = 0, cm[4] = {0u, 0u, 0u, 0u};
+    for (uint32_t sr = blockIdx.x / bands; sr < strips_r; sr += per_band) {
+        const int64_t r0 = (int64_t)sr * 64 + 8 * warp;
         uint4 v[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i)  // C % 8 == 0: a vector is wholly inside or outside
             v[i] = (c < C && r0 + i < R) ? ld_nc_v4(x + (r0 + i) * C + c) : make_uint4(0u, 0u, 0u, 0u);
-        uint32_t cm[4] = {0u, 0u, 0u, 0u};
+        // packed maxima of the magnitude bits, NaN / Inf included (they are
+        // >= 0x7F80, so the fold of all of them flags any)
+        uint32_t sm[4] = {0u, 0u, 0u, 0u}, rm[8], all = 0;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-            uint32_t rm = 0;
+            const uint32_t M = 0x7FFF7FFFu;
+            const uint32_t w[4] = {v[i].x & M, v[i].y & M, v[i].z & M, v[i].w & M};
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const uint32_t f = finite_mag2(w[k]);
-                nf += nonfinite2(w[k]);
-                cm[k] = max_u16x2(cm[k], f);
-                rm = max_u16x2(rm, f);
-            }
-            if constexpr (ROW) {
-                const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, fold16(rm));
+            for (int k = 0; k < 4; ++k) sm[k] = max_u16x2(sm[k], w[k]);
+            rm[i] = max_u16x2(max_u16x2(w[0], w[1]), max_u16x2(w[2], w[3]));
+            all = max_u16x2(all, rm[i]);
+        }
+        if (__any_sync(0xFFFFFFFFu, fold16(all) >= 0x7F80u)) {  // NaN / Inf in the warp's rows: exact maxima
+            const StripMax e = strip_exact(x, R, C, r0, c);
+            nf += e.nf;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) sm[k] = e.cm[k];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) rm[i] = e.rm[i];
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) cm[k] = max_u16x2(cm[k], sm[k]);
+        if constexpr (ROW) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, fold16(rm[i]));
                 if (lane == 0 && m != 0u && r0 + i < R) atomicMax(rowmax + r0 + i, m);
             }
         }
-        if constexpr (COL) {
+    }
+    if constexpr (COL) {
 #pragma unroll
-            for (int k = 0; k < 4; ++k) cred[warp][4 * lane + k] = cm[k];
-            __syncthreads();
-            if (threadIdx.x < 128) {
-                uint32_t m = 0;
+        for (int k = 0; k < 4; ++k) cred[warp][4 * lane + k] = cm[k];
+        __syncthreads();
+        if (threadIdx.x < 128) {
+            uint32_t m = 0;
 #pragma unroll
-                for (int w = 0; w < 8; ++w) m = max_u16x2(m, cred[w][threadIdx.x]);
-                const int64_t cc = cs + 2 * threadIdx.x;
-                if (cc < C) {
-                    if (m & 0xFFFFu) atomicMax(colmax + cc, m & 0xFFFFu);
-                    if (m >> 16) atomicMax(colmax + cc + 1, m >> 16);
-                }
+            for (int w = 0; w < 8; ++w) m = max_u16x2(m, cred[w][threadIdx.x]);
+            const int64_t cc = cs + 2 * threadIdx.x;
+            if (cc < C) {
+                if (m & 0xFFFFu) atomicMax(colmax + cc, m & 0xFFFFu);
+                if (m >> 16) atomicMax(colmax + cc + 1, m >> 16);
             }
-            __syncthreads();  // cred is rewritten by the next strip
         }
     }
     nf = warp_sum_u32(nf);
@@ -1404,9 +1453,14 @@ fp8q_status launch_perchannel(const QuantArgs& a, int fmt, bool row, bool col, c
     uint32_t* rm = a.s_row ? (uint32_t*)a.s_row + a.row0 : nullptr;
     if (row && cudaMemsetAsync(rm, 0, (size_t)Rp * sizeof(float), s) != cudaSuccess) return FP8Q_ERR_CUDA;
     if (col && cudaMemsetAsync(a.s_col, 0, (size_t)Cp * sizeof(float), s) != cudaSuccess) return FP8Q_ERR_CUDA;
-    const int64_t strips = ((a.R + 63) / 64) * ((a.C + 255) / 256);
-    int64_t grid = (int64_t)num_sms() * 8;
-    if (strips < grid) grid = strips;
+    const int64_t bands = (a.C + 255) / 256, strips_r = (a.R + 63) / 64;
+    if (bands * strips_r >= ((int64_t)1 << 31)) return FP8Q_ERR_SHAPE;  // strips counted in 32 bits
+    // CTAs per column band: about four resident CTAs per SM in all, at most
+    // one per strip of the band; the grid is a multiple of the band count
+    int64_t per_band = (int64_t)num_sms() * 4 / bands;
+    if (per_band < 1) per_band = 1;
+    if (per_band > strips_r) per_band = strips_r;
+    const int64_t grid = bands * per_band;
     uint32_t* cm = (uint32_t*)a.s_col;
     if (row && col)
         pc_amax_kernel<true, true><<<(unsigned)grid, 256, 0, s>>>(a.x, a.R, a.C, rm, cm, a.counters);
