@@ -738,19 +738,17 @@ def run_modes(args):
             for kind in (0, 1, 2, 3, 4, 5):
                 print(json.dumps(quantize_point(kind, rows, 4096, True, True, args.steps, args.warmup, flush, x)),
                       flush=True)
+            if mib == 256:  # generic sub-channel blocks, both copies
+                for blk in ((1, 32), (1, 64), (1, 256), (32, 32), (64, 64), (256, 256)):
+                    print(json.dumps(quantize_point(6, rows, 4096, True, True, args.steps, args.warmup, flush, x,
+                                                    blk)), flush=True)
             del x
         for kind in (4, 2, 0, 5):
             for K in (1024, 2048, 4096, 8192, 16384):
                 print(json.dumps(gemm_point(kind, 8192, 8192, K, args.steps, args.warmup, flush)), flush=True)
         for kind in (4, 2, 0, 5):
             print(json.dumps(gemm_point(kind, 8192, 53248, 16384, args.steps, args.warmup, flush)), flush=True)
-        # generic sub-channel blocks: quantize (both copies, 256 MiB) and the GEMM
-        # at 8192^2 x 4096 for each K block, 1D2D and 1D1D
-        x = _device_tensor(32768, 4096, 5)
-        for blk in ((1, 32), (1, 64), (1, 256), (32, 32), (64, 64), (256, 256)):
-            print(json.dumps(quantize_point(6, 32768, 4096, True, True, args.steps, args.warmup, flush, x, blk)),
-                  flush=True)
-        del x
+        # generic sub-channel blocks: the GEMM at 8192^2 x 4096 for each K block, 1D2D and 1D1D
         for b in (32, 64, 128, 256):
             for b2d in (True, False):
                 print(json.dumps(gemm_point(6, 8192, 8192, 4096, args.steps, args.warmup, flush, "bf16", b, b2d)),

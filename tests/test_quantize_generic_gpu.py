@@ -78,3 +78,29 @@ def test_generic_blocks_invalid_shapes_are_refused():
             api.quantize(x, O.BLOCK_GENERIC, O.E4M3, True, False, block=block)
         assert e.value.status == L.ERR_UNSUPPORTED
     assert api.device_errors() == 0
+
+
+def test_generic_blocks_in_a_multi_call():
+    """fp8q_quantize_multi with generic-block jobs of both kinds of pass (1 x 32
+    and 64 x 64 in one tile pass, 1 x 256 and 256 x 256 after their amax pass)
+    beside a 1 x 128 job, on streams of their own: every output equals the
+    oracle's."""
+    import torch
+    api = _api()
+    specs = [((1, 32), O.E4M3, (400, 1040), True, True),
+             ((64, 64), O.E5M2, (336, 528), True, True),
+             ((1, 256), O.E4M3, (272, 768), True, True),
+             ((256, 256), O.E4M3, (528, 400), False, True)]
+    xs = [_mixed(sh, 120 + i) for i, (_, _, sh, _, _) in enumerate(specs)]
+    qts = [api.alloc(O.BLOCK_GENERIC, f, *sh, r, c, "cuda", block=b) for b, f, sh, r, c in specs]
+    x1 = _mixed((400, 1040), 130)
+    q1 = api.alloc(O.BLOCK_1x128, O.E4M3, 400, 1040, True, True, "cuda")
+    jobs = [(x.cuda(), q) for x, q in zip(xs, qts)] + [(x1.cuda(), q1)]
+    api.quantize_multi(jobs)
+    torch.cuda.synchronize()
+    for (b, f, sh, r, c), x, q in zip(specs, xs, qts):
+        ref = O.quantize_generic(f, bits_of(x), *b, r, c)
+        assert_quant_equal(O.BLOCK_GENERIC, gpu_outputs(q), ref, r, c, f"multi generic {b}")
+    ref1 = O.quantize(O.BLOCK_1x128, O.E4M3, bits_of(x1), True, True)
+    assert_quant_equal(O.BLOCK_1x128, gpu_outputs(q1), ref1, True, True, "multi 1x128")
+    assert api.device_errors() == 0
