@@ -284,26 +284,29 @@ __device__ __forceinline__ void transpose4(uint32_t h0, uint32_t h1, uint32_t h2
     y = __byte_perm(a, b, 0x7632);
 }
 
-// Number of the bf16 of v whose magnitude bits equal m.
-__device__ __forceinline__ uint32_t count_equal8(const uint4& v, uint32_t m) {
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    uint32_t c = 0;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) c += ((w[i] & 0x7FFFu) == m) + (((w[i] >> 16) & 0x7FFFu) == m);
-    return c;
+// Per 16-bit lane of the packed magnitudes of w (both no larger than their
+// lane's m): 1 where the magnitude equals m, else 0, counted in the lane.
+// c2 = (0x8000 - m_lo) | (0x8000 - m_hi) << 16: |x| + 0x8000 - m reaches bit
+// 15 of its lane exactly when |x| == m, and no lane carries into the next.
+__device__ __forceinline__ uint32_t lanes_at_max(uint32_t w, uint32_t c2) {
+    return (((w & 0x7FFF7FFFu) + c2) >> 15) & 0x00010001u;
 }
 // Saturated elements of a per-tensor-current, per-channel or blockwise block whose maximum
 // m can saturate.  Those scales are one correctly rounded division of fmax and
 // amax (relative error <= 2^-24) and the next bf16 below m is at least 2^-8
 // smaller, so only elements equal to m in magnitude can exceed fmax once
-// scaled: count those, looking only inside the vectors whose maximum is m.
+// scaled: count those, looking only inside the vectors whose packed maxima
+// vp (from the analysis) hold m.  No element of v exceeds m.
 template <int J0, int J1>
-__device__ __forceinline__ uint32_t count_at_max(const uint4 (&v)[8], uint32_t m) {
-    uint32_t c = 0;
+__device__ __forceinline__ uint32_t count_at_max(const uint4 (&v)[8], const uint32_t (&vp)[8], uint32_t m) {
+    const uint32_t c2 = (0x8000u - m) * 0x00010001u;
+    uint32_t acc = 0;
 #pragma unroll
     for (int j = J0; j < J1; ++j)
-        if (fold16(vec_pmax(v[j])) == m) c += count_equal8(v[j], m);
-    return c;
+        if (fold16(vp[j]) == m)
+            acc += lanes_at_max(v[j].x, c2) + lanes_at_max(v[j].y, c2) + lanes_at_max(v[j].z, c2) +
+                   lanes_at_max(v[j].w, c2);
+    return (acc & 0xFFFFu) + (acc >> 16);
 }
 
 // The rare paths of a tile -- a NaN / Inf in the data, or a blockwise divisor
@@ -524,11 +527,12 @@ __device__ __forceinline__ void tile_body(const QuantArgs& a, const CUtensorMap*
     uint32_t vnf = 0;       // bit j: vector j holds a NaN / Inf
     uint32_t mq[2];         // MX: the two 1x32 blocks' maxima; else mq[0] = the half-row maximum
     uint32_t mh[2];         // the maxima of vectors 0-3 and 4-7 (NaN / Inf-free halves)
+    uint32_t vp[8];         // each vector's packed maxima (NaN / Inf included)
     {
-        const uint32_t p0 = max_u16x2(max_u16x2(vec_pmax(v[0]), vec_pmax(v[1])),
-                                      max_u16x2(vec_pmax(v[2]), vec_pmax(v[3])));
-        const uint32_t p1 = max_u16x2(max_u16x2(vec_pmax(v[4]), vec_pmax(v[5])),
-                                      max_u16x2(vec_pmax(v[6]), vec_pmax(v[7])));
+#pragma unroll
+        for (int j = 0; j < 8; ++j) vp[j] = vec_pmax(v[j]);
+        const uint32_t p0 = max_u16x2(max_u16x2(vp[0], vp[1]), max_u16x2(vp[2], vp[3]));
+        const uint32_t p1 = max_u16x2(max_u16x2(vp[4], vp[5]), max_u16x2(vp[6], vp[7]));
         mh[0] = fold16(p0);
         mh[1] = fold16(p1);
         if (KIND == kMX || (KIND == kGen && a.bc == 32)) {
@@ -673,14 +677,17 @@ __device__ __forceinline__ void tile_body(const QuantArgs& a, const CUtensorMap*
         if (vnf == 0 && f0.fast && f1.fast) {  // the common case: one straight-line block
             const Factor2 g0 = pair_factor(f0, f0), g1 = pair_factor(f1, f1);
             constexpr bool kAtMax = KIND == kCur || KIND == kB1 || KIND == kB128 || KIND == kPC || KIND == kGen;
+            // only elements equal to the block maximum can saturate; counted
+            // before the conversions, so that each vector's registers are free
+            // once it is converted
+            if (kAtMax) {
+                if (s0 && mh[0] == mq[0]) nsat_rc += count_at_max<0, 4>(v, vp, mq[0]);
+                if (s1 && mh[1] == mq[1]) nsat_rc += count_at_max<4, 8>(v, vp, mq[1]);
+            }
 #pragma unroll
             for (int j = 0; j < 8; ++j)
                 q[j] = convert8_packed<KIND, FMT>(v[j], (j < 4) ? g0 : g1, nsat_rc,
                                                   kAtMax ? false : ((j < 4) ? s0 : s1));
-            if (kAtMax) {  // only elements equal to the block maximum can saturate
-                if (s0 && mh[0] == mq[0]) nsat_rc += count_at_max<0, 4>(v, mq[0]);
-                if (s1 && mh[1] == mq[1]) nsat_rc += count_at_max<4, 8>(v, mq[1]);
-            }
         } else {
             Row8 r;
 #pragma unroll
@@ -809,6 +816,22 @@ __device__ __forceinline__ void tile_body(const QuantArgs& a, const CUtensorMap*
         if (!col_nf && f0.fast && f1.fast) {
             const bool c0s = may_saturate<KIND, FMT>(m0, f0), c1s = may_saturate<KIND, FMT>(m1, f1);
             const Factor2 g = pair_factor(f0, f1);  // lanes: column 2p, column 2p + 1
+            if ((KIND == kB1 || KIND == kPC || KIND == kGen) && ((c0s && own0 == m0) || (c1s && own1 == m1))) {
+                // only elements equal to the block maximum can saturate (as in
+                // count_at_max), looked for in the 8-row groups whose maximum it
+                // is, before the conversions
+                const uint32_t c2 = (0x8000u - m0) | ((0x8000u - m1) << 16);
+#pragma unroll
+                for (int gi = 0; gi < 4; ++gi) {
+                    const bool lo = c0s && (pmg[gi] & 0xFFFFu) == m0, hi = c1s && (pmg[gi] >> 16) == m1;
+                    if (lo || hi) {
+                        uint32_t acc = 0;
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) acc += lanes_at_max(w[8 * gi + i], c2);
+                        ns += (lo ? (acc & 0xFFFFu) : 0u) + (hi ? (acc >> 16) : 0u);
+                    }
+                }
+            }
 #pragma unroll
             for (int j = 0; j < 32; j += 4) {
                 const float2 y0 = apply2<KIND>(bf16x2_f32(w[j]), g), y1 = apply2<KIND>(bf16x2_f32(w[j + 1]), g);
@@ -818,19 +841,6 @@ __device__ __forceinline__ void tile_body(const QuantArgs& a, const CUtensorMap*
                           sat2<FMT>(y3, c0s, c1s);
                 o0[j / 4] = cvt4_applied<KIND, FMT>(y0.x, y1.x, y2.x, y3.x);
                 o1[j / 4] = cvt4_applied<KIND, FMT>(y0.y, y1.y, y2.y, y3.y);
-            }
-            if ((KIND == kB1 || KIND == kPC || KIND == kGen) && ((c0s && own0 == m0) || (c1s && own1 == m1))) {
-                // only elements equal to the block maximum can saturate (count_at_max),
-                // looked for in the 8-row groups whose maximum it is
-#pragma unroll
-                for (int g = 0; g < 4; ++g) {
-                    const bool lo = c0s && (pmg[g] & 0xFFFFu) == m0, hi = c1s && (pmg[g] >> 16) == m1;
-                    if (lo || hi) {
-#pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            ns += (lo && (w[8 * g + i] & 0x7FFFu) == m0) + (hi && ((w[8 * g + i] >> 16) & 0x7FFFu) == m1);
-                    }
-                }
             }
         } else {
             Col32 cw;
