@@ -60,12 +60,14 @@ def test_generic_blocks_special_values(block):
     assert got["nonfinite"] == 4
 
 
-def test_generic_blocks_full_size_sweep_tensor():
-    """A 64 MiB sweep tensor (0.1 % of elements x1000) with 1 x 64 and 64 x 64
-    blocks, both copies, every byte."""
+@pytest.mark.parametrize("block", [(1, 32), (1, 64), (1, 256), (32, 32), (64, 64), (256, 256)],
+                         ids=["1x32", "1x64", "1x256", "32x32", "64x64", "256x256"])
+def test_generic_blocks_full_size_sweep_tensor(block):
+    """A 64 MiB sweep tensor (0.1 % of elements x1000) with every block shape
+    that has no specialised kernel (one tile pass for 32 and 64, an amax pass
+    first for 256), both copies, every byte."""
     x = inputs.sweep_tensor(64)
-    for block in ((1, 64), (64, 64)):
-        _check(x, block, O.E4M3, True, True, f"sweep {block}")
+    _check(x, block, O.E4M3, True, True, f"sweep {block}")
 
 
 def test_generic_blocks_invalid_shapes_are_refused():
