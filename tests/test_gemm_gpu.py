@@ -170,7 +170,7 @@ def test_full_config_blockwise_llama8b_up_proj(variant):
     if variant == 2:   # SM pairs, the bench's kernel: every one of the 4096 x 14336 outputs
         _check(api, qx, False, qw, False, ctx="up-proj fprop, full output")
     else:
-        _check(api, qx, False, qw, False, sample=_edge_sample(30), ctx="up-proj fprop (32 rows + 32 cols)")
+        _check(api, qx, False, qw, False, sample=_edge_sample(254), ctx="up-proj fprop (256 rows + 256 cols)")
 
 
 def test_full_config_perchannel_llama8b_up_proj():
@@ -180,7 +180,7 @@ def test_full_config_perchannel_llama8b_up_proj():
     X, W = inputs.llama8b_up_proj()
     qx = _quant(api, X.cuda(), 5, O.E4M3, True, True)
     qw = _quant(api, W.cuda(), 5, O.E4M3, True, True)
-    s = _edge_sample(10)
+    s = _edge_sample(254)
     _check(api, qx, False, qw, False, sample=s, ctx="perchannel fprop")
     # the column copies (per-column factors): W^T W (K = 14336) and X^T X (K = 4096)
     _check(api, qw, True, qw, True, sample=s, ctx="perchannel W^T . W")
@@ -193,7 +193,7 @@ def test_full_config_mxfp8_llama8b_mlp(variant):
     qx = _quant(api, X.cuda(), 4, O.E4M3, True, True)
     qw = _quant(api, W.cuda(), 4, O.E4M3, True, True)
     qd = _quant(api, dY.cuda(), 4, O.E4M3, True, True)
-    s = _edge_sample(62 if variant == 2 else 14)
+    s = _edge_sample(254)   # 256 rows x every column and every row x 256 columns
     _check(api, qx, False, qw, False, sample=s, ctx="MXFP8 MLP fprop")
     _check(api, qd, False, qw, True, sample=s, ctx="MXFP8 MLP dgrad")
     _check(api, qd, True, qx, True, sample=s, ctx="MXFP8 MLP wgrad")

@@ -311,8 +311,8 @@ def test_bench_step_as_timed_matches_oracle():
     (1x128) and W (128x128) of the Llama-3-8B up-projection, both copies, in
     one fp8q_quantize_multi call, then the fprop GEMM with the automatic
     kernel choice.  Every byte, scale and counter of both tensors equals the
-    oracle's; the GEMM matches the oracle's fp64 sum on every output of 8
-    rows and of 8 columns (the first and last of each among them)."""
+    oracle's; the GEMM matches the oracle's fp64 sum on every output of 256
+    rows and of 256 columns (the first and last of each among them)."""
     api = _api()
     X, W = inputs.llama8b_up_proj()
     T, H = X.shape
@@ -328,8 +328,8 @@ def test_bench_step_as_timed_matches_oracle():
     Y = api.scaled_gemm(qx, False, qw, False)
     torch.cuda.synchronize()
     g = np.random.default_rng(2024)
-    rows = np.unique(np.concatenate([[0, T - 1], g.choice(T, 6, replace=False)]))
-    cols = np.unique(np.concatenate([[0, F - 1], g.choice(F, 6, replace=False)]))
+    rows = np.unique(np.concatenate([[0, T - 1], g.choice(np.arange(1, T - 1), 254, replace=False)]))
+    cols = np.unique(np.concatenate([[0, F - 1], g.choice(np.arange(1, F - 1), 254, replace=False)]))
     pm1, pn1 = [a.ravel() for a in np.meshgrid(rows, np.arange(F), indexing="ij")]
     pm2, pn2 = [a.ravel() for a in np.meshgrid(np.arange(T), cols, indexing="ij")]
     pm, pn = np.concatenate([pm1, pm2]), np.concatenate([pn1, pn2])
