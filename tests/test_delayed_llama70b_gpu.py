@@ -14,8 +14,9 @@ Every step, through the C ABI:
   dgrad dX = dY W (dY's row copy with W's column copy, E5M2 x E4M3) and
   wgrad dW = dY^T X (the two column copies) -- bf16 output, against the fp64
   oracle on the same quantized operands: rows {0, last, 6 seeded} x every
-  column and every row x columns {0, last, 6 seeded}, normwise relative
-  error <= 2e-3 on each of the 3 x 32 GEMMs.
+  column and every row x columns {0, last, 6 seeded} (254 seeded at the
+  first step and at the spike's step 20: 256 rows and 256 columns),
+  normwise relative error <= 2e-3 on each of the 3 x 32 GEMMs.
 
 The oracle's codes come from the oracle alone: per step and tensor the
 oracle encodes every one of the 65536 bf16 bit patterns at the step's scale
@@ -37,16 +38,16 @@ FMTS = (O.E4M3, O.E4M3, O.E5M2)      # X, W, dY
 ALL_BITS = np.arange(65536, dtype=np.uint16)
 
 
-def _samples(n: int, rng) -> np.ndarray:
-    """{0, n - 1} and 6 seeded indices in between."""
-    return np.unique(np.concatenate([[0, n - 1], rng.choice(np.arange(1, n - 1), 6, replace=False)]))
+def _samples(n: int, rng, k: int = 6) -> np.ndarray:
+    """{0, n - 1} and k seeded indices in between."""
+    return np.unique(np.concatenate([[0, n - 1], rng.choice(np.arange(1, n - 1), k, replace=False)]))
 
 
-def _gemm_rel(D: torch.Tensor, A, fa, sa, B, fb, sb, rng) -> float:
+def _gemm_rel(D: torch.Tensor, A, fa, sa, B, fb, sb, rng, k: int = 6) -> float:
     """Normwise relative error of the GPU D = A . B^T (bf16) against the fp64
     oracle over the sampled rows x all columns and all rows x sampled columns."""
     M, N = D.shape
-    rows, cols = _samples(M, rng), _samples(N, rng)
+    rows, cols = _samples(M, rng, k), _samples(N, rng, k)
     pm = np.concatenate([np.repeat(rows, N), np.tile(np.arange(M), cols.size)])
     pn = np.concatenate([np.tile(np.arange(N), rows.size), np.repeat(cols, M)])
     K = A.shape[1]
@@ -98,10 +99,11 @@ def test_delayed_llama70b_32_steps_codes_and_gemms():
         api.scaled_gemm(qdy, False, qw, True, out=dX)        # dgrad: dY . W
         api.scaled_gemm(qdy, True, qx, True, out=dW)         # wgrad: dY^T . X
         torch.cuda.synchronize()
-        rels = (_gemm_rel(Y, cx, FMTS[0], sinv[0], cw, FMTS[1], sinv[1], rng),
-                _gemm_rel(dX, cdy, FMTS[2], sinv[2], np.ascontiguousarray(cw.T), FMTS[1], sinv[1], rng),
+        k = 254 if t in (0, 20) else 6
+        rels = (_gemm_rel(Y, cx, FMTS[0], sinv[0], cw, FMTS[1], sinv[1], rng, k),
+                _gemm_rel(dX, cdy, FMTS[2], sinv[2], np.ascontiguousarray(cw.T), FMTS[1], sinv[1], rng, k),
                 _gemm_rel(dW, np.ascontiguousarray(cdy.T), FMTS[2], sinv[2], np.ascontiguousarray(cx.T), FMTS[0],
-                          sinv[0], rng))
+                          sinv[0], rng, k))
         for name, rel in zip(("fprop", "dgrad", "wgrad"), rels):
             assert rel <= 2e-3, f"step {t} {name}: normwise relative error {rel:.3e}"
         worst = max(worst, *rels)

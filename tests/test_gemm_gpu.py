@@ -199,6 +199,21 @@ def test_full_config_mxfp8_llama8b_mlp(variant):
     _check(api, qd, True, qx, True, sample=s, ctx="MXFP8 MLP wgrad")
 
 
+@pytest.mark.parametrize("recipe", ["blockwise", "mxfp8"])
+def test_full_config_405b_fprop(recipe):
+    """The Llama-3.1-405B fprop of the roofline sweep (8192 x 53248 x 16384)
+    on the kernel the sweep times (the automatic choice: SM pairs): 256 rows
+    x every column and every row x 256 columns against the oracle's fp64
+    sums on its own quantization of the same bf16 inputs."""
+    api = _api()
+    X = inputs.normal_bf16((8192, 16384), 405)
+    W = inputs.normal_bf16((53248, 16384), 406, 0.02)
+    ka, kb = (2, 3) if recipe == "blockwise" else (4, 4)
+    qx = _quant(api, X.cuda(), ka, O.E4M3, True, False)
+    qw = _quant(api, W.cuda(), kb, O.E4M3, True, False)
+    _check(api, qx, False, qw, False, sample=_edge_sample(254), ctx=f"405B fprop {recipe}")
+
+
 @pytest.mark.parametrize("ka,kb", [(2, 3), (4, 4), (0, 0), (5, 5)], ids=["blockwise", "mxfp8", "pertensor", "perchannel"])
 def test_gemm_on_row_blocks_of_b(ka, kb):
     """D = A . B^T computed on row blocks of B (api.row_block: the weight in
