@@ -1,6 +1,8 @@
 // Quantize kernels: per-tensor current / delayed, blockwise 1x128 / 128x128,
 // MXFP8 1x32 ("2025 FP8 quantized-training guide", sec. 2.1-2.3; "mastering
-// FP8 LLM training 1.5x speedup", scaling strategies 1-4).
+// FP8 LLM training 1.5x speedup", scaling strategies 1-4), per-channel
+// current and sub-channel blocks of 1 x b / b x b (the same page, scaling
+// strategy 3 and Figure 1's channel-wise scaling).
 //
 // One tile kernel serves every recipe.  A persistent CTA of 256 threads walks
 // 128x128 tiles of x; TMA loads each tile (two 64-column boxes in the 128-byte
@@ -8,10 +10,12 @@
 // thread t owns row t % 128 and the 64-column half t / 128, i.e. two whole
 // 1x32 blocks or half of a 1x128 block, so block maxima are packed u16x2
 // maxima inside the thread and each scale is computed once per 32 or 64
-// elements.  Column path (1x128, MXFP8): thread t reads rows 32 (t / 64) .. +31
-// of columns 2 (t % 64), +1 from the same swizzled tile (conflict-free) and
-// reduces the 1x32 / 1x128 column blocks; for per-tensor and 128x128 scales
-// the column copy is the byte transpose of the row codes.  Once the bf16 tile
+// elements.  Column path (1x128, MXFP8, per channel, 1 x b): thread t reads
+// rows 32 (t / 64) .. +31 of columns 2 (t % 64), +1 from the same swizzled
+// tile (conflict-free) and reduces the column blocks; for per-tensor, 128x128
+// and b x b scales the column copy is the byte transpose of the row codes.
+// Per-channel scales and 256-wide blocks span tiles: a pass over x leaves
+// their maxima in the scale buffers before the tile pass.  Once the bf16 tile
 // is consumed, its stage takes the two 128x128 code tiles, which TMA stores
 // write out; the stage is reloaded after those stores have read it.  The
 // 128-aligned tiles make every scale-layout pad entry the scale of an all-zero
