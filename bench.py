@@ -280,13 +280,23 @@ def run_ours(args):
     # as it lands (fp8q_quantize_rows, both copies) and the GEMM of the matching
     # column block of Y (api.row_block of W) runs at once, its result copied
     # back on a third stream while later blocks still arrive.  Every byte of X,
-    # W and Y crosses inside the timed region.
-    NC = args.e2e_blocks
-    Nc = F // NC
+    # W and Y crosses inside the timed region.  The "ramp" plan (an option)
+    # makes the first and last blocks small so that Y starts back sooner; it
+    # measured no faster: with both directions busy the link moves about
+    # 260-320 GB/s in all, which the 268 MB of a step fill either way.
+    if args.e2e_plan == "ramp" and F == 14336:
+        sizes = [256, 512, 1024, 2048, 2048, 2048, 2048, 2048, 1536, 512, 256]
+    else:
+        sizes = [F // args.e2e_blocks] * args.e2e_blocks
+    bounds = [0]
+    for n in sizes:
+        bounds.append(bounds[-1] + n)
+    assert bounds[-1] == F and all(b % 128 == 0 for b in bounds[:-1])
+    NC = len(sizes)
     Xp, Wp = Xh.pin_memory(), Wh.pin_memory()
-    Yps = [torch.empty((T, Nc), dtype=torch.bfloat16).pin_memory() for _ in range(NC)]
-    Ycs = [torch.empty((T, Nc), dtype=torch.bfloat16, device=dev) for _ in range(NC)]
-    qw_blocks = [api.row_block(qw, c * Nc, (c + 1) * Nc) for c in range(NC)]
+    Yps = [torch.empty((T, n), dtype=torch.bfloat16).pin_memory() for n in sizes]
+    Ycs = [torch.empty((T, n), dtype=torch.bfloat16, device=dev) for n in sizes]
+    qw_blocks = [api.row_block(qw, bounds[c], bounds[c + 1]) for c in range(NC)]
     s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
     ev_x = torch.cuda.Event()
     ev_w = [torch.cuda.Event() for _ in range(NC)]
@@ -297,14 +307,14 @@ def run_ours(args):
             X.copy_(Xp, non_blocking=True)
             ev_x.record(s_in)
             for c in range(NC):
-                W[c * Nc:(c + 1) * Nc].copy_(Wp[c * Nc:(c + 1) * Nc], non_blocking=True)
+                W[bounds[c]:bounds[c + 1]].copy_(Wp[bounds[c]:bounds[c + 1]], non_blocking=True)
                 ev_w[c].record(s_in)
         qw.counters.zero_()
         st.wait_event(ev_x)
         api.quantize_into(X, qx, stream=st)
         for c in range(NC):
             st.wait_event(ev_w[c])
-            api.quantize_rows_into(W[c * Nc:(c + 1) * Nc], qw, c * Nc, stream=st)
+            api.quantize_rows_into(W[bounds[c]:bounds[c + 1]], qw, bounds[c], stream=st)
             api.scaled_gemm(qx, False, qw_blocks[c], False, out=Ycs[c], stream=st)
             s_out.wait_stream(st)
             with torch.cuda.stream(s_out):
@@ -498,8 +508,9 @@ def run_ours(args):
                 "ms_per_step_eager": round(e2e_eager, 4),
                 "ms_per_step_graph": round(e2e_graph_ms, 4) if e2e_graph_ms else None,
                 "result_equals_device_step": e2e_ok,
-                "overlap": f"W crosses in {NC} row blocks, each quantized on arrival (fp8q_quantize_rows) and its "
-                           "column block of Y computed and copied back while later blocks still cross"},
+                "overlap": f"W crosses in {NC} row blocks of {sizes} rows, each quantized on arrival "
+                           "(fp8q_quantize_rows) and its column block of Y computed and copied back while later "
+                           "blocks still cross"},
         "gpu_launches": launches + e2e_launches,
         "clocks": clocks,
         "device_errors": errs,
@@ -874,8 +885,11 @@ def main():
     ap.add_argument("--block", type=int, choices=[32, 64, 128, 256], default=128,
                     help="generic kind: block width b (quantize b x b unless --block-1d; GEMM A 1 x b, B b x b)")
     ap.add_argument("--block-1d", action="store_true", help="generic kind: 1 x b blocks (GEMM: B 1 x b too)")
+    ap.add_argument("--e2e-plan", choices=["ramp", "even"], default="even",
+                    help="end-to-end pipeline: --e2e-blocks equal W row blocks (even) or small ones first and last "
+                         "(ramp: measured 1.036 against 1.025 ms)")
     ap.add_argument("--e2e-blocks", type=int, choices=[1, 2, 4, 7, 8, 14, 16], default=8,
-                    help="row blocks of W in the end-to-end pipeline (F = 14336 = 112 x 128)")
+                    help="even plan: row blocks of W in the end-to-end pipeline (F = 14336 = 112 x 128)")
     ap.add_argument("--rows", type=int, default=16384)
     ap.add_argument("--cols", type=int, default=8192)
     ap.add_argument("--no-rowwise", action="store_true")
