@@ -729,15 +729,19 @@ def run_modes(args):
                 ("sweep tensor 64 MiB N(0,1), 0.1% elements x1000", inputs.sweep_tensor(64), api.E4M3),
                 ("Llama-3-8B MLP dY 8192x14336 N(0,1e-4^2)", inputs.normal_bf16((8192, 14336), 2, 1e-4), api.E4M3),
                 ("Llama-3-8B MLP dY 8192x14336 N(0,1e-4^2)", inputs.normal_bf16((8192, 14336), 2, 1e-4), api.E5M2)]
+        # the recipes, then the sub-channel block shapes of the same rule
+        recipes = [(k, (0, 0)) for k in (0, 5, 2, 3, 4)] + [(6, b) for b in ((1, 32), (1, 64), (1, 256), (32, 32),
+                                                                             (64, 64), (256, 256))]
         for name, x, fmt in data:
             xd = x.cuda()
             base = None
-            for kind in (0, 5, 2, 3, 4):
-                qt = api.quantize(xd, kind, fmt, True, False)
+            for kind, blk in recipes:
+                qt = api.quantize(xd, kind, fmt, True, False, block=blk)
                 e = qerror.error(xd.float(), qerror.dequantize_rowwise(qt))
                 base = e["rel_err"] if kind == 0 else base
                 print(json.dumps({"mode": "qerror", "data": name, "fmt": "e4m3" if fmt == api.E4M3 else "e5m2",
-                                  "recipe": [k for k, v in KINDS.items() if v == kind][0],
+                                  "recipe": [k for k, v in KINDS.items() if v == kind][0] +
+                                  (f" {blk[0]}x{blk[1]}" if kind == 6 else ""),
                                   "rel_err": round(e["rel_err"], 6), "sqnr_db": round(e["sqnr_db"], 2),
                                   "vs_pertensor": round(e["rel_err"] / base, 3),
                                   "saturated": int(qt.counters[0].item())}), flush=True)

@@ -19,7 +19,8 @@ import math
 
 import torch
 
-from ._lib import BLOCK_1x128, BLOCK_128x128, E4M3, MXFP8_1x32, PERCHANNEL_CURRENT, PERTENSOR_CURRENT, PERTENSOR_DELAYED
+from ._lib import (BLOCK_1x128, BLOCK_128x128, BLOCK_GENERIC, E4M3, MXFP8_1x32, PERCHANNEL_CURRENT, PERTENSOR_CURRENT,
+                   PERTENSOR_DELAYED)
 
 
 def _cdiv(a: int, b: int) -> int:
@@ -45,10 +46,15 @@ def row_scales(qt) -> torch.Tensor:
     if qt.kind == BLOCK_128x128:
         s = buf.view(torch.float32)[: _cdiv(R, 128) * _cdiv(C, 128)].reshape(_cdiv(R, 128), _cdiv(C, 128))
         return s.repeat_interleave(128, 0)[:R].repeat_interleave(128, 1)[:, :C]
-    if qt.kind == BLOCK_1x128:
+    if qt.kind == BLOCK_1x128 or (qt.kind == BLOCK_GENERIC and qt.block[0] == 1):
+        b = 128 if qt.kind == BLOCK_1x128 else qt.block[1]
         Rp = _cdiv(R, 128) * 128
-        s = buf.view(torch.float32)[: _cdiv(C, 128) * Rp].reshape(_cdiv(C, 128), Rp)[:, :R].t()
-        return s.repeat_interleave(128, 1)[:, :C]
+        s = buf.view(torch.float32)[: _cdiv(C, b) * Rp].reshape(_cdiv(C, b), Rp)[:, :R].t()
+        return s.repeat_interleave(b, 1)[:, :C]
+    if qt.kind == BLOCK_GENERIC:  # b x b blocks: [ceil(R/b)][ceil(C/b)]
+        b = qt.block[1]
+        s = buf.view(torch.float32)[: _cdiv(R, b) * _cdiv(C, b)].reshape(_cdiv(R, b), _cdiv(C, b))
+        return s.repeat_interleave(b, 0)[:R].repeat_interleave(b, 1)[:, :C]
     if qt.kind == MXFP8_1x32:
         S, tiles_c = _cdiv(C, 32), _cdiv(C, 128)
         r = torch.arange(R, device=dev).reshape(R, 1)

@@ -41,3 +41,23 @@ def test_dequantize_layouts_match_the_oracle(kind, fmt):
     assert np.allclose(got, want, rtol=2.0 ** -23, atol=0.0)
     e = qerror.error(x.float(), torch.from_numpy(want))
     assert 0.0 < e["rel_err"] < 0.1 and math.isfinite(e["sqnr_db"])
+
+
+@pytest.mark.parametrize("block", [(1, 32), (1, 64), (1, 256), (32, 32), (64, 64), (256, 256)],
+                         ids=["1x32", "1x64", "1x256", "32x32", "64x64", "256x256"])
+def test_dequantize_generic_layouts_match_the_oracle(block):
+    """The sub-channel block layouts (1 x b: [ceil(C/b)][R up to 128], b x b:
+    [ceil(R/b)][ceil(C/b)]) expanded by qerror.py equal the oracle's plain
+    block scales, on a shape with ragged edges."""
+    R, C = 200, 272
+    x = inputs.to_bf16(inputs.with_outlier_elements(inputs.normal_f32((R, C), 13), 0.01, 100.0, 14))
+    ref = O.quantize_generic(O.E4M3, inputs.bf16_bits(x), *block, True, False)
+    sb = expected_scale_bytes(O.BLOCK_GENERIC, ref, "row")
+    qt = types.SimpleNamespace(kind=O.BLOCK_GENERIC, fmt=O.E4M3, rows=R, cols=C, block=block,
+                               data_row=torch.from_numpy(ref["data_row"]),
+                               scale_row=torch.from_numpy(np.ascontiguousarray(sb)), scale_inv=None)
+    got = qerror.dequantize_rowwise(qt).double().numpy()
+    s, bm, bk = O.dequant_scales(O.BLOCK_GENERIC, ref, "row", R, C, block=block)
+    full = np.repeat(np.repeat(np.asarray(s, dtype=np.float64), bm, 0)[:R], bk, 1)[:, :C]
+    want = O.decode(ref["data_row"], O.E4M3) * full
+    assert np.allclose(got, want, rtol=2.0 ** -23, atol=0.0)
