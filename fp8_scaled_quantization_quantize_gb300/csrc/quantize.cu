@@ -23,6 +23,7 @@
 #include <string.h>
 
 #include <mutex>
+#include <type_traits>
 
 #include "fp8q_internal.cuh"
 #include "ptx.cuh"
@@ -994,19 +995,28 @@ __global__ void __launch_bounds__(kThreads, 2)
 
 // Per-tensor current scaling, pass 1: amax over the finite elements of x and
 // the NaN / Inf count.  Four independent 16-byte loads in flight per thread.
+// The common path takes the packed maxima of the magnitude bits (one AND and
+// one u16x2 maximum a word); a thread whose maximum flags a NaN / Inf (>=
+// 0x7F80) reads its vectors again with the exact per-element test.
 __global__ void __launch_bounds__(kThreads) amax_kernel(const uint16_t* x, int64_t nvec, float* amax,
                                                         unsigned long long* counters) {
     __shared__ uint32_t redm[kThreads / 32], redn[kThreads / 32];
     const uint4* xv = (const uint4*)x;
-    uint32_t m = 0, nf = 0;
+    uint32_t pm = 0, nf = 0;
     const int64_t stride = (int64_t)gridDim.x * kThreads;
-    int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    const int64_t i0 = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    int64_t i = i0;
     for (; i + 3 * stride < nvec; i += 4 * stride) {
-        uint4 v0 = ld_nc_v4(xv + i), v1 = ld_nc_v4(xv + i + stride);
-        uint4 v2 = ld_nc_v4(xv + i + 2 * stride), v3 = ld_nc_v4(xv + i + 3 * stride);
-        m = max(m, max(max(vec_absmax(v0, nf), vec_absmax(v1, nf)), max(vec_absmax(v2, nf), vec_absmax(v3, nf))));
+        const uint4 v0 = ld_nc_v4(xv + i), v1 = ld_nc_v4(xv + i + stride);
+        const uint4 v2 = ld_nc_v4(xv + i + 2 * stride), v3 = ld_nc_v4(xv + i + 3 * stride);
+        pm = max_u16x2(pm, max_u16x2(max_u16x2(vec_pmax(v0), vec_pmax(v1)), max_u16x2(vec_pmax(v2), vec_pmax(v3))));
     }
-    for (; i < nvec; i += stride) m = max(m, vec_absmax(ld_nc_v4(xv + i), nf));
+    for (; i < nvec; i += stride) pm = max_u16x2(pm, vec_pmax(ld_nc_v4(xv + i)));
+    uint32_t m = fold16(pm);
+    if (m >= 0x7F80u) {  // a NaN / Inf among this thread's elements (rare): exact finite maximum and count
+        m = 0;
+        for (i = i0; i < nvec; i += stride) m = max(m, vec_absmax(ld_nc_v4(xv + i), nf));
+    }
     m = warp_max_u32(m);
     nf = warp_sum_u32(nf);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -1171,24 +1181,37 @@ __global__ void __launch_bounds__(256) gen_amax_kernel(const uint16_t* x, int64_
             v[i] = (c < C && r0 + i < R) ? ld_nc_v4(x + (r0 + i) * C + c) : make_uint4(0u, 0u, 0u, 0u);
         uint32_t cm[4] = {0u, 0u, 0u, 0u};
         uint32_t sq = 0;
+        // packed magnitudes (one AND a word) unless a NaN / Inf is in the warp's
+        // rows (a warp vote on their packed maximum): then the exact finite test
+        uint32_t all = 0;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-            uint32_t rm = 0;
+        for (int i = 0; i < 8; ++i) all = max_u16x2(all, vec_pmax(v[i]));
+        const bool exact = __any_sync(0xFFFFFFFFu, fold16(all) >= 0x7F80u);
+        auto rows = [&](auto exact_tag) {
+            constexpr bool kExact = decltype(exact_tag)::value;
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const uint32_t f = finite_mag2(w[k]);
-                nf += nonfinite2(w[k]);
-                cm[k] = max_u16x2(cm[k], f);
-                rm = max_u16x2(rm, f);
+            for (int i = 0; i < 8; ++i) {
+                const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+                uint32_t rm = 0;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const uint32_t f = kExact ? finite_mag2(w[k]) : (w[k] & 0x7FFF7FFFu);
+                    if (kExact) nf += nonfinite2(w[k]);
+                    cm[k] = max_u16x2(cm[k], f);
+                    rm = max_u16x2(rm, f);
+                }
+                uint32_t m = fold16(rm);
+                if constexpr (!SQ && ROW) {
+                    for (int o = 1; o < lg; o <<= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+                    if (lane % lg == 0 && m != 0u && r0 + i < R && c < C) atomicMax(srow + (c >> sh) * Rp + r0 + i, m);
+                }
+                sq = max(sq, m);
             }
-            uint32_t m = fold16(rm);
-            if constexpr (!SQ && ROW) {
-                for (int o = 1; o < lg; o <<= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-                if (lane % lg == 0 && m != 0u && r0 + i < R && c < C) atomicMax(srow + (c >> sh) * Rp + r0 + i, m);
-            }
-            sq = max(sq, m);
-        }
+        };
+        if (exact)
+            rows(std::true_type{});
+        else
+            rows(std::false_type{});
         if constexpr (SQ) {  // the warp's 8 rows lie in one block row (b >= 32)
             for (int o = 1; o < lg; o <<= 1) sq = max(sq, __shfl_xor_sync(0xFFFFFFFFu, sq, o));
             if (lane % lg == 0 && sq != 0u && c < C) {
