@@ -97,3 +97,33 @@ def test_gemm_random_cases(case):
     rel = np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-300)
     assert np.all(np.isfinite(got)) and rel <= 2e-3, (case, ka, kb, gb, M, N, K, fa, rel)
     assert api.device_errors() == 0
+
+
+FUSED_RECIPES = [(O.PERTENSOR_CURRENT, O.PERTENSOR_CURRENT), (O.BLOCK_1x128, O.BLOCK_128x128),
+                 (O.BLOCK_1x128, O.BLOCK_1x128), (O.MXFP8_1x32, O.MXFP8_1x32), (O.PERCHANNEL_CURRENT, O.PERCHANNEL_CURRENT)]
+
+
+@pytest.mark.parametrize("case", range(60))
+def test_fused_output_quantize_random_cases(case):
+    """The GEMM with the next layer's quantize in its epilogue on random
+    shapes: the fused codes, scales and counters equal the oracle's quantize
+    of the kernel's own bf16 D (MXFP8 1x32 or 1x128 output, either format)."""
+    from fp8_scaled_quantization_quantize_gb300 import api
+    rng = np.random.default_rng(3000 + case)
+    ka, kb = FUSED_RECIPES[case % len(FUSED_RECIPES)]
+    out_kind = O.MXFP8_1x32 if case % 2 else O.BLOCK_1x128
+    fmt = O.E4M3 if rng.random() < 0.6 else O.E5M2
+    M = int(rng.integers(1, 40)) * 16
+    N = int(rng.integers(1, 40)) * 32
+    K = int(rng.integers(1, 20)) * 32
+    scale = np.float32(10.0 ** rng.uniform(-3, 3))
+    a = inputs.to_bf16(rng.standard_normal((M, K), dtype=np.float32) * scale)
+    b = inputs.to_bf16(rng.standard_normal((N, K), dtype=np.float32) * np.float32(0.02))
+    qa = api.quantize(a.cuda(), ka, O.E4M3, True, False)
+    qb = api.quantize(b.cuda(), kb, O.E4M3, True, False)
+    D, Dq = api.scaled_gemm_q(qa, False, qb, False, out_kind, fmt, want_d=True)
+    torch.cuda.synchronize()
+    ref = O.quantize(out_kind, fmt, inputs.bf16_bits(D.cpu()), True, False)
+    assert_quant_equal(out_kind, gpu_outputs(Dq), ref, True, False,
+                       f"case {case}: {ka}x{kb} out {out_kind} fmt {fmt} {M}x{N}x{K}")
+    assert api.device_errors() == 0
