@@ -649,12 +649,17 @@ def gemm_point(kind, M, N, K, steps, warmup, flush, out="bf16", block=0, b2d=Tru
     D = torch.empty((M, N), dtype=torch.bfloat16 if out == "bf16" else torch.float32, device="cuda")
     ms = _time_ms(lambda: api.scaled_gemm(qa, False, qb, False, out=D), steps, warmup, flush)
     tf = 2.0 * M * N * K / ms / 1e9
+    # the HBM side of the same launch: FP8 operands read once, D written once
+    # (scales are a few percent of the operands at most and left out)
+    nbytes = (M + N) * K + M * N * D.element_size()
+    gbs = nbytes / ms / 1e6
     name = {0: "pertensor", 2: "blockwise 1x128 x 128x128", 4: "mxfp8", 5: "perchannel"}.get(
         kind, f"generic 1x{block} x {bb[0]}x{bb[1]}")
     del qa, qb, D
     torch.cuda.synchronize()
     return {"mode": "gemm", "recipe": name, "M": M, "N": N, "K": K, "out": out, "ms": round(ms, 4),
-            "tflops": round(tf, 1), "frac_of_fp8_peak": round(tf / fp8_peak, 3)}
+            "tflops": round(tf, 1), "frac_of_fp8_peak": round(tf / fp8_peak, 3),
+            "gbs": round(gbs, 1), "frac_of_hbm": round(gbs / peaks()[0], 3)}
 
 
 def run_modes(args):
