@@ -13,12 +13,17 @@
 // single-thread MMA issuer; then the epilogue warps for the CTA's own 128
 // rows (TMEM lanes 32 (w % 4) .., columns EC ((w - 2) / 4) ..), which release
 // TMEM on the leader's barrier and store D by TMA: eight warps of 128
-// columns (320 threads).  Blockwise: one more warp (352 threads) loads each
-// K block's scales into a ring of shared-memory slots, apart from the
-// operand producer, whose loads would otherwise queue behind the ring's
-// waits (measured: 0.626 -> 0.646 of peak at the Llama-3-8B up-projection).  Blockwise: with two K-block partial buffers the
-// MMAs of K block g + 2 wait for the epilogue to release block g, which is
-// what limits this recipe (measured: about 445 cycles from a partial's
+// columns (320 threads).  One more warp (352 threads) for two recipes.
+// Blockwise: it loads each K block's scales into a ring of shared-memory
+// slots, apart from the operand producer, whose loads would otherwise queue
+// behind the ring's waits (measured: 0.626 -> 0.646 of peak at the
+// Llama-3-8B up-projection).  MXFP8: in the leader it copies each stage's
+// scale tiles (landed with the operands) into both CTAs' TMEM with
+// tcgen05.cp and commits to a barrier the MMA issuer waits on (measured:
+// 0.763 -> 0.799 at the Llama-3-8B MLP fprop against moving them with the
+// epilogue warps' tcgen05.st).  Blockwise: with two K-block partial buffers
+// the MMAs of K block g + 2 wait for the epilogue to release block g, which
+// is what limits this recipe (measured: about 445 cycles from a partial's
 // arrival to its release against about 600 cycles of MMAs per K block).
 // TMEM per CTA: per-tensor two 256-column accumulators; MXFP8 one accumulator
 // plus 12 scale columns per stage; blockwise two 256-column partial buffers,
@@ -52,8 +57,10 @@ struct Cfg {
     static constexpr int BN = 256;
     static constexpr int BH = BN / 2;  // B rows per CTA
     static constexpr int EPI_WARPS = 8;
-    static constexpr int SCALE_WARP = 2 + EPI_WARPS;  // blockwise: the scale ring's producer
-    static constexpr int THREADS = 64 + 32 * EPI_WARPS + (BLOCKWISE ? 32 : 0);
+    // blockwise: the scale ring's producer; MXFP8: the copier of each stage's
+    // scale tiles into TMEM (in the leader CTA)
+    static constexpr int SCALE_WARP = 2 + EPI_WARPS;
+    static constexpr int THREADS = 64 + 32 * EPI_WARPS + ((BLOCKWISE || REC == REC_MX) ? 32 : 0);
     static constexpr int STAGES = BLOCKWISE ? 4 : 5;
     static constexpr int NACC = (REC == REC_MX) ? 1 : 2;  // TMEM accumulators (blockwise: K-block partials)
     static constexpr int EPI_COLS = BN / (EPI_WARPS / 4);
@@ -71,8 +78,8 @@ struct Cfg {
     static constexpr uint32_t OFF_STG = OFF_SCL + SR * SLOT;
     static constexpr uint32_t STG_WARP = 4096;  // four 1 KB output boxes per epilogue warp
     static constexpr uint32_t OFF_BAR = OFF_STG + EPI_WARPS * STG_WARP;
-    static constexpr int NSFB = (REC == REC_MX) ? STAGES : 0;  // MXFP8 scale-tile barriers per kind
-    static constexpr uint32_t NBARS = 2 * STAGES + 2 * NACC + 1 + 2 * SR + 2 * NSFB;
+    static constexpr int NSFB = (REC == REC_MX) ? STAGES : 0;  // MXFP8: a stage's scale tiles are in TMEM
+    static constexpr uint32_t NBARS = 2 * STAGES + 2 * NACC + 1 + 2 * SR + NSFB;
     static constexpr uint32_t OFF_MISC = OFF_BAR + 8 * NBARS;
     static constexpr uint32_t SMEM = OFF_MISC + 16 + 1024;
     static_assert(SMEM <= 232448, "shared memory budget of one CTA");
@@ -153,6 +160,11 @@ __device__ __forceinline__ void tc2_commit_both(uint32_t mbar) {
         "h"(mask)
         : "memory");
 }
+// 32 rows x 128 bits of shared memory into TMEM, replicated to the four lane
+// quarters, in both CTAs of the pair (each from its own shared memory)
+__device__ __forceinline__ void tc2_cp_32x128b(uint32_t taddr, uint64_t desc) {
+    asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
+}
 __device__ __forceinline__ void tc2_commit_local(uint32_t mbar) {
     asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(mbar) : "memory");
 }
@@ -170,27 +182,14 @@ __device__ __forceinline__ void mma2_mx(uint32_t d, uint64_t a, uint64_t b, uint
             d),
         "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc));
 }
-// Four TMEM columns of the warp's 32 lanes from registers, and the wait for
-// this thread's TMEM stores.
-__device__ __forceinline__ void tc_st_x4(uint32_t taddr, const uint4& v) {
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(v.x), "r"(v.y),
-                 "r"(v.z), "r"(v.w)
-                 : "memory");
-}
-__device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // Stores this warp's 32 rows x COLS columns through its staging area of NBOX
 // 1 KB boxes of 32-byte row pieces (32-byte swizzle: chunk c of row r at
 // r*32 + (c ^ ((r / 4) % 2))*16); waits for the staging to be read out each
 // time all NBOX boxes are in flight.
-struct NoPoll {
-    __device__ __forceinline__ void operator()() const {}
-};
-
-template <bool OUT_F32, int COLS, int NBOX, typename Poll = NoPoll>
+template <bool OUT_F32, int COLS, int NBOX>
 __device__ __forceinline__ void store_slice2(const CUtensorMap* mapD, uint8_t* stg, uint32_t stg_s, int lane, int x0,
-                                             int y0, int n_extent, int m_extent, const float* v, float scale,
-                                             const Poll& poll = Poll()) {
+                                             int y0, int n_extent, int m_extent, const float* v, float scale) {
     constexpr int kPiece = OUT_F32 ? 8 : 16;  // columns per 32-byte row piece
     constexpr int kBoxes = COLS / kPiece;
     const int r = lane, sw = (r >> 2) & 1;
@@ -224,7 +223,6 @@ __device__ __forceinline__ void store_slice2(const CUtensorMap* mapD, uint8_t* s
             tma_store_2d(mapD, x0 + kPiece * bx, y0, stg_s + (bx % NBOX) * 1024);
             bulk_commit();
         }
-        poll();
     }
 }
 
@@ -239,10 +237,9 @@ __device__ __forceinline__ void store_slice2(const CUtensorMap* mapD, uint8_t* s
 // 128x4 tile layout.  Blocks past N and rows past M are not counted; scales
 // are written for rows up to Mp and columns up to Np (blocks past M or N get
 // code 127, the pad).
-template <int QFMT, int COLS, int NBOX, typename Poll = NoPoll>
+template <int QFMT, int COLS, int NBOX>
 __device__ __forceinline__ void store_q(const CUtensorMap* mapQ, uint8_t* stg, uint32_t stg_s, int lane, int x0, int y0,
-                                        const Params2& p, const float* v, float scale, uint32_t& nsat, uint32_t& nnf,
-                                        const Poll& poll = Poll()) {
+                                        const Params2& p, const float* v, float scale, uint32_t& nsat, uint32_t& nnf) {
     static_assert(COLS == 128 || COLS == 64, "a slice is all or half of one 128-column scale group");
     const int r = lane, sw = (r >> 2) & 1;
     const int64_t row = (int64_t)y0 + r;
@@ -313,7 +310,6 @@ __device__ __forceinline__ void store_q(const CUtensorMap* mapQ, uint8_t* stg, u
             tma_store_2d(mapQ, x0 + 32 * b, y0, stg_s + (b % NBOX) * 1024);
             bulk_commit();
         }
-        poll();
     }
     if (row < p.Mp && (int64_t)x0 < p.Np) {  // pads of the last 128-column group included (code 127)
         const int64_t tile = (row / 128) * p.nbn128 + x0 / 128;
@@ -467,10 +463,9 @@ __global__ void __launch_bounds__(Cfg<REC>::THREADS, 1)
     const uint32_t mma_done = sb + C::OFF_BAR + 8u * (2 * STAGES + 2 * NACC);
     auto sfull = [&](int r) { return sb + C::OFF_BAR + 8u * (2 * STAGES + 2 * NACC + 1 + r); };
     auto sempty = [&](int r) { return sb + C::OFF_BAR + 8u * (2 * STAGES + 2 * NACC + 1 + C::SR + r); };
-    // MXFP8: stage s's scale tiles have landed in this CTA (sfl) / are in both
-    // CTAs' TMEM (sfr, the leader's, one arrival per lane-quarter warp and CTA)
-    auto sfl = [&](int st) { return sb + C::OFF_BAR + 8u * (2 * STAGES + 2 * NACC + 1 + 2 * C::SR + st); };
-    auto sfr = [&](int st) { return sb + C::OFF_BAR + 8u * (2 * STAGES + 2 * NACC + 1 + 2 * C::SR + C::NSFB + st); };
+    // MXFP8: stage s's scale tiles are in both CTAs' TMEM (the leader's
+    // barrier; the copier's commit arrives once the copies are complete)
+    auto sfr = [&](int st) { return sb + C::OFF_BAR + 8u * (2 * STAGES + 2 * NACC + 1 + 2 * C::SR + st); };
     uint32_t* tmem_slot = (uint32_t*)(smem + C::OFF_MISC);
     volatile int* abort_flag = (volatile int*)(smem + C::OFF_MISC + 4);
 
@@ -491,10 +486,7 @@ __global__ void __launch_bounds__(Cfg<REC>::THREADS, 1)
             mbar_init(sfull(r), REC == REC_B2D ? 2 : 1);
             mbar_init(sempty(r), C::EPI_WARPS);
         }
-        for (int st = 0; st < C::NSFB; ++st) {
-            mbar_init(sfl(st), 1);
-            mbar_init(sfr(st), 2 * 4);
-        }
+        for (int st = 0; st < C::NSFB; ++st) mbar_init(sfr(st), 1);
         *abort_flag = 0;
         mbar_fence_init();
     }
@@ -533,16 +525,19 @@ __global__ void __launch_bounds__(Cfg<REC>::THREADS, 1)
                         break;
                     }
                     const uint32_t fl = mapa(full(s), 0);
-                    if (leader) mbar_expect_tx(full(s), 2 * (C::A_STAGE + C::B_STAGE));
+                    // MXFP8: each CTA's scale tiles (its A rows' tile, B's one or two)
+                    // land on the leader's stage barrier with the operands
+                    if (leader)
+                        mbar_expect_tx(full(s), 2 * (C::A_STAGE + C::B_STAGE) +
+                                                    (REC == REC_MX ? 2 * (512 + (b2 ? 1024u : 512u)) : 0u));
                     tma_load_2d_pair(sb + C::OFF_A + s * C::A_STAGE, &tmA, (int)(kb * BK), (int)(mp * 256 + BM * cr), fl);
                     tma_load_2d_pair(sb + C::OFF_B + s * C::B_STAGE, &tmB, (int)(kb * BK), (int)(nb * BN + BH * cr), fl);
-                    if (REC == REC_MX) {  // scale tiles into this CTA, for its epilogue warps to move to TMEM
-                        mbar_expect_tx(sfl(s), 512 + (b2 ? 1024u : 512u));
-                        tma_load_2d(sb + C::OFF_SFA + s * 512, &tmSFA, 0, (int)((2 * mp + cr) * p.nkb + kb), sfl(s));
-                        tma_load_2d(sb + C::OFF_SFB + s * 1024, &tmSFB, 0, (int)((2 * nb) * p.nkb + kb), sfl(s));
+                    if (REC == REC_MX) {
+                        tma_load_2d_pair(sb + C::OFF_SFA + s * 512, &tmSFA, 0, (int)((2 * mp + cr) * p.nkb + kb), fl);
+                        tma_load_2d_pair(sb + C::OFF_SFB + s * 1024, &tmSFB, 0, (int)((2 * nb) * p.nkb + kb), fl);
                         if (b2)
-                            tma_load_2d(sb + C::OFF_SFB + s * 1024 + 512, &tmSFB, 0, (int)((2 * nb + 1) * p.nkb + kb),
-                                        sfl(s));
+                            tma_load_2d_pair(sb + C::OFF_SFB + s * 1024 + 512, &tmSFB, 0,
+                                             (int)((2 * nb + 1) * p.nkb + kb), fl);
                     }
                     if (++s == STAGES) {
                         s = 0;
@@ -640,36 +635,75 @@ __global__ void __launch_bounds__(Cfg<REC>::THREADS, 1)
             tc2_commit_local(mma_done);
             mbar_drain(mma_done, 0, p.wait_ns);
         }
-    } else if (C::BLOCKWISE && warp == C::SCALE_WARP) {
-        // ------------------------------------------------ scale producer (blockwise, both CTAs)
-        // the scales of every K block (partial) of each tile in turn: this
-        // CTA's A-row scales, and the tile's B scales, into the next ring slot
-        if (lane == 0 && !p.stall) {  // a stalled launch (diagnostic) loads nothing
-            uint32_t kbp = 0;
-            bool ok = true;
-            for (int64_t t = cid; t < npt && ok; t += ncl) {
-                int64_t mp, nb;
-                tile_coords(t, p.tiles_m2, p.tiles_n, mp, nb);
-                const int64_t rs = mp * 256 + BM * cr;  // this CTA's first row
-                const bool arow = rs < p.Mp;           // else all its rows are past M: no A scales
-                // 1 x KB B scales of the tile's columns that exist (Np is a multiple of 128)
-                const uint32_t bbytes = (p.Np - nb * BN >= BN) ? 4u * BN : 4u * (uint32_t)(p.Np - nb * BN);
-                for (int64_t kq = 0; kq < p.nkbq; ++kq, ++kbp) {
-                    const uint32_t r = kbp % C::SR;
-                    if (!mbar_wait2(sempty(r), ((kbp / C::SR) & 1u) ^ 1u, abort_flag, p.wait_ns)) {
-                        ok = false;
-                        break;
+    } else if ((REC == REC_MX || C::BLOCKWISE) && warp == C::SCALE_WARP) {
+        if constexpr (REC == REC_MX) {
+            // ------------------------------------------------ scale-tile copier (MXFP8, leader only)
+            // stage s's scale tiles from both CTAs' shared memory into their TMEM
+            // (tcgen05.cp.cta_group::2, the replicated 32-row layout the
+            // block-scaled MMA reads), then a commit that the MMA issuer waits on;
+            // a stage's TMEM slot is rewritten only after its operands landed
+            // again, i.e. after the MMAs that read it
+            if (leader && lane == 0) {
+                int s = 0;
+                uint32_t ph = 0;
+                bool ok = true, any = false;
+                int last_s = 0;
+                uint32_t last_ph = 0;
+                for (int64_t t = cid; t < npt && ok; t += ncl) {
+                    for (int64_t kb = 0; kb < p.nkb; ++kb) {
+                        if (!mbar_wait2(full(s), ph, abort_flag, p.wait_ns)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t sft = tmem + SF_TMEM_COL + 12u * s;
+                        tc2_cp_32x128b(sft, smem_desc(sb + C::OFF_SFA + s * 512, 0, 128, 0));
+                        tc2_cp_32x128b(sft + 4, smem_desc(sb + C::OFF_SFB + s * 1024, 0, 128, 0));
+                        tc2_cp_32x128b(sft + 8, smem_desc(sb + C::OFF_SFB + s * 1024 + 512, 0, 128, 0));
+                        tc2_commit_local(sfr(s));
+                        any = true;
+                        last_s = s;
+                        last_ph = ph;
+                        if (++s == STAGES) {
+                            s = 0;
+                            ph ^= 1u;
+                        }
                     }
-                    const uint32_t dst = sb + C::OFF_SCL + r * C::SLOT;
-                    mbar_expect_tx(sfull(r), (arow ? 512u : 0u) + (REC == REC_B1D ? bbytes : 0u));
-                    if (arow) bulk_load(dst, p.bsa + kq * p.Mp + rs, 512, sfull(r));
-                    if (REC == REC_B1D) bulk_load(dst + 512, p.bsb + kq * p.Np + nb * BN, bbytes, sfull(r));
-                    if (REC == REC_B2D) {  // the scales of the tile's KB-row B blocks (BN / KB, at least one)
-                        const int64_t b0 = (nb * BN) / KB;
-#pragma unroll
-                        for (int u = 0; u < (BN >= KB ? BN / KB : 1); ++u)
-                            if (b0 + u < p.nbnq) cp_async_4(dst + 512 + 4 * u, p.bsb + (b0 + u) * p.nkbq + kq);
-                        cp_async_arrive(sfull(r));
+                }
+                // the copies are complete before this CTA can free TMEM (bounded)
+                if (any) mbar_drain(sfr(last_s), last_ph, p.wait_ns);
+            }
+        } else if constexpr (C::BLOCKWISE) {
+            // ------------------------------------------------ scale producer (blockwise, both CTAs)
+            // the scales of every K block (partial) of each tile in turn: this
+            // CTA's A-row scales, and the tile's B scales, into the next ring slot
+            if (lane == 0 && !p.stall) {  // a stalled launch (diagnostic) loads nothing
+                uint32_t kbp = 0;
+                bool ok = true;
+                for (int64_t t = cid; t < npt && ok; t += ncl) {
+                    int64_t mp, nb;
+                    tile_coords(t, p.tiles_m2, p.tiles_n, mp, nb);
+                    const int64_t rs = mp * 256 + BM * cr;  // this CTA's first row
+                    const bool arow = rs < p.Mp;           // else all its rows are past M: no A scales
+                    // 1 x KB B scales of the tile's columns that exist (Np is a multiple of 128)
+                    const uint32_t bbytes = (p.Np - nb * BN >= BN) ? 4u * BN : 4u * (uint32_t)(p.Np - nb * BN);
+                    for (int64_t kq = 0; kq < p.nkbq; ++kq, ++kbp) {
+                        const uint32_t r = kbp % C::SR;
+                        if (!mbar_wait2(sempty(r), ((kbp / C::SR) & 1u) ^ 1u, abort_flag, p.wait_ns)) {
+                            ok = false;
+                            break;
+                        }
+                        const uint32_t dst = sb + C::OFF_SCL + r * C::SLOT;
+                        mbar_expect_tx(sfull(r), (arow ? 512u : 0u) + (REC == REC_B1D ? bbytes : 0u));
+                        if (arow) bulk_load(dst, p.bsa + kq * p.Mp + rs, 512, sfull(r));
+                        if (REC == REC_B1D) bulk_load(dst + 512, p.bsb + kq * p.Np + nb * BN, bbytes, sfull(r));
+                        if (REC == REC_B2D) {  // the scales of the tile's KB-row B blocks (BN / KB, at least one)
+                            const int64_t b0 = (nb * BN) / KB;
+    #pragma unroll
+                            for (int u = 0; u < (BN >= KB ? BN / KB : 1); ++u)
+                                if (b0 + u < p.nbnq) cp_async_4(dst + 512 + 4 * u, p.bsb + (b0 + u) * p.nkbq + kq);
+                            cp_async_arrive(sfull(r));
+                        }
                     }
                 }
             }
@@ -688,65 +722,11 @@ __global__ void __launch_bounds__(Cfg<REC>::THREADS, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive_remote(mapa(tempty(b), 0));
         };
-        // MXFP8: these warps also move each K block's scale tiles from shared
-        // memory into TMEM with tcgen05.st (keeping the copies off the MMA
-        // issue stream): every lane quarter gets the tile's 32 rows of 16 bytes,
-        // the replicated layout the block-scaled MMA reads.  The two warps of a
-        // lane quarter take alternate K blocks, running up to STAGES - 1 K
-        // blocks past the tile being drained (further would wait on MMAs that
-        // wait on this warp's release of the accumulator).
         uint32_t q_sat = 0, q_nf = 0;  // fused output quantization's counters
-        uint64_t g_sf = (uint64_t)j;
-        const uint64_t my_tiles = npt > cid ? (uint64_t)((npt - cid + ncl - 1) / ncl) : 0;
-        const uint64_t total_kb = my_tiles * (uint64_t)p.nkb;
-        bool sf_ok = true;
-        auto move_one_sf = [&](int st) {  // stage st's scale tiles have landed: into TMEM
-            const uint4 sa4 = *(const uint4*)(smem + C::OFF_SFA + st * 512 + lane * 16);
-            const uint4 sb0 = *(const uint4*)(smem + C::OFF_SFB + st * 1024 + lane * 16);
-            const uint4 sb1 = *(const uint4*)(smem + C::OFF_SFB + st * 1024 + 512 + lane * 16);
-            const uint32_t sft = tmem + lane_base + SF_TMEM_COL + 12u * st;
-            tc_st_x4(sft, sa4);
-            tc_st_x4(sft + 4, sb0);
-            tc_st_x4(sft + 8, sb1);
-            tc_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_remote(mapa(sfr(st), 0));
-            g_sf += 2;
-        };
-        auto move_sf_upto = [&](uint64_t limit) {
-            if constexpr (REC == REC_MX) {
-                while (sf_ok && g_sf < limit) {
-                    const int st = (int)(g_sf % STAGES);
-                    if (!mbar_wait2(sfl(st), (uint32_t)((g_sf / STAGES) & 1u), abort_flag, p.wait_ns)) {
-                        sf_ok = false;
-                        break;
-                    }
-                    move_one_sf(st);
-                }
-            }
-        };
-        // while the warp drains and stores a tile: move the next K block's
-        // scale tiles if they have landed (a non-blocking test: a try_wait here
-        // held each of a tile's eight store boxes while the scales were still
-        // in flight, about 15 us a tile at K = 1024), so the MMAs of the next
-        // tile do not stall on them behind this tile's stores
-        auto poll_sf = [&]() {
-            if constexpr (REC == REC_MX) {
-                if (sf_ok && g_sf < total_kb) {
-                    const int st = (int)(g_sf % STAGES);
-                    if (__all_sync(0xffffffffu, mbar_test(sfl(st), (uint32_t)((g_sf / STAGES) & 1u)))) move_one_sf(st);
-                }
-            }
-        };
         uint32_t tile_i = 0, kbg = 0;
         for (int64_t t = cid; t < npt; t += ncl, ++tile_i) {
             int64_t mp, nb;
             tile_coords(t, p.tiles_m2, p.tiles_n, mp, nb);
-            if constexpr (REC == REC_MX) {
-                const uint64_t lim = (uint64_t)(tile_i + 1) * (uint64_t)p.nkb + (uint64_t)(STAGES - 1);
-                move_sf_upto(lim < total_kb ? lim : total_kb);
-            }
             const int64_t row0 = mp * 256 + BM * cr + 32 * q;  // this warp's first row
             const int64_t col0 = nb * BN + EC * j;
             if constexpr (!C::BLOCKWISE) {
@@ -784,10 +764,10 @@ __global__ void __launch_bounds__(Cfg<REC>::THREADS, 1)
                 const float osc = (REC == REC_PC) ? 1.0f : sab;
                 if (QF == 0 || p.hasD)
                     store_slice2<OUT_F32, EC, C::STG_WARP / 1024>(&tmD, stg, stg_s, lane, (int)col0, (int)row0, (int)p.N,
-                                                                  (int)p.M, vf, osc, poll_sf);
+                                                                  (int)p.M, vf, osc);
                 if constexpr (QF == 1 || QF == 2)
                     store_q<QF - 1, EC, C::STG_WARP / 1024>(&tmQ, stg, stg_s, lane, (int)col0, (int)row0, p, vf, osc,
-                                                            q_sat, q_nf, poll_sf);
+                                                            q_sat, q_nf);
                 if constexpr (QF == 3 || QF == 4)
                     store_q128<QF - 3, C::STG_WARP / 1024>(&tmQ, stg, stg_s, lane, (int)col0, (int)row0, p, vf, osc,
                                                            q_sat, q_nf);
