@@ -414,9 +414,20 @@ def run_ours(args):
             api.scaled_gemm_mxq(q3[0], False, q3[1], False, api.E4M3, want_d=with_d, out=qy,
                                 d_out=outs[0] if with_d else None, stream=stream)
 
+        # both copies of Y (the column-wise one for the next wgrad)
+        qy2 = api.alloc(api.MXFP8_1x32, api.E4M3, T3, F, True, True, dev)
+
+        def sep_both():
+            api.scaled_gemm(q3[0], False, q3[1], False, out=outs[0], stream=stream)
+            api.quantize_into(outs[0], qy2, stream=stream)
+
+        def fused_both():
+            api.scaled_gemm_mxq(q3[0], False, q3[1], False, api.E4M3, want_d=False, out=qy2, stream=stream)
+
         fus = {}
         for name, fn in (("gemm_then_quantize", sep), ("fused_with_bf16_y", lambda: fused(True)),
-                         ("fused_fp8_only", lambda: fused(False))):
+                         ("fused_fp8_only", lambda: fused(False)), ("gemm_then_quantize_both_copies", sep_both),
+                         ("fused_both_copies_fp8_only", fused_both)):
             for _ in range(args.warmup):
                 flush.zero_()
                 fn()
@@ -431,7 +442,8 @@ def run_ours(args):
         mx["fprop_next_quantize_ms"] = fus
         mx["fprop_fused_tflops"] = round(f3 / fus["fused_fp8_only"] / 1e9, 1)
         errs |= api.device_errors()
-        launches += 6 * args.steps + 4 * args.steps
+        launches += 6 * args.steps + 7 * args.steps
+        del qy2
 
     # ---- the same quantize phase as two separate calls
     def two_calls():
@@ -453,10 +465,22 @@ def run_ours(args):
         api.scaled_gemm_q(qx, False, qw, False, api.BLOCK_1x128, api.E4M3, want_d=with_d, out=qy1,
                           d_out=Y if with_d else None, stream=stream)
 
+    qy12 = api.alloc(api.BLOCK_1x128, api.E4M3, T, F, True, True, dev)  # both copies of Y
+
+    def gemm_then_quantize_both():
+        api.scaled_gemm(qx, False, qw, False, out=Y, stream=stream)
+        api.quantize_into(Y, qy12, stream=stream)
+
+    def fused_both():
+        api.scaled_gemm_q(qx, False, qw, False, api.BLOCK_1x128, api.E4M3, want_d=False, out=qy12, stream=stream)
+
     bfus = {name: round(_time_ms(fn, args.steps, args.warmup, flush), 4)
             for name, fn in (("gemm_then_quantize", gemm_then_quantize), ("fused_with_bf16_y", lambda: fused_next(True)),
-                             ("fused_fp8_only", lambda: fused_next(False)))}
-    launches += 4 * args.steps
+                             ("fused_fp8_only", lambda: fused_next(False)),
+                             ("gemm_then_quantize_both_copies", gemm_then_quantize_both),
+                             ("fused_both_copies_fp8_only", fused_both))}
+    launches += 7 * args.steps
+    del qy12
     errs |= api.device_errors()
 
     # ---- scaling granularity at the bench shape ("mastering FP8 LLM training

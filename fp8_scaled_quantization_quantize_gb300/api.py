@@ -273,10 +273,11 @@ def scaled_gemm(A: QTensor, a_use_col: bool, B: QTensor, b_use_col: bool, out_dt
 
 def scaled_gemm_q(A: QTensor, a_use_col: bool, B: QTensor, b_use_col: bool, kind: int = MXFP8_1x32,
                   fmt: int = E4M3, want_d: bool = True, out: QTensor | None = None,
-                  d_out: torch.Tensor | None = None, stream=None):
-    """The GEMM with its bf16 output also quantized row-wise in the epilogue
-    (fp8q_scaled_gemm_q), kind MXFP8_1x32 or BLOCK_1x128: returns
-    (D bf16 or None, QTensor)."""
+                  d_out: torch.Tensor | None = None, stream=None, colwise: bool = False):
+    """The GEMM with its bf16 output also quantized in the epilogue
+    (fp8q_scaled_gemm_q), kind MXFP8_1x32 or BLOCK_1x128: the row-wise copy,
+    and with colwise (or an `out` holding a column copy) the column-wise copy
+    too (blocks along M; M % 16 == 0).  Returns (D bf16 or None, QTensor)."""
     M = A.cols if a_use_col else A.rows
     K = A.rows if a_use_col else A.cols
     N = B.cols if b_use_col else B.rows
@@ -284,11 +285,19 @@ def scaled_gemm_q(A: QTensor, a_use_col: bool, B: QTensor, b_use_col: bool, kind
     if kind not in (MXFP8_1x32, BLOCK_1x128):
         raise ValueError("kind must be MXFP8_1x32 or BLOCK_1x128")
     if out is None:
-        out = alloc(kind, fmt, M, N, True, False, dev)
+        out = alloc(kind, fmt, M, N, True, colwise, dev)
     if (out.rows, out.cols) != (M, N) or out.data_row is None or out.scale_row is None or out.kind != kind:
         raise ValueError(f"out must hold a row-wise copy of kind {kind} and shape {(M, N)}")
-    if out.scale_row.numel() < scale_bytes(kind, M, N, True, False)[0]:
+    rb, cb = scale_bytes(kind, M, N, True, out.data_col is not None)
+    if out.scale_row.numel() < rb:
         raise ValueError("out.scale_row is smaller than the recipe's scale bytes")
+    if out.data_col is not None:
+        if tuple(out.data_col.shape) != (N, M) or out.scale_col is None or out.scale_col.numel() < cb:
+            raise ValueError(f"out's column copy must be [{N}, {M}] with its scale bytes")
+        if M % 16:
+            raise ValueError("a column-wise copy needs M % 16 == 0")
+        _check_device(out.data_col, out.counters, "out's buffers")
+        _check_device(out.scale_col, out.counters, "out's buffers")
     _check_device(out.data_row, out.counters, "out's buffers")
     _check_device(out.counters, A.counters, "out's buffers")
     if want_d and d_out is None:
@@ -306,10 +315,11 @@ def scaled_gemm_q(A: QTensor, a_use_col: bool, B: QTensor, b_use_col: bool, kind
 
 def scaled_gemm_mxq(A: QTensor, a_use_col: bool, B: QTensor, b_use_col: bool, fmt: int = E4M3,
                     want_d: bool = True, out: QTensor | None = None, d_out: torch.Tensor | None = None,
-                    stream=None):
-    """The GEMM with its bf16 output also quantized MXFP8 1x32 row-wise in the
-    epilogue (fp8q_scaled_gemm_mxq): returns (D bf16 or None, QTensor)."""
-    return scaled_gemm_q(A, a_use_col, B, b_use_col, MXFP8_1x32, fmt, want_d, out, d_out, stream)
+                    stream=None, colwise: bool = False):
+    """The GEMM with its bf16 output also quantized MXFP8 1x32 in the epilogue
+    (fp8q_scaled_gemm_mxq), row-wise and optionally column-wise: returns
+    (D bf16 or None, QTensor)."""
+    return scaled_gemm_q(A, a_use_col, B, b_use_col, MXFP8_1x32, fmt, want_d, out, d_out, stream, colwise)
 
 
 def gemm_set_variant(variant: int):

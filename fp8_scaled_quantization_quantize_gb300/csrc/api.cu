@@ -416,6 +416,12 @@ fp8q_status fp8q_scaled_gemm_q(const fp8q_tensor* A, int a_use_col, const fp8q_t
     if (!Dq->data_row || !Dq->scale_row || !Dq->counters) return FP8Q_ERR_ARG;
     if (!aligned16(Dq->data_row) || !aligned16(Dq->scale_row) || (D && !aligned16(D))) return FP8Q_ERR_ALIGN;
     if (((uintptr_t)Dq->counters & 7u) != 0) return FP8Q_ERR_ALIGN;
+    const bool col = Dq->data_col != nullptr;  // the column-wise copy too
+    if (col) {
+        if (!Dq->scale_col) return FP8Q_ERR_ARG;
+        if (M % 16 != 0) return FP8Q_ERR_SHAPE;  // rows of the [N][M] copy are 16-byte multiples
+        if (!aligned16(Dq->data_col) || !aligned16(Dq->scale_col)) return FP8Q_ERR_ALIGN;
+    }
     GemmOperand ga, gb;
     const fp8q_status v = prepare_operands(A, a_use_col, B, b_use_col, M, N, K, ga, gb);
     if (v != FP8Q_OK) return v;
@@ -424,7 +430,7 @@ fp8q_status fp8q_scaled_gemm_q(const fp8q_tensor* A, int a_use_col, const fp8q_t
     Dq->fmt = fmt;
     Dq->kind = out_kind;
     return launch_gemm_pair(ga, gb, D, 0, M, N, K, (cudaStream_t)stream, out_kind, fmt, Dq->data_row, Dq->scale_row,
-                            Dq->counters);
+                            Dq->counters, col ? Dq->data_col : nullptr, col ? Dq->scale_col : nullptr);
 }
 
 fp8q_status fp8q_scaled_gemm_mxq(const fp8q_tensor* A, int a_use_col, const fp8q_tensor* B, int b_use_col, void* D,

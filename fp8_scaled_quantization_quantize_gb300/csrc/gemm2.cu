@@ -25,6 +25,12 @@
 // the MMAs of K block g + 2 wait for the epilogue to release block g, which
 // is what limits this recipe (measured: about 445 cycles from a partial's
 // arrival to its release against about 600 cycles of MMAs per K block).
+// The epilogue can also quantize D for the next layer (MXFP8 1x32 or 1x128,
+// row-wise along N and optionally column-wise along M, the transposed copy a
+// wgrad reads): the row blocks lie in a warp's registers, a 32-row column
+// block is a warp's rows (a warp maximum), a 128-row one the rows of the four
+// warps of a column half (an exchange through shared memory on a bounded
+// mbarrier).
 // TMEM per CTA: per-tensor two 256-column accumulators; MXFP8 one accumulator
 // plus 12 scale columns per stage; blockwise two 256-column partial buffers,
 // so the MMAs run one K block ahead of the epilogue.
@@ -82,6 +88,13 @@ struct Cfg {
     static constexpr uint32_t NBARS = 2 * STAGES + 2 * NACC + 1 + 2 * SR + NSFB;
     static constexpr uint32_t OFF_MISC = OFF_BAR + 8 * NBARS;
     static constexpr uint32_t SMEM = OFF_MISC + 16 + 1024;
+    // the fused 1x128 column copy's exchange of column maxima: [tile parity]
+    // [column half][4 warps][128 columns] words, then its four mbarriers
+    // ([tile parity][column half]); only kernels with that copy allocate it
+    static constexpr uint32_t OFF_XB = OFF_MISC + 16;
+    static constexpr uint32_t OFF_XBAR = OFF_XB + 2 * 2 * 4 * 128 * 4;
+    static constexpr uint32_t SMEM_XB = OFF_XBAR + 4 * 8 + 1024;
+    static_assert(SMEM_XB <= 232448, "shared memory budget of one CTA with the column exchange");
     static_assert(SMEM <= 232448, "shared memory budget of one CTA");
 };
 
@@ -98,10 +111,10 @@ struct Params2 {
     const float* bsb;
     int64_t Mp, Np;
     uint32_t idesc;
-    // fused row-wise quantization of the bf16 output (QF != 0: MXFP8 for
-    // QF 1, 2, 1x128 for QF 3, 4)
+    // fused quantization of the bf16 output (QOut<QF> below)
     uint8_t* qscale;                 // MXFP8: packed 128x4 E8M0 tiles; 1x128: fp32 [ceil(N/128)][Mp]
-    unsigned long long* qcounters;   // [0] saturated, [2] NaN / Inf elements
+    void* qscale_col;                // column copy: MXFP8 packed tiles of [N][ceil(M/32)]; 1x128 fp32 [ceil(M/128)][Np]
+    unsigned long long* qcounters;   // [0] saturated (row copy), [1] saturated (column copy), [2] NaN / Inf
     int hasD;                        // also store the bf16 D
     uint64_t wait_ns;                // bounded-wait limit
     int stall;                       // 1: the producers issue no loads (diagnostic)
@@ -441,6 +454,238 @@ __device__ __forceinline__ void store_q128(const CUtensorMap* mapQ, uint8_t* stg
     if (row < p.Mp && (int64_t)x0 < p.N) ((float*)p.qscale)[(int64_t)(x0 / 128) * p.Mp + row] = d;
 }
 
+// The column-wise copy of the fused output quantization (codes of D^T, blocks
+// along M): shared by the MXFP8 and 1x128 column paths below.
+//
+// Four FP8 codes (byte k from element k) with a NaN element given its sign:
+// the hardware's NaN code is 0x7F whatever the sign.  w0 holds bf16 elements
+// 0, 1 and w1 elements 2, 3.
+__device__ __forceinline__ uint32_t nan_signs4(uint32_t c, uint32_t w0, uint32_t w1) {
+    uint32_t lo = c & 0xFFFFu, hi = c >> 16;
+    if ((w0 & 0x7FFFu) > 0x7F80u) lo = (lo & ~0xFFu) | ((w0 >> 8) & 0x80u) | 0x7Fu;
+    if ((w0 & 0x7FFF0000u) > 0x7F800000u) lo = (lo & ~0xFF00u) | ((w0 >> 16) & 0x8000u) | 0x7F00u;
+    if ((w1 & 0x7FFFu) > 0x7F80u) hi = (hi & ~0xFFu) | ((w1 >> 8) & 0x80u) | 0x7Fu;
+    if ((w1 & 0x7FFF0000u) > 0x7F800000u) hi = (hi & ~0xFF00u) | ((w1 >> 16) & 0x8000u) | 0x7F00u;
+    return lo | (hi << 16);
+}
+// This lane's (row m's) codes of 32 columns (column 4 i + k in byte k of
+// c[i]) into a 32 x 32 box of the transposed copy: the 32 codes of column n
+// (rows 0 .. 31, one per lane) are row n of the box, 32 bytes, no swizzle.
+__device__ __forceinline__ void put_transposed(uint8_t* box, int lane, const uint32_t (&c)[8]) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) box[(4 * i + k) * 32 + lane] = (uint8_t)(c[i] >> (8 * k));
+}
+// This lane's 128 values of D as stored in bf16 (RN(v scale)), two to a word:
+// the column paths work on these, so the fp32 values are dead by then.
+__device__ __forceinline__ void bf16_row(const float* v, float scale, uint32_t (&h)[64]) {
+#pragma unroll
+    for (int i = 0; i < 64; ++i) h[i] = pack_bf16(v[2 * i] * scale, v[2 * i + 1] * scale);
+}
+// Chunk b (columns 32 b .. 32 b + 31) of the row, picked by selects so that
+// the chunk loops stay rolled and the row stays in registers.
+__device__ __forceinline__ void take_chunk(const uint32_t (&hr)[64], int b, uint32_t (&h)[16]) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const uint32_t lo = (b & 1) ? hr[16 + i] : hr[i];
+        const uint32_t hi = (b & 1) ? hr[48 + i] : hr[32 + i];
+        h[i] = (b & 2) ? hi : lo;
+    }
+}
+// The 32 column maxima of a chunk over the warp's 32 rows (finite
+// magnitudes; rows past M count as 0): the maximum of column c is kept by
+// lane c.  *nf: this lane's row holds a NaN / Inf in the chunk.
+__device__ __forceinline__ uint32_t chunk_col_max(const uint32_t (&h)[16], bool row_live, int lane, bool* nf) {
+    uint32_t mine = 0;
+    bool anynf = false;
+#pragma unroll
+    for (int c = 0; c < 32; ++c) {
+        const uint32_t a = (h[c / 2] >> (16 * (c & 1))) & 0x7FFFu;
+        const bool fin = a < 0x7F80u;
+        anynf |= row_live && !fin;
+        const uint32_t mc = __reduce_max_sync(0xFFFFFFFFu, (row_live && fin) ? a : 0u);
+        if (lane == c) mine = mc;
+    }
+    *nf = anynf;
+    return mine;
+}
+
+// MXFP8 column-wise copy (1x32 blocks along M) of this warp's 32 rows x 128
+// columns of D as stored in bf16: the block of column n is the warp's rows
+// y0 .. y0 + 31 (one per lane; y0 is a multiple of 32), so its amax is one
+// warp maximum of the finite magnitudes.  e, the codes sat_rne(x 2^-e), the
+// NaN signs and the saturation count (finite |y| > fmax) as the row path;
+// the codes leave transposed ([N][M], uint8 32 x 32 boxes by TMA) and each
+// column's E8M0 byte goes to the packed 128x4 tiles of the [N][ceil(M/32)]
+// scale matrix -- the quantize kernel's MXFP8 column copy of these values.
+template <int QFMT>
+__device__ __forceinline__ void store_qc_mx(const CUtensorMap* mapQc, uint8_t* stg, uint32_t stg_s, int lane, int x0,
+                                            int y0, const Params2& p, const uint32_t (&hr)[64], uint32_t& nsat) {
+    const bool row_live = (int64_t)y0 + lane < p.M;
+    bulk_wait_read();  // the row codes' boxes have left the staging area
+    __syncwarp();
+#pragma unroll 1
+    for (int b = 0; b < 4; ++b) {
+        uint32_t h[16];
+        take_chunk(hr, b, h);
+        bool nf;
+        const uint32_t mine = chunk_col_max(h, row_live, lane, &nf);
+        const int64_t n = (int64_t)x0 + 32 * b + lane;  // this lane's column
+        const int e = mx_exponent<QFMT>(mine << 16);
+        const float k = exp2_neg(e);
+        const uint32_t satm = __ballot_sync(0xFFFFFFFFu, __uint_as_float(mine << 16) * k > Fmt<QFMT>::fmax);
+        const bool anynf = __any_sync(0xFFFFFFFFu, nf);
+        if (n < p.Np && (int64_t)y0 < p.Mp) {  // pads (columns past N, blocks past M) get 127
+            const int64_t tile = (n / 128) * p.tiles_m128 + y0 / 128;
+            ((uint8_t*)p.qscale_col)[tile * 512 + (n % 32) * 16 + ((n % 128) / 32) * 4 + (y0 / 32) % 4] =
+                (uint8_t)(e + 127);
+        }
+        uint32_t c[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float k0 = __shfl_sync(0xFFFFFFFFu, k, 4 * i), k1 = __shfl_sync(0xFFFFFFFFu, k, 4 * i + 1);
+            const float k2 = __shfl_sync(0xFFFFFFFFu, k, 4 * i + 2), k3 = __shfl_sync(0xFFFFFFFFu, k, 4 * i + 3);
+            const uint32_t w0 = h[2 * i], w1 = h[2 * i + 1];
+            const float2 ya = __fmul2_rn(make_float2(__uint_as_float(w0 << 16), __uint_as_float(w0 & 0xFFFF0000u)),
+                                         make_float2(k0, k1));
+            const float2 yb = __fmul2_rn(make_float2(__uint_as_float(w1 << 16), __uint_as_float(w1 & 0xFFFF0000u)),
+                                         make_float2(k2, k3));
+            c[i] = cvt4<QFMT>(ya.x, ya.y, yb.x, yb.y);
+            const uint32_t sm = (satm >> (4 * i)) & 0xFu;
+            if (sm) {  // a saturating block: count its finite elements past fmax
+                const float y[4] = {ya.x, ya.y, yb.x, yb.y};
+#pragma unroll
+                for (int t = 0; t < 4; ++t)
+                    nsat += ((sm >> t) & 1u) && fabsf(y[t]) <= 3.402823466e38f && fabsf(y[t]) > Fmt<QFMT>::fmax;
+            }
+            if (anynf) c[i] = nan_signs4(c[i], w0, w1);
+        }
+        uint8_t* box = stg + b * 1024;
+        put_transposed(box, lane, c);
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0 && (int64_t)x0 + 32 * b < p.N && (int64_t)y0 < p.M) {
+            tma_store_2d(mapQc, y0, x0 + 32 * b, stg_s + b * 1024);
+            bulk_commit();
+        }
+    }
+}
+
+// 1x128 column-wise copy (blocks of 128 rows of one column) of this warp's
+// 32 rows x 128 columns of D as stored in bf16.  A CTA's 128 tile rows are
+// one 128-row group, so the block of column n is the rows of the four warps
+// of this column half: each warp takes its 32-row maxima by warp maxima of
+// the finite magnitudes, the four meet in shared memory (xb: [4 warps][128
+// columns], one arrival per warp on the mbarrier xbar, whose wait is bounded
+// like every other), and each lane turns the maxima of its column in each
+// chunk into d = RN(amax / fmax); the codes sat_rne(x / d) (Markstein's
+// division from RN(1 / d), or IEEE division for d below 2^-80 or a block
+// holding NaN / Inf, with the NaN signs), saturation counted at the elements
+// equal to a saturating block's maximum (the row path's argument); codes
+// transposed by TMA, d into the [ceil(M/128)][Np] scale array by the first
+// warp -- the quantize kernel's 1x128 column copy of these values.  Returns
+// false when the exchange's wait gave up (the caller leaves its tile loop).
+template <int QFMT>
+__device__ __forceinline__ bool store_qc128(const CUtensorMap* mapQc, uint8_t* stg, uint32_t stg_s, int lane, int q,
+                                            int x0, int y0, const Params2& p, const uint32_t (&hr)[64],
+                                            uint32_t& nsat, uint32_t* xb, uint32_t xbar, uint32_t xph,
+                                            volatile int* abort_flag) {
+    const bool row_live = (int64_t)y0 + lane < p.M;
+#pragma unroll 1
+    for (int b = 0; b < 4; ++b) {
+        uint32_t h[16];
+        take_chunk(hr, b, h);
+        bool nf;
+        const uint32_t mine = chunk_col_max(h, row_live, lane, &nf);
+        bool nfc = false;
+        if (__any_sync(0xFFFFFFFFu, nf)) {  // which columns hold a NaN / Inf (rare)
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+                const uint32_t a = (h[c / 2] >> (16 * (c & 1))) & 0x7FFFu;
+                const uint32_t bal = __ballot_sync(0xFFFFFFFFu, row_live && a >= 0x7F80u);
+                if (lane == c) nfc = bal != 0u;
+            }
+        }
+        xb[q * 128 + 32 * b + lane] = mine | (nfc ? 0x10000u : 0u);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(xbar);
+    if (!mbar_wait2(xbar, xph, abort_flag, p.wait_ns)) return false;
+    bulk_wait_read();  // the row codes' boxes have left the staging area
+    __syncwarp();
+#pragma unroll 1
+    for (int b = 0; b < 4; ++b) {
+        // this lane's column of the chunk: the block maximum over the four warps, d, -RN(1 / d)
+        uint32_t m = 0, f = 0;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            const uint32_t x = xb[w * 128 + 32 * b + lane];
+            m = max(m, x & 0xFFFFu);
+            f |= x >> 16;
+        }
+        const float d = block_scale<QFMT>(__uint_as_float(m << 16));
+        const bool fastl = f == 0u && d >= 0x1p-80f;
+        const float nrd = fastl ? -rcp_rn(d) : -1.0f;
+        const bool fast = __all_sync(0xFFFFFFFFu, fastl);
+        const uint32_t satm =
+            __ballot_sync(0xFFFFFFFFu, fabsf(__fdiv_rn(__uint_as_float(m << 16), d)) > Fmt<QFMT>::fmax);
+        const int64_t n = (int64_t)x0 + 32 * b + lane;
+        if (q == 0 && n < p.Np && (int64_t)y0 < p.Mp)  // y0: the 128-row group's first row (pads: d = 1)
+            ((float*)p.qscale_col)[(int64_t)(y0 / 128) * p.Np + n] = d;
+        uint32_t h[16];
+        take_chunk(hr, b, h);
+        uint32_t c[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t w0 = h[2 * i], w1 = h[2 * i + 1];
+            const float2 a0 = make_float2(__uint_as_float(w0 << 16), __uint_as_float(w0 & 0xFFFF0000u));
+            const float2 a1 = make_float2(__uint_as_float(w1 << 16), __uint_as_float(w1 & 0xFFFF0000u));
+            const float d0 = __shfl_sync(0xFFFFFFFFu, d, 4 * i), d1 = __shfl_sync(0xFFFFFFFFu, d, 4 * i + 1);
+            const float d2 = __shfl_sync(0xFFFFFFFFu, d, 4 * i + 2), d3 = __shfl_sync(0xFFFFFFFFu, d, 4 * i + 3);
+            if (fast) {
+                const float r0 = __shfl_sync(0xFFFFFFFFu, nrd, 4 * i), r1 = __shfl_sync(0xFFFFFFFFu, nrd, 4 * i + 1);
+                const float r2 = __shfl_sync(0xFFFFFFFFu, nrd, 4 * i + 2), r3 = __shfl_sync(0xFFFFFFFFu, nrd, 4 * i + 3);
+                const float2 ya = div2_neg(a0, make_float2(d0, d1), make_float2(r0, r1));
+                const float2 yb = div2_neg(a1, make_float2(d2, d3), make_float2(r2, r3));
+                c[i] = cvt4<QFMT>(ya.x, ya.y, yb.x, yb.y) ^ 0x80808080u;
+            } else {
+                c[i] = cvt4<QFMT>(__fdiv_rn(a0.x, d0), __fdiv_rn(a0.y, d1), __fdiv_rn(a1.x, d2), __fdiv_rn(a1.y, d3));
+                c[i] = nan_signs4(c[i], w0, w1);
+            }
+            const uint32_t sm = (satm >> (4 * i)) & 0xFu;
+            if (sm) {  // only elements equal to a saturating block's maximum exceed fmax
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    const uint32_t mt = __shfl_sync(0xFFFFFFFFu, m, 4 * i + t);
+                    const uint32_t a = ((t < 2 ? w0 : w1) >> (16 * (t & 1))) & 0x7FFFu;
+                    nsat += ((sm >> t) & 1u) && row_live && a == mt;
+                }
+            }
+        }
+        uint8_t* box = stg + b * 1024;
+        put_transposed(box, lane, c);
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0 && (int64_t)x0 + 32 * b < p.N && (int64_t)y0 < p.M) {
+            tma_store_2d(mapQc, y0, x0 + 32 * b, stg_s + b * 1024);
+            bulk_commit();
+        }
+    }
+    return true;
+}
+
+// QF, the fused quantization of the bf16 output: 0 none; 1, 2 MXFP8 1x32
+// (E4M3, E5M2) and 3, 4 1x128, row-wise along N; 5, 6 and 7, 8 the same with
+// the column-wise copy (blocks along M) as well.
+template <int QF>
+struct QOut {
+    static constexpr bool mx = QF == 1 || QF == 2 || QF == 5 || QF == 6;
+    static constexpr bool b128 = QF == 3 || QF == 4 || QF == 7 || QF == 8;
+    static constexpr bool col = QF >= 5;
+    static constexpr int fmt = (QF + 1) % 2;  // QF 1, 3, 5, 7: E4M3
+};
+
 // KB (blockwise recipes): the K block of the scales, i.e. of the partial sums
 // the epilogue promotes -- 128 for the 1x128 / 128x128 recipes, 32, 64 or 256
 // for the generic sub-channel blocks ("mastering FP8 LLM training 1.5x
@@ -450,7 +695,8 @@ template <int REC, bool OUT_F32, int QF, int KB = 128>
 __global__ void __launch_bounds__(Cfg<REC>::THREADS, 1)
     gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmSFA,
-                 const __grid_constant__ CUtensorMap tmSFB, const __grid_constant__ CUtensorMap tmQ, const Params2 p) {
+                 const __grid_constant__ CUtensorMap tmSFB, const __grid_constant__ CUtensorMap tmQ,
+                 const __grid_constant__ CUtensorMap tmQc, const Params2 p) {
     using C = Cfg<REC>;
     constexpr int BN = C::BN, BH = C::BH, STAGES = C::STAGES, NACC = C::NACC, EC = C::EPI_COLS;
     extern __shared__ uint8_t smem_raw[];
@@ -487,6 +733,8 @@ __global__ void __launch_bounds__(Cfg<REC>::THREADS, 1)
             mbar_init(sempty(r), C::EPI_WARPS);
         }
         for (int st = 0; st < C::NSFB; ++st) mbar_init(sfr(st), 1);
+        if constexpr (QOut<QF>::col && QOut<QF>::b128)
+            for (int i = 0; i < 4; ++i) mbar_init(sb + C::OFF_XBAR + 8u * i, 4);
         *abort_flag = 0;
         mbar_fence_init();
     }
@@ -722,7 +970,7 @@ __global__ void __launch_bounds__(Cfg<REC>::THREADS, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive_remote(mapa(tempty(b), 0));
         };
-        uint32_t q_sat = 0, q_nf = 0;  // fused output quantization's counters
+        uint32_t q_sat = 0, q_nf = 0, q_satc = 0;  // fused output quantization's counters
         uint32_t tile_i = 0, kbg = 0;
         for (int64_t t = cid; t < npt; t += ncl, ++tile_i) {
             int64_t mp, nb;
@@ -765,12 +1013,25 @@ __global__ void __launch_bounds__(Cfg<REC>::THREADS, 1)
                 if (QF == 0 || p.hasD)
                     store_slice2<OUT_F32, EC, C::STG_WARP / 1024>(&tmD, stg, stg_s, lane, (int)col0, (int)row0, (int)p.N,
                                                                   (int)p.M, vf, osc);
-                if constexpr (QF == 1 || QF == 2)
-                    store_q<QF - 1, EC, C::STG_WARP / 1024>(&tmQ, stg, stg_s, lane, (int)col0, (int)row0, p, vf, osc,
-                                                            q_sat, q_nf);
-                if constexpr (QF == 3 || QF == 4)
-                    store_q128<QF - 3, C::STG_WARP / 1024>(&tmQ, stg, stg_s, lane, (int)col0, (int)row0, p, vf, osc,
-                                                           q_sat, q_nf);
+                if constexpr (QOut<QF>::mx)
+                    store_q<QOut<QF>::fmt, EC, C::STG_WARP / 1024>(&tmQ, stg, stg_s, lane, (int)col0, (int)row0, p, vf,
+                                                                   osc, q_sat, q_nf);
+                if constexpr (QOut<QF>::b128)
+                    store_q128<QOut<QF>::fmt, C::STG_WARP / 1024>(&tmQ, stg, stg_s, lane, (int)col0, (int)row0, p, vf,
+                                                                  osc, q_sat, q_nf);
+                if constexpr (QOut<QF>::col) {
+                    uint32_t hc[64];
+                    bf16_row(vf, osc, hc);
+                    if constexpr (QOut<QF>::mx)
+                        store_qc_mx<QOut<QF>::fmt>(&tmQc, stg, stg_s, lane, (int)col0, (int)row0, p, hc, q_satc);
+                    if constexpr (QOut<QF>::b128) {
+                        const uint32_t x = (tile_i & 1u) * 2 + (uint32_t)j;  // [tile parity][column half]
+                        if (!store_qc128<QOut<QF>::fmt>(&tmQc, stg, stg_s, lane, q, (int)col0, (int)row0, p, hc, q_satc,
+                                                        (uint32_t*)(smem + C::OFF_XB) + x * 512,
+                                                        sb + C::OFF_XBAR + 8u * x, (tile_i >> 1) & 1u, abort_flag))
+                            break;
+                    }
+                }
             } else {
                 float2 acc[EC / 2];  // packed pairs: Blackwell's two-lane FMA halves the promotion's instructions
 #pragma unroll
@@ -824,20 +1085,36 @@ __global__ void __launch_bounds__(Cfg<REC>::THREADS, 1)
                 if (QF == 0 || p.hasD)
                     store_slice2<OUT_F32, EC, C::STG_WARP / 1024>(&tmD, stg, stg_s, lane, (int)col0, (int)row0, (int)p.N,
                                                                   (int)p.M, reinterpret_cast<const float*>(acc), 1.0f);
-                if constexpr (QF == 1 || QF == 2)
-                    store_q<QF - 1, EC, C::STG_WARP / 1024>(&tmQ, stg, stg_s, lane, (int)col0, (int)row0, p,
-                                                            reinterpret_cast<const float*>(acc), 1.0f, q_sat, q_nf);
-                if constexpr (QF == 3 || QF == 4)
-                    store_q128<QF - 3, C::STG_WARP / 1024>(&tmQ, stg, stg_s, lane, (int)col0, (int)row0, p,
-                                                           reinterpret_cast<const float*>(acc), 1.0f, q_sat, q_nf);
+                const float* accf = reinterpret_cast<const float*>(acc);
+                if constexpr (QOut<QF>::mx)
+                    store_q<QOut<QF>::fmt, EC, C::STG_WARP / 1024>(&tmQ, stg, stg_s, lane, (int)col0, (int)row0, p, accf,
+                                                                   1.0f, q_sat, q_nf);
+                if constexpr (QOut<QF>::b128)
+                    store_q128<QOut<QF>::fmt, C::STG_WARP / 1024>(&tmQ, stg, stg_s, lane, (int)col0, (int)row0, p, accf,
+                                                                  1.0f, q_sat, q_nf);
+                if constexpr (QOut<QF>::col) {
+                    uint32_t hc[64];
+                    bf16_row(accf, 1.0f, hc);
+                    if constexpr (QOut<QF>::mx)
+                        store_qc_mx<QOut<QF>::fmt>(&tmQc, stg, stg_s, lane, (int)col0, (int)row0, p, hc, q_satc);
+                    if constexpr (QOut<QF>::b128) {
+                        const uint32_t x = (tile_i & 1u) * 2 + (uint32_t)j;  // [tile parity][column half]
+                        if (!store_qc128<QOut<QF>::fmt>(&tmQc, stg, stg_s, lane, q, (int)col0, (int)row0, p, hc, q_satc,
+                                                        (uint32_t*)(smem + C::OFF_XB) + x * 512,
+                                                        sb + C::OFF_XBAR + 8u * x, (tile_i >> 1) & 1u, abort_flag))
+                            break;
+                    }
+                }
             }
         }
         if (lane == 0) bulk_wait_all();
         if constexpr (QF != 0) {
             q_sat = warp_sum_u32(q_sat);
             q_nf = warp_sum_u32(q_nf);
+            q_satc = warp_sum_u32(q_satc);
             if (lane == 0) {
                 if (q_sat) atomicAdd(&p.qcounters[0], (unsigned long long)q_sat);
+                if (q_satc) atomicAdd(&p.qcounters[1], (unsigned long long)q_satc);
                 if (q_nf) atomicAdd(&p.qcounters[2], (unsigned long long)q_nf);
             }
         }
@@ -858,15 +1135,16 @@ template <int REC, bool F32, int QF, int KB = 128>
 fp8q_status launch2_t(const CUtensorMap* maps, const Params2& p, cudaStream_t s) {
     using C = Cfg<REC>;
     auto kern = gemm2_kernel<REC, F32, QF, KB>;
+    constexpr uint32_t smem = (QOut<QF>::col && QOut<QF>::b128) ? C::SMEM_XB : C::SMEM;
     static PerDevice<bool> attr;
-    if (!smem_opt_in(attr, kern, C::SMEM)) return FP8Q_ERR_CUDA;
+    if (!smem_opt_in(attr, kern, smem)) return FP8Q_ERR_CUDA;
     const int sms = sm_count();
     if (sms < 2) return FP8Q_ERR_CUDA;
     const int64_t npt = p.tiles_m2 * p.tiles_n;
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof(cfg));
     cfg.blockDim = dim3(C::THREADS, 1, 1);
-    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute la[1];
     la[0].id = cudaLaunchAttributeClusterDimension;
@@ -887,14 +1165,15 @@ fp8q_status launch2_t(const CUtensorMap* maps, const Params2& p, cudaStream_t s)
     if (max_clusters < 1) max_clusters = sms / 2;
     const int64_t ncl = npt < max_clusters ? npt : max_clusters;
     cfg.gridDim = dim3((unsigned)(2 * ncl), 1, 1);
-    if (cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p) != cudaSuccess)
+    if (cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], p) !=
+        cudaSuccess)
         return FP8Q_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? FP8Q_OK : FP8Q_ERR_CUDA;
 }
 
 template <int REC>
 fp8q_status launch2_rec(CUtensorMap* maps, const Params2& p, void* D, int out_dtype, int qkind, int qfmt,
-                        void* qdata, cudaStream_t s) {
+                        void* qdata, void* qcol, cudaStream_t s) {
     const bool f32 = out_dtype == 1;
     if (D != nullptr && !make_map_2d(&maps[2], f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                                      f32 ? 4 : 2, D, p.M, p.N, f32 ? 8 : 16, 32, CU_TENSOR_MAP_SWIZZLE_32B))
@@ -904,6 +1183,16 @@ fp8q_status launch2_rec(CUtensorMap* maps, const Params2& p, void* D, int out_dt
     if (f32 || !make_map_2d(&maps[5], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, qdata, p.M, p.N, 32, 32,
                             CU_TENSOR_MAP_SWIZZLE_32B))
         return f32 ? FP8Q_ERR_ARG : FP8Q_ERR_CUDA;
+    if (qcol != nullptr) {
+        // the column copy's codes: uint8 [N][M] in 32 x 32 boxes (no swizzle)
+        if (!make_map_2d(&maps[6], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, qcol, p.N, p.M, 32, 32, CU_TENSOR_MAP_SWIZZLE_NONE))
+            return FP8Q_ERR_CUDA;
+        if (qkind == FP8Q_BLOCK_1x128)
+            return qfmt == FP8Q_E4M3 ? launch2_t<REC, false, 7 + FP8Q_E4M3>(maps, p, s)
+                                     : launch2_t<REC, false, 7 + FP8Q_E5M2>(maps, p, s);
+        return qfmt == FP8Q_E4M3 ? launch2_t<REC, false, 5 + FP8Q_E4M3>(maps, p, s)
+                                 : launch2_t<REC, false, 5 + FP8Q_E5M2>(maps, p, s);
+    }
     if (qkind == FP8Q_BLOCK_1x128)
         return qfmt == FP8Q_E4M3 ? launch2_t<REC, false, 3 + FP8Q_E4M3>(maps, p, s)
                                  : launch2_t<REC, false, 3 + FP8Q_E5M2>(maps, p, s);
@@ -924,14 +1213,14 @@ fp8q_status read_device_errors2(unsigned int* flags) {
 
 fp8q_status launch_gemm_pair(const GemmOperand& A, const GemmOperand& B, void* D, int out_dtype, int64_t M,
                              int64_t N, int64_t K, cudaStream_t s, int qkind, int qfmt, void* qdata, void* qscale,
-                             unsigned long long* qcounters) {
+                             unsigned long long* qcounters, void* qcol, void* qscale_col) {
     if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return FP8Q_ERR_SHAPE;
     const bool mx = A.kind == FP8Q_MXFP8_1x32;
     const bool pt = A.kind == FP8Q_PERTENSOR_CURRENT || A.kind == FP8Q_PERTENSOR_DELAYED;
     const bool pc = A.kind == FP8Q_PERCHANNEL_CURRENT;
     static_assert(Cfg<REC_MX>::BN == Cfg<REC_PT>::BN && Cfg<REC_B2D>::BN == Cfg<REC_B1D>::BN, "tile widths");
     const int bn = (mx || pt || pc) ? Cfg<REC_PT>::BN : Cfg<REC_B2D>::BN;
-    CUtensorMap maps[6];
+    CUtensorMap maps[7];
     memset(maps, 0, sizeof(maps));
     Params2 p;
     memset(&p, 0, sizeof(p));
@@ -939,6 +1228,7 @@ fp8q_status launch_gemm_pair(const GemmOperand& A, const GemmOperand& B, void* D
     p.wait_ns = wait_limit_ns();
     p.stall = take_stall();
     p.qscale = (uint8_t*)qscale;
+    p.qscale_col = qscale_col;
     p.qcounters = qcounters;
     if (qkind >= 0 && qcounters != nullptr && cudaMemsetAsync(qcounters, 0, 3 * sizeof(unsigned long long), s) != cudaSuccess)
         return FP8Q_ERR_CUDA;
@@ -968,7 +1258,7 @@ fp8q_status launch_gemm_pair(const GemmOperand& A, const GemmOperand& B, void* D
                          CU_TENSOR_MAP_SWIZZLE_NONE))
             return FP8Q_ERR_CUDA;
         p.idesc = shape | fmts | (1u << 23);
-        return launch2_rec<REC_MX>(maps, p, D, out_dtype, qkind, qfmt, qdata, s);
+        return launch2_rec<REC_MX>(maps, p, D, out_dtype, qkind, qfmt, qdata, qcol, s);
     }
     maps[3] = maps[0];
     maps[4] = maps[1];
@@ -976,13 +1266,13 @@ fp8q_status launch_gemm_pair(const GemmOperand& A, const GemmOperand& B, void* D
     if (pt) {
         p.sa_inv = A.scale_inv;
         p.sb_inv = B.scale_inv;
-        return launch2_rec<REC_PT>(maps, p, D, out_dtype, qkind, qfmt, qdata, s);
+        return launch2_rec<REC_PT>(maps, p, D, out_dtype, qkind, qfmt, qdata, qcol, s);
     }
     if (pc) {  // the copies' per-row factors, fp32 padded to 128 entries
         if (((uintptr_t)A.scale | (uintptr_t)B.scale) & 15) return FP8Q_ERR_ARG;
         p.bsa = (const float*)A.scale;
         p.bsb = (const float*)B.scale;
-        return launch2_rec<REC_PC>(maps, p, D, out_dtype, qkind, qfmt, qdata, s);
+        return launch2_rec<REC_PC>(maps, p, D, out_dtype, qkind, qfmt, qdata, qcol, s);
     }
     // blockwise scale rows are fetched by bulk copies: 16-byte aligned bases
     if (((uintptr_t)A.scale | (uintptr_t)B.scale) & 15) return FP8Q_ERR_ARG;
@@ -994,8 +1284,8 @@ fp8q_status launch_gemm_pair(const GemmOperand& A, const GemmOperand& B, void* D
     if (p.Mp * p.nkbq >= ((int64_t)1 << 31) || p.Np * p.nkbq >= ((int64_t)1 << 31)) return FP8Q_ERR_SHAPE;
     const bool b2 = B.kind == FP8Q_BLOCK_128x128;
     if (kbs == 128)
-        return b2 ? launch2_rec<REC_B2D>(maps, p, D, out_dtype, qkind, qfmt, qdata, s)
-                  : launch2_rec<REC_B1D>(maps, p, D, out_dtype, qkind, qfmt, qdata, s);
+        return b2 ? launch2_rec<REC_B2D>(maps, p, D, out_dtype, qkind, qfmt, qdata, qcol, s)
+                  : launch2_rec<REC_B1D>(maps, p, D, out_dtype, qkind, qfmt, qdata, qcol, s);
     if (qkind >= 0) return FP8Q_ERR_UNSUPPORTED;  // the fused output quantize takes 128-wide K blocks
     if (D == nullptr) return FP8Q_ERR_ARG;
     const bool f32 = out_dtype == 1;

@@ -314,12 +314,17 @@ FP8Q_API fp8q_status fp8q_scaled_gemm(const fp8q_tensor* A, int a_use_col, const
  * is the next layer's input; [nemo] strategy 4), so that Dq->data_row,
  * Dq->scale_row and Dq->counters ([0] saturated, [1] 0, [2] NaN / Inf) equal
  * what fp8q_quantize(MXFP8_1x32, fmt, row-wise only) of that bf16 D writes.
+ * With Dq->data_col non-NULL the column-wise copy is written as well (codes
+ * uint8 [N][M] in Dq->data_col, blocks of 32 along M, E8M0 tiles in
+ * Dq->scale_col, its saturation count in counters[1]), equal to what
+ * fp8q_quantize(MXFP8_1x32, fmt, row-wise and column-wise) of D writes: the
+ * copy the next wgrad reads; it needs M % 16 == 0 and Dq->scale_col.
  * D (bf16 [M][N]) may be NULL: then only the quantized output is written.
- * Dq is caller-owned: data_row uint8 [M][N], scale_row of
+ * Dq is caller-owned: data_row uint8 [M][N], scale_row (and scale_col) of
  * fp8q_scale_bytes(MXFP8_1x32, M, N) bytes, counters uint64[3]; its rows /
- * cols / fmt / kind are filled in (data_col / scale_col / amax / scale /
- * scale_inv are not used).  Constraints as fp8q_scaled_gemm plus N % 32 == 0
- * and 16-byte aligned Dq buffers.  Runs on the SM-pair kernel whatever
+ * cols / fmt / kind are filled in (amax / scale / scale_inv are not used).
+ * Constraints as fp8q_scaled_gemm plus N % 32 == 0 and 16-byte aligned Dq
+ * buffers.  Runs on the SM-pair kernel whatever
  * fp8q_gemm_set_variant chose.  This entry point has no counterpart on the
  * pages: they describe the quantize and the GEMM as separate steps.
  */
@@ -334,7 +339,10 @@ FP8Q_API fp8q_status fp8q_scaled_gemm_mxq(const fp8q_tensor* A, int a_use_col, c
  * columns of D).  For 1x128, Dq->data_row, Dq->scale_row (fp32
  * [ceil(N/128)][ceil(M/128) * 128], K-block-major, pads 1.0) and Dq->counters
  * equal what fp8q_quantize(BLOCK_1x128, fmt, row-wise only) of the bf16 D
- * writes; N % 16 == 0.  Other kinds: FP8Q_ERR_UNSUPPORTED.  Same buffers,
+ * writes; N % 16 == 0; with Dq->data_col the column-wise copy too (blocks of
+ * 128 rows of one column, fp32 scales [ceil(M/128)][ceil(N/128) * 128] in
+ * Dq->scale_col; M % 16 == 0), as fp8q_quantize(BLOCK_1x128, fmt, both
+ * copies) writes it.  Other kinds: FP8Q_ERR_UNSUPPORTED.  Same buffers,
  * constraints and kernel otherwise.  No counterpart on the pages (a fusion of
  * two steps they describe separately).
  */

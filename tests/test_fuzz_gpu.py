@@ -107,7 +107,8 @@ FUSED_RECIPES = [(O.PERTENSOR_CURRENT, O.PERTENSOR_CURRENT), (O.BLOCK_1x128, O.B
 def test_fused_output_quantize_random_cases(case):
     """The GEMM with the next layer's quantize in its epilogue on random
     shapes: the fused codes, scales and counters equal the oracle's quantize
-    of the kernel's own bf16 D (MXFP8 1x32 or 1x128 output, either format)."""
+    of the kernel's own bf16 D (MXFP8 1x32 or 1x128 output, either format,
+    the column-wise copy as well in half of the cases)."""
     from fp8_scaled_quantization_quantize_gb300 import api
     rng = np.random.default_rng(3000 + case)
     ka, kb = FUSED_RECIPES[case % len(FUSED_RECIPES)]
@@ -121,9 +122,10 @@ def test_fused_output_quantize_random_cases(case):
     b = inputs.to_bf16(rng.standard_normal((N, K), dtype=np.float32) * np.float32(0.02))
     qa = api.quantize(a.cuda(), ka, O.E4M3, True, False)
     qb = api.quantize(b.cuda(), kb, O.E4M3, True, False)
-    D, Dq = api.scaled_gemm_q(qa, False, qb, False, out_kind, fmt, want_d=True)
+    col = (case // 2) % 2 == 1
+    D, Dq = api.scaled_gemm_q(qa, False, qb, False, out_kind, fmt, want_d=True, colwise=col)
     torch.cuda.synchronize()
-    ref = O.quantize(out_kind, fmt, inputs.bf16_bits(D.cpu()), True, False)
-    assert_quant_equal(out_kind, gpu_outputs(Dq), ref, True, False,
-                       f"case {case}: {ka}x{kb} out {out_kind} fmt {fmt} {M}x{N}x{K}")
+    ref = O.quantize(out_kind, fmt, inputs.bf16_bits(D.cpu()), True, col)
+    assert_quant_equal(out_kind, gpu_outputs(Dq), ref, True, col,
+                       f"case {case}: {ka}x{kb} out {out_kind} fmt {fmt} {M}x{N}x{K} col {col}")
     assert api.device_errors() == 0

@@ -173,3 +173,132 @@ def test_fused_1x128_output_llama8b_up_proj_sampled_rows():
     sc = Dq.scale_row.cpu().numpy().view(np.float32).reshape(14336 // 128, 4096)
     assert np.array_equal(sc[:, rows].T, ref["scale_row"])
     assert api.device_errors() == 0
+
+
+# ---------------------------------------------------------------- the column-wise copy too
+# The next layer's wgrad reads the column-wise copy of this GEMM's output
+# (blocks along M); with colwise the epilogue writes it as well, and the codes,
+# scales and counters of both copies must equal the oracle's quantize of the
+# kernel's own bf16 D with both copies.
+
+def _check_fused_both(api, qa, qb, fmt, ctx, kind):
+    D, Dq = api.scaled_gemm_q(qa, False, qb, False, kind, fmt, want_d=True, colwise=True)
+    torch.cuda.synchronize()
+    got = gpu_outputs(Dq)
+    ref = O.quantize(kind, fmt, inputs.bf16_bits(D.cpu()), True, True)
+    assert_quant_equal(kind, got, ref, True, True, ctx)
+    return D, Dq, got
+
+
+@pytest.mark.parametrize("name,kA,kB,fA,fB", RECIPES, ids=[r[0] for r in RECIPES])
+@pytest.mark.parametrize("M,N,K", SHAPES)
+@pytest.mark.parametrize("fmt", [O.E4M3, O.E5M2])
+@pytest.mark.parametrize("out_kind", list(OUT_KINDS))
+def test_fused_column_copy_matches_quantize_of_d(name, kA, kB, fA, fB, M, N, K, fmt, out_kind):
+    kind = OUT_KINDS[out_kind]
+    if kind == O.MXFP8_1x32 and N % 32:
+        pytest.skip("the MXFP8 output takes N % 32 == 0")
+    api = _api()
+    qa, qb = _operands(api, kA, kB, fA, fB, M, N, K, 160 + M)
+    D, Dq, got = _check_fused_both(api, qa, qb, fmt, f"{name} {M}x{N}x{K} fmt={fmt} out={out_kind} +col", kind)
+    # the row copy is the one the row-only call writes
+    _, Dr = api.scaled_gemm_q(qa, False, qb, False, kind, fmt, want_d=False)
+    torch.cuda.synchronize()
+    rb = api.scale_bytes(kind, M, N, True, False)[0]
+    assert torch.equal(Dr.data_row, Dq.data_row) and torch.equal(Dr.scale_row[:rb], Dq.scale_row[:rb])
+    assert api.device_errors() == 0
+
+
+@pytest.mark.parametrize("out_kind", list(OUT_KINDS))
+def test_fused_column_copy_counts_saturation(out_kind):
+    """Column blocks saturate like row blocks (a block's scaled maximum above
+    fmax): the column copy's count, counters[1], equals the oracle's."""
+    api = _api()
+    qa, qb = _operands(api, 4, 4, O.E4M3, O.E4M3, 512, 1024, 512, 15)
+    _, _, got = _check_fused_both(api, qa, qb, O.E4M3, "column saturation", OUT_KINDS[out_kind])
+    assert got["sat_col"] > 0
+
+
+@pytest.mark.parametrize("out_kind", list(OUT_KINDS))
+def test_fused_column_copy_of_overflowing_d(out_kind):
+    """An overflowing per-tensor GEMM (D all +-Inf): both copies encode +-fmax,
+    every block's finite maximum is 0."""
+    api = _api()
+    M, N, K = 256, 256, 128
+    big = torch.full((M, K), 1e30, dtype=torch.bfloat16)
+    qa = api.quantize(big.cuda(), 0, O.E4M3, True, False)
+    qb = api.quantize(big[:N].clone().cuda(), 0, O.E4M3, True, False)
+    D, Dq, got = _check_fused_both(api, qa, qb, O.E4M3, "overflow +col", OUT_KINDS[out_kind])
+    assert got["nonfinite"] == M * N
+
+
+@pytest.mark.parametrize("out_kind", list(OUT_KINDS))
+def test_fused_column_copy_with_nan_and_tiny_blocks(out_kind):
+    """Columns of D holding a NaN (from a NaN operand row) and rows of D near
+    2^-76 (1x128 column blocks with d below the reciprocal shortcut's range
+    mix with normal ones): both copies equal the oracle's quantize of D."""
+    api = _api()
+    M, N, K = 384, 384, 256
+    a = inputs.normal_f32((M, K), 93)
+    a[7, 3] = np.nan
+    a[128:256, :] *= np.float32(2.0 ** -80)
+    b = inputs.normal_f32((N, K), 94)
+    qa = api.quantize(inputs.to_bf16(a).cuda(), O.BLOCK_1x128, O.E4M3, True, False)
+    qb = api.quantize(inputs.to_bf16(b).cuda(), O.BLOCK_128x128, O.E4M3, True, False)
+    D, Dq, got = _check_fused_both(api, qa, qb, O.E4M3, "nan / tiny +col", OUT_KINDS[out_kind])
+    assert got["nonfinite"] > 0
+
+
+@pytest.mark.parametrize("out_kind", list(OUT_KINDS))
+def test_fused_column_copy_many_tiles_per_pair(out_kind):
+    """More tiles than SM pairs (each pair's epilogue runs several tiles, so the
+    1x128 exchange alternates its two buffers): both copies of a
+    2048 x 4096 x 256 output equal the oracle's."""
+    api = _api()
+    qa, qb = _operands(api, 2, 3, O.E4M3, O.E4M3, 2048, 4096, 256, 21)
+    _check_fused_both(api, qa, qb, O.E5M2, "many tiles +col", OUT_KINDS[out_kind])
+    assert api.device_errors() == 0
+
+
+def test_fused_column_copy_llama8b_fprop_sampled_columns():
+    """The Llama-3-8B MLP fprop (MXFP8 X [8192x4096] . W^T [14336x4096]) with
+    both copies of Y fused: 64 sampled columns of Y -- rows of the column copy
+    -- against the oracle's quantize of those rows of Y^T (the column copy of
+    Y is the row copy of Y^T), codes and E8M0 bytes."""
+    api = _api()
+    X, W, _ = inputs.llama8b_mlp()
+    qx = api.quantize(X.cuda(), 4, O.E4M3, True, False)
+    qw = api.quantize(W.cuda(), 4, O.E4M3, True, False)
+    D, Dq = api.scaled_gemm_mxq(qx, False, qw, False, O.E4M3, want_d=True, colwise=True)
+    torch.cuda.synchronize()
+    cols = np.sort(np.random.default_rng(5).choice(14336, 64, replace=False))
+    idx = torch.as_tensor(cols, device=D.device)
+    ref = O.quantize(O.MXFP8_1x32, O.E4M3, inputs.bf16_bits(D.t()[idx].contiguous().cpu()), True, False)
+    assert np.array_equal(Dq.data_col[idx].cpu().numpy(), ref["data_row"])
+    sb = Dq.scale_col.cpu().numpy()
+    S = 8192 // 32
+    tiles_c = 8192 // 128
+    k = np.arange(S)[None, :]
+    r = cols[:, None]
+    off = ((r // 128) * tiles_c + k // 4) * 512 + (r % 32) * 16 + ((r % 128) // 32) * 4 + k % 4
+    assert np.array_equal(sb[off], ref["scale_row"])
+    assert api.device_errors() == 0
+
+
+def test_fused_1x128_column_copy_llama8b_up_proj_sampled_columns():
+    """The blockwise Llama-3-8B up-projection with both 1x128 copies of Y
+    fused: 64 sampled columns of Y against the oracle's quantize of those rows
+    of Y^T: codes and the fp32 scales [32][14336] of those columns."""
+    api = _api()
+    X, W = inputs.llama8b_up_proj()
+    qx = api.quantize(X.cuda(), O.BLOCK_1x128, O.E4M3, True, False)
+    qw = api.quantize(W.cuda(), O.BLOCK_128x128, O.E4M3, True, False)
+    D, Dq = api.scaled_gemm_q(qx, False, qw, False, O.BLOCK_1x128, O.E4M3, want_d=True, colwise=True)
+    torch.cuda.synchronize()
+    cols = np.sort(np.random.default_rng(6).choice(14336, 64, replace=False))
+    idx = torch.as_tensor(cols, device=D.device)
+    ref = O.quantize(O.BLOCK_1x128, O.E4M3, inputs.bf16_bits(D.t()[idx].contiguous().cpu()), True, False)
+    assert np.array_equal(Dq.data_col[idx].cpu().numpy(), ref["data_row"])
+    sc = Dq.scale_col.cpu().numpy().view(np.float32).reshape(4096 // 128, 14336)
+    assert np.array_equal(sc[:, cols].T, ref["scale_row"])
+    assert api.device_errors() == 0
