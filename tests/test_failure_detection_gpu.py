@@ -112,3 +112,28 @@ def test_stalled_gemm_times_out_and_the_next_call_is_right(variant, recipe):
     rel = np.linalg.norm(got - ref) / np.linalg.norm(ref)
     assert rel <= 2e-3, rel
     assert _errors() == (L.OK, 0)
+
+
+@pytest.mark.parametrize("out_kind", [O.MXFP8_1x32, O.BLOCK_1x128], ids=["mxfp8_out", "1x128_out"])
+def test_stalled_fused_both_copies_times_out_and_the_next_call_is_exact(out_kind):
+    """The fused output quantize with both copies (whose 1x128 column path
+    adds an exchange between warps on a bounded mbarrier), stalled: every
+    wait gives up, the timeout is reported, and the next call's two copies
+    equal the oracle's quantize of its D."""
+    api = _api()
+    M, N, K = 512, 512, 384
+    a = inputs.normal_bf16((M, K), 45)
+    b = inputs.normal_bf16((N, K), 46, 0.02)
+    qa = api.quantize(a.cuda(), O.BLOCK_1x128, O.E4M3, True, False)
+    qb = api.quantize(b.cuda(), O.BLOCK_128x128, O.E4M3, True, False)
+    api.set_wait_limit(LIMIT_NS)
+    api.stall_next(1)
+    api.scaled_gemm_q(qa, False, qb, False, out_kind, O.E4M3, want_d=False, colwise=True)
+    st, flags = _errors()
+    assert st == L.ERR_TIMEOUT and flags == 1, (st, flags)
+    api.set_wait_limit(0)
+    D, Dq = api.scaled_gemm_q(qa, False, qb, False, out_kind, O.E4M3, want_d=True, colwise=True)
+    torch.cuda.synchronize()
+    ref = O.quantize(out_kind, O.E4M3, inputs.bf16_bits(D.cpu()), True, True)
+    assert_quant_equal(out_kind, gpu_outputs(Dq), ref, True, True, "after a stalled fused launch")
+    assert _errors() == (L.OK, 0)
