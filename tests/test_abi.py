@@ -148,6 +148,24 @@ def test_gemm_validation_without_gpu(lib):
     assert g(64, 96, 128, A=blk, B=blkb) == L.ERR_DTYPE     # blockwise A must be 1x128
 
 
+def test_fused_gemm_validation_without_gpu(lib):
+    """fp8q_scaled_gemm_q refuses, before any launch, a column-wise output copy
+    it cannot write: M % 16 != 0 (the [N][M] copy's rows must be 16-byte
+    multiples), no column scale buffer, a misaligned column buffer; and an
+    output kind it does not fuse."""
+    a = L.Tensor(16, 32, 64, 128, 256, 272, 288, 512, 72, 128, L.E4M3, L.MXFP8_1x32)
+    b = L.Tensor(16, 32, 64, 128, 256, 272, 288, 512, 96, 128, L.E4M3, L.MXFP8_1x32)
+
+    def g(M, kind=L.MXFP8_1x32, col=4096, scol=8192):
+        dq = L.Tensor(1024, col, 2048, scol, 0, 0, 0, 3072, 0, 0, 0, 0)
+        return lib.fp8q_scaled_gemm_q(ctypes.byref(a), 0, ctypes.byref(b), 0, None, kind, L.E4M3,
+                                      ctypes.byref(dq), M, 96, 128, None)
+    assert g(72) == L.ERR_SHAPE                      # column copy with M % 16 != 0
+    assert g(64, scol=0) == L.ERR_ARG                # column copy without its scales
+    assert g(64, col=4104) == L.ERR_ALIGN            # misaligned column codes
+    assert g(64, kind=L.BLOCK_128x128) == L.ERR_UNSUPPORTED
+
+
 def test_delayed_validation_without_gpu(lib):
     h = ctypes.c_void_p(0)
     assert lib.fp8q_delayed_create(0, L.E4M3, 0, ctypes.byref(h)) == L.ERR_ARG
