@@ -88,13 +88,15 @@ struct Cfg {
     static constexpr uint32_t NBARS = 2 * STAGES + 2 * NACC + 1 + 2 * SR + NSFB;
     static constexpr uint32_t OFF_MISC = OFF_BAR + 8 * NBARS;
     static constexpr uint32_t SMEM = OFF_MISC + 16 + 1024;
-    // the fused 1x128 column copy's exchange of column maxima: [tile parity]
-    // [column half][4 warps][128 columns] words, then its four mbarriers
-    // ([tile parity][column half]); only kernels with that copy allocate it
+    // the fused column-wise copy (kernels with it allocate these): the 1x128
+    // exchange of column maxima ([tile parity][column half][4 warps][128
+    // columns] words) and its four mbarriers ([tile parity][column half]),
+    // then each epilogue warp's 2 KB transpose area
     static constexpr uint32_t OFF_XB = OFF_MISC + 16;
     static constexpr uint32_t OFF_XBAR = OFF_XB + 2 * 2 * 4 * 128 * 4;
-    static constexpr uint32_t SMEM_XB = OFF_XBAR + 4 * 8 + 1024;
-    static_assert(SMEM_XB <= 232448, "shared memory budget of one CTA with the column exchange");
+    static constexpr uint32_t OFF_TR = OFF_XBAR + 4 * 8;
+    static constexpr uint32_t SMEM_COL = OFF_TR + EPI_WARPS * 2048 + 1024;
+    static_assert(SMEM_COL <= 232448, "shared memory budget of one CTA with the column-wise copy");
     static_assert(SMEM <= 232448, "shared memory budget of one CTA");
 };
 
@@ -355,8 +357,36 @@ __device__ __noinline__ MaxCount exact_max128(Bf16x128 h, int live) {
     return r;
 }
 
+// The codes of 32 bf16 values (two to a word) divided by d with IEEE division,
+// a NaN keeping its sign (the hardware's NaN code is 0x7F whatever the sign):
+// the rare path of the 1x128 conversions (a block holding NaN / Inf, or d
+// below 2^-80), out of line so that the common path's code stays compact.
+struct Bf16x32 {
+    uint32_t w[16];
+};
+struct Codes32 {
+    uint32_t c[8];
+};
+template <int QFMT>
+__device__ __noinline__ Codes32 codes_ieee_div(Bf16x32 x, float d) {
+    Codes32 r;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t w0 = x.w[2 * i], w1 = x.w[2 * i + 1];
+        uint32_t c = cvt4<QFMT>(__fdiv_rn(__uint_as_float(w0 << 16), d), __fdiv_rn(__uint_as_float(w0 & 0xFFFF0000u), d),
+                                __fdiv_rn(__uint_as_float(w1 << 16), d), __fdiv_rn(__uint_as_float(w1 & 0xFFFF0000u), d));
+        uint32_t lo = c & 0xFFFFu, hi = c >> 16;
+        if ((w0 & 0x7FFFu) > 0x7F80u) lo = (lo & ~0xFFu) | ((w0 >> 8) & 0x80u) | 0x7Fu;
+        if ((w0 & 0x7FFF0000u) > 0x7F800000u) lo = (lo & ~0xFF00u) | ((w0 >> 16) & 0x8000u) | 0x7F00u;
+        if ((w1 & 0x7FFFu) > 0x7F80u) hi = (hi & ~0xFFu) | ((w1 >> 8) & 0x80u) | 0x7Fu;
+        if ((w1 & 0x7FFF0000u) > 0x7F800000u) hi = (hi & ~0xFF00u) | ((w1 >> 16) & 0x8000u) | 0x7F00u;
+        r.c[i] = lo | (hi << 16);
+    }
+    return r;
+}
+
 // 1x128 (along N) quantization of this warp's 32 rows x 128 columns of D as
-// stored in bf16 (RN(v scale), as store_slice2 writes it): per row the amax of
+// stored in bf16 (h: RN(v scale) two to a word, as store_slice2 writes it): per row the amax of
 // the 128 bf16 over the finite ones (NaN / Inf counted), d = RN(amax / fmax)
 // (block_scale: 1 for amax 0), codes sat_rne(x / d) correctly rounded
 // (Markstein's division from RN(1 / d), two lanes, negated; IEEE division for
@@ -370,16 +400,13 @@ __device__ __noinline__ MaxCount exact_max128(Bf16x128 h, int live) {
 // at (x0 / 128) Mp + row (rows past M, up to Mp, get the pad 1.0).
 template <int QFMT, int NBOX>
 __device__ __forceinline__ void store_q128(const CUtensorMap* mapQ, uint8_t* stg, uint32_t stg_s, int lane, int x0,
-                                           int y0, const Params2& p, const float* v, float scale, uint32_t& nsat,
+                                           int y0, const Params2& p, const uint32_t (&h)[64], uint32_t& nsat,
                                            uint32_t& nnf) {
     static_assert(NBOX >= 4, "a warp's 128 code columns fill four staging boxes");
     const int r = lane, sw = (r >> 2) & 1;
     const int64_t row = (int64_t)y0 + r;
     const bool row_live = row < p.M;
     const int live = !row_live ? 0 : ((int64_t)x0 + 128 <= p.N ? 128 : (int)(p.N - x0));  // columns inside D
-    uint32_t h[64];
-#pragma unroll
-    for (int i = 0; i < 64; ++i) h[i] = pack_bf16(v[2 * i] * scale, v[2 * i + 1] * scale);
     uint32_t cm[8];  // packed maxima of each 16-column chunk
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
@@ -421,25 +448,22 @@ __device__ __forceinline__ void store_q128(const CUtensorMap* mapQ, uint8_t* stg
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
         uint32_t c[8];
+        if (fast) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const uint32_t w0 = h[16 * b + 2 * i], w1 = h[16 * b + 2 * i + 1];
-            const float2 a0 = make_float2(__uint_as_float(w0 << 16), __uint_as_float(w0 & 0xFFFF0000u));
-            const float2 a1 = make_float2(__uint_as_float(w1 << 16), __uint_as_float(w1 & 0xFFFF0000u));
-            if (fast) {
+            for (int i = 0; i < 8; ++i) {
+                const uint32_t w0 = h[16 * b + 2 * i], w1 = h[16 * b + 2 * i + 1];
+                const float2 a0 = make_float2(__uint_as_float(w0 << 16), __uint_as_float(w0 & 0xFFFF0000u));
+                const float2 a1 = make_float2(__uint_as_float(w1 << 16), __uint_as_float(w1 & 0xFFFF0000u));
                 const float2 y0 = div2_neg(a0, d2, nr2), y1 = div2_neg(a1, d2, nr2);
                 c[i] = cvt4<QFMT>(y0.x, y0.y, y1.x, y1.y) ^ 0x80808080u;
-            } else {
-                c[i] = cvt4<QFMT>(__fdiv_rn(a0.x, d), __fdiv_rn(a0.y, d), __fdiv_rn(a1.x, d), __fdiv_rn(a1.y, d));
-                if (nf) {  // the hardware's NaN code is 0x7F whatever the sign
-                    uint32_t lo = c[i] & 0xFFFFu, hi = c[i] >> 16;
-                    if ((w0 & 0x7FFFu) > 0x7F80u) lo = (lo & ~0xFFu) | ((w0 >> 8) & 0x80u) | 0x7Fu;
-                    if ((w0 & 0x7FFF0000u) > 0x7F800000u) lo = (lo & ~0xFF00u) | ((w0 >> 16) & 0x8000u) | 0x7F00u;
-                    if ((w1 & 0x7FFFu) > 0x7F80u) hi = (hi & ~0xFFu) | ((w1 >> 8) & 0x80u) | 0x7Fu;
-                    if ((w1 & 0x7FFF0000u) > 0x7F800000u) hi = (hi & ~0xFF00u) | ((w1 >> 16) & 0x8000u) | 0x7F00u;
-                    c[i] = lo | (hi << 16);
-                }
             }
+        } else {
+            Bf16x32 x;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) x.w[i] = h[16 * b + i];
+            const Codes32 k = codes_ieee_div<QFMT>(x, d);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) c[i] = k.c[i];
         }
         uint8_t* box = stg + b * 1024;
         *(uint4*)(box + r * 32 + ((0 ^ sw) << 4)) = make_uint4(c[0], c[1], c[2], c[3]);
@@ -468,24 +492,15 @@ __device__ __forceinline__ uint32_t nan_signs4(uint32_t c, uint32_t w0, uint32_t
     if ((w1 & 0x7FFF0000u) > 0x7F800000u) hi = (hi & ~0xFF00u) | ((w1 >> 16) & 0x8000u) | 0x7F00u;
     return lo | (hi << 16);
 }
-// This lane's (row m's) codes of 32 columns (column 4 i + k in byte k of
-// c[i]) into a 32 x 32 box of the transposed copy: the 32 codes of column n
-// (rows 0 .. 31, one per lane) are row n of the box, 32 bytes, no swizzle.
-__device__ __forceinline__ void put_transposed(uint8_t* box, int lane, const uint32_t (&c)[8]) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-#pragma unroll
-        for (int k = 0; k < 4; ++k) box[(4 * i + k) * 32 + lane] = (uint8_t)(c[i] >> (8 * k));
-}
 // This lane's 128 values of D as stored in bf16 (RN(v scale)), two to a word:
 // the column paths work on these, so the fp32 values are dead by then.
 __device__ __forceinline__ void bf16_row(const float* v, float scale, uint32_t (&h)[64]) {
 #pragma unroll
     for (int i = 0; i < 64; ++i) h[i] = pack_bf16(v[2 * i] * scale, v[2 * i + 1] * scale);
 }
-// Chunk b (columns 32 b .. 32 b + 31) of the row, picked by selects so that
-// the chunk loops stay rolled and the row stays in registers.
-__device__ __forceinline__ void take_chunk(const uint32_t (&hr)[64], int b, uint32_t (&h)[16]) {
+// Chunk b (columns 32 b .. 32 b + 31) of this lane's row, picked by selects so
+// that a chunk loop can stay rolled and the row stay in registers.
+__device__ __forceinline__ void pick_chunk(const uint32_t (&hr)[64], int b, uint32_t (&h)[16]) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
         const uint32_t lo = (b & 1) ? hr[16 + i] : hr[i];
@@ -493,76 +508,102 @@ __device__ __forceinline__ void take_chunk(const uint32_t (&hr)[64], int b, uint
         h[i] = (b & 2) ? hi : lo;
     }
 }
-// The 32 column maxima of a chunk over the warp's 32 rows (finite
-// magnitudes; rows past M count as 0): the maximum of column c is kept by
-// lane c.  *nf: this lane's row holds a NaN / Inf in the chunk.
-__device__ __forceinline__ uint32_t chunk_col_max(const uint32_t (&h)[16], bool row_live, int lane, bool* nf) {
-    uint32_t mine = 0;
-    bool anynf = false;
+// A 32 x 32 chunk of the warp's rows (h: this lane's row, two columns to a
+// word) transposed through the warp's area T (32 rows x 16 words; word w of
+// row r at r * 16 + ((w + r) & 15), so that the column reads are
+// conflict-free): afterwards lane c holds column c of the chunk, rows 2 i and
+// 2 i + 1 in the low and high halves of hv[i].
+__device__ __forceinline__ void transpose32(uint32_t* T, int lane, const uint32_t (&h)[16], uint32_t (&hv)[16]) {
+    __syncwarp();  // the previous chunk's reads of T are done
 #pragma unroll
-    for (int c = 0; c < 32; ++c) {
-        const uint32_t a = (h[c / 2] >> (16 * (c & 1))) & 0x7FFFu;
-        const bool fin = a < 0x7F80u;
-        anynf |= row_live && !fin;
-        const uint32_t mc = __reduce_max_sync(0xFFFFFFFFu, (row_live && fin) ? a : 0u);
-        if (lane == c) mine = mc;
+    for (int w = 0; w < 16; ++w) T[lane * 16 + ((w + lane) & 15)] = h[w];
+    __syncwarp();
+    const int wc = lane >> 1;
+    const uint32_t sel = (lane & 1) ? 0x7632u : 0x5410u;  // the high or the low halves
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const uint32_t a = T[(2 * i) * 16 + ((wc + 2 * i) & 15)];
+        const uint32_t b = T[(2 * i + 1) * 16 + ((wc + 2 * i + 1) & 15)];
+        hv[i] = __byte_perm(a, b, sel);
     }
-    *nf = anynf;
-    return mine;
+}
+// The largest finite magnitude among a column's 32 values (two to a word) and
+// whether a NaN / Inf is among them: packed maxima, the exact pass only when
+// they flag a NaN / Inf.
+__device__ __forceinline__ uint32_t col_max32(const uint32_t (&hv)[16], bool* nf) {
+    uint32_t pm = 0;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) pm = max_u16x2(pm, hv[i] & 0x7FFF7FFFu);
+    uint32_t m = max(pm & 0xFFFFu, pm >> 16);
+    *nf = m >= 0x7F80u;
+    if (*nf) {
+        m = 0;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const uint32_t a = (hv[i / 2] >> (16 * (i & 1))) & 0x7FFFu;
+            if (a < 0x7F80u) m = a > m ? a : m;
+        }
+    }
+    return m;
+}
+// A column's 32 codes (rows 4 i .. 4 i + 3 in c[i]) as row `lane` of a 32 x 32
+// box of the transposed copy (32 bytes, no swizzle).
+__device__ __forceinline__ void put_col_codes(uint8_t* box, int lane, const uint32_t (&c)[8]) {
+    *(uint4*)(box + lane * 32) = make_uint4(c[0], c[1], c[2], c[3]);
+    *(uint4*)(box + lane * 32 + 16) = make_uint4(c[4], c[5], c[6], c[7]);
 }
 
 // MXFP8 column-wise copy (1x32 blocks along M) of this warp's 32 rows x 128
 // columns of D as stored in bf16: the block of column n is the warp's rows
-// y0 .. y0 + 31 (one per lane; y0 is a multiple of 32), so its amax is one
-// warp maximum of the finite magnitudes.  e, the codes sat_rne(x 2^-e), the
-// NaN signs and the saturation count (finite |y| > fmax) as the row path;
-// the codes leave transposed ([N][M], uint8 32 x 32 boxes by TMA) and each
-// column's E8M0 byte goes to the packed 128x4 tiles of the [N][ceil(M/32)]
-// scale matrix -- the quantize kernel's MXFP8 column copy of these values.
+// y0 .. y0 + 31 (y0 a multiple of 32; rows past M are zeros of the GEMM), so
+// after a transpose through shared memory each lane holds one column's block
+// and finds its amax, e, the codes sat_rne(x 2^-e), the NaN signs and the
+// saturation count (finite |y| > fmax) alone, as the row path does for a
+// row's block; the codes leave transposed ([N][M], uint8 32 x 32 boxes by
+// TMA) and each column's E8M0 byte goes to the packed 128x4 tiles of the
+// [N][ceil(M/32)] scale matrix -- the quantize kernel's MXFP8 column copy of
+// these values.
 template <int QFMT>
-__device__ __forceinline__ void store_qc_mx(const CUtensorMap* mapQc, uint8_t* stg, uint32_t stg_s, int lane, int x0,
-                                            int y0, const Params2& p, const uint32_t (&hr)[64], uint32_t& nsat) {
-    const bool row_live = (int64_t)y0 + lane < p.M;
+__device__ __forceinline__ void store_qc_mx(const CUtensorMap* mapQc, uint8_t* stg, uint32_t stg_s, uint32_t* T,
+                                            int lane, int x0, int y0, const Params2& p, const uint32_t (&hr)[64],
+                                            uint32_t& nsat) {
     bulk_wait_read();  // the row codes' boxes have left the staging area
     __syncwarp();
 #pragma unroll 1
     for (int b = 0; b < 4; ++b) {
-        uint32_t h[16];
-        take_chunk(hr, b, h);
+        uint32_t h[16], hv[16];
+        pick_chunk(hr, b, h);
+        transpose32(T, lane, h, hv);
         bool nf;
-        const uint32_t mine = chunk_col_max(h, row_live, lane, &nf);
+        const uint32_t m = col_max32(hv, &nf);
         const int64_t n = (int64_t)x0 + 32 * b + lane;  // this lane's column
-        const int e = mx_exponent<QFMT>(mine << 16);
+        const int e = mx_exponent<QFMT>(m << 16);
         const float k = exp2_neg(e);
-        const uint32_t satm = __ballot_sync(0xFFFFFFFFu, __uint_as_float(mine << 16) * k > Fmt<QFMT>::fmax);
-        const bool anynf = __any_sync(0xFFFFFFFFu, nf);
         if (n < p.Np && (int64_t)y0 < p.Mp) {  // pads (columns past N, blocks past M) get 127
             const int64_t tile = (n / 128) * p.tiles_m128 + y0 / 128;
             ((uint8_t*)p.qscale_col)[tile * 512 + (n % 32) * 16 + ((n % 128) / 32) * 4 + (y0 / 32) % 4] =
                 (uint8_t)(e + 127);
         }
+        const bool sat = __uint_as_float(m << 16) * k > Fmt<QFMT>::fmax;
+        const float2 k2 = make_float2(k, k);
         uint32_t c[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const float k0 = __shfl_sync(0xFFFFFFFFu, k, 4 * i), k1 = __shfl_sync(0xFFFFFFFFu, k, 4 * i + 1);
-            const float k2 = __shfl_sync(0xFFFFFFFFu, k, 4 * i + 2), k3 = __shfl_sync(0xFFFFFFFFu, k, 4 * i + 3);
-            const uint32_t w0 = h[2 * i], w1 = h[2 * i + 1];
-            const float2 ya = __fmul2_rn(make_float2(__uint_as_float(w0 << 16), __uint_as_float(w0 & 0xFFFF0000u)),
-                                         make_float2(k0, k1));
-            const float2 yb = __fmul2_rn(make_float2(__uint_as_float(w1 << 16), __uint_as_float(w1 & 0xFFFF0000u)),
-                                         make_float2(k2, k3));
+            const uint32_t w0 = hv[2 * i], w1 = hv[2 * i + 1];
+            const float2 ya =
+                __fmul2_rn(make_float2(__uint_as_float(w0 << 16), __uint_as_float(w0 & 0xFFFF0000u)), k2);
+            const float2 yb =
+                __fmul2_rn(make_float2(__uint_as_float(w1 << 16), __uint_as_float(w1 & 0xFFFF0000u)), k2);
             c[i] = cvt4<QFMT>(ya.x, ya.y, yb.x, yb.y);
-            const uint32_t sm = (satm >> (4 * i)) & 0xFu;
-            if (sm) {  // a saturating block: count its finite elements past fmax
+            if (sat) {  // a saturating block: count its finite elements past fmax
                 const float y[4] = {ya.x, ya.y, yb.x, yb.y};
 #pragma unroll
-                for (int t = 0; t < 4; ++t)
-                    nsat += ((sm >> t) & 1u) && fabsf(y[t]) <= 3.402823466e38f && fabsf(y[t]) > Fmt<QFMT>::fmax;
+                for (int t = 0; t < 4; ++t) nsat += fabsf(y[t]) <= 3.402823466e38f && fabsf(y[t]) > Fmt<QFMT>::fmax;
             }
-            if (anynf) c[i] = nan_signs4(c[i], w0, w1);
+            if (nf) c[i] = nan_signs4(c[i], w0, w1);
         }
         uint8_t* box = stg + b * 1024;
-        put_transposed(box, lane, c);
+        put_col_codes(box, lane, c);
         fence_async_smem();
         __syncwarp();
         if (lane == 0 && (int64_t)x0 + 32 * b < p.N && (int64_t)y0 < p.M) {
@@ -575,49 +616,46 @@ __device__ __forceinline__ void store_qc_mx(const CUtensorMap* mapQc, uint8_t* s
 // 1x128 column-wise copy (blocks of 128 rows of one column) of this warp's
 // 32 rows x 128 columns of D as stored in bf16.  A CTA's 128 tile rows are
 // one 128-row group, so the block of column n is the rows of the four warps
-// of this column half: each warp takes its 32-row maxima by warp maxima of
-// the finite magnitudes, the four meet in shared memory (xb: [4 warps][128
-// columns], one arrival per warp on the mbarrier xbar, whose wait is bounded
-// like every other), and each lane turns the maxima of its column in each
-// chunk into d = RN(amax / fmax); the codes sat_rne(x / d) (Markstein's
-// division from RN(1 / d), or IEEE division for d below 2^-80 or a block
-// holding NaN / Inf, with the NaN signs), saturation counted at the elements
-// equal to a saturating block's maximum (the row path's argument); codes
-// transposed by TMA, d into the [ceil(M/128)][Np] scale array by the first
-// warp -- the quantize kernel's 1x128 column copy of these values.  Returns
-// false when the exchange's wait gave up (the caller leaves its tile loop).
-template <int QFMT>
-__device__ __forceinline__ bool store_qc128(const CUtensorMap* mapQc, uint8_t* stg, uint32_t stg_s, int lane, int q,
-                                            int x0, int y0, const Params2& p, const uint32_t (&hr)[64],
-                                            uint32_t& nsat, uint32_t* xb, uint32_t xbar, uint32_t xph,
-                                            volatile int* abort_flag) {
-    const bool row_live = (int64_t)y0 + lane < p.M;
+// of this column half.  First (qc128_post_maxima, before the row path, so
+// that the four warps' maxima are in by the time they are needed) each warp
+// transposes its chunks through shared memory (a lane then holds one column's
+// 32 rows), takes each column's 32-row maximum in the lane and posts it to xb
+// ([4 warps][128 columns]) with one arrival on the mbarrier xbar.  Then
+// (qc128_codes) it waits for the four (bounded, like every other wait),
+// transposes each chunk again and turns its column's maxima into d =
+// RN(amax / fmax) and the codes sat_rne(x / d) (Markstein's division from
+// RN(1 / d), or IEEE division for d below 2^-80 or a block holding NaN / Inf,
+// with the NaN signs), saturation counted at the elements equal to a
+// saturating block's maximum (the row path's argument); codes transposed by
+// TMA, d into the [ceil(M/128)][Np] scale array by the first warp -- the
+// quantize kernel's 1x128 column copy of these values.
+__device__ __forceinline__ void qc128_post_maxima(uint32_t* T, int lane, int q, const uint32_t (&hr)[64],
+                                                  uint32_t* xb, uint32_t xbar) {
 #pragma unroll 1
     for (int b = 0; b < 4; ++b) {
-        uint32_t h[16];
-        take_chunk(hr, b, h);
+        uint32_t h[16], hv[16];
+        pick_chunk(hr, b, h);
+        transpose32(T, lane, h, hv);
         bool nf;
-        const uint32_t mine = chunk_col_max(h, row_live, lane, &nf);
-        bool nfc = false;
-        if (__any_sync(0xFFFFFFFFu, nf)) {  // which columns hold a NaN / Inf (rare)
-#pragma unroll
-            for (int c = 0; c < 32; ++c) {
-                const uint32_t a = (h[c / 2] >> (16 * (c & 1))) & 0x7FFFu;
-                const uint32_t bal = __ballot_sync(0xFFFFFFFFu, row_live && a >= 0x7F80u);
-                if (lane == c) nfc = bal != 0u;
-            }
-        }
-        xb[q * 128 + 32 * b + lane] = mine | (nfc ? 0x10000u : 0u);
+        const uint32_t m = col_max32(hv, &nf);
+        xb[q * 128 + 32 * b + lane] = m | (nf ? 0x10000u : 0u);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(xbar);
+}
+// Returns false when the exchange's wait gave up (the caller leaves its tile
+// loop).
+template <int QFMT>
+__device__ __forceinline__ bool qc128_codes(const CUtensorMap* mapQc, uint8_t* stg, uint32_t stg_s, uint32_t* T,
+                                            int lane, int q, int x0, int y0, const Params2& p,
+                                            const uint32_t (&hr)[64], uint32_t& nsat, const uint32_t* xb,
+                                            uint32_t xbar, uint32_t xph, volatile int* abort_flag) {
     if (!mbar_wait2(xbar, xph, abort_flag, p.wait_ns)) return false;
     bulk_wait_read();  // the row codes' boxes have left the staging area
     __syncwarp();
 #pragma unroll 1
     for (int b = 0; b < 4; ++b) {
-        // this lane's column of the chunk: the block maximum over the four warps, d, -RN(1 / d)
-        uint32_t m = 0, f = 0;
+        uint32_t m = 0, f = 0;  // this lane's column: the block maximum over the four warps
 #pragma unroll
         for (int w = 0; w < 4; ++w) {
             const uint32_t x = xb[w * 128 + 32 * b + lane];
@@ -625,46 +663,40 @@ __device__ __forceinline__ bool store_qc128(const CUtensorMap* mapQc, uint8_t* s
             f |= x >> 16;
         }
         const float d = block_scale<QFMT>(__uint_as_float(m << 16));
-        const bool fastl = f == 0u && d >= 0x1p-80f;
-        const float nrd = fastl ? -rcp_rn(d) : -1.0f;
-        const bool fast = __all_sync(0xFFFFFFFFu, fastl);
-        const uint32_t satm =
-            __ballot_sync(0xFFFFFFFFu, fabsf(__fdiv_rn(__uint_as_float(m << 16), d)) > Fmt<QFMT>::fmax);
+        const bool fast = f == 0u && d >= 0x1p-80f;
         const int64_t n = (int64_t)x0 + 32 * b + lane;
         if (q == 0 && n < p.Np && (int64_t)y0 < p.Mp)  // y0: the 128-row group's first row (pads: d = 1)
             ((float*)p.qscale_col)[(int64_t)(y0 / 128) * p.Np + n] = d;
-        uint32_t h[16];
-        take_chunk(hr, b, h);
+        const bool may_sat = fabsf(__fdiv_rn(__uint_as_float(m << 16), d)) > Fmt<QFMT>::fmax;
+        uint32_t h[16], hv[16];
+        pick_chunk(hr, b, h);
+        transpose32(T, lane, h, hv);
         uint32_t c[8];
+        if (fast) {
+            const float nrd = -rcp_rn(d);
+            const float2 d2 = make_float2(d, d), nr2 = make_float2(nrd, nrd);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const uint32_t w0 = h[2 * i], w1 = h[2 * i + 1];
-            const float2 a0 = make_float2(__uint_as_float(w0 << 16), __uint_as_float(w0 & 0xFFFF0000u));
-            const float2 a1 = make_float2(__uint_as_float(w1 << 16), __uint_as_float(w1 & 0xFFFF0000u));
-            const float d0 = __shfl_sync(0xFFFFFFFFu, d, 4 * i), d1 = __shfl_sync(0xFFFFFFFFu, d, 4 * i + 1);
-            const float d2 = __shfl_sync(0xFFFFFFFFu, d, 4 * i + 2), d3 = __shfl_sync(0xFFFFFFFFu, d, 4 * i + 3);
-            if (fast) {
-                const float r0 = __shfl_sync(0xFFFFFFFFu, nrd, 4 * i), r1 = __shfl_sync(0xFFFFFFFFu, nrd, 4 * i + 1);
-                const float r2 = __shfl_sync(0xFFFFFFFFu, nrd, 4 * i + 2), r3 = __shfl_sync(0xFFFFFFFFu, nrd, 4 * i + 3);
-                const float2 ya = div2_neg(a0, make_float2(d0, d1), make_float2(r0, r1));
-                const float2 yb = div2_neg(a1, make_float2(d2, d3), make_float2(r2, r3));
+            for (int i = 0; i < 8; ++i) {
+                const uint32_t w0 = hv[2 * i], w1 = hv[2 * i + 1];
+                const float2 a0 = make_float2(__uint_as_float(w0 << 16), __uint_as_float(w0 & 0xFFFF0000u));
+                const float2 a1 = make_float2(__uint_as_float(w1 << 16), __uint_as_float(w1 & 0xFFFF0000u));
+                const float2 ya = div2_neg(a0, d2, nr2), yb = div2_neg(a1, d2, nr2);
                 c[i] = cvt4<QFMT>(ya.x, ya.y, yb.x, yb.y) ^ 0x80808080u;
-            } else {
-                c[i] = cvt4<QFMT>(__fdiv_rn(a0.x, d0), __fdiv_rn(a0.y, d1), __fdiv_rn(a1.x, d2), __fdiv_rn(a1.y, d3));
-                c[i] = nan_signs4(c[i], w0, w1);
             }
-            const uint32_t sm = (satm >> (4 * i)) & 0xFu;
-            if (sm) {  // only elements equal to a saturating block's maximum exceed fmax
+        } else {
+            Bf16x32 x;
 #pragma unroll
-                for (int t = 0; t < 4; ++t) {
-                    const uint32_t mt = __shfl_sync(0xFFFFFFFFu, m, 4 * i + t);
-                    const uint32_t a = ((t < 2 ? w0 : w1) >> (16 * (t & 1))) & 0x7FFFu;
-                    nsat += ((sm >> t) & 1u) && row_live && a == mt;
-                }
-            }
+            for (int i = 0; i < 16; ++i) x.w[i] = hv[i];
+            const Codes32 kc = codes_ieee_div<QFMT>(x, d);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) c[i] = kc.c[i];
+        }
+        if (may_sat) {  // only elements equal to a saturating block's maximum exceed fmax
+#pragma unroll
+            for (int i = 0; i < 16; ++i) nsat += ((hv[i] & 0x7FFFu) == m) + (((hv[i] >> 16) & 0x7FFFu) == m);
         }
         uint8_t* box = stg + b * 1024;
-        put_transposed(box, lane, c);
+        put_col_codes(box, lane, c);
         fence_async_smem();
         __syncwarp();
         if (lane == 0 && (int64_t)x0 + 32 * b < p.N && (int64_t)y0 < p.M) {
@@ -1016,19 +1048,30 @@ __global__ void __launch_bounds__(Cfg<REC>::THREADS, 1)
                 if constexpr (QOut<QF>::mx)
                     store_q<QOut<QF>::fmt, EC, C::STG_WARP / 1024>(&tmQ, stg, stg_s, lane, (int)col0, (int)row0, p, vf,
                                                                    osc, q_sat, q_nf);
-                if constexpr (QOut<QF>::b128)
-                    store_q128<QOut<QF>::fmt, C::STG_WARP / 1024>(&tmQ, stg, stg_s, lane, (int)col0, (int)row0, p, vf,
-                                                                  osc, q_sat, q_nf);
-                if constexpr (QOut<QF>::col) {
-                    uint32_t hc[64];
+                if constexpr (QOut<QF>::b128 || QOut<QF>::col) {
+                    uint32_t hc[64];  // D as stored in bf16, two to a word: the 1x128 row path and the column paths
                     bf16_row(vf, osc, hc);
-                    if constexpr (QOut<QF>::mx)
-                        store_qc_mx<QOut<QF>::fmt>(&tmQc, stg, stg_s, lane, (int)col0, (int)row0, p, hc, q_satc);
-                    if constexpr (QOut<QF>::b128) {
-                        const uint32_t x = (tile_i & 1u) * 2 + (uint32_t)j;  // [tile parity][column half]
-                        if (!store_qc128<QOut<QF>::fmt>(&tmQc, stg, stg_s, lane, q, (int)col0, (int)row0, p, hc, q_satc,
-                                                        (uint32_t*)(smem + C::OFF_XB) + x * 512,
-                                                        sb + C::OFF_XBAR + 8u * x, (tile_i >> 1) & 1u, abort_flag))
+                    if constexpr (QOut<QF>::col) {
+                        if (row0 + lane >= p.M) {  // rows past M take no part in a column block
+#pragma unroll
+                            for (int i = 0; i < 64; ++i) hc[i] = 0u;
+                        }
+                    }
+                    // the column copy's transpose area of this warp and its 1x128 exchange
+                    // slot [tile parity][column half]
+                    uint32_t* const tr = (uint32_t*)(smem + C::OFF_TR) + ew * 512;
+                    const uint32_t xs = (tile_i & 1u) * 2 + (uint32_t)j;
+                    uint32_t* const xb = (uint32_t*)(smem + C::OFF_XB) + xs * 512;
+                    const uint32_t xbar = sb + C::OFF_XBAR + 8u * xs;
+                    if constexpr (QOut<QF>::col && QOut<QF>::b128) qc128_post_maxima(tr, lane, q, hc, xb, xbar);
+                    if constexpr (QOut<QF>::b128)
+                        store_q128<QOut<QF>::fmt, C::STG_WARP / 1024>(&tmQ, stg, stg_s, lane, (int)col0, (int)row0, p,
+                                                                      hc, q_sat, q_nf);
+                    if constexpr (QOut<QF>::col && QOut<QF>::mx)
+                        store_qc_mx<QOut<QF>::fmt>(&tmQc, stg, stg_s, tr, lane, (int)col0, (int)row0, p, hc, q_satc);
+                    if constexpr (QOut<QF>::col && QOut<QF>::b128) {
+                        if (!qc128_codes<QOut<QF>::fmt>(&tmQc, stg, stg_s, tr, lane, q, (int)col0, (int)row0, p, hc,
+                                                        q_satc, xb, xbar, (tile_i >> 1) & 1u, abort_flag))
                             break;
                     }
                 }
@@ -1089,19 +1132,30 @@ __global__ void __launch_bounds__(Cfg<REC>::THREADS, 1)
                 if constexpr (QOut<QF>::mx)
                     store_q<QOut<QF>::fmt, EC, C::STG_WARP / 1024>(&tmQ, stg, stg_s, lane, (int)col0, (int)row0, p, accf,
                                                                    1.0f, q_sat, q_nf);
-                if constexpr (QOut<QF>::b128)
-                    store_q128<QOut<QF>::fmt, C::STG_WARP / 1024>(&tmQ, stg, stg_s, lane, (int)col0, (int)row0, p, accf,
-                                                                  1.0f, q_sat, q_nf);
-                if constexpr (QOut<QF>::col) {
-                    uint32_t hc[64];
+                if constexpr (QOut<QF>::b128 || QOut<QF>::col) {
+                    uint32_t hc[64];  // D as stored in bf16, two to a word: the 1x128 row path and the column paths
                     bf16_row(accf, 1.0f, hc);
-                    if constexpr (QOut<QF>::mx)
-                        store_qc_mx<QOut<QF>::fmt>(&tmQc, stg, stg_s, lane, (int)col0, (int)row0, p, hc, q_satc);
-                    if constexpr (QOut<QF>::b128) {
-                        const uint32_t x = (tile_i & 1u) * 2 + (uint32_t)j;  // [tile parity][column half]
-                        if (!store_qc128<QOut<QF>::fmt>(&tmQc, stg, stg_s, lane, q, (int)col0, (int)row0, p, hc, q_satc,
-                                                        (uint32_t*)(smem + C::OFF_XB) + x * 512,
-                                                        sb + C::OFF_XBAR + 8u * x, (tile_i >> 1) & 1u, abort_flag))
+                    if constexpr (QOut<QF>::col) {
+                        if (row0 + lane >= p.M) {  // rows past M take no part in a column block
+#pragma unroll
+                            for (int i = 0; i < 64; ++i) hc[i] = 0u;
+                        }
+                    }
+                    // the column copy's transpose area of this warp and its 1x128 exchange
+                    // slot [tile parity][column half]
+                    uint32_t* const tr = (uint32_t*)(smem + C::OFF_TR) + ew * 512;
+                    const uint32_t xs = (tile_i & 1u) * 2 + (uint32_t)j;
+                    uint32_t* const xb = (uint32_t*)(smem + C::OFF_XB) + xs * 512;
+                    const uint32_t xbar = sb + C::OFF_XBAR + 8u * xs;
+                    if constexpr (QOut<QF>::col && QOut<QF>::b128) qc128_post_maxima(tr, lane, q, hc, xb, xbar);
+                    if constexpr (QOut<QF>::b128)
+                        store_q128<QOut<QF>::fmt, C::STG_WARP / 1024>(&tmQ, stg, stg_s, lane, (int)col0, (int)row0, p,
+                                                                      hc, q_sat, q_nf);
+                    if constexpr (QOut<QF>::col && QOut<QF>::mx)
+                        store_qc_mx<QOut<QF>::fmt>(&tmQc, stg, stg_s, tr, lane, (int)col0, (int)row0, p, hc, q_satc);
+                    if constexpr (QOut<QF>::col && QOut<QF>::b128) {
+                        if (!qc128_codes<QOut<QF>::fmt>(&tmQc, stg, stg_s, tr, lane, q, (int)col0, (int)row0, p, hc,
+                                                        q_satc, xb, xbar, (tile_i >> 1) & 1u, abort_flag))
                             break;
                     }
                 }
@@ -1135,7 +1189,7 @@ template <int REC, bool F32, int QF, int KB = 128>
 fp8q_status launch2_t(const CUtensorMap* maps, const Params2& p, cudaStream_t s) {
     using C = Cfg<REC>;
     auto kern = gemm2_kernel<REC, F32, QF, KB>;
-    constexpr uint32_t smem = (QOut<QF>::col && QOut<QF>::b128) ? C::SMEM_XB : C::SMEM;
+    constexpr uint32_t smem = QOut<QF>::col ? C::SMEM_COL : C::SMEM;
     static PerDevice<bool> attr;
     if (!smem_opt_in(attr, kern, smem)) return FP8Q_ERR_CUDA;
     const int sms = sm_count();
