@@ -91,11 +91,12 @@ struct Cfg {
     // the fused column-wise copy (kernels with it allocate these): the 1x128
     // exchange of column maxima ([tile parity][column half][4 warps][128
     // columns] words) and its four mbarriers ([tile parity][column half]),
-    // then each epilogue warp's 2 KB transpose area
+    // then each epilogue warp's transpose area (2.25 KB)
     static constexpr uint32_t OFF_XB = OFF_MISC + 16;
     static constexpr uint32_t OFF_XBAR = OFF_XB + 2 * 2 * 4 * 128 * 4;
-    static constexpr uint32_t OFF_TR = OFF_XBAR + 4 * 8;
-    static constexpr uint32_t SMEM_COL = OFF_TR + EPI_WARPS * 2048 + 1024;
+    static constexpr uint32_t OFF_TR = (OFF_XBAR + 4 * 8 + 15) / 16 * 16;
+    static constexpr uint32_t TR_WARP = 16 * 36 * 4;  // 16 words of 32 rows, 36-word stride
+    static constexpr uint32_t SMEM_COL = OFF_TR + EPI_WARPS * TR_WARP + 1024;
     static_assert(SMEM_COL <= 232448, "shared memory budget of one CTA with the column-wise copy");
     static_assert(SMEM <= 232448, "shared memory budget of one CTA");
 };
@@ -509,22 +510,24 @@ __device__ __forceinline__ void pick_chunk(const uint32_t (&hr)[64], int b, uint
     }
 }
 // A 32 x 32 chunk of the warp's rows (h: this lane's row, two columns to a
-// word) transposed through the warp's area T (32 rows x 16 words; word w of
-// row r at r * 16 + ((w + r) & 15), so that the column reads are
-// conflict-free): afterwards lane c holds column c of the chunk, rows 2 i and
-// 2 i + 1 in the low and high halves of hv[i].
+// word) transposed through the warp's area T (16-byte aligned, 16 x 36
+// words; word w of row r at w * 36 + r): the writes of one w by the 32 lanes
+// are consecutive words, and lane c reads the 32 words of its column pair as
+// eight 16-byte loads at (c / 2) * 36, which the 36-word stride spreads over
+// distinct banks.  Afterwards lane c holds column c of the chunk, rows 2 i
+// and 2 i + 1 in the low and high halves of hv[i].
 __device__ __forceinline__ void transpose32(uint32_t* T, int lane, const uint32_t (&h)[16], uint32_t (&hv)[16]) {
     __syncwarp();  // the previous chunk's reads of T are done
 #pragma unroll
-    for (int w = 0; w < 16; ++w) T[lane * 16 + ((w + lane) & 15)] = h[w];
+    for (int w = 0; w < 16; ++w) T[w * 36 + lane] = h[w];
     __syncwarp();
-    const int wc = lane >> 1;
+    const uint4* src = (const uint4*)(T + (lane >> 1) * 36);
     const uint32_t sel = (lane & 1) ? 0x7632u : 0x5410u;  // the high or the low halves
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        const uint32_t a = T[(2 * i) * 16 + ((wc + 2 * i) & 15)];
-        const uint32_t b = T[(2 * i + 1) * 16 + ((wc + 2 * i + 1) & 15)];
-        hv[i] = __byte_perm(a, b, sel);
+    for (int t = 0; t < 8; ++t) {  // rows 4 t .. 4 t + 3
+        const uint4 v = src[t];
+        hv[2 * t] = __byte_perm(v.x, v.y, sel);
+        hv[2 * t + 1] = __byte_perm(v.z, v.w, sel);
     }
 }
 // The largest finite magnitude among a column's 32 values (two to a word) and
@@ -1059,7 +1062,7 @@ __global__ void __launch_bounds__(Cfg<REC>::THREADS, 1)
                     }
                     // the column copy's transpose area of this warp and its 1x128 exchange
                     // slot [tile parity][column half]
-                    uint32_t* const tr = (uint32_t*)(smem + C::OFF_TR) + ew * 512;
+                    uint32_t* const tr = (uint32_t*)(smem + C::OFF_TR + ew * C::TR_WARP);
                     const uint32_t xs = (tile_i & 1u) * 2 + (uint32_t)j;
                     uint32_t* const xb = (uint32_t*)(smem + C::OFF_XB) + xs * 512;
                     const uint32_t xbar = sb + C::OFF_XBAR + 8u * xs;
@@ -1143,7 +1146,7 @@ __global__ void __launch_bounds__(Cfg<REC>::THREADS, 1)
                     }
                     // the column copy's transpose area of this warp and its 1x128 exchange
                     // slot [tile parity][column half]
-                    uint32_t* const tr = (uint32_t*)(smem + C::OFF_TR) + ew * 512;
+                    uint32_t* const tr = (uint32_t*)(smem + C::OFF_TR + ew * C::TR_WARP);
                     const uint32_t xs = (tile_i & 1u) * 2 + (uint32_t)j;
                     uint32_t* const xb = (uint32_t*)(smem + C::OFF_XB) + xs * 512;
                     const uint32_t xbar = sb + C::OFF_XBAR + 8u * xs;
