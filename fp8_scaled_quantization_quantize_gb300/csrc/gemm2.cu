@@ -27,10 +27,11 @@
 // arrival to its release against about 600 cycles of MMAs per K block).
 // The epilogue can also quantize D for the next layer (MXFP8 1x32 or 1x128,
 // row-wise along N and optionally column-wise along M, the transposed copy a
-// wgrad reads): the row blocks lie in a warp's registers, a 32-row column
-// block is a warp's rows (a warp maximum), a 128-row one the rows of the four
-// warps of a column half (an exchange through shared memory on a bounded
-// mbarrier).
+// wgrad reads): the row blocks lie in a lane's registers; for the column
+// blocks each warp transposes its rows through shared memory, 32 columns at
+// a time, so that a lane holds a column's 32 rows -- a whole 32-row block,
+// or a quarter of a 128-row one, whose four warps then exchange their maxima
+// through shared memory on a bounded mbarrier.
 // TMEM per CTA: per-tensor two 256-column accumulators; MXFP8 one accumulator
 // plus 12 scale columns per stage; blockwise two 256-column partial buffers,
 // so the MMAs run one K block ahead of the epilogue.
