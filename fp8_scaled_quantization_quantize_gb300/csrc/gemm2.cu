@@ -40,6 +40,8 @@
 // can still be used by the pair.
 #include <string.h>
 
+#include <type_traits>
+
 #include "fp8q_internal.cuh"
 #include "ptx.cuh"
 #include "umma.cuh"
@@ -91,11 +93,11 @@ struct Cfg {
     static constexpr uint32_t SMEM = OFF_MISC + 16 + 1024;
     // the fused column-wise copy (kernels with it allocate these): the 1x128
     // exchange of column maxima ([tile parity][column half][4 warps][128
-    // columns] words) and its four mbarriers ([tile parity][column half]),
-    // then each epilogue warp's transpose area (2.25 KB)
+    // columns] words) and its mbarriers ([tile parity][column half][32-column
+    // chunk]), then each epilogue warp's transpose area (2.25 KB)
     static constexpr uint32_t OFF_XB = OFF_MISC + 16;
     static constexpr uint32_t OFF_XBAR = OFF_XB + 2 * 2 * 4 * 128 * 4;
-    static constexpr uint32_t OFF_TR = (OFF_XBAR + 4 * 8 + 15) / 16 * 16;
+    static constexpr uint32_t OFF_TR = (OFF_XBAR + 16 * 8 + 15) / 16 * 16;
     static constexpr uint32_t TR_WARP = 16 * 36 * 4;  // 16 words of 32 rows, 36-word stride
     static constexpr uint32_t SMEM_COL = OFF_TR + EPI_WARPS * TR_WARP + 1024;
     static_assert(SMEM_COL <= 232448, "shared memory budget of one CTA with the column-wise copy");
@@ -618,47 +620,58 @@ __device__ __forceinline__ void store_qc_mx(const CUtensorMap* mapQc, uint8_t* s
 }
 
 // 1x128 column-wise copy (blocks of 128 rows of one column) of this warp's
-// 32 rows x 128 columns of D as stored in bf16.  A CTA's 128 tile rows are
-// one 128-row group, so the block of column n is the rows of the four warps
-// of this column half.  First (qc128_post_maxima, before the row path, so
-// that the four warps' maxima are in by the time they are needed) each warp
-// transposes its chunks through shared memory (a lane then holds one column's
-// 32 rows), takes each column's 32-row maximum in the lane and posts it to xb
-// ([4 warps][128 columns]) with one arrival on the mbarrier xbar.  Then
-// (qc128_codes) it waits for the four (bounded, like every other wait),
-// transposes each chunk again and turns its column's maxima into d =
-// RN(amax / fmax) and the codes sat_rne(x / d) (Markstein's division from
-// RN(1 / d), or IEEE division for d below 2^-80 or a block holding NaN / Inf,
-// with the NaN signs), saturation counted at the elements equal to a
-// saturating block's maximum (the row path's argument); codes transposed by
-// TMA, d into the [ceil(M/128)][Np] scale array by the first warp -- the
-// quantize kernel's 1x128 column copy of these values.
-__device__ __forceinline__ void qc128_post_maxima(uint32_t* T, int lane, int q, const uint32_t (&hr)[64],
-                                                  uint32_t* xb, uint32_t xbar) {
-#pragma unroll 1
-    for (int b = 0; b < 4; ++b) {
+// 32 rows x 128 columns of D as stored in bf16, after the row path.  A CTA's
+// 128 tile rows are one 128-row group, so the block of column n is the rows
+// of the four warps of this column half.  Each warp transposes its chunks
+// through shared memory (a lane then holds one column's 32 rows, kept in
+// registers), takes each column's 32-row maximum in the lane and posts it to
+// xb ([4 warps][128 columns]) with one arrival per chunk on that chunk's
+// mbarrier (xbar0 + 8 chunk); then, chunk by chunk, it waits for the four
+// warps' maxima (bounded, like every other wait; the first chunk's are in
+// while the later ones are still being posted) and turns its column's
+// maxima into d = RN(amax / fmax) and the codes sat_rne(x / d) (Markstein's
+// division from RN(1 / d), or IEEE division for d below 2^-80 or a block
+// holding NaN / Inf, with the NaN signs), saturation counted at the
+// elements equal to a saturating block's maximum (the row path's argument);
+// codes transposed by TMA, d into the [ceil(M/128)][Np] scale array by the
+// first warp -- the quantize kernel's 1x128 column copy of these values.
+// Returns false when an exchange wait gave up (the caller leaves its tile
+// loop).
+template <int QFMT>
+__device__ __forceinline__ bool store_qc128(const CUtensorMap* mapQc, uint8_t* stg, uint32_t stg_s, uint32_t* T,
+                                            int lane, int q, int x0, int y0, const Params2& p,
+                                            const uint32_t (&hr)[64], uint32_t& nsat, uint32_t* xb, uint32_t xbar0,
+                                            uint32_t xph, volatile int* abort_flag) {
+    uint32_t ht[64];  // this lane's column of each chunk, two rows to a word
+    auto post = [&](auto bc) {
+        constexpr int b = decltype(bc)::value;
         uint32_t h[16], hv[16];
-        pick_chunk(hr, b, h);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) h[i] = hr[16 * b + i];
         transpose32(T, lane, h, hv);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) ht[16 * b + i] = hv[i];
         bool nf;
         const uint32_t m = col_max32(hv, &nf);
         xb[q * 128 + 32 * b + lane] = m | (nf ? 0x10000u : 0u);
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(xbar);
-}
-// Returns false when the exchange's wait gave up (the caller leaves its tile
-// loop).
-template <int QFMT>
-__device__ __forceinline__ bool qc128_codes(const CUtensorMap* mapQc, uint8_t* stg, uint32_t stg_s, uint32_t* T,
-                                            int lane, int q, int x0, int y0, const Params2& p,
-                                            const uint32_t (&hr)[64], uint32_t& nsat, const uint32_t* xb,
-                                            uint32_t xbar, uint32_t xph, volatile int* abort_flag) {
-    if (!mbar_wait2(xbar, xph, abort_flag, p.wait_ns)) return false;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(xbar0 + 8u * b);
+    };
+    post(std::integral_constant<int, 0>{});
+    post(std::integral_constant<int, 1>{});
+    post(std::integral_constant<int, 2>{});
+    post(std::integral_constant<int, 3>{});
     bulk_wait_read();  // the row codes' boxes have left the staging area
     __syncwarp();
-#pragma unroll 1
-    for (int b = 0; b < 4; ++b) {
+    bool ok = true;
+    auto codes = [&](auto bc) {
+        constexpr int b = decltype(bc)::value;
+        if (!ok) return;
+        if (!mbar_wait2(xbar0 + 8u * b, xph, abort_flag, p.wait_ns)) {
+            ok = false;
+            return;
+        }
+        const uint32_t* hv = ht + 16 * b;
         uint32_t m = 0, f = 0;  // this lane's column: the block maximum over the four warps
 #pragma unroll
         for (int w = 0; w < 4; ++w) {
@@ -672,9 +685,6 @@ __device__ __forceinline__ bool qc128_codes(const CUtensorMap* mapQc, uint8_t* s
         if (q == 0 && n < p.Np && (int64_t)y0 < p.Mp)  // y0: the 128-row group's first row (pads: d = 1)
             ((float*)p.qscale_col)[(int64_t)(y0 / 128) * p.Np + n] = d;
         const bool may_sat = fabsf(__fdiv_rn(__uint_as_float(m << 16), d)) > Fmt<QFMT>::fmax;
-        uint32_t h[16], hv[16];
-        pick_chunk(hr, b, h);
-        transpose32(T, lane, h, hv);
         uint32_t c[8];
         if (fast) {
             const float nrd = -rcp_rn(d);
@@ -707,8 +717,12 @@ __device__ __forceinline__ bool qc128_codes(const CUtensorMap* mapQc, uint8_t* s
             tma_store_2d(mapQc, y0, x0 + 32 * b, stg_s + b * 1024);
             bulk_commit();
         }
-    }
-    return true;
+    };
+    codes(std::integral_constant<int, 0>{});
+    codes(std::integral_constant<int, 1>{});
+    codes(std::integral_constant<int, 2>{});
+    codes(std::integral_constant<int, 3>{});
+    return ok;
 }
 
 // QF, the fused quantization of the bf16 output: 0 none; 1, 2 MXFP8 1x32
@@ -770,7 +784,7 @@ __global__ void __launch_bounds__(Cfg<REC>::THREADS, 1)
         }
         for (int st = 0; st < C::NSFB; ++st) mbar_init(sfr(st), 1);
         if constexpr (QOut<QF>::col && QOut<QF>::b128)
-            for (int i = 0; i < 4; ++i) mbar_init(sb + C::OFF_XBAR + 8u * i, 4);
+            for (int i = 0; i < 16; ++i) mbar_init(sb + C::OFF_XBAR + 8u * i, 4);
         *abort_flag = 0;
         mbar_fence_init();
     }
@@ -1062,20 +1076,19 @@ __global__ void __launch_bounds__(Cfg<REC>::THREADS, 1)
                         }
                     }
                     // the column copy's transpose area of this warp and its 1x128 exchange
-                    // slot [tile parity][column half]
+                    // slot [tile parity][column half] (buffer, and the chunks' mbarriers)
                     uint32_t* const tr = (uint32_t*)(smem + C::OFF_TR + ew * C::TR_WARP);
                     const uint32_t xs = (tile_i & 1u) * 2 + (uint32_t)j;
-                    uint32_t* const xb = (uint32_t*)(smem + C::OFF_XB) + xs * 512;
-                    const uint32_t xbar = sb + C::OFF_XBAR + 8u * xs;
-                    if constexpr (QOut<QF>::col && QOut<QF>::b128) qc128_post_maxima(tr, lane, q, hc, xb, xbar);
                     if constexpr (QOut<QF>::b128)
                         store_q128<QOut<QF>::fmt, C::STG_WARP / 1024>(&tmQ, stg, stg_s, lane, (int)col0, (int)row0, p,
                                                                       hc, q_sat, q_nf);
                     if constexpr (QOut<QF>::col && QOut<QF>::mx)
                         store_qc_mx<QOut<QF>::fmt>(&tmQc, stg, stg_s, tr, lane, (int)col0, (int)row0, p, hc, q_satc);
                     if constexpr (QOut<QF>::col && QOut<QF>::b128) {
-                        if (!qc128_codes<QOut<QF>::fmt>(&tmQc, stg, stg_s, tr, lane, q, (int)col0, (int)row0, p, hc,
-                                                        q_satc, xb, xbar, (tile_i >> 1) & 1u, abort_flag))
+                        if (!store_qc128<QOut<QF>::fmt>(&tmQc, stg, stg_s, tr, lane, q, (int)col0, (int)row0, p, hc,
+                                                        q_satc, (uint32_t*)(smem + C::OFF_XB) + xs * 512,
+                                                        sb + C::OFF_XBAR + 8u * (4 * xs), (tile_i >> 1) & 1u,
+                                                        abort_flag))
                             break;
                     }
                 }
@@ -1146,20 +1159,19 @@ __global__ void __launch_bounds__(Cfg<REC>::THREADS, 1)
                         }
                     }
                     // the column copy's transpose area of this warp and its 1x128 exchange
-                    // slot [tile parity][column half]
+                    // slot [tile parity][column half] (buffer, and the chunks' mbarriers)
                     uint32_t* const tr = (uint32_t*)(smem + C::OFF_TR + ew * C::TR_WARP);
                     const uint32_t xs = (tile_i & 1u) * 2 + (uint32_t)j;
-                    uint32_t* const xb = (uint32_t*)(smem + C::OFF_XB) + xs * 512;
-                    const uint32_t xbar = sb + C::OFF_XBAR + 8u * xs;
-                    if constexpr (QOut<QF>::col && QOut<QF>::b128) qc128_post_maxima(tr, lane, q, hc, xb, xbar);
                     if constexpr (QOut<QF>::b128)
                         store_q128<QOut<QF>::fmt, C::STG_WARP / 1024>(&tmQ, stg, stg_s, lane, (int)col0, (int)row0, p,
                                                                       hc, q_sat, q_nf);
                     if constexpr (QOut<QF>::col && QOut<QF>::mx)
                         store_qc_mx<QOut<QF>::fmt>(&tmQc, stg, stg_s, tr, lane, (int)col0, (int)row0, p, hc, q_satc);
                     if constexpr (QOut<QF>::col && QOut<QF>::b128) {
-                        if (!qc128_codes<QOut<QF>::fmt>(&tmQc, stg, stg_s, tr, lane, q, (int)col0, (int)row0, p, hc,
-                                                        q_satc, xb, xbar, (tile_i >> 1) & 1u, abort_flag))
+                        if (!store_qc128<QOut<QF>::fmt>(&tmQc, stg, stg_s, tr, lane, q, (int)col0, (int)row0, p, hc,
+                                                        q_satc, (uint32_t*)(smem + C::OFF_XB) + xs * 512,
+                                                        sb + C::OFF_XBAR + 8u * (4 * xs), (tile_i >> 1) & 1u,
+                                                        abort_flag))
                             break;
                     }
                 }
